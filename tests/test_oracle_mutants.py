@@ -1,0 +1,49 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each one.
+
+Every mutant is a one-line edit of ``oracle/pkd_oracle.c`` in a scratch copy (never the
+oracle itself): a wrong GQA head map, an off-by-one window, a dropped max-subtraction, a
+wrong lse, a soft cap without the division, swapped strides, a wrong kv-length rule, an
+unweighted merge, a missing v_scale, and wrong fp16 / e4m3 decoders.  The pin suite in
+``test_oracle_pins.py`` runs against each mutant and must fail.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "gqa_head_map": ("const int h = g / group;", "const int h = g % p->num_kv_heads;"),
+    "window_off_by_one": ("first = n - 1 - p->window_left;", "first = n - p->window_left;"),
+    "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "soft_cap_no_division": ("tanh(x / p->logits_soft_cap)", "tanh(x)"),
+    "slot_head_strides_swapped": ("slot * p->slot_stride + (int64_t)h * p->head_stride",
+                                  "slot * p->head_stride + (int64_t)h * p->slot_stride"),
+    "kv_len_rule": ("(int64_t)page_size * (pages - 1) + last_page_len[i]",
+                    "(int64_t)page_size * pages + last_page_len[i] - page_size - 1"),
+    "merge_unweighted": ("const double w = exp(lse_parts[c] - M);", "const double w = 1.0;"),
+    "v_scale_dropped": ("w * p->v_scale * load_elem", "w * load_elem"),
+    "f16_exponent_bias": ("ldexp(1024.0 + (double)m, e - 25)",
+                          "ldexp(1024.0 + (double)m, e - 24)"),
+    "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "pkd_oracle.c")).read()
+    assert src.count(before) == 1, f"mutation site for {name} not found"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    (tmp_path / "oracle" / "pkd_oracle.c").write_text(src.replace(before, after))
+    shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__"))
+    shutil.copy(os.path.join(ROOT, "workloads.py"), tmp_path / "workloads.py")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -1,0 +1,366 @@
+"""Pins for the fp64 oracle: checks against facts fixed outside the oracle itself.
+
+Each test ties the oracle to something it cannot agree with by construction: values the
+FlashInfer attention API page prints for its worked example, library casts of every
+fp16 / bf16 / e4m3 bit pattern, dense brute-force attention written a different way (numpy
+einsum + scipy softmax over K/V that are scattered into random pages), closed forms
+(single key, two keys, constant V, zero query, window 0) and invariants (page permutation,
+GQA as MHA with repeated kv heads, split-and-merge, garbage in unused slots).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- element decoders
+
+def test_f16_decoder_all_codes():
+    codes = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode_array(codes, oracle.F16)
+    ref = codes.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_decoder_all_codes():
+    codes = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode_array(codes, oracle.BF16)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_array(codes, oracle.E4M3)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    ref = ref.astype(np.float64)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # S.1111.111 for both signs
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.nanmax(got) == 448.0
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_kv_len_and_shape():
+    g = json.load(open(os.path.join(GOLDEN, "worked_example.json")))
+    kv = oracle.kv_len(g["kv_page_indptr"], g["kv_last_page_len"], g["page_size"])
+    assert kv.tolist() == g["kv_len_expected"]
+    w = W.workload("worked")
+    assert list(W.pool_shape(w)) == g["kv_cache_shape_nhd"]
+    q = W.make_q(w)
+    pool = W.make_pool(w)
+    o, lse = oracle.batch_decode_pool(w.indptr, w.indices, w.last_page_len, W.raw_bits(q),
+                                      oracle.F16, W.raw_bits(pool), oracle.F16, "NHD",
+                                      sm_scale=w.sm_scale)
+    assert list(o.shape) == g["output_shape"]
+    assert list(lse.shape) == g["output_shape"][:2]
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute(kv_lens, Hq, Hkv, D, q, K, V, sm_scale, cap=0.0, window_left=-1):
+    """Dense attention on per-request K/V [n, Hkv, D] (float64), no page table involved."""
+    G = Hq // Hkv
+    B = len(kv_lens)
+    o = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), -np.inf)
+    for i in range(B):
+        n = kv_lens[i]
+        if n == 0:
+            continue
+        lo = 0 if window_left < 0 else max(0, n - 1 - window_left)
+        Kr = np.repeat(K[i][lo:n], G, axis=1)   # [a, Hq, D]
+        Vr = np.repeat(V[i][lo:n], G, axis=1)
+        x = sm_scale * np.einsum("hd,thd->ht", q[i], Kr)
+        s = cap * np.tanh(x / cap) if cap > 0 else x
+        o[i] = np.einsum("ht,thd->hd", scipy.special.softmax(s, axis=1), Vr)
+        lse[i] = scipy.special.logsumexp(s, axis=1)
+    return o, lse
+
+
+def _scatter(kv_lens, K, V, page_size, layout, rng, extra_pages=3, fill=0.0):
+    """Scatter dense per-request K/V into a float64 5-D pool at random pages."""
+    Hkv, D = K[0].shape[1], K[0].shape[2]
+    npages = [(n + page_size - 1) // page_size for n in kv_lens]
+    total = sum(npages)
+    P = total + extra_pages
+    perm = rng.permutation(P)
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    indices = perm[:total].astype(np.int32)
+    lpl = np.array([n - (p - 1) * page_size if p else 0 for n, p in zip(kv_lens, npages)],
+                   dtype=np.int32)
+    shape = (P, 2, page_size, Hkv, D) if layout == "NHD" else (P, 2, Hkv, page_size, D)
+    pool = np.full(shape, fill, dtype=np.float64)
+    for i, n in enumerate(kv_lens):
+        for t in range(n):
+            page = indices[indptr[i] + t // page_size]
+            slot = t % page_size
+            if layout == "NHD":
+                pool[page, 0, slot] = K[i][t]
+                pool[page, 1, slot] = V[i][t]
+            else:
+                pool[page, 0, :, slot] = K[i][t]
+                pool[page, 1, :, slot] = V[i][t]
+    return indptr, indices, lpl, pool
+
+
+def _run_f64(indptr, indices, lpl, q, pool, layout, **kw):
+    return oracle.batch_decode_pool(indptr, indices, lpl, np.ascontiguousarray(q), oracle.F64,
+                                    pool, oracle.F64, layout, **kw)
+
+
+def _rand_problem(rng, kv_lens, Hq, Hkv, D):
+    q = rng.standard_normal((len(kv_lens), Hq, D))
+    K = [rng.standard_normal((n, Hkv, D)) for n in kv_lens]
+    V = [rng.standard_normal((n, Hkv, D)) for n in kv_lens]
+    return q, K, V
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("case", [
+    dict(kv_lens=[5, 17, 40], Hq=4, Hkv=2, D=8, ps=4),
+    dict(kv_lens=[1, 16, 33], Hq=6, Hkv=3, D=16, ps=8, cap=2.5),
+    dict(kv_lens=[9, 31, 2], Hq=4, Hkv=1, D=4, ps=3, window_left=5),
+    dict(kv_lens=[0, 12, 7], Hq=2, Hkv=2, D=8, ps=4, cap=1.0, window_left=0),
+])
+def test_brute_force_agreement(layout, case):
+    rng = np.random.default_rng(1234)
+    kv_lens, Hq, Hkv, D, ps = case["kv_lens"], case["Hq"], case["Hkv"], case["D"], case["ps"]
+    cap, wl = case.get("cap", 0.0), case.get("window_left", -1)
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    sm = 0.37
+    ref_o, ref_lse = _brute(kv_lens, Hq, Hkv, D, q, K, V, sm, cap, wl)
+    indptr, indices, lpl, pool = _scatter(kv_lens, K, V, ps, layout, rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, layout, sm_scale=sm, logits_soft_cap=cap,
+                      window_left=wl)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-12)
+
+
+def test_scales_multiply_inputs():
+    rng = np.random.default_rng(7)
+    kv_lens, Hq, Hkv, D = [6, 11], 4, 2, 8
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    qs, ks, vs = 0.5, 3.0, 0.25
+    ref_o, ref_lse = _brute(kv_lens, Hq, Hkv, D, qs * q, [ks * k for k in K],
+                            [vs * v for v in V], 0.3)
+    indptr, indices, lpl, pool = _scatter(kv_lens, K, V, 4, "NHD", rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=0.3, q_scale=qs,
+                      k_scale=ks, v_scale=vs)
+    np.testing.assert_allclose(o, ref_o, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def test_default_sm_scale_is_inverse_sqrt_head_dim():
+    rng = np.random.default_rng(8)
+    kv_lens, Hq, Hkv, D = [7, 3], 2, 1, 16
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    ref_o, ref_lse = _brute(kv_lens, Hq, Hkv, D, q, K, V, 0.25)
+    indptr, indices, lpl, pool = _scatter(kv_lens, K, V, 4, "NHD", rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD")
+    np.testing.assert_allclose(o, ref_o, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def _single_request(rng, n, D=8, Hkv=1, Hq=1, ps=4):
+    q, K, V = _rand_problem(rng, [n], Hq, Hkv, D)
+    indptr, indices, lpl, pool = _scatter([n], K, V, ps, "NHD", rng)
+    return q, K, V, indptr, indices, lpl, pool
+
+
+def test_single_key_returns_v0_and_its_logit():
+    rng = np.random.default_rng(3)
+    q, K, V, indptr, indices, lpl, pool = _single_request(rng, 1)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=0.5)
+    assert np.array_equal(o[0, 0], V[0][0, 0])
+    assert lse[0, 0] == pytest.approx(0.5 * float(np.dot(q[0, 0], K[0][0, 0])), abs=1e-13)
+
+
+def test_two_keys_closed_form():
+    rng = np.random.default_rng(4)
+    q, K, V, indptr, indices, lpl, pool = _single_request(rng, 2, D=4)
+    sm = 0.7
+    s0 = sm * sum(a * b for a, b in zip(q[0, 0], K[0][0, 0]))
+    s1 = sm * sum(a * b for a, b in zip(q[0, 0], K[0][1, 0]))
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    expect = [w0 * a + w1 * b for a, b in zip(V[0][0, 0], V[0][1, 0])]
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=sm)
+    np.testing.assert_allclose(o[0, 0], expect, atol=1e-14)
+    assert lse[0, 0] == pytest.approx(max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))),
+                                      abs=1e-13)
+
+
+def test_window_zero_returns_last_value():
+    rng = np.random.default_rng(5)
+    q, K, V, indptr, indices, lpl, pool = _single_request(rng, 23)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", window_left=0, sm_scale=0.3)
+    assert np.array_equal(o[0, 0], V[0][22, 0])
+    assert lse[0, 0] == pytest.approx(0.3 * float(np.dot(q[0, 0], K[0][22, 0])), abs=1e-13)
+
+
+def test_constant_v_is_returned_unchanged():
+    rng = np.random.default_rng(6)
+    n, D = 37, 8
+    q, K, V = _rand_problem(rng, [n], 2, 1, D)
+    c = rng.standard_normal(D)
+    V = [np.broadcast_to(c, (n, 1, D)).copy()]
+    indptr, indices, lpl, pool = _scatter([n], K, V, 8, "HND", rng)
+    o, _ = _run_f64(indptr, indices, lpl, q, pool, "HND", sm_scale=1.3)
+    np.testing.assert_allclose(o[0, 0], c, atol=1e-12)
+    np.testing.assert_allclose(o[0, 1], c, atol=1e-12)
+
+
+def test_zero_query_gives_mean_and_log_count():
+    rng = np.random.default_rng(9)
+    n, D, wl = 29, 8, 10
+    q, K, V = _rand_problem(rng, [n], 1, 1, D)
+    q[:] = 0.0
+    indptr, indices, lpl, pool = _scatter([n], K, V, 4, "NHD", rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", window_left=wl)
+    np.testing.assert_allclose(o[0, 0], V[0][n - 1 - wl:, 0].mean(axis=0), atol=1e-13)
+    assert lse[0, 0] == pytest.approx(math.log(wl + 1), abs=1e-13)
+
+
+def test_empty_request_gives_zero_and_minus_inf():
+    rng = np.random.default_rng(10)
+    q, K, V = _rand_problem(rng, [0, 5], 2, 1, 8)
+    indptr, indices, lpl, pool = _scatter([0, 5], K, V, 4, "NHD", rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD")
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.isfinite(lse[1]).all()
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_page_permutation_invariance_bitwise():
+    rng = np.random.default_rng(11)
+    kv_lens, Hq, Hkv, D, ps = [13, 40, 7], 4, 2, 8, 4
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    a = _run_f64(*_scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(1))[:3], q,
+                 _scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(1))[3], "NHD")
+    ip, ix, lpl, pool = _scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(2))
+    b = _run_f64(ip, ix, lpl, q, pool, "NHD")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_unused_slots_never_matter():
+    """Slots past last_page_len and pages no request owns may hold NaN / Inf."""
+    rng = np.random.default_rng(12)
+    kv_lens, Hq, Hkv, D, ps = [13, 6, 21], 4, 2, 8, 8
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    ip, ix, lpl, clean = _scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(5), fill=0.0)
+    _, _, _, dirty = _scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(5), fill=np.nan)
+    dirty[-1] = np.inf
+    a = _run_f64(ip, ix, lpl, q, clean, "NHD", window_left=9)
+    b = _run_f64(ip, ix, lpl, q, dirty, "NHD", window_left=9)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    rng = np.random.default_rng(13)
+    kv_lens, Hq, Hkv, D, ps = [19, 8], 6, 2, 8, 4
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    G = Hq // Hkv
+    ip, ix, lpl, pool = _scatter(kv_lens, K, V, ps, "NHD", np.random.default_rng(3))
+    gqa = _run_f64(ip, ix, lpl, q, pool, "NHD", num_qo_heads=Hq)
+    K2 = [np.repeat(k, G, axis=1) for k in K]
+    V2 = [np.repeat(v, G, axis=1) for v in V]
+    ip2, ix2, lpl2, pool2 = _scatter(kv_lens, K2, V2, ps, "NHD", np.random.default_rng(3))
+    mha = _run_f64(ip2, ix2, lpl2, q, pool2, "NHD")
+    np.testing.assert_allclose(gqa[0], mha[0], atol=1e-13)
+    np.testing.assert_allclose(gqa[1], mha[1], atol=1e-13)
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 7, 16, 1000])
+def test_split_and_merge_equals_unsplit(chunk):
+    rng = np.random.default_rng(14)
+    kv_lens, Hq, Hkv, D, ps = [33, 1, 60, 0], 4, 2, 8, 4
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    ip, ix, lpl, pool = _scatter(kv_lens, K, V, ps, "HND", rng)
+    for wl, cap in ((-1, 0.0), (20, 3.0)):
+        a = _run_f64(ip, ix, lpl, q, pool, "HND", window_left=wl, logits_soft_cap=cap)
+        b = _run_f64(ip, ix, lpl, q, pool, "HND", window_left=wl, logits_soft_cap=cap,
+                     chunk_tokens=chunk)
+        np.testing.assert_allclose(b[0], a[0], atol=1e-12)
+        np.testing.assert_allclose(b[1], a[1], atol=1e-12)
+
+
+def test_merge_states_against_concatenation():
+    """Merging two disjoint key sets equals attending over their union (brute force)."""
+    rng = np.random.default_rng(15)
+    s = rng.standard_normal(11) * 3
+    v = rng.standard_normal((11, 5))
+    parts_o, parts_lse = [], []
+    for lo, hi in ((0, 4), (4, 11)):
+        w = scipy.special.softmax(s[lo:hi])
+        parts_o.append(w @ v[lo:hi])
+        parts_lse.append(scipy.special.logsumexp(s[lo:hi]))
+    o, lse = oracle.merge_states(np.array(parts_o), np.array(parts_lse))
+    np.testing.assert_allclose(o, scipy.special.softmax(s) @ v, atol=1e-14)
+    assert lse == pytest.approx(scipy.special.logsumexp(s), abs=1e-14)
+    o2, lse2 = oracle.merge_states(np.array(parts_o + [np.zeros(5)]),
+                                   np.array(parts_lse + [-np.inf]))
+    np.testing.assert_array_equal(o2, o)
+    assert lse2 == lse
+
+
+def test_window_at_least_length_is_no_window_and_large_cap_is_no_cap():
+    rng = np.random.default_rng(16)
+    kv_lens = [12, 30]
+    q, K, V = _rand_problem(rng, kv_lens, 2, 1, 8)
+    ip, ix, lpl, pool = _scatter(kv_lens, K, V, 4, "NHD", rng)
+    base = _run_f64(ip, ix, lpl, q, pool, "NHD")
+    for wl in (29, 30, 10 ** 6):
+        a = _run_f64(ip, ix, lpl, q, pool, "NHD", window_left=wl)
+        assert np.array_equal(a[0], base[0]) and np.array_equal(a[1], base[1])
+    b = _run_f64(ip, ix, lpl, q, pool, "NHD", logits_soft_cap=1e6)
+    np.testing.assert_allclose(b[0], base[0], atol=1e-9)
+    np.testing.assert_allclose(b[1], base[1], atol=1e-9)
+
+
+def test_soft_cap_bounds_lse():
+    """With cap c every logit lies in [-c, c], so lse lies in [-c, c] + ln(#keys)."""
+    rng = np.random.default_rng(17)
+    kv_lens = [50]
+    q, K, V = _rand_problem(rng, kv_lens, 2, 1, 8)
+    q *= 40.0
+    ip, ix, lpl, pool = _scatter(kv_lens, K, V, 8, "NHD", rng)
+    cap = 2.0
+    _, lse = _run_f64(ip, ix, lpl, q, pool, "NHD", logits_soft_cap=cap, sm_scale=1.0)
+    assert np.all(lse <= cap + math.log(50) + 1e-12)
+    assert np.all(lse >= -cap + math.log(50) - 1e-12)
+
+
+def test_rejects_malformed_tables():
+    rng = np.random.default_rng(18)
+    q, K, V = _rand_problem(rng, [5], 3, 2, 8)   # 3 qo heads, 2 kv heads: not a multiple
+    ip, ix, lpl, pool = _scatter([5], K, V, 4, "NHD", rng)
+    with pytest.raises(ValueError):
+        _run_f64(ip, ix, lpl, q, pool, "NHD")
+    q, K, V = _rand_problem(rng, [5], 2, 2, 8)
+    ip, ix, lpl, pool = _scatter([5], K, V, 4, "NHD", rng)
+    bad = lpl.copy()
+    bad[0] = 5                                  # last_page_len > page_size
+    with pytest.raises(ValueError):
+        _run_f64(ip, ix, bad, q, pool, "NHD")
