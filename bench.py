@@ -1,0 +1,403 @@
+"""Benchmark: batch decode attention over a paged KV cache on GB300.
+
+Workload (default ``uniform``): batch 64, kv_len ~ U{512..4096}, page 16, 32 qo / 8 kv heads,
+head_dim 128, bf16 q/K/V/o, NHD, one plan reused over 32 layers of independent KV pools.
+One step = plan() + run() on each of the 32 layers (decode kernel, plus merge_states when a
+request is split).  Every layer reads its own 1.2 GB pool, so a step streams ~19 GB: inputs
+are far larger than L2 and each layer starts cold.  Smaller workloads flush L2 between calls.
+
+Prints one JSON line.  ``value`` is algorithmic GB/s: per call, the K and V bytes of every
+attended token plus q and o, summed over the step and divided by the step time.
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded sample of the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: µs/call and KV-read GB/s as % of GB300 HBM peak"
+ELT = {"f16": 2, "bf16": 2, "e4m3": 1}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algorithmic_bytes(w) -> int:
+    """K and V of every attended token, plus q and o, for one call."""
+    lens = np.asarray(w.kv_lens, dtype=np.int64)
+    att = lens if w.window_left < 0 else np.minimum(lens, w.window_left + 1)
+    kv = int(att.sum()) * w.num_kv_heads * w.head_dim * ELT[w.kv_dtype] * 2
+    qo = w.batch * w.num_qo_heads * w.head_dim * (ELT[w.q_dtype] + ELT[w.o_dtype])
+    return kv + qo
+
+
+def describe(w) -> str:
+    extra = []
+    if w.logits_soft_cap:
+        extra.append(f"soft cap {w.logits_soft_cap:g}")
+    if w.window_left >= 0:
+        extra.append(f"window_left {w.window_left}")
+    if w.fixed_split_size:
+        extra.append(f"fixed split {w.fixed_split_size} pages")
+    lens = np.asarray(w.kv_lens)
+    return (f"{w.name}: batch {w.batch}, kv_len {lens.min()}..{lens.max()} (sum {lens.sum()}), "
+            f"page {w.page_size}, {w.num_qo_heads}/{w.num_kv_heads} heads, D {w.head_dim}, "
+            f"q {w.q_dtype} kv {w.kv_dtype} o {w.o_dtype}, {w.layout}"
+            + (", " + ", ".join(extra) if extra else "")
+            + (f", {w.layers} layers of independent pools, one plan per step" if w.layers > 1 else ""))
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def _host_sample(w, budget_s: float, seed: int = 0):
+    """A bounded sample of the workload for the CPU oracle: the first requests (in a seeded
+    order) whose total attended tokens fit the time budget at the oracle's measured speed."""
+    import oracle
+    import workloads as W
+
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.batch)
+
+    def build(reqs):
+        lens = np.asarray(w.kv_lens)[reqs]
+        sw = W.custom(lens, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                      layout=w.layout, q_dtype=w.q_dtype, kv_dtype=w.kv_dtype,
+                      seed=w.seed + 1, pool_factor=1.0, logits_soft_cap=w.logits_soft_cap,
+                      window_left=w.window_left, kv_store_scale=w.kv_store_scale,
+                      k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=w.sm_scale,
+                      o_dtype=w.o_dtype)
+        return sw, W.make_q(sw), W.make_pool(sw)
+
+    def run(sw, q, pool):
+        code = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+        t0 = time.perf_counter()
+        oracle.batch_decode_pool(sw.indptr, sw.indices, sw.last_page_len, W.raw_bits(q),
+                                 code[sw.q_dtype], W.raw_bits(pool), code[sw.kv_dtype], sw.layout,
+                                 sm_scale=sw.sm_scale, logits_soft_cap=sw.logits_soft_cap,
+                                 window_left=sw.window_left, k_scale=sw.k_scale,
+                                 v_scale=sw.v_scale)
+        return time.perf_counter() - t0
+
+    # calibrate on one request, then size the sample to the budget
+    cal = build(order[:1])
+    t_cal = max(run(*cal), 1e-4)
+    rate = algorithmic_bytes(cal[0]) / t_cal
+    target = rate * budget_s
+    acc, take = 0, []
+    full = algorithmic_bytes(w) / max(1, w.batch)
+    for i in order:
+        take.append(int(i))
+        acc += full
+        if acc >= target:
+            break
+    sw, q, pool = build(np.asarray(take))
+    return sw, q, pool, run
+
+
+def cpu_baseline(w, budget_s: float):
+    import oracle
+    sw, q, pool, run = _host_sample(w, budget_s)
+    t = run(sw, q, pool)
+    b = algorithmic_bytes(sw)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{sw.batch} of {w.batch} requests of one layer "
+                      f"({int(np.sum(sw.kv_lens))} tokens), fp64 oracle, {t:.1f} s"}
+
+
+def reference_arm(args, w):
+    import oracle
+    steps, warmup = args.steps, args.warmup
+    per_step = max(1.0, min(20.0, 150.0 / max(1, steps + warmup)))
+    sw, q, pool, run = _host_sample(w, per_step)
+    for _ in range(warmup):
+        run(sw, q, pool)
+    times = [run(sw, q, pool) for _ in range(steps)]
+    t = sum(times)
+    b = algorithmic_bytes(sw) * steps
+    val = b / t / 1e9
+    out = {
+        "metric": METRIC, "impl": "reference", "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warmup, "ms_per_step": t / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, args),
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{sw.batch} of {w.batch} requests of one layer per step "
+                                   f"({int(np.sum(sw.kv_lens))} tokens)"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def config_of(w, args):
+    return {"workload": describe(w), "batch": w.batch, "layers": w.layers,
+            "kv_tokens": int(np.sum(w.kv_lens)),
+            "l2": "inputs larger than L2 (each call streams its own pool)"
+            if algorithmic_bytes(w) > 4 * L2_BYTES else "L2 flushed between calls",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def gpu_arm(args, w, rank, world):
+    import torch
+
+    import workloads as W
+    from paged_kv_decode_23_gb300 import BatchDecodePagedKV
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    layers = w.layers
+    qs = [W.make_q(w, device=dev, layer=l) for l in range(layers)]
+    pools = [W.make_pool(w, device=dev, layer=l) for l in range(layers)]
+    outs = [torch.empty_like(qs[0], dtype=W.TORCH_DTYPES[w.o_dtype]) for _ in range(layers)]
+    lses = [torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device=dev)
+            for _ in range(layers)]
+    indices = torch.from_numpy(w.indices).to(dev)
+    indptr_t = torch.from_numpy(w.indptr)
+    lpl_t = torch.from_numpy(w.last_page_len)
+    ws = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    dec = BatchDecodePagedKV(ws, w.layout, int_workspace_buffer=torch.zeros(
+        16 << 20, dtype=torch.uint8, device=dev))
+    plan_kw = dict(q_data_type=W.TORCH_DTYPES[w.q_dtype], kv_data_type=W.TORCH_DTYPES[w.kv_dtype],
+                   o_data_type=W.TORCH_DTYPES[w.o_dtype], sm_scale=w.sm_scale,
+                   logits_soft_cap=w.logits_soft_cap or None, window_left=w.window_left,
+                   fixed_split_size=w.fixed_split_size or None,
+                   disable_split_kv=w.disable_split_kv)
+    if args.kernel != "auto":
+        plan_kw["use_tensor_cores"] = args.kernel == "tc"
+    flush = None
+    if algorithmic_bytes(w) <= 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    n_calls = layers
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_calls * args.steps)]
+
+    def step(k=None):
+        dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                 w.page_size, **plan_kw)
+        for l in range(layers):
+            if flush is not None:
+                flush.fill_(float(l))
+            e = ev[k * n_calls + l] if k is not None else None
+            dec.run(qs[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale, out=outs[l],
+                    lse=lses[l], timing_events=e)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert dec.check_status() == 0, "device status word reports a failure"
+    n_merge = 1 if _has_merges(w, dec) else 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(k)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    assert dec.check_status() == 0, "device status word reports a failure"
+
+    # end to end through the public API with host buffers: q / page table in, o / lse out
+    q_host = [q.cpu().pin_memory() for q in qs]
+    o_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    l_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in lses]
+    idx_host = torch.from_numpy(w.indices).pin_memory()
+    q_dev = [torch.empty_like(q) for q in qs]
+    idx_dev = torch.empty_like(indices)
+
+    def e2e_step():
+        idx_dev.copy_(idx_host, non_blocking=True)
+        dec.plan(indptr_t, idx_dev, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                 w.page_size, **plan_kw)
+        for l in range(layers):
+            if flush is not None:
+                flush.fill_(float(l))
+            q_dev[l].copy_(q_host[l], non_blocking=True)
+            dec.run(q_dev[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale, out=outs[l],
+                    lse=lses[l])
+            o_host[l].copy_(outs[l], non_blocking=True)
+            l_host[l].copy_(lses[l], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    h2d = sum(q.numel() * q.element_size() for q in q_host) + idx_host.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in o_host) + sum(
+        x.numel() * x.element_size() for x in l_host)
+
+    if world > 1:
+        t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total, e2e_s = float(t[0]), float(t[1])
+
+    bytes_call = algorithmic_bytes(w)
+    bytes_step = bytes_call * layers
+    ms_step = ms_total / args.steps
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    kern_avg_ms = statistics.mean(kern_ms)
+    achieved = bytes_call / (kern_avg_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": w.kv_dtype if w.kv_dtype == w.q_dtype else f"{w.q_dtype}/{w.kv_dtype}",
+        "data": "synthetic", "config": config_of(w, args),
+        "us_per_call": ms_step * 1e3 / layers,
+        "pct_of_hbm_peak": 100.0 * (value / world) / peak,
+        "peak_kind": peak_kind,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": args.traffic,
+                     "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
+                     "algorithmic_bytes_per_launch": bytes_call},
+        "e2e": {"value": world * bytes_step / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s / args.steps * 1e3},
+        "gpu_launches": args.steps * layers * (1 + n_merge),
+        "clocks": clk,
+    }
+    return res
+
+
+def _has_merges(w, dec):
+    from paged_kv_decode_23_gb300 import plan_host
+    p = plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                  w.page_size, window_left=w.window_left, fixed_split_size=w.fixed_split_size,
+                  disable_split_kv=w.disable_split_kv,
+                  kv_dtype={"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype])
+    return len(p["merges"]) > 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="uniform",
+                    choices=["worked", "uniform", "lognormal", "long", "mix"])
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per decode launch from an ncu capture of this kernel")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    import workloads as W
+    w = W.workload(args.workload)
+    if args.layers:
+        w.layers = args.layers
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, w)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = gpu_arm(args, w, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

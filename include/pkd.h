@@ -1,0 +1,179 @@
+/*
+ * pkd.h -- C ABI of libpkd: batch decode attention over a paged KV cache on one GB300 GPU.
+ *
+ * The calls mirror the plan/run split of the FlashInfer attention API page
+ * (docs.flashinfer.cn, api/attention.html), class BatchDecodeWithPagedKVCacheWrapper:
+ *   - the constructor takes a user-owned float workspace for split-KV partial results and a
+ *     KV layout (NHD or HND)                                  -> pkd_create
+ *   - reset_workspace_buffer(float_ws, int_ws)                -> pkd_reset_workspace
+ *   - plan(indptr, indices, last_page_len, num_qo_heads, num_kv_heads, head_dim, page_size,
+ *          window_left, logits_soft_cap, q/kv/o data types, sm_scale, fixed_split_size,
+ *          disable_split_kv) builds auxiliary data once and reuses it over many run calls
+ *                                                             -> pkd_plan
+ *   - run(q, paged_kv_cache, q_scale, k_scale, v_scale, out, lse) -> (o, lse)
+ *                                                             -> pkd_run
+ *
+ * Conventions for every call:
+ *   - All functions return PKD_OK (0) or a negative PKD_ERR_* code.  No exception, abort or
+ *     exit crosses this boundary.  pkd_last_error() returns a message for the most recent
+ *     failure on the calling thread.
+ *   - "device" pointers are CUDA device (or managed) addresses on the current device;
+ *     "host" pointers are ordinary CPU memory.  Every buffer is owned by the caller.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - dtype codes: PKD_DTYPE_F16 (IEEE half), PKD_DTYPE_BF16, PKD_DTYPE_E4M3 (fp8 e4m3fn,
+ *     KV only).
+ *
+ * Semantics (the page fixes the shapes; these readings fill what it leaves open):
+ *   kv_len[i] = page_size * (indptr[i+1] - indptr[i] - 1) + last_page_len[i]  (0 if the
+ *   request has no page); token t of request i is slot t % page_size of page
+ *   indices[indptr[i] + t / page_size]; qo head g reads kv head g / (Hq / Hkv);
+ *   x_t = sm_scale * q_scale * k_scale * <q, K_t>; s_t = cap * tanh(x_t / cap) if cap > 0
+ *   else x_t; the attended keys are t >= kv_len - 1 - window_left (all keys if
+ *   window_left < 0); o = v_scale * sum_t softmax(s)_t V_t; lse = ln(sum_t exp(s_t)).
+ *   A request with no attended key gets o = 0 and lse = -inf.
+ */
+#ifndef PKD_H_
+#define PKD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKD_OK 0
+#define PKD_ERR_INVALID_ARG (-1)         /* malformed table, shape, dtype or pointer */
+#define PKD_ERR_NOT_PLANNED (-2)         /* pkd_run before a successful pkd_plan */
+#define PKD_ERR_WORKSPACE_TOO_SMALL (-3) /* see pkd_workspace_bytes */
+#define PKD_ERR_CUDA (-4)                /* a CUDA runtime/driver call failed */
+#define PKD_ERR_UNSUPPORTED (-5)         /* valid but not built (head_dim, page_size, dtypes) */
+#define PKD_ERR_DEVICE (-6)              /* a kernel reported an error in the status word */
+
+#define PKD_DTYPE_F16 0
+#define PKD_DTYPE_BF16 1
+#define PKD_DTYPE_E4M3 2
+
+#define PKD_LAYOUT_NHD 0 /* page block [page_size, num_kv_heads, head_dim] */
+#define PKD_LAYOUT_HND 1 /* page block [num_kv_heads, page_size, head_dim] */
+
+/* Kernel choice for pkd_plan's use_tensor_cores argument (the page's use_tensor_cores). */
+#define PKD_KERNEL_AUTO (-1)
+#define PKD_KERNEL_CUDA_CORE 0
+#define PKD_KERNEL_TENSOR_CORE 1
+
+typedef struct pkd_handle pkd_handle;
+
+/*
+ * Create a handle.  float_ws (device, >= 256-byte aligned) receives split-KV partial
+ * outputs and lses; int_ws (device, >= 256-byte aligned) receives the work list, the merge
+ * list and a device status word.  Their needed sizes depend on the plan
+ * (pkd_workspace_bytes); 128 MiB of float workspace covers every plan whose split slots
+ * times num_qo_heads times head_dim stays under 32 M floats.  kv_layout: PKD_LAYOUT_*.
+ * The handle keeps the pointers; the caller keeps the buffers alive until pkd_destroy.
+ */
+int pkd_create(pkd_handle** out, void* float_ws, size_t float_ws_bytes, void* int_ws,
+               size_t int_ws_bytes, int kv_layout);
+
+/* Replace both workspaces (FlashInfer's reset_workspace_buffer).  Drops the current plan. */
+int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, void* int_ws,
+                        size_t int_ws_bytes);
+
+/*
+ * Plan a batch.  Host work O(batch + chunks), then one asynchronous host->device copy of
+ * the work list into int_ws on `stream`.  Not capturable in a CUDA graph.
+ *   indptr_host [batch+1], last_page_len_host [batch]: host int32 copies of the page table
+ *     (indptr non-decreasing from 0; 1 <= last_page_len <= page_size for requests that have
+ *     pages; ignored for requests without pages).
+ *   indices_dev [num_indices]: device int32 physical page ids, num_indices >= indptr[batch].
+ *     The pointer is stored and read by every later pkd_run: keep it valid and unchanged.
+ *     Ids outside [0, num_pages) read zeros (the hardware bounds-checks them).
+ *   num_qo_heads must be a multiple of num_kv_heads.  head_dim in {64, 128, 256}
+ *   (e4m3 KV: {128, 256}).  page_size a power of two in [8, 256].
+ *   sm_scale: NaN selects 1/sqrt(head_dim).  logits_soft_cap <= 0: no cap.
+ *   window_left < 0: no window.  fixed_split_size > 0: split every request into chunks of
+ *   that many pages counted from its first page, so the result of a request does not depend
+ *   on the rest of the batch; disable_split_kv != 0: one chunk per request; otherwise a
+ *   heuristic sizes chunks to fill the GPU.
+ *   q_dtype / o_dtype: F16 or BF16, equal; kv_dtype: q_dtype or E4M3.
+ *   use_tensor_cores: PKD_KERNEL_AUTO, PKD_KERNEL_CUDA_CORE or PKD_KERNEL_TENSOR_CORE.
+ * Errors: INVALID_ARG (shapes, table), UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
+ */
+int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page_len_host,
+             int batch, const int32_t* indices_dev, int64_t num_indices, int num_qo_heads,
+             int num_kv_heads, int head_dim, int page_size, float sm_scale,
+             float logits_soft_cap, int window_left, int fixed_split_size,
+             int disable_split_kv, int q_dtype, int kv_dtype, int o_dtype,
+             int use_tensor_cores, void* stream);
+
+/*
+ * Run the planned batch on one layer's KV pool.  Asynchronous on `stream`; never syncs.
+ *   q (device) [batch, num_qo_heads, head_dim], contiguous, q_dtype.
+ *   k_base / v_base (device): element (page, slot, head, 0) of K / V lives at
+ *     base + page*kv_strides[0] + slot*kv_strides[1] + head*kv_strides[2] (elements of
+ *     kv_dtype, head_dim contiguous).  A 5-D pool [pages, 2, ...] passes v_base =
+ *     k_base + its K/V stride; a (k_cache, v_cache) pair passes the two tensors.  Bases must
+ *     be 16-byte aligned and the strides multiples of 16 bytes.  The two inner strides must
+ *     match the handle's layout (NHD: slot stride > head stride; HND: the reverse).
+ *   num_pages: pages in the pool (the extent of the page axis).
+ *   q_scale, k_scale, v_scale: calibration scales (1.0 when unused).
+ *   o (device) [batch, num_qo_heads, head_dim] o_dtype; lse (device) [batch, num_qo_heads]
+ *     float32 natural log, or NULL to skip it.
+ * Launches one decode kernel, plus one merge kernel when any request was split.
+ */
+int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
+            int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
+            float v_scale, void* o, float* lse, void* stream);
+
+/* Same as pkd_run, and records ev_start / ev_end (cudaEvent_t as void*, may be NULL)
+ * immediately before and after the decode kernel's launch, so a caller can time that
+ * kernel alone on its own stream. */
+int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
+                  int64_t num_pages, const int64_t kv_strides[3], float q_scale,
+                  float k_scale, float v_scale, void* o, float* lse, void* stream,
+                  void* ev_start, void* ev_end);
+
+/* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
+int pkd_destroy(pkd_handle* h);
+
+/* Message of the last failure on this thread ("" if none).  Valid until the next call. */
+const char* pkd_last_error(void);
+
+/*
+ * Workspace bytes a plan with these arguments needs (host-only; no CUDA call).  Arguments
+ * as in pkd_plan; num_sms is the SM count the heuristic assumes (0 = 152).
+ */
+int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len_host,
+                        int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                        int page_size, int window_left, int fixed_split_size,
+                        int disable_split_kv, int kv_dtype, int use_tensor_cores, int num_sms,
+                        size_t* float_ws_bytes, size_t* int_ws_bytes);
+
+/*
+ * The planner alone (host-only; no CUDA call), for inspection and tests.  Writes up to
+ * max_items work items of 8 int32 each:
+ *   {request, first page index into `indices`, chunk start token, first attended token,
+ *    end token, partial slot (-1 = final), 0, 0}   (tokens count from the request's start)
+ * in launch order, and up to max_merges merge entries of 4 int32 {request, first slot,
+ * chunk count, 0}.  n_items / n_merges / n_slots receive the full counts.  kernel_out
+ * receives the chosen PKD_KERNEL_* and tile_tokens_out the tokens per pipeline stage.
+ */
+int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
+                  int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                  int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
+                  int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
+                  int32_t* merges_out, int max_merges, int* n_items, int* n_merges,
+                  int* n_slots, int* kernel_out, int* tile_tokens_out);
+
+/*
+ * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no
+ * kernel since the last plan or check reported a problem, else a bit set: 1 = a pipeline
+ * wait timed out (the kernel gave up and left its outputs incomplete).
+ */
+int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H_ */

@@ -1,0 +1,710 @@
+// decode_kernels.cuh -- batch decode attention over a paged KV cache, sm_103a.
+//
+// What one CTA computes (FlashInfer attention API page, BatchDecodeWithPagedKVCacheWrapper,
+// plan()/run()): for one work item (a chunk of one request's KV tokens) and one kv head, the
+// attention of the group's qo heads (GQA: qo head g reads kv head g / group) over the
+// chunk's attended tokens: s_t = soft_cap(sm_scale * <q, k_t>), online softmax, o = sum p_t v_t.
+//
+// Structure (one CTA = NW consumer warps + 1 producer warp):
+//   producer  streams the chunk tile by tile (TS tokens per tile) with 4-D TMA tensor loads:
+//             one box per (page, 128-byte column block, K|V), the page id read from the CSR
+//             `indices`; the box lands 128-byte swizzled in a shared-memory stage; completion
+//             is an mbarrier transaction count.  NSTAGES stages ring between producer and
+//             consumers (full / empty mbarriers, every wait bounded).
+//   consumers each own 16 tokens of every tile and keep their own online-softmax state.
+//             Tensor-core variant: S^T = K_tile * Q^T with mma.m16n8k16 (16 tokens on M, 8
+//             qo heads on N, head_dim on K), the P^T operand built in registers with
+//             movmatrix, O^T += V_tile^T * P^T (ldmatrix.trans).  CUDA-core variant: lanes
+//             own head_dim slices, dot products are finished with a 31-shuffle
+//             reduce-scatter over 32 (token, head) pairs, P*V with fp32 FMAs.
+//   epilogue  merges the warps' states in shared memory and writes either the final o / lse
+//             or an fp32 partial (normalised o, base-2 lse) for merge_states.
+// Slots past a request's last token and pages outside the chunk are loaded or left stale;
+// their logits are replaced by -inf (a select, so NaN/Inf garbage cannot leak) and their V
+// rows are zeroed or skipped before P*V.
+#pragma once
+
+#include <type_traits>
+
+#include "pkd_device.cuh"
+#include "pkd_internal.h"
+
+namespace pkd {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, bool CONV>
+struct DecodeGeom {
+  static constexpr int NW = TS / 16;  // consumer warps; each owns 16 tokens of a tile
+  static constexpr int NCONS = NW * 32;
+  static constexpr int THREADS = NCONS + 32;
+  static constexpr int KV_ELT = KV_FP8 ? 1 : 2;
+  static constexpr int ROW_BYTES = D * KV_ELT;
+  static constexpr int NBLK = ROW_BYTES / 128;  // 128-byte column blocks per K/V row
+  static constexpr int BOX_ELEMS = 128 / KV_ELT;
+  static constexpr int TILE_BYTES = TS * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int CONV_BYTES = CONV ? NW * 16 * D * 2 : 0;  // 16-bit copy of 16 rows/warp
+  static constexpr int EPI_BYTES = NW * (8 * D + 16) * 4;
+  static constexpr int PIPE_BYTES = NSTAGES * STAGE_BYTES + CONV_BYTES;
+  static constexpr int SMEM_BYTES = (PIPE_BYTES > EPI_BYTES ? PIPE_BYTES : EPI_BYTES) + 1024;
+  static_assert(ROW_BYTES % 128 == 0, "K/V rows must be whole 128-byte blocks");
+  static_assert(TS % 16 == 0 && NW >= 1 && NW <= 8, "tile of 16-token warp slices");
+};
+
+struct BlockCoords {
+  WorkItem it;
+  int kvh;    // kv head
+  int g0;     // first qo head of this CTA
+  int gcnt;   // qo heads of this CTA
+  int j0;     // first tile (relative to the chunk start)
+  int ntiles;
+};
+
+template <int TS, int HEADS>
+__device__ __forceinline__ BlockCoords block_coords(const DecodeParams& p) {
+  BlockCoords b;
+  const int per_item = p.num_kv_heads * p.gslices;
+  const int item = blockIdx.x / per_item;
+  const int rem = blockIdx.x - item * per_item;
+  b.kvh = rem / p.gslices;
+  const int gs = rem - b.kvh * p.gslices;
+  b.it = p.items[item];
+  b.g0 = b.kvh * p.group + gs * HEADS;
+  b.gcnt = min(HEADS, p.group - gs * HEADS);
+  if (b.it.tok_end > b.it.tok_begin) {
+    b.j0 = (b.it.tok_begin - b.it.chunk_tok0) / TS;
+    b.ntiles = (b.it.tok_end - b.it.chunk_tok0 + TS - 1) / TS - b.j0;
+  } else {
+    b.j0 = 0;
+    b.ntiles = 0;
+  }
+  return b;
+}
+
+// ------------------------------------------------------------------------------ producer
+template <class G, int TS, int NSTAGES>
+__device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
+                                        uint32_t full0, uint32_t empty0, volatile int* abort_flag,
+                                        int lane) {
+  using namespace dev;
+  const int ps = p.page_size;
+  const int br = ps < TS ? ps : TS;  // rows per box: a whole page, or a tile inside a page
+  const int boxes = TS / br;
+  const uint32_t tx_per_box = 2u * G::NBLK * br * 128u;
+  const uint64_t pol = policy_evict_first();
+  if (lane == 0) {
+    prefetch_tmap(&p.tmap_k);
+    prefetch_tmap(&p.tmap_v);
+  }
+  int issued = 0;
+  bool ok = true;
+  for (int i = 0; i < b.ntiles; ++i) {
+    const int s = i % NSTAGES;
+    if (i >= NSTAGES && !mbar_wait(empty0 + 8 * s, ((i / NSTAGES) - 1) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const int t0 = b.it.chunk_tok0 + (b.j0 + i) * TS;
+    const int bt0 = t0 + lane * br;
+    const bool need = lane < boxes && bt0 < b.it.tok_end && bt0 + br > b.it.tok_begin;
+    int pid = 0;
+    if (need) pid = __ldg(p.indices + b.it.page_base + bt0 / ps);
+    const unsigned m = __ballot_sync(0xffffffffu, need);
+    if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, __popc(m) * tx_per_box);
+    __syncwarp();
+    if (need) {
+      const int slot0 = bt0 % ps;
+      const int c1 = p.hnd ? slot0 : b.kvh;
+      const int c2 = p.hnd ? b.kvh : slot0;
+      const uint32_t kdst = smem + s * G::STAGE_BYTES + lane * br * 128;
+#pragma unroll
+      for (int blk = 0; blk < G::NBLK; ++blk) {
+        tma_load_4d(kdst + blk * TS * 128, &p.tmap_k, blk * G::BOX_ELEMS, c1, c2, pid,
+                    full0 + 8 * s, pol);
+        tma_load_4d(kdst + G::TILE_BYTES + blk * TS * 128, &p.tmap_v, blk * G::BOX_ELEMS, c1, c2,
+                    pid, full0 + 8 * s, pol);
+      }
+    }
+    issued = i + 1;
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    if (lane == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      // Let the copies already in flight land before the CTA may exit.
+      volatile int never = 0;
+      for (int u = issued - NSTAGES < 0 ? 0 : issued - NSTAGES; u < issued; ++u)
+        mbar_wait(full0 + 8 * (u % NSTAGES), (u / NSTAGES) & 1, &never);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ epilogue
+// Shared-memory image of the consumer warps' states: acc[w][g][d] (unnormalised, relative
+// to m[w][g]), m[w][g] (base-2 running max), l[w][g] (sum of exp2(s - m)).
+template <int D>
+struct EpiView {
+  float* acc;
+  float* m;
+  float* l;
+  __device__ __forceinline__ EpiView(uint8_t* base, int nw) {
+    acc = reinterpret_cast<float*>(base);
+    m = acc + nw * 8 * D;
+    l = m + nw * 8;
+  }
+};
+
+template <typename TQ, int D, int NW>
+__device__ __forceinline__ void combine_and_store(const DecodeParams& p, const BlockCoords& b,
+                                                  const EpiView<D>& e, int tid, bool aborted) {
+  using namespace dev;
+  constexpr int NCONS = NW * 32;
+  constexpr int D8 = D / 8;
+  for (int u = tid; u < b.gcnt * D8; u += NCONS) {
+    const int g = u / D8;
+    const int d0 = (u - g * D8) * 8;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, e.m[w * 8 + g]);
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = 0.f;
+    float L = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = fast_exp2(e.m[w * 8 + g] - M);
+        L += f * e.l[w * 8 + g];
+        const float4* a = reinterpret_cast<const float4*>(e.acc + (w * 8 + g) * D + d0);
+        const float4 a0 = a[0], a1 = a[1];
+        o[0] += f * a0.x; o[1] += f * a0.y; o[2] += f * a0.z; o[3] += f * a0.w;
+        o[4] += f * a1.x; o[5] += f * a1.y; o[6] += f * a1.z; o[7] += f * a1.w;
+      }
+    }
+    const float inv = L > 0.f ? p.v_scale / L : 0.f;
+    const float lse2 = L > 0.f ? M + log2f(L) : kNegInf;
+    const int qo = b.g0 + g;
+    if (aborted) continue;
+    if (b.it.out_slot < 0) {
+      uint4 v;
+      v.x = pack2<TQ>(o[0] * inv, o[1] * inv);
+      v.y = pack2<TQ>(o[2] * inv, o[3] * inv);
+      v.z = pack2<TQ>(o[4] * inv, o[5] * inv);
+      v.w = pack2<TQ>(o[6] * inv, o[7] * inv);
+      TQ* dst = reinterpret_cast<TQ*>(p.o) + ((size_t)b.it.req * p.num_qo_heads + qo) * D + d0;
+      *reinterpret_cast<uint4*>(dst) = v;
+      if (d0 == 0 && p.lse) p.lse[(size_t)b.it.req * p.num_qo_heads + qo] = lse2 * kLn2;
+    } else {
+      float* dst = p.part_o + ((size_t)b.it.out_slot * p.num_qo_heads + qo) * D + d0;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+      if (d0 == 0) p.part_lse[(size_t)b.it.out_slot * p.num_qo_heads + qo] = lse2;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ score
+__device__ __forceinline__ float score_log2(float dot, float scale_qk, float cap_log2) {
+  const float x = dot * scale_qk;
+  return cap_log2 > 0.f ? cap_log2 * tanhf(x) : x;
+}
+
+// ------------------------------------------------------------------------------ tensor core
+// Loads the B fragments of Q^T (mma k = head_dim, n = 8 qo heads) for this lane.  For e4m3
+// KV the MMA runs in fp16: q is scaled by 2^-qexp (exact) so it fits fp16's range; the
+// caller multiplies the scores back by 2^qexp.
+template <typename TQ, typename T, int D>
+__device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockCoords& b, int lane,
+                                             uint32_t (&qb)[D / 16][2], float& qmul) {
+  using namespace dev;
+  const int g = lane >> 2, tig = lane & 3;
+  const bool live = g < b.gcnt;
+  const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
+                   ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D;
+  qmul = 1.f;
+  if constexpr (sizeof(TQ) == sizeof(T) && std::is_same<TQ, T>::value) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qb[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + tig * 2) : 0u;
+      qb[kk][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + tig * 2) : 0u;
+    }
+  } else {
+    float2 f[D / 16][2];
+    float amax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t raw =
+            live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + h * 8 + tig * 2) : 0u;
+        f[kk][h] = unpack2<TQ>(raw);
+        amax = fmaxf(amax, fmaxf(fabsf(f[kk][h].x), fabsf(f[kk][h].y)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, off));
+    int qexp = 0;
+    if (amax > 16384.f) qexp = ilogbf(amax) - 13;  // keeps |q| * 2^-qexp below 2^15
+    const float down = exp2f(static_cast<float>(-qexp));
+    qmul = exp2f(static_cast<float>(qexp));
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) qb[kk][h] = pack2<T>(f[kk][h].x * down, f[kk][h].y * down);
+  }
+}
+
+// Converts this warp's 16 rows of an e4m3 tile into the warp's fp16 staging area (same
+// swizzled layout, 16 rows per column block).  Rows outside [vlo, vhi) become zeros when
+// `zero_invalid` is set.
+template <int D, int TS>
+__device__ __forceinline__ void convert_rows_e4m3(uint32_t src_tile, int row0, uint32_t dst, int vlo,
+                                                  int vhi, bool zero_invalid, int lane) {
+  using namespace dev;
+  constexpr int C8 = D / 16;  // 16-byte chunks per fp8 row
+#pragma unroll
+  for (int k = 0; k < (16 * C8) / 32; ++k) {
+    const int ci = lane + 32 * k;
+    const int r = ci / C8;
+    const int c = ci - r * C8;
+    uint4 in;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(in.x), "=r"(in.y), "=r"(in.z), "=r"(in.w)
+                 : "r"(src_tile + swz_off(row0 + r, c, TS)));
+    uint4 lo, hi;
+    if (zero_invalid && (r < vlo || r >= vhi)) {
+      lo = make_uint4(0, 0, 0, 0);
+      hi = lo;
+    } else {
+      lo.x = e4m3x2_to_half2(in.x & 0xffff); lo.y = e4m3x2_to_half2(in.x >> 16);
+      lo.z = e4m3x2_to_half2(in.y & 0xffff); lo.w = e4m3x2_to_half2(in.y >> 16);
+      hi.x = e4m3x2_to_half2(in.z & 0xffff); hi.y = e4m3x2_to_half2(in.z >> 16);
+      hi.z = e4m3x2_to_half2(in.w & 0xffff); hi.w = e4m3x2_to_half2(in.w >> 16);
+    }
+    const uint32_t d_lo = dst + swz_off(r, 2 * c, 16);
+    const uint32_t d_hi = dst + swz_off(r, 2 * c + 1, 16);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d_lo), "r"(lo.x), "r"(lo.y),
+                 "r"(lo.z), "r"(lo.w)
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d_hi), "r"(hi.x), "r"(hi.y),
+                 "r"(hi.z), "r"(hi.w)
+                 : "memory");
+  }
+}
+
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES>
+__device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
+                                           uint32_t full0, uint32_t empty0, volatile int* abort_flag,
+                                           int warp, int lane, float (&m2)[2], float (&lsum)[2],
+                                           float (&acc)[D / 16][4]) {
+  using namespace dev;
+  using T = typename std::conditional<KV_FP8, __half, TQ>::type;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, KV_FP8>;
+  uint32_t qb[D / 16][2];
+  float qmul;
+  load_q_frags<TQ, T, D>(p, b, lane, qb, qmul);
+  const float scale_qk = p.scale_qk * qmul;
+  const float cap_log2 = p.cap_log2;
+  const uint32_t conv = smem + NSTAGES * G::STAGE_BYTES + warp * (16 * D * 2);
+  const int g_row = lane >> 2;
+
+  for (int i = 0; i < b.ntiles; ++i) {
+    const int s = i % NSTAGES;
+    if (!mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag)) {
+      *abort_flag = 1;
+      atomicOr(p.status, kStatusTimeout);
+      break;
+    }
+    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
+    const int vlo = max(0, b.it.tok_begin - t_w);
+    const int vhi = min(16, b.it.tok_end - t_w);
+    const uint32_t ktile = smem + s * G::STAGE_BYTES;
+    const uint32_t vtile = ktile + G::TILE_BYTES;
+    bool wrote_stage = false;
+    if (vhi > vlo) {
+      const bool partial = vlo > 0 || vhi < 16;
+      uint32_t kview;
+      int rb, r0;
+      if constexpr (KV_FP8) {
+        convert_rows_e4m3<D, TS>(ktile, warp * 16, conv, vlo, vhi, false, lane);
+        __syncwarp();
+        kview = conv;
+        rb = 16;
+        r0 = 0;
+      } else {
+        kview = ktile;
+        rb = TS;
+        r0 = warp * 16;
+        if (partial) {
+          // Zero the V rows this slice does not attend, so 0 * garbage cannot reach O.
+          constexpr int CPR = D / 8;  // 16-byte chunks per 16-bit row
+          for (int idx = lane; idx < 16 * CPR; idx += 32) {
+            const int r = idx / CPR;
+            if (r < vlo || r >= vhi) {
+              const uint32_t a = vtile + swz_off(r0 + r, idx - r * CPR, TS);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+            }
+          }
+          wrote_stage = true;
+          __syncwarp();
+        }
+      }
+      // ---- S^T = K * Q^T : rows = 16 tokens, cols = 8 qo heads
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t a[4];
+          ldsm_x4(kview + swz_off(r0 + row, kk * 2 + csel, rb), a);
+          mma_16816<T>(c, a, qb[kk][0], qb[kk][1]);
+        }
+      }
+      if constexpr (KV_FP8) {
+        __syncwarp();
+        convert_rows_e4m3<D, TS>(vtile, warp * 16, conv, vlo, vhi, true, lane);
+        __syncwarp();
+      }
+      // ---- online softmax over the 16 tokens, per qo-head column
+      float sc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g_row + (e >= 2 ? 8 : 0);
+        const float sv = score_log2(c[e], scale_qk, cap_log2);
+        sc[e] = (r >= vlo && r < vhi) ? sv : kNegInf;
+      }
+      float alpha[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(sc[j], sc[j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 16));
+        const float mnew = fmaxf(m2[j], mx);
+        const float ref = mnew == kNegInf ? 0.f : mnew;
+        alpha[j] = fast_exp2(m2[j] - ref);
+        sc[j] = fast_exp2(sc[j] - ref);
+        sc[j + 2] = fast_exp2(sc[j + 2] - ref);
+        lsum[j] = lsum[j] * alpha[j] + sc[j] + sc[j + 2];
+        m2[j] = mnew;
+      }
+#pragma unroll
+      for (int mb = 0; mb < D / 16; ++mb) {
+        acc[mb][0] *= alpha[0];
+        acc[mb][1] *= alpha[1];
+        acc[mb][2] *= alpha[0];
+        acc[mb][3] *= alpha[1];
+      }
+      // ---- P^T as the B operand (k = token, n = qo head): transpose the C fragment
+      const uint32_t b0 = movmatrix_trans(pack2<T>(sc[0], sc[1]));
+      const uint32_t b1 = movmatrix_trans(pack2<T>(sc[2], sc[3]));
+      // ---- O^T += V^T * P^T : rows = head_dim (16 per block), cols = 8 qo heads
+      {
+        const uint32_t vview_ = KV_FP8 ? conv : vtile;
+        const int row = (lane & 7) + (lane >> 4) * 8;
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+          uint32_t a[4];
+          ldsm_x4_trans(vview_ + swz_off(r0 + row, mb * 2 + csel, rb), a);
+          mma_16816<T>(acc[mb], a, b0, b1);
+        }
+      }
+    }
+    if (wrote_stage) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane, float (&m2)[2],
+                                         float (&lsum)[2], float (&acc)[D / 16][4]) {
+  const int gr = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float l = lsum[j];
+    l += __shfl_xor_sync(~0u, l, 4);
+    l += __shfl_xor_sync(~0u, l, 8);
+    l += __shfl_xor_sync(~0u, l, 16);
+    if (gr == 0) {
+      e.m[warp * 8 + tig * 2 + j] = m2[j];
+      e.l[warp * 8 + tig * 2 + j] = l;
+    }
+  }
+  float* a = e.acc + warp * 8 * D;
+#pragma unroll
+  for (int mb = 0; mb < D / 16; ++mb) {
+    const int d = mb * 16 + gr;
+    a[(tig * 2) * D + d] = acc[mb][0];
+    a[(tig * 2 + 1) * D + d] = acc[mb][1];
+    a[(tig * 2) * D + d + 8] = acc[mb][2];
+    a[(tig * 2 + 1) * D + d + 8] = acc[mb][3];
+  }
+}
+
+// ------------------------------------------------------------------------------ CUDA core
+// Lane layout: lane owns head_dim elements [lane*EPL, lane*EPL + EPL) of every row.
+template <typename TQ, bool KV_FP8, int D>
+struct CcRow {
+  static constexpr int EPL = D / 32;
+  static constexpr int BYTES = EPL * (KV_FP8 ? 1 : 2);  // bytes a lane reads per row
+  // Loads this lane's slice of row r of a swizzled tile and widens it to fp32.
+  template <int TS>
+  __device__ __forceinline__ static void load(uint32_t tile, int r, int lane, float (&x)[EPL]) {
+    using namespace dev;
+    const int off = lane * BYTES;
+    const uint32_t a = tile + swz_off(r, off >> 4, TS) + (off & 15);
+    if constexpr (!KV_FP8) {
+      if constexpr (BYTES == 4) {
+        uint32_t v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+        const float2 f = unpack2<TQ>(v);
+        x[0] = f.x; x[1] = f.y;
+      } else if constexpr (BYTES == 8) {
+        uint32_t v0, v1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(a));
+        const float2 f0 = unpack2<TQ>(v0), f1 = unpack2<TQ>(v1);
+        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+      } else {
+        uint32_t v[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = unpack2<TQ>(v[k]);
+          x[2 * k] = f.x; x[2 * k + 1] = f.y;
+        }
+      }
+    } else {
+      if constexpr (BYTES == 4) {
+        uint32_t v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+        const float2 f0 = unpack2<__half>(e4m3x2_to_half2(v & 0xffff));
+        const float2 f1 = unpack2<__half>(e4m3x2_to_half2(v >> 16));
+        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+      } else {
+        uint32_t v0, v1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(a));
+        const uint32_t vv[2] = {v0, v1};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float2 f0 = unpack2<__half>(e4m3x2_to_half2(vv[k] & 0xffff));
+          const float2 f1 = unpack2<__half>(e4m3x2_to_half2(vv[k] >> 16));
+          x[4 * k] = f0.x; x[4 * k + 1] = f0.y; x[4 * k + 2] = f1.x; x[4 * k + 3] = f1.y;
+        }
+      }
+    }
+  }
+};
+
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int GP>
+__device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
+                                           uint32_t full0, uint32_t empty0, volatile int* abort_flag,
+                                           int warp, int lane, float& m2, float& lsum,
+                                           float (&acc)[GP][D / 32]) {
+  using namespace dev;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, false>;
+  using R = CcRow<TQ, KV_FP8, D>;
+  constexpr int EPL = R::EPL;
+  constexpr int TW = 32 / GP;  // tokens per reduce-scatter group
+  static_assert(GP >= 2 && GP <= 8 && 16 % TW == 0, "CUDA-core head group");
+  float qf[GP][EPL];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    const bool live = g < b.gcnt;
+    const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
+                     ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D + lane * EPL;
+#pragma unroll
+    for (int k = 0; k < EPL; k += 2) {
+      const float2 f = unpack2<TQ>(*reinterpret_cast<const uint32_t*>(qrow + k));
+      qf[g][k] = live ? f.x : 0.f;
+      qf[g][k + 1] = live ? f.y : 0.f;
+    }
+  }
+  const float scale_qk = p.scale_qk;
+  const float cap_log2 = p.cap_log2;
+  const int my_g = lane % GP;
+  const int my_j = lane / GP;
+
+  for (int i = 0; i < b.ntiles; ++i) {
+    const int s = i % NSTAGES;
+    if (!mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag)) {
+      *abort_flag = 1;
+      atomicOr(p.status, kStatusTimeout);
+      break;
+    }
+    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;
+    const int vlo = max(0, b.it.tok_begin - t_w);
+    const int vhi = min(16, b.it.tok_end - t_w);
+    const uint32_t ktile = smem + s * G::STAGE_BYTES;
+    const uint32_t vtile = ktile + G::TILE_BYTES;
+#pragma unroll
+    for (int grp = 0; grp < 16 / TW; ++grp) {
+      const int r0 = grp * TW;
+      if (r0 + TW <= vlo || r0 >= vhi) continue;  // warp-uniform
+      float part[32];
+#pragma unroll
+      for (int j = 0; j < TW; ++j) {
+        float kx[EPL];
+        R::template load<TS>(ktile, warp * 16 + r0 + j, lane, kx);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) d = fmaf(qf[g][e], kx[e], d);
+          part[j * GP + g] = d;
+        }
+      }
+      // reduce-scatter: lane l ends with the full dot product of pair l = j*GP + g
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < off; ++k) {
+          const float send = upper ? part[k] : part[k + off];
+          const float keep = upper ? part[k + off] : part[k];
+          part[k] = keep + __shfl_xor_sync(~0u, send, off);
+        }
+      }
+      const int r = r0 + my_j;
+      float sv = score_log2(part[0], scale_qk, cap_log2);
+      sv = (r >= vlo && r < vhi) ? sv : kNegInf;
+      float mx = sv;
+#pragma unroll
+      for (int off = GP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
+      const float mnew = fmaxf(m2, mx);
+      const float ref = mnew == kNegInf ? 0.f : mnew;
+      const float alpha = fast_exp2(m2 - ref);
+      const float pr = fast_exp2(sv - ref);
+      lsum = lsum * alpha + pr;
+      m2 = mnew;
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float a = __shfl_sync(~0u, alpha, g);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[g][e] *= a;
+      }
+#pragma unroll
+      for (int j = 0; j < TW; ++j) {
+        if (r0 + j < vlo || r0 + j >= vhi) continue;  // warp-uniform: skip unattended rows
+        float vx[EPL];
+        R::template load<TS>(vtile, warp * 16 + r0 + j, lane, vx);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float pj = __shfl_sync(~0u, pr, j * GP + g);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pj, vx[e], acc[g][e]);
+        }
+      }
+    }
+    (void)my_g;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+}
+
+template <int D, int GP>
+__device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane, float m2, float lsum,
+                                         float (&acc)[GP][D / 32]) {
+  constexpr int EPL = D / 32;
+  float l = lsum;
+#pragma unroll
+  for (int off = GP; off < 32; off <<= 1) l += __shfl_xor_sync(~0u, l, off);
+  if (lane < GP) {
+    e.m[warp * 8 + lane] = m2;
+    e.l[warp * 8 + lane] = l;
+  }
+  float* a = e.acc + warp * 8 * D;
+#pragma unroll
+  for (int g = 0; g < GP; ++g)
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) a[g * D + lane * EPL + k] = acc[g][k];
+}
+
+// ------------------------------------------------------------------------------ kernel
+// KIND: kTensorCore (HEADS = 8 qo heads per CTA) or kCudaCore (HEADS = GP).
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
+__global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES,
+                                             (KIND == kTensorCore && KV_FP8)>::THREADS, 1)
+    decode_paged_kernel(const __grid_constant__ DecodeParams p) {
+  using namespace dev;
+  constexpr bool CONV = (KIND == kTensorCore) && KV_FP8;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, CONV>;
+  constexpr int HEADS = KIND == kTensorCore ? 8 : GP;
+  __shared__ __align__(8) uint64_t bars[2 * NSTAGES];
+  __shared__ int abort_flag_s;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem_p =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem = smem_u32(smem_p);
+  const uint32_t full0 = smem_u32(&bars[0]);
+  const uint32_t empty0 = smem_u32(&bars[NSTAGES]);
+  volatile int* abort_flag = &abort_flag_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const BlockCoords b = block_coords<TS, HEADS>(p);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < NSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, G::NW);
+    }
+    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (abort_flag_s) return;  // an earlier launch reported a failure: touch nothing
+
+  if (warp == G::NW) {
+    produce<G, TS, NSTAGES>(p, b, smem, full0, empty0, abort_flag, lane);
+    return;
+  }
+  const EpiView<D> epi(smem_p, G::NW);
+  if constexpr (KIND == kTensorCore) {
+    float m2[2] = {kNegInf, kNegInf}, lsum[2] = {0.f, 0.f};
+    float acc[D / 16][4];
+#pragma unroll
+    for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+    consume_tc<TQ, KV_FP8, D, TS, NSTAGES>(p, b, smem, full0, empty0, abort_flag, warp, lane, m2,
+                                           lsum, acc);
+    named_bar_sync(1, G::NCONS);  // every consumer is done with the stages
+    stash_tc<D>(epi, warp, lane, m2, lsum, acc);
+  } else {
+    float m2 = kNegInf, lsum = 0.f;
+    float acc[GP][D / 32];
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) acc[g][k] = 0.f;
+    consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP>(p, b, smem, full0, empty0, abort_flag, warp, lane,
+                                               m2, lsum, acc);
+    named_bar_sync(1, G::NCONS);
+    stash_cc<D, GP>(epi, warp, lane, m2, lsum, acc);
+  }
+  named_bar_sync(1, G::NCONS);
+  combine_and_store<TQ, D, G::NW>(p, b, epi, threadIdx.x, *abort_flag != 0);
+}
+
+// ------------------------------------------------------------------------------ registry
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
+DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
+  constexpr bool CONV = (KIND == kTensorCore) && KV_FP8;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, CONV>;
+  DecodeKernel k;
+  k.kind = KIND;
+  k.q_dtype = q_dtype;
+  k.kv_dtype = kv_dtype;
+  k.head_dim = D;
+  k.heads_per_cta = KIND == kTensorCore ? 8 : GP;
+  k.fn = reinterpret_cast<const void*>(&decode_paged_kernel<TQ, KV_FP8, D, TS, NSTAGES, KIND, GP>);
+  k.threads = G::THREADS;
+  k.smem_bytes = G::SMEM_BYTES;
+  k.tile_tokens = TS;
+  return k;
+}
+
+}  // namespace pkd

@@ -1,0 +1,521 @@
+// pkd_api.cpp -- the C ABI declared in include/pkd.h: handle, plan, run, status.
+//
+// Mirrors FlashInfer's BatchDecodeWithPagedKVCacheWrapper (FlashInfer attention API page):
+// the constructor takes the workspaces and KV layout, plan() runs once per batch on the host
+// and leaves the auxiliary data in the int workspace, run() launches the kernels for one
+// layer's pool and may be called any number of times per plan.
+#include "../../include/pkd.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkd_internal.h"
+
+using namespace pkd;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+std::once_flag g_registry_once;
+std::vector<DecodeKernel> g_decode;
+std::vector<MergeKernel> g_merge;
+
+void init_registry() {
+  std::call_once(g_registry_once, [] {
+    register_decode_f16(g_decode);
+    register_decode_bf16(g_decode);
+    register_decode_e4m3(g_decode);
+    register_merge(g_merge);
+  });
+}
+
+const DecodeKernel* find_decode(int kind, int q_dtype, int kv_dtype, int head_dim, int heads) {
+  init_registry();
+  for (const auto& k : g_decode)
+    if (k.kind == kind && k.q_dtype == q_dtype && k.kv_dtype == kv_dtype &&
+        k.head_dim == head_dim && k.heads_per_cta == heads)
+      return &k;
+  return nullptr;
+}
+
+const MergeKernel* find_merge(int o_dtype, int head_dim) {
+  init_registry();
+  for (const auto& k : g_merge)
+    if (k.o_dtype == o_dtype && k.head_dim == head_dim) return &k;
+  return nullptr;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn(std::string* why) {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  static std::string err;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+      err = "cuTensorMapEncodeTiled is not available from the driver";
+    else
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn) *why = err;
+  return fn;
+}
+
+}  // namespace
+
+struct pkd_handle {
+  void* float_ws = nullptr;
+  size_t float_bytes = 0;
+  void* int_ws = nullptr;
+  size_t int_bytes = 0;
+  int layout = PKD_LAYOUT_NHD;
+  int device = 0;
+  int num_sms = 152;
+
+  bool planned = false;
+  Plan plan;
+  int batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, page_size = 0;
+  int q_dtype = 0, kv_dtype = 0, o_dtype = 0;
+  float sm_scale = 0.f, cap = 0.f;
+  const int32_t* indices = nullptr;
+  const DecodeKernel* kernel = nullptr;
+  const MergeKernel* merge = nullptr;
+
+  void* staging = nullptr;  // pinned copy of the work list for the async upload
+  size_t staging_bytes = 0;
+  cudaEvent_t staging_done = nullptr;
+  bool staging_pending = false;
+};
+
+namespace {
+
+// 4-D TMA view of one K or V pool: dims (d, head, slot, page) for NHD and (d, slot, head, page)
+// for HND, i.e. ordered by increasing stride; a box is 128 bytes of d by `box_rows` slots of
+// one head of one page, landing 128-byte swizzled in shared memory.
+int make_kv_tensor_map(CUtensorMap* map, const void* base, int kv_dtype, int head_dim, int page_size,
+                       int num_kv_heads, int64_t num_pages, const int64_t strides[3], int layout,
+                       int box_rows) {
+  std::string why;
+  EncodeTiledFn enc = get_encode_fn(&why);
+  if (!enc) return fail(PKD_ERR_CUDA, why);
+  const int elt = kv_dtype == kE4M3 ? 1 : 2;
+  const CUtensorMapDataType dt = kv_dtype == kF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : kv_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int64_t page_b = strides[0] * elt, slot_b = strides[1] * elt, head_b = strides[2] * elt;
+  cuuint64_t dims[4], gstr[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  if (layout == PKD_LAYOUT_NHD) {
+    dims[1] = (cuuint64_t)num_kv_heads;
+    dims[2] = (cuuint64_t)page_size;
+    gstr[0] = (cuuint64_t)head_b;
+    gstr[1] = (cuuint64_t)slot_b;
+    box[1] = 1;
+    box[2] = (cuuint32_t)box_rows;
+  } else {
+    dims[1] = (cuuint64_t)page_size;
+    dims[2] = (cuuint64_t)num_kv_heads;
+    gstr[0] = (cuuint64_t)slot_b;
+    gstr[1] = (cuuint64_t)head_b;
+    box[1] = (cuuint32_t)box_rows;
+    box[2] = 1;
+  }
+  dims[0] = (cuuint64_t)head_dim;
+  dims[3] = (cuuint64_t)num_pages;
+  gstr[2] = (cuuint64_t)page_b;
+  box[0] = (cuuint32_t)(128 / elt);
+  box[3] = 1;
+  CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, gstr, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[256];
+    std::snprintf(buf, sizeof buf,
+                  "cuTensorMapEncodeTiled failed (%d) for strides page=%lld slot=%lld head=%lld "
+                  "bytes",
+                  (int)r, (long long)page_b, (long long)slot_b, (long long)head_b);
+    return fail(PKD_ERR_INVALID_ARG, buf);
+  }
+  return PKD_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl, int batch,
+                      int hq, int hkv, int d, int ps, int window_left, int fixed_split,
+                      int disable_split, int kv_dtype, int use_tc, int num_sms) {
+  r->indptr = indptr;
+  r->last_page_len = lpl;
+  r->batch = batch;
+  r->num_qo_heads = hq;
+  r->num_kv_heads = hkv;
+  r->head_dim = d;
+  r->page_size = ps;
+  r->window_left = window_left;
+  r->fixed_split_size = fixed_split;
+  r->disable_split_kv = disable_split;
+  r->kv_dtype = kv_dtype;
+  r->use_tensor_cores = use_tc;
+  r->num_sms = num_sms;
+  if (use_tc < -1 || use_tc > 1) return fail(PKD_ERR_INVALID_ARG, "use_tensor_cores must be -1, 0 or 1");
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkd_last_error(void) { return g_last_error.c_str(); }
+
+int pkd_create(pkd_handle** out, void* float_ws, size_t float_ws_bytes, void* int_ws,
+               size_t int_ws_bytes, int kv_layout) {
+  if (!out) return fail(PKD_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (kv_layout != PKD_LAYOUT_NHD && kv_layout != PKD_LAYOUT_HND)
+    return fail(PKD_ERR_INVALID_ARG, "kv_layout must be PKD_LAYOUT_NHD or PKD_LAYOUT_HND");
+  if (!aligned(float_ws, 256) || !aligned(int_ws, 256))
+    return fail(PKD_ERR_INVALID_ARG, "workspaces must be 256-byte aligned");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  pkd_handle* h = new pkd_handle();
+  h->float_ws = float_ws;
+  h->float_bytes = float_ws_bytes;
+  h->int_ws = int_ws;
+  h->int_bytes = int_ws_bytes;
+  h->layout = kv_layout;
+  h->device = dev;
+  h->num_sms = sms;
+  e = cudaEventCreateWithFlags(&h->staging_done, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "cudaEventCreate");
+  }
+  *out = h;
+  g_last_error.clear();
+  return PKD_OK;
+}
+
+int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, void* int_ws,
+                        size_t int_ws_bytes) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (!aligned(float_ws, 256) || !aligned(int_ws, 256))
+    return fail(PKD_ERR_INVALID_ARG, "workspaces must be 256-byte aligned");
+  h->float_ws = float_ws;
+  h->float_bytes = float_ws_bytes;
+  h->int_ws = int_ws;
+  h->int_bytes = int_ws_bytes;
+  h->planned = false;
+  return PKD_OK;
+}
+
+int pkd_destroy(pkd_handle* h) {
+  if (!h) return PKD_OK;
+  if (h->staging_pending) cudaEventSynchronize(h->staging_done);
+  if (h->staging) cudaFreeHost(h->staging);
+  if (h->staging_done) cudaEventDestroy(h->staging_done);
+  delete h;
+  return PKD_OK;
+}
+
+int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
+                  int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                  int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
+                  int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
+                  int32_t* merges_out, int max_merges, int* n_items, int* n_merges, int* n_slots,
+                  int* kernel_out, int* tile_tokens_out) {
+  PlanRequest r;
+  int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
+                             num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
+                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms);
+  if (rc) return rc;
+  Plan plan;
+  const char* err = "";
+  rc = build_plan(r, &plan, &err);
+  if (rc) return fail(rc, err);
+  if (n_items) *n_items = (int)plan.items.size();
+  if (n_merges) *n_merges = (int)plan.merges.size();
+  if (n_slots) *n_slots = plan.num_slots;
+  if (kernel_out) *kernel_out = plan.kind;
+  if (tile_tokens_out) *tile_tokens_out = plan.tile_tokens;
+  if (items_out)
+    std::memcpy(items_out, plan.items.data(),
+                sizeof(WorkItem) * std::min<size_t>(plan.items.size(), (size_t)std::max(0, max_items)));
+  if (merges_out)
+    std::memcpy(merges_out, plan.merges.data(),
+                sizeof(MergeEntry) *
+                    std::min<size_t>(plan.merges.size(), (size_t)std::max(0, max_merges)));
+  g_last_error.clear();
+  return PKD_OK;
+}
+
+int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
+                        int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                        int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
+                        int use_tensor_cores, int num_sms, size_t* float_ws_bytes,
+                        size_t* int_ws_bytes) {
+  PlanRequest r;
+  int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
+                             num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
+                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms);
+  if (rc) return rc;
+  Plan plan;
+  const char* err = "";
+  rc = build_plan(r, &plan, &err);
+  if (rc) return fail(rc, err);
+  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(plan, num_qo_heads, head_dim);
+  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(plan);
+  return PKD_OK;
+}
+
+int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page_len_host,
+             int batch, const int32_t* indices_dev, int64_t num_indices, int num_qo_heads,
+             int num_kv_heads, int head_dim, int page_size, float sm_scale, float logits_soft_cap,
+             int window_left, int fixed_split_size, int disable_split_kv, int q_dtype,
+             int kv_dtype, int o_dtype, int use_tensor_cores, void* stream) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  h->planned = false;
+  if (q_dtype != PKD_DTYPE_F16 && q_dtype != PKD_DTYPE_BF16)
+    return fail(PKD_ERR_INVALID_ARG, "q_dtype must be F16 or BF16");
+  if (o_dtype != q_dtype) return fail(PKD_ERR_UNSUPPORTED, "o_dtype must equal q_dtype");
+  if (kv_dtype != q_dtype && kv_dtype != PKD_DTYPE_E4M3)
+    return fail(PKD_ERR_UNSUPPORTED, "kv_dtype must equal q_dtype or be E4M3");
+  if (batch > 0 && !indices_dev) return fail(PKD_ERR_INVALID_ARG, "indices_dev is null");
+  if (batch > 0 && num_indices < (int64_t)indptr_host[batch])
+    return fail(PKD_ERR_INVALID_ARG, "indices holds fewer than indptr[batch] page ids");
+  if (!(std::isnan(sm_scale) || (sm_scale > 0.f && std::isfinite(sm_scale))))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be positive and finite, or NaN for the default");
+  if (!std::isfinite(logits_soft_cap))
+    return fail(PKD_ERR_INVALID_ARG, "logits_soft_cap must be finite");
+
+  PlanRequest r;
+  int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
+                             num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
+                             disable_split_kv, kv_dtype, use_tensor_cores, h->num_sms);
+  if (rc) return rc;
+  Plan plan;
+  const char* err = "";
+  rc = build_plan(r, &plan, &err);
+  if (rc) return fail(rc, err);
+
+  const DecodeKernel* k = find_decode(plan.kind, q_dtype, kv_dtype, head_dim, plan.heads_per_cta);
+  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no decode kernel built for this dtype / head_dim");
+  const MergeKernel* mk = find_merge(o_dtype, head_dim);
+  if (!plan.merges.empty() && !mk)
+    return fail(PKD_ERR_UNSUPPORTED, "no merge kernel built for this dtype / head_dim");
+
+  const size_t need_f = float_ws_bytes_of(plan, num_qo_heads, head_dim);
+  const size_t need_i = int_ws_bytes_of(plan);
+  if (need_f > h->float_bytes || need_i > h->int_bytes) {
+    char buf[200];
+    std::snprintf(buf, sizeof buf, "workspace too small: need %zu float / %zu int bytes", need_f,
+                  need_i);
+    return fail(PKD_ERR_WORKSPACE_TOO_SMALL, buf);
+  }
+
+  cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       k->smem_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+
+  // Upload the work list: wait for the previous upload to leave the pinned buffer first.
+  const size_t items_b = plan.items.size() * sizeof(WorkItem);
+  const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
+  const size_t bytes = items_b + merges_b;
+  if (h->staging_pending) {
+    e = cudaEventSynchronize(h->staging_done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    h->staging_pending = false;
+  }
+  if (bytes > h->staging_bytes) {
+    if (h->staging) cudaFreeHost(h->staging);
+    h->staging = nullptr;
+    h->staging_bytes = 0;
+    const size_t cap = std::max<size_t>(bytes * 2, 1 << 16);
+    e = cudaHostAlloc(&h->staging, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    h->staging_bytes = cap;
+  }
+  if (items_b) std::memcpy(h->staging, plan.items.data(), items_b);
+  if (merges_b) std::memcpy(static_cast<char*>(h->staging) + items_b, plan.merges.data(), merges_b);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(h->int_ws, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  if (bytes) {
+    e = cudaMemcpyAsync(static_cast<char*>(h->int_ws) + kStatusBytes, h->staging, bytes,
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    e = cudaEventRecord(h->staging_done, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    h->staging_pending = true;
+  }
+
+  h->plan = std::move(plan);
+  h->batch = batch;
+  h->num_qo_heads = num_qo_heads;
+  h->num_kv_heads = num_kv_heads;
+  h->head_dim = head_dim;
+  h->page_size = page_size;
+  h->q_dtype = q_dtype;
+  h->kv_dtype = kv_dtype;
+  h->o_dtype = o_dtype;
+  h->sm_scale = std::isnan(sm_scale) ? 1.0f / std::sqrt((float)head_dim) : sm_scale;
+  h->cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
+  h->indices = indices_dev;
+  h->kernel = k;
+  h->merge = mk;
+  h->planned = true;
+  g_last_error.clear();
+  return PKD_OK;
+}
+
+int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
+                  int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
+                  float v_scale, void* o, float* lse, void* stream, void* ev_start, void* ev_end) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (!h->planned) return fail(PKD_ERR_NOT_PLANNED, "pkd_run called before a successful pkd_plan");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->plan.items.empty()) return PKD_OK;  // empty batch
+  if (!q || !k_base || !v_base || !o || !kv_strides)
+    return fail(PKD_ERR_INVALID_ARG, "null q / k_base / v_base / o / kv_strides");
+  if (num_pages <= 0 || num_pages > (int64_t(1) << 31))
+    return fail(PKD_ERR_INVALID_ARG, "num_pages must lie in [1, 2^31]");
+  if (!aligned(k_base, 16) || !aligned(v_base, 16) || !aligned(q, 16) || !aligned(o, 16))
+    return fail(PKD_ERR_INVALID_ARG, "q, o and the K/V bases must be 16-byte aligned");
+  const int elt = h->kv_dtype == kE4M3 ? 1 : 2;
+  for (int i = 0; i < 3; ++i)
+    if (kv_strides[i] <= 0 || (kv_strides[i] * elt) % 16 != 0)
+      return fail(PKD_ERR_INVALID_ARG, "kv strides must be positive multiples of 16 bytes");
+  const int64_t D = h->head_dim;
+  const bool nhd = h->layout == PKD_LAYOUT_NHD;
+  const int64_t inner = nhd ? kv_strides[2] : kv_strides[1];  // stride of the faster of slot/head
+  const int64_t outer = nhd ? kv_strides[1] : kv_strides[2];
+  const int64_t inner_n = nhd ? h->num_kv_heads : h->page_size;
+  const int64_t outer_n = nhd ? h->page_size : h->num_kv_heads;
+  if (inner < D || outer < inner * inner_n || kv_strides[0] < outer * outer_n)
+    return fail(PKD_ERR_INVALID_ARG,
+                "kv strides do not match the handle's layout (NHD: page > slot > head >= "
+                "head_dim; HND: page > head > slot >= head_dim, without overlap)");
+
+  DecodeParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  const int tile = h->kernel->tile_tokens;
+  const int box_rows = h->page_size < tile ? h->page_size : tile;
+  int rc = make_kv_tensor_map(&prm.tmap_k, k_base, h->kv_dtype, h->head_dim, h->page_size,
+                              h->num_kv_heads, num_pages, kv_strides, h->layout, box_rows);
+  if (rc) return rc;
+  rc = make_kv_tensor_map(&prm.tmap_v, v_base, h->kv_dtype, h->head_dim, h->page_size,
+                          h->num_kv_heads, num_pages, kv_strides, h->layout, box_rows);
+  if (rc) return rc;
+
+  char* iws = static_cast<char*>(h->int_ws);
+  char* fws = static_cast<char*>(h->float_ws);
+  const size_t part_o_bytes =
+      ((size_t)h->plan.num_slots * h->num_qo_heads * h->head_dim * sizeof(float) + 255) / 256 * 256;
+  prm.items = reinterpret_cast<const WorkItem*>(iws + kStatusBytes);
+  prm.indices = h->indices;
+  prm.q = q;
+  prm.o = o;
+  prm.lse = lse;
+  prm.part_o = reinterpret_cast<float*>(fws);
+  prm.part_lse = reinterpret_cast<float*>(fws + part_o_bytes);
+  prm.status = reinterpret_cast<uint32_t*>(iws);
+  prm.num_qo_heads = h->num_qo_heads;
+  prm.num_kv_heads = h->num_kv_heads;
+  prm.group = h->num_qo_heads / h->num_kv_heads;
+  prm.gslices = h->plan.gslices;
+  prm.page_size = h->page_size;
+  prm.hnd = nhd ? 0 : 1;
+  const double log2e = 1.4426950408889634;
+  const double sm = (double)h->sm_scale * q_scale * k_scale;
+  if (h->cap > 0.f) {
+    prm.scale_qk = (float)(sm / h->cap);
+    prm.cap_log2 = (float)(h->cap * log2e);
+  } else {
+    prm.scale_qk = (float)(sm * log2e);
+    prm.cap_log2 = 0.f;
+  }
+  prm.v_scale = v_scale;
+
+  const int64_t grid = (int64_t)h->plan.items.size() * h->num_kv_heads * h->plan.gslices;
+  void* args[] = {&prm};
+  cudaError_t e;
+  if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
+  e = cudaLaunchKernel(h->kernel->fn, dim3((unsigned)grid), dim3(h->kernel->threads), args,
+                       (size_t)h->kernel->smem_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
+
+  if (!h->plan.merges.empty()) {
+    MergeParams mp;
+    mp.merges = reinterpret_cast<const MergeEntry*>(iws + kStatusBytes +
+                                                     h->plan.items.size() * sizeof(WorkItem));
+    mp.part_o = prm.part_o;
+    mp.part_lse = prm.part_lse;
+    mp.o = o;
+    mp.lse = lse;
+    mp.status = prm.status;
+    mp.num_merges = (int)h->plan.merges.size();
+    mp.num_qo_heads = h->num_qo_heads;
+    const int64_t warps = (int64_t)mp.num_merges * mp.num_qo_heads;
+    const int64_t blocks = (warps + h->merge->heads_per_block - 1) / h->merge->heads_per_block;
+    void* margs[] = {&mp};
+    e = cudaLaunchKernel(h->merge->fn, dim3((unsigned)blocks), dim3(h->merge->threads), margs, 0,
+                         s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  }
+  return PKD_OK;
+}
+
+int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
+            int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
+            float v_scale, void* o, float* lse, void* stream) {
+  return pkd_run_timed(h, q, k_base, v_base, num_pages, kv_strides, q_scale, k_scale, v_scale, o,
+                       lse, stream, nullptr, nullptr);
+}
+
+int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
+  if (!h || !status) return fail(PKD_ERR_INVALID_ARG, "null handle or status");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, h->int_ws, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  *status = v;
+  if (v) {
+    e = cudaMemsetAsync(h->int_ws, 0, sizeof v, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  }
+  return PKD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// pkd_internal.h -- types shared by the host API/planner and the kernel translation units.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (a 128-byte opaque descriptor; no driver call is made here)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+namespace pkd {
+
+// One CTA-group of work: a chunk of one request's KV tokens.  Tokens count from the
+// request's first token.  The chunk covers pages starting at chunk_tok0 / page_size; the
+// attended tokens of the chunk are [tok_begin, tok_end).  out_slot < 0 means the chunk is
+// the whole request and the kernel writes the final o / lse; otherwise it writes an fp32
+// partial into slot out_slot of the float workspace.
+struct WorkItem {
+  int32_t req;
+  int32_t page_base;   // indptr[req]: offset of the request's first page id in `indices`
+  int32_t chunk_tok0;  // first token of the chunk's first page
+  int32_t tok_begin;
+  int32_t tok_end;
+  int32_t out_slot;
+  int32_t pad0;
+  int32_t pad1;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
+
+// A request whose chunks wrote partials into slots [first_slot, first_slot + n_chunks).
+struct MergeEntry {
+  int32_t req;
+  int32_t first_slot;
+  int32_t n_chunks;
+  int32_t pad;
+};
+static_assert(sizeof(MergeEntry) == 16, "MergeEntry is 4 int32");
+
+enum DType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+enum KernelKind { kCudaCore = 0, kTensorCore = 1 };
+
+// Kernel parameters, passed by value as a __grid_constant__ so the tensor maps stay in
+// parameter space (where the TMA unit may read them).
+struct DecodeParams {
+  CUtensorMap tmap_k;  // 4-D view of the K pool, see make_kv_tensor_map
+  CUtensorMap tmap_v;
+  const WorkItem* items;
+  const int32_t* indices;
+  const void* q;        // [batch, Hq, D] q dtype
+  void* o;              // [batch, Hq, D] o dtype
+  float* lse;           // [batch, Hq] natural log, may be null
+  float* part_o;        // [slots, Hq, D] fp32, normalised partial outputs
+  float* part_lse;      // [slots, Hq] fp32, base-2 log-sum-exp of the partial
+  uint32_t* status;     // device status word (bit 0: a pipeline wait timed out)
+  int num_qo_heads;
+  int num_kv_heads;
+  int group;            // Hq / Hkv
+  int gslices;          // CTAs per (item, kv head): ceil(group / heads per CTA)
+  int page_size;
+  int hnd;              // 1: the tensor map's dims are (d, slot, head, page); 0: (d, head, slot, page)
+  float scale_qk;       // multiplies <q, k>: sm_scale*q_scale*k_scale, times log2(e) without a
+                        // cap or divided by the cap with one
+  float cap_log2;       // cap * log2(e), 0 = no cap
+  float v_scale;
+};
+
+struct MergeParams {
+  const MergeEntry* merges;
+  const float* part_o;
+  const float* part_lse;
+  void* o;
+  float* lse;
+  uint32_t* status;
+  int num_merges;
+  int num_qo_heads;
+};
+
+// A compiled decode kernel and how to launch it.
+struct DecodeKernel {
+  int kind;         // KernelKind
+  int q_dtype;      // DType of q and o
+  int kv_dtype;     // DType of K/V
+  int head_dim;
+  int heads_per_cta;  // qo heads one CTA serves (the CUDA-core kernel is built per power of 2)
+  const void* fn;
+  int threads;
+  int smem_bytes;   // dynamic shared memory
+  int tile_tokens;  // tokens per pipeline stage
+};
+
+struct MergeKernel {
+  int o_dtype;
+  int head_dim;
+  const void* fn;
+  int threads;
+  int heads_per_block;
+};
+
+// Registries filled by the kernel translation units.
+void register_decode_f16(std::vector<DecodeKernel>& out);
+void register_decode_bf16(std::vector<DecodeKernel>& out);
+void register_decode_e4m3(std::vector<DecodeKernel>& out);
+void register_merge(std::vector<MergeKernel>& out);
+
+// ----------------------------------------------------------------------------- planner
+struct PlanRequest {
+  const int32_t* indptr;
+  const int32_t* last_page_len;
+  int batch;
+  int num_qo_heads;
+  int num_kv_heads;
+  int head_dim;
+  int page_size;
+  int window_left;
+  int fixed_split_size;
+  int disable_split_kv;
+  int kv_dtype;
+  int use_tensor_cores;  // -1 auto, 0, 1
+  int num_sms;
+};
+
+struct Plan {
+  std::vector<WorkItem> items;
+  std::vector<MergeEntry> merges;
+  int num_slots = 0;
+  int kind = kTensorCore;
+  int heads_per_cta = 8;
+  int gslices = 1;
+  int tile_tokens = 64;
+  int64_t chunk_tokens = 0;  // 0 = no split
+};
+
+// Returns 0 or a PKD_ERR_* code with a message in *err.
+int build_plan(const PlanRequest& r, Plan* plan, const char** err);
+
+// Byte offsets inside the int workspace.
+constexpr size_t kStatusBytes = 256;
+inline size_t int_ws_bytes_of(const Plan& p) {
+  return kStatusBytes + p.items.size() * sizeof(WorkItem) +
+         p.merges.size() * sizeof(MergeEntry) + 256;
+}
+inline size_t float_ws_bytes_of(const Plan& p, int num_qo_heads, int head_dim) {
+  size_t o = (size_t)p.num_slots * num_qo_heads * head_dim * sizeof(float);
+  size_t l = (size_t)p.num_slots * num_qo_heads * sizeof(float);
+  return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
+}
+
+}  // namespace pkd

@@ -1,0 +1,180 @@
+// planner.cpp -- host planner: turns a CSR page table into the split-KV work list.
+//
+// FlashInfer attention API page, BatchDecodeWithPagedKVCacheWrapper:
+//   - plan() builds auxiliary data structures once and every later run() reuses them
+//     (across layers);
+//   - indptr / indices / last_page_len describe each request's pages, with
+//     kv_len = page_size * (pages - 1) + last_page_len (batch prefill example);
+//   - window_left keeps the keys t >= kv_len - 1 - window_left;
+//   - fixed_split_size (pages) fixes the split-KV chunk so that the merge, and thus the
+//     output, does not depend on the batch; disable_split_kv keeps one chunk per request.
+// Chunks are cut at multiples of the chunk size counted from the request's first token, so
+// a request's partition depends only on its own length, its window and the chunk size.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <limits>
+
+#include "pkd_internal.h"
+
+namespace pkd {
+
+namespace {
+
+constexpr int kErrInvalid = -1;
+constexpr int kErrUnsupported = -5;
+constexpr int kCtasPerSm = 2;        // every decode kernel is sized for two resident CTAs
+constexpr int kWavesTarget = 2;      // the heuristic aims for about two waves of CTAs
+constexpr int64_t kMinChunk = 256;   // never split below this many tokens
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int tile_tokens_for(int head_dim, int kv_dtype) {
+  const int row_bytes = head_dim * (kv_dtype == kE4M3 ? 1 : 2);
+  return 16384 / row_bytes;  // a K tile is 16 KiB; K + V make a 32 KiB stage
+}
+
+}  // namespace
+
+int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
+  *plan = Plan();
+  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || !r.last_page_len))) {
+    *err = "batch must be >= 0 and the page table pointers non-null";
+    return kErrInvalid;
+  }
+  if (r.num_qo_heads <= 0 || r.num_kv_heads <= 0 || r.num_qo_heads % r.num_kv_heads != 0) {
+    *err = "num_qo_heads must be a positive multiple of num_kv_heads";
+    return kErrInvalid;
+  }
+  if (r.kv_dtype != kF16 && r.kv_dtype != kBF16 && r.kv_dtype != kE4M3) {
+    *err = "kv_dtype must be F16, BF16 or E4M3";
+    return kErrInvalid;
+  }
+  if (r.head_dim != 64 && r.head_dim != 128 && r.head_dim != 256) {
+    *err = "head_dim must be 64, 128 or 256";
+    return kErrUnsupported;
+  }
+  if (r.kv_dtype == kE4M3 && r.head_dim == 64) {
+    *err = "e4m3 KV needs head_dim 128 or 256 (rows of whole 128-byte blocks)";
+    return kErrUnsupported;
+  }
+  if (!is_pow2(r.page_size) || r.page_size < 8 || r.page_size > 256) {
+    *err = "page_size must be a power of two in [8, 256]";
+    return kErrUnsupported;
+  }
+  if (r.batch > 0 && r.indptr[0] < 0) {
+    *err = "indptr[0] must be >= 0";
+    return kErrInvalid;
+  }
+  const int ps = r.page_size;
+  const int group = r.num_qo_heads / r.num_kv_heads;
+  const int G = group;
+
+  // kernel choice (use_tensor_cores): auto takes the tensor-core kernel
+  plan->kind = r.use_tensor_cores == 0 ? kCudaCore : kTensorCore;
+  if (plan->kind == kTensorCore) {
+    plan->heads_per_cta = 8;
+  } else {
+    int gp = 2;
+    while (gp < G && gp < 8) gp <<= 1;
+    plan->heads_per_cta = gp;
+  }
+  plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
+  plan->tile_tokens = tile_tokens_for(r.head_dim, r.kv_dtype);
+
+  // per-request lengths and attended ranges
+  std::vector<int64_t> n(r.batch), w(r.batch);
+  int64_t total = 0, longest = 0;
+  for (int i = 0; i < r.batch; ++i) {
+    const int64_t pages = (int64_t)r.indptr[i + 1] - r.indptr[i];
+    if (pages < 0) {
+      *err = "indptr must be non-decreasing";
+      return kErrInvalid;
+    }
+    if (pages == 0) {
+      n[i] = 0;
+      w[i] = 0;
+      continue;
+    }
+    const int lpl = r.last_page_len[i];
+    if (lpl < 1 || lpl > ps) {
+      *err = "last_page_len must lie in [1, page_size] for every request with pages";
+      return kErrInvalid;
+    }
+    n[i] = (int64_t)ps * (pages - 1) + lpl;
+    if (n[i] > (int64_t)std::numeric_limits<int32_t>::max() - 4096) {
+      *err = "a request is longer than 2^31 - 4096 tokens";
+      return kErrInvalid;
+    }
+    w[i] = (r.window_left >= 0 && n[i] - 1 - r.window_left > 0) ? n[i] - 1 - r.window_left : 0;
+    total += n[i] - w[i];
+    longest = std::max(longest, n[i] - w[i]);
+  }
+
+  // chunk size in tokens (a multiple of the page size); 0 = one chunk per request
+  int64_t C = 0;
+  if (r.disable_split_kv) {
+    C = 0;
+  } else if (r.fixed_split_size > 0) {
+    C = (int64_t)r.fixed_split_size * ps;
+  } else {
+    const int sms = r.num_sms > 0 ? r.num_sms : 152;
+    const int64_t slots = (int64_t)sms * kCtasPerSm * kWavesTarget;
+    const int64_t per_cta = (total * r.num_kv_heads * plan->gslices + slots - 1) / slots;
+    int64_t c = std::max<int64_t>(kMinChunk, per_cta);
+    c = (c + ps - 1) / ps * ps;
+    C = longest > c ? c : 0;
+  }
+  plan->chunk_tokens = C;
+
+  // work items, partial slots in request order, merge entries
+  std::vector<WorkItem>& items = plan->items;
+  for (int i = 0; i < r.batch; ++i) {
+    WorkItem it;
+    std::memset(&it, 0, sizeof it);
+    it.req = i;
+    it.page_base = r.indptr[i];
+    if (n[i] == 0) {
+      it.chunk_tok0 = 0;
+      it.tok_begin = 0;
+      it.tok_end = 0;
+      it.out_slot = -1;
+      items.push_back(it);
+      continue;
+    }
+    const int64_t k0 = C > 0 ? w[i] / C : 0;
+    const int64_t k1 = C > 0 ? (n[i] - 1) / C : 0;
+    const int64_t nchunks = k1 - k0 + 1;
+    const int first_slot = plan->num_slots;
+    for (int64_t k = k0; k <= k1; ++k) {
+      const int64_t c0 = C > 0 ? k * C : 0;
+      const int64_t c1 = C > 0 ? std::min(n[i], (k + 1) * C) : n[i];
+      it.chunk_tok0 = (int32_t)c0;
+      it.tok_begin = (int32_t)std::max(c0, w[i]);
+      it.tok_end = (int32_t)c1;
+      it.out_slot = nchunks > 1 ? plan->num_slots++ : -1;
+      items.push_back(it);
+    }
+    if (nchunks > 1) {
+      MergeEntry me;
+      me.req = i;
+      me.first_slot = first_slot;
+      me.n_chunks = (int32_t)nchunks;
+      me.pad = 0;
+      plan->merges.push_back(me);
+    }
+  }
+  // longest chunks launch first (their CTAs bound the tail of the grid)
+  std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) {
+    return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+  });
+  const int64_t ctas = (int64_t)items.size() * r.num_kv_heads * plan->gslices;
+  if (ctas > (int64_t)std::numeric_limits<int32_t>::max()) {
+    *err = "too many work items for one grid";
+    return kErrInvalid;
+  }
+  *err = "";
+  return 0;
+}
+
+}  // namespace pkd

@@ -1,0 +1,250 @@
+"""Python face of libpkd: ``BatchDecodePagedKV`` with FlashInfer-style plan()/run().
+
+Mirrors BatchDecodeWithPagedKVCacheWrapper from the FlashInfer attention API page
+(constructor with a float workspace and a KV layout; plan(indptr, indices, last_page_len,
+num_qo_heads, num_kv_heads, head_dim, page_size, ...); run(q, paged_kv_cache, q_scale,
+k_scale, v_scale, out, lse, return_lse)).  This module only checks shapes and marshals
+pointers: every step of the computation runs in libpkd's CUDA kernels.  PyTorch supplies
+device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple, Union
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+_DTYPE_CODE = {torch.float16: L.DTYPE_F16, torch.bfloat16: L.DTYPE_BF16,
+               torch.float8_e4m3fn: L.DTYPE_E4M3}
+_STR_DTYPE = {"float16": torch.float16, "half": torch.float16, "bfloat16": torch.bfloat16,
+              "float8_e4m3fn": torch.float8_e4m3fn, "e4m3": torch.float8_e4m3fn}
+
+
+def _as_dtype(x):
+    if x is None or isinstance(x, torch.dtype):
+        return x
+    return _STR_DTYPE[str(x).replace("torch.", "")]
+
+
+def _host_i32(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().to("cpu")
+        return np.ascontiguousarray(t.numpy().astype(np.int32, copy=False))
+    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class BatchDecodePagedKV:
+    """Batch decode attention over a paged KV cache (one query token per request and head).
+
+    ``float_workspace_buffer``: a CUDA uint8 tensor for split-KV partials (128 MiB is the
+    usual size).  ``int_workspace_buffer``: CUDA uint8 tensor for the work list (allocated
+    here, 8 MiB, if not given).  ``kv_layout``: "NHD" or "HND".
+    """
+
+    def __init__(self, float_workspace_buffer: torch.Tensor, kv_layout: str = "NHD",
+                 int_workspace_buffer: Optional[torch.Tensor] = None,
+                 use_tensor_cores: Optional[bool] = None):
+        if kv_layout not in ("NHD", "HND"):
+            raise ValueError("kv_layout must be 'NHD' or 'HND'")
+        if not float_workspace_buffer.is_cuda:
+            raise ValueError("the float workspace must be a CUDA tensor")
+        if int_workspace_buffer is None:
+            int_workspace_buffer = torch.empty(8 << 20, dtype=torch.uint8,
+                                               device=float_workspace_buffer.device)
+        self.kv_layout = kv_layout
+        self._use_tc = use_tensor_cores
+        self._float_ws = float_workspace_buffer
+        self._int_ws = int_workspace_buffer
+        self._plan_args = None
+        self._indices = None
+        h = ctypes.c_void_p()
+        L.check(L.lib().pkd_create(ctypes.byref(h), self._float_ws.data_ptr(),
+                                   self._float_ws.numel() * self._float_ws.element_size(),
+                                   self._int_ws.data_ptr(),
+                                   self._int_ws.numel() * self._int_ws.element_size(),
+                                   L.LAYOUT_NHD if kv_layout == "NHD" else L.LAYOUT_HND))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                L.lib().pkd_destroy(h)
+            except Exception:
+                pass
+            self._h = None
+
+    def reset_workspace_buffer(self, float_workspace_buffer: torch.Tensor,
+                               int_workspace_buffer: torch.Tensor) -> None:
+        L.check(L.lib().pkd_reset_workspace(
+            self._h, float_workspace_buffer.data_ptr(),
+            float_workspace_buffer.numel() * float_workspace_buffer.element_size(),
+            int_workspace_buffer.data_ptr(),
+            int_workspace_buffer.numel() * int_workspace_buffer.element_size()))
+        self._float_ws, self._int_ws = float_workspace_buffer, int_workspace_buffer
+        self._plan_args = None
+
+    # ------------------------------------------------------------------ plan
+    def plan(self, indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int,
+             num_kv_heads: int, head_dim: int, page_size: int, pos_encoding_mode: str = "NONE",
+             window_left: int = -1, logits_soft_cap: Optional[float] = None,
+             q_data_type=torch.float16, kv_data_type=None, o_data_type=None, data_type=None,
+             sm_scale: Optional[float] = None, non_blocking: bool = True,
+             fixed_split_size: Optional[int] = None, disable_split_kv: bool = False,
+             use_tensor_cores: Optional[bool] = None, stream=None) -> None:
+        """Plan a batch; ``indptr`` / ``last_page_len`` may live on the host or the device
+        (a device copy is read back once here), ``indices`` must be a CUDA int32 tensor and
+        stay unchanged while runs of this plan are in flight."""
+        if pos_encoding_mode != "NONE":
+            raise NotImplementedError("only pos_encoding_mode='NONE' is implemented")
+        if data_type is not None:
+            q_data_type = data_type
+        q_dt = _as_dtype(q_data_type)
+        kv_dt = _as_dtype(kv_data_type) or q_dt
+        o_dt = _as_dtype(o_data_type) or q_dt
+        if not (isinstance(indices, torch.Tensor) and indices.is_cuda
+                and indices.dtype == torch.int32 and indices.is_contiguous()):
+            raise ValueError("indices must be a contiguous CUDA int32 tensor")
+        ip = _host_i32(indptr)
+        lpl = _host_i32(last_page_len)
+        batch = len(lpl)
+        if len(ip) != batch + 1:
+            raise ValueError("indptr must have batch + 1 entries")
+        utc = use_tensor_cores if use_tensor_cores is not None else self._use_tc
+        kernel = L.KERNEL_AUTO if utc is None else (L.KERNEL_TENSOR_CORE if utc else L.KERNEL_CUDA_CORE)
+        sm = float("nan") if sm_scale is None else float(sm_scale)
+        L.check(L.lib().pkd_plan(
+            self._h, _i32p(ip), _i32p(lpl), batch, indices.data_ptr(), indices.numel(),
+            num_qo_heads, num_kv_heads, head_dim, page_size, sm,
+            float(logits_soft_cap or 0.0), int(window_left), int(fixed_split_size or 0),
+            int(bool(disable_split_kv)), _DTYPE_CODE[q_dt], _DTYPE_CODE[kv_dt], _DTYPE_CODE[o_dt],
+            kernel, _stream_ptr(stream)))
+        self._indices = indices
+        self._plan_args = dict(batch=batch, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                               head_dim=head_dim, page_size=page_size, q_dtype=q_dt,
+                               kv_dtype=kv_dt, o_dtype=o_dt)
+
+    # ------------------------------------------------------------------ run
+    def _kv_pointers(self, paged_kv_cache):
+        a = self._plan_args
+        if isinstance(paged_kv_cache, (tuple, list)):
+            k, v = paged_kv_cache
+            if k.dim() != 4 or v.dim() != 4 or k.shape != v.shape or k.stride() != v.stride():
+                raise ValueError("(k_cache, v_cache) must be 4-D tensors of one shape and stride")
+            if self.kv_layout == "NHD":
+                exp = (a["page_size"], a["num_kv_heads"], a["head_dim"])
+                strides = (k.stride(0), k.stride(1), k.stride(2))
+            else:
+                exp = (a["num_kv_heads"], a["page_size"], a["head_dim"])
+                strides = (k.stride(0), k.stride(2), k.stride(1))
+            if tuple(k.shape[1:]) != exp or k.stride(3) != 1:
+                raise ValueError(f"k/v cache shape {tuple(k.shape)} does not match the plan")
+            return k, k.data_ptr(), v.data_ptr(), k.shape[0], strides
+        kv = paged_kv_cache
+        if kv.dim() != 5 or kv.shape[1] != 2 or kv.stride(4) != 1:
+            raise ValueError("paged_kv_cache must be [pages, 2, ...] with head_dim contiguous")
+        if self.kv_layout == "NHD":
+            exp = (a["page_size"], a["num_kv_heads"], a["head_dim"])
+            strides = (kv.stride(0), kv.stride(2), kv.stride(3))
+        else:
+            exp = (a["num_kv_heads"], a["page_size"], a["head_dim"])
+            strides = (kv.stride(0), kv.stride(3), kv.stride(2))
+        if tuple(kv.shape[2:]) != exp:
+            raise ValueError(f"paged_kv_cache shape {tuple(kv.shape)} does not match the plan")
+        base = kv.data_ptr()
+        return kv, base, base + kv.stride(1) * kv.element_size(), kv.shape[0], strides
+
+    def run(self, q: torch.Tensor, paged_kv_cache: Union[torch.Tensor, Tuple[torch.Tensor, torch.Tensor]],
+            q_scale: Optional[float] = None, k_scale: Optional[float] = None,
+            v_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, return_lse: bool = False, stream=None,
+            timing_events=None):
+        """Decode attention for the planned batch on one layer's pool: returns ``o`` or
+        ``(o, lse)`` (lse: float32 natural log, ``[batch, num_qo_heads]``)."""
+        a = self._plan_args
+        if a is None:
+            raise RuntimeError("plan() must be called before run()")
+        exp_q = (a["batch"], a["num_qo_heads"], a["head_dim"])
+        if tuple(q.shape) != exp_q or q.dtype != a["q_dtype"] or not q.is_contiguous():
+            raise ValueError(f"q must be a contiguous {a['q_dtype']} tensor of shape {exp_q}")
+        kv, k_ptr, v_ptr, num_pages, strides = self._kv_pointers(paged_kv_cache)
+        if kv.dtype != a["kv_dtype"]:
+            raise ValueError(f"KV dtype {kv.dtype} does not match the plan ({a['kv_dtype']})")
+        if out is None:
+            out = torch.empty(exp_q, dtype=a["o_dtype"], device=q.device)
+        elif tuple(out.shape) != exp_q or out.dtype != a["o_dtype"] or not out.is_contiguous():
+            raise ValueError("out has the wrong shape, dtype or layout")
+        if lse is None and return_lse:
+            lse = torch.empty(exp_q[:2], dtype=torch.float32, device=q.device)
+        if lse is not None and (tuple(lse.shape) != exp_q[:2] or lse.dtype != torch.float32):
+            raise ValueError("lse must be float32 [batch, num_qo_heads]")
+        st = (ctypes.c_int64 * 3)(*strides)
+        ev0, ev1 = timing_events if timing_events is not None else (None, None)
+        L.check(L.lib().pkd_run_timed(
+            self._h, q.data_ptr(), k_ptr, v_ptr, num_pages, st,
+            1.0 if q_scale is None else float(q_scale), 1.0 if k_scale is None else float(k_scale),
+            1.0 if v_scale is None else float(v_scale), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, _stream_ptr(stream),
+            ev0.cuda_event if ev0 is not None else None,
+            ev1.cuda_event if ev1 is not None else None))
+        return (out, lse) if return_lse else out
+
+    def check_status(self, stream=None) -> int:
+        """Read and clear the device status word (synchronises the stream); 0 = no error."""
+        v = ctypes.c_uint32()
+        L.check(L.lib().pkd_check_status(self._h, ctypes.byref(v), _stream_ptr(stream)))
+        return v.value
+
+
+def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+              page_size: int, window_left: int = -1, fixed_split_size: int = 0,
+              disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
+              use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152):
+    """Run the host planner alone (no GPU): returns a dict with the work items
+    ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, 0, 0), the merge
+    entries ``[m, 4]``, the slot count, the chosen kernel and the tile size."""
+    ip = _host_i32(indptr)
+    lpl = _host_i32(last_page_len)
+    batch = len(lpl)
+    n_items, n_merges, n_slots = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    kern, tile = ctypes.c_int(), ctypes.c_int()
+    args = (_i32p(ip), _i32p(lpl), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+            window_left, fixed_split_size, int(disable_split_kv), kv_dtype, use_tensor_cores,
+            num_sms)
+    L.check(L.lib().pkd_plan_host(*args, None, 0, None, 0, ctypes.byref(n_items),
+                                  ctypes.byref(n_merges), ctypes.byref(n_slots),
+                                  ctypes.byref(kern), ctypes.byref(tile)))
+    items = np.zeros((max(1, n_items.value), 8), dtype=np.int32)
+    merges = np.zeros((max(1, n_merges.value), 4), dtype=np.int32)
+    L.check(L.lib().pkd_plan_host(*args, _i32p(items), n_items.value, _i32p(merges),
+                                  n_merges.value, ctypes.byref(n_items), ctypes.byref(n_merges),
+                                  ctypes.byref(n_slots), ctypes.byref(kern), ctypes.byref(tile)))
+    return dict(items=items[:n_items.value], merges=merges[:n_merges.value],
+                num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
+
+
+def workspace_bytes(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                    page_size: int, window_left: int = -1, fixed_split_size: int = 0,
+                    disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
+                    use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152):
+    ip = _host_i32(indptr)
+    lpl = _host_i32(last_page_len)
+    fb, ib = ctypes.c_size_t(), ctypes.c_size_t()
+    L.check(L.lib().pkd_workspace_bytes(_i32p(ip), _i32p(lpl), len(lpl), num_qo_heads,
+                                        num_kv_heads, head_dim, page_size, window_left,
+                                        fixed_split_size, int(disable_split_kv), kv_dtype,
+                                        use_tensor_cores, num_sms, ctypes.byref(fb),
+                                        ctypes.byref(ib)))
+    return fb.value, ib.value

@@ -1,0 +1,217 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI (libpkd).
+
+Small cases span several tiles and a ragged tail and run every variant (tensor-core and
+CUDA-core kernels, NHD/HND, 5-D pool and (k, v) pair, fp16/bf16/e4m3, head_dim 64/128/256,
+GQA groups 1..16, page sizes 8..128, soft cap, window, split modes).  Edge cases: empty
+requests, single tokens, window 0, an empty batch, NaN/Inf in every slot no request owns.
+Properties the pages fix: batch invariance under fixed_split_size, run-to-run determinism.
+Full-size workloads are checked on sampled requests in the same launch configuration the
+benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import assert_close, gpu_decoder, run_gpu, run_oracle, sub_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(lens, hq, hkv, d, ps, layout="NHD", dt="f16", kv=None, seed=0, **kw):
+    w = W.custom(lens, hq, hkv, d, ps, layout=layout, q_dtype=dt, kv_dtype=kv or dt, seed=seed, **kw)
+    if w.kv_dtype == "e4m3":
+        w.kv_store_scale, w.k_scale, w.v_scale = 0.5, 0.5, 0.5
+    return w, W.make_q(w), W.make_pool(w)
+
+
+LENS = [1, 15, 16, 17, 64, 65, 300, 777, 0, 129]
+
+
+def test_worked_example_both_kernels():
+    w = W.workload("worked")
+    q, pool = W.make_q(w), W.make_pool(w)
+    ref = run_oracle(w, q, pool)
+    for tc in (True, False):
+        assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), ref, f"worked tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_dtypes_layouts_head_dims(tc, layout, dt, d):
+    w, q, pool = _case(LENS, 8, 2, d, 16, layout, dt, seed=d)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"{layout} {dt} D{d} tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 3), (16, 2), (16, 1), (32, 2), (6, 1)])
+def test_gqa_groups(tc, hq, hkv):
+    w, q, pool = _case([33, 250, 1, 96], hq, hkv, 128, 16, seed=hq * 7 + hkv)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"G{hq // hkv} tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("ps", [8, 32, 64, 128])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_page_sizes(tc, ps, layout):
+    w, q, pool = _case([5, ps, ps + 1, 3 * ps - 1, 700], 8, 1, 128, ps, layout, "bf16", seed=ps)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"ps{ps} {layout} tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("cap,window", [(0.0, 0), (0.0, 37), (30.0, -1), (5.0, 100), (1.0, 5000)])
+def test_soft_cap_and_window(tc, cap, window):
+    w, q, pool = _case(LENS, 8, 2, 128, 16, "NHD", "f16", seed=3, logits_soft_cap=cap,
+                       window_left=window)
+    q = q * 4  # larger logits so the cap matters
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"cap{cap} win{window} tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("mode", [dict(fixed_split_size=1), dict(fixed_split_size=3),
+                                  dict(fixed_split_size=50), dict(disable_split_kv=True), {}])
+def test_split_modes(tc, mode):
+    w, q, pool = _case([1, 16, 130, 1000, 2047, 0], 8, 2, 128, 16, "HND", "bf16", seed=4,
+                       window_left=900 if mode.get("fixed_split_size") == 3 else -1)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc, **mode), run_oracle(w, q, pool),
+                 f"{mode} tc={tc}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("qdt", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [128, 256])
+def test_e4m3_kv(tc, qdt, d):
+    w, q, pool = _case(LENS, 16, 2, d, 32, "NHD", qdt, kv="e4m3", seed=d + 1,
+                       logits_soft_cap=30.0, window_left=200)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"e4m3 {qdt} D{d} tc={tc}")
+
+
+def test_e4m3_large_query_values():
+    """bf16 q far outside fp16 range still works with e4m3 KV (the tensor-core kernel rescales q)."""
+    w, q, pool = _case([40, 300], 8, 1, 128, 16, "NHD", "bf16", kv="e4m3", seed=9,
+                       logits_soft_cap=50.0)
+    q = (q.float() * 1e5).to(torch.bfloat16)
+    for tc in (True, False):
+        assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                     f"large q tc={tc}")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_kv_tuple_matches_5d(layout):
+    w, q, pool = _case(LENS, 8, 4, 128, 16, layout, "f16", seed=5)
+    k, v = pool[:, 0].contiguous(), pool[:, 1].contiguous()
+    got = run_gpu(w, q, (k, v))
+    assert_close(w, got, run_oracle(w, q, pool), f"tuple {layout}")
+    five = run_gpu(w, q, pool)
+    assert np.array_equal(got[0], five[0]) and np.array_equal(got[1], five[1])
+
+
+@pytest.mark.parametrize("tc", [True, False])
+def test_garbage_in_unowned_slots_is_ignored(tc):
+    """Slots past last_page_len and pages no request owns hold NaN/Inf (FlashInfer users have
+    met this hazard: a masked-but-read tail poisons the output)."""
+    w, q, pool = _case([1, 17, 250, 33, 0], 8, 2, 128, 16, "NHD", "bf16", seed=6,
+                       window_left=40)
+    clean = run_gpu(w, q, pool, use_tensor_cores=tc)
+    dirty = pool.clone()
+    owned = np.zeros(w.num_pages, dtype=bool)
+    owned[w.indices] = True
+    dirty[torch.from_numpy(~owned)] = float("nan")
+    for i in range(w.batch):
+        if w.indptr[i + 1] > w.indptr[i]:
+            last = int(w.indices[w.indptr[i + 1] - 1])
+            lp = int(w.last_page_len[i])
+            dirty[last, :, lp:] = float("inf") if i % 2 else float("nan")
+    got = run_gpu(w, q, dirty, use_tensor_cores=tc)
+    assert np.array_equal(got[0], clean[0]) and np.array_equal(got[1], clean[1])
+    assert_close(w, got, run_oracle(w, q, pool), f"garbage tc={tc}")
+
+
+def test_empty_requests_and_empty_batch():
+    w, q, pool = _case([0, 0, 5, 0], 4, 2, 64, 8, seed=7)
+    o, lse = run_gpu(w, q, pool)
+    assert np.all(o[[0, 1, 3]] == 0) and np.all(np.isneginf(lse[[0, 1, 3]]))
+    assert_close(w, (o, lse), run_oracle(w, q, pool), "empty requests")
+    w0, q0, pool0 = _case([], 4, 2, 64, 8, seed=7)
+    o0, lse0 = run_gpu(w0, q0, pool0)
+    assert o0.shape == (0, 4, 64) and lse0.shape == (0, 4)
+
+
+@pytest.mark.parametrize("tc", [True, False])
+def test_batch_invariance_with_fixed_split(tc):
+    """With fixed_split_size a request's output is bitwise the same alone or in any batch."""
+    lens = [3000, 17, 1200, 4096, 64]
+    w, q, pool = _case(lens, 16, 2, 128, 16, "HND", "bf16", seed=8)
+    full = run_gpu(w, q, pool, use_tensor_cores=tc, fixed_split_size=32)
+    for i in (0, 2, 3):
+        sub, qs, ps_ = sub_problem(w, [i], q, pool)
+        alone = run_gpu(sub, qs, ps_, use_tensor_cores=tc, fixed_split_size=32)
+        assert np.array_equal(alone[0][0], full[0][i]), f"request {i} o differs"
+        assert np.array_equal(alone[1][0], full[1][i]), f"request {i} lse differs"
+
+
+@pytest.mark.parametrize("tc", [True, False])
+def test_run_to_run_determinism(tc):
+    w, q, pool = _case([2500, 100, 7000], 8, 2, 128, 16, "NHD", "f16", seed=10)
+    dec = gpu_decoder(w, use_tensor_cores=tc)
+    a = run_gpu(w, q, pool, dec=dec)
+    b = run_gpu(w, q, pool, dec=dec)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_plan_reused_across_layers():
+    w, q, pool = _case([300, 45, 1000], 8, 2, 128, 16, "NHD", "f16", seed=11)
+    dec = gpu_decoder(w)
+    for layer in range(3):
+        ql, pl = W.make_q(w, layer=layer), W.make_pool(w, layer=layer)
+        assert_close(w, run_gpu(w, ql, pl, dec=dec), run_oracle(w, ql, pl), f"layer {layer}")
+
+
+# ----------------------------------------------------------------- full-size workloads
+def _full(name, sample, layers=(0,), tc=None):
+    w = W.workload(name)
+    dev = torch.device("cuda")
+    dec = gpu_decoder(w, **({} if tc is None else dict(use_tensor_cores=tc)))
+    for layer in layers:
+        q = W.make_q(w, device=dev, layer=layer)
+        pool = W.make_pool(w, device=dev, layer=layer)
+        got = run_gpu(w, q, pool, dec=dec)
+        sub, qs, ps_ = sub_problem(w, sample, q, pool)
+        ref = run_oracle(sub, qs, ps_)
+        assert_close(sub, (got[0][sample], got[1][sample]), ref, f"{name} layer {layer}")
+        del pool
+        torch.cuda.empty_cache()
+
+
+def _sample(w, k=4, seed=0):
+    lens = np.asarray(w.kv_lens)
+    rng = np.random.default_rng(seed)
+    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+    pick.update(int(x) for x in rng.choice(len(lens), size=k, replace=False))
+    return sorted(pick)
+
+
+def test_full_uniform_bf16_nhd():
+    w = W.workload("uniform")
+    _full("uniform", _sample(w), layers=(0, 31))
+
+
+def test_full_lognormal_f16_split():
+    w = W.workload("lognormal")
+    _full("lognormal", _sample(w, 3))
+
+
+def test_full_long_hnd_fixed_split():
+    _full("long", [0, 3])
+
+
+def test_full_mix_e4m3_cap_window():
+    w = W.workload("mix")
+    _full("mix", _sample(w, 6))

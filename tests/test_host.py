@@ -1,0 +1,168 @@
+"""Host-side tests (no GPU): the C ABI loads and exports what include/pkd.h declares, and the
+planner's work list is a correct partition of every request's attended keys."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkd():
+    import __graft_entry__ as g
+    from paged_kv_decode_23_gb300 import build
+    build.build()
+    import paged_kv_decode_23_gb300 as p
+    return p
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pkd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkd_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(pkd):
+    from paged_kv_decode_23_gb300 import _lib as L
+    lib = L.lib()
+    declared = _declared_symbols()
+    assert len(declared) >= 10
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in pkd.h but not exported"
+        assert name in L.SIGNATURES, f"{name} has no ctypes signature in the binding"
+
+
+def test_create_without_device_fails_cleanly(pkd):
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    from paged_kv_decode_23_gb300 import _lib as L
+    h = ctypes.c_void_p()
+    rc = L.lib().pkd_create(ctypes.byref(h), 0, 0, 0, 0, L.LAYOUT_NHD)
+    assert rc == -4 and not h.value
+    assert L.lib().pkd_last_error().decode()
+
+
+def _check_partition(w, plan, C):
+    """Every request's attended tokens are covered exactly once, chunks start at multiples of C
+    from token 0, finals and partial slots agree with the merge list."""
+    items, merges = plan["items"], plan["merges"]
+    n = W.page_table  # noqa: F841  (lengths come from the workload)
+    by_req = {}
+    for it in items:
+        by_req.setdefault(int(it[0]), []).append(it)
+    merge_of = {int(m[0]): m for m in merges}
+    slots = []
+    for i in range(w.batch):
+        L = int(w.kv_lens[i])
+        lo = 0 if w.window_left < 0 else max(0, L - 1 - w.window_left)
+        its = sorted(by_req[i], key=lambda x: x[3])
+        assert all(int(it[1]) == int(w.indptr[i]) for it in its)
+        if L == 0:
+            assert len(its) == 1 and its[0][3] == its[0][4] == 0 and its[0][5] == -1
+            continue
+        assert int(its[0][3]) == lo and int(its[-1][4]) == L
+        for a, b in zip(its, its[1:]):
+            assert int(a[4]) == int(b[3])
+        for it in its:
+            c0, b0, e0 = int(it[2]), int(it[3]), int(it[4])
+            assert c0 % w.page_size == 0 and c0 <= b0 < e0
+            if C:
+                assert c0 % C == 0 and e0 - c0 <= C
+        if len(its) == 1:
+            assert its[0][5] == -1 and i not in merge_of
+        else:
+            m = merge_of[i]
+            assert int(m[2]) == len(its)
+            assert [int(it[5]) for it in its] == list(range(int(m[1]), int(m[1]) + len(its)))
+            slots += [int(it[5]) for it in its]
+    assert sorted(slots) == list(range(plan["num_slots"]))
+    lens = items[:, 4] - items[:, 3]
+    assert np.all(np.diff(lens) <= 0), "items are launched longest first"
+
+
+@pytest.mark.parametrize("name", ["worked", "uniform", "lognormal", "long", "mix"])
+def test_plan_partitions_every_workload(pkd, name):
+    w = W.workload(name)
+    plan = pkd.plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                         w.page_size, window_left=w.window_left,
+                         fixed_split_size=w.fixed_split_size,
+                         kv_dtype={"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype])
+    C = w.fixed_split_size * w.page_size
+    _check_partition(w, plan, C)
+    if name == "long":
+        assert len(plan["items"]) == 4 * 8 and len(plan["merges"]) == 4
+
+
+@pytest.mark.parametrize("fixed", [0, 1, 2, 7, 64])
+@pytest.mark.parametrize("window", [-1, 0, 10, 1000])
+def test_plan_modes(pkd, fixed, window):
+    lens = [0, 1, 7, 8, 9, 100, 1000, 5000]
+    w = W.custom(lens, 8, 2, 128, 8, window_left=window)
+    plan = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 8, window_left=window,
+                         fixed_split_size=fixed)
+    _check_partition(w, plan, fixed * 8)
+    nosplit = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 8, window_left=window,
+                            fixed_split_size=fixed, disable_split_kv=True)
+    _check_partition(w, nosplit, 0)
+    assert len(nosplit["items"]) == len(lens) and len(nosplit["merges"]) == 0
+
+
+def test_fixed_split_is_batch_invariant(pkd):
+    lens = [5000, 33, 1200]
+    w = W.custom(lens, 8, 2, 128, 16)
+    full = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 16, fixed_split_size=16)
+    for i in range(3):
+        wi = W.custom([lens[i]], 8, 2, 128, 16)
+        alone = pkd.plan_host(wi.indptr, wi.last_page_len, 8, 2, 128, 16, fixed_split_size=16)
+        mine = sorted((int(x[2]), int(x[3]), int(x[4])) for x in full["items"] if x[0] == i)
+        theirs = sorted((int(x[2]), int(x[3]), int(x[4])) for x in alone["items"])
+        assert mine == theirs
+
+
+def test_kernel_choice_and_tiles(pkd):
+    w = W.workload("worked")
+    auto = pkd.plan_host(w.indptr, w.last_page_len, 64, 8, 128, 16)
+    cc = pkd.plan_host(w.indptr, w.last_page_len, 64, 8, 128, 16, use_tensor_cores=0)
+    assert auto["kernel"] == 1 and cc["kernel"] == 0
+    assert auto["tile_tokens"] == 64
+    assert pkd.plan_host(w.indptr, w.last_page_len, 64, 8, 256, 16)["tile_tokens"] == 32
+    assert pkd.plan_host(w.indptr, w.last_page_len, 64, 8, 256, 16, kv_dtype=2)["tile_tokens"] == 64
+
+
+@pytest.mark.parametrize("bad", [
+    dict(num_qo_heads=12, num_kv_heads=8),           # not a multiple
+    dict(head_dim=96),                               # unsupported head_dim
+    dict(page_size=24),                              # not a power of two
+    dict(page_size=4),                               # below 8
+    dict(lpl_fix=0),                                 # last_page_len 0 on a request with pages
+    dict(lpl_fix=17),                                # last_page_len > page_size
+    dict(indptr_fix=True),                           # decreasing indptr
+    dict(head_dim=64, kv_dtype=2),                   # e4m3 needs head_dim >= 128
+])
+def test_plan_rejects_bad_input(pkd, bad):
+    from paged_kv_decode_23_gb300 import PkdError
+    ip = np.array([0, 3, 5, 9], dtype=np.int32)
+    lpl = np.array([4, 16, 1], dtype=np.int32)
+    if "lpl_fix" in bad:
+        lpl[1] = bad.pop("lpl_fix")
+    if bad.pop("indptr_fix", False):
+        ip[2] = 2
+    args = dict(num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16)
+    args.update(bad)
+    with pytest.raises(PkdError) as e:
+        pkd.plan_host(ip, lpl, **args)
+    assert e.value.code in (-1, -5)
+
+
+def test_workspace_bytes_covers_partials(pkd):
+    w = W.workload("long")
+    fb, ib = pkd.workspace_bytes(w.indptr, w.last_page_len, 32, 8, 128, 64,
+                                 fixed_split_size=256, kv_dtype=1)
+    assert fb >= 32 * 32 * 128 * 4 + 32 * 32 * 4
+    assert ib >= 256 + 32 * 32 + 4 * 16
