@@ -243,6 +243,9 @@ def gpu_arm(args, w, rank, world):
     n_calls = layers
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_calls * args.steps)]
+    for a, b in ev:  # torch creates the CUDA event on first record; the C ABI records it again
+        a.record(stream)
+        b.record(stream)
 
     def step(k=None):
         dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
