@@ -172,6 +172,53 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
  */
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
 
+/*
+ * pkd_decode_noalloc -- plan + run in one call, using only scratch memory built into the
+ * library.  The FlashInfer pages have no counterpart of this call.
+ *
+ * Who it is for: callers that cannot allocate device memory and have no workspace to lend.
+ * A runtime that owns every device allocation (a fixed memory pool, or a hard memory budget
+ * shared with other engines) does not let its plug-ins call cudaMalloc: an allocation outside
+ * the pool can fail at any point, and it hides memory from the runtime's accounting.  Such a
+ * caller passes only its inputs and outputs.
+ *
+ * Scratch: one file-scope device array of PKD_NOALLOC_SCRATCH_BYTES (16 MiB) inside libpkd.
+ * Every GPU that loads the library holds it until the process exits.  It holds the status
+ * word, the work list (at most PKD_NOALLOC_MAX_ITEMS chunks and PKD_NOALLOC_MAX_MERGES split
+ * requests) and the split partials (4 * slots * num_qo_heads * (head_dim + 1) bytes, at most
+ * PKD_NOALLOC_PARTIAL_BYTES).  A plan that needs more fails with PKD_ERR_WORKSPACE_TOO_SMALL
+ * and a message saying which limit it hit.  With neither fixed_split_size nor
+ * disable_split_kv set, the chunk size grows until the partials fit.
+ *
+ * A call allocates nothing: no cudaMalloc / cudaFree, no pinned or heap memory (the plan is
+ * built in static host storage).  The first call on a device does a one-time set-up with that
+ * device current: it reads the array's device address (cudaGetSymbolAddress) and raises the
+ * kernels' shared-memory limit.  Make that first call before any stream capture.
+ *
+ * Every call shares the one array and overwrites what the last call left there.  Calls whose
+ * GPU work overlaps (on two streams, or from two host threads) race and corrupt each other's
+ * results: serialise them.  The work list is uploaded from pageable host memory, so the call
+ * waits for earlier work on `stream` before it returns.
+ *
+ * Arguments: those of pkd_plan followed by those of pkd_run, with kv_layout as in pkd_create.
+ * Only the tensor-core kernel is built into this variant: use_tensor_cores must be
+ * PKD_KERNEL_AUTO or PKD_KERNEL_TENSOR_CORE, and a kv head may serve at most 8 qo heads.
+ * Returns PKD_OK or a PKD_ERR_* code (a failing call may allocate to format its message).
+ */
+#define PKD_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define PKD_NOALLOC_MAX_ITEMS 24576
+#define PKD_NOALLOC_MAX_MERGES 16384
+#define PKD_NOALLOC_PARTIAL_BYTES ((16u << 20) - (1u << 20) - 512u)
+int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
+                       const int32_t* indices_dev, int64_t num_indices, int num_qo_heads,
+                       int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                       float logits_soft_cap, int window_left, int fixed_split_size,
+                       int disable_split_kv, int q_dtype, int kv_dtype, int o_dtype,
+                       int use_tensor_cores, int kv_layout, const void* q, const void* k_base,
+                       const void* v_base, int64_t num_pages, const int64_t kv_strides[3],
+                       float q_scale, float k_scale, float v_scale, void* o, float* lse,
+                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

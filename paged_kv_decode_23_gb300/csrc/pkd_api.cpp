@@ -188,6 +188,11 @@ int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl,
 
 }  // namespace
 
+namespace pkd {
+// Lets other translation units of the library report a failure through pkd_last_error().
+void set_error_message(const char* msg) { g_last_error.assign(msg); }
+}  // namespace pkd
+
 extern "C" {
 
 const char* pkd_last_error(void) { return g_last_error.c_str(); }
