@@ -252,12 +252,16 @@ def gpu_arm(args, w, rank, world):
     seg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range((layers + 1) * args.steps)] if flush is not None else None
 
+    host_plan_s = [0.0]
+
     def step(k=None):
         timed = seg is not None and k is not None
         if timed:
             seg[k * (layers + 1)][0].record(stream)
+        t_h = time.perf_counter()
         dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                  w.page_size, **plan_kw)
+        host_plan_s[0] += time.perf_counter() - t_h
         if timed:
             seg[k * (layers + 1)][1].record(stream)
         for l in range(layers):
@@ -279,7 +283,6 @@ def gpu_arm(args, w, rank, world):
         step()
     torch.cuda.synchronize()
     assert dec.check_status() == 0, "device status word reports a failure"
-    n_merge = 1 if _has_merges(w, dec) else 0
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -287,39 +290,50 @@ def gpu_arm(args, w, rank, world):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")  # lets a profiler restrict itself to the timed steps
     t_start.record(stream)
     for k in range(args.steps):
         step(k)
     t_end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
+    seg_detail = None
     if seg is not None:
         ms_total = sum(a.elapsed_time(b) for a, b in seg)
+        plan_ms = sum(seg[k * (layers + 1)][0].elapsed_time(seg[k * (layers + 1)][1])
+                      for k in range(args.steps))
+        seg_detail = {"plan_us_per_step": plan_ms * 1e3 / args.steps,
+                      "run_us_per_call": (ms_total - plan_ms) * 1e3 / (args.steps * layers)}
+    host_plan_us = host_plan_s[0] * 1e6 / (args.steps + args.warmup)
     kern_ms = [a.elapsed_time(b) for a, b in ev]
     assert dec.check_status() == 0, "device status word reports a failure"
 
-    # end to end through the public API with host buffers: q / page table in, o / lse out
-    q_host = [q.cpu().pin_memory() for q in qs]
-    o_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    l_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in lses]
+    # End to end through the public API with host buffers: every step copies all layers' q and
+    # the page ids in from pinned host memory (one copy each) and all layers' o and lse out.
+    q_all_host = torch.stack([q.cpu() for q in qs]).pin_memory()
+    q_all_dev = torch.empty_like(q_all_host, device=dev)
+    o_all_dev = torch.empty((layers,) + tuple(outs[0].shape), dtype=outs[0].dtype, device=dev)
+    l_all_dev = torch.empty((layers,) + tuple(lses[0].shape), dtype=torch.float32, device=dev)
+    o_all_host = torch.empty(o_all_dev.shape, dtype=o_all_dev.dtype).pin_memory()
+    l_all_host = torch.empty(l_all_dev.shape, dtype=torch.float32).pin_memory()
     idx_host = torch.from_numpy(w.indices).pin_memory()
-    q_dev = [torch.empty_like(q) for q in qs]
     idx_dev = torch.empty_like(indices)
 
     def e2e_step():
         idx_dev.copy_(idx_host, non_blocking=True)
+        q_all_dev.copy_(q_all_host, non_blocking=True)
         dec.plan(indptr_t, idx_dev, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                  w.page_size, **plan_kw)
         for l in range(layers):
             if flush is not None:
                 flush.fill_(float(l))
-            q_dev[l].copy_(q_host[l], non_blocking=True)
-            dec.run(q_dev[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale, out=outs[l],
-                    lse=lses[l])
-            o_host[l].copy_(outs[l], non_blocking=True)
-            l_host[l].copy_(lses[l], non_blocking=True)
+            dec.run(q_all_dev[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale,
+                    out=o_all_dev[l], lse=l_all_dev[l])
+        o_all_host.copy_(o_all_dev, non_blocking=True)
+        l_all_host.copy_(l_all_dev, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(args.warmup):
@@ -330,9 +344,8 @@ def gpu_arm(args, w, rank, world):
         e2e_step()
     barrier()
     e2e_s = time.perf_counter() - t0
-    h2d = sum(q.numel() * q.element_size() for q in q_host) + idx_host.numel() * 4
-    d2h = sum(o.numel() * o.element_size() for o in o_host) + sum(
-        x.numel() * x.element_size() for x in l_host)
+    h2d = q_all_host.numel() * q_all_host.element_size() + idx_host.numel() * 4
+    d2h = o_all_host.numel() * o_all_host.element_size() + l_all_host.numel() * 4
 
     if world > 1:
         t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=dev)
@@ -362,19 +375,13 @@ def gpu_arm(args, w, rank, world):
         "e2e": {"value": world * bytes_step / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s / args.steps * 1e3},
-        "gpu_launches": args.steps * layers * (1 + n_merge),
+        "gpu_launches": args.steps * layers,
         "clocks": clk,
+        "host_plan_us": host_plan_us,
     }
+    if seg_detail:
+        res["segments"] = seg_detail
     return res
-
-
-def _has_merges(w, dec):
-    from paged_kv_decode_23_gb300 import plan_host
-    p = plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads, w.head_dim,
-                  w.page_size, window_left=w.window_left, fixed_split_size=w.fixed_split_size,
-                  disable_split_kv=w.disable_split_kv,
-                  kv_dtype={"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype])
-    return len(p["merges"]) > 0
 
 
 def main():

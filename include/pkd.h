@@ -153,7 +153,8 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
  * The planner alone (host-only; no CUDA call), for inspection and tests.  Writes up to
  * max_items work items of 8 int32 each:
  *   {request, first page index into `indices`, chunk start token, first attended token,
- *    end token, partial slot (-1 = final), 0, 0}   (tokens count from the request's start)
+ *    end token, partial slot (-1 = final), merge entry (-1 = none), 0}
+ *   (tokens count from the request's start)
  * in launch order, and up to max_merges merge entries of 4 int32 {request, first slot,
  * chunk count, 0}.  n_items / n_merges / n_slots receive the full counts.  kernel_out
  * receives the chosen PKD_KERNEL_* and tile_tokens_out the tokens per pipeline stage.

@@ -34,7 +34,7 @@ namespace pkd {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, bool CONV>
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES>
 struct DecodeGeom {
   static constexpr int NW = TS / 16;  // consumer warps; each owns 16 tokens of a tile
   static constexpr int NCONS = NW * 32;
@@ -45,9 +45,8 @@ struct DecodeGeom {
   static constexpr int BOX_ELEMS = 128 / KV_ELT;
   static constexpr int TILE_BYTES = TS * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int CONV_BYTES = CONV ? NW * 16 * D * 2 : 0;  // 16-bit copy of 16 rows/warp
   static constexpr int EPI_BYTES = NW * (8 * D + 16) * 4;
-  static constexpr int PIPE_BYTES = NSTAGES * STAGE_BYTES + CONV_BYTES;
+  static constexpr int PIPE_BYTES = NSTAGES * STAGE_BYTES;
   static constexpr int SMEM_BYTES = (PIPE_BYTES > EPI_BYTES ? PIPE_BYTES : EPI_BYTES) + 1024;
   static_assert(ROW_BYTES % 128 == 0, "K/V rows must be whole 128-byte blocks");
   static_assert(TS % 16 == 0 && NW >= 1 && NW <= 8, "tile of 16-token warp slices");
@@ -58,6 +57,7 @@ struct BlockCoords {
   int kvh;    // kv head
   int g0;     // first qo head of this CTA
   int gcnt;   // qo heads of this CTA
+  int gs;     // which slice of the kv head's qo-head group
   int j0;     // first tile (relative to the chunk start)
   int ntiles;
 };
@@ -70,6 +70,7 @@ __device__ __forceinline__ BlockCoords block_coords(const DecodeParams& p) {
   const int rem = blockIdx.x - item * per_item;
   b.kvh = rem / p.gslices;
   const int gs = rem - b.kvh * p.gslices;
+  b.gs = gs;
   b.it = p.items[item];
   b.g0 = b.kvh * p.group + gs * HEADS;
   b.gcnt = min(HEADS, p.group - gs * HEADS);
@@ -205,21 +206,125 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const B
   }
 }
 
+// merge_states fused into the decode kernel: the CTA that finishes a split request's last
+// chunk (for its kv head and head slice) combines all chunks' partials, in chunk order, with
+// the arithmetic of merge_states_kernel.  Writers publish their partial with a fence before
+// counting; the last CTA fences again, reads the partials from L2 and resets the counter for
+// the next run of the plan.  No CTA waits for another.
+template <typename TQ, int D, int NW>
+__device__ __forceinline__ void fused_merge_tail(const DecodeParams& p, const BlockCoords& b,
+                                                 int tid, bool aborted, volatile int* last_flag) {
+  using namespace dev;
+  constexpr int NCONS = NW * 32;
+  constexpr int D8 = D / 8;
+  if (!p.fuse_merge || b.it.out_slot < 0) return;  // uniform over the CTA
+  __threadfence();
+  named_bar_sync(1, NCONS);
+  if (tid == 0) {
+    int last = 0;
+    if (!aborted) {
+      uint32_t* ctr = p.counters +
+                      ((size_t)b.it.merge_idx * p.num_kv_heads + b.kvh) * p.gslices + b.gs;
+      const uint32_t prev = atomicAdd(ctr, 1u);
+      last = (prev + 1u == (uint32_t)p.merges[b.it.merge_idx].n_chunks) ? 1 : 0;
+      if (last) *ctr = 0u;
+    }
+    *last_flag = last;
+  }
+  named_bar_sync(1, NCONS);
+  if (!*last_flag) return;
+  __threadfence();
+  const MergeEntry me = p.merges[b.it.merge_idx];
+  const int hq = p.num_qo_heads;
+  for (int u = tid; u < b.gcnt * D8; u += NCONS) {
+    const int g = u / D8;
+    const int d0 = (u - g * D8) * 8;
+    const int qo = b.g0 + g;
+    // Loads go four chunks at a time, independent of each other, so a merge costs about two
+    // L2 round trips; the sums still run in chunk order.
+    constexpr int U = 4;
+    float M = kNegInf;
+    for (int c0 = 0; c0 < me.n_chunks; c0 += U) {
+      float l[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j)
+        l[j] = c0 + j < me.n_chunks
+                   ? __ldcg(p.part_lse + (size_t)(me.first_slot + c0 + j) * hq + qo)
+                   : kNegInf;
+#pragma unroll
+      for (int j = 0; j < U; ++j) M = fmaxf(M, l[j]);
+    }
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = 0.f;
+    float L = 0.f;
+    if (M != kNegInf) {
+      for (int c0 = 0; c0 < me.n_chunks; c0 += U) {
+        float l[U];
+        float4 a[U][2];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const bool in = c0 + j < me.n_chunks;
+          const size_t row = (size_t)(me.first_slot + (in ? c0 + j : 0)) * hq + qo;
+          const float4* src = reinterpret_cast<const float4*>(p.part_o + row * D + d0);
+          l[j] = in ? __ldcg(p.part_lse + row) : kNegInf;
+          a[j][0] = __ldcg(src);
+          a[j][1] = __ldcg(src + 1);
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          if (c0 + j >= me.n_chunks) break;
+          const float f = fast_exp2(l[j] - M);
+          L += f;
+          o[0] = fmaf(f, a[j][0].x, o[0]); o[1] = fmaf(f, a[j][0].y, o[1]);
+          o[2] = fmaf(f, a[j][0].z, o[2]); o[3] = fmaf(f, a[j][0].w, o[3]);
+          o[4] = fmaf(f, a[j][1].x, o[4]); o[5] = fmaf(f, a[j][1].y, o[5]);
+          o[6] = fmaf(f, a[j][1].z, o[6]); o[7] = fmaf(f, a[j][1].w, o[7]);
+        }
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint4 v;
+    v.x = pack2<TQ>(o[0] * inv, o[1] * inv);
+    v.y = pack2<TQ>(o[2] * inv, o[3] * inv);
+    v.z = pack2<TQ>(o[4] * inv, o[5] * inv);
+    v.w = pack2<TQ>(o[6] * inv, o[7] * inv);
+    TQ* dst = reinterpret_cast<TQ*>(p.o) + ((size_t)me.req * hq + qo) * D + d0;
+    *reinterpret_cast<uint4*>(dst) = v;
+    if (d0 == 0 && p.lse)
+      p.lse[(size_t)me.req * hq + qo] = L > 0.f ? (M + log2f(L)) * kLn2 : kNegInf;
+  }
+}
+
 // ------------------------------------------------------------------------------ score
+// tanh(x) = 1 - 2 / (e^(2x) + 1): one ex2.approx and one reciprocal.  Saturates to +-1 for
+// large |x| (e^(2x) overflows to inf, or underflows to 0); near 0 its absolute error is a few
+// 1e-7, far below what the soft-capped logits need.
+__device__ __forceinline__ float tanh_via_exp2(float x) {
+  const float e = dev::fast_exp2(x * 2.8853900817779268f);  // 2 * log2(e)
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
 __device__ __forceinline__ float score_log2(float dot, float scale_qk, float cap_log2) {
   const float x = dot * scale_qk;
-  return cap_log2 > 0.f ? cap_log2 * tanhf(x) : x;
+  return cap_log2 > 0.f ? cap_log2 * tanh_via_exp2(x) : x;
 }
 
 // ------------------------------------------------------------------------------ tensor core
 // Loads the B fragments of Q^T (mma k = head_dim, n = 8 qo heads) for this lane.  For e4m3
 // KV the MMA runs in fp16: q is scaled by 2^-qexp (exact) so it fits fp16's range; the
 // caller multiplies the scores back by 2^qexp.
-template <typename TQ, typename T, int D>
+// With PERM (the e4m3 path), the 16 head_dim values of k-step kk are assigned to the MMA's k
+// slots so that lane tig's four slots {2tig, 2tig+1, 2tig+8, 2tig+9} hold d = kk*16 + 4tig ..
+// kk*16 + 4tig + 3: the matching K bytes are then one 32-bit load.  A dot product does not
+// depend on the order of its terms, so K and Q only have to agree.
+template <typename TQ, typename T, int D, bool PERM = false>
 __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockCoords& b, int lane,
                                              uint32_t (&qb)[D / 16][2], float& qmul) {
   using namespace dev;
   const int g = lane >> 2, tig = lane & 3;
+  const int off0 = PERM ? tig * 4 : tig * 2;      // d of slot pair 0 within the k-step
+  const int off1 = PERM ? tig * 4 + 2 : tig * 2 + 8;  // d of slot pair 1
   const bool live = g < b.gcnt;
   const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
                    ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D;
@@ -227,8 +332,8 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
   if constexpr (sizeof(TQ) == sizeof(T) && std::is_same<TQ, T>::value) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qb[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + tig * 2) : 0u;
-      qb[kk][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + tig * 2) : 0u;
+      qb[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + off0) : 0u;
+      qb[kk][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + off1) : 0u;
     }
   } else {
     float2 f[D / 16][2];
@@ -238,7 +343,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t raw =
-            live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + h * 8 + tig * 2) : 0u;
+            live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + (h ? off1 : off0)) : 0u;
         f[kk][h] = unpack2<TQ>(raw);
         amax = fmaxf(amax, fmaxf(fabsf(f[kk][h].x), fabsf(f[kk][h].y)));
       }
@@ -256,41 +361,33 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
   }
 }
 
-// Converts this warp's 16 rows of an e4m3 tile into the warp's fp16 staging area (same
-// swizzled layout, 16 rows per column block).  Rows outside [vlo, vhi) become zeros when
-// `zero_invalid` is set.
-template <int D, int TS>
-__device__ __forceinline__ void convert_rows_e4m3(uint32_t src_tile, int row0, uint32_t dst, int vlo,
-                                                  int vhi, bool zero_invalid, int lane) {
-  using namespace dev;
-  constexpr int C8 = D / 16;  // 16-byte chunks per fp8 row
-#pragma unroll
-  for (int k = 0; k < (16 * C8) / 32; ++k) {
-    const int ci = lane + 32 * k;
-    const int r = ci / C8;
-    const int c = ci - r * C8;
-    uint4 in;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(in.x), "=r"(in.y), "=r"(in.z), "=r"(in.w)
-                 : "r"(src_tile + swz_off(row0 + r, c, TS)));
-    uint4 lo, hi;
-    if (zero_invalid && (r < vlo || r >= vhi)) {
-      lo = make_uint4(0, 0, 0, 0);
-      hi = lo;
-    } else {
-      lo.x = e4m3x2_to_half2(in.x & 0xffff); lo.y = e4m3x2_to_half2(in.x >> 16);
-      lo.z = e4m3x2_to_half2(in.y & 0xffff); lo.w = e4m3x2_to_half2(in.y >> 16);
-      hi.x = e4m3x2_to_half2(in.z & 0xffff); hi.y = e4m3x2_to_half2(in.z >> 16);
-      hi.z = e4m3x2_to_half2(in.w & 0xffff); hi.w = e4m3x2_to_half2(in.w >> 16);
-    }
-    const uint32_t d_lo = dst + swz_off(r, 2 * c, 16);
-    const uint32_t d_hi = dst + swz_off(r, 2 * c + 1, 16);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d_lo), "r"(lo.x), "r"(lo.y),
-                 "r"(lo.z), "r"(lo.w)
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d_hi), "r"(hi.x), "r"(hi.y),
-                 "r"(hi.z), "r"(hi.w)
-                 : "memory");
+// The e4m3 tensor-core path never widens a tile in shared memory.  Instead it reorders the
+// MMA operands so that every lane's operand bytes are contiguous:
+//   * tokens: row j of S^T (= k slot j of P^T) holds token perm_tok(j) of the warp's slice,
+//     chosen so that lane tig's k slots {2tig, 2tig+1, 2tig+8, 2tig+9} are tokens
+//     tig, tig+4, tig+8, tig+12 (and the eight S^T rows a K load touches fall in eight
+//     different swizzle phases, so those loads are free of bank conflicts);
+//   * head_dim: rows r and r+8 of O^T block mb = 4q + jj hold d = 64q + 8r + 2jj and
+//     64q + 8r + 2jj + 1, so lane r reads bytes 64q + 8r .. 64q + 8r + 7 of each of its four
+//     tokens (one 64-bit load) and builds the V^T fragments with two byte permutes per block.
+// Every e4m3 value is an fp16 value, so the widening (cvt.f16x2.e4m3x2) is exact.
+__device__ __forceinline__ int perm_tok(int j) {
+  return ((j & 7) >> 1) + 4 * (j & 1) + 8 * (j >> 3);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// d index held by accumulator row `row` (0..15) of O^T block mb.
+template <bool KV_FP8>
+__device__ __forceinline__ int acc_dim(int mb, int row) {
+  if constexpr (KV_FP8) {
+    return 64 * (mb >> 2) + 8 * (row & 7) + 2 * (mb & 3) + (row >> 3);
+  } else {
+    return mb * 16 + row;
   }
 }
 
@@ -301,14 +398,16 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
                                            float (&acc)[D / 16][4]) {
   using namespace dev;
   using T = typename std::conditional<KV_FP8, __half, TQ>::type;
-  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, KV_FP8>;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   uint32_t qb[D / 16][2];
   float qmul;
-  load_q_frags<TQ, T, D>(p, b, lane, qb, qmul);
+  load_q_frags<TQ, T, D, KV_FP8>(p, b, lane, qb, qmul);
   const float scale_qk = p.scale_qk * qmul;
   const float cap_log2 = p.cap_log2;
-  const uint32_t conv = smem + NSTAGES * G::STAGE_BYTES + warp * (16 * D * 2);
-  const int g_row = lane >> 2;
+  const int g_row = lane >> 2, tig = lane & 3;
+  // tokens (within the warp's 16-token slice) of this lane's two S^T rows
+  const int tok_a = KV_FP8 ? perm_tok(g_row) : g_row;
+  const int tok_b = KV_FP8 ? perm_tok(g_row + 8) : g_row + 8;
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
@@ -322,21 +421,11 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
     const int vhi = min(16, b.it.tok_end - t_w);
     const uint32_t ktile = smem + s * G::STAGE_BYTES;
     const uint32_t vtile = ktile + G::TILE_BYTES;
+    const int r0 = warp * 16;  // first tile row of my slice
     bool wrote_stage = false;
     if (vhi > vlo) {
       const bool partial = vlo > 0 || vhi < 16;
-      uint32_t kview;
-      int rb, r0;
-      if constexpr (KV_FP8) {
-        convert_rows_e4m3<D, TS>(ktile, warp * 16, conv, vlo, vhi, false, lane);
-        __syncwarp();
-        kview = conv;
-        rb = 16;
-        r0 = 0;
-      } else {
-        kview = ktile;
-        rb = TS;
-        r0 = warp * 16;
+      if constexpr (!KV_FP8) {
         if (partial) {
           // Zero the V rows this slice does not attend, so 0 * garbage cannot reach O.
           constexpr int CPR = D / 8;  // 16-byte chunks per 16-bit row
@@ -353,28 +442,42 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
       }
       // ---- S^T = K * Q^T : rows = 16 tokens, cols = 8 qo heads
       float c[4] = {0.f, 0.f, 0.f, 0.f};
-      {
+      if constexpr (KV_FP8) {
+        // rows tok_a / tok_b; k slots as in load_q_frags<PERM>: four consecutive e4m3 bytes
+        const int ra = r0 + tok_a, rbw = r0 + tok_b;
+        const uint32_t base_a = ktile + ra * 128 + tig * 4, base_b = ktile + rbw * 128 + tig * 4;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t blk = (kk >> 3) * TS * 128;  // 128-byte column block of the chunk
+          uint32_t wa, wb;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa)
+                       : "r"(base_a + blk + (((kk & 7) ^ (ra & 7)) << 4)));
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb)
+                       : "r"(base_b + blk + (((kk & 7) ^ (rbw & 7)) << 4)));
+          uint32_t a[4];
+          a[0] = e4m3x2_to_half2(wa & 0xffff);
+          a[2] = e4m3x2_to_half2(wa >> 16);
+          a[1] = e4m3x2_to_half2(wb & 0xffff);
+          a[3] = e4m3x2_to_half2(wb >> 16);
+          mma_16816<T>(c, a, qb[kk][0], qb[kk][1]);
+        }
+      } else {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int csel = lane >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t a[4];
-          ldsm_x4(kview + swz_off(r0 + row, kk * 2 + csel, rb), a);
+          ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
           mma_16816<T>(c, a, qb[kk][0], qb[kk][1]);
         }
-      }
-      if constexpr (KV_FP8) {
-        __syncwarp();
-        convert_rows_e4m3<D, TS>(vtile, warp * 16, conv, vlo, vhi, true, lane);
-        __syncwarp();
       }
       // ---- online softmax over the 16 tokens, per qo-head column
       float sc[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = g_row + (e >= 2 ? 8 : 0);
+        const int t = e >= 2 ? tok_b : tok_a;
         const float sv = score_log2(c[e], scale_qk, cap_log2);
-        sc[e] = (r >= vlo && r < vhi) ? sv : kNegInf;
+        sc[e] = (t >= vlo && t < vhi) ? sv : kNegInf;
       }
       float alpha[2];
 #pragma unroll
@@ -391,25 +494,57 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
         lsum[j] = lsum[j] * alpha[j] + sc[j] + sc[j + 2];
         m2[j] = mnew;
       }
+      // rescale O only when some column's running max moved (alpha is exactly 1 otherwise)
+      if (__any_sync(~0u, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int mb = 0; mb < D / 16; ++mb) {
-        acc[mb][0] *= alpha[0];
-        acc[mb][1] *= alpha[1];
-        acc[mb][2] *= alpha[0];
-        acc[mb][3] *= alpha[1];
+        for (int mb = 0; mb < D / 16; ++mb) {
+          acc[mb][0] *= alpha[0];
+          acc[mb][1] *= alpha[1];
+          acc[mb][2] *= alpha[0];
+          acc[mb][3] *= alpha[1];
+        }
       }
       // ---- P^T as the B operand (k = token, n = qo head): transpose the C fragment
       const uint32_t b0 = movmatrix_trans(pack2<T>(sc[0], sc[1]));
       const uint32_t b1 = movmatrix_trans(pack2<T>(sc[2], sc[3]));
       // ---- O^T += V^T * P^T : rows = head_dim (16 per block), cols = 8 qo heads
-      {
-        const uint32_t vview_ = KV_FP8 ? conv : vtile;
+      if constexpr (KV_FP8) {
+#pragma unroll
+        for (int q4 = 0; q4 < D / 64; ++q4) {
+          // bytes 64*q4 + 8*g_row .. +7 of tokens tig + 4*t4 (zero if not attended)
+          const int c16 = 4 * q4 + (g_row >> 1);  // 16-byte chunk index in the fp8 row
+          uint32_t w[4][2];
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const int tok = tig + 4 * t4;
+            const int row = r0 + tok;
+            const uint32_t addr = vtile + (c16 >> 3) * TS * 128 + row * 128 +
+                                  (((c16 & 7) ^ (row & 7)) << 4) + (g_row & 1) * 8;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(w[t4][0]), "=r"(w[t4][1]) : "r"(addr));
+            if (tok < vlo || tok >= vhi) w[t4][0] = w[t4][1] = 0u;
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int wd = jj >> 1;
+            const uint32_t sel = (jj & 1) ? 0x7362u : 0x5140u;  // bytes (b, b') of two words
+            const uint32_t x01 = prmt(w[0][wd], w[1][wd], sel);
+            const uint32_t x23 = prmt(w[2][wd], w[3][wd], sel);
+            uint32_t a[4];
+            a[0] = e4m3x2_to_half2(x01 & 0xffff);  // d = c0, tokens tig, tig+4
+            a[1] = e4m3x2_to_half2(x01 >> 16);     // d = c0 + 1
+            a[2] = e4m3x2_to_half2(x23 & 0xffff);  // d = c0, tokens tig+8, tig+12
+            a[3] = e4m3x2_to_half2(x23 >> 16);
+            mma_16816<T>(acc[4 * q4 + jj], a, b0, b1);
+          }
+        }
+      } else {
         const int row = (lane & 7) + (lane >> 4) * 8;
         const int csel = (lane >> 3) & 1;
 #pragma unroll
         for (int mb = 0; mb < D / 16; ++mb) {
           uint32_t a[4];
-          ldsm_x4_trans(vview_ + swz_off(r0 + row, mb * 2 + csel, rb), a);
+          ldsm_x4_trans(vtile + swz_off(r0 + row, mb * 2 + csel, TS), a);
           mma_16816<T>(acc[mb], a, b0, b1);
         }
       }
@@ -420,7 +555,7 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   }
 }
 
-template <int D>
+template <int D, bool KV_FP8>
 __device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane, float (&m2)[2],
                                          float (&lsum)[2], float (&acc)[D / 16][4]) {
   const int gr = lane >> 2, tig = lane & 3;
@@ -438,11 +573,11 @@ __device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane
   float* a = e.acc + warp * 8 * D;
 #pragma unroll
   for (int mb = 0; mb < D / 16; ++mb) {
-    const int d = mb * 16 + gr;
-    a[(tig * 2) * D + d] = acc[mb][0];
-    a[(tig * 2 + 1) * D + d] = acc[mb][1];
-    a[(tig * 2) * D + d + 8] = acc[mb][2];
-    a[(tig * 2 + 1) * D + d + 8] = acc[mb][3];
+    const int da = acc_dim<KV_FP8>(mb, gr), db = acc_dim<KV_FP8>(mb, gr + 8);
+    a[(tig * 2) * D + da] = acc[mb][0];
+    a[(tig * 2 + 1) * D + da] = acc[mb][1];
+    a[(tig * 2) * D + db] = acc[mb][2];
+    a[(tig * 2 + 1) * D + db] = acc[mb][3];
   }
 }
 
@@ -507,7 +642,7 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
                                            int warp, int lane, float& m2, float& lsum,
                                            float (&acc)[GP][D / 32]) {
   using namespace dev;
-  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, false>;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   using R = CcRow<TQ, KV_FP8, D>;
   constexpr int EPL = R::EPL;
   constexpr int TW = 32 / GP;  // tokens per reduce-scatter group
@@ -628,15 +763,15 @@ __device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane
 // ------------------------------------------------------------------------------ kernel
 // KIND: kTensorCore (HEADS = 8 qo heads per CTA) or kCudaCore (HEADS = GP).
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
-__global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES,
-                                             (KIND == kTensorCore && KV_FP8)>::THREADS, 1)
+__global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREADS,
+                                  KIND == kTensorCore ? 2 : 1)
     decode_paged_kernel(const __grid_constant__ DecodeParams p) {
   using namespace dev;
-  constexpr bool CONV = (KIND == kTensorCore) && KV_FP8;
-  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, CONV>;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   constexpr int HEADS = KIND == kTensorCore ? 8 : GP;
   __shared__ __align__(8) uint64_t bars[2 * NSTAGES];
   __shared__ int abort_flag_s;
+  __shared__ int merge_last_s;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem_p =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -672,7 +807,7 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES,
     consume_tc<TQ, KV_FP8, D, TS, NSTAGES>(p, b, smem, full0, empty0, abort_flag, warp, lane, m2,
                                            lsum, acc);
     named_bar_sync(1, G::NCONS);  // every consumer is done with the stages
-    stash_tc<D>(epi, warp, lane, m2, lsum, acc);
+    stash_tc<D, KV_FP8>(epi, warp, lane, m2, lsum, acc);
   } else {
     float m2 = kNegInf, lsum = 0.f;
     float acc[GP][D / 32];
@@ -686,14 +821,15 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES,
     stash_cc<D, GP>(epi, warp, lane, m2, lsum, acc);
   }
   named_bar_sync(1, G::NCONS);
-  combine_and_store<TQ, D, G::NW>(p, b, epi, threadIdx.x, *abort_flag != 0);
+  const bool aborted = *abort_flag != 0;
+  combine_and_store<TQ, D, G::NW>(p, b, epi, threadIdx.x, aborted);
+  fused_merge_tail<TQ, D, G::NW>(p, b, threadIdx.x, aborted, &merge_last_s);
 }
 
 // ------------------------------------------------------------------------------ registry
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
 DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
-  constexpr bool CONV = (KIND == kTensorCore) && KV_FP8;
-  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES, CONV>;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   DecodeKernel k;
   k.kind = KIND;
   k.q_dtype = q_dtype;

@@ -50,7 +50,7 @@ struct NaDecode {
 #define PKD_NA_DEC(TQ, FP8, D, TS, NS, QC, KC)                                              \
   NaDecode {                                                                                \
     QC, KC, D, reinterpret_cast<const void*>(&decode_paged_kernel<TQ, FP8, D, TS, NS, kTensorCore, 8>), \
-        DecodeGeom<TQ, FP8, D, TS, NS, FP8>::THREADS, DecodeGeom<TQ, FP8, D, TS, NS, FP8>::SMEM_BYTES, TS \
+        DecodeGeom<TQ, FP8, D, TS, NS>::THREADS, DecodeGeom<TQ, FP8, D, TS, NS>::SMEM_BYTES, TS \
   }
 
 // The tensor-core kernels of decode_f16.cu / decode_bf16.cu / decode_e4m3.cu.
@@ -61,10 +61,10 @@ const NaDecode kNaDecode[] = {
     PKD_NA_DEC(__nv_bfloat16, false, 64, 128, 3, kBF16, kBF16),
     PKD_NA_DEC(__nv_bfloat16, false, 128, 64, 3, kBF16, kBF16),
     PKD_NA_DEC(__nv_bfloat16, false, 256, 32, 3, kBF16, kBF16),
-    PKD_NA_DEC(__half, true, 128, 128, 2, kF16, kE4M3),
-    PKD_NA_DEC(__half, true, 256, 64, 2, kF16, kE4M3),
-    PKD_NA_DEC(__nv_bfloat16, true, 128, 128, 2, kBF16, kE4M3),
-    PKD_NA_DEC(__nv_bfloat16, true, 256, 64, 2, kBF16, kE4M3),
+    PKD_NA_DEC(__half, true, 128, 128, 3, kF16, kE4M3),
+    PKD_NA_DEC(__half, true, 256, 64, 3, kF16, kE4M3),
+    PKD_NA_DEC(__nv_bfloat16, true, 128, 128, 3, kBF16, kE4M3),
+    PKD_NA_DEC(__nv_bfloat16, true, 256, 64, 3, kBF16, kE4M3),
 };
 #undef PKD_NA_DEC
 

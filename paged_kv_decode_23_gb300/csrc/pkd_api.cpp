@@ -166,6 +166,19 @@ int make_kv_tensor_map(CUtensorMap* map, const void* base, int kv_dtype, int hea
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Raise a decode kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t set_smem_limit_once(const DecodeKernel* k, int device) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == k->fn && d.second == device) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes);
+  if (e == cudaSuccess) done.emplace_back(k->fn, device);
+  return e;
+}
+
 int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl, int batch,
                       int hq, int hkv, int d, int ps, int window_left, int fixed_split,
                       int disable_split, int kv_dtype, int use_tc, int num_sms) {
@@ -296,7 +309,7 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
   rc = build_plan(r, &plan, &err);
   if (rc) return fail(rc, err);
   if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(plan, num_qo_heads, head_dim);
-  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(plan);
+  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(plan, num_kv_heads);
   return PKD_OK;
 }
 
@@ -337,7 +350,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     return fail(PKD_ERR_UNSUPPORTED, "no merge kernel built for this dtype / head_dim");
 
   const size_t need_f = float_ws_bytes_of(plan, num_qo_heads, head_dim);
-  const size_t need_i = int_ws_bytes_of(plan);
+  const size_t need_i = int_ws_bytes_of(plan, num_kv_heads);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
     char buf[200];
     std::snprintf(buf, sizeof buf, "workspace too small: need %zu float / %zu int bytes", need_f,
@@ -345,8 +358,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     return fail(PKD_ERR_WORKSPACE_TOO_SMALL, buf);
   }
 
-  cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       k->smem_bytes);
+  cudaError_t e = set_smem_limit_once(k, h->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
   // Upload the work list: wait for the previous upload to leave the pinned buffer first.
@@ -370,10 +382,11 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (items_b) std::memcpy(h->staging, plan.items.data(), items_b);
   if (merges_b) std::memcpy(static_cast<char*>(h->staging) + items_b, plan.merges.data(), merges_b);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(h->int_ws, 0, kStatusBytes, s);
+  const size_t items_off = items_offset(plan, num_kv_heads);
+  e = cudaMemsetAsync(h->int_ws, 0, items_off, s);  // status word and merge counters
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   if (bytes) {
-    e = cudaMemcpyAsync(static_cast<char*>(h->int_ws) + kStatusBytes, h->staging, bytes,
+    e = cudaMemcpyAsync(static_cast<char*>(h->int_ws) + items_off, h->staging, bytes,
                         cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
     e = cudaEventRecord(h->staging_done, s);
@@ -443,7 +456,10 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   char* fws = static_cast<char*>(h->float_ws);
   const size_t part_o_bytes =
       ((size_t)h->plan.num_slots * h->num_qo_heads * h->head_dim * sizeof(float) + 255) / 256 * 256;
-  prm.items = reinterpret_cast<const WorkItem*>(iws + kStatusBytes);
+  prm.items = reinterpret_cast<const WorkItem*>(iws + items_offset(h->plan, h->num_kv_heads));
+  prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(h->plan, h->num_kv_heads));
+  prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
+  prm.fuse_merge = 1;
   prm.indices = h->indices;
   prm.q = q;
   prm.o = o;
@@ -479,24 +495,7 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
 
-  if (!h->plan.merges.empty()) {
-    MergeParams mp;
-    mp.merges = reinterpret_cast<const MergeEntry*>(iws + kStatusBytes +
-                                                     h->plan.items.size() * sizeof(WorkItem));
-    mp.part_o = prm.part_o;
-    mp.part_lse = prm.part_lse;
-    mp.o = o;
-    mp.lse = lse;
-    mp.status = prm.status;
-    mp.num_merges = (int)h->plan.merges.size();
-    mp.num_qo_heads = h->num_qo_heads;
-    const int64_t warps = (int64_t)mp.num_merges * mp.num_qo_heads;
-    const int64_t blocks = (warps + h->merge->heads_per_block - 1) / h->merge->heads_per_block;
-    void* margs[] = {&mp};
-    e = cudaLaunchKernel(h->merge->fn, dim3((unsigned)blocks), dim3(h->merge->threads), margs, 0,
-                         s);
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-  }
+  // split requests are merged by the decode kernel's last CTA per request (fuse_merge)
   return PKD_OK;
 }
 

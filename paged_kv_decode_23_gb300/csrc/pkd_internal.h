@@ -21,7 +21,7 @@ struct WorkItem {
   int32_t tok_begin;
   int32_t tok_end;
   int32_t out_slot;
-  int32_t pad0;
+  int32_t merge_idx;   // index of the request's MergeEntry when out_slot >= 0, else -1
   int32_t pad1;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
@@ -51,6 +51,9 @@ struct DecodeParams {
   float* part_o;        // [slots, Hq, D] fp32, normalised partial outputs
   float* part_lse;      // [slots, Hq] fp32, base-2 log-sum-exp of the partial
   uint32_t* status;     // device status word (bit 0: a pipeline wait timed out)
+  const MergeEntry* merges;  // with fuse_merge: the split requests
+  uint32_t* counters;   // with fuse_merge: finished chunks per (merge entry, kv head, slice)
+  int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
   int num_qo_heads;
   int num_kv_heads;
   int group;            // Hq / Hkv
@@ -134,9 +137,19 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err);
 
 // Byte offsets inside the int workspace.
 constexpr size_t kStatusBytes = 256;
-inline size_t int_ws_bytes_of(const Plan& p) {
-  return kStatusBytes + p.items.size() * sizeof(WorkItem) +
-         p.merges.size() * sizeof(MergeEntry) + 256;
+// int workspace: [status word | merge counters | work items | merge entries]; plan() zeroes
+// everything before the work items.
+inline size_t merge_counter_count(const Plan& p, int num_kv_heads) {
+  return p.merges.size() * (size_t)num_kv_heads * p.gslices;
+}
+inline size_t items_offset(const Plan& p, int num_kv_heads) {
+  return kStatusBytes + (merge_counter_count(p, num_kv_heads) * 4 + 255) / 256 * 256;
+}
+inline size_t merges_offset(const Plan& p, int num_kv_heads) {
+  return items_offset(p, num_kv_heads) + p.items.size() * sizeof(WorkItem);
+}
+inline size_t int_ws_bytes_of(const Plan& p, int num_kv_heads) {
+  return merges_offset(p, num_kv_heads) + p.merges.size() * sizeof(MergeEntry) + 256;
 }
 inline size_t float_ws_bytes_of(const Plan& p, int num_qo_heads, int head_dim) {
   size_t o = (size_t)p.num_slots * num_qo_heads * head_dim * sizeof(float);

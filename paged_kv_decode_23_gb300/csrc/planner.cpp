@@ -134,6 +134,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     std::memset(&it, 0, sizeof it);
     it.req = i;
     it.page_base = r.indptr[i];
+    it.merge_idx = -1;
     if (n[i] == 0) {
       it.chunk_tok0 = 0;
       it.tok_begin = 0;
@@ -146,6 +147,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     const int64_t k1 = C > 0 ? (n[i] - 1) / C : 0;
     const int64_t nchunks = k1 - k0 + 1;
     const int first_slot = plan->num_slots;
+    it.merge_idx = nchunks > 1 ? (int32_t)plan->merges.size() : -1;
     for (int64_t k = k0; k <= k1; ++k) {
       const int64_t c0 = C > 0 ? k * C : 0;
       const int64_t c1 = C > 0 ? std::min(n[i], (k + 1) * C) : n[i];

@@ -213,7 +213,7 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
               disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
               use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152):
     """Run the host planner alone (no GPU): returns a dict with the work items
-    ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, 0, 0), the merge
+    ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, merge entry, 0), the merge
     entries ``[m, 4]``, the slot count, the chosen kernel and the tile size."""
     ip = _host_i32(indptr)
     lpl = _host_i32(last_page_len)

@@ -75,9 +75,10 @@ def _check_partition(w, plan, C):
             if C:
                 assert c0 % C == 0 and e0 - c0 <= C
         if len(its) == 1:
-            assert its[0][5] == -1 and i not in merge_of
+            assert its[0][5] == -1 and i not in merge_of and its[0][6] == -1
         else:
             m = merge_of[i]
+            assert all(merges[int(it[6])][0] == i for it in its)
             assert int(m[2]) == len(its)
             assert [int(it[5]) for it in its] == list(range(int(m[1]), int(m[1]) + len(its)))
             slots += [int(it[5]) for it in its]
