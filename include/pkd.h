@@ -133,6 +133,15 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
                   float k_scale, float v_scale, void* o, float* lse, void* stream,
                   void* ev_start, void* ev_end);
 
+/*
+ * Programmatic dependent launch (the page's run(enable_pdl=...)), on by default.  When on, the
+ * decode kernel is launched with programmatic stream serialization: the GPU may schedule it
+ * while the previous kernel in the stream is still finishing, and the kernel waits
+ * (griddepcontrol.wait) before it reads anything, so results are the same either way; only
+ * the launch gap is hidden.  Off: ordinary stream order.
+ */
+int pkd_set_pdl(pkd_handle* h, int enable);
+
 /* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
 int pkd_destroy(pkd_handle* h);
 

@@ -52,6 +52,7 @@ SIGNATURES = {
                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int)]),
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "pkd_set_pdl": (_c_int, [_vp, _c_int]),
     "pkd_decode_noalloc": (_c_int, [_i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
                                     _c_int, _c_int, _c_float, _c_float, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,

@@ -781,6 +781,12 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
   volatile int* abort_flag = &abort_flag_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Programmatic dependent launch: this grid may have been started while the previous kernel
+  // in the stream was still running; nothing here is read before that kernel has finished
+  // (its results, and its use of the shared workspaces, are then complete).  The next kernel
+  // may start its own launch as soon as every CTA of this one is running.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const BlockCoords b = block_coords<TS, HEADS>(p);
   if (threadIdx.x == 0) {
 #pragma unroll

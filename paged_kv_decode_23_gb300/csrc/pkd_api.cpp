@@ -110,6 +110,7 @@ struct pkd_handle {
   size_t staging_bytes = 0;
   cudaEvent_t staging_done = nullptr;
   bool staging_pending = false;
+  bool pdl = true;  // launch the decode kernel as a programmatic dependent of its predecessor
 };
 
 namespace {
@@ -489,8 +490,20 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   cudaError_t e;
   if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
-  e = cudaLaunchKernel(h->kernel->fn, dim3((unsigned)grid), dim3(h->kernel->threads), args,
-                       (size_t)h->kernel->smem_bytes, s);
+  {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(h->kernel->threads);
+    cfg.dynamicSmemBytes = (size_t)h->kernel->smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = h->pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, h->kernel->fn, args);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
@@ -504,6 +517,12 @@ int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base
             float v_scale, void* o, float* lse, void* stream) {
   return pkd_run_timed(h, q, k_base, v_base, num_pages, kv_strides, q_scale, k_scale, v_scale, o,
                        lse, stream, nullptr, nullptr);
+}
+
+int pkd_set_pdl(pkd_handle* h, int enable) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  h->pdl = enable != 0;
+  return PKD_OK;
 }
 
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {

@@ -8,8 +8,9 @@
 //   - window_left keeps the keys t >= kv_len - 1 - window_left;
 //   - fixed_split_size (pages) fixes the split-KV chunk so that the merge, and thus the
 //     output, does not depend on the batch; disable_split_kv keeps one chunk per request.
-// Chunks are cut at multiples of the chunk size counted from the request's first token, so
-// a request's partition depends only on its own length, its window and the chunk size.
+// With a fixed split, chunks are cut at multiples of the chunk size counted from the request's
+// first token, so a request's partition depends only on its own length, its window and the
+// chunk size.  The heuristic split cuts a long request into equal page-aligned chunks.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -129,6 +130,8 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
 
   // work items, partial slots in request order, merge entries
   std::vector<WorkItem>& items = plan->items;
+  const bool fixed = !r.disable_split_kv && r.fixed_split_size > 0;
+  std::vector<int64_t> bounds, tile0;
   for (int i = 0; i < r.batch; ++i) {
     WorkItem it;
     std::memset(&it, 0, sizeof it);
@@ -143,17 +146,42 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       items.push_back(it);
       continue;
     }
-    const int64_t k0 = C > 0 ? w[i] / C : 0;
-    const int64_t k1 = C > 0 ? (n[i] - 1) / C : 0;
-    const int64_t nchunks = k1 - k0 + 1;
+    // chunk boundaries: [bounds[j], bounds[j+1]); chunk j's tiles start at tile0[j]
+    bounds.clear();
+    tile0.clear();
+    if (C == 0) {
+      bounds = {w[i], n[i]};
+      tile0 = {0};
+    } else if (fixed) {
+      // multiples of C counted from token 0: independent of the rest of the batch
+      for (int64_t k = w[i] / C; k <= (n[i] - 1) / C; ++k) {
+        bounds.push_back(std::max(k * C, w[i]));
+        tile0.push_back(k * C);
+      }
+      bounds.push_back(n[i]);
+    } else {
+      // heuristic: k equal page-aligned chunks, so no short remainder chunk (which would
+      // launch last and do the request's merge at the very end of the grid)
+      const int64_t a = n[i] - w[i];
+      const int64_t k = (a + C - 1) / C;
+      bounds.push_back(w[i]);
+      tile0.push_back(w[i] / ps * ps);
+      for (int64_t j = 1; j < k; ++j) {
+        const int64_t b = (w[i] + a * j / k) / ps * ps;
+        if (b > bounds.back() && b < n[i]) {
+          bounds.push_back(b);
+          tile0.push_back(b);
+        }
+      }
+      bounds.push_back(n[i]);
+    }
+    const int64_t nchunks = (int64_t)tile0.size();
     const int first_slot = plan->num_slots;
     it.merge_idx = nchunks > 1 ? (int32_t)plan->merges.size() : -1;
-    for (int64_t k = k0; k <= k1; ++k) {
-      const int64_t c0 = C > 0 ? k * C : 0;
-      const int64_t c1 = C > 0 ? std::min(n[i], (k + 1) * C) : n[i];
-      it.chunk_tok0 = (int32_t)c0;
-      it.tok_begin = (int32_t)std::max(c0, w[i]);
-      it.tok_end = (int32_t)c1;
+    for (int64_t k = 0; k < nchunks; ++k) {
+      it.chunk_tok0 = (int32_t)tile0[k];
+      it.tok_begin = (int32_t)bounds[k];
+      it.tok_end = (int32_t)bounds[k + 1];
       it.out_slot = nchunks > 1 ? plan->num_slots++ : -1;
       items.push_back(it);
     }

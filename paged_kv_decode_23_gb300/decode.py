@@ -170,9 +170,10 @@ class BatchDecodePagedKV:
             q_scale: Optional[float] = None, k_scale: Optional[float] = None,
             v_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, return_lse: bool = False, stream=None,
-            timing_events=None):
+            timing_events=None, enable_pdl: Optional[bool] = None):
         """Decode attention for the planned batch on one layer's pool: returns ``o`` or
-        ``(o, lse)`` (lse: float32 natural log, ``[batch, num_qo_heads]``)."""
+        ``(o, lse)`` (lse: float32 natural log, ``[batch, num_qo_heads]``).  ``enable_pdl``
+        switches programmatic dependent launch for this and later runs (on by default)."""
         a = self._plan_args
         if a is None:
             raise RuntimeError("plan() must be called before run()")
@@ -191,6 +192,8 @@ class BatchDecodePagedKV:
         if lse is not None and (tuple(lse.shape) != exp_q[:2] or lse.dtype != torch.float32):
             raise ValueError("lse must be float32 [batch, num_qo_heads]")
         st = (ctypes.c_int64 * 3)(*strides)
+        if enable_pdl is not None:
+            L.check(L.lib().pkd_set_pdl(self._h, int(bool(enable_pdl))))
         ev0, ev1 = timing_events if timing_events is not None else (None, None)
         L.check(L.lib().pkd_run_timed(
             self._h, q.data_ptr(), k_ptr, v_ptr, num_pages, st,

@@ -166,6 +166,22 @@ def test_run_to_run_determinism(tc):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_pdl_on_and_off_agree():
+    """Programmatic dependent launch changes only when the kernel is scheduled, not results."""
+    w, q, pool = _case([900, 40, 2500], 8, 2, 128, 16, "NHD", "bf16", seed=12)
+    dec = gpu_decoder(w)
+    dev = torch.device("cuda")
+    qd, pd = q.to(dev), pool.to(dev)
+    outs = []
+    for pdl in (False, True, True, False):
+        o, lse = dec.run(qd, pd, return_lse=True, enable_pdl=pdl)
+        outs.append((o.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert dec.check_status() == 0
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
 def test_plan_reused_across_layers():
     w, q, pool = _case([300, 45, 1000], 8, 2, 128, 16, "NHD", "f16", seed=11)
     dec = gpu_decoder(w)
