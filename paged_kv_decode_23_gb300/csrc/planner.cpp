@@ -25,7 +25,7 @@ namespace {
 constexpr int kErrInvalid = -1;
 constexpr int kErrUnsupported = -5;
 constexpr int kCtasPerSm = 2;        // every decode kernel is sized for two resident CTAs
-constexpr int kWavesTarget = 2;      // the heuristic aims for about two waves of CTAs
+constexpr int kWavesTarget = 1;      // heuristic: about one wave of CTAs (measured best on GB300)
 constexpr int64_t kMinChunk = 256;   // never split below this many tokens
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
