@@ -408,6 +408,21 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   // tokens (within the warp's 16-token slice) of this lane's two S^T rows
   const int tok_a = KV_FP8 ? perm_tok(g_row) : g_row;
   const int tok_b = KV_FP8 ? perm_tok(g_row + 8) : g_row + 8;
+  // e4m3 path: this lane's byte offsets inside a stage tile, with the 128-byte swizzle of the
+  // row already folded in (a chunk index is then applied with one XOR).  K: rows tok_a, tok_b,
+  // bytes 4tig.. of each 16-byte chunk.  V: rows tig + 4*t4, bytes 8*(g_row&1).. of chunk
+  // (g_row>>1) of each 64-byte group (bit 6 flips for odd groups).
+  uint32_t koff_a = 0, koff_b = 0, voff[4] = {0, 0, 0, 0};
+  if constexpr (KV_FP8) {
+    const int ra = warp * 16 + tok_a, rb = warp * 16 + tok_b;
+    koff_a = (uint32_t)(ra * 128 + tig * 4) ^ (uint32_t)((ra & 7) << 4);
+    koff_b = (uint32_t)(rb * 128 + tig * 4) ^ (uint32_t)((rb & 7) << 4);
+#pragma unroll
+    for (int t4 = 0; t4 < 4; ++t4) {
+      const int row = warp * 16 + tig + 4 * t4;
+      voff[t4] = (uint32_t)(row * 128 + ((((g_row >> 1) ^ (row & 7))) << 4) + (g_row & 1) * 8);
+    }
+  }
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
@@ -419,8 +434,8 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
     const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
     const int vlo = max(0, b.it.tok_begin - t_w);
     const int vhi = min(16, b.it.tok_end - t_w);
-    const uint32_t ktile = smem + s * G::STAGE_BYTES;
-    const uint32_t vtile = ktile + G::TILE_BYTES;
+    const uint32_t ktile = stage_after_wait(smem + s * G::STAGE_BYTES);
+    uint32_t vtile = ktile + G::TILE_BYTES;
     const int r0 = warp * 16;  // first tile row of my slice
     bool wrote_stage = false;
     if (vhi > vlo) {
@@ -438,28 +453,24 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
           }
           wrote_stage = true;
           __syncwarp();
+          vtile = stage_after_wait(vtile);  // V reads come after the zeroing stores
         }
       }
-      // ---- S^T = K * Q^T : rows = 16 tokens, cols = 8 qo heads
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K * Q^T : rows = 16 tokens, cols = 8 qo heads.  Even and odd k steps go to
+      // two accumulators, halving the chain of dependent MMAs.
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV_FP8) {
         // rows tok_a / tok_b; k slots as in load_q_frags<PERM>: four consecutive e4m3 bytes
-        const int ra = r0 + tok_a, rbw = r0 + tok_b;
-        const uint32_t base_a = ktile + ra * 128 + tig * 4, base_b = ktile + rbw * 128 + tig * 4;
+        const uint32_t ka = ktile + koff_a, kb = ktile + koff_b;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t blk = (kk >> 3) * TS * 128;  // 128-byte column block of the chunk
-          uint32_t wa, wb;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa)
-                       : "r"(base_a + blk + (((kk & 7) ^ (ra & 7)) << 4)));
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb)
-                       : "r"(base_b + blk + (((kk & 7) ^ (rbw & 7)) << 4)));
+          const uint32_t wa = lds_u32((ka ^ ((kk & 7) << 4)) + blk);
+          const uint32_t wb = lds_u32((kb ^ ((kk & 7) << 4)) + blk);
           uint32_t a[4];
-          a[0] = e4m3x2_to_half2(wa & 0xffff);
-          a[2] = e4m3x2_to_half2(wa >> 16);
-          a[1] = e4m3x2_to_half2(wb & 0xffff);
-          a[3] = e4m3x2_to_half2(wb >> 16);
-          mma_16816<T>(c, a, qb[kk][0], qb[kk][1]);
+          e4m3x4_to_half2x2(wa, a[0], a[2]);
+          e4m3x4_to_half2x2(wb, a[1], a[3]);
+          mma_16816<T>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
         }
       } else {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -468,9 +479,11 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t a[4];
           ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
-          mma_16816<T>(c, a, qb[kk][0], qb[kk][1]);
+          mma_16816<T>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] += c2[e];
       // ---- online softmax over the 16 tokens, per qo-head column
       float sc[4];
 #pragma unroll
@@ -509,32 +522,34 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
       const uint32_t b1 = movmatrix_trans(pack2<T>(sc[2], sc[3]));
       // ---- O^T += V^T * P^T : rows = head_dim (16 per block), cols = 8 qo heads
       if constexpr (KV_FP8) {
+        uint32_t va[4], vb[4];  // even / odd 64-byte groups
+#pragma unroll
+        for (int t4 = 0; t4 < 4; ++t4) {
+          va[t4] = vtile + voff[t4];
+          vb[t4] = va[t4] ^ 64u;
+        }
 #pragma unroll
         for (int q4 = 0; q4 < D / 64; ++q4) {
           // bytes 64*q4 + 8*g_row .. +7 of tokens tig + 4*t4 (zero if not attended)
-          const int c16 = 4 * q4 + (g_row >> 1);  // 16-byte chunk index in the fp8 row
-          uint32_t w[4][2];
+          uint2 w[4];
 #pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            const int tok = tig + 4 * t4;
-            const int row = r0 + tok;
-            const uint32_t addr = vtile + (c16 >> 3) * TS * 128 + row * 128 +
-                                  (((c16 & 7) ^ (row & 7)) << 4) + (g_row & 1) * 8;
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(w[t4][0]), "=r"(w[t4][1]) : "r"(addr));
-            if (tok < vlo || tok >= vhi) w[t4][0] = w[t4][1] = 0u;
+          for (int t4 = 0; t4 < 4; ++t4)
+            w[t4] = lds_v2(((q4 & 1) ? vb[t4] : va[t4]) + (q4 >> 1) * TS * 128);
+          if (partial) {
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {
+              const int tok = tig + 4 * t4;
+              if (tok < vlo || tok >= vhi) w[t4] = make_uint2(0u, 0u);
+            }
           }
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
-            const int wd = jj >> 1;
             const uint32_t sel = (jj & 1) ? 0x7362u : 0x5140u;  // bytes (b, b') of two words
-            const uint32_t x01 = prmt(w[0][wd], w[1][wd], sel);
-            const uint32_t x23 = prmt(w[2][wd], w[3][wd], sel);
+            const uint32_t x01 = prmt(jj >> 1 ? w[0].y : w[0].x, jj >> 1 ? w[1].y : w[1].x, sel);
+            const uint32_t x23 = prmt(jj >> 1 ? w[2].y : w[2].x, jj >> 1 ? w[3].y : w[3].x, sel);
             uint32_t a[4];
-            a[0] = e4m3x2_to_half2(x01 & 0xffff);  // d = c0, tokens tig, tig+4
-            a[1] = e4m3x2_to_half2(x01 >> 16);     // d = c0 + 1
-            a[2] = e4m3x2_to_half2(x23 & 0xffff);  // d = c0, tokens tig+8, tig+12
-            a[3] = e4m3x2_to_half2(x23 >> 16);
+            e4m3x4_to_half2x2(x01, a[0], a[1]);  // d = c0 / c0 + 1, tokens tig, tig+4
+            e4m3x4_to_half2x2(x23, a[2], a[3]);  // d = c0 / c0 + 1, tokens tig+8, tig+12
             mma_16816<T>(acc[4 * q4 + jj], a, b0, b1);
           }
         }
@@ -587,7 +602,9 @@ template <typename TQ, bool KV_FP8, int D>
 struct CcRow {
   static constexpr int EPL = D / 32;
   static constexpr int BYTES = EPL * (KV_FP8 ? 1 : 2);  // bytes a lane reads per row
-  // Loads this lane's slice of row r of a swizzled tile and widens it to fp32.
+  // Loads this lane's slice of row r of a swizzled tile and widens it to fp32.  The loads are
+  // volatile: their values feed plain FMAs, so only this keeps them ahead of the stage's
+  // release.
   template <int TS>
   __device__ __forceinline__ static void load(uint32_t tile, int r, int lane, float (&x)[EPL]) {
     using namespace dev;
@@ -605,9 +622,8 @@ struct CcRow {
         const float2 f0 = unpack2<TQ>(v0), f1 = unpack2<TQ>(v1);
         x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
       } else {
-        uint32_t v[4];
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a));
+        const uint4 v4 = lds_v4(a);
+        const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 f = unpack2<TQ>(v[k]);
@@ -617,13 +633,13 @@ struct CcRow {
     } else {
       if constexpr (BYTES == 4) {
         uint32_t v;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+        v = lds_u32(a);
         const float2 f0 = unpack2<__half>(e4m3x2_to_half2(v & 0xffff));
         const float2 f1 = unpack2<__half>(e4m3x2_to_half2(v >> 16));
         x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
       } else {
-        uint32_t v0, v1;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(a));
+        const uint2 vv2 = lds_v2(a);
+        const uint32_t v0 = vv2.x, v1 = vv2.y;
         const uint32_t vv[2] = {v0, v1};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -675,7 +691,7 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
     const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;
     const int vlo = max(0, b.it.tok_begin - t_w);
     const int vhi = min(16, b.it.tok_end - t_w);
-    const uint32_t ktile = smem + s * G::STAGE_BYTES;
+    const uint32_t ktile = stage_after_wait(smem + s * G::STAGE_BYTES);
     const uint32_t vtile = ktile + G::TILE_BYTES;
 #pragma unroll
     for (int grp = 0; grp < 16 / TW; ++grp) {
