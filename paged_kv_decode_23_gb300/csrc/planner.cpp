@@ -120,11 +120,38 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     C = (int64_t)r.fixed_split_size * ps;
   } else {
     const int sms = r.num_sms > 0 ? r.num_sms : 152;
-    const int64_t slots = (int64_t)sms * kCtasPerSm * kWavesTarget;
-    const int64_t per_cta = (total * r.num_kv_heads * plan->gslices + slots - 1) / slots;
-    int64_t c = std::max<int64_t>(kMinChunk, per_cta);
-    c = (c + ps - 1) / ps * ps;
-    C = longest > c ? c : 0;
+    const int64_t slots = (int64_t)sms * kCtasPerSm;
+    const int64_t ctas_per_item = (int64_t)r.num_kv_heads * plan->gslices;
+    // CTAs launched with chunk size c (equal chunks; an empty request still takes one CTA)
+    auto ctas_with = [&](int64_t c) {
+      int64_t items = 0;
+      for (int i = 0; i < r.batch; ++i) {
+        const int64_t a = n[i] - w[i];
+        items += a > c ? (a + c - 1) / c : 1;
+      }
+      return items * ctas_per_item;
+    };
+    const int64_t c_min = (kMinChunk + ps - 1) / ps * ps;
+    const int64_t c_max = (longest + ps - 1) / ps * ps;
+    if ((int64_t)r.batch * ctas_per_item <= slots) {
+      // The unsplit requests already fit in one wave: split only as far as the grid stays
+      // one wave, i.e. the smallest page-aligned chunk whose CTAs all start at once.  A second,
+      // partial wave of chunks measured slower than no split at all on GB300.
+      int64_t lo = c_min, hi = std::max(c_min, c_max);
+      while (lo < hi) {
+        const int64_t mid = (lo / ps + (hi / ps - lo / ps) / 2) * ps;
+        if (ctas_with(mid) <= slots) hi = mid; else lo = mid + ps;
+      }
+      C = longest > lo ? lo : 0;
+    } else {
+      // More requests than one wave: chunks of about the average load of a CTA slot over
+      // kWavesTarget waves, so the longest requests stop bounding the tail.
+      const int64_t per_cta = (total * ctas_per_item + slots * kWavesTarget - 1) /
+                              (slots * kWavesTarget);
+      int64_t c = std::max<int64_t>(c_min, per_cta);
+      c = (c + ps - 1) / ps * ps;
+      C = longest > c ? c : 0;
+    }
   }
   plan->chunk_tokens = C;
 
