@@ -33,6 +33,8 @@ namespace pkd {
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
+// Largest log2 headroom a running softmax reference may lag behind the scores (p <= 2^8).
+constexpr float kLazyMax = 8.f;
 
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES>
 struct DecodeGeom {
@@ -367,9 +369,13 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
 //     chosen so that lane tig's k slots {2tig, 2tig+1, 2tig+8, 2tig+9} are tokens
 //     tig, tig+4, tig+8, tig+12 (and the eight S^T rows a K load touches fall in eight
 //     different swizzle phases, so those loads are free of bank conflicts);
-//   * head_dim: rows r and r+8 of O^T block mb = 4q + jj hold d = 64q + 8r + 2jj and
-//     64q + 8r + 2jj + 1, so lane r reads bytes 64q + 8r .. 64q + 8r + 7 of each of its four
-//     tokens (one 64-bit load) and builds the V^T fragments with two byte permutes per block.
+//   * head_dim: rows r and r+8 of O^T block mb = 4q + jj hold d = d0(r, q) + 2jj and
+//     d0(r, q) + 2jj + 1, where d0(r, q) = 128(q/2) + 16 vchunk(r, q%2) + 8(r%2) and
+//     vchunk(r, p) = 4((r/2)%2) + r/4 + 2p.  So lane r reads bytes d0 .. d0 + 7 of each of its
+//     four tokens (one 64-bit load) and builds the V^T fragments with two byte permutes per
+//     block.  The chunk order puts the four rows a half-warp reads (tokens tig + 4t4, whose
+//     swizzle phases are 0..3 or 4..7) on eight distinct 16-byte positions of the 128-byte
+//     swizzle pattern, so the V loads are free of bank conflicts too.
 // Every e4m3 value is an fp16 value, so the widening (cvt.f16x2.e4m3x2) is exact.
 __device__ __forceinline__ int perm_tok(int j) {
   return ((j & 7) >> 1) + 4 * (j & 1) + 8 * (j >> 3);
@@ -385,7 +391,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 template <bool KV_FP8>
 __device__ __forceinline__ int acc_dim(int mb, int row) {
   if constexpr (KV_FP8) {
-    return 64 * (mb >> 2) + 8 * (row & 7) + 2 * (mb & 3) + (row >> 3);
+    const int r = row & 7, q = mb >> 2;
+    return 128 * (q >> 1) + 16 * (4 * ((r >> 1) & 1) + (r >> 2) + 2 * (q & 1)) + 8 * (r & 1) +
+           2 * (mb & 3) + (row >> 3);
   } else {
     return mb * 16 + row;
   }
@@ -411,7 +419,7 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   // e4m3 path: this lane's byte offsets inside a stage tile, with the 128-byte swizzle of the
   // row already folded in (a chunk index is then applied with one XOR).  K: rows tok_a, tok_b,
   // bytes 4tig.. of each 16-byte chunk.  V: rows tig + 4*t4, bytes 8*(g_row&1).. of chunk
-  // (g_row>>1) of each 64-byte group (bit 6 flips for odd groups).
+  // vchunk(g_row, q4 % 2) of each 128-byte block (odd q4: chunk ^ 2, i.e. offset bit 5 flips).
   uint32_t koff_a = 0, koff_b = 0, voff[4] = {0, 0, 0, 0};
   if constexpr (KV_FP8) {
     const int ra = warp * 16 + tok_a, rb = warp * 16 + tok_b;
@@ -420,7 +428,8 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
 #pragma unroll
     for (int t4 = 0; t4 < 4; ++t4) {
       const int row = warp * 16 + tig + 4 * t4;
-      voff[t4] = (uint32_t)(row * 128 + ((((g_row >> 1) ^ (row & 7))) << 4) + (g_row & 1) * 8);
+      const int vchunk = 4 * ((g_row >> 1) & 1) + (g_row >> 2);  // vchunk(g_row, 0)
+      voff[t4] = (uint32_t)(row * 128 + ((vchunk ^ (row & 7)) << 4) + (g_row & 1) * 8);
     }
   }
 
@@ -492,29 +501,45 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
         const float sv = score_log2(c[e], scale_qk, cap_log2);
         sc[e] = (t >= vlo && t < vhi) ? sv : kNegInf;
       }
-      float alpha[2];
+      // The reference m2 of a column only moves when one of its scores exceeds it by more
+      // than kLazyMax: until then p = 2^(s - m2) <= 2^kLazyMax, far inside the 16-bit P
+      // operand's range, and o = acc / l and lse = m2 + log2(l) are unchanged by the choice
+      // of m2.  Most tiles thus skip the cross-lane max and the rescale of O.
+      const bool grow = sc[0] > m2[0] + kLazyMax || sc[2] > m2[0] + kLazyMax ||
+                        sc[1] > m2[1] + kLazyMax || sc[3] > m2[1] + kLazyMax;
+      if (__any_sync(~0u, grow)) {
+        float alpha[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float mx = fmaxf(sc[j], sc[j + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 16));
-        const float mnew = fmaxf(m2[j], mx);
-        const float ref = mnew == kNegInf ? 0.f : mnew;
-        alpha[j] = fast_exp2(m2[j] - ref);
-        sc[j] = fast_exp2(sc[j] - ref);
-        sc[j + 2] = fast_exp2(sc[j + 2] - ref);
-        lsum[j] = lsum[j] * alpha[j] + sc[j] + sc[j + 2];
-        m2[j] = mnew;
-      }
-      // rescale O only when some column's running max moved (alpha is exactly 1 otherwise)
-      if (__any_sync(~0u, alpha[0] != 1.f || alpha[1] != 1.f)) {
+        for (int j = 0; j < 2; ++j) {
+          float mx = fmaxf(sc[j], sc[j + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 16));
+          const float mnew = fmaxf(m2[j], mx);
+          const float ref = mnew == kNegInf ? 0.f : mnew;
+          alpha[j] = fast_exp2(m2[j] - ref);
+          sc[j] = fast_exp2(sc[j] - ref);
+          sc[j + 2] = fast_exp2(sc[j + 2] - ref);
+          lsum[j] = lsum[j] * alpha[j] + sc[j] + sc[j + 2];
+          m2[j] = mnew;
+        }
+        // rescale O only when some column's reference moved (alpha is exactly 1 otherwise)
+        if (__any_sync(~0u, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-        for (int mb = 0; mb < D / 16; ++mb) {
-          acc[mb][0] *= alpha[0];
-          acc[mb][1] *= alpha[1];
-          acc[mb][2] *= alpha[0];
-          acc[mb][3] *= alpha[1];
+          for (int mb = 0; mb < D / 16; ++mb) {
+            acc[mb][0] *= alpha[0];
+            acc[mb][1] *= alpha[1];
+            acc[mb][2] *= alpha[0];
+            acc[mb][3] *= alpha[1];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float ref = m2[j] == kNegInf ? 0.f : m2[j];
+          sc[j] = fast_exp2(sc[j] - ref);
+          sc[j + 2] = fast_exp2(sc[j + 2] - ref);
+          lsum[j] += sc[j] + sc[j + 2];
         }
       }
       // ---- P^T as the B operand (k = token, n = qo head): transpose the C fragment
@@ -522,15 +547,15 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
       const uint32_t b1 = movmatrix_trans(pack2<T>(sc[2], sc[3]));
       // ---- O^T += V^T * P^T : rows = head_dim (16 per block), cols = 8 qo heads
       if constexpr (KV_FP8) {
-        uint32_t va[4], vb[4];  // even / odd 64-byte groups
+        uint32_t va[4], vb[4];  // even / odd q4
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
           va[t4] = vtile + voff[t4];
-          vb[t4] = va[t4] ^ 64u;
+          vb[t4] = va[t4] ^ 32u;  // vchunk(g_row, 1) = vchunk(g_row, 0) ^ 2
         }
 #pragma unroll
         for (int q4 = 0; q4 < D / 64; ++q4) {
-          // bytes 64*q4 + 8*g_row .. +7 of tokens tig + 4*t4 (zero if not attended)
+          // bytes d0(g_row, q4) .. +7 of tokens tig + 4*t4 (zero if not attended)
           uint2 w[4];
 #pragma unroll
           for (int t4 = 0; t4 < 4; ++t4)

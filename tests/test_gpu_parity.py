@@ -231,3 +231,25 @@ def test_full_long_hnd_fixed_split():
 def test_full_mix_e4m3_cap_window():
     w = W.workload("mix")
     _full("mix", _sample(w, 6))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("order", ["rising", "falling"])
+@pytest.mark.parametrize("tc", [True, False])
+def test_scores_drifting_along_the_sequence(kv, order, tc):
+    """K rows are constant along head_dim and grow (or shrink) with the token index, so the
+    logits sweep ~30 natural-log units along each request: the online softmax's reference
+    max has to move many times (rising) or never after the first tile (falling)."""
+    lens = [1500, 700, 33, 2100]
+    w, q, pool = _case(lens, 16, 2, 128, 16, "NHD", "bf16", kv=kv, seed=13)
+    q = torch.ones_like(q)
+    vals = pool.float()
+    for i, n in enumerate(lens):
+        t = np.arange(n)
+        ramp = (t if order == "rising" else n - 1 - t) * (2.6 / 2100)
+        pages = w.indices[w.indptr[i] + t // w.page_size]
+        vals[torch.from_numpy(pages).long(), 0, torch.from_numpy(t % w.page_size).long()] = (
+            torch.from_numpy(ramp).float()[:, None, None] / (w.k_scale if kv == "e4m3" else 1.0))
+    pool = vals.to(pool.dtype)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
+                 f"{order} {kv} tc={tc}")
