@@ -178,7 +178,9 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
 /*
  * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no
  * kernel since the last plan or check reported a problem, else a bit set: 1 = a pipeline
- * wait timed out (the kernel gave up and left its outputs incomplete).
+ * wait timed out (the kernel gave up and left its outputs incomplete).  When it is nonzero,
+ * the split-merge chunk counters in the int workspace are zeroed with it, so later runs of
+ * the same plan start clean.
  */
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
 

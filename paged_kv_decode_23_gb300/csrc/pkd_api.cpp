@@ -362,10 +362,13 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   cudaError_t e = set_smem_limit_once(k, h->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
-  // Upload the work list: wait for the previous upload to leave the pinned buffer first.
+  // Upload the int workspace image -- zeroed status word and merge counters, then the work
+  // list -- with one copy; wait for the previous upload to leave the pinned buffer first.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t items_off = items_offset(plan, num_kv_heads);
   const size_t items_b = plan.items.size() * sizeof(WorkItem);
   const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
-  const size_t bytes = items_b + merges_b;
+  const size_t bytes = items_off + items_b + merges_b;
   if (h->staging_pending) {
     e = cudaEventSynchronize(h->staging_done);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
@@ -380,20 +383,15 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
     h->staging_bytes = cap;
   }
-  if (items_b) std::memcpy(h->staging, plan.items.data(), items_b);
-  if (merges_b) std::memcpy(static_cast<char*>(h->staging) + items_b, plan.merges.data(), merges_b);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t items_off = items_offset(plan, num_kv_heads);
-  e = cudaMemsetAsync(h->int_ws, 0, items_off, s);  // status word and merge counters
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-  if (bytes) {
-    e = cudaMemcpyAsync(static_cast<char*>(h->int_ws) + items_off, h->staging, bytes,
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
-    e = cudaEventRecord(h->staging_done, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    h->staging_pending = true;
-  }
+  char* img = static_cast<char*>(h->staging);
+  std::memset(img, 0, items_off);
+  if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
+  if (merges_b) std::memcpy(img + items_off + items_b, plan.merges.data(), merges_b);
+  e = cudaMemcpyAsync(h->int_ws, img, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  e = cudaEventRecord(h->staging_done, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  h->staging_pending = true;
 
   h->plan = std::move(plan);
   h->batch = batch;
@@ -534,7 +532,10 @@ int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
   *status = v;
   if (v) {
-    e = cudaMemsetAsync(h->int_ws, 0, sizeof v, s);
+    // A kernel that gave up may have left a split request's chunk counter part-way; zero the
+    // counters with the status word so the next run of this plan merges at the right count.
+    const size_t clear = h->planned ? items_offset(h->plan, h->num_kv_heads) : sizeof v;
+    e = cudaMemsetAsync(h->int_ws, 0, clear, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
   }
