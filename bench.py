@@ -15,6 +15,7 @@ same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -31,6 +32,34 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: µs/call and KV-read GB/s as % of GB300 HBM peak"
 ELT = {"f16": 2, "bf16": 2, "e4m3": 1}
 L2_BYTES = 129 * 1024 * 1024
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode-kernel launch, from
+# the ncu captures summarised in profiles/, and the digest of the kernel sources they were
+# taken on: once the sources differ, the figure no longer describes the kernel and the line
+# reports null.
+MEASURED_TRAFFIC = {
+    "sources_sha256": "629d2cfbb559849d9457ce0f5e2ccbc55d73f4ef43b1bec2ebca02b12e258bb1",
+    "uniform": 618.92e6,  # profiles/decode_paged_kernel_uniform.md (2 launches averaged)
+    "mix": 418.19e6,      # profiles/decode_paged_kernel_mix.md
+}
+
+
+def kernel_sources_digest() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_decode_23_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(name: str):
+    if MEASURED_TRAFFIC.get("sources_sha256") != kernel_sources_digest():
+        return None
+    return MEASURED_TRAFFIC.get(name)
 
 
 def algorithmic_bytes(w) -> int:
@@ -390,7 +419,8 @@ def gpu_arm(args, w, rank, world):
         "pct_of_hbm_peak": 100.0 * (value / world) / peak,
         "peak_kind": peak_kind,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": args.traffic,
+                     "frac": achieved / peak,
+                     "traffic": args.traffic if args.traffic is not None else measured_traffic(w.name),
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": {"value": world * bytes_step / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
