@@ -119,7 +119,8 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
  *   q_scale, k_scale, v_scale: calibration scales (1.0 when unused).
  *   o (device) [batch, num_qo_heads, head_dim] o_dtype; lse (device) [batch, num_qo_heads]
  *     float32 natural log, or NULL to skip it.
- * Launches one decode kernel, plus one merge kernel when any request was split.
+ * Launches one decode kernel; the CTA that finishes a split request's last chunk merges the
+ * request's partial results inside that launch.
  */
 int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
             int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
@@ -141,6 +142,34 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
  * the launch gap is hidden.  Off: ordinary stream order.
  */
 int pkd_set_pdl(pkd_handle* h, int enable);
+
+/*
+ * CUDA-graph mode: the page's BatchDecodeWithPagedKVCacheWrapper(use_cuda_graph=True,
+ * paged_kv_indptr_buffer, paged_kv_indices_buffer, paged_kv_last_page_len_buffer) and
+ * CUDAGraphBatchDecodeWithPagedKVCacheWrapper(workspace, indptr_buffer, indices_buffer,
+ * last_page_len_buffer).  After this call (it cannot be undone on the handle):
+ *   - pkd_plan copies the page table into the caller's device buffers (indptr_buf: >=
+ *     max_batch + 1 int32, indices_buf: >= max_pages int32, last_page_len_buf: >= max_batch
+ *     int32) and the kernel reads page ids from indices_buf;
+ *   - the batch size is fixed by the first plan (a shorter batch is padded with zero-length
+ *     requests: repeat the last indptr value; their o rows are 0 and lse -inf);
+ *   - the work list holds at most max_items chunks (<= 0: max_batch + 2 x the SM count); the
+ *     heuristic split grows its chunks to fit, a fixed_split_size that does not fit fails with
+ *     PKD_ERR_WORKSPACE_TOO_SMALL; the workspaces must hold pkd_graph_workspace_bytes;
+ *   - pkd_run launches the same grid with the same kernel arguments for every plan (CTAs past
+ *     the plan's chunk count exit at once), so a run captured in a CUDA graph replays
+ *     correctly after later plans.  pkd_plan itself is not capturable, as the page notes for
+ *     plan().
+ * The buffers are the caller's and must outlive every run.
+ */
+int pkd_enable_cuda_graph(pkd_handle* h, int32_t* indptr_buf, int32_t* indices_buf,
+                          int32_t* last_page_len_buf, int max_batch, int64_t max_pages,
+                          int max_items);
+
+/* Workspace bytes CUDA-graph mode needs for a work list of max_items chunks. */
+int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads, int head_dim,
+                              int use_tensor_cores, size_t* float_ws_bytes,
+                              size_t* int_ws_bytes);
 
 /* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
 int pkd_destroy(pkd_handle* h);
@@ -167,13 +196,15 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
  * in launch order, and up to max_merges merge entries of 4 int32 {request, first slot,
  * chunk count, 0}.  n_items / n_merges / n_slots receive the full counts.  kernel_out
  * receives the chosen PKD_KERNEL_* and tile_tokens_out the tokens per pipeline stage.
+ * work_capacity > 0 bounds the work list the way CUDA-graph mode does (pkd_enable_cuda_graph's
+ * max_items); 0 leaves it unbounded.
  */
 int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
                   int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
                   int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
                   int32_t* merges_out, int max_merges, int* n_items, int* n_merges,
-                  int* n_slots, int* kernel_out, int* tile_tokens_out);
+                  int* n_slots, int* kernel_out, int* tile_tokens_out, int work_capacity);
 
 /*
  * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no

@@ -50,9 +50,12 @@ SIGNATURES = {
                                _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _c_int, _i32p,
                                _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
-                               ctypes.POINTER(_c_int)]),
+                               ctypes.POINTER(_c_int), _c_int]),
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkd_set_pdl": (_c_int, [_vp, _c_int]),
+    "pkd_enable_cuda_graph": (_c_int, [_vp, _vp, _vp, _vp, _c_int, ctypes.c_int64, _c_int]),
+    "pkd_graph_workspace_bytes": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                           ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
     "pkd_decode_noalloc": (_c_int, [_i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
                                     _c_int, _c_int, _c_float, _c_float, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,

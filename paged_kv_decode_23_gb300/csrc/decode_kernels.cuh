@@ -828,6 +828,11 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
   // may start its own launch as soon as every CTA of this one is running.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // CUDA-graph mode: the grid is cut for a fixed work-list capacity; CTAs past this plan's
+  // items have nothing to do (the whole CTA leaves before touching shared memory).
+  if (p.item_count != nullptr &&
+      (int)(blockIdx.x / (p.num_kv_heads * p.gslices)) >= *p.item_count)
+    return;
   const BlockCoords b = block_coords<TS, HEADS>(p);
   if (threadIdx.x == 0) {
 #pragma unroll

@@ -111,6 +111,21 @@ struct pkd_handle {
   cudaEvent_t staging_done = nullptr;
   bool staging_pending = false;
   bool pdl = true;  // launch the decode kernel as a programmatic dependent of its predecessor
+
+  // The workspace layout the current plan was uploaded in (its own counts, or capacities).
+  WsLayout ws_layout{};
+
+  // CUDA-graph mode (pkd_enable_cuda_graph): the page table lives in the caller's fixed
+  // buffers, the workspaces are cut for fixed capacities, and every run launches the same
+  // grid, so a captured run stays valid across later plans of the same batch size.
+  bool graph = false;
+  int32_t* g_indptr = nullptr;
+  int32_t* g_indices = nullptr;
+  int32_t* g_lpl = nullptr;
+  int g_max_batch = 0;
+  int64_t g_max_pages = 0;
+  int g_max_items = 0;
+  int g_batch = -1;  // fixed by the first plan in graph mode
 };
 
 namespace {
@@ -269,12 +284,13 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
                   int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
                   int32_t* merges_out, int max_merges, int* n_items, int* n_merges, int* n_slots,
-                  int* kernel_out, int* tile_tokens_out) {
+                  int* kernel_out, int* tile_tokens_out, int work_capacity) {
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
                              disable_split_kv, kv_dtype, use_tensor_cores, num_sms);
   if (rc) return rc;
+  r.max_items = work_capacity > 0 ? work_capacity : 0;
   Plan plan;
   const char* err = "";
   rc = build_plan(r, &plan, &err);
@@ -334,11 +350,23 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (!std::isfinite(logits_soft_cap))
     return fail(PKD_ERR_INVALID_ARG, "logits_soft_cap must be finite");
 
+  if (h->graph) {
+    if (batch < 1 || batch > h->g_max_batch)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: batch must lie in [1, max_batch]");
+    if (h->g_batch >= 0 && batch != h->g_batch)
+      return fail(PKD_ERR_INVALID_ARG,
+                  "CUDA-graph mode: the batch size is fixed by the first plan (pad the batch "
+                  "with zero-length requests instead)");
+    if ((int64_t)indptr_host[batch] > h->g_max_pages)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: indptr[batch] exceeds max_pages");
+  }
+
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
                              disable_split_kv, kv_dtype, use_tensor_cores, h->num_sms);
   if (rc) return rc;
+  if (h->graph) r.max_items = h->g_max_items;
   Plan plan;
   const char* err = "";
   rc = build_plan(r, &plan, &err);
@@ -350,8 +378,10 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (!plan.merges.empty() && !mk)
     return fail(PKD_ERR_UNSUPPORTED, "no merge kernel built for this dtype / head_dim");
 
-  const size_t need_f = float_ws_bytes_of(plan, num_qo_heads, head_dim);
-  const size_t need_i = int_ws_bytes_of(plan, num_kv_heads);
+  const WsLayout lay = h->graph ? capacity_layout(h->g_max_items, num_kv_heads, plan.gslices)
+                                : layout_of(plan, num_kv_heads);
+  const size_t need_f = float_ws_bytes_of(lay, num_qo_heads, head_dim);
+  const size_t need_i = int_ws_bytes_of(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
     char buf[200];
     std::snprintf(buf, sizeof buf, "workspace too small: need %zu float / %zu int bytes", need_f,
@@ -362,13 +392,18 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   cudaError_t e = set_smem_limit_once(k, h->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
-  // Upload the int workspace image -- zeroed status word and merge counters, then the work
-  // list -- with one copy; wait for the previous upload to leave the pinned buffer first.
+  // Upload the int workspace image -- zeroed status block and merge counters, then the work
+  // list and the merge list at the layout's offsets -- with one copy (graph mode adds the page
+  // table's copies into the fixed buffers); wait for the previous upload to leave the pinned
+  // buffer first.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t items_off = items_offset(plan, num_kv_heads);
+  const size_t items_off = items_offset(lay);
+  const size_t merges_off = merges_offset(lay);
   const size_t items_b = plan.items.size() * sizeof(WorkItem);
   const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
-  const size_t bytes = items_off + items_b + merges_b;
+  const size_t img_bytes = merges_off + merges_b;
+  const size_t table_b = h->graph ? (size_t)(2 * batch + 1) * sizeof(int32_t) : 0;
+  const size_t bytes = img_bytes + table_b;
   if (h->staging_pending) {
     e = cudaEventSynchronize(h->staging_done);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
@@ -384,11 +419,30 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     h->staging_bytes = cap;
   }
   char* img = static_cast<char*>(h->staging);
-  std::memset(img, 0, items_off);
+  std::memset(img, 0, merges_off);
+  if (h->graph) {
+    const int32_t count = (int32_t)plan.items.size();
+    std::memcpy(img + kItemCountOffset, &count, sizeof count);
+  }
   if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
-  if (merges_b) std::memcpy(img + items_off + items_b, plan.merges.data(), merges_b);
-  e = cudaMemcpyAsync(h->int_ws, img, bytes, cudaMemcpyHostToDevice, s);
+  if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
+  e = cudaMemcpyAsync(h->int_ws, img, img_bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  if (h->graph) {
+    int32_t* tbl = reinterpret_cast<int32_t*>(img + img_bytes);
+    std::memcpy(tbl, indptr_host, (size_t)(batch + 1) * sizeof(int32_t));
+    std::memcpy(tbl + batch + 1, last_page_len_host, (size_t)batch * sizeof(int32_t));
+    e = cudaMemcpyAsync(h->g_indptr, tbl, (size_t)(batch + 1) * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->g_lpl, tbl + batch + 1, (size_t)batch * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, s);
+    const int64_t n_ids = indptr_host[batch];
+    if (e == cudaSuccess && n_ids > 0 && indices_dev != h->g_indices)
+      e = cudaMemcpyAsync(h->g_indices, indices_dev, (size_t)n_ids * sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the page table into the graph buffers");
+  }
   e = cudaEventRecord(h->staging_done, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   h->staging_pending = true;
@@ -404,7 +458,9 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   h->o_dtype = o_dtype;
   h->sm_scale = std::isnan(sm_scale) ? 1.0f / std::sqrt((float)head_dim) : sm_scale;
   h->cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
-  h->indices = indices_dev;
+  h->indices = h->graph ? h->g_indices : indices_dev;
+  h->ws_layout = lay;
+  if (h->graph) h->g_batch = batch;
   h->kernel = k;
   h->merge = mk;
   h->planned = true;
@@ -418,7 +474,7 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
   if (!h->planned) return fail(PKD_ERR_NOT_PLANNED, "pkd_run called before a successful pkd_plan");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (h->plan.items.empty()) return PKD_OK;  // empty batch
+  if (h->plan.items.empty() && !h->graph) return PKD_OK;  // empty batch
   if (!q || !k_base || !v_base || !o || !kv_strides)
     return fail(PKD_ERR_INVALID_ARG, "null q / k_base / v_base / o / kv_strides");
   if (num_pages <= 0 || num_pages > (int64_t(1) << 31))
@@ -453,11 +509,12 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
 
   char* iws = static_cast<char*>(h->int_ws);
   char* fws = static_cast<char*>(h->float_ws);
-  const size_t part_o_bytes =
-      ((size_t)h->plan.num_slots * h->num_qo_heads * h->head_dim * sizeof(float) + 255) / 256 * 256;
-  prm.items = reinterpret_cast<const WorkItem*>(iws + items_offset(h->plan, h->num_kv_heads));
-  prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(h->plan, h->num_kv_heads));
+  const WsLayout& lay = h->ws_layout;
+  const size_t part_o_bytes = part_lse_offset(lay, h->num_qo_heads, h->head_dim);
+  prm.items = reinterpret_cast<const WorkItem*>(iws + items_offset(lay));
+  prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(lay));
   prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
+  prm.item_count = h->graph ? reinterpret_cast<const int32_t*>(iws + kItemCountOffset) : nullptr;
   prm.fuse_merge = 1;
   prm.indices = h->indices;
   prm.q = q;
@@ -483,7 +540,8 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   }
   prm.v_scale = v_scale;
 
-  const int64_t grid = (int64_t)h->plan.items.size() * h->num_kv_heads * h->plan.gslices;
+  const int64_t n_items = h->graph ? (int64_t)h->g_max_items : (int64_t)h->plan.items.size();
+  const int64_t grid = n_items * h->num_kv_heads * h->plan.gslices;
   void* args[] = {&prm};
   cudaError_t e;
   if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
@@ -523,6 +581,50 @@ int pkd_set_pdl(pkd_handle* h, int enable) {
   return PKD_OK;
 }
 
+int pkd_enable_cuda_graph(pkd_handle* h, int32_t* indptr_buf, int32_t* indices_buf,
+                          int32_t* last_page_len_buf, int max_batch, int64_t max_pages,
+                          int max_items) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (!indptr_buf || !indices_buf || !last_page_len_buf)
+    return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode needs the indptr, indices and "
+                                     "last_page_len buffers");
+  if (!aligned(indptr_buf, 4) || !aligned(indices_buf, 4) || !aligned(last_page_len_buf, 4))
+    return fail(PKD_ERR_INVALID_ARG, "graph buffers must be 4-byte aligned");
+  if (max_batch < 1 || max_pages < 0)
+    return fail(PKD_ERR_INVALID_ARG, "max_batch must be >= 1 and max_pages >= 0");
+  if (max_items <= 0) max_items = max_batch + 2 * h->num_sms;
+  if (max_items < max_batch)
+    return fail(PKD_ERR_INVALID_ARG, "max_items must be >= max_batch");
+  h->graph = true;
+  h->g_indptr = indptr_buf;
+  h->g_indices = indices_buf;
+  h->g_lpl = last_page_len_buf;
+  h->g_max_batch = max_batch;
+  h->g_max_pages = max_pages;
+  h->g_max_items = max_items;
+  h->g_batch = -1;
+  h->planned = false;
+  return PKD_OK;
+}
+
+int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads, int head_dim,
+                              int use_tensor_cores, size_t* float_ws_bytes,
+                              size_t* int_ws_bytes) {
+  if (max_items < 1 || num_qo_heads <= 0 || num_kv_heads <= 0 ||
+      num_qo_heads % num_kv_heads != 0 || head_dim <= 0)
+    return fail(PKD_ERR_INVALID_ARG, "bad capacity or head configuration");
+  const int G = num_qo_heads / num_kv_heads;
+  int hpc = 8;  // heads per CTA: 8 on tensor cores, else the power of two >= G, at most 8
+  if (use_tensor_cores == 0) {
+    hpc = 2;
+    while (hpc < G && hpc < 8) hpc <<= 1;
+  }
+  const WsLayout lay = capacity_layout(max_items, num_kv_heads, (G + hpc - 1) / hpc);
+  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(lay, num_qo_heads, head_dim);
+  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(lay);
+  return PKD_OK;
+}
+
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
   if (!h || !status) return fail(PKD_ERR_INVALID_ARG, "null handle or status");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -534,8 +636,11 @@ int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
   if (v) {
     // A kernel that gave up may have left a split request's chunk counter part-way; zero the
     // counters with the status word so the next run of this plan merges at the right count.
-    const size_t clear = h->planned ? items_offset(h->plan, h->num_kv_heads) : sizeof v;
-    e = cudaMemsetAsync(h->int_ws, 0, clear, s);
+    e = cudaMemsetAsync(h->int_ws, 0, sizeof v, s);
+    const size_t counters_end = h->planned ? items_offset(h->ws_layout) : kStatusBytes;
+    if (e == cudaSuccess && counters_end > kStatusBytes)
+      e = cudaMemsetAsync(static_cast<char*>(h->int_ws) + kStatusBytes, 0,
+                          counters_end - kStatusBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
   }

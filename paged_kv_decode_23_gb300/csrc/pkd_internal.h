@@ -53,6 +53,8 @@ struct DecodeParams {
   uint32_t* status;     // device status word (bit 0: a pipeline wait timed out)
   const MergeEntry* merges;  // with fuse_merge: the split requests
   uint32_t* counters;   // with fuse_merge: finished chunks per (merge entry, kv head, slice)
+  const int32_t* item_count;  // CUDA-graph mode: the plan's work-item count, read on the device
+                              // (the grid is cut for a fixed capacity); null: the grid is exact
   int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
   int num_qo_heads;
   int num_kv_heads;
@@ -119,6 +121,7 @@ struct PlanRequest {
   int kv_dtype;
   int use_tensor_cores;  // -1 auto, 0, 1
   int num_sms;
+  int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode)
 };
 
 struct Plan {
@@ -137,24 +140,54 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err);
 
 // Byte offsets inside the int workspace.
 constexpr size_t kStatusBytes = 256;
-// int workspace: [status word | merge counters | work items | merge entries]; plan() zeroes
-// everything before the work items.
-inline size_t merge_counter_count(const Plan& p, int num_kv_heads) {
-  return p.merges.size() * (size_t)num_kv_heads * p.gslices;
+constexpr size_t kItemCountOffset = 64;  // int32 inside the status block (CUDA-graph mode)
+
+// Capacities the workspaces are cut for: a plan's own counts, or in CUDA-graph mode fixed
+// maxima, so that every address a captured launch holds stays valid for later plans.
+struct WsLayout {
+  size_t counters;  // fused-merge counters
+  size_t items;
+  size_t merges;
+  size_t slots;     // split partials
+};
+inline WsLayout layout_of(const Plan& p, int num_kv_heads) {
+  return {p.merges.size() * (size_t)num_kv_heads * p.gslices, p.items.size(), p.merges.size(),
+          (size_t)p.num_slots};
+}
+// A work list of at most max_items items has at most max_items / 2 split requests (each has
+// two or more chunks) and at most max_items partial slots.
+inline WsLayout capacity_layout(size_t max_items, int num_kv_heads, int gslices) {
+  const size_t merges = max_items / 2;
+  return {merges * (size_t)num_kv_heads * gslices, max_items, merges, max_items};
+}
+// int workspace: [status block | merge counters | work items | merge entries]; plan() writes
+// everything up to the end of the merge entries in one upload (counters zeroed).
+inline size_t items_offset(const WsLayout& l) {
+  return kStatusBytes + (l.counters * 4 + 255) / 256 * 256;
+}
+inline size_t merges_offset(const WsLayout& l) { return items_offset(l) + l.items * sizeof(WorkItem); }
+inline size_t int_ws_bytes_of(const WsLayout& l) {
+  return merges_offset(l) + l.merges * sizeof(MergeEntry) + 256;
+}
+// float workspace: [part_o (slots x Hq x D) | part_lse (slots x Hq)], each 256-byte aligned
+inline size_t part_lse_offset(const WsLayout& l, int num_qo_heads, int head_dim) {
+  return (l.slots * num_qo_heads * head_dim * sizeof(float) + 255) / 256 * 256;
+}
+inline size_t float_ws_bytes_of(const WsLayout& l, int num_qo_heads, int head_dim) {
+  return part_lse_offset(l, num_qo_heads, head_dim) +
+         (l.slots * num_qo_heads * sizeof(float) + 255) / 256 * 256;
 }
 inline size_t items_offset(const Plan& p, int num_kv_heads) {
-  return kStatusBytes + (merge_counter_count(p, num_kv_heads) * 4 + 255) / 256 * 256;
+  return items_offset(layout_of(p, num_kv_heads));
 }
 inline size_t merges_offset(const Plan& p, int num_kv_heads) {
-  return items_offset(p, num_kv_heads) + p.items.size() * sizeof(WorkItem);
+  return merges_offset(layout_of(p, num_kv_heads));
 }
 inline size_t int_ws_bytes_of(const Plan& p, int num_kv_heads) {
-  return merges_offset(p, num_kv_heads) + p.merges.size() * sizeof(MergeEntry) + 256;
+  return int_ws_bytes_of(layout_of(p, num_kv_heads));
 }
 inline size_t float_ws_bytes_of(const Plan& p, int num_qo_heads, int head_dim) {
-  size_t o = (size_t)p.num_slots * num_qo_heads * head_dim * sizeof(float);
-  size_t l = (size_t)p.num_slots * num_qo_heads * sizeof(float);
-  return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
+  return float_ws_bytes_of(layout_of(p, 1), num_qo_heads, head_dim);
 }
 
 }  // namespace pkd

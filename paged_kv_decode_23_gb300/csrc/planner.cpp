@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kErrInvalid = -1;
 constexpr int kErrUnsupported = -5;
+constexpr int kErrWorkspace = -3;
 constexpr int kCtasPerSm = 2;        // every decode kernel is sized for two resident CTAs
 constexpr int kWavesTarget = 1;      // heuristic: about one wave of CTAs (measured best on GB300)
 constexpr int64_t kMinChunk = 256;   // never split below this many tokens
@@ -114,6 +115,23 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
 
   // chunk size in tokens (a multiple of the page size); 0 = one chunk per request
   int64_t C = 0;
+  const int64_t ctas_per_item = (int64_t)r.num_kv_heads * plan->gslices;
+  // work items with heuristic (equal) chunks of c tokens; an empty request is one item
+  auto items_with = [&](int64_t c) {
+    int64_t items = 0;
+    for (int i = 0; i < r.batch; ++i) {
+      const int64_t a = n[i] - w[i];
+      items += a > c ? (a + c - 1) / c : 1;
+    }
+    return items;
+  };
+  auto ctas_with = [&](int64_t c) { return items_with(c) * ctas_per_item; };
+  const int64_t c_min = (kMinChunk + ps - 1) / ps * ps;
+  const int64_t c_max = (longest + ps - 1) / ps * ps;
+  if (r.max_items > 0 && r.batch > r.max_items) {
+    *err = "the batch has more requests than the work-list capacity";
+    return kErrInvalid;
+  }
   if (r.disable_split_kv) {
     C = 0;
   } else if (r.fixed_split_size > 0) {
@@ -121,18 +139,6 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   } else {
     const int sms = r.num_sms > 0 ? r.num_sms : 152;
     const int64_t slots = (int64_t)sms * kCtasPerSm;
-    const int64_t ctas_per_item = (int64_t)r.num_kv_heads * plan->gslices;
-    // CTAs launched with chunk size c (equal chunks; an empty request still takes one CTA)
-    auto ctas_with = [&](int64_t c) {
-      int64_t items = 0;
-      for (int i = 0; i < r.batch; ++i) {
-        const int64_t a = n[i] - w[i];
-        items += a > c ? (a + c - 1) / c : 1;
-      }
-      return items * ctas_per_item;
-    };
-    const int64_t c_min = (kMinChunk + ps - 1) / ps * ps;
-    const int64_t c_max = (longest + ps - 1) / ps * ps;
     if ((int64_t)r.batch * ctas_per_item <= slots) {
       // The unsplit requests already fit in one wave: split only as far as the grid stays
       // one wave, i.e. the smallest page-aligned chunk whose CTAs all start at once.  A second,
@@ -151,6 +157,15 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       int64_t c = std::max<int64_t>(c_min, per_cta);
       c = (c + ps - 1) / ps * ps;
       C = longest > c ? c : 0;
+    }
+    if (C > 0 && r.max_items > 0 && items_with(C) > r.max_items) {
+      // a bounded work list (CUDA-graph mode): the smallest larger chunk that fits
+      int64_t lo = C, hi = std::max(C, c_max);
+      while (lo < hi) {
+        const int64_t mid = (lo / ps + (hi / ps - lo / ps) / 2) * ps;
+        if (items_with(mid) <= r.max_items) hi = mid; else lo = mid + ps;
+      }
+      C = longest > lo ? lo : 0;
     }
   }
   plan->chunk_tokens = C;
@@ -229,6 +244,11 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   if (ctas > (int64_t)std::numeric_limits<int32_t>::max()) {
     *err = "too many work items for one grid";
     return kErrInvalid;
+  }
+  if (r.max_items > 0 && (int64_t)items.size() > r.max_items) {
+    // only a fixed split can get here: the heuristic already fits the capacity
+    *err = "fixed_split_size cuts this batch into more work items than the work-list capacity";
+    return kErrWorkspace;
   }
   *err = "";
   return 0;

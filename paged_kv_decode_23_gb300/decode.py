@@ -45,17 +45,37 @@ def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
+def _graph_buffer(t, name: str, need: int) -> torch.Tensor:
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
+            and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    if t.numel() < need:
+        raise ValueError(f"{name} holds {t.numel()} entries, needs at least {need}")
+    return t
+
+
 class BatchDecodePagedKV:
     """Batch decode attention over a paged KV cache (one query token per request and head).
 
     ``float_workspace_buffer``: a CUDA uint8 tensor for split-KV partials (128 MiB is the
     usual size).  ``int_workspace_buffer``: CUDA uint8 tensor for the work list (allocated
     here, 8 MiB, if not given).  ``kv_layout``: "NHD" or "HND".
+
+    ``use_cuda_graph=True`` (with the three ``paged_kv_*_buffer`` device int32 tensors: indptr
+    ``[max_batch + 1]``, indices ``[max_pages]``, last_page_len ``[max_batch]``) makes ``run``
+    capturable in a CUDA graph whose replays stay valid across later ``plan`` calls: ``plan``
+    copies the page table into those buffers, the batch size is fixed by the first plan (pad
+    with zero-length requests), and the work list holds at most ``max_items`` chunks
+    (default: max_batch + 2 x the SM count).
     """
 
     def __init__(self, float_workspace_buffer: torch.Tensor, kv_layout: str = "NHD",
+                 use_cuda_graph: bool = False, use_tensor_cores: Optional[bool] = None,
+                 paged_kv_indptr_buffer: Optional[torch.Tensor] = None,
+                 paged_kv_indices_buffer: Optional[torch.Tensor] = None,
+                 paged_kv_last_page_len_buffer: Optional[torch.Tensor] = None,
                  int_workspace_buffer: Optional[torch.Tensor] = None,
-                 use_tensor_cores: Optional[bool] = None):
+                 max_items: Optional[int] = None):
         if kv_layout not in ("NHD", "HND"):
             raise ValueError("kv_layout must be 'NHD' or 'HND'")
         if not float_workspace_buffer.is_cuda:
@@ -69,6 +89,7 @@ class BatchDecodePagedKV:
         self._int_ws = int_workspace_buffer
         self._plan_args = None
         self._indices = None
+        self.use_cuda_graph = bool(use_cuda_graph)
         h = ctypes.c_void_p()
         L.check(L.lib().pkd_create(ctypes.byref(h), self._float_ws.data_ptr(),
                                    self._float_ws.numel() * self._float_ws.element_size(),
@@ -76,6 +97,18 @@ class BatchDecodePagedKV:
                                    self._int_ws.numel() * self._int_ws.element_size(),
                                    L.LAYOUT_NHD if kv_layout == "NHD" else L.LAYOUT_HND))
         self._h = h
+        if self.use_cuda_graph:
+            lpl = paged_kv_last_page_len_buffer
+            if lpl is None or paged_kv_indptr_buffer is None or paged_kv_indices_buffer is None:
+                raise ValueError("use_cuda_graph=True needs paged_kv_indptr_buffer, "
+                                 "paged_kv_indices_buffer and paged_kv_last_page_len_buffer")
+            max_batch = _graph_buffer(lpl, "paged_kv_last_page_len_buffer", 1).numel()
+            ip = _graph_buffer(paged_kv_indptr_buffer, "paged_kv_indptr_buffer", max_batch + 1)
+            ix = _graph_buffer(paged_kv_indices_buffer, "paged_kv_indices_buffer", 0)
+            self._graph_buffers = (ip, ix, lpl)
+            L.check(L.lib().pkd_enable_cuda_graph(self._h, ip.data_ptr(), ix.data_ptr(),
+                                                  lpl.data_ptr(), max_batch, ix.numel(),
+                                                  int(max_items or 0)))
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -214,10 +247,12 @@ class BatchDecodePagedKV:
 def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,
               page_size: int, window_left: int = -1, fixed_split_size: int = 0,
               disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
-              use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152):
+              use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152,
+              work_capacity: int = 0):
     """Run the host planner alone (no GPU): returns a dict with the work items
     ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, merge entry, 0), the merge
-    entries ``[m, 4]``, the slot count, the chosen kernel and the tile size."""
+    entries ``[m, 4]``, the slot count, the chosen kernel and the tile size.  ``work_capacity``
+    > 0 bounds the work list as CUDA-graph mode does."""
     ip = _host_i32(indptr)
     lpl = _host_i32(last_page_len)
     batch = len(lpl)
@@ -228,12 +263,13 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
             num_sms)
     L.check(L.lib().pkd_plan_host(*args, None, 0, None, 0, ctypes.byref(n_items),
                                   ctypes.byref(n_merges), ctypes.byref(n_slots),
-                                  ctypes.byref(kern), ctypes.byref(tile)))
+                                  ctypes.byref(kern), ctypes.byref(tile), int(work_capacity)))
     items = np.zeros((max(1, n_items.value), 8), dtype=np.int32)
     merges = np.zeros((max(1, n_merges.value), 4), dtype=np.int32)
     L.check(L.lib().pkd_plan_host(*args, _i32p(items), n_items.value, _i32p(merges),
                                   n_merges.value, ctypes.byref(n_items), ctypes.byref(n_merges),
-                                  ctypes.byref(n_slots), ctypes.byref(kern), ctypes.byref(tile)))
+                                  ctypes.byref(n_slots), ctypes.byref(kern), ctypes.byref(tile),
+                                  int(work_capacity)))
     return dict(items=items[:n_items.value], merges=merges[:n_merges.value],
                 num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
 
@@ -251,3 +287,31 @@ def workspace_bytes(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int,
                                         use_tensor_cores, num_sms, ctypes.byref(fb),
                                         ctypes.byref(ib)))
     return fb.value, ib.value
+
+
+def graph_workspace_bytes(max_items: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                          use_tensor_cores: int = L.KERNEL_AUTO):
+    """(float, int) workspace bytes that CUDA-graph mode needs for ``max_items`` chunks."""
+    fb, ib = ctypes.c_size_t(), ctypes.c_size_t()
+    L.check(L.lib().pkd_graph_workspace_bytes(int(max_items), num_qo_heads, num_kv_heads,
+                                              head_dim, use_tensor_cores, ctypes.byref(fb),
+                                              ctypes.byref(ib)))
+    return fb.value, ib.value
+
+
+class CUDAGraphBatchDecodePagedKV(BatchDecodePagedKV):
+    """The pages' CUDAGraphBatchDecodeWithPagedKVCacheWrapper: BatchDecodePagedKV in CUDA-graph
+    mode with the page-table buffers given up front (``indptr_buffer [max_batch + 1]``,
+    ``indices_buffer [max_pages]``, ``last_page_len_buffer [max_batch]``, device int32)."""
+
+    def __init__(self, workspace_buffer: torch.Tensor, indptr_buffer: torch.Tensor,
+                 indices_buffer: torch.Tensor, last_page_len_buffer: torch.Tensor,
+                 kv_layout: str = "NHD", use_tensor_cores: Optional[bool] = None,
+                 int_workspace_buffer: Optional[torch.Tensor] = None,
+                 max_items: Optional[int] = None):
+        super().__init__(workspace_buffer, kv_layout, use_cuda_graph=True,
+                         use_tensor_cores=use_tensor_cores,
+                         paged_kv_indptr_buffer=indptr_buffer,
+                         paged_kv_indices_buffer=indices_buffer,
+                         paged_kv_last_page_len_buffer=last_page_len_buffer,
+                         int_workspace_buffer=int_workspace_buffer, max_items=max_items)

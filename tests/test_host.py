@@ -167,3 +167,38 @@ def test_workspace_bytes_covers_partials(pkd):
                                  fixed_split_size=256, kv_dtype=1)
     assert fb >= 32 * 32 * 128 * 4 + 32 * 32 * 4
     assert ib >= 256 + 32 * 32 + 4 * 16
+
+
+@pytest.mark.parametrize("name", ["uniform", "lognormal", "mix", "worked"])
+def test_work_capacity_bounds_the_plan(pkd, name):
+    """CUDA-graph mode bounds the work list: the heuristic grows its chunks until the items fit,
+    and the result is still a valid partition of every request."""
+    w = W.workload(name)
+    kv = {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype]
+    for cap in (w.batch, w.batch + 1, w.batch + 7, w.batch + 100, 10 * w.batch):
+        plan = pkd.plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads,
+                             w.head_dim, w.page_size, window_left=w.window_left, kv_dtype=kv,
+                             work_capacity=cap)
+        assert len(plan["items"]) <= cap
+        _check_partition(w, plan, 0)
+
+
+def test_work_capacity_rejects_what_cannot_fit(pkd):
+    from paged_kv_decode_23_gb300 import PkdError
+    w = W.workload("long")  # fixed split of 256 pages: 8 chunks per request, 32 items
+    with pytest.raises(PkdError) as e:
+        pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, fixed_split_size=256,
+                      kv_dtype=1, work_capacity=31)
+    assert e.value.code == -3
+    ok = pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, fixed_split_size=256,
+                       kv_dtype=1, work_capacity=32)
+    assert len(ok["items"]) == 32
+    with pytest.raises(PkdError):  # more requests than items
+        pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, work_capacity=3)
+
+
+def test_graph_workspace_bytes(pkd):
+    fb, ib = pkd.graph_workspace_bytes(100, 32, 8, 128)
+    # 100 partial slots x 32 heads x 128 floats, their lses, and 100 items + 50 merges
+    assert fb >= 100 * 32 * 128 * 4 + 100 * 32 * 4
+    assert ib >= 256 + 50 * 8 * 4 + 100 * 32 + 50 * 16
