@@ -39,20 +39,28 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on: once the sources differ, the figure no longer describes the kernel and the line
 # reports null.
 MEASURED_TRAFFIC = {
-    "sources_sha256": "629d2cfbb559849d9457ce0f5e2ccbc55d73f4ef43b1bec2ebca02b12e258bb1",
-    "uniform": 618.92e6,  # profiles/decode_paged_kernel_uniform.md (2 launches averaged)
-    "mix": 418.19e6,      # profiles/decode_paged_kernel_mix.md
+    "sources_sha256": "a1d1d623e9ff105b52265e0316fdffd1bafe5c7895ba1a570d4cf03cdb2d1812",
+    # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set)
+    "uniform": 618.43e6,
+    "mix": 417.75e6,
+    "long": 2.153e9,
+    "lognormal": 3.524e9,
 }
+
+
+# The files that decide what the decode kernel reads and writes: its device code and the
+# planner that cuts its work list (host API and no-allocation code are left out).
+KERNEL_SOURCES = ("decode_kernels.cuh", "pkd_device.cuh", "pkd_internal.h", "decode_f16.cu",
+                  "decode_bf16.cu", "decode_e4m3.cu", "planner.cpp")
 
 
 def kernel_sources_digest() -> str:
     csrc = os.path.join(ROOT, "paged_kv_decode_23_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(name.encode())
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in KERNEL_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
