@@ -71,6 +71,15 @@ def _load():
                 ctypes.c_double, ctypes.c_double, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
                 vp, vp, ctypes.c_int]
+            lib.oracle_batch_decode_q.restype = ctypes.c_int
+            lib.oracle_batch_decode_q.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, i32p, i32p, i32p,
+                vp, ctypes.c_int, vp, vp, ctypes.c_int,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
+                vp, vp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -123,14 +132,17 @@ def batch_decode(indptr, indices, last_page_len, q_raw: np.ndarray, q_dtype: int
                  page_size: int, sm_scale: float | None = None,
                  logits_soft_cap: float = 0.0, window_left: int = -1,
                  q_scale: float = 1.0, k_scale: float = 1.0, v_scale: float = 1.0,
-                 chunk_tokens: int = 0, num_threads: int = 0):
+                 chunk_tokens: int = 0, num_threads: int = 0, q_len: int = 1):
     """Batch decode attention in fp64.
 
-    ``q_raw``: element bits of q ``[batch, num_qo_heads, head_dim]`` (contiguous).
+    ``q_raw``: element bits of q ``[batch * q_len, num_qo_heads, head_dim]`` (contiguous,
+    request-major; ``q_len`` query tokens per request, the last ``q_len`` positions, each
+    masked causally).
     ``k_raw`` / ``v_raw``: element bits of the key and value pools; ``strides`` =
     ``(page, slot, head)`` strides in elements, the head_dim axis contiguous.  For a 5-D pool,
     pass the same array twice with ``v_raw`` offset by the K/V stride (see ``tests``).
-    Returns ``(o [batch, num_qo_heads, head_dim] float64, lse [batch, num_qo_heads] float64)``.
+    Returns ``(o [batch * q_len, num_qo_heads, head_dim] float64, lse [batch * q_len,
+    num_qo_heads] float64)``.
     """
     indptr = _i32(indptr)
     indices = _i32(indices) if len(indices) else np.zeros(1, dtype=np.int32)
@@ -140,13 +152,14 @@ def batch_decode(indptr, indices, last_page_len, q_raw: np.ndarray, q_dtype: int
     q_raw = np.ascontiguousarray(q_raw)
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(head_dim)
-    o = np.zeros((batch, num_qo_heads, head_dim), dtype=np.float64)
-    lse = np.zeros((batch, num_qo_heads), dtype=np.float64)
+    rows = batch * int(q_len)
+    o = np.zeros((rows, num_qo_heads, head_dim), dtype=np.float64)
+    lse = np.zeros((rows, num_qo_heads), dtype=np.float64)
     ps, ss, hs = (int(s) for s in strides)
     k_ptr = k_raw.ctypes.data if isinstance(k_raw, np.ndarray) else int(k_raw)
     v_ptr = v_raw.ctypes.data if isinstance(v_raw, np.ndarray) else int(v_raw)
-    rc = _load().oracle_batch_decode(
-        batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+    rc = _load().oracle_batch_decode_q(
+        batch, int(q_len), num_qo_heads, num_kv_heads, head_dim, page_size,
         _ptr_i32(indptr), _ptr_i32(indices), _ptr_i32(lpl),
         q_raw.ctypes.data, q_dtype, k_ptr, v_ptr, kv_dtype, ps, ss, hs,
         float(sm_scale), float(logits_soft_cap or 0.0), int(window_left),

@@ -27,7 +27,11 @@
  *   - qo head g reads kv head g / (num_qo_heads / num_kv_heads);
  *   - calibration scales multiply: q = q_scale*Q, k = k_scale*K, v = v_scale*V;
  *   - a request with zero pages has kv_len 0, o = 0 and lse = -inf;
- *   - sm_scale defaults to 1/sqrt(head_dim) (that default is applied by the caller).
+ *   - sm_scale defaults to 1/sqrt(head_dim) (that default is applied by the caller);
+ *   - run()'s q_len_per_req (query tokens per request, default 1): the q_len tokens are the
+ *     last positions of the request, token j at n - q_len + j, each with the causal mask of
+ *     the page's batch prefill example (keys t <= its position) and its own window; q / o
+ *     rows are request-major [batch * q_len, ...].
  *
  * Every floating-point step is in double precision; inputs are decoded exactly from
  * their bit patterns (fp16, bf16, fp8 e4m3fn).
@@ -130,6 +134,7 @@ typedef struct {
   double sm_scale, logits_soft_cap;
   int window_left;
   double q_scale, k_scale, v_scale;
+  int q_len; /* query tokens per request (run's q_len_per_req), >= 1 */
 } oracle_problem;
 
 /* Element offset of K/V token t of request i, kv head h, dim 0: token t lives in page
@@ -140,25 +145,30 @@ static int64_t kv_offset(const oracle_problem* p, int i, int64_t t, int h) {
   return page * p->page_stride + slot * p->slot_stride + (int64_t)h * p->head_stride;
 }
 
-/* Attention of (request i, qo head g) restricted to the tokens t in [t_begin, t_end) that
- * the window admits.  Writes o[D] and lse; if no token is admitted, o = 0, lse = -inf.
- * Two passes over the keys: the logits and their maximum, then the weights. */
-static void attend_range(const oracle_problem* p, int i, int g, int64_t t_begin,
+/* Attention of query token j of request i, qo head g, restricted to the tokens t in
+ * [t_begin, t_end) that its mask admits.  The request's q_len query tokens are the last
+ * q_len positions of its sequence: token j sits at position pos = n - q_len + j and sees the
+ * keys t <= pos (the causal mask of the prefill example, tril(diagonal = kv_len - qo_len)),
+ * and with a window only t >= pos - window_left.  With q_len = 1 that is the decode query at
+ * n - 1.  Writes o[D] and lse; if no token is admitted, o = 0, lse = -inf.  Two passes over
+ * the keys: the logits and their maximum, then the weights. */
+static void attend_range(const oracle_problem* p, int i, int j, int g, int64_t t_begin,
                          int64_t t_end, double* o, double* lse, double* s_buf) {
   const int D = p->head_dim;
   const int group = p->num_qo_heads / p->num_kv_heads;
   const int h = g / group;
   const int64_t n = kv_len_of(p->indptr, p->last_page_len, i, p->page_size);
+  const int64_t pos = n - p->q_len + j;
   int64_t first = 0;
-  if (p->window_left >= 0 && n - 1 - p->window_left > 0) first = n - 1 - p->window_left;
+  if (p->window_left >= 0 && pos - p->window_left > 0) first = pos - p->window_left;
   if (t_begin < first) t_begin = first;
-  if (t_end > n) t_end = n;
+  if (t_end > pos + 1) t_end = pos + 1;
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (t_end <= t_begin) {
     *lse = -INFINITY;
     return;
   }
-  const int64_t q_off = ((int64_t)i * p->num_qo_heads + g) * D;
+  const int64_t q_off = (((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D;
   double m = -INFINITY;
   for (int64_t t = t_begin; t < t_end; ++t) {
     const int64_t off = kv_offset(p, i, t, h);
@@ -212,7 +222,7 @@ int oracle_merge_states(int n, int head_dim, const double* o_parts, const double
 
 static int check_problem(const oracle_problem* p) {
   if (p->batch < 0 || p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
-      p->page_size <= 0)
+      p->page_size <= 0 || p->q_len < 1)
     return -1;
   if (p->num_qo_heads % p->num_kv_heads != 0) return -2;
   for (int i = 0; i < p->batch; ++i) {
@@ -234,28 +244,29 @@ static int64_t max_kv_len(const oracle_problem* p) {
 }
 
 /*
- * Full batch decode.  chunk_tokens <= 0: every (request, head) attends over all its keys
- * in one pass.  chunk_tokens > 0: the keys are cut into consecutive chunks of that many
- * tokens counted from token 0, each chunk is attended separately and the chunks are
- * combined with oracle_merge_states in chunk order (the split-KV path written plainly).
- * num_threads <= 0 uses the OpenMP default.
+ * Full batch decode with q_len query tokens per request (q and o rows: request-major,
+ * [batch * q_len, num_qo_heads, head_dim]; q_len = 1 is plain decode).  chunk_tokens <= 0:
+ * every (query token, head) attends over all its keys in one pass.  chunk_tokens > 0: the
+ * keys are cut into consecutive chunks of that many tokens counted from token 0, each chunk
+ * is attended separately and the chunks are combined with oracle_merge_states in chunk order
+ * (the split-KV path written plainly).  num_threads <= 0 uses the OpenMP default.
  */
-int oracle_batch_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                        int page_size, const int32_t* indptr, const int32_t* indices,
-                        const int32_t* last_page_len, const void* q, int q_dtype,
-                        const void* k_base, const void* v_base, int kv_dtype,
-                        int64_t page_stride, int64_t slot_stride, int64_t head_stride,
-                        double sm_scale, double logits_soft_cap, int window_left,
-                        double q_scale, double k_scale, double v_scale, int64_t chunk_tokens,
-                        double* o, double* lse, int num_threads) {
+int oracle_batch_decode_q(int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                          int head_dim, int page_size, const int32_t* indptr,
+                          const int32_t* indices, const int32_t* last_page_len, const void* q,
+                          int q_dtype, const void* k_base, const void* v_base, int kv_dtype,
+                          int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                          double sm_scale, double logits_soft_cap, int window_left,
+                          double q_scale, double k_scale, double v_scale, int64_t chunk_tokens,
+                          double* o, double* lse, int num_threads) {
   oracle_problem p = {batch, num_qo_heads, num_kv_heads, head_dim, page_size, indptr,
                       indices, last_page_len, q, q_dtype, k_base, v_base, kv_dtype,
                       page_stride, slot_stride, head_stride, sm_scale, logits_soft_cap,
-                      window_left, q_scale, k_scale, v_scale};
+                      window_left, q_scale, k_scale, v_scale, q_len};
   int rc = check_problem(&p);
   if (rc != 0) return rc;
   const int64_t nmax = max_kv_len(&p);
-  const int64_t work = (int64_t)batch * num_qo_heads;
+  const int64_t work = (int64_t)batch * q_len * num_qo_heads;
   int bad = 0;
 #ifdef _OPENMP
   if (num_threads > 0) omp_set_num_threads(num_threads);
@@ -272,16 +283,18 @@ int oracle_batch_decode(int batch, int num_qo_heads, int num_kv_heads, int head_
 #endif
     for (int64_t w = 0; w < work; ++w) {
       if (bad) continue;
-      const int i = (int)(w / num_qo_heads);
+      const int64_t row = w / num_qo_heads;  /* = i * q_len + j */
+      const int i = (int)(row / q_len);
+      const int j = (int)(row % q_len);
       const int g = (int)(w % num_qo_heads);
       double* o_ig = o + w * head_dim;
       if (chunk_tokens <= 0) {
-        attend_range(&p, i, g, 0, nmax + 1, o_ig, &lse[w], s_buf);
+        attend_range(&p, i, j, g, 0, nmax + 1, o_ig, &lse[w], s_buf);
       } else {
         const int64_t n = kv_len_of(indptr, last_page_len, i, page_size);
         int nc = 0;
         for (int64_t t0 = 0; t0 < n; t0 += chunk_tokens, ++nc)
-          attend_range(&p, i, g, t0, t0 + chunk_tokens, o_parts + (int64_t)nc * head_dim,
+          attend_range(&p, i, j, g, t0, t0 + chunk_tokens, o_parts + (int64_t)nc * head_dim,
                        &lse_parts[nc], s_buf);
         oracle_merge_states(nc, head_dim, o_parts, lse_parts, o_ig, &lse[w]);
       }
@@ -291,6 +304,22 @@ int oracle_batch_decode(int batch, int num_qo_heads, int num_kv_heads, int head_
     free(lse_parts);
   }
   return bad ? -5 : 0;
+}
+
+/* Plain decode: one query token per request. */
+int oracle_batch_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                        int page_size, const int32_t* indptr, const int32_t* indices,
+                        const int32_t* last_page_len, const void* q, int q_dtype,
+                        const void* k_base, const void* v_base, int kv_dtype,
+                        int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                        double sm_scale, double logits_soft_cap, int window_left,
+                        double q_scale, double k_scale, double v_scale, int64_t chunk_tokens,
+                        double* o, double* lse, int num_threads) {
+  return oracle_batch_decode_q(batch, 1, num_qo_heads, num_kv_heads, head_dim, page_size, indptr,
+                               indices, last_page_len, q, q_dtype, k_base, v_base, kv_dtype,
+                               page_stride, slot_stride, head_stride, sm_scale, logits_soft_cap,
+                               window_left, q_scale, k_scale, v_scale, chunk_tokens, o, lse,
+                               num_threads);
 }
 
 /* The number of threads an OpenMP region would use (reported with timings). */

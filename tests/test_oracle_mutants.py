@@ -3,7 +3,8 @@
 Every mutant is a one-line edit of ``oracle/pkd_oracle.c`` in a scratch copy (never the
 oracle itself): a wrong GQA head map, an off-by-one window, a dropped max-subtraction, a
 wrong lse, a soft cap without the division, swapped strides, a wrong kv-length rule, an
-unweighted merge, a missing v_scale, and wrong fp16 / e4m3 decoders.  The pin suite in
+unweighted merge, a missing v_scale, wrong fp16 / e4m3 decoders, and for several query tokens
+per request a causal limit one past the query, reversed token positions and token-major rows.  The pin suite in
 ``test_oracle_pins.py`` runs against each mutant and must fail.
 """
 import os
@@ -17,7 +18,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTANTS = {
     "gqa_head_map": ("const int h = g / group;", "const int h = g % p->num_kv_heads;"),
-    "window_off_by_one": ("first = n - 1 - p->window_left;", "first = n - p->window_left;"),
+    "window_off_by_one": ("first = pos - p->window_left;", "first = pos + 1 - p->window_left;"),
+    "causal_limit_past_query": ("if (t_end > pos + 1) t_end = pos + 1;",
+                                "if (t_end > pos + 2) t_end = pos + 2;"),
+    "query_tokens_reversed": ("const int64_t pos = n - p->q_len + j;",
+                              "const int64_t pos = n - 1 - j;"),
+    "query_rows_token_major": ("(((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D",
+                               "(((int64_t)j * p->batch + i) * p->num_qo_heads + g) * D"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "soft_cap_no_division": ("tanh(x / p->logits_soft_cap)", "tanh(x)"),
     "slot_head_strides_swapped": ("slot * p->slot_stride + (int64_t)h * p->head_stride",

@@ -155,6 +155,65 @@ def test_brute_force_agreement(layout, case):
     np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-12)
 
 
+def _brute_multi(kv_lens, q_len, Hq, Hkv, D, q, K, V, sm_scale, cap=0.0, window_left=-1):
+    """Dense attention of q_len query tokens per request under the causal mask of the batch
+    prefill example, tril(ones(qo_len, kv_len), diagonal=kv_len - qo_len), narrowed by a
+    left window band of window_left + 1 keys per row.  q: [B, q_len, Hq, D]."""
+    G = Hq // Hkv
+    B = len(kv_lens)
+    o = np.zeros((B, q_len, Hq, D))
+    lse = np.full((B, q_len, Hq), -np.inf)
+    for i in range(B):
+        n = kv_lens[i]
+        if n == 0:
+            continue
+        mask = np.tril(np.ones((q_len, n), dtype=bool), k=n - q_len)
+        if window_left >= 0:
+            mask &= ~np.tril(np.ones((q_len, n), dtype=bool), k=n - q_len - window_left - 1)
+        Kr = np.repeat(K[i], G, axis=1)  # [n, Hq, D]
+        Vr = np.repeat(V[i], G, axis=1)
+        for j in range(q_len):
+            if not mask[j].any():
+                continue
+            x = sm_scale * np.einsum("hd,thd->ht", q[i, j], Kr[mask[j]])
+            s = cap * np.tanh(x / cap) if cap > 0 else x
+            o[i, j] = np.einsum("ht,thd->hd", scipy.special.softmax(s, axis=1), Vr[mask[j]])
+            lse[i, j] = scipy.special.logsumexp(s, axis=1)
+    return o.reshape(B * q_len, Hq, D), lse.reshape(B * q_len, Hq)
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("case", [
+    dict(kv_lens=[5, 17, 40], q_len=3, Hq=4, Hkv=2, D=8, ps=4),
+    dict(kv_lens=[1, 2, 33], q_len=4, Hq=6, Hkv=3, D=16, ps=8, cap=2.5),
+    dict(kv_lens=[9, 31, 0], q_len=2, Hq=4, Hkv=1, D=4, ps=3, window_left=5),
+    dict(kv_lens=[12, 7], q_len=5, Hq=2, Hkv=2, D=8, ps=4, window_left=0),
+])
+def test_multi_token_queries_brute_force(layout, case):
+    """q_len_per_req > 1 (run's q_len_per_req): each request's last q_len positions attend
+    causally; requests shorter than q_len leave their first query tokens with no key."""
+    rng = np.random.default_rng(4321)
+    kv_lens, ql = case["kv_lens"], case["q_len"]
+    Hq, Hkv, D, ps = case["Hq"], case["Hkv"], case["D"], case["ps"]
+    cap, wl = case.get("cap", 0.0), case.get("window_left", -1)
+    q = rng.standard_normal((len(kv_lens), ql, Hq, D))
+    K = [rng.standard_normal((n, Hkv, D)) for n in kv_lens]
+    V = [rng.standard_normal((n, Hkv, D)) for n in kv_lens]
+    sm = 0.41
+    ref_o, ref_lse = _brute_multi(kv_lens, ql, Hq, Hkv, D, q, K, V, sm, cap, wl)
+    indptr, indices, lpl, pool = _scatter(kv_lens, K, V, ps, layout, rng)
+    o, lse = _run_f64(indptr, indices, lpl, q.reshape(-1, Hq, D), pool, layout, sm_scale=sm,
+                      logits_soft_cap=cap, window_left=wl, q_len=ql)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-12)
+    # the last query token of every request is plain decode
+    o1, lse1 = _run_f64(indptr, indices, lpl, np.ascontiguousarray(q[:, -1]), pool, layout,
+                        sm_scale=sm, logits_soft_cap=cap, window_left=wl)
+    np.testing.assert_array_equal(o.reshape(len(kv_lens), ql, Hq, D)[:, -1], o1)
+
+
 def test_scales_multiply_inputs():
     rng = np.random.default_rng(7)
     kv_lens, Hq, Hkv, D = [6, 11], 4, 2, 8
