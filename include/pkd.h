@@ -97,6 +97,11 @@ int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, vo
  *   heuristic sizes chunks to fill the GPU.
  *   q_dtype / o_dtype: F16 or BF16, equal; kv_dtype: q_dtype or E4M3.
  *   use_tensor_cores: PKD_KERNEL_AUTO, PKD_KERNEL_CUDA_CORE or PKD_KERNEL_TENSOR_CORE.
+ *   q_len_per_req >= 1 (the page's run(q_len_per_req), fixed here because the work list
+ *     depends on it): query tokens per request.  They are the request's last positions:
+ *     token j of a request with kv_len n sits at n - q_len + j and attends the keys up to its
+ *     own position (causal inside the request) and its own window.  q, o and lse then have
+ *     batch * q_len_per_req rows, request-major (row = request * q_len_per_req + j).
  * Errors: INVALID_ARG (shapes, table), UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
  */
 int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page_len_host,
@@ -104,11 +109,11 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
              int num_kv_heads, int head_dim, int page_size, float sm_scale,
              float logits_soft_cap, int window_left, int fixed_split_size,
              int disable_split_kv, int q_dtype, int kv_dtype, int o_dtype,
-             int use_tensor_cores, void* stream);
+             int use_tensor_cores, int q_len_per_req, void* stream);
 
 /*
  * Run the planned batch on one layer's KV pool.  Asynchronous on `stream`; never syncs.
- *   q (device) [batch, num_qo_heads, head_dim], contiguous, q_dtype.
+ *   q (device) [batch * q_len_per_req, num_qo_heads, head_dim], contiguous, q_dtype.
  *   k_base / v_base (device): element (page, slot, head, 0) of K / V lives at
  *     base + page*kv_strides[0] + slot*kv_strides[1] + head*kv_strides[2] (elements of
  *     kv_dtype, head_dim contiguous).  A 5-D pool [pages, 2, ...] passes v_base =
@@ -117,8 +122,8 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
  *     match the handle's layout (NHD: slot stride > head stride; HND: the reverse).
  *   num_pages: pages in the pool (the extent of the page axis).
  *   q_scale, k_scale, v_scale: calibration scales (1.0 when unused).
- *   o (device) [batch, num_qo_heads, head_dim] o_dtype; lse (device) [batch, num_qo_heads]
- *     float32 natural log, or NULL to skip it.
+ *   o (device) [batch * q_len_per_req, num_qo_heads, head_dim] o_dtype; lse (device)
+ *     [batch * q_len_per_req, num_qo_heads] float32 natural log, or NULL to skip it.
  * Launches one decode kernel; the CTA that finishes a split request's last chunk merges the
  * request's partial results inside that launch.
  */
@@ -185,7 +190,7 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
                         int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                         int page_size, int window_left, int fixed_split_size,
                         int disable_split_kv, int kv_dtype, int use_tensor_cores, int num_sms,
-                        size_t* float_ws_bytes, size_t* int_ws_bytes);
+                        int q_len_per_req, size_t* float_ws_bytes, size_t* int_ws_bytes);
 
 /*
  * The planner alone (host-only; no CUDA call), for inspection and tests.  Writes up to
@@ -204,7 +209,8 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
                   int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
                   int32_t* merges_out, int max_merges, int* n_items, int* n_merges,
-                  int* n_slots, int* kernel_out, int* tile_tokens_out, int work_capacity);
+                  int* n_slots, int* kernel_out, int* tile_tokens_out, int work_capacity,
+                  int q_len_per_req);
 
 /*
  * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no

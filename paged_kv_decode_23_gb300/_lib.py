@@ -36,7 +36,7 @@ SIGNATURES = {
     "pkd_reset_workspace": (_c_int, [_vp, _vp, _c_size, _vp, _c_size]),
     "pkd_plan": (_c_int, [_vp, _i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int, _c_int,
                           _c_int, _c_float, _c_float, _c_int, _c_int, _c_int, _c_int, _c_int,
-                          _c_int, _c_int, _vp]),
+                          _c_int, _c_int, _c_int, _vp]),
     "pkd_run": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, _i64p, _c_float, _c_float, _c_float,
                          _vp, _vp, _vp]),
     "pkd_run_timed": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, _i64p, _c_float, _c_float,
@@ -44,13 +44,13 @@ SIGNATURES = {
     "pkd_destroy": (_c_int, [_vp]),
     "pkd_last_error": (ctypes.c_char_p, []),
     "pkd_workspace_bytes": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                     _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
     "pkd_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _c_int, _i32p,
                                _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
-                               ctypes.POINTER(_c_int), _c_int]),
+                               ctypes.POINTER(_c_int), _c_int, _c_int]),
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkd_set_pdl": (_c_int, [_vp, _c_int]),
     "pkd_enable_cuda_graph": (_c_int, [_vp, _vp, _vp, _vp, _c_int, ctypes.c_int64, _c_int]),

@@ -100,6 +100,7 @@ struct pkd_handle {
   bool planned = false;
   Plan plan;
   int batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, page_size = 0;
+  int q_len = 1;  // query tokens per request: q / o / lse have batch * q_len rows
   int q_dtype = 0, kv_dtype = 0, o_dtype = 0;
   float sm_scale = 0.f, cap = 0.f;
   const int32_t* indices = nullptr;
@@ -197,7 +198,7 @@ cudaError_t set_smem_limit_once(const DecodeKernel* k, int device) {
 
 int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl, int batch,
                       int hq, int hkv, int d, int ps, int window_left, int fixed_split,
-                      int disable_split, int kv_dtype, int use_tc, int num_sms) {
+                      int disable_split, int kv_dtype, int use_tc, int num_sms, int q_len) {
   r->indptr = indptr;
   r->last_page_len = lpl;
   r->batch = batch;
@@ -211,7 +212,9 @@ int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl,
   r->kv_dtype = kv_dtype;
   r->use_tensor_cores = use_tc;
   r->num_sms = num_sms;
+  r->q_len = q_len;
   if (use_tc < -1 || use_tc > 1) return fail(PKD_ERR_INVALID_ARG, "use_tensor_cores must be -1, 0 or 1");
+  if (q_len < 1) return fail(PKD_ERR_INVALID_ARG, "q_len_per_req must be >= 1");
   return PKD_OK;
 }
 
@@ -284,11 +287,12 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
                   int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
                   int32_t* merges_out, int max_merges, int* n_items, int* n_merges, int* n_slots,
-                  int* kernel_out, int* tile_tokens_out, int work_capacity) {
+                  int* kernel_out, int* tile_tokens_out, int work_capacity, int q_len_per_req) {
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
-                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms);
+                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms,
+                             q_len_per_req);
   if (rc) return rc;
   r.max_items = work_capacity > 0 ? work_capacity : 0;
   Plan plan;
@@ -314,12 +318,13 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
 int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
                         int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                         int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
-                        int use_tensor_cores, int num_sms, size_t* float_ws_bytes,
-                        size_t* int_ws_bytes) {
+                        int use_tensor_cores, int num_sms, int q_len_per_req,
+                        size_t* float_ws_bytes, size_t* int_ws_bytes) {
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
-                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms);
+                             disable_split_kv, kv_dtype, use_tensor_cores, num_sms,
+                             q_len_per_req);
   if (rc) return rc;
   Plan plan;
   const char* err = "";
@@ -334,7 +339,8 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
              int batch, const int32_t* indices_dev, int64_t num_indices, int num_qo_heads,
              int num_kv_heads, int head_dim, int page_size, float sm_scale, float logits_soft_cap,
              int window_left, int fixed_split_size, int disable_split_kv, int q_dtype,
-             int kv_dtype, int o_dtype, int use_tensor_cores, void* stream) {
+             int kv_dtype, int o_dtype, int use_tensor_cores, int q_len_per_req,
+             void* stream) {
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
   h->planned = false;
   if (q_dtype != PKD_DTYPE_F16 && q_dtype != PKD_DTYPE_BF16)
@@ -359,12 +365,16 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
                   "with zero-length requests instead)");
     if ((int64_t)indptr_host[batch] > h->g_max_pages)
       return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: indptr[batch] exceeds max_pages");
+    if (h->g_batch >= 0 && q_len_per_req != h->q_len)
+      return fail(PKD_ERR_INVALID_ARG,
+                  "CUDA-graph mode: q_len_per_req is fixed by the first plan");
   }
 
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
-                             disable_split_kv, kv_dtype, use_tensor_cores, h->num_sms);
+                             disable_split_kv, kv_dtype, use_tensor_cores, h->num_sms,
+                             q_len_per_req);
   if (rc) return rc;
   if (h->graph) r.max_items = h->g_max_items;
   Plan plan;
@@ -449,6 +459,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
 
   h->plan = std::move(plan);
   h->batch = batch;
+  h->q_len = q_len_per_req;
   h->num_qo_heads = num_qo_heads;
   h->num_kv_heads = num_kv_heads;
   h->head_dim = head_dim;

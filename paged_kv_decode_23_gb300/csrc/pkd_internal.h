@@ -9,14 +9,15 @@
 
 namespace pkd {
 
-// One CTA-group of work: a chunk of one request's KV tokens.  Tokens count from the
+// One CTA-group of work: a chunk of one output row's KV tokens (a row is one query token of
+// one request; with one query token per request, the request).  Tokens count from the
 // request's first token.  The chunk covers pages starting at chunk_tok0 / page_size; the
 // attended tokens of the chunk are [tok_begin, tok_end).  out_slot < 0 means the chunk is
 // the whole request and the kernel writes the final o / lse; otherwise it writes an fp32
 // partial into slot out_slot of the float workspace.
 struct WorkItem {
-  int32_t req;
-  int32_t page_base;   // indptr[req]: offset of the request's first page id in `indices`
+  int32_t req;         // output row: q / o / lse row index
+  int32_t page_base;   // indptr[request]: offset of the request's first page id in `indices`
   int32_t chunk_tok0;  // first token of the chunk's first page
   int32_t tok_begin;
   int32_t tok_end;
@@ -122,6 +123,7 @@ struct PlanRequest {
   int use_tensor_cores;  // -1 auto, 0, 1
   int num_sms;
   int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode)
+  int q_len = 1;         // query tokens per request (run's q_len_per_req)
 };
 
 struct Plan {

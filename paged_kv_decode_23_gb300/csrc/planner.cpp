@@ -84,9 +84,8 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
   plan->tile_tokens = tile_tokens_for(r.head_dim, r.kv_dtype);
 
-  // per-request lengths and attended ranges
-  std::vector<int64_t> n(r.batch), w(r.batch);
-  int64_t total = 0, longest = 0;
+  // per-request lengths
+  std::vector<int64_t> n_req(r.batch);
   for (int i = 0; i < r.batch; ++i) {
     const int64_t pages = (int64_t)r.indptr[i + 1] - r.indptr[i];
     if (pages < 0) {
@@ -94,8 +93,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       return kErrInvalid;
     }
     if (pages == 0) {
-      n[i] = 0;
-      w[i] = 0;
+      n_req[i] = 0;
       continue;
     }
     const int lpl = r.last_page_len[i];
@@ -103,14 +101,36 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       *err = "last_page_len must lie in [1, page_size] for every request with pages";
       return kErrInvalid;
     }
-    n[i] = (int64_t)ps * (pages - 1) + lpl;
-    if (n[i] > (int64_t)std::numeric_limits<int32_t>::max() - 4096) {
+    n_req[i] = (int64_t)ps * (pages - 1) + lpl;
+    if (n_req[i] > (int64_t)std::numeric_limits<int32_t>::max() - 4096) {
       *err = "a request is longer than 2^31 - 4096 tokens";
       return kErrInvalid;
     }
-    w[i] = (r.window_left >= 0 && n[i] - 1 - r.window_left > 0) ? n[i] - 1 - r.window_left : 0;
-    total += n[i] - w[i];
-    longest = std::max(longest, n[i] - w[i]);
+  }
+
+  // Output rows: query token j of request i is row i * q_len + j, at position
+  // n - q_len + j, and sees the keys up to that position -- a decode query over the
+  // request's first n - q_len + j + 1 keys, read through the request's own pages.  Each row
+  // is planned as a request of its own (with q_len = 1 the rows are the requests).
+  const int ql = r.q_len > 0 ? r.q_len : 1;
+  const int64_t rows64 = (int64_t)r.batch * ql;
+  if (rows64 > (int64_t)std::numeric_limits<int32_t>::max() / 2) {
+    *err = "batch * q_len_per_req is too large";
+    return kErrInvalid;
+  }
+  const int rows = (int)rows64;
+  std::vector<int64_t> n(rows), w(rows);
+  std::vector<int32_t> base(rows);
+  int64_t total = 0, longest = 0;
+  for (int row = 0; row < rows; ++row) {
+    const int i = row / ql, j = row % ql;
+    n[row] = std::max<int64_t>(0, n_req[i] - (ql - 1 - j));
+    base[row] = r.indptr[i];
+    w[row] = (r.window_left >= 0 && n[row] - 1 - r.window_left > 0)
+                 ? n[row] - 1 - r.window_left
+                 : 0;
+    total += n[row] - w[row];
+    longest = std::max(longest, n[row] - w[row]);
   }
 
   // chunk size in tokens (a multiple of the page size); 0 = one chunk per request
@@ -119,7 +139,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   // work items with heuristic (equal) chunks of c tokens; an empty request is one item
   auto items_with = [&](int64_t c) {
     int64_t items = 0;
-    for (int i = 0; i < r.batch; ++i) {
+    for (int i = 0; i < rows; ++i) {
       const int64_t a = n[i] - w[i];
       items += a > c ? (a + c - 1) / c : 1;
     }
@@ -128,8 +148,8 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   auto ctas_with = [&](int64_t c) { return items_with(c) * ctas_per_item; };
   const int64_t c_min = (kMinChunk + ps - 1) / ps * ps;
   const int64_t c_max = (longest + ps - 1) / ps * ps;
-  if (r.max_items > 0 && r.batch > r.max_items) {
-    *err = "the batch has more requests than the work-list capacity";
+  if (r.max_items > 0 && rows > r.max_items) {
+    *err = "the batch has more query rows (requests x q_len_per_req) than the work-list capacity";
     return kErrInvalid;
   }
   if (r.disable_split_kv) {
@@ -139,7 +159,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   } else {
     const int sms = r.num_sms > 0 ? r.num_sms : 152;
     const int64_t slots = (int64_t)sms * kCtasPerSm;
-    if ((int64_t)r.batch * ctas_per_item <= slots) {
+    if ((int64_t)rows * ctas_per_item <= slots) {
       // The unsplit requests already fit in one wave: split only as far as the grid stays
       // one wave, i.e. the smallest page-aligned chunk whose CTAs all start at once.  A second,
       // partial wave of chunks measured slower than no split at all on GB300.
@@ -174,11 +194,11 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   std::vector<WorkItem>& items = plan->items;
   const bool fixed = !r.disable_split_kv && r.fixed_split_size > 0;
   std::vector<int64_t> bounds, tile0;
-  for (int i = 0; i < r.batch; ++i) {
+  for (int i = 0; i < rows; ++i) {
     WorkItem it;
     std::memset(&it, 0, sizeof it);
-    it.req = i;
-    it.page_base = r.indptr[i];
+    it.req = i;  // the output row
+    it.page_base = base[i];
     it.merge_idx = -1;
     if (n[i] == 0) {
       it.chunk_tok0 = 0;

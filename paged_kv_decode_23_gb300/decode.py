@@ -136,10 +136,14 @@ class BatchDecodePagedKV:
              q_data_type=torch.float16, kv_data_type=None, o_data_type=None, data_type=None,
              sm_scale: Optional[float] = None, non_blocking: bool = True,
              fixed_split_size: Optional[int] = None, disable_split_kv: bool = False,
-             use_tensor_cores: Optional[bool] = None, stream=None) -> None:
+             use_tensor_cores: Optional[bool] = None, stream=None,
+             q_len_per_req: int = 1) -> None:
         """Plan a batch; ``indptr`` / ``last_page_len`` may live on the host or the device
         (a device copy is read back once here), ``indices`` must be a CUDA int32 tensor and
-        stay unchanged while runs of this plan are in flight."""
+        stay unchanged while runs of this plan are in flight.  ``q_len_per_req`` query tokens
+        per request (run's parameter of that name; the work list depends on it, so it is fixed
+        here): the request's last positions, each attending causally; q / o then have
+        ``batch * q_len_per_req`` rows, request-major."""
         if pos_encoding_mode != "NONE":
             raise NotImplementedError("only pos_encoding_mode='NONE' is implemented")
         if data_type is not None:
@@ -163,9 +167,10 @@ class BatchDecodePagedKV:
             num_qo_heads, num_kv_heads, head_dim, page_size, sm,
             float(logits_soft_cap or 0.0), int(window_left), int(fixed_split_size or 0),
             int(bool(disable_split_kv)), _DTYPE_CODE[q_dt], _DTYPE_CODE[kv_dt], _DTYPE_CODE[o_dt],
-            kernel, _stream_ptr(stream)))
+            kernel, int(q_len_per_req), _stream_ptr(stream)))
         self._indices = indices
-        self._plan_args = dict(batch=batch, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+        self._plan_args = dict(batch=batch, q_len=int(q_len_per_req),
+                               num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
                                head_dim=head_dim, page_size=page_size, q_dtype=q_dt,
                                kv_dtype=kv_dt, o_dtype=o_dt)
 
@@ -203,14 +208,18 @@ class BatchDecodePagedKV:
             q_scale: Optional[float] = None, k_scale: Optional[float] = None,
             v_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, return_lse: bool = False, stream=None,
-            timing_events=None, enable_pdl: Optional[bool] = None):
+            timing_events=None, enable_pdl: Optional[bool] = None,
+            q_len_per_req: Optional[int] = None):
         """Decode attention for the planned batch on one layer's pool: returns ``o`` or
         ``(o, lse)`` (lse: float32 natural log, ``[batch, num_qo_heads]``).  ``enable_pdl``
         switches programmatic dependent launch for this and later runs (on by default)."""
         a = self._plan_args
         if a is None:
             raise RuntimeError("plan() must be called before run()")
-        exp_q = (a["batch"], a["num_qo_heads"], a["head_dim"])
+        if q_len_per_req is not None and int(q_len_per_req) != a["q_len"]:
+            raise ValueError(f"q_len_per_req={q_len_per_req} differs from the plan's "
+                             f"{a['q_len']} (the work list depends on it: re-plan)")
+        exp_q = (a["batch"] * a["q_len"], a["num_qo_heads"], a["head_dim"])
         if tuple(q.shape) != exp_q or q.dtype != a["q_dtype"] or not q.is_contiguous():
             raise ValueError(f"q must be a contiguous {a['q_dtype']} tensor of shape {exp_q}")
         kv, k_ptr, v_ptr, num_pages, strides = self._kv_pointers(paged_kv_cache)
@@ -223,7 +232,7 @@ class BatchDecodePagedKV:
         if lse is None and return_lse:
             lse = torch.empty(exp_q[:2], dtype=torch.float32, device=q.device)
         if lse is not None and (tuple(lse.shape) != exp_q[:2] or lse.dtype != torch.float32):
-            raise ValueError("lse must be float32 [batch, num_qo_heads]")
+            raise ValueError("lse must be float32 [batch * q_len_per_req, num_qo_heads]")
         st = (ctypes.c_int64 * 3)(*strides)
         if enable_pdl is not None:
             L.check(L.lib().pkd_set_pdl(self._h, int(bool(enable_pdl))))
@@ -248,7 +257,7 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
               page_size: int, window_left: int = -1, fixed_split_size: int = 0,
               disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
               use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152,
-              work_capacity: int = 0):
+              work_capacity: int = 0, q_len_per_req: int = 1):
     """Run the host planner alone (no GPU): returns a dict with the work items
     ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, merge entry, 0), the merge
     entries ``[m, 4]``, the slot count, the chosen kernel and the tile size.  ``work_capacity``
@@ -263,13 +272,14 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
             num_sms)
     L.check(L.lib().pkd_plan_host(*args, None, 0, None, 0, ctypes.byref(n_items),
                                   ctypes.byref(n_merges), ctypes.byref(n_slots),
-                                  ctypes.byref(kern), ctypes.byref(tile), int(work_capacity)))
+                                  ctypes.byref(kern), ctypes.byref(tile), int(work_capacity),
+                                  int(q_len_per_req)))
     items = np.zeros((max(1, n_items.value), 8), dtype=np.int32)
     merges = np.zeros((max(1, n_merges.value), 4), dtype=np.int32)
     L.check(L.lib().pkd_plan_host(*args, _i32p(items), n_items.value, _i32p(merges),
                                   n_merges.value, ctypes.byref(n_items), ctypes.byref(n_merges),
                                   ctypes.byref(n_slots), ctypes.byref(kern), ctypes.byref(tile),
-                                  int(work_capacity)))
+                                  int(work_capacity), int(q_len_per_req)))
     return dict(items=items[:n_items.value], merges=merges[:n_merges.value],
                 num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
 
@@ -277,15 +287,16 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
 def workspace_bytes(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                     page_size: int, window_left: int = -1, fixed_split_size: int = 0,
                     disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
-                    use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152):
+                    use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152,
+                    q_len_per_req: int = 1):
     ip = _host_i32(indptr)
     lpl = _host_i32(last_page_len)
     fb, ib = ctypes.c_size_t(), ctypes.c_size_t()
     L.check(L.lib().pkd_workspace_bytes(_i32p(ip), _i32p(lpl), len(lpl), num_qo_heads,
                                         num_kv_heads, head_dim, page_size, window_left,
                                         fixed_split_size, int(disable_split_kv), kv_dtype,
-                                        use_tensor_cores, num_sms, ctypes.byref(fb),
-                                        ctypes.byref(ib)))
+                                        use_tensor_cores, num_sms, int(q_len_per_req),
+                                        ctypes.byref(fb), ctypes.byref(ib)))
     return fb.value, ib.value
 
 

@@ -253,3 +253,25 @@ def test_scores_drifting_along_the_sequence(kv, order, tc):
     pool = vals.to(pool.dtype)
     assert_close(w, run_gpu(w, q, pool, use_tensor_cores=tc), run_oracle(w, q, pool),
                  f"{order} {kv} tc={tc}")
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 5])
+@pytest.mark.parametrize("kv,tc", [("bf16", True), ("bf16", False), ("e4m3", True), ("e4m3", False)])
+def test_several_query_tokens_per_request(q_len, kv, tc):
+    """run's q_len_per_req > 1: each request's last q_len positions attend causally (and
+    through their own windows); rows are request-major.  Lengths include requests shorter
+    than q_len, whose first query tokens see no key."""
+    lens = [1, 2, 16, 17, 300, 1500, 0, 777]
+    for mode in (dict(), dict(fixed_split_size=4, window_left=120)):
+        w = W.custom(lens, 16, 2, 128, 16, layout="NHD", q_dtype="bf16", kv_dtype=kv,
+                     seed=30 + q_len, logits_soft_cap=30.0 if kv == "e4m3" else 0.0,
+                     window_left=mode.get("window_left", -1))
+        if kv == "e4m3":
+            w.kv_store_scale, w.k_scale, w.v_scale = 0.5, 0.5, 0.5
+        gen = torch.Generator().manual_seed(77 + q_len)
+        q = torch.randn(len(lens) * q_len, 16, 128, generator=gen).to(torch.bfloat16)
+        pool = W.make_pool(w)
+        got = run_gpu(w, q, pool, use_tensor_cores=tc, q_len_per_req=q_len,
+                      fixed_split_size=mode.get("fixed_split_size"))
+        assert_close(w, got, run_oracle(w, q, pool, q_len=q_len),
+                     f"q_len {q_len} {kv} tc={tc} {mode}")

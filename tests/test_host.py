@@ -202,3 +202,34 @@ def test_graph_workspace_bytes(pkd):
     # 100 partial slots x 32 heads x 128 floats, their lses, and 100 items + 50 merges
     assert fb >= 100 * 32 * 128 * 4 + 100 * 32 * 4
     assert ib >= 256 + 50 * 8 * 4 + 100 * 32 + 50 * 16
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 5])
+@pytest.mark.parametrize("mode", [dict(), dict(fixed_split_size=3), dict(disable_split_kv=True)])
+def test_multi_token_rows_partition_their_causal_keys(pkd, q_len, mode):
+    """q_len_per_req > 1: output row i*q_len + j covers exactly the keys its query token sees,
+    t <= n - q_len + j within its window, read through request i's pages."""
+    lens = [0, 1, 3, 16, 17, 300, 2000]
+    window = 40 if "fixed_split_size" in mode else -1
+    w = W.custom(lens, 8, 2, 128, 16, window_left=window)
+    plan = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 16, window_left=window,
+                         q_len_per_req=q_len, **mode)
+    items = plan["items"]
+    by_row = {}
+    for it in items:
+        by_row.setdefault(int(it[0]), []).append(it)
+    assert sorted(by_row) == list(range(len(lens) * q_len))
+    for row, its in by_row.items():
+        i, j = divmod(row, q_len)
+        n = max(0, lens[i] - (q_len - 1 - j))
+        lo = 0 if window < 0 else max(0, n - 1 - window)
+        its = sorted(its, key=lambda x: x[3])
+        assert all(int(it[1]) == int(w.indptr[i]) for it in its)
+        if n == 0:
+            assert len(its) == 1 and its[0][3] == its[0][4] == 0
+            continue
+        assert int(its[0][3]) == lo and int(its[-1][4]) == n
+        for a, b in zip(its, its[1:]):
+            assert int(a[4]) == int(b[3])
+        if len(its) > 1:
+            assert plan["merges"][int(its[0][6])][0] == row
