@@ -80,6 +80,16 @@ def _load():
                 ctypes.c_double, ctypes.c_double, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
                 vp, vp, ctypes.c_int]
+            lib.oracle_batch_decode_pos.restype = ctypes.c_int
+            lib.oracle_batch_decode_pos.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, i32p, i32p, i32p,
+                vp, ctypes.c_int, vp, vp, ctypes.c_int,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
+                vp, vp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -132,12 +142,16 @@ def batch_decode(indptr, indices, last_page_len, q_raw: np.ndarray, q_dtype: int
                  page_size: int, sm_scale: float | None = None,
                  logits_soft_cap: float = 0.0, window_left: int = -1,
                  q_scale: float = 1.0, k_scale: float = 1.0, v_scale: float = 1.0,
-                 chunk_tokens: int = 0, num_threads: int = 0, q_len: int = 1):
+                 chunk_tokens: int = 0, num_threads: int = 0, q_len: int = 1,
+                 pos_encoding_mode: str = "NONE", rope_scale: float = 1.0,
+                 rope_theta: float = 1e4):
     """Batch decode attention in fp64.
 
     ``q_raw``: element bits of q ``[batch * q_len, num_qo_heads, head_dim]`` (contiguous,
     request-major; ``q_len`` query tokens per request, the last ``q_len`` positions, each
-    masked causally).
+    masked causally).  ``pos_encoding_mode``: "NONE", "ROPE_LLAMA" (q rotated at its position,
+    each key at its token index, pairs (i, i + D/2), angle pos / rope_scale *
+    rope_theta^(-2i/D)) or "ALIBI" (slope_g * (t - pos) added to the scaled logit).
     ``k_raw`` / ``v_raw``: element bits of the key and value pools; ``strides`` =
     ``(page, slot, head)`` strides in elements, the head_dim axis contiguous.  For a 5-D pool,
     pass the same array twice with ``v_raw`` offset by the K/V stride (see ``tests``).
@@ -158,12 +172,15 @@ def batch_decode(indptr, indices, last_page_len, q_raw: np.ndarray, q_dtype: int
     ps, ss, hs = (int(s) for s in strides)
     k_ptr = k_raw.ctypes.data if isinstance(k_raw, np.ndarray) else int(k_raw)
     v_ptr = v_raw.ctypes.data if isinstance(v_raw, np.ndarray) else int(v_raw)
-    rc = _load().oracle_batch_decode_q(
+    mode = {"NONE": 0, "ROPE_LLAMA": 1, "ALIBI": 2}[pos_encoding_mode]
+    rc = _load().oracle_batch_decode_pos(
         batch, int(q_len), num_qo_heads, num_kv_heads, head_dim, page_size,
         _ptr_i32(indptr), _ptr_i32(indices), _ptr_i32(lpl),
         q_raw.ctypes.data, q_dtype, k_ptr, v_ptr, kv_dtype, ps, ss, hs,
         float(sm_scale), float(logits_soft_cap or 0.0), int(window_left),
-        float(q_scale), float(k_scale), float(v_scale), int(chunk_tokens),
+        float(q_scale), float(k_scale), float(v_scale), mode,
+        float(1.0 if rope_scale is None else rope_scale),
+        float(1e4 if rope_theta is None else rope_theta), int(chunk_tokens),
         o.ctypes.data, lse.ctypes.data, int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle_batch_decode rejected the problem (code {rc})")

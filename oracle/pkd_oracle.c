@@ -135,7 +135,33 @@ typedef struct {
   int window_left;
   double q_scale, k_scale, v_scale;
   int q_len; /* query tokens per request (run's q_len_per_req), >= 1 */
+  int pos_mode; /* 0 NONE, 1 ROPE_LLAMA, 2 ALIBI (plan's pos_encoding_mode) */
+  double rope_scale, rope_theta;
 } oracle_problem;
+
+/* ROPE_LLAMA ("LLaMA-style rotary embedding"): the vector x[D] at position pos is rotated
+ * pairwise, dims (i, i + D/2) for i < D/2, by the angle (pos / rope_scale) * theta^(-2i/D):
+ *   x_i' = x_i cos a - x_{i+D/2} sin a,   x_{i+D/2}' = x_{i+D/2} cos a + x_i sin a. */
+static void rope_rotate(double* x, int D, double pos, double rope_scale, double rope_theta) {
+  const int half = D / 2;
+  for (int i = 0; i < half; ++i) {
+    const double a = (pos / rope_scale) * pow(rope_theta, -2.0 * i / D);
+    const double c = cos(a), s = sin(a);
+    const double x0 = x[i], x1 = x[i + half];
+    x[i] = x0 * c - x1 * s;
+    x[i + half] = x1 * c + x0 * s;
+  }
+}
+
+/* ALIBI: the slope of qo head g of H.  With m the largest power of two <= H, heads g < m take
+ * 2^(-8 (g+1) / m) (the geometric sequence of the ALiBi paper), and the remaining heads take
+ * every other slope of the 2m-head sequence, 2^(-4 (2 (g-m) + 1) / m). */
+static double alibi_slope(int g, int H) {
+  int m = 1;
+  while (m * 2 <= H) m *= 2;
+  if (g < m) return pow(2.0, -8.0 * (g + 1) / m);
+  return pow(2.0, -4.0 * (2 * (g - m) + 1) / m);
+}
 
 /* Element offset of K/V token t of request i, kv head h, dim 0: token t lives in page
  * indices[indptr[i] + t / page_size] at slot t % page_size. */
@@ -153,7 +179,8 @@ static int64_t kv_offset(const oracle_problem* p, int i, int64_t t, int h) {
  * n - 1.  Writes o[D] and lse; if no token is admitted, o = 0, lse = -inf.  Two passes over
  * the keys: the logits and their maximum, then the weights. */
 static void attend_range(const oracle_problem* p, int i, int j, int g, int64_t t_begin,
-                         int64_t t_end, double* o, double* lse, double* s_buf) {
+                         int64_t t_end, double* o, double* lse, double* s_buf, double* qv,
+                         double* kv) {
   const int D = p->head_dim;
   const int group = p->num_qo_heads / p->num_kv_heads;
   const int h = g / group;
@@ -169,16 +196,19 @@ static void attend_range(const oracle_problem* p, int i, int j, int g, int64_t t
     return;
   }
   const int64_t q_off = (((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D;
+  for (int d = 0; d < D; ++d) qv[d] = p->q_scale * load_elem(p->q, q_off + d, p->q_dtype);
+  if (p->pos_mode == 1) rope_rotate(qv, D, (double)pos, p->rope_scale, p->rope_theta);
+  const double slope = p->pos_mode == 2 ? alibi_slope(g, p->num_qo_heads) : 0.0;
   double m = -INFINITY;
   for (int64_t t = t_begin; t < t_end; ++t) {
     const int64_t off = kv_offset(p, i, t, h);
+    for (int d = 0; d < D; ++d) kv[d] = p->k_scale * load_elem(p->k_base, off + d, p->kv_dtype);
+    if (p->pos_mode == 1) rope_rotate(kv, D, (double)t, p->rope_scale, p->rope_theta);
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) {
-      double qd = p->q_scale * load_elem(p->q, q_off + d, p->q_dtype);
-      double kd = p->k_scale * load_elem(p->k_base, off + d, p->kv_dtype);
-      dot += qd * kd;
-    }
-    double x = p->sm_scale * dot;
+    for (int d = 0; d < D; ++d) dot += qv[d] * kv[d];
+    /* ALiBi adds slope * (t - pos), a penalty growing with the distance to the query, to the
+     * scaled logit before the soft cap */
+    double x = p->sm_scale * dot + slope * (double)(t - pos);
     double s = (p->logits_soft_cap > 0.0) ? p->logits_soft_cap * tanh(x / p->logits_soft_cap) : x;
     s_buf[t - t_begin] = s;
     if (s > m) m = s;
@@ -224,6 +254,9 @@ static int check_problem(const oracle_problem* p) {
   if (p->batch < 0 || p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
       p->page_size <= 0 || p->q_len < 1)
     return -1;
+  if (p->pos_mode < 0 || p->pos_mode > 2) return -1;
+  if (p->pos_mode == 1 && (p->head_dim % 2 != 0 || !(p->rope_scale > 0) || !(p->rope_theta > 0)))
+    return -1;
   if (p->num_qo_heads % p->num_kv_heads != 0) return -2;
   for (int i = 0; i < p->batch; ++i) {
     if (p->indptr[i + 1] < p->indptr[i]) return -3;
@@ -251,18 +284,20 @@ static int64_t max_kv_len(const oracle_problem* p) {
  * is attended separately and the chunks are combined with oracle_merge_states in chunk order
  * (the split-KV path written plainly).  num_threads <= 0 uses the OpenMP default.
  */
-int oracle_batch_decode_q(int batch, int q_len, int num_qo_heads, int num_kv_heads,
-                          int head_dim, int page_size, const int32_t* indptr,
-                          const int32_t* indices, const int32_t* last_page_len, const void* q,
-                          int q_dtype, const void* k_base, const void* v_base, int kv_dtype,
-                          int64_t page_stride, int64_t slot_stride, int64_t head_stride,
-                          double sm_scale, double logits_soft_cap, int window_left,
-                          double q_scale, double k_scale, double v_scale, int64_t chunk_tokens,
-                          double* o, double* lse, int num_threads) {
+int oracle_batch_decode_pos(int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int page_size, const int32_t* indptr,
+                            const int32_t* indices, const int32_t* last_page_len, const void* q,
+                            int q_dtype, const void* k_base, const void* v_base, int kv_dtype,
+                            int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                            double sm_scale, double logits_soft_cap, int window_left,
+                            double q_scale, double k_scale, double v_scale, int pos_mode,
+                            double rope_scale, double rope_theta, int64_t chunk_tokens,
+                            double* o, double* lse, int num_threads) {
   oracle_problem p = {batch, num_qo_heads, num_kv_heads, head_dim, page_size, indptr,
                       indices, last_page_len, q, q_dtype, k_base, v_base, kv_dtype,
                       page_stride, slot_stride, head_stride, sm_scale, logits_soft_cap,
-                      window_left, q_scale, k_scale, v_scale, q_len};
+                      window_left, q_scale, k_scale, v_scale, q_len, pos_mode, rope_scale,
+                      rope_theta};
   int rc = check_problem(&p);
   if (rc != 0) return rc;
   const int64_t nmax = max_kv_len(&p);
@@ -274,6 +309,9 @@ int oracle_batch_decode_q(int batch, int q_len, int num_qo_heads, int num_kv_hea
 #endif
   {
     double* s_buf = (double*)malloc(sizeof(double) * (size_t)nmax);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    double* kv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    if (!qv || !kv) bad = 1;
     int64_t max_chunks = chunk_tokens > 0 ? (nmax + chunk_tokens - 1) / chunk_tokens : 1;
     double* o_parts = (double*)malloc(sizeof(double) * (size_t)(max_chunks * head_dim));
     double* lse_parts = (double*)malloc(sizeof(double) * (size_t)max_chunks);
@@ -289,21 +327,39 @@ int oracle_batch_decode_q(int batch, int q_len, int num_qo_heads, int num_kv_hea
       const int g = (int)(w % num_qo_heads);
       double* o_ig = o + w * head_dim;
       if (chunk_tokens <= 0) {
-        attend_range(&p, i, j, g, 0, nmax + 1, o_ig, &lse[w], s_buf);
+        attend_range(&p, i, j, g, 0, nmax + 1, o_ig, &lse[w], s_buf, qv, kv);
       } else {
         const int64_t n = kv_len_of(indptr, last_page_len, i, page_size);
         int nc = 0;
         for (int64_t t0 = 0; t0 < n; t0 += chunk_tokens, ++nc)
           attend_range(&p, i, j, g, t0, t0 + chunk_tokens, o_parts + (int64_t)nc * head_dim,
-                       &lse_parts[nc], s_buf);
+                       &lse_parts[nc], s_buf, qv, kv);
         oracle_merge_states(nc, head_dim, o_parts, lse_parts, o_ig, &lse[w]);
       }
     }
     free(s_buf);
+    free(qv);
+    free(kv);
     free(o_parts);
     free(lse_parts);
   }
   return bad ? -5 : 0;
+}
+
+/* Several query tokens per request, no positional encoding. */
+int oracle_batch_decode_q(int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                          int head_dim, int page_size, const int32_t* indptr,
+                          const int32_t* indices, const int32_t* last_page_len, const void* q,
+                          int q_dtype, const void* k_base, const void* v_base, int kv_dtype,
+                          int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                          double sm_scale, double logits_soft_cap, int window_left,
+                          double q_scale, double k_scale, double v_scale, int64_t chunk_tokens,
+                          double* o, double* lse, int num_threads) {
+  return oracle_batch_decode_pos(batch, q_len, num_qo_heads, num_kv_heads, head_dim, page_size,
+                                 indptr, indices, last_page_len, q, q_dtype, k_base, v_base,
+                                 kv_dtype, page_stride, slot_stride, head_stride, sm_scale,
+                                 logits_soft_cap, window_left, q_scale, k_scale, v_scale, 0, 1.0,
+                                 1e4, chunk_tokens, o, lse, num_threads);
 }
 
 /* Plain decode: one query token per request. */

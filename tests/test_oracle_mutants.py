@@ -4,7 +4,9 @@ Every mutant is a one-line edit of ``oracle/pkd_oracle.c`` in a scratch copy (ne
 oracle itself): a wrong GQA head map, an off-by-one window, a dropped max-subtraction, a
 wrong lse, a soft cap without the division, swapped strides, a wrong kv-length rule, an
 unweighted merge, a missing v_scale, wrong fp16 / e4m3 decoders, and for several query tokens
-per request a causal limit one past the query, reversed token positions and token-major rows.  The pin suite in
+per request a causal limit one past the query, reversed token positions and token-major rows,
+and for the positional encodings a reversed RoPE rotation, a rope_scale that multiplies and an
+ALiBi bias of the wrong sign.  The pin suite in
 ``test_oracle_pins.py`` runs against each mutant and must fail.
 """
 import os
@@ -23,6 +25,9 @@ MUTANTS = {
                                 "if (t_end > pos + 2) t_end = pos + 2;"),
     "query_tokens_reversed": ("const int64_t pos = n - p->q_len + j;",
                               "const int64_t pos = n - 1 - j;"),
+    "rope_rotation_reversed": ("x[i] = x0 * c - x1 * s;", "x[i] = x0 * c + x1 * s;"),
+    "rope_scale_multiplies": ("const double a = (pos / rope_scale)", "const double a = (pos * rope_scale)"),
+    "alibi_distance_sign": ("slope * (double)(t - pos)", "slope * (double)(pos - t)"),
     "query_rows_token_major": ("(((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D",
                                "(((int64_t)j * p->batch + i) * p->num_qo_heads + g) * D"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),

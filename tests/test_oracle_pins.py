@@ -214,6 +214,124 @@ def test_multi_token_queries_brute_force(layout, case):
     np.testing.assert_array_equal(o.reshape(len(kv_lens), ql, Hq, D)[:, -1], o1)
 
 
+# ------------------------------------------------- positional encoding (pos_encoding_mode)
+
+def _rope_complex(x, pos, theta, scale):
+    """ROPE_LLAMA written with complex numbers: pair (x_i, x_{i+D/2}) is z = x_i + i*x_{i+D/2},
+    rotated by multiplying with exp(i * (pos / scale) * theta^(-2i/D))."""
+    D = x.shape[-1]
+    half = D // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    ang = (pos / scale) * theta ** (-2.0 * np.arange(half) / D)
+    z = z * np.exp(1j * ang)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _alibi_slopes(H):
+    """ALiBi slopes: the geometric sequence starting at 2^(-8/m) with ratio 2^(-8/m) for the
+    largest power of two m <= H, completed by every other slope of the 2m-head sequence."""
+    m = 2 ** int(np.floor(np.log2(H)))
+    first = [(2.0 ** (-8.0 / m)) ** (k + 1) for k in range(m)]
+    rest = [(2.0 ** (-8.0 / (2 * m))) ** (k + 1) for k in range(0, 2 * (H - m), 2)]
+    return np.array(first + rest)
+
+
+def _brute_pos(kv_lens, Hq, Hkv, D, q, K, V, sm, mode, theta=1e4, scale=1.0, window_left=-1,
+               cap=0.0):
+    """Dense decode attention with the positional encoding applied to dense q / K."""
+    G = Hq // Hkv
+    o = np.zeros((len(kv_lens), Hq, D))
+    lse = np.full((len(kv_lens), Hq), -np.inf)
+    slopes = _alibi_slopes(Hq)
+    for i, n in enumerate(kv_lens):
+        if n == 0:
+            continue
+        lo = 0 if window_left < 0 else max(0, n - 1 - window_left)
+        t = np.arange(lo, n)
+        Kr = np.repeat(K[i][lo:n], G, axis=1)
+        Vr = np.repeat(V[i][lo:n], G, axis=1)
+        qi = q[i]
+        if mode == "ROPE_LLAMA":
+            qi = _rope_complex(qi, n - 1, theta, scale)
+            Kr = np.stack([_rope_complex(Kr[k], t[k], theta, scale) for k in range(len(t))])
+        x = sm * np.einsum("hd,thd->ht", qi, Kr)
+        if mode == "ALIBI":
+            x = x + slopes[:, None] * (t[None, :] - (n - 1))
+        s = cap * np.tanh(x / cap) if cap > 0 else x
+        o[i] = np.einsum("ht,thd->hd", scipy.special.softmax(s, axis=1), Vr)
+        lse[i] = scipy.special.logsumexp(s, axis=1)
+    return o, lse
+
+
+@pytest.mark.parametrize("case", [
+    dict(mode="ROPE_LLAMA", kv_lens=[5, 40, 0, 17], Hq=4, Hkv=2, D=8),
+    dict(mode="ROPE_LLAMA", kv_lens=[300, 33], Hq=2, Hkv=1, D=16, theta=500.0, scale=2.5,
+         window_left=50),
+    dict(mode="ALIBI", kv_lens=[5, 40, 17], Hq=8, Hkv=2, D=8),
+    dict(mode="ALIBI", kv_lens=[60, 3], Hq=6, Hkv=3, D=8, cap=3.0),
+])
+def test_positional_encoding_brute_force(case):
+    rng = np.random.default_rng(99)
+    kv_lens, Hq, Hkv, D = case["kv_lens"], case["Hq"], case["Hkv"], case["D"]
+    q, K, V = _rand_problem(rng, kv_lens, Hq, Hkv, D)
+    kw = dict(theta=case.get("theta", 1e4), scale=case.get("scale", 1.0),
+              window_left=case.get("window_left", -1), cap=case.get("cap", 0.0))
+    ref_o, ref_lse = _brute_pos(kv_lens, Hq, Hkv, D, q, K, V, 0.3, case["mode"], **kw)
+    indptr, indices, lpl, pool = _scatter(kv_lens, K, V, 4, "NHD", rng)
+    o, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=0.3,
+                      pos_encoding_mode=case["mode"], rope_theta=kw["theta"],
+                      rope_scale=kw["scale"], window_left=kw["window_left"],
+                      logits_soft_cap=kw["cap"])
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-11)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-11)
+
+
+def test_alibi_slopes_of_eight_heads_are_powers_of_one_half():
+    """The ALiBi paper's example: 8 heads take 1/2, 1/4, ..., 1/256.  One key at distance d
+    behind the query, with q = 0, gets logit -slope*d: lse over {d, 0} = log(1 + 2^(-d*k))."""
+    np.testing.assert_allclose(_alibi_slopes(8), [2.0 ** -(k + 1) for k in range(8)], rtol=1e-15)
+    D, H = 4, 8
+    q = np.zeros((1, H, D))
+    K = [np.zeros((2, 1, D))]
+    V = [np.ones((2, 1, D))]
+    rng = np.random.default_rng(3)
+    indptr, indices, lpl, pool = _scatter([2], K, V, 4, "NHD", rng)
+    _, lse = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=1.0,
+                      pos_encoding_mode="ALIBI")
+    np.testing.assert_allclose(lse[0], np.log1p(np.exp(-2.0 ** -(np.arange(H) + 1.0))),
+                               rtol=0, atol=1e-14)
+
+
+def test_rope_depends_only_on_relative_position():
+    """Rotating q at p and k at t gives a logit that depends only on t - p: a request whose
+    keys are preceded by s unattended tokens (window) returns the same output as the bare
+    request (ALiBi's bias depends on t - p as well)."""
+    rng = np.random.default_rng(11)
+    D, m, s_pad = 16, 9, 23
+    q = rng.standard_normal((1, 2, D))
+    Kc = rng.standard_normal((m, 1, D))
+    Vc = rng.standard_normal((m, 1, D))
+    junk = rng.standard_normal((s_pad, 1, D))
+    i1, x1, l1, p1 = _scatter([m], [Kc], [Vc], 4, "NHD", rng)
+    i2, x2, l2, p2 = _scatter([m + s_pad], [np.concatenate([junk, Kc])],
+                              [np.concatenate([junk, Vc])], 4, "NHD", rng)
+    for mode in ("ROPE_LLAMA", "ALIBI"):
+        o1, lse1 = _run_f64(i1, x1, l1, q, p1, "NHD", sm_scale=0.5, pos_encoding_mode=mode)
+        o2, lse2 = _run_f64(i2, x2, l2, q, p2, "NHD", sm_scale=0.5, pos_encoding_mode=mode,
+                            window_left=m - 1)
+        np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse1, rtol=0, atol=1e-12)
+    # a key equal to q at the query's own position: both get the same rotation, so the logit
+    # is |q|^2 (a rotation preserves dot products)
+    K1 = [np.repeat(q[:, :1, :], 1, axis=0).reshape(1, 1, D)]
+    i3, x3, l3, p3 = _scatter([1], K1, [np.ones((1, 1, D))], 4, "NHD", rng)
+    _, lse3 = _run_f64(i3, x3, l3, q[:, :1, :].copy(), p3, "NHD", sm_scale=1.0,
+                       num_qo_heads=1, pos_encoding_mode="ROPE_LLAMA")
+    np.testing.assert_allclose(lse3[0, 0], np.sum(q[0, 0] ** 2), rtol=1e-13)
+
+
 def test_scales_multiply_inputs():
     rng = np.random.default_rng(7)
     kv_lens, Hq, Hkv, D = [6, 11], 4, 2, 8
