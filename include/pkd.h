@@ -57,6 +57,11 @@ extern "C" {
 #define PKD_LAYOUT_NHD 0 /* page block [page_size, num_kv_heads, head_dim] */
 #define PKD_LAYOUT_HND 1 /* page block [num_kv_heads, page_size, head_dim] */
 
+/* pkd_plan's pos_encoding_mode (the page's pos_encoding_mode NONE / ROPE_LLAMA / ALIBI). */
+#define PKD_POS_NONE 0
+#define PKD_POS_ROPE_LLAMA 1
+#define PKD_POS_ALIBI 2
+
 /* Kernel choice for pkd_plan's use_tensor_cores argument (the page's use_tensor_cores). */
 #define PKD_KERNEL_AUTO (-1)
 #define PKD_KERNEL_CUDA_CORE 0
@@ -102,6 +107,16 @@ int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, vo
  *     token j of a request with kv_len n sits at n - q_len + j and attends the keys up to its
  *     own position (causal inside the request) and its own window.  q, o and lse then have
  *     batch * q_len_per_req rows, request-major (row = request * q_len_per_req + j).
+ *   pos_encoding_mode (the page's NONE / ROPE_LLAMA / ALIBI, with rope_scale and rope_theta,
+ *     the page's defaults 1 and 1e4; both ignored unless ROPE_LLAMA):
+ *     PKD_POS_ROPE_LLAMA rotates q (at its position) and each key (at its token index) in
+ *       pairs of dims (i, i + head_dim/2) by the angle pos / rope_scale * rope_theta^(-2i/D)
+ *       before the dot product; the rotated q and K are rounded to fp16 for the product.
+ *       Built for the tensor-core kernel only (PKD_KERNEL_CUDA_CORE gives UNSUPPORTED).
+ *       Angles are accurate to ~1e-6 rad for positions below 2^24.
+ *     PKD_POS_ALIBI adds slope_g * (t - pos) to the scaled logit of qo head g (before the soft
+ *       cap), with the ALiBi paper's slopes 2^(-8 (g+1) / m) for the largest power of two
+ *       m <= num_qo_heads and 2^(-4 (2 (g-m) + 1) / m) for the heads beyond m.
  * Errors: INVALID_ARG (shapes, table), UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
  */
 int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page_len_host,
@@ -109,7 +124,8 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
              int num_kv_heads, int head_dim, int page_size, float sm_scale,
              float logits_soft_cap, int window_left, int fixed_split_size,
              int disable_split_kv, int q_dtype, int kv_dtype, int o_dtype,
-             int use_tensor_cores, int q_len_per_req, void* stream);
+             int use_tensor_cores, int q_len_per_req, int pos_encoding_mode, float rope_scale,
+             float rope_theta, void* stream);
 
 /*
  * Run the planned batch on one layer's KV pool.  Asynchronous on `stream`; never syncs.

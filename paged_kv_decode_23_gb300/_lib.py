@@ -36,7 +36,7 @@ SIGNATURES = {
     "pkd_reset_workspace": (_c_int, [_vp, _vp, _c_size, _vp, _c_size]),
     "pkd_plan": (_c_int, [_vp, _i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int, _c_int,
                           _c_int, _c_float, _c_float, _c_int, _c_int, _c_int, _c_int, _c_int,
-                          _c_int, _c_int, _c_int, _vp]),
+                          _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _vp]),
     "pkd_run": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, _i64p, _c_float, _c_float, _c_float,
                          _vp, _vp, _vp]),
     "pkd_run_timed": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, _i64p, _c_float, _c_float,

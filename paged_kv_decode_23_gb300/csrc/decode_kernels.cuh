@@ -307,9 +307,31 @@ __device__ __forceinline__ float tanh_via_exp2(float x) {
   return 1.f - __fdividef(2.f, e + 1.f);
 }
 
-__device__ __forceinline__ float score_log2(float dot, float scale_qk, float cap_log2) {
-  const float x = dot * scale_qk;
+// The logit in base-2 units: dot * scale_qk (sm_scale and the calibration scales, times
+// log2 e, or divided by the cap) plus the ALiBi bias in the same units, then the soft cap.
+__device__ __forceinline__ float score_log2(float dot, float scale_qk, float bias, float cap_log2) {
+  const float x = fmaf(dot, scale_qk, bias);
   return cap_log2 > 0.f ? cap_log2 * tanh_via_exp2(x) : x;
+}
+
+// ALiBi slope of a qo head, in score units (0 without ALiBi).
+template <int D>
+__device__ __forceinline__ float alibi_slope(const DecodeParams& p, int qo_head) {
+  return p.alibi ? __ldg(p.pos_table + D + qo_head) : 0.f;
+}
+
+// ROPE_LLAMA on two 16-bit pairs held in registers: lo holds dims (i, i+1) and hi the partner
+// dims (i + D/2, i + D/2 + 1), of a token at position t; rates points at rate pairs {hi, lo}
+// of dims i, i+1.  x' = x cos a - y sin a, y' = y cos a + x sin a, rounded to fp16.
+template <typename TIN>
+__device__ __forceinline__ void rope_pair(uint32_t& lo, uint32_t& hi, float t, float4 rates) {
+  using namespace dev;
+  const float2 x = unpack2<TIN>(lo), y = unpack2<TIN>(hi);
+  float s0, c0, s1, c1;
+  rope_sincos(t, rates.x, rates.y, s0, c0);
+  rope_sincos(t, rates.z, rates.w, s1, c1);
+  lo = pack2<__half>(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
+  hi = pack2<__half>(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
 }
 
 // ------------------------------------------------------------------------------ tensor core
@@ -320,7 +342,9 @@ __device__ __forceinline__ float score_log2(float dot, float scale_qk, float cap
 // slots so that lane tig's four slots {2tig, 2tig+1, 2tig+8, 2tig+9} hold d = kk*16 + 4tig ..
 // kk*16 + 4tig + 3: the matching K bytes are then one 32-bit load.  A dot product does not
 // depend on the order of its terms, so K and Q only have to agree.
-template <typename TQ, typename T, int D, bool PERM = false>
+// With ROPE, q is rotated at its position (the work item's q_pos) in fp32 before the rounding
+// to fp16: the two halves of a rotation pair sit in k steps kk and kk + D/32 of the same lane.
+template <typename TQ, typename T, int D, bool PERM = false, bool ROPE = false>
 __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockCoords& b, int lane,
                                              uint32_t (&qb)[D / 16][2], float& qmul) {
   using namespace dev;
@@ -331,7 +355,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
   const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
                    ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D;
   qmul = 1.f;
-  if constexpr (sizeof(TQ) == sizeof(T) && std::is_same<TQ, T>::value) {
+  if constexpr (!ROPE && std::is_same<TQ, T>::value) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       qb[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + off0) : 0u;
@@ -347,9 +371,31 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
         const uint32_t raw =
             live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + (h ? off1 : off0)) : 0u;
         f[kk][h] = unpack2<TQ>(raw);
-        amax = fmaxf(amax, fmaxf(fabsf(f[kk][h].x), fabsf(f[kk][h].y)));
       }
     }
+    if constexpr (ROPE) {
+      const float pos = (float)b.it.q_pos;
+      const float4* rates = reinterpret_cast<const float4*>(p.pos_table);
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = kk * 16 + (h ? off1 : off0);  // dims i, i+1; partners i + D/2, i + D/2 + 1
+          const float4 r = __ldg(rates + i / 2);
+          float s0, c0, s1, c1;
+          rope_sincos(pos, r.x, r.y, s0, c0);
+          rope_sincos(pos, r.z, r.w, s1, c1);
+          const float2 x = f[kk][h], y = f[kk + D / 32][h];
+          f[kk][h] = make_float2(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
+          f[kk + D / 32][h] = make_float2(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
+        }
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        amax = fmaxf(amax, fmaxf(fabsf(f[kk][h].x), fabsf(f[kk][h].y)));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, off));
     int qexp = 0;
@@ -399,23 +445,32 @@ __device__ __forceinline__ int acc_dim(int mb, int row) {
   }
 }
 
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES>
+// ROPE: K is rotated in registers before the QK MMAs (the two halves of a rotation pair are
+// k steps kk and kk + D/32 of the same lane) and rounded to fp16, so QK runs in fp16 (q is
+// rotated and rounded the same way); P*V keeps V's type.
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, bool ROPE = false>
 __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
                                            uint32_t full0, uint32_t empty0, volatile int* abort_flag,
                                            int warp, int lane, float (&m2)[2], float (&lsum)[2],
                                            float (&acc)[D / 16][4]) {
   using namespace dev;
-  using T = typename std::conditional<KV_FP8, __half, TQ>::type;
+  using T = typename std::conditional<KV_FP8, __half, TQ>::type;      // P*V operand type
+  using TQK = typename std::conditional<KV_FP8 || ROPE, __half, TQ>::type;  // QK operand type
   using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   uint32_t qb[D / 16][2];
   float qmul;
-  load_q_frags<TQ, T, D, KV_FP8>(p, b, lane, qb, qmul);
+  load_q_frags<TQ, TQK, D, KV_FP8, ROPE>(p, b, lane, qb, qmul);
   const float scale_qk = p.scale_qk * qmul;
   const float cap_log2 = p.cap_log2;
   const int g_row = lane >> 2, tig = lane & 3;
   // tokens (within the warp's 16-token slice) of this lane's two S^T rows
   const int tok_a = KV_FP8 ? perm_tok(g_row) : g_row;
   const int tok_b = KV_FP8 ? perm_tok(g_row + 8) : g_row + 8;
+  // ALiBi slopes of this lane's two C columns (qo heads g0 + 2tig, + 1; dead columns of a
+  // partial head slice read the last live head's slope, their results are discarded)
+  const float slope0 = alibi_slope<D>(p, b.g0 + min(2 * tig, b.gcnt - 1));
+  const float slope1 = alibi_slope<D>(p, b.g0 + min(2 * tig + 1, b.gcnt - 1));
+  const float4* rope_rates = reinterpret_cast<const float4*>(p.pos_table);
   // e4m3 path: this lane's byte offsets inside a stage tile, with the 128-byte swizzle of the
   // row already folded in (a chunk index is then applied with one XOR).  K: rows tok_a, tok_b,
   // bytes 4tig.. of each 16-byte chunk.  V: rows tig + 4*t4, bytes 8*(g_row&1).. of chunk
@@ -471,24 +526,65 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
       if constexpr (KV_FP8) {
         // rows tok_a / tok_b; k slots as in load_q_frags<PERM>: four consecutive e4m3 bytes
         const uint32_t ka = ktile + koff_a, kb = ktile + koff_b;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        auto load_k = [&](int kk, uint32_t (&a)[4]) {
           const uint32_t blk = (kk >> 3) * TS * 128;  // 128-byte column block of the chunk
           const uint32_t wa = lds_u32((ka ^ ((kk & 7) << 4)) + blk);
           const uint32_t wb = lds_u32((kb ^ ((kk & 7) << 4)) + blk);
-          uint32_t a[4];
           e4m3x4_to_half2x2(wa, a[0], a[2]);
           e4m3x4_to_half2x2(wb, a[1], a[3]);
-          mma_16816<T>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
+        };
+        if constexpr (ROPE) {
+          const float ta = (float)(t_w + tok_a), tb = (float)(t_w + tok_b);
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            uint32_t a[4], h[4];  // k steps kk and kk + D/32: dims i and i + D/2
+            load_k(kk, a);
+            load_k(kk + D / 32, h);
+            const float4 r0 = __ldg(rope_rates + (kk * 16 + tig * 4) / 2);
+            const float4 r1 = __ldg(rope_rates + (kk * 16 + tig * 4 + 2) / 2);
+            rope_pair<__half>(a[0], h[0], ta, r0);
+            rope_pair<__half>(a[1], h[1], tb, r0);
+            rope_pair<__half>(a[2], h[2], ta, r1);
+            rope_pair<__half>(a[3], h[3], tb, r1);
+            mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
+            mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4];
+            load_k(kk, a);
+            mma_16816<TQK>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
+          }
         }
       } else {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int csel = lane >> 4;
+        if constexpr (ROPE) {
+          // ldmatrix: a[0] / a[2] are row g_row (token tok_a), dims 16kk + 2tig (+1) and
+          // 16kk + 8 + 2tig (+1); a[1] / a[3] the same dims of row g_row + 8 (tok_b)
+          const float ta = (float)(t_w + tok_a), tb = (float)(t_w + tok_b);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          uint32_t a[4];
-          ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
-          mma_16816<T>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
+          for (int kk = 0; kk < D / 32; ++kk) {
+            uint32_t a[4], h[4];
+            ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
+            ldsm_x4(ktile + swz_off(r0 + row, (kk + D / 32) * 2 + csel, TS), h);
+            const float4 r0 = __ldg(rope_rates + (kk * 16 + tig * 2) / 2);
+            const float4 r1 = __ldg(rope_rates + (kk * 16 + 8 + tig * 2) / 2);
+            rope_pair<TQ>(a[0], h[0], ta, r0);
+            rope_pair<TQ>(a[1], h[1], tb, r0);
+            rope_pair<TQ>(a[2], h[2], ta, r1);
+            rope_pair<TQ>(a[3], h[3], tb, r1);
+            mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
+            mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
+            mma_16816<TQK>((kk & 1) ? c2 : c, a, qb[kk][0], qb[kk][1]);
+          }
         }
       }
 #pragma unroll
@@ -498,7 +594,8 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = e >= 2 ? tok_b : tok_a;
-        const float sv = score_log2(c[e], scale_qk, cap_log2);
+        const float bias = ((e & 1) ? slope1 : slope0) * (float)(t_w + t - b.it.q_pos);
+        const float sv = score_log2(c[e], scale_qk, bias, cap_log2);
         sc[e] = (t >= vlo && t < vhi) ? sv : kNegInf;
       }
       // The reference m2 of a column only moves when one of its scores exceeds it by more
@@ -705,6 +802,7 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
   const float cap_log2 = p.cap_log2;
   const int my_g = lane % GP;
   const int my_j = lane / GP;
+  const float slope = alibi_slope<D>(p, b.g0 + min(my_g, b.gcnt - 1));
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
@@ -747,7 +845,8 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
         }
       }
       const int r = r0 + my_j;
-      float sv = score_log2(part[0], scale_qk, cap_log2);
+      const float bias = slope * (float)(t_w + r - b.it.q_pos);
+      float sv = score_log2(part[0], scale_qk, bias, cap_log2);
       sv = (r >= vlo && r < vhi) ? sv : kNegInf;
       float mx = sv;
 #pragma unroll
@@ -802,8 +901,9 @@ __device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane
 }
 
 // ------------------------------------------------------------------------------ kernel
-// KIND: kTensorCore (HEADS = 8 qo heads per CTA) or kCudaCore (HEADS = GP).
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
+// KIND: kTensorCore (HEADS = 8 qo heads per CTA) or kCudaCore (HEADS = GP).  ROPE: the
+// tensor-core kernel with ROPE_LLAMA applied to q and K.
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP, bool ROPE = false>
 __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREADS,
                                   KIND == kTensorCore ? 2 : 1)
     decode_paged_kernel(const __grid_constant__ DecodeParams p) {
@@ -856,8 +956,8 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
     float acc[D / 16][4];
 #pragma unroll
     for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
-    consume_tc<TQ, KV_FP8, D, TS, NSTAGES>(p, b, smem, full0, empty0, abort_flag, warp, lane, m2,
-                                           lsum, acc);
+    consume_tc<TQ, KV_FP8, D, TS, NSTAGES, ROPE>(p, b, smem, full0, empty0, abort_flag, warp,
+                                                 lane, m2, lsum, acc);
     named_bar_sync(1, G::NCONS);  // every consumer is done with the stages
     stash_tc<D, KV_FP8>(epi, warp, lane, m2, lsum, acc);
   } else {
@@ -879,7 +979,7 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
 }
 
 // ------------------------------------------------------------------------------ registry
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP>
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP, bool ROPE = false>
 DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   DecodeKernel k;
@@ -888,7 +988,9 @@ DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   k.kv_dtype = kv_dtype;
   k.head_dim = D;
   k.heads_per_cta = KIND == kTensorCore ? 8 : GP;
-  k.fn = reinterpret_cast<const void*>(&decode_paged_kernel<TQ, KV_FP8, D, TS, NSTAGES, KIND, GP>);
+  k.fn = reinterpret_cast<const void*>(
+      &decode_paged_kernel<TQ, KV_FP8, D, TS, NSTAGES, KIND, GP, ROPE>);
+  k.rope = ROPE ? 1 : 0;
   k.threads = G::THREADS;
   k.smem_bytes = G::SMEM_BYTES;
   k.tile_tokens = TS;

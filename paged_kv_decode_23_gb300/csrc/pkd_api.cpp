@@ -42,17 +42,28 @@ void init_registry() {
     register_decode_f16(g_decode);
     register_decode_bf16(g_decode);
     register_decode_e4m3(g_decode);
+    register_decode_rope(g_decode);
     register_merge(g_merge);
   });
 }
 
-const DecodeKernel* find_decode(int kind, int q_dtype, int kv_dtype, int head_dim, int heads) {
+const DecodeKernel* find_decode(int kind, int q_dtype, int kv_dtype, int head_dim, int heads,
+                                int rope) {
   init_registry();
   for (const auto& k : g_decode)
     if (k.kind == kind && k.q_dtype == q_dtype && k.kv_dtype == kv_dtype &&
-        k.head_dim == head_dim && k.heads_per_cta == heads)
+        k.head_dim == head_dim && k.heads_per_cta == heads && k.rope == rope)
       return &k;
   return nullptr;
+}
+
+// ALiBi slope of qo head g of H heads (the ALiBi paper's set): with m the largest power of two
+// <= H, heads below m take 2^(-8 (g + 1) / m); the others take the odd-indexed slopes of the
+// 2m-head sequence, 2^(-4 (2 (g - m) + 1) / m).
+double alibi_slope_of(int g, int H) {
+  int m = 1;
+  while (2 * m <= H) m *= 2;
+  return g < m ? std::exp2(-8.0 * (g + 1) / m) : std::exp2(-4.0 * (2 * (g - m) + 1) / m);
 }
 
 const MergeKernel* find_merge(int o_dtype, int head_dim) {
@@ -101,6 +112,7 @@ struct pkd_handle {
   Plan plan;
   int batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, page_size = 0;
   int q_len = 1;  // query tokens per request: q / o / lse have batch * q_len rows
+  int pos_mode = 0;  // PKD_POS_*
   int q_dtype = 0, kv_dtype = 0, o_dtype = 0;
   float sm_scale = 0.f, cap = 0.f;
   const int32_t* indices = nullptr;
@@ -340,7 +352,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
              int num_kv_heads, int head_dim, int page_size, float sm_scale, float logits_soft_cap,
              int window_left, int fixed_split_size, int disable_split_kv, int q_dtype,
              int kv_dtype, int o_dtype, int use_tensor_cores, int q_len_per_req,
-             void* stream) {
+             int pos_encoding_mode, float rope_scale, float rope_theta, void* stream) {
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
   h->planned = false;
   if (q_dtype != PKD_DTYPE_F16 && q_dtype != PKD_DTYPE_BF16)
@@ -355,6 +367,13 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     return fail(PKD_ERR_INVALID_ARG, "sm_scale must be positive and finite, or NaN for the default");
   if (!std::isfinite(logits_soft_cap))
     return fail(PKD_ERR_INVALID_ARG, "logits_soft_cap must be finite");
+  if (pos_encoding_mode != PKD_POS_NONE && pos_encoding_mode != PKD_POS_ROPE_LLAMA &&
+      pos_encoding_mode != PKD_POS_ALIBI)
+    return fail(PKD_ERR_INVALID_ARG, "pos_encoding_mode must be PKD_POS_NONE, _ROPE_LLAMA or _ALIBI");
+  if (pos_encoding_mode == PKD_POS_ROPE_LLAMA &&
+      !(rope_scale > 0.f && std::isfinite(rope_scale) && rope_theta > 0.f &&
+        std::isfinite(rope_theta)))
+    return fail(PKD_ERR_INVALID_ARG, "rope_scale and rope_theta must be positive and finite");
 
   if (h->graph) {
     if (batch < 1 || batch > h->g_max_batch)
@@ -377,19 +396,22 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
                              q_len_per_req);
   if (rc) return rc;
   if (h->graph) r.max_items = h->g_max_items;
+  r.rope = pos_encoding_mode == PKD_POS_ROPE_LLAMA ? 1 : 0;
   Plan plan;
   const char* err = "";
   rc = build_plan(r, &plan, &err);
   if (rc) return fail(rc, err);
 
-  const DecodeKernel* k = find_decode(plan.kind, q_dtype, kv_dtype, head_dim, plan.heads_per_cta);
+  const DecodeKernel* k =
+      find_decode(plan.kind, q_dtype, kv_dtype, head_dim, plan.heads_per_cta, r.rope);
   if (!k) return fail(PKD_ERR_UNSUPPORTED, "no decode kernel built for this dtype / head_dim");
   const MergeKernel* mk = find_merge(o_dtype, head_dim);
   if (!plan.merges.empty() && !mk)
     return fail(PKD_ERR_UNSUPPORTED, "no merge kernel built for this dtype / head_dim");
 
-  const WsLayout lay = h->graph ? capacity_layout(h->g_max_items, num_kv_heads, plan.gslices)
-                                : layout_of(plan, num_kv_heads);
+  WsLayout lay = h->graph ? capacity_layout(h->g_max_items, num_kv_heads, plan.gslices)
+                          : layout_of(plan, num_kv_heads);
+  if (pos_encoding_mode != PKD_POS_NONE) lay.pos_floats = (size_t)head_dim + num_qo_heads;
   const size_t need_f = float_ws_bytes_of(lay, num_qo_heads, head_dim);
   const size_t need_i = int_ws_bytes_of(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
@@ -411,7 +433,9 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   const size_t merges_off = merges_offset(lay);
   const size_t items_b = plan.items.size() * sizeof(WorkItem);
   const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
-  const size_t img_bytes = merges_off + merges_b;
+  const size_t pos_off = pos_table_offset(lay);
+  const size_t img_bytes = lay.pos_floats ? pos_off + lay.pos_floats * sizeof(float)
+                                          : merges_off + merges_b;
   const size_t table_b = h->graph ? (size_t)(2 * batch + 1) * sizeof(int32_t) : 0;
   const size_t bytes = img_bytes + table_b;
   if (h->staging_pending) {
@@ -436,6 +460,24 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   }
   if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
   if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
+  if (lay.pos_floats) {
+    // [head_dim / 2] x {hi, lo}: the RoPE angle rate theta^(-2i/D) / rope_scale of dim pair i
+    // as a float pair; then [num_qo_heads] ALiBi slopes in score units (per unit of t - pos)
+    float* tbl = reinterpret_cast<float*>(img + pos_off);
+    std::memset(tbl, 0, lay.pos_floats * sizeof(float));
+    if (pos_encoding_mode == PKD_POS_ROPE_LLAMA) {
+      for (int i = 0; i < head_dim / 2; ++i) {
+        const double rate = std::pow((double)rope_theta, -2.0 * i / head_dim) / rope_scale;
+        const float hi = (float)rate;
+        tbl[2 * i] = hi;
+        tbl[2 * i + 1] = (float)(rate - (double)hi);
+      }
+    } else {
+      const double unit = logits_soft_cap > 0.f ? 1.0 / logits_soft_cap : 1.4426950408889634;
+      for (int g = 0; g < num_qo_heads; ++g)
+        tbl[head_dim + g] = (float)(alibi_slope_of(g, num_qo_heads) * unit);
+    }
+  }
   e = cudaMemcpyAsync(h->int_ws, img, img_bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
   if (h->graph) {
@@ -473,6 +515,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   h->ws_layout = lay;
   if (h->graph) h->g_batch = batch;
   h->kernel = k;
+  h->pos_mode = pos_encoding_mode;
   h->merge = mk;
   h->planned = true;
   g_last_error.clear();
@@ -526,6 +569,9 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(lay));
   prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
   prm.item_count = h->graph ? reinterpret_cast<const int32_t*>(iws + kItemCountOffset) : nullptr;
+  prm.pos_table =
+      lay.pos_floats ? reinterpret_cast<const float*>(iws + pos_table_offset(lay)) : nullptr;
+  prm.alibi = h->pos_mode == PKD_POS_ALIBI ? 1 : 0;
   prm.fuse_merge = 1;
   prm.indices = h->indices;
   prm.q = q;

@@ -217,6 +217,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t v) {
   return out;
 }
 
+// sin and cos of the RoPE angle t * rate, where rate = hi + lo is a double held as a float
+// pair and t an integer position (exact as a float below 2^24).  The product is kept exact
+// (t * hi rounded, its rounding error by FMA, plus t * lo), the nearest multiple of 2*pi is
+// removed in two parts (Cody and Waite's reduction, 2*pi = 6.28125 + 0.0019353071795864769),
+// and only the reduced angle, within about [-pi, pi], goes to the fast sine and cosine.
+// Angle error about 1e-6 rad for positions below 2^24.
+__device__ __forceinline__ void rope_sincos(float t, float hi, float lo, float& s, float& c) {
+  const float p = t * hi;
+  const float e = fmaf(t, hi, -p) + t * lo;
+  const float k = rintf(p * 0.15915494309189535f);
+  float r = fmaf(-k, 6.28125f, p);
+  r = fmaf(-k, 0.0019353071795864769f, r);
+  __sincosf(r + e, &s, &c);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

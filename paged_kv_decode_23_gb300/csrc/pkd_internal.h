@@ -23,7 +23,7 @@ struct WorkItem {
   int32_t tok_end;
   int32_t out_slot;
   int32_t merge_idx;   // index of the request's MergeEntry when out_slot >= 0, else -1
-  int32_t pad1;
+  int32_t q_pos;       // the row's query position (its last key, n - 1): ALiBi / RoPE
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
 
@@ -56,6 +56,11 @@ struct DecodeParams {
   uint32_t* counters;   // with fuse_merge: finished chunks per (merge entry, kv head, slice)
   const int32_t* item_count;  // CUDA-graph mode: the plan's work-item count, read on the device
                               // (the grid is cut for a fixed capacity); null: the grid is exact
+  // Positional-encoding table (plan's pos_encoding_mode), in the int workspace, 256-byte
+  // aligned: [head_dim / 2] x {hi, lo} RoPE angle rates (rope_theta^(-2i/D) / rope_scale as a
+  // float pair), then [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
+  const float* pos_table;
+  int alibi;            // 1: add pos_table[qo head] * (t - q_pos) to every logit
   int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
   int num_qo_heads;
   int num_kv_heads;
@@ -91,6 +96,7 @@ struct DecodeKernel {
   int threads;
   int smem_bytes;   // dynamic shared memory
   int tile_tokens;  // tokens per pipeline stage
+  int rope;         // 1: rotates q and K (ROPE_LLAMA) before the QK product
 };
 
 struct MergeKernel {
@@ -105,6 +111,7 @@ struct MergeKernel {
 void register_decode_f16(std::vector<DecodeKernel>& out);
 void register_decode_bf16(std::vector<DecodeKernel>& out);
 void register_decode_e4m3(std::vector<DecodeKernel>& out);
+void register_decode_rope(std::vector<DecodeKernel>& out);
 void register_merge(std::vector<MergeKernel>& out);
 
 // ----------------------------------------------------------------------------- planner
@@ -124,6 +131,7 @@ struct PlanRequest {
   int num_sms;
   int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode)
   int q_len = 1;         // query tokens per request (run's q_len_per_req)
+  int rope = 0;          // 1: ROPE_LLAMA (only the tensor-core kernel is built for it)
 };
 
 struct Plan {
@@ -151,16 +159,17 @@ struct WsLayout {
   size_t items;
   size_t merges;
   size_t slots;     // split partials
+  size_t pos_floats = 0;  // positional-encoding table (num_qo_heads + head_dim floats, or 0)
 };
 inline WsLayout layout_of(const Plan& p, int num_kv_heads) {
   return {p.merges.size() * (size_t)num_kv_heads * p.gslices, p.items.size(), p.merges.size(),
-          (size_t)p.num_slots};
+          (size_t)p.num_slots, 0};
 }
 // A work list of at most max_items items has at most max_items / 2 split requests (each has
 // two or more chunks) and at most max_items partial slots.
 inline WsLayout capacity_layout(size_t max_items, int num_kv_heads, int gslices) {
   const size_t merges = max_items / 2;
-  return {merges * (size_t)num_kv_heads * gslices, max_items, merges, max_items};
+  return {merges * (size_t)num_kv_heads * gslices, max_items, merges, max_items, 0};
 }
 // int workspace: [status block | merge counters | work items | merge entries]; plan() writes
 // everything up to the end of the merge entries in one upload (counters zeroed).
@@ -168,8 +177,11 @@ inline size_t items_offset(const WsLayout& l) {
   return kStatusBytes + (l.counters * 4 + 255) / 256 * 256;
 }
 inline size_t merges_offset(const WsLayout& l) { return items_offset(l) + l.items * sizeof(WorkItem); }
+inline size_t pos_table_offset(const WsLayout& l) {
+  return (merges_offset(l) + l.merges * sizeof(MergeEntry) + 255) / 256 * 256;
+}
 inline size_t int_ws_bytes_of(const WsLayout& l) {
-  return merges_offset(l) + l.merges * sizeof(MergeEntry) + 256;
+  return pos_table_offset(l) + l.pos_floats * sizeof(float) + 256;
 }
 // float workspace: [part_o (slots x Hq x D) | part_lse (slots x Hq)], each 256-byte aligned
 inline size_t part_lse_offset(const WsLayout& l, int num_qo_heads, int head_dim) {

@@ -82,6 +82,10 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     plan->heads_per_cta = gp;
   }
   plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
+  if (r.rope && plan->kind == kCudaCore) {
+    *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
+    return kErrUnsupported;
+  }
   plan->tile_tokens = tile_tokens_for(r.head_dim, r.kv_dtype);
 
   // per-request lengths
@@ -200,6 +204,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     it.req = i;  // the output row
     it.page_base = base[i];
     it.merge_idx = -1;
+    it.q_pos = n[i] > 0 ? (int32_t)(n[i] - 1) : 0;
     if (n[i] == 0) {
       it.chunk_tok0 = 0;
       it.tok_begin = 0;

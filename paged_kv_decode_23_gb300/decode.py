@@ -45,6 +45,9 @@ def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
+_POS_CODE = {"NONE": 0, "ROPE_LLAMA": 1, "ALIBI": 2}
+
+
 def _graph_buffer(t, name: str, need: int) -> torch.Tensor:
     if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
             and t.is_contiguous()):
@@ -137,15 +140,19 @@ class BatchDecodePagedKV:
              sm_scale: Optional[float] = None, non_blocking: bool = True,
              fixed_split_size: Optional[int] = None, disable_split_kv: bool = False,
              use_tensor_cores: Optional[bool] = None, stream=None,
-             q_len_per_req: int = 1) -> None:
+             q_len_per_req: int = 1, rope_scale: Optional[float] = None,
+             rope_theta: Optional[float] = None) -> None:
         """Plan a batch; ``indptr`` / ``last_page_len`` may live on the host or the device
         (a device copy is read back once here), ``indices`` must be a CUDA int32 tensor and
         stay unchanged while runs of this plan are in flight.  ``q_len_per_req`` query tokens
         per request (run's parameter of that name; the work list depends on it, so it is fixed
         here): the request's last positions, each attending causally; q / o then have
-        ``batch * q_len_per_req`` rows, request-major."""
-        if pos_encoding_mode != "NONE":
-            raise NotImplementedError("only pos_encoding_mode='NONE' is implemented")
+        ``batch * q_len_per_req`` rows, request-major.  ``pos_encoding_mode``: "NONE",
+        "ROPE_LLAMA" (with ``rope_scale`` / ``rope_theta``, defaults 1 and 1e4; tensor-core
+        kernel only) or "ALIBI"."""
+        pos_code = _POS_CODE.get(pos_encoding_mode)
+        if pos_code is None:
+            raise ValueError("pos_encoding_mode must be 'NONE', 'ROPE_LLAMA' or 'ALIBI'")
         if data_type is not None:
             q_data_type = data_type
         q_dt = _as_dtype(q_data_type)
@@ -167,7 +174,9 @@ class BatchDecodePagedKV:
             num_qo_heads, num_kv_heads, head_dim, page_size, sm,
             float(logits_soft_cap or 0.0), int(window_left), int(fixed_split_size or 0),
             int(bool(disable_split_kv)), _DTYPE_CODE[q_dt], _DTYPE_CODE[kv_dt], _DTYPE_CODE[o_dt],
-            kernel, int(q_len_per_req), _stream_ptr(stream)))
+            kernel, int(q_len_per_req), pos_code,
+            1.0 if rope_scale is None else float(rope_scale),
+            1e4 if rope_theta is None else float(rope_theta), _stream_ptr(stream)))
         self._indices = indices
         self._plan_args = dict(batch=batch, q_len=int(q_len_per_req),
                                num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,

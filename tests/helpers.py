@@ -52,12 +52,13 @@ def run_gpu(w: W.Workload, q: torch.Tensor, pool, dec=None, **plan_over):
 
 
 def run_oracle(w: W.Workload, q: torch.Tensor, pool: torch.Tensor, chunk_tokens: int = 0,
-               q_len: int = 1):
+               q_len: int = 1, **pos):
+    """``pos``: pos_encoding_mode / rope_scale / rope_theta, passed to the oracle."""
     return oracle.batch_decode_pool(
         w.indptr, w.indices, w.last_page_len, W.raw_bits(q.cpu()), ORACLE_CODE[w.q_dtype],
         W.raw_bits(pool.cpu()), ORACLE_CODE[w.kv_dtype], w.layout, sm_scale=w.sm_scale,
         logits_soft_cap=w.logits_soft_cap, window_left=w.window_left, k_scale=w.k_scale,
-        v_scale=w.v_scale, chunk_tokens=chunk_tokens, q_len=q_len)
+        v_scale=w.v_scale, chunk_tokens=chunk_tokens, q_len=q_len, **pos)
 
 
 def assert_close(w: W.Workload, got, ref, what=""):

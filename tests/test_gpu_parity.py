@@ -275,3 +275,55 @@ def test_several_query_tokens_per_request(q_len, kv, tc):
                       fixed_split_size=mode.get("fixed_split_size"))
         assert_close(w, got, run_oracle(w, q, pool, q_len=q_len),
                      f"q_len {q_len} {kv} tc={tc} {mode}")
+
+
+@pytest.mark.parametrize("kv", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("tc", [True, False])
+def test_alibi(kv, tc):
+    """pos_encoding_mode ALIBI: slope_g * (t - pos) added to every logit (qo heads 12: slopes
+    beyond the largest power of two), with a split, a window and several query tokens."""
+    lens = [1, 40, 300, 1200, 0, 2600]
+    w, q, pool = _case(lens, 12, 3, 128, 16, "NHD", "bf16" if kv == "e4m3" else kv, kv=kv,
+                       seed=41, window_left=700, logits_soft_cap=20.0 if kv == "e4m3" else 0.0)
+    for q_len in (1, 2):
+        qq = q if q_len == 1 else torch.cat([q, q * 0.5]).reshape(2, -1, 12, 128).transpose(0, 1) \
+            .reshape(-1, 12, 128).contiguous()
+        got = run_gpu(w, qq, pool, use_tensor_cores=tc, pos_encoding_mode="ALIBI",
+                      q_len_per_req=q_len, fixed_split_size=8 if q_len == 2 else None)
+        assert_close(w, got, run_oracle(w, qq, pool, q_len=q_len, pos_encoding_mode="ALIBI"),
+                     f"alibi {kv} tc={tc} q_len={q_len}")
+
+
+@pytest.mark.parametrize("kv,d", [("f16", 64), ("bf16", 128), ("bf16", 256), ("f16", 256),
+                                  ("e4m3", 128), ("e4m3", 256)])
+def test_rope_llama(kv, d):
+    """pos_encoding_mode ROPE_LLAMA (tensor-core kernel): q rotated at its position, every key
+    at its index; non-default theta and scale; a split, a window, a soft cap and two query
+    tokens per request on the second pass."""
+    lens = [1, 17, 333, 1500, 0, 4100]
+    qdt = "bf16" if kv == "e4m3" else kv
+    w, q, pool = _case(lens, 16, 2, d, 32, "NHD", qdt, kv=kv, seed=d + 5, window_left=2000,
+                       logits_soft_cap=30.0)
+    for q_len, theta, scale in ((1, 1e4, 1.0), (2, 5e5, 4.0)):
+        qq = q.repeat_interleave(q_len, dim=0).contiguous()
+        pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=theta, rope_scale=scale)
+        got = run_gpu(w, qq, pool, q_len_per_req=q_len, **pos)
+        assert_close(w, got, run_oracle(w, qq, pool, q_len=q_len, **pos),
+                     f"rope {kv} D{d} q_len={q_len} theta={theta}")
+
+
+def test_rope_long_positions_keep_precision():
+    """Positions up to ~20k: the kernel's reduced-angle sine / cosine must track the fp64
+    oracle (an fp32 angle t * rate alone would drift by ~1e-3 rad there)."""
+    w, q, pool = _case([20000, 9000], 8, 1, 128, 64, "HND", "bf16", seed=77)
+    pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=1e4, rope_scale=1.0)
+    got = run_gpu(w, q, pool, **pos)
+    assert_close(w, got, run_oracle(w, q, pool, **pos), "rope long positions")
+
+
+def test_rope_on_cuda_cores_is_refused():
+    from paged_kv_decode_23_gb300 import PkdError
+    w, q, pool = _case([40], 8, 2, 128, 16, seed=1)
+    with pytest.raises(PkdError) as e:
+        gpu_decoder(w, use_tensor_cores=False, pos_encoding_mode="ROPE_LLAMA")
+    assert e.value.code == -5
