@@ -237,7 +237,9 @@ def reference_arm(args, w):
 
 
 def config_of(w, args):
-    return {"workload": describe(w), "batch": w.batch, "layers": w.layers,
+    extra = {} if getattr(args, "pos_encoding", "NONE") == "NONE" else \
+        {"pos_encoding_mode": args.pos_encoding}
+    return {"workload": describe(w), **extra, "batch": w.batch, "layers": w.layers,
             "kv_tokens": int(np.sum(w.kv_lens)),
             "l2": "inputs larger than L2 (each call streams its own pool)"
             if algorithmic_bytes(w) > 4 * L2_BYTES else
@@ -274,6 +276,8 @@ def gpu_arm(args, w, rank, world):
                    logits_soft_cap=w.logits_soft_cap or None, window_left=w.window_left,
                    fixed_split_size=w.fixed_split_size or None,
                    disable_split_kv=w.disable_split_kv)
+    if args.pos_encoding != "NONE":
+        plan_kw["pos_encoding_mode"] = args.pos_encoding
     if args.kernel != "auto":
         plan_kw["use_tensor_cores"] = args.kernel == "tc"
     flush = None
@@ -428,7 +432,9 @@ def gpu_arm(args, w, rank, world):
         "peak_kind": peak_kind,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": args.traffic if args.traffic is not None else measured_traffic(w.name),
+                     "traffic": args.traffic if args.traffic is not None else
+                     measured_traffic(w.name) if (args.kernel, args.pos_encoding) == ("auto", "NONE")
+                     else None,
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": {"value": world * bytes_step / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
@@ -453,6 +459,8 @@ def main():
                     choices=["worked", "uniform", "lognormal", "long", "mix"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
+    ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
+                    help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -317,19 +317,35 @@ __device__ __forceinline__ float score_log2(float dot, float scale_qk, float bia
 // ALiBi slope of a qo head, in score units (0 without ALiBi).
 template <int D>
 __device__ __forceinline__ float alibi_slope(const DecodeParams& p, int qo_head) {
-  return p.alibi ? __ldg(p.pos_table + D + qo_head) : 0.f;
+  return p.alibi ? __ldg(p.pos_table + 2 * D + qo_head) : 0.f;
 }
 
-// ROPE_LLAMA on two 16-bit pairs held in registers: lo holds dims (i, i+1) and hi the partner
-// dims (i + D/2, i + D/2 + 1), of a token at position t; rates points at rate pairs {hi, lo}
-// of dims i, i+1.  x' = x cos a - y sin a, y' = y cos a + x sin a, rounded to fp16.
+// RoPE angle of dims i and i+1 at positions t (row a) and t + 8 (row b), as cos / sin: the
+// row-a angles come reduced from rope_sincos; row b's follow by the fixed rotation by 8 * rate
+// (cos and sin of it from the table: rate entry = {rate hi, rate lo, cos 8 rate, sin 8 rate}).
+struct RopeCS {
+  float c[2][2], s[2][2];  // [row a | row b][dim i | i+1]
+};
+__device__ __forceinline__ RopeCS rope_cs(float t, float4 ri, float4 rj) {
+  using namespace dev;
+  RopeCS r;
+  rope_sincos(t, ri.x, ri.y, r.s[0][0], r.c[0][0]);
+  rope_sincos(t, rj.x, rj.y, r.s[0][1], r.c[0][1]);
+  r.c[1][0] = r.c[0][0] * ri.z - r.s[0][0] * ri.w;
+  r.s[1][0] = r.s[0][0] * ri.z + r.c[0][0] * ri.w;
+  r.c[1][1] = r.c[0][1] * rj.z - r.s[0][1] * rj.w;
+  r.s[1][1] = r.s[0][1] * rj.z + r.c[0][1] * rj.w;
+  return r;
+}
+
+// ROPE_LLAMA on a 16-bit pair held in registers: lo holds dims (i, i+1) and hi the partner
+// dims (i + D/2, i + D/2 + 1) of one token (row 0 or 1 of cs).  x' = x cos a - y sin a,
+// y' = y cos a + x sin a, rounded to fp16.
 template <typename TIN>
-__device__ __forceinline__ void rope_pair(uint32_t& lo, uint32_t& hi, float t, float4 rates) {
+__device__ __forceinline__ void rope_pair(uint32_t& lo, uint32_t& hi, const RopeCS& cs, int row) {
   using namespace dev;
   const float2 x = unpack2<TIN>(lo), y = unpack2<TIN>(hi);
-  float s0, c0, s1, c1;
-  rope_sincos(t, rates.x, rates.y, s0, c0);
-  rope_sincos(t, rates.z, rates.w, s1, c1);
+  const float c0 = cs.c[row][0], s0 = cs.s[row][0], c1 = cs.c[row][1], s1 = cs.s[row][1];
   lo = pack2<__half>(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
   hi = pack2<__half>(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
 }
@@ -381,10 +397,10 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = kk * 16 + (h ? off1 : off0);  // dims i, i+1; partners i + D/2, i + D/2 + 1
-          const float4 r = __ldg(rates + i / 2);
+          const float4 ri = __ldg(rates + i), rj = __ldg(rates + i + 1);
           float s0, c0, s1, c1;
-          rope_sincos(pos, r.x, r.y, s0, c0);
-          rope_sincos(pos, r.z, r.w, s1, c1);
+          rope_sincos(pos, ri.x, ri.y, s0, c0);
+          rope_sincos(pos, rj.x, rj.y, s1, c1);
           const float2 x = f[kk][h], y = f[kk + D / 32][h];
           f[kk][h] = make_float2(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
           f[kk + D / 32][h] = make_float2(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
@@ -534,18 +550,19 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
           e4m3x4_to_half2x2(wb, a[1], a[3]);
         };
         if constexpr (ROPE) {
-          const float ta = (float)(t_w + tok_a), tb = (float)(t_w + tok_b);
+          const float ta = (float)(t_w + tok_a);  // row b (tok_b) is ta + 8
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
             uint32_t a[4], h[4];  // k steps kk and kk + D/32: dims i and i + D/2
             load_k(kk, a);
             load_k(kk + D / 32, h);
-            const float4 r0 = __ldg(rope_rates + (kk * 16 + tig * 4) / 2);
-            const float4 r1 = __ldg(rope_rates + (kk * 16 + tig * 4 + 2) / 2);
-            rope_pair<__half>(a[0], h[0], ta, r0);
-            rope_pair<__half>(a[1], h[1], tb, r0);
-            rope_pair<__half>(a[2], h[2], ta, r1);
-            rope_pair<__half>(a[3], h[3], tb, r1);
+            const int i0 = kk * 16 + tig * 4;  // a[0]/a[1]: dims i0, i0+1; a[2]/a[3]: +2, +3
+            const RopeCS cs0 = rope_cs(ta, __ldg(rope_rates + i0), __ldg(rope_rates + i0 + 1));
+            const RopeCS cs1 = rope_cs(ta, __ldg(rope_rates + i0 + 2), __ldg(rope_rates + i0 + 3));
+            rope_pair<__half>(a[0], h[0], cs0, 0);
+            rope_pair<__half>(a[1], h[1], cs0, 1);
+            rope_pair<__half>(a[2], h[2], cs1, 0);
+            rope_pair<__half>(a[3], h[3], cs1, 1);
             mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
             mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
           }
@@ -563,18 +580,19 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
         if constexpr (ROPE) {
           // ldmatrix: a[0] / a[2] are row g_row (token tok_a), dims 16kk + 2tig (+1) and
           // 16kk + 8 + 2tig (+1); a[1] / a[3] the same dims of row g_row + 8 (tok_b)
-          const float ta = (float)(t_w + tok_a), tb = (float)(t_w + tok_b);
+          const float ta = (float)(t_w + tok_a);  // row b (tok_b) is ta + 8
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
             uint32_t a[4], h[4];
             ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
             ldsm_x4(ktile + swz_off(r0 + row, (kk + D / 32) * 2 + csel, TS), h);
-            const float4 r0 = __ldg(rope_rates + (kk * 16 + tig * 2) / 2);
-            const float4 r1 = __ldg(rope_rates + (kk * 16 + 8 + tig * 2) / 2);
-            rope_pair<TQ>(a[0], h[0], ta, r0);
-            rope_pair<TQ>(a[1], h[1], tb, r0);
-            rope_pair<TQ>(a[2], h[2], ta, r1);
-            rope_pair<TQ>(a[3], h[3], tb, r1);
+            const int i0 = kk * 16 + tig * 2, i1 = i0 + 8;
+            const RopeCS cs0 = rope_cs(ta, __ldg(rope_rates + i0), __ldg(rope_rates + i0 + 1));
+            const RopeCS cs1 = rope_cs(ta, __ldg(rope_rates + i1), __ldg(rope_rates + i1 + 1));
+            rope_pair<TQ>(a[0], h[0], cs0, 0);
+            rope_pair<TQ>(a[1], h[1], cs0, 1);
+            rope_pair<TQ>(a[2], h[2], cs1, 0);
+            rope_pair<TQ>(a[3], h[3], cs1, 1);
             mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
             mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
           }

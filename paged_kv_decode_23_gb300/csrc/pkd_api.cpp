@@ -411,7 +411,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
 
   WsLayout lay = h->graph ? capacity_layout(h->g_max_items, num_kv_heads, plan.gslices)
                           : layout_of(plan, num_kv_heads);
-  if (pos_encoding_mode != PKD_POS_NONE) lay.pos_floats = (size_t)head_dim + num_qo_heads;
+  if (pos_encoding_mode != PKD_POS_NONE) lay.pos_floats = 2 * (size_t)head_dim + num_qo_heads;
   const size_t need_f = float_ws_bytes_of(lay, num_qo_heads, head_dim);
   const size_t need_i = int_ws_bytes_of(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
@@ -461,21 +461,24 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
   if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
   if (lay.pos_floats) {
-    // [head_dim / 2] x {hi, lo}: the RoPE angle rate theta^(-2i/D) / rope_scale of dim pair i
-    // as a float pair; then [num_qo_heads] ALiBi slopes in score units (per unit of t - pos)
+    // [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate}: the RoPE angle rate
+    // theta^(-2i/D) / rope_scale of dim pair i as a float pair, and the rotation across 8
+    // positions; then [num_qo_heads] ALiBi slopes in score units (per unit of t - pos)
     float* tbl = reinterpret_cast<float*>(img + pos_off);
     std::memset(tbl, 0, lay.pos_floats * sizeof(float));
     if (pos_encoding_mode == PKD_POS_ROPE_LLAMA) {
       for (int i = 0; i < head_dim / 2; ++i) {
         const double rate = std::pow((double)rope_theta, -2.0 * i / head_dim) / rope_scale;
         const float hi = (float)rate;
-        tbl[2 * i] = hi;
-        tbl[2 * i + 1] = (float)(rate - (double)hi);
+        tbl[4 * i] = hi;
+        tbl[4 * i + 1] = (float)(rate - (double)hi);
+        tbl[4 * i + 2] = (float)std::cos(8.0 * rate);
+        tbl[4 * i + 3] = (float)std::sin(8.0 * rate);
       }
     } else {
       const double unit = logits_soft_cap > 0.f ? 1.0 / logits_soft_cap : 1.4426950408889634;
       for (int g = 0; g < num_qo_heads; ++g)
-        tbl[head_dim + g] = (float)(alibi_slope_of(g, num_qo_heads) * unit);
+        tbl[2 * head_dim + g] = (float)(alibi_slope_of(g, num_qo_heads) * unit);
     }
   }
   e = cudaMemcpyAsync(h->int_ws, img, img_bytes, cudaMemcpyHostToDevice, s);

@@ -57,8 +57,9 @@ struct DecodeParams {
   const int32_t* item_count;  // CUDA-graph mode: the plan's work-item count, read on the device
                               // (the grid is cut for a fixed capacity); null: the grid is exact
   // Positional-encoding table (plan's pos_encoding_mode), in the int workspace, 256-byte
-  // aligned: [head_dim / 2] x {hi, lo} RoPE angle rates (rope_theta^(-2i/D) / rope_scale as a
-  // float pair), then [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
+  // aligned: [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate} for the RoPE angle
+  // rate rope_theta^(-2i/D) / rope_scale (a float pair) and the rotation across 8 positions,
+  // then [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
   const float* pos_table;
   int alibi;            // 1: add pos_table[qo head] * (t - q_pos) to every logit
   int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
@@ -159,7 +160,7 @@ struct WsLayout {
   size_t items;
   size_t merges;
   size_t slots;     // split partials
-  size_t pos_floats = 0;  // positional-encoding table (num_qo_heads + head_dim floats, or 0)
+  size_t pos_floats = 0;  // positional-encoding table (2 head_dim + num_qo_heads floats, or 0)
 };
 inline WsLayout layout_of(const Plan& p, int num_kv_heads) {
   return {p.merges.size() * (size_t)num_kv_heads * p.gslices, p.items.size(), p.merges.size(),
