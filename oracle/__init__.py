@@ -90,6 +90,11 @@ def _load():
                 ctypes.c_double, ctypes.c_double, ctypes.c_double,
                 ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
                 vp, vp, ctypes.c_int]
+            lib.oracle_mla_decode.restype = ctypes.c_int
+            lib.oracle_mla_decode.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                i32p, i32p, i32p, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int,
+                ctypes.c_double, vp, vp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -210,3 +215,33 @@ def batch_decode_pool(indptr, indices, last_page_len, q_raw, q_dtype, pool_raw: 
     num_qo_heads = kw.pop("num_qo_heads", q_raw.shape[1])
     return batch_decode(indptr, indices, last_page_len, q_raw, q_dtype, base, v_base, kv_dtype,
                         strides, num_qo_heads, num_kv_heads, head_dim, page_size, **kw)
+
+
+def mla_decode(kv_indptr, kv_indices, kv_len, q_nope_raw: np.ndarray, q_pe_raw: np.ndarray,
+               q_dtype: int, ckv_raw: np.ndarray, kpe_raw: np.ndarray, kv_dtype: int,
+               page_size: int, sm_scale: float, num_threads: int = 0):
+    """MLA paged decode in fp64 (BatchMLAPagedAttentionWrapper): key = [ckv, kpe], value = ckv.
+
+    ``q_nope_raw`` ``[batch, H, Dc]`` and ``q_pe_raw`` ``[batch, H, Dp]``, ``ckv_raw``
+    ``[pages, page_size, Dc]`` and ``kpe_raw`` ``[pages, page_size, Dp]``: element bits.
+    Returns ``(o [batch, H, Dc] float64, lse [batch, H] float64, natural log)``.
+    """
+    kv_indptr = _i32(kv_indptr)
+    kv_indices = _i32(kv_indices) if len(kv_indices) else np.zeros(1, dtype=np.int32)
+    kv_len = _i32(kv_len)
+    q_nope_raw = np.ascontiguousarray(q_nope_raw)
+    q_pe_raw = np.ascontiguousarray(q_pe_raw)
+    ckv_raw = np.ascontiguousarray(ckv_raw)
+    kpe_raw = np.ascontiguousarray(kpe_raw)
+    batch, heads, dc = q_nope_raw.shape
+    dp = q_pe_raw.shape[2]
+    o = np.zeros((batch, heads, dc), dtype=np.float64)
+    lse = np.zeros((batch, heads), dtype=np.float64)
+    rc = _load().oracle_mla_decode(batch, heads, dc, dp, int(page_size), _ptr_i32(kv_indptr),
+                                   _ptr_i32(kv_indices), _ptr_i32(kv_len), q_nope_raw.ctypes.data,
+                                   q_pe_raw.ctypes.data, q_dtype, ckv_raw.ctypes.data,
+                                   kpe_raw.ctypes.data, kv_dtype, float(sm_scale),
+                                   o.ctypes.data, lse.ctypes.data, int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_mla_decode rejected the problem (code {rc})")
+    return o, lse

@@ -386,3 +386,80 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * MLA paged decode (FlashInfer attention API page, flashinfer.mla /
+ * BatchMLAPagedAttentionWrapper, plan() and run()).  With the matrix-absorption trick the
+ * page describes, every query head attends over one shared latent cache: the key of token t is
+ * the concatenation [ckv_t, kpe_t] (head_dim_ckv + head_dim_kpe) and its value is ckv_t.
+ *   q_nope [batch, H, Dc], q_pe [batch, H, Dp]; ckv_cache [pages, page_size, Dc],
+ *   kpe_cache [pages, page_size, Dp]; request i owns pages kv_indices[kv_indptr[i] ..] and
+ *   kv_len[i] tokens (token t in page kv_indices[kv_indptr[i] + t / page_size], slot
+ *   t % page_size).
+ *   logit_t = sm_scale * (<q_nope, ckv_t> + <q_pe, kpe_t>),  o = sum_t softmax(logit)_t ckv_t,
+ *   lse = ln sum_t exp(logit_t) (the caller converts to base 2, run()'s default).
+ * Decode: one query per request (qo_indptr = 0, 1, ..., batch); causal changes nothing then.
+ * ckv / kpe rows are contiguous: element (page, slot, d) at (page * page_size + slot) * D + d.
+ */
+int oracle_mla_decode(int batch, int num_heads, int dc, int dp, int page_size,
+                      const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_len,
+                      const void* q_nope, const void* q_pe, int q_dtype, const void* ckv,
+                      const void* kpe, int kv_dtype, double sm_scale, double* o, double* lse,
+                      int num_threads) {
+  if (batch < 0 || num_heads <= 0 || dc <= 0 || dp < 0 || page_size <= 0) return -1;
+  int64_t nmax = 1;
+  for (int i = 0; i < batch; ++i) {
+    if (kv_len[i] < 0) return -4;
+    const int64_t pages = (int64_t)kv_indptr[i + 1] - kv_indptr[i];
+    if (pages < 0 || (int64_t)kv_len[i] > pages * page_size) return -3;
+    if (kv_len[i] > nmax) nmax = kv_len[i];
+  }
+  const int64_t work = (int64_t)batch * num_heads;
+  int bad = 0;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel reduction(| : bad)
+#endif
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    if (!s) bad = 1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+      if (bad) continue;
+      const int i = (int)(w / num_heads);
+      const int64_t n = kv_len[i];
+      double* ow = o + w * dc;
+      for (int d = 0; d < dc; ++d) ow[d] = 0.0;
+      if (n == 0) {
+        lse[w] = -INFINITY;
+        continue;
+      }
+      double m = -INFINITY;
+      for (int64_t t = 0; t < n; ++t) {
+        const int64_t row = (int64_t)kv_indices[(int64_t)kv_indptr[i] + t / page_size] * page_size +
+                            t % page_size;
+        double dot = 0.0;
+        for (int d = 0; d < dc; ++d)
+          dot += load_elem(q_nope, w * dc + d, q_dtype) * load_elem(ckv, row * dc + d, kv_dtype);
+        for (int d = 0; d < dp; ++d)
+          dot += load_elem(q_pe, w * dp + d, q_dtype) * load_elem(kpe, row * dp + d, kv_dtype);
+        s[t] = sm_scale * dot;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < n; ++t) {
+        const int64_t row = (int64_t)kv_indices[(int64_t)kv_indptr[i] + t / page_size] * page_size +
+                            t % page_size;
+        const double p = exp(s[t] - m);
+        l += p;
+        for (int d = 0; d < dc; ++d) ow[d] += p * load_elem(ckv, row * dc + d, kv_dtype);
+      }
+      for (int d = 0; d < dc; ++d) ow[d] /= l;
+      lse[w] = m + log(l);
+    }
+    free(s);
+  }
+  return bad ? -5 : 0;
+}

@@ -5,8 +5,8 @@ oracle itself): a wrong GQA head map, an off-by-one window, a dropped max-subtra
 wrong lse, a soft cap without the division, swapped strides, a wrong kv-length rule, an
 unweighted merge, a missing v_scale, wrong fp16 / e4m3 decoders, and for several query tokens
 per request a causal limit one past the query, reversed token positions and token-major rows,
-and for the positional encodings a reversed RoPE rotation, a rope_scale that multiplies and an
-ALiBi bias of the wrong sign.  The pin suite in
+for the positional encodings a reversed RoPE rotation, a rope_scale that multiplies and an
+ALiBi bias of the wrong sign, and an MLA logit without its rope (kpe) part.  The pin suite in
 ``test_oracle_pins.py`` runs against each mutant and must fail.
 """
 import os
@@ -28,6 +28,8 @@ MUTANTS = {
     "rope_rotation_reversed": ("x[i] = x0 * c - x1 * s;", "x[i] = x0 * c + x1 * s;"),
     "rope_scale_multiplies": ("const double a = (pos / rope_scale)", "const double a = (pos * rope_scale)"),
     "alibi_distance_sign": ("slope * (double)(t - pos)", "slope * (double)(pos - t)"),
+    "mla_rope_part_dropped": ("dot += load_elem(q_pe, w * dp + d, q_dtype) * load_elem(kpe, row * dp + d, kv_dtype);",
+                              "dot += 0.0;"),
     "query_rows_token_major": ("(((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D",
                                "(((int64_t)j * p->batch + i) * p->num_qo_heads + g) * D"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),

@@ -541,3 +541,69 @@ def test_rejects_malformed_tables():
     bad[0] = 5                                  # last_page_len > page_size
     with pytest.raises(ValueError):
         _run_f64(ip, ix, bad, q, pool, "NHD")
+
+
+# ---------------------------------------------------------------- MLA decode
+
+def _mla_problem(rng, kv_lens, H, dc, dp, ps, extra_pages=5):
+    pages = [(n + ps - 1) // ps for n in kv_lens]
+    P = sum(pages) + extra_pages
+    perm = rng.permutation(P)
+    kv_indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    kv_indices = perm[:kv_indptr[-1]].astype(np.int32)
+    ckv = rng.standard_normal((P, ps, dc))
+    kpe = rng.standard_normal((P, ps, dp))
+    q_nope = rng.standard_normal((len(kv_lens), H, dc))
+    q_pe = rng.standard_normal((len(kv_lens), H, dp))
+    return kv_indptr, kv_indices, np.asarray(kv_lens, np.int32), q_nope, q_pe, ckv, kpe
+
+
+@pytest.mark.parametrize("case", [dict(kv_lens=[1, 7, 33, 0], H=4, dc=16, dp=8, ps=1),
+                                  dict(kv_lens=[50, 3], H=3, dc=32, dp=8, ps=4)])
+def test_mla_against_dense_latent_attention(case):
+    """Key = [ckv, kpe], value = ckv, one latent cache shared by every head (the page's
+    matrix-absorbed MLA), computed densely with numpy."""
+    rng = np.random.default_rng(123)
+    ip, ix, lens, qn, qp, ckv, kpe = _mla_problem(rng, case["kv_lens"], case["H"], case["dc"],
+                                                  case["dp"], case["ps"])
+    sm = 0.21
+    o, lse = oracle.mla_decode(ip, ix, lens, qn, qp, oracle.F64, ckv, kpe, oracle.F64,
+                               case["ps"], sm)
+    for i, n in enumerate(lens):
+        if n == 0:
+            assert np.all(o[i] == 0) and np.all(np.isneginf(lse[i]))
+            continue
+        t = np.arange(n)
+        rows = ix[ip[i] + t // case["ps"]], t % case["ps"]
+        C, Pe = ckv[rows], kpe[rows]          # [n, dc], [n, dp]
+        logits = sm * (qn[i] @ C.T + qp[i] @ Pe.T)
+        np.testing.assert_allclose(o[i], scipy.special.softmax(logits, axis=1) @ C, atol=1e-12)
+        np.testing.assert_allclose(lse[i], scipy.special.logsumexp(logits, axis=1), atol=1e-12)
+
+
+def test_mla_is_decode_with_one_concatenated_kv_head():
+    """MLA equals the (separately pinned) GQA decode oracle with one kv head of dim dc + dp,
+    K = [ckv, kpe], V = [ckv, 0], q = [q_nope, q_pe], on the first dc output dims."""
+    rng = np.random.default_rng(7)
+    H, dc, dp, ps = 4, 16, 8, 2
+    ip, ix, lens, qn, qp, ckv, kpe = _mla_problem(rng, [9, 1, 20], H, dc, dp, ps)
+    o, lse = oracle.mla_decode(ip, ix, lens, qn, qp, oracle.F64, ckv, kpe, oracle.F64, ps, 0.4)
+    P = ckv.shape[0]
+    pool = np.zeros((P, 2, ps, 1, dc + dp))
+    pool[:, 0, :, 0, :dc] = ckv
+    pool[:, 0, :, 0, dc:] = kpe
+    pool[:, 1, :, 0, :dc] = ckv
+    lpl = np.array([n - (ip[i + 1] - ip[i] - 1) * ps for i, n in enumerate(lens)], np.int32)
+    q = np.concatenate([qn, qp], axis=2)
+    o2, lse2 = _run_f64(ip, ix, lpl, q, pool, "NHD", sm_scale=0.4)
+    np.testing.assert_allclose(o, o2[:, :, :dc], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+def test_mla_single_token_returns_its_latent_row():
+    rng = np.random.default_rng(8)
+    ip, ix, lens, qn, qp, ckv, kpe = _mla_problem(rng, [1], 2, 8, 4, 1)
+    o, lse = oracle.mla_decode(ip, ix, lens, qn, qp, oracle.F64, ckv, kpe, oracle.F64, 1, 0.5)
+    row = ckv[ix[0], 0]
+    np.testing.assert_array_equal(o[0], np.stack([row, row]))
+    np.testing.assert_allclose(lse[0], 0.5 * (qn[0] @ row + qp[0] @ kpe[ix[0], 0]), atol=1e-13)
