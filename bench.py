@@ -449,6 +449,228 @@ def gpu_arm(args, w, rank, world):
     return res
 
 
+# ----------------------------------------------------------------------------- MLA
+def mla_bytes_flops(w):
+    """Algorithmic bytes (latent rows of every attended token, plus q and o) and flops
+    (QK over 576 dims and PV over 512, per head and token) of one MLA decode call."""
+    toks = int(np.sum(w.kv_lens))
+    kv = toks * (w.head_dim_ckv + w.head_dim_kpe) * 2
+    qo = w.batch * w.num_heads * (w.head_dim_ckv * 2 + w.head_dim_kpe) * 2
+    flops = toks * w.num_heads * (w.head_dim_ckv + w.head_dim_kpe + w.head_dim_ckv) * 2
+    return kv + qo, flops
+
+
+def mla_describe(w) -> str:
+    return (f"mla: batch {w.batch}, kv_len {int(w.kv_lens.min())}..{int(w.kv_lens.max())} "
+            f"(sum {int(np.sum(w.kv_lens))}), page {w.page_size}, {w.num_heads} heads, ckv 512 + "
+            f"kpe 64, {w.dtype}, sm_scale 1/sqrt(192) (the MLA wrapper's example)")
+
+
+def _mla_sample(w, budget_s: float):
+    """A bounded sample of the MLA workload for the CPU oracle (its first requests)."""
+    import oracle
+    import workloads as W
+    code = {"bf16": oracle.BF16, "f16": oracle.F16}[w.dtype]
+
+    def build(n):
+        sub = W.mla_custom(w.kv_lens[:n], w.num_heads, w.page_size, w.dtype, seed=w.seed + 1,
+                           pool_factor=1.0)
+        return sub, W.make_mla_q(sub), W.make_mla_cache(sub)
+
+    def run(sub, q, c):
+        t0 = time.perf_counter()
+        oracle.mla_decode(sub.kv_indptr, sub.kv_indices, sub.kv_lens, W.raw_bits(q[0]),
+                          W.raw_bits(q[1]), code, W.raw_bits(c[0]), W.raw_bits(c[1]), code,
+                          sub.page_size, sub.sm_scale)
+        return time.perf_counter() - t0
+
+    cal = build(1)
+    t1 = max(run(*cal), 1e-4)
+    n = int(max(1, min(w.batch, budget_s / t1)))
+    return build(n), run
+
+
+def mla_cpu_baseline(w, budget_s: float):
+    import oracle
+    (sub, q, c), run = _mla_sample(w, budget_s)
+    t = run(sub, q, c)
+    b, _ = mla_bytes_flops(sub)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{sub.batch} of {w.batch} requests ({int(np.sum(sub.kv_lens))} tokens), "
+                      f"fp64 MLA oracle, {t:.1f} s"}
+
+
+def mla_reference_arm(args, w):
+    import oracle
+    steps, warmup = args.steps, args.warmup
+    per_step = max(1.0, min(20.0, 150.0 / max(1, steps + warmup)))
+    (sub, q, c), run = _mla_sample(w, per_step)
+    for _ in range(warmup):
+        run(sub, q, c)
+    t = sum(run(sub, q, c) for _ in range(steps))
+    b, _ = mla_bytes_flops(sub)
+    value = b * steps / t / 1e9
+    sample = (f"{sub.batch} of {w.batch} requests ({int(np.sum(sub.kv_lens))} tokens) per step, "
+              f"fp64 MLA oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": steps, "warmup": warmup, "ms_per_step": t / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "config": {"workload": mla_describe(w), "batch": w.batch},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def mla_gpu_arm(args, w, rank, world):
+    import torch
+
+    import workloads as W
+    from paged_kv_decode_23_gb300 import BatchMLAPagedAttention
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    qn, qp = W.make_mla_q(w, device=dev)
+    ckv, kpe = W.make_mla_cache(w, device=dev)
+    out = torch.empty_like(qn)
+    lse = torch.empty(w.batch, w.num_heads, dtype=torch.float32, device=dev)
+    idx = torch.from_numpy(w.kv_indices).to(dev)
+    qo_ip = torch.arange(w.batch + 1, dtype=torch.int32)
+    kv_ip, kv_len = torch.from_numpy(w.kv_indptr), torch.from_numpy(w.kv_lens)
+    mla = BatchMLAPagedAttention(torch.zeros(256 << 20, dtype=torch.uint8, device=dev))
+    dt = W.TORCH_DTYPES[w.dtype]
+    flush_w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush(v):
+        flush_w.fill_(v)
+        torch.sum(flush_r, dim=0, out=flush_sum)
+
+    def plan(indices):
+        mla.plan(qo_ip, kv_ip, indices, kv_len, w.num_heads, 512, 64, w.page_size, False,
+                 w.sm_scale, dt, dt)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    seg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(2 * args.steps)]
+    for a, b in ev + seg:
+        a.record(stream)
+        b.record(stream)
+
+    def step(k=None, kernel_pass=False):
+        if k is not None and not kernel_pass:
+            seg[2 * k][0].record(stream)
+        plan(idx)
+        if k is not None and not kernel_pass:
+            seg[2 * k][1].record(stream)
+        flush(float(k or 0))
+        if k is not None and not kernel_pass:
+            seg[2 * k + 1][0].record(stream)
+        mla.run(qn, qp, ckv, kpe, out=out, lse=lse,
+                timing_events=ev[k] if (k is not None and kernel_pass) else None,
+                enable_pdl=not kernel_pass)
+        if k is not None and not kernel_pass:
+            seg[2 * k + 1][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mla.check_status() == 0, "device status word reports a failure"
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    for k in range(args.steps):
+        step(k)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_total = sum(a.elapsed_time(b) for a, b in seg)
+    plan_ms = sum(seg[2 * k][0].elapsed_time(seg[2 * k][1]) for k in range(args.steps))
+    for k in range(args.steps):
+        step(k, kernel_pass=True)
+    torch.cuda.synchronize()
+    assert mla.check_status() == 0, "device status word reports a failure"
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end with host buffers: q and the page ids in, o and lse out, every step
+    qn_h, qp_h = qn.cpu().pin_memory(), qp.cpu().pin_memory()
+    idx_h = torch.from_numpy(w.kv_indices).pin_memory()
+    qn_d, qp_d, idx_d = torch.empty_like(qn), torch.empty_like(qp), torch.empty_like(idx)
+    o_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    l_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        idx_d.copy_(idx_h, non_blocking=True)
+        qn_d.copy_(qn_h, non_blocking=True)
+        qp_d.copy_(qp_h, non_blocking=True)
+        plan(idx_d)
+        flush(1.0)
+        mla.run(qn_d, qp_d, ckv, kpe, out=out, lse=lse)
+        o_h.copy_(out, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total, e2e_s = float(t[0]), float(t[1])
+    bytes_call, flops_call = mla_bytes_flops(w)
+    ms_step = ms_total / args.steps
+    hbm_peak, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_peak, tf_kind = float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        tf_peak, tf_kind = 1900.0, "fallback"
+    tflops = flops_call / (kern_ms * 1e-3) / 1e12
+    h2d = (qn_h.numel() + qp_h.numel()) * qn_h.element_size() + idx_h.numel() * 4
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+    return {
+        "metric": METRIC, "value": world * bytes_call / (ms_step * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": mla_describe(w), "batch": w.batch, "layers": 1,
+                   "kv_tokens": int(np.sum(w.kv_lens)),
+                   "l2": "L2 flushed between calls (2x L2 written, then 2x L2 of other data "
+                         "read, outside the timed segments)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_call": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * (bytes_call / (ms_step * 1e-3) / 1e9) / hbm_peak,
+        "peak_kind": peak_kind,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": tflops / tf_peak, "traffic": None, "kernel": "mla_decode_kernel",
+                     "kernel_us": kern_ms * 1e3, "algorithmic_flops_per_launch": flops_call,
+                     "peak_kind": tf_kind,
+                     "hbm": {"achieved": bytes_call / (kern_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": bytes_call / (kern_ms * 1e-3) / 1e9 / hbm_peak,
+                             "algorithmic_bytes_per_launch": bytes_call}},
+        "e2e": {"value": world * bytes_call / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s / args.steps * 1e3},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "segments": {"plan_us_per_step": plan_ms * 1e3 / args.steps,
+                     "run_us_per_call": (ms_total - plan_ms) * 1e3 / args.steps},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,7 +678,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="uniform",
-                    choices=["worked", "uniform", "lognormal", "long", "mix"])
+                    choices=["worked", "uniform", "lognormal", "long", "mix", "mla"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
@@ -469,12 +691,29 @@ def main():
     args.warmup = max(3, args.warmup)
 
     import workloads as W
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.workload == "mla":
+        w = W.mla_workload()
+        if args.impl == "reference":
+            if rank == 0:
+                mla_reference_arm(args, w)
+            return
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl")
+        res = mla_gpu_arm(args, w, rank, world)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = mla_cpu_baseline(w, args.cpu_budget)
+            print(json.dumps(res))
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     w = W.workload(args.workload)
     if args.layers:
         w.layers = args.layers
-
-    rank = int(os.environ.get("RANK", 0))
-    world = int(os.environ.get("WORLD_SIZE", 1))
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, w)

@@ -192,6 +192,36 @@ int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads,
                               int use_tensor_cores, size_t* float_ws_bytes,
                               size_t* int_ws_bytes);
 
+/*
+ * MLA paged decode: the page's flashinfer.mla.BatchMLAPagedAttentionWrapper plan() / run()
+ * (decode: qo_indptr = 0, 1, ..., batch, one query per request).  With matrix absorption all
+ * num_heads query heads attend over one latent cache: key of token t = [ckv_t, kpe_t],
+ * value = ckv_t, logit = sm_scale * (<q_nope, ckv_t> + <q_pe, kpe_t>).
+ * pkd_mla_plan:
+ *   kv_indptr_host [batch+1] (non-decreasing), kv_len_host [batch] (0 <= kv_len <= pages *
+ *     page_size; extra pages are ignored): host int32.  kv_indices_dev [num_indices >=
+ *     kv_indptr[batch]]: device int32 page ids, stored and read by later runs.
+ *   head_dim_ckv must be 512 and head_dim_kpe 64 (the DeepSeek shapes the page names);
+ *   page_size >= 1 (any integer, 1 included); sm_scale > 0 (the page's example uses
+ *   1 / sqrt(128 + 64)); q_dtype == kv_dtype in {F16, BF16}; causal is accepted and has no
+ *   effect with one query per request.  The handle then holds an MLA plan: pkd_run refuses
+ *   it, pkd_mla_run refuses a pkd_plan plan.  Not capturable; CUDA-graph mode is refused.
+ * pkd_mla_run:
+ *   q_nope [batch, num_heads, 512], q_pe [batch, num_heads, 64]; ckv_cache [num_pages,
+ *   page_size, 512], kpe_cache [num_pages, page_size, 64] (all device, contiguous, 16-byte
+ *   aligned); page ids outside [0, num_pages) read as zero rows.  o [batch, num_heads, 512];
+ *   lse [batch, num_heads] float32 or NULL, base 2 unless lse_base_e (the page's
+ *   return_lse_base_on_e).  ev_start / ev_end (cudaEvent_t or NULL) are recorded around the
+ *   kernel.  One launch; split requests are merged inside it.
+ */
+int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv_len_host,
+                 int batch, const int32_t* kv_indices_dev, int64_t num_indices, int num_heads,
+                 int head_dim_ckv, int head_dim_kpe, int page_size, int causal, float sm_scale,
+                 int q_dtype, int kv_dtype, void* stream);
+int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                const void* kpe_cache, int64_t num_pages, void* o, float* lse, int lse_base_e,
+                void* stream, void* ev_start, void* ev_end);
+
 /* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
 int pkd_destroy(pkd_handle* h);
 

@@ -5,8 +5,9 @@ the work happens in ``_build/libpkd.so`` (hand-written CUDA kernels behind a C A
 in ``include/pkd.h``).  Build it with ``paged_kv_decode_23_gb300.build.build()``.
 """
 from ._lib import PkdError, LIB_PATH  # noqa: F401
-from .decode import (BatchDecodePagedKV, CUDAGraphBatchDecodePagedKV,  # noqa: F401
-                     graph_workspace_bytes, plan_host, workspace_bytes)
+from .decode import (BatchDecodePagedKV, BatchMLAPagedAttention,  # noqa: F401
+                     CUDAGraphBatchDecodePagedKV, graph_workspace_bytes, plan_host,
+                     workspace_bytes)
 
-__all__ = ["BatchDecodePagedKV", "CUDAGraphBatchDecodePagedKV", "PkdError",
-           "graph_workspace_bytes", "plan_host", "workspace_bytes"]
+__all__ = ["BatchDecodePagedKV", "BatchMLAPagedAttention", "CUDAGraphBatchDecodePagedKV",
+           "PkdError", "graph_workspace_bytes", "plan_host", "workspace_bytes"]

@@ -36,6 +36,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 std::once_flag g_registry_once;
 std::vector<DecodeKernel> g_decode;
 std::vector<MergeKernel> g_merge;
+std::vector<MlaKernel> g_mla;
 
 void init_registry() {
   std::call_once(g_registry_once, [] {
@@ -44,7 +45,15 @@ void init_registry() {
     register_decode_e4m3(g_decode);
     register_decode_rope(g_decode);
     register_merge(g_merge);
+    register_mla(g_mla);
   });
+}
+
+const MlaKernel* find_mla(int dtype) {
+  init_registry();
+  for (const auto& k : g_mla)
+    if (k.dtype == dtype) return &k;
+  return nullptr;
 }
 
 const DecodeKernel* find_decode(int kind, int q_dtype, int kv_dtype, int head_dim, int heads,
@@ -113,6 +122,8 @@ struct pkd_handle {
   int batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, page_size = 0;
   int q_len = 1;  // query tokens per request: q / o / lse have batch * q_len rows
   int pos_mode = 0;  // PKD_POS_*
+  bool mla = false;  // the current plan is an MLA plan (pkd_mla_plan)
+  const MlaKernel* mla_kernel = nullptr;
   int q_dtype = 0, kv_dtype = 0, o_dtype = 0;
   float sm_scale = 0.f, cap = 0.f;
   const int32_t* indices = nullptr;
@@ -519,6 +530,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (h->graph) h->g_batch = batch;
   h->kernel = k;
   h->pos_mode = pos_encoding_mode;
+  h->mla = false;
   h->merge = mk;
   h->planned = true;
   g_last_error.clear();
@@ -529,7 +541,8 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
                   int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
                   float v_scale, void* o, float* lse, void* stream, void* ev_start, void* ev_end) {
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
-  if (!h->planned) return fail(PKD_ERR_NOT_PLANNED, "pkd_run called before a successful pkd_plan");
+  if (!h->planned || h->mla)
+    return fail(PKD_ERR_NOT_PLANNED, "pkd_run called before a successful pkd_plan");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (h->plan.items.empty() && !h->graph) return PKD_OK;  // empty batch
   if (!q || !k_base || !v_base || !o || !kv_strides)
@@ -633,6 +646,185 @@ int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base
             float v_scale, void* o, float* lse, void* stream) {
   return pkd_run_timed(h, q, k_base, v_base, num_pages, kv_strides, q_scale, k_scale, v_scale, o,
                        lse, stream, nullptr, nullptr);
+}
+
+int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv_len_host,
+                 int batch, const int32_t* kv_indices_dev, int64_t num_indices, int num_heads,
+                 int head_dim_ckv, int head_dim_kpe, int page_size, int causal, float sm_scale,
+                 int q_dtype, int kv_dtype, void* stream) {
+  (void)causal;  // one query per request: nothing is masked
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  h->planned = false;
+  if (h->graph) return fail(PKD_ERR_UNSUPPORTED, "CUDA-graph mode is built for pkd_plan only");
+  if (head_dim_ckv != 512 || head_dim_kpe != 64)
+    return fail(PKD_ERR_UNSUPPORTED, "MLA is built for head_dim_ckv 512 and head_dim_kpe 64");
+  if (q_dtype != kv_dtype || (q_dtype != PKD_DTYPE_F16 && q_dtype != PKD_DTYPE_BF16))
+    return fail(PKD_ERR_UNSUPPORTED, "MLA takes F16 or BF16 q and caches of the same dtype");
+  if (num_heads <= 0) return fail(PKD_ERR_INVALID_ARG, "num_heads must be positive");
+  if (!(sm_scale > 0.f && std::isfinite(sm_scale)))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be positive and finite");
+  if (batch < 0 || (batch > 0 && (!kv_indptr_host || !kv_len_host)))
+    return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0 and the tables non-null");
+  if (batch > 0 && (!kv_indices_dev || num_indices < (int64_t)kv_indptr_host[batch]))
+    return fail(PKD_ERR_INVALID_ARG, "kv_indices holds fewer than kv_indptr[batch] page ids");
+
+  PlanRequest r;
+  std::memset(&r, 0, sizeof r);
+  r.indptr = kv_indptr_host;
+  r.kv_len = kv_len_host;
+  r.batch = batch;
+  r.num_qo_heads = num_heads;
+  r.num_kv_heads = 1;
+  r.head_dim = head_dim_ckv;
+  r.page_size = page_size;
+  r.window_left = -1;
+  r.kv_dtype = kv_dtype;
+  r.use_tensor_cores = 1;
+  r.num_sms = h->num_sms;
+  r.q_len = 1;
+  r.mla = 1;
+  r.mla_heads_per_cta = 32;
+  r.mla_tile_tokens = 32;
+  r.ctas_per_sm = 1;  // the MLA kernel takes most of an SM's shared memory
+  Plan plan;
+  const char* err = "";
+  int rc = build_plan(r, &plan, &err);
+  if (rc) return fail(rc, err);
+  const MlaKernel* k = find_mla(q_dtype);
+  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
+
+  const WsLayout lay = layout_of(plan, 1);
+  const size_t need_f = float_ws_bytes_of(lay, num_heads, head_dim_ckv);
+  const size_t need_i = int_ws_bytes_of(lay);
+  if (need_f > h->float_bytes || need_i > h->int_bytes) {
+    char buf[200];
+    std::snprintf(buf, sizeof buf, "workspace too small: need %zu float / %zu int bytes", need_f,
+                  need_i);
+    return fail(PKD_ERR_WORKSPACE_TOO_SMALL, buf);
+  }
+  static std::once_flag smem_once;
+  cudaError_t e = cudaSuccess;
+  std::call_once(smem_once, [&] {
+    for (const auto& m : g_mla)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(m.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, m.smem_bytes);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+
+  // one upload of the int workspace image: zeroed status block and counters, items, merges
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t items_off = items_offset(lay), merges_off = merges_offset(lay);
+  const size_t items_b = plan.items.size() * sizeof(WorkItem);
+  const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
+  const size_t bytes = merges_off + merges_b;
+  if (h->staging_pending) {
+    e = cudaEventSynchronize(h->staging_done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    h->staging_pending = false;
+  }
+  if (bytes > h->staging_bytes) {
+    if (h->staging) cudaFreeHost(h->staging);
+    h->staging = nullptr;
+    h->staging_bytes = 0;
+    const size_t cap = std::max<size_t>(bytes * 2, 1 << 16);
+    e = cudaHostAlloc(&h->staging, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    h->staging_bytes = cap;
+  }
+  char* img = static_cast<char*>(h->staging);
+  std::memset(img, 0, merges_off);
+  if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
+  if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
+  e = cudaMemcpyAsync(h->int_ws, img, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  e = cudaEventRecord(h->staging_done, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  h->staging_pending = true;
+
+  h->plan = std::move(plan);
+  h->batch = batch;
+  h->q_len = 1;
+  h->num_qo_heads = num_heads;
+  h->num_kv_heads = 1;
+  h->head_dim = head_dim_ckv;
+  h->page_size = page_size;
+  h->q_dtype = q_dtype;
+  h->kv_dtype = kv_dtype;
+  h->o_dtype = q_dtype;
+  h->sm_scale = sm_scale;
+  h->cap = 0.f;
+  h->indices = kv_indices_dev;
+  h->ws_layout = lay;
+  h->pos_mode = PKD_POS_NONE;
+  h->kernel = nullptr;
+  h->mla = true;
+  h->mla_kernel = k;
+  h->planned = true;
+  g_last_error.clear();
+  return PKD_OK;
+}
+
+int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                const void* kpe_cache, int64_t num_pages, void* o, float* lse, int lse_base_e,
+                void* stream, void* ev_start, void* ev_end) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (!h->planned || !h->mla)
+    return fail(PKD_ERR_NOT_PLANNED, "pkd_mla_run called without a successful pkd_mla_plan");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->plan.items.empty()) return PKD_OK;
+  if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !o)
+    return fail(PKD_ERR_INVALID_ARG, "null q_nope / q_pe / ckv / kpe / o");
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(ckv_cache, 16) ||
+      !aligned(kpe_cache, 16) || !aligned(o, 16))
+    return fail(PKD_ERR_INVALID_ARG, "q, the caches and o must be 16-byte aligned");
+  if (num_pages <= 0) return fail(PKD_ERR_INVALID_ARG, "num_pages must be positive");
+  char* iws = static_cast<char*>(h->int_ws);
+  char* fws = static_cast<char*>(h->float_ws);
+  const WsLayout& lay = h->ws_layout;
+  MlaParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.items = reinterpret_cast<const WorkItem*>(iws + items_offset(lay));
+  prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(lay));
+  prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
+  prm.status = reinterpret_cast<uint32_t*>(iws);
+  prm.indices = h->indices;
+  prm.ckv = ckv_cache;
+  prm.kpe = kpe_cache;
+  prm.q_nope = q_nope;
+  prm.q_pe = q_pe;
+  prm.o = o;
+  prm.lse = lse;
+  prm.part_o = reinterpret_cast<float*>(fws);
+  prm.part_lse = reinterpret_cast<float*>(fws + part_lse_offset(lay, h->num_qo_heads, h->head_dim));
+  prm.num_pages = num_pages;
+  prm.num_heads = h->num_qo_heads;
+  prm.gslices = h->plan.gslices;
+  prm.page_size = h->page_size;
+  prm.lse_base_e = lse_base_e ? 1 : 0;
+  prm.scale_log2 = (float)((double)h->sm_scale * 1.4426950408889634);
+  const int64_t grid = (int64_t)h->plan.items.size() * h->plan.gslices;
+  void* args[] = {&prm};
+  cudaError_t e;
+  if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
+  {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(h->mla_kernel->threads);
+    cfg.dynamicSmemBytes = (size_t)h->mla_kernel->smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = h->pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, h->mla_kernel->fn, args);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "MLA decode kernel launch");
+  if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
+  return PKD_OK;
 }
 
 int pkd_set_pdl(pkd_handle* h, int enable) {

@@ -113,6 +113,40 @@ void register_decode_f16(std::vector<DecodeKernel>& out);
 void register_decode_bf16(std::vector<DecodeKernel>& out);
 void register_decode_e4m3(std::vector<DecodeKernel>& out);
 void register_decode_rope(std::vector<DecodeKernel>& out);
+
+// MLA decode kernel parameters (pkd_mla_run -> mla_decode_kernel).
+struct MlaParams {
+  const WorkItem* items;
+  const int32_t* indices;
+  const void* ckv;        // [pages, page_size, 512]
+  const void* kpe;        // [pages, page_size, 64]
+  const void* q_nope;     // [rows, H, 512]
+  const void* q_pe;       // [rows, H, 64]
+  void* o;                // [rows, H, 512]
+  float* lse;             // [rows, H] or null
+  float* part_o;          // [slots, H, 512] fp32, normalised
+  float* part_lse;        // [slots, H] fp32, base 2
+  uint32_t* status;
+  const MergeEntry* merges;
+  uint32_t* counters;     // per (merge entry, head slice)
+  int64_t num_pages;      // pages in the caches: ids outside [0, num_pages) read as zeros
+  int num_heads;
+  int gslices;            // ceil(H / 32)
+  int page_size;
+  int lse_base_e;         // 1: lse as natural log, 0: base 2 (run()'s default)
+  float scale_log2;       // sm_scale * log2(e)
+};
+
+// MLA decode kernels (mla.cu): latent 512 + rope 64, one kernel per q / cache dtype.
+struct MlaKernel {
+  int dtype;
+  const void* fn;
+  int threads;
+  int smem_bytes;
+  int heads_per_cta;
+  int tile_tokens;
+};
+void register_mla(std::vector<MlaKernel>& out);
 void register_merge(std::vector<MergeKernel>& out);
 
 // ----------------------------------------------------------------------------- planner
@@ -133,6 +167,13 @@ struct PlanRequest {
   int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode)
   int q_len = 1;         // query tokens per request (run's q_len_per_req)
   int rope = 0;          // 1: ROPE_LLAMA (only the tensor-core kernel is built for it)
+  // MLA plans (pkd_mla_plan): lengths come from kv_len (pages may be more than needed), any
+  // page size >= 1, a fixed head tile and token tile, and the kernel's CTAs per SM.
+  const int32_t* kv_len = nullptr;
+  int mla = 0;
+  int mla_heads_per_cta = 32;
+  int mla_tile_tokens = 32;
+  int ctas_per_sm = 2;
 };
 
 struct Plan {

@@ -40,7 +40,7 @@ int tile_tokens_for(int head_dim, int kv_dtype) {
 
 int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   *plan = Plan();
-  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || !r.last_page_len))) {
+  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || (!r.last_page_len && !r.kv_len)))) {
     *err = "batch must be >= 0 and the page table pointers non-null";
     return kErrInvalid;
   }
@@ -52,7 +52,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     *err = "kv_dtype must be F16, BF16 or E4M3";
     return kErrInvalid;
   }
-  if (r.head_dim != 64 && r.head_dim != 128 && r.head_dim != 256) {
+  if (!r.mla && r.head_dim != 64 && r.head_dim != 128 && r.head_dim != 256) {
     *err = "head_dim must be 64, 128 or 256";
     return kErrUnsupported;
   }
@@ -60,8 +60,8 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     *err = "e4m3 KV needs head_dim 128 or 256 (rows of whole 128-byte blocks)";
     return kErrUnsupported;
   }
-  if (!is_pow2(r.page_size) || r.page_size < 8 || r.page_size > 256) {
-    *err = "page_size must be a power of two in [8, 256]";
+  if (r.mla ? r.page_size < 1 : (!is_pow2(r.page_size) || r.page_size < 8 || r.page_size > 256)) {
+    *err = r.mla ? "page_size must be >= 1" : "page_size must be a power of two in [8, 256]";
     return kErrUnsupported;
   }
   if (r.batch > 0 && r.indptr[0] < 0) {
@@ -81,12 +81,16 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     while (gp < G && gp < 8) gp <<= 1;
     plan->heads_per_cta = gp;
   }
+  if (r.mla) {
+    plan->kind = kTensorCore;
+    plan->heads_per_cta = r.mla_heads_per_cta;
+  }
   plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
   if (r.rope && plan->kind == kCudaCore) {
     *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
     return kErrUnsupported;
   }
-  plan->tile_tokens = tile_tokens_for(r.head_dim, r.kv_dtype);
+  plan->tile_tokens = r.mla ? r.mla_tile_tokens : tile_tokens_for(r.head_dim, r.kv_dtype);
 
   // per-request lengths
   std::vector<int64_t> n_req(r.batch);
@@ -95,6 +99,14 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     if (pages < 0) {
       *err = "indptr must be non-decreasing";
       return kErrInvalid;
+    }
+    if (r.kv_len) {  // lengths given directly (MLA's kv_len_arr); extra pages are ignored
+      if (r.kv_len[i] < 0 || (int64_t)r.kv_len[i] > pages * ps) {
+        *err = "kv_len must lie in [0, pages * page_size] for every request";
+        return kErrInvalid;
+      }
+      n_req[i] = r.kv_len[i];
+      continue;
     }
     if (pages == 0) {
       n_req[i] = 0;
@@ -162,7 +174,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     C = (int64_t)r.fixed_split_size * ps;
   } else {
     const int sms = r.num_sms > 0 ? r.num_sms : 152;
-    const int64_t slots = (int64_t)sms * kCtasPerSm;
+    const int64_t slots = (int64_t)sms * (r.ctas_per_sm > 0 ? r.ctas_per_sm : kCtasPerSm);
     if ((int64_t)rows * ctas_per_item <= slots) {
       // The unsplit requests already fit in one wave: split only as far as the grid stays
       // one wave, i.e. the smallest page-aligned chunk whose CTAs all start at once.  A second,

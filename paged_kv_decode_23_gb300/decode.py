@@ -335,3 +335,102 @@ class CUDAGraphBatchDecodePagedKV(BatchDecodePagedKV):
                          paged_kv_indices_buffer=indices_buffer,
                          paged_kv_last_page_len_buffer=last_page_len_buffer,
                          int_workspace_buffer=int_workspace_buffer, max_items=max_items)
+
+
+class BatchMLAPagedAttention:
+    """MLA paged decode (the pages' BatchMLAPagedAttentionWrapper): every query head attends
+    over one latent cache; key = [ckv, kpe] (512 + 64), value = ckv.  Decode only: every
+    query length in ``qo_indptr`` must be 1."""
+
+    def __init__(self, float_workspace_buffer: torch.Tensor,
+                 int_workspace_buffer: Optional[torch.Tensor] = None):
+        if not float_workspace_buffer.is_cuda:
+            raise ValueError("the float workspace must be a CUDA tensor")
+        if int_workspace_buffer is None:
+            int_workspace_buffer = torch.empty(8 << 20, dtype=torch.uint8,
+                                               device=float_workspace_buffer.device)
+        self._float_ws = float_workspace_buffer
+        self._int_ws = int_workspace_buffer
+        self._plan_args = None
+        h = ctypes.c_void_p()
+        L.check(L.lib().pkd_create(ctypes.byref(h), self._float_ws.data_ptr(),
+                                   self._float_ws.numel() * self._float_ws.element_size(),
+                                   self._int_ws.data_ptr(),
+                                   self._int_ws.numel() * self._int_ws.element_size(),
+                                   L.LAYOUT_NHD))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                L.lib().pkd_destroy(h)
+            except Exception:
+                pass
+            self._h = None
+
+    def plan(self, qo_indptr, kv_indptr, kv_indices: torch.Tensor, kv_len_arr, num_heads: int,
+             head_dim_ckv: int, head_dim_kpe: int, page_size: int, causal: bool, sm_scale: float,
+             q_data_type=torch.bfloat16, kv_data_type=None, use_profiler: bool = False,
+             stream=None) -> None:
+        q_ip = _host_i32(qo_indptr)
+        kv_ip = _host_i32(kv_indptr)
+        kv_len = _host_i32(kv_len_arr)
+        batch = len(kv_len)
+        if len(kv_ip) != batch + 1 or len(q_ip) != batch + 1:
+            raise ValueError("qo_indptr and kv_indptr must have batch + 1 entries")
+        if not np.array_equal(np.diff(q_ip), np.ones(batch, dtype=np.int32)):
+            raise NotImplementedError("only decode (one query per request) is built for MLA")
+        if use_profiler:
+            raise NotImplementedError("the in-kernel profiler is not built")
+        if not (isinstance(kv_indices, torch.Tensor) and kv_indices.is_cuda
+                and kv_indices.dtype == torch.int32 and kv_indices.is_contiguous()):
+            raise ValueError("kv_indices must be a contiguous CUDA int32 tensor")
+        q_dt = _as_dtype(q_data_type)
+        kv_dt = _as_dtype(kv_data_type) or q_dt
+        L.check(L.lib().pkd_mla_plan(
+            self._h, _i32p(kv_ip), _i32p(kv_len), batch, kv_indices.data_ptr(),
+            kv_indices.numel(), num_heads, head_dim_ckv, head_dim_kpe, page_size,
+            int(bool(causal)), float(sm_scale), _DTYPE_CODE[q_dt], _DTYPE_CODE[kv_dt],
+            _stream_ptr(stream)))
+        self._indices = kv_indices
+        self._plan_args = dict(batch=batch, num_heads=num_heads, page_size=page_size, dtype=q_dt)
+
+    def run(self, q_nope: torch.Tensor, q_pe: torch.Tensor, ckv_cache: torch.Tensor,
+            kpe_cache: torch.Tensor, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, return_lse: bool = False,
+            return_lse_base_on_e: bool = False, stream=None, timing_events=None,
+            enable_pdl: Optional[bool] = None):
+        a = self._plan_args
+        if a is None:
+            raise RuntimeError("plan() must be called before run()")
+        B, H, dt = a["batch"], a["num_heads"], a["dtype"]
+        for name, t, shape in (("q_nope", q_nope, (B, H, 512)), ("q_pe", q_pe, (B, H, 64))):
+            if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape}")
+        ps = a["page_size"]
+        if (ckv_cache.dim() != 3 or tuple(ckv_cache.shape[1:]) != (ps, 512)
+                or ckv_cache.dtype != dt or not ckv_cache.is_contiguous()):
+            raise ValueError(f"ckv_cache must be a contiguous {dt} [pages, {ps}, 512] tensor")
+        if (tuple(kpe_cache.shape) != (ckv_cache.shape[0], ps, 64) or kpe_cache.dtype != dt
+                or not kpe_cache.is_contiguous()):
+            raise ValueError(f"kpe_cache must be a contiguous {dt} [pages, {ps}, 64] tensor")
+        if out is None:
+            out = torch.empty((B, H, 512), dtype=dt, device=q_nope.device)
+        if lse is None and return_lse:
+            lse = torch.empty((B, H), dtype=torch.float32, device=q_nope.device)
+        if enable_pdl is not None:
+            L.check(L.lib().pkd_set_pdl(self._h, int(bool(enable_pdl))))
+        ev0, ev1 = timing_events if timing_events is not None else (None, None)
+        L.check(L.lib().pkd_mla_run(
+            self._h, q_nope.data_ptr(), q_pe.data_ptr(), ckv_cache.data_ptr(),
+            kpe_cache.data_ptr(), ckv_cache.shape[0], out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, int(bool(return_lse_base_on_e)),
+            _stream_ptr(stream), ev0.cuda_event if ev0 is not None else None,
+            ev1.cuda_event if ev1 is not None else None))
+        return (out, lse) if return_lse else out
+
+    def check_status(self, stream=None) -> int:
+        v = ctypes.c_uint32()
+        L.check(L.lib().pkd_check_status(self._h, ctypes.byref(v), _stream_ptr(stream)))
+        return v.value

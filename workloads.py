@@ -194,3 +194,67 @@ def raw_bits(t: torch.Tensor) -> np.ndarray:
     if t.element_size() == 1:
         return t.view(torch.uint8).numpy()
     raise TypeError(t.dtype)
+
+
+# ----------------------------------------------------------------------------- MLA
+@dataclass
+class MlaWorkload:
+    """MLA paged decode (latent cache): per-request kv lengths, a CSR page table over a pool
+    of pages of ``page_size`` latent rows (ckv 512 + kpe 64), ``num_heads`` query heads."""
+    name: str
+    batch: int
+    num_heads: int
+    page_size: int
+    dtype: str
+    kv_lens: np.ndarray     # int32 [batch]
+    kv_indptr: np.ndarray   # int32 [batch + 1]
+    kv_indices: np.ndarray  # int32 [kv_indptr[-1]]
+    num_pages: int
+    sm_scale: float
+    layers: int = 1
+    seed: int = 0
+    head_dim_ckv: int = 512
+    head_dim_kpe: int = 64
+
+
+def mla_custom(kv_lens, num_heads: int, page_size: int, dtype: str = "bf16", seed: int = 0,
+               pool_factor: float = 2.0, extra_pages: int = 0) -> MlaWorkload:
+    """An MLA workload with explicit lengths; ``extra_pages`` gives every request that many
+    unused pages past its last one (the page table may hold more pages than the length)."""
+    kv_lens = np.asarray(kv_lens, dtype=np.int64)
+    need = np.where(kv_lens > 0, (kv_lens + page_size - 1) // page_size, 0) + extra_pages
+    indptr = np.zeros(len(kv_lens) + 1, dtype=np.int64)
+    np.cumsum(need, out=indptr[1:])
+    total = int(indptr[-1])
+    num_pages = max(1, int(np.ceil(total * pool_factor)))
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    indices = rng.permutation(num_pages)[:total].astype(np.int32)
+    return MlaWorkload("mla-custom", len(kv_lens), num_heads, page_size, dtype,
+                       kv_lens.astype(np.int32), indptr.astype(np.int32), indices, num_pages,
+                       sm_scale=1.0 / np.sqrt(128.0 + 64.0), seed=seed)
+
+
+def mla_workload(seed: int = 0) -> MlaWorkload:
+    """The MLA example of the pages' BatchMLAPagedAttentionWrapper: batch 114, 128 heads,
+    kv_len 999 per request, page_size 1, bf16, sm_scale 1/sqrt(128 + 64).  Pages are the
+    leading entries of a seeded permutation of a pool twice the size needed."""
+    w = mla_custom([999] * 114, 128, 1, "bf16", seed=seed)
+    w.name = "mla"
+    return w
+
+
+def make_mla_q(w: MlaWorkload, device="cpu", layer: int = 0):
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 1000003 + 29 + layer)
+    qn = _normal((w.batch, w.num_heads, w.head_dim_ckv), device, gen)
+    qp = _normal((w.batch, w.num_heads, w.head_dim_kpe), device, gen)
+    return qn.to(TORCH_DTYPES[w.dtype]), qp.to(TORCH_DTYPES[w.dtype])
+
+
+def make_mla_cache(w: MlaWorkload, device="cpu", layer: int = 0):
+    """ckv [pages, page_size, 512] and kpe [pages, page_size, 64], N(0, 1)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 1000003 + 200003 + layer)
+    ckv = _normal((w.num_pages, w.page_size, w.head_dim_ckv), device, gen)
+    kpe = _normal((w.num_pages, w.page_size, w.head_dim_kpe), device, gen)
+    return ckv.to(TORCH_DTYPES[w.dtype]), kpe.to(TORCH_DTYPES[w.dtype])
