@@ -523,6 +523,11 @@ def mla_reference_arm(args, w):
                 "d2h_bytes_per_step": 0}}))
 
 
+def mla_kernel_name(args, w) -> str:
+    tc = args.mla_backend == "tcgen05" or (args.mla_backend == "auto" and w.num_heads > 64)
+    return "mla_tc_kernel" if tc else "mla_decode_kernel"
+
+
 def mla_gpu_arm(args, w, rank, world):
     import torch
 
@@ -540,7 +545,8 @@ def mla_gpu_arm(args, w, rank, world):
     idx = torch.from_numpy(w.kv_indices).to(dev)
     qo_ip = torch.arange(w.batch + 1, dtype=torch.int32)
     kv_ip, kv_len = torch.from_numpy(w.kv_indptr), torch.from_numpy(w.kv_lens)
-    mla = BatchMLAPagedAttention(torch.zeros(256 << 20, dtype=torch.uint8, device=dev))
+    mla = BatchMLAPagedAttention(torch.zeros(256 << 20, dtype=torch.uint8, device=dev),
+                                 backend=args.mla_backend)
     dt = W.TORCH_DTYPES[w.dtype]
     flush_w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -647,6 +653,7 @@ def mla_gpu_arm(args, w, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": mla_describe(w), "batch": w.batch, "layers": 1,
+                   "mla_kernel": mla_kernel_name(args, w),
                    "kv_tokens": int(np.sum(w.kv_lens)),
                    "l2": "L2 flushed between calls (2x L2 written, then 2x L2 of other data "
                          "read, outside the timed segments)",
@@ -655,7 +662,7 @@ def mla_gpu_arm(args, w, rank, world):
         "pct_of_hbm_peak": 100.0 * (bytes_call / (ms_step * 1e-3) / 1e9) / hbm_peak,
         "peak_kind": peak_kind,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s",
-                     "frac": tflops / tf_peak, "traffic": None, "kernel": "mla_decode_kernel",
+                     "frac": tflops / tf_peak, "traffic": None, "kernel": mla_kernel_name(args, w),
                      "kernel_us": kern_ms * 1e3, "algorithmic_flops_per_launch": flops_call,
                      "peak_kind": tf_kind,
                      "hbm": {"achieved": bytes_call / (kern_ms * 1e-3) / 1e9, "peak": hbm_peak,
@@ -683,6 +690,8 @@ def main():
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
                     help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
+    ap.add_argument("--mla-backend", choices=["auto", "fa2", "tcgen05"], default="auto",
+                    help="MLA kernel (--workload mla): auto picks tcgen05 for > 64 heads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -209,7 +209,7 @@ int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads,
  * pkd_mla_run:
  *   q_nope [batch, num_heads, 512], q_pe [batch, num_heads, 64]; ckv_cache [num_pages,
  *   page_size, 512], kpe_cache [num_pages, page_size, 64] (all device, contiguous, 16-byte
- *   aligned); page ids outside [0, num_pages) read as zero rows.  o [batch, num_heads, 512];
+ *   aligned); a page id outside [0, num_pages) reads as a zero row (logit 0, value 0).  o [batch, num_heads, 512];
  *   lse [batch, num_heads] float32 or NULL, base 2 unless lse_base_e (the page's
  *   return_lse_base_on_e).  ev_start / ev_end (cudaEvent_t or NULL) are recorded around the
  *   kernel.  One launch; split requests are merged inside it.
@@ -221,6 +221,19 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
 int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void* ckv_cache,
                 const void* kpe_cache, int64_t num_pages, void* o, float* lse, int lse_base_e,
                 void* stream, void* ev_start, void* ev_end);
+
+/*
+ * MLA kernel used by later pkd_mla_plan calls on this handle (the wrapper's backend argument):
+ *   PKD_MLA_BACKEND_AUTO      the tcgen05 kernel when num_heads > 64, else the mma.sync kernel;
+ *   PKD_MLA_BACKEND_MMA_SYNC  32 heads per CTA, mma.sync with register accumulators;
+ *   PKD_MLA_BACKEND_TCGEN05   128 heads per 2-CTA cluster (the pair splits the 576 features),
+ *                             tcgen05 MMAs with accumulators in tensor memory.
+ * Both compute the same result within rounding.  PKD_ERR_INVALID_ARG for other values.
+ */
+#define PKD_MLA_BACKEND_AUTO 0
+#define PKD_MLA_BACKEND_MMA_SYNC 1
+#define PKD_MLA_BACKEND_TCGEN05 2
+int pkd_mla_set_backend(pkd_handle* h, int backend);
 
 /* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
 int pkd_destroy(pkd_handle* h);

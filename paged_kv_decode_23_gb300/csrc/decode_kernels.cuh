@@ -105,7 +105,9 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords
   bool ok = true;
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    if (i >= NSTAGES && !mbar_wait(empty0 + 8 * s, ((i / NSTAGES) - 1) & 1, abort_flag)) {
+    // one decision per warp: a lane that gave up takes the whole warp out of the loop
+    if (i >= NSTAGES &&
+        !__all_sync(~0u, mbar_wait(empty0 + 8 * s, ((i / NSTAGES) - 1) & 1, abort_flag))) {
       ok = false;
       break;
     }
@@ -506,8 +508,8 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    if (!mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag)) {
-      *abort_flag = 1;
+    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag))) {
+      *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
     }
@@ -824,8 +826,8 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    if (!mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag)) {
-      *abort_flag = 1;
+    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag))) {
+      *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
     }

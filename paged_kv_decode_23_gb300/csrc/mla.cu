@@ -5,6 +5,8 @@ namespace pkd {
 
 void register_mla(std::vector<MlaKernel>& out) {
   MlaKernel k;
+  k.variant = kMlaMmaSync;
+  k.ctas_per_head_tile = 1;
   k.threads = mla::THREADS;
   k.smem_bytes = mla::SMEM_BYTES;
   k.heads_per_cta = mla::HT;

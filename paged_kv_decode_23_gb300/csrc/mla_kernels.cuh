@@ -13,6 +13,12 @@
 //             apart (1152 + 16: eight consecutive rows fall in eight different 16-byte bank
 //             groups, so ldmatrix reads are conflict-free without a swizzle).  Completion is
 //             the stage's full mbarrier transaction count.
+//   cluster   the head-slice CTAs of one work item (up to 8) form a thread-block cluster and
+//             read every row once: CTA k copies rows r with r % size == k and multicasts
+//             them into every CTA of the cluster.  A stage is refilled only after the
+//             consumers of every CTA have released it (each consumer warp arrives on the
+//             stage's empty barrier in every CTA).  Cluster barriers after the barriers' init
+//             and before exit; no CTA returns early, so every CTA reaches both.
 //   consumers warp w owns latent dims [64w, 64w + 64): it forms the partial logits S_w^T
 //             (32 tokens x 32 heads) over those dims with mma.m16n8k16 (warps 0-3 also add
 //             one 16-dim k step of the kpe part each), the partials meet in shared memory,
@@ -50,7 +56,7 @@ constexpr int SPART_BYTES = NW * HT * SPART_STRIDE * 4;
 constexpr int P_STRIDE = 80;                    // bytes per head row of P (32 tokens + pad)
 constexpr int P_BYTES = HT * P_STRIDE;
 constexpr int EPI_BYTES = HT * DC * 4;          // fp32 O staging in the epilogue
-constexpr int SMEM_BYTES = PIPE_BYTES + SPART_BYTES + P_BYTES + 3 * HT * 4 + 1024;
+constexpr int SMEM_BYTES = PIPE_BYTES + SPART_BYTES + 2 * P_BYTES + 3 * HT * 4 + 1024;
 static_assert(EPI_BYTES <= PIPE_BYTES, "the epilogue reuses the pipeline buffers");
 
 }  // namespace mla
@@ -70,6 +76,36 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// The same copy delivered to the same offsets (data and mbarrier) in every CTA of `mask`.
+__device__ __forceinline__ void bulk_copy_multicast(uint32_t dst, const void* src, uint32_t bytes,
+                                                    uint32_t bar, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1], %2, [%3], %4, %5;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// Arrive on the mbarrier at local shared address `bar` of CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+               : "memory");
+}
+
 // Byte offset of 16-byte chunk c (0..63 ckv, 64..71 kpe) of tile row r inside a stage.
 __device__ __forceinline__ uint32_t row_chunk(int r, int c) {
   return (uint32_t)(r * mla::ROW_STRIDE + c * 16);
@@ -78,7 +114,8 @@ __device__ __forceinline__ uint32_t row_chunk(int r, int c) {
 template <typename T>
 __device__ __forceinline__ void produce(const MlaParams& p, const WorkItem& it, int j0, int ntiles,
                                         uint32_t smem, uint32_t full0, uint32_t empty0,
-                                        volatile int* abort_flag, int lane) {
+                                        volatile int* abort_flag, int lane, int csize, int rank,
+                                        volatile uint32_t* bad_rows) {
   const int ps = p.page_size;
   const char* ckv = static_cast<const char*>(p.ckv);
   const char* kpe = static_cast<const char*>(p.kpe);
@@ -98,22 +135,40 @@ __device__ __forceinline__ void produce(const MlaParams& p, const WorkItem& it, 
     const int s = i % mla::NSTAGES;
     const int64_t pid = pid_next;
     pid_next = page_of(i + 1);
-    if (i >= mla::NSTAGES &&
-        !mbar_wait(empty0 + 8 * s, ((i / mla::NSTAGES) - 1) & 1, abort_flag)) {
-      ok = false;
-      break;
+    if (i >= mla::NSTAGES) {  // lane 0 waits, so the whole warp takes one decision
+      int freed = 1;
+      if (lane == 0) freed = mbar_wait(empty0 + 8 * s, ((i / mla::NSTAGES) - 1) & 1, abort_flag);
+      if (!__shfl_sync(~0u, freed, 0)) {
+        ok = false;
+        break;
+      }
     }
     const int t = it.chunk_tok0 + (j0 + i) * mla::TS + lane;
     const bool ok_row = pid >= 0 && pid < p.num_pages;  // ids outside the caches: not copied
     const int64_t prow = ok_row ? pid * ps + t % ps : 0;
     const uint32_t stage = smem + s * mla::STAGE_BYTES;
     const unsigned m = __ballot_sync(~0u, ok_row);
-    if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, __popc(m) * (uint32_t)mla::ROW_BYTES);
+    // tokens of the item whose page id lies outside the caches: zero rows (the consumers zero
+    // them before use, as a TMA read past the end would)
+    const unsigned bad = __ballot_sync(~0u, !ok_row && t >= it.tok_begin && t < it.tok_end);
+    if (lane == 0) {
+      bad_rows[s] = bad;
+      mbar_arrive_expect_tx(full0 + 8 * s, __popc(m) * (uint32_t)mla::ROW_BYTES);
+    }
     __syncwarp();
-    if (ok_row) {  // rows not copied keep stale data: their logits are masked, V zeroed
+    // rows not copied keep stale data: their logits are masked, their V zeroed.  In a
+    // cluster this CTA copies rows lane % csize == rank into every CTA.
+    if (ok_row && lane % csize == rank) {
       const uint32_t dst = stage + lane * mla::ROW_STRIDE;
-      bulk_copy(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, pol);
-      bulk_copy(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2, full0 + 8 * s, pol);
+      if (csize == 1) {
+        bulk_copy(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, pol);
+        bulk_copy(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2, full0 + 8 * s, pol);
+      } else {
+        const uint16_t mask = (uint16_t)((1u << csize) - 1u);
+        bulk_copy_multicast(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, mask, pol);
+        bulk_copy_multicast(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2,
+                            full0 + 8 * s, mask, pol);
+      }
     }
     issued = i + 1;
   }
@@ -156,58 +211,23 @@ __device__ __forceinline__ void load_q(const MlaParams& p, int row, int g0, int 
 
 }  // namespace mla_detail
 
+// The consumer warps' part of mla_decode_kernel: attention over the item's tiles, the
+// epilogue and the fused merge.
 template <typename T>
-__global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaParams p) {
+__device__ __forceinline__ void consume(const MlaParams& p, const WorkItem& it, int j0, int ntiles,
+                                        int gs, int g0, int gcnt, uint8_t* base, uint32_t smem,
+                                        uint32_t full0, uint32_t empty0, volatile int* abort_flag,
+                                        int* merge_last_s, int csize,
+                                        const volatile uint32_t* bad_rows) {
   using namespace dev;
   using namespace mla_detail;
   constexpr float kNegInfF = -__builtin_huge_valf();
-  __shared__ __align__(8) uint64_t bars[2 * mla::NSTAGES];
-  __shared__ int abort_flag_s;
-  __shared__ int merge_last_s;
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* base =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  const uint32_t smem = smem_u32(base);
   float* spart = reinterpret_cast<float*>(base + mla::PIPE_BYTES);
   uint8_t* pbuf = base + mla::PIPE_BYTES + mla::SPART_BYTES;
-  float* alpha_s = reinterpret_cast<float*>(pbuf + mla::P_BYTES);
+  float* alpha_s = reinterpret_cast<float*>(pbuf + 2 * mla::P_BYTES);  // after P hi and P lo
   float* m_s = alpha_s + mla::HT;
   float* l_s = m_s + mla::HT;
-  const uint32_t full0 = smem_u32(&bars[0]);
-  const uint32_t empty0 = smem_u32(&bars[mla::NSTAGES]);
-  volatile int* abort_flag = &abort_flag_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int item = blockIdx.x / p.gslices;
-  const int gs = blockIdx.x - item * p.gslices;
-  const WorkItem it = p.items[item];
-  const int g0 = gs * mla::HT;
-  const int gcnt = min(mla::HT, p.num_heads - g0);
-  int j0 = 0, ntiles = 0;
-  if (it.tok_end > it.tok_begin) {
-    j0 = (it.tok_begin - it.chunk_tok0) / mla::TS;
-    ntiles = (it.tok_end - it.chunk_tok0 + mla::TS - 1) / mla::TS - j0;
-  }
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int s = 0; s < mla::NSTAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);         // the producer's expect_tx arrival
-      mbar_init(empty0 + 8 * s, mla::NW);  // one per consumer warp
-    }
-    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (abort_flag_s) return;
-
-  if (warp == mla::NW) {
-    produce<T>(p, it, j0, ntiles, smem, full0, empty0, abort_flag, lane);
-    return;
-  }
-
-  // ---------------------------------------------------------------- consumers
   const int tid = threadIdx.x;
   const int g = lane >> 2, tig = lane & 3;
   uint32_t qn[4][4][2], qp[4][2];
@@ -231,8 +251,28 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       *abort_flag = 1;
       atomicOr(p.status, kStatusTimeout);
     }
-    const uint32_t stage = stage_after_wait(smem + s * mla::STAGE_BYTES);
+    // after a timeout the loop runs on without waiting (every wait sees the abort flag), so
+    // all consumer warps meet the same named barriers; the output is not written
+    __syncwarp();
+    uint32_t stage = stage_after_wait(smem + s * mla::STAGE_BYTES);
     const int tt0 = it.chunk_tok0 + (j0 + i) * mla::TS;  // first token of the tile
+    bool wrote = false;
+    const uint32_t bad = bad_rows[s];
+    if (bad) {
+      // rows with a page id outside the caches were not copied: zero the dims this warp reads
+      // (ckv chunks 8w .. 8w + 7, kpe chunks 64 + 2w, 65 + 2w for w < 4)
+      for (int u = lane; u < mla::TS * 10; u += 32) {
+        const int r = u / 10, c = u - r * 10;
+        const int chunk = c < 8 ? warp * 8 + c : (warp < 4 ? 64 + warp * 2 + (c - 8) : -1);
+        if (((bad >> r) & 1u) && chunk >= 0)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(stage + row_chunk(r, chunk)),
+                       "r"(0)
+                       : "memory");
+      }
+      wrote = true;
+      __syncwarp();
+      stage = stage_after_wait(stage);  // the MMA operand reads come after the zeroing
+    }
     // ---- partial S^T over my dims: 2 token m tiles x 4 head n tiles
     float sa[2][4][4];
 #pragma unroll
@@ -303,16 +343,20 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       ps += __shfl_xor_sync(~0u, ps, 4);
       lsum = lsum * alpha + ps;
       m2 = mnew;
-      uint2 pk;
+      // P rounded to 16 bits, and the rounding remainder (P V = P_hi V + P_lo V to ~2^-17)
+      uint2 pk, pl;
       pk.x = pack2<T>(sc[0], sc[1]);
       pk.y = pack2<T>(sc[2], sc[3]);
+      const float2 r0 = unpack2<T>(pk.x), r1 = unpack2<T>(pk.y);
+      pl.x = pack2<T>(sc[0] - r0.x, sc[1] - r0.y);
+      pl.y = pack2<T>(sc[2] - r1.x, sc[3] - r1.y);
       *reinterpret_cast<uint2*>(pbuf + sh * mla::P_STRIDE + stg * 8) = pk;
+      *reinterpret_cast<uint2*>(pbuf + mla::P_BYTES + sh * mla::P_STRIDE + stg * 8) = pl;
       if (stg == 0) alpha_s[sh] = alpha;
     }
     named_bar_sync(1, mla::NCONS);
     // ---- O^T += V^T P^T for my 64 dims (rescale by alpha of each head column first)
     uint32_t vst = stage;
-    bool wrote = false;
     if (tt0 < it.tok_begin || tt0 + mla::TS > it.tok_end) {
       // rows outside [tok_begin, tok_end) were not copied: zero my 64 dims of them, so that
       // 0 * stale data cannot reach O (their logits are already -inf)
@@ -351,33 +395,43 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       const uint32_t pb = smem_u32(pbuf);
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
-        // P^T B fragments for n tiles (2q, 2q+1): matrices (nt, tokens 0-7 / 8-15 of the step)
-        uint32_t bf[4][2];
+        // P^T B fragments (hi and lo) for n tiles (2q, 2q+1): matrices (nt, tokens 0-7 /
+        // 8-15 of the step)
+        uint32_t bf[2][4][2];
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          const int mtx = lane >> 3;
-          const int hd = (q2 * 2 + (mtx >> 1)) * 8 + (lane & 7);
-          const uint32_t addr = pb + hd * mla::P_STRIDE + (ks * 16 + (mtx & 1) * 8) * 2;
-          uint32_t r[4];
-          ldsm_x4(addr, r);
-          bf[q2 * 2][0] = r[0];
-          bf[q2 * 2][1] = r[1];
-          bf[q2 * 2 + 1][0] = r[2];
-          bf[q2 * 2 + 1][1] = r[3];
-        }
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int mtx = lane >> 3;
+            const int hd = (q2 * 2 + (mtx >> 1)) * 8 + (lane & 7);
+            const uint32_t addr = pb + part * mla::P_BYTES + hd * mla::P_STRIDE +
+                                  (ks * 16 + (mtx & 1) * 8) * 2;
+            uint32_t r[4];
+            ldsm_x4(addr, r);
+            bf[part][q2 * 2][0] = r[0];
+            bf[part][q2 * 2][1] = r[1];
+            bf[part][q2 * 2 + 1][0] = r[2];
+            bf[part][q2 * 2 + 1][1] = r[3];
+          }
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           uint32_t a[4];
           ldsm_x4_trans(vst + row_chunk(ks * 16 + row_v, warp * 8 + mt * 2 + csel_v), a);
 #pragma unroll
-          for (int nt = 0; nt < 4; ++nt) mma_16816<T>(acc[mt][nt], a, bf[nt][0], bf[nt][1]);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+              mma_16816<T>(acc[mt][nt], a, bf[part][nt][0], bf[part][nt][1]);
         }
       }
     }
     if (wrote) fence_proxy_async_smem();  // the zeroing stores before the next TMA copies
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    if (*abort_flag) break;
+    if (csize == 1) {
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    } else if (lane < csize) {
+      mbar_arrive_cluster(empty0 + 8 * s, (uint32_t)lane);  // the stage in every CTA
+    }
   }
   if (stg == 0) {
     m_s[sh] = m2;
@@ -450,10 +504,10 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       last = (prev + 1u == (uint32_t)p.merges[it.merge_idx].n_chunks) ? 1 : 0;
       if (last) *ctr = 0u;
     }
-    merge_last_s = last;
+    *merge_last_s = last;
   }
   named_bar_sync(1, mla::NCONS);
-  if (!merge_last_s) return;
+  if (!*merge_last_s) return;
   __threadfence();
   const MergeEntry me = p.merges[it.merge_idx];
   constexpr float kLn2f = 0.6931471805599453f;
@@ -490,6 +544,66 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       p.lse[(size_t)me.req * p.num_heads + h] = p.lse_base_e ? lse2 * kLn2f : lse2;
     }
   }
+}
+
+
+template <typename T>
+__global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaParams p) {
+  using namespace dev;
+  using namespace mla_detail;
+  __shared__ __align__(8) uint64_t bars[2 * mla::NSTAGES];
+  __shared__ int abort_flag_s;
+  __shared__ int merge_last_s;
+  __shared__ uint32_t bad_rows_s[mla::NSTAGES];
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* base =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem = smem_u32(base);
+  const uint32_t full0 = smem_u32(&bars[0]);
+  const uint32_t empty0 = smem_u32(&bars[mla::NSTAGES]);
+  volatile int* abort_flag = &abort_flag_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int csize = p.cluster_size;  // CTAs of the cluster: head slices of one work item
+  const int rank = csize > 1 ? (int)cluster_rank() : 0;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int item = blockIdx.x / p.gslices;
+  const int gs = blockIdx.x - item * p.gslices;
+  const WorkItem it = p.items[item];
+  const int g0 = gs * mla::HT;
+  const int gcnt = min(mla::HT, p.num_heads - g0);
+  int j0 = 0, ntiles = 0;
+  if (it.tok_end > it.tok_begin) {
+    j0 = (it.tok_begin - it.chunk_tok0) / mla::TS;
+    ntiles = (it.tok_end - it.chunk_tok0 + mla::TS - 1) / mla::TS - j0;
+  }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < mla::NSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);         // the producer's expect_tx arrival
+      mbar_init(empty0 + 8 * s, mla::NW * csize);  // one per consumer warp of the cluster
+    }
+    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    fence_mbar_init();
+  }
+  // peers' copies and arrivals reach this CTA's barriers only after their init
+  if (csize > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  // an earlier launch timed out: do nothing (a peer that read the status word before it was
+  // set finds its waits bounded); the output is left unwritten
+  if (abort_flag_s) ntiles = 0;
+
+  if (warp == mla::NW)
+    produce<T>(p, it, j0, ntiles, smem, full0, empty0, abort_flag, lane, csize, rank, bad_rows_s);
+  else
+    consume<T>(p, it, j0, ntiles, gs, g0, gcnt, base, smem, full0, empty0, abort_flag,
+               &merge_last_s, csize, bad_rows_s);
+  __syncwarp();
+  // no CTA leaves while a peer may still copy into its shared memory or arrive on its barriers
+  if (csize > 1) cluster_sync();
 }
 
 }  // namespace pkd

@@ -1,0 +1,672 @@
+// mla_tc_kernels.cuh -- MLA paged decode on the 5th-generation tensor cores (tcgen05 + TMEM),
+// sm_103a.  Same operation as mla_kernels.cuh (FlashInfer attention API page, flashinfer.mla /
+// BatchMLAPagedAttentionWrapper): logit = sm_scale * (<q_nope, ckv_t> + <q_pe, kpe_t>), value
+// ckv_t, for 128 query heads per CTA pair.
+//
+// Why a CTA pair: one SM's tensor memory (512 columns x 128 lanes of fp32) holds O for 128
+// heads x 512 dims and nothing else, so the two CTAs of a cluster split the work by feature:
+//   CTA 0 holds q_nope[:, 0:256], loads ckv[t, 0:256] and owns O[:, 0:256];
+//   CTA 1 holds q_nope[:, 256:512] and q_pe, loads ckv[t, 256:512] and kpe[t], owns O[:, 256:512].
+// Each CTA's logit MMA gives a partial S over its features; the two partials are exchanged
+// through distributed shared memory and added (a + b == b + a exactly, so both CTAs hold the
+// same S, the same softmax and the same P), and each CTA multiplies P by the value columns it
+// loaded itself.  Every byte of the caches is read once, by one CTA.
+//
+// Roles (288 threads):
+//   warps 0-3  softmax: thread h owns head h (TMEM lane h): reads its partial S row, exchanges
+//              it, runs the online softmax (lazy reference, rescaling O in TMEM only when the
+//              running maximum grows by more than 2^8), writes P (bf16 / fp16) to shared memory;
+//              epilogue and fused merge.
+//   warps 4-7  producer: 16-byte cp.async gathers of the token rows (any page size; a TMA
+//              request per row is rate-bound for rows this small), zero-filled for tokens
+//              outside the item and for page ids outside the caches, into NST stages laid out
+//              as the MMA's 128-byte-swizzled K-major blocks (8 rows x 128 bytes per atom).
+//   warp 8     MMA issuer (one thread) and TMEM owner: S = Q K^T as M=128 x N=32 MMAs over
+//              16-feature steps into one of two S buffers, then O += P V as two M=128 x N=256
+//              MMAs with V read MN-major from the same stage blocks.  tcgen05.commit signals the
+//              softmax (S ready, PV done) and the producer (stage free).
+// Every wait is bounded; a timeout sets the status word and the kernel runs on without waiting
+// (the output is then not written).  No CTA leaves before its peer (cluster barrier).
+#pragma once
+
+#include <type_traits>
+
+#include "pkd_device.cuh"
+#include "pkd_internal.h"
+
+namespace pkd {
+
+namespace mlatc {
+
+constexpr int DC = 512;
+constexpr int DP = 64;
+constexpr int HT = 128;                       // heads per CTA: the MMA's M
+constexpr int TS = 32;                        // tokens per tile: the logit MMA's N
+constexpr int NST = 3;                        // pipeline stages
+constexpr int QBLK = 5;                       // 64-feature blocks held by CTA 1 (CTA 0: 4)
+constexpr int QBLK_BYTES = HT * 128;          // 16384
+constexpr int BLK_BYTES = TS * 128;           // 4096: one 64-feature block of a tile
+constexpr int STAGE_BYTES = QBLK * BLK_BYTES;  // 20480
+constexpr int XBUF_BYTES = HT * TS * 4;      // 16384: a partial S tile, 128-byte rows, chunk
+                                              // q of head h at chunk q ^ (h & 7)
+constexpr int P_BYTES = HT * 64;              // 32 tokens x 2 bytes per head, 64-byte swizzle
+constexpr int OFF_Q = 0;
+constexpr int OFF_STAGE = OFF_Q + QBLK * QBLK_BYTES;         // 81920
+constexpr int OFF_XOUT = OFF_STAGE + NST * STAGE_BYTES;      // 143360: my partial, 2 buffers
+constexpr int OFF_XIN = OFF_XOUT + 2 * XBUF_BYTES;           // 176128: the peer's, 2 buffers
+constexpr int OFF_P = OFF_XIN + 2 * XBUF_BYTES;              // 208896: P hi, then P lo
+constexpr int SMEM_BYTES = OFF_P + 2 * P_BYTES + 1024;       // + alignment slack
+constexpr int NSOFT = 128;
+constexpr int NPROD = 128;
+constexpr int THREADS = NSOFT + NPROD + 32;
+constexpr int TMEM_COLS = 512;
+constexpr int TM_S = 0;    // two S buffers: columns [0, 32) and [32, 64)
+constexpr int TM_O = 256;  // O: columns [256, 512)
+constexpr float kLazyMax = 8.f;  // log2 growth of the running maximum that forces a rescale
+static_assert(OFF_STAGE % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_P % 1024 == 0 &&
+                  OFF_XOUT % 1024 == 0 && OFF_XIN % 1024 == 0,
+              "align");
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+
+// mbarriers
+enum {
+  B_FULL = 0,                 // [NST] producer -> MMA: stage filled (128 cp.async arrivals)
+  B_EMPTY = B_FULL + NST,     // [NST] MMA -> producer: stage read (tcgen05.commit)
+  B_SFULL = B_EMPTY + NST,    // [2]   MMA -> softmax: S buffer ready (tcgen05.commit)
+  B_PFULL = B_SFULL + 2,      //       softmax -> MMA: P written (128 arrivals)
+  B_PVDONE = B_PFULL + 1,     //       MMA -> softmax: P V done (tcgen05.commit)
+  B_XFULL = B_PVDONE + 1,     // [2]   the peer's partial S landed (own expect_tx + the
+                              //       peer's bulk copy bytes)
+  B_XEMPTY = B_XFULL + 2,     // [2]   the peer read the partial I sent (4 remote arrivals)
+  B_FINAL = B_XEMPTY + 2,     //       every MMA of the CTA complete
+  NBARS = B_FINAL + 1
+};
+
+}  // namespace mlatc
+
+namespace mlatc_detail {
+
+using namespace dev;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Wait with cluster-scope acquire (the barrier's arrivals come from the peer CTA).
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory into the peer's (cluster addresses for
+// the destination and its mbarrier), completing as transaction bytes on that mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// 16-byte global -> shared copy, zero-filled when src_bytes == 0 (nothing is read then).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+      "r"(src_bytes), "l"(policy)
+      : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets, swizzle
+// (2 = 128-byte, 4 = 64-byte), fixed version bits 46-47 = 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)swizzle << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A / B both bf16 (ab = 1) or both
+// fp16 (ab = 0), B MN-major when b_mn, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, uint32_t ab, uint32_t b_mn) {
+  return (1u << 4) | (ab << 7) | (ab << 10) | (b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+}  // namespace mlatc_detail
+
+template <typename T>
+__global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaParams p) {
+  using namespace dev;
+  using namespace mlatc;
+  using namespace mlatc_detail;
+  constexpr float kNegInfF = -__builtin_huge_valf();
+  constexpr uint32_t kAB = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  __shared__ __align__(8) uint64_t bars[NBARS];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag_s;
+  __shared__ int merge_last_s;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* base =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(base);
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  volatile int* abort_flag = &abort_flag_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();  // 0: features [0, 256); 1: [256, 512) and the rope part
+  const int nblk = rank ? QBLK : QBLK - 1;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int item = blockIdx.x / p.gslices;
+  const int gs = blockIdx.x - item * p.gslices;  // head tile * 2 + rank
+  const WorkItem it = p.items[item];
+  const int H = p.num_heads;
+  const int g0 = (gs >> 1) * HT;
+  const int gcnt = min(HT, H - g0);
+  int j0 = 0, ntiles = 0;
+  if (it.tok_end > it.tok_begin) {
+    j0 = (it.tok_begin - it.chunk_tok0) / TS;
+    ntiles = (it.tok_end - it.chunk_tok0 + TS - 1) / TS - j0;
+  }
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(B_FULL + s), NPROD);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFULL + 1), 1);
+    mbar_init(bar(B_PFULL), NSOFT);
+    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_XFULL), 1);
+    mbar_init(bar(B_XFULL + 1), 1);
+    mbar_init(bar(B_XEMPTY), NSOFT / 32);
+    mbar_init(bar(B_XEMPTY + 1), NSOFT / 32);
+    mbar_init(bar(B_FINAL), 1);
+    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // Q part of this CTA -> 128-byte-swizzled K-major blocks (heads past H are zero rows); all
+  // loads are issued before the first store so their latencies overlap
+  {
+    constexpr int kQIter = (HT * QBLK * 8 + THREADS - 1) / THREADS;
+    const int nch = nblk * 8;
+    uint4 v[kQIter];
+#pragma unroll
+    for (int k = 0; k < kQIter; ++k) {
+      const int u = threadIdx.x + k * THREADS;
+      const int h = u / nch, c = u - h * nch;
+      const int b = c >> 3, ch = c & 7;
+      v[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (u < HT * nch && h < gcnt) {
+        const size_t row = (size_t)it.req * H + g0 + h;
+        const T* src = b < 4 ? static_cast<const T*>(p.q_nope) + row * DC + rank * 256 + b * 64 + ch * 8
+                             : static_cast<const T*>(p.q_pe) + row * DP + ch * 8;
+        v[k] = __ldg(reinterpret_cast<const uint4*>(src));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kQIter; ++k) {
+      const int u = threadIdx.x + k * THREADS;
+      const int h = u / nch, c = u - h * nch;
+      const int b = c >> 3, ch = c & 7;
+      if (u < HT * nch)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         sb + OFF_Q + b * QBLK_BYTES + h * 128 + ((ch ^ (h & 7)) << 4)),
+                     "r"(v[k].x), "r"(v[k].y), "r"(v[k].z), "r"(v[k].w)
+                     : "memory");
+    }
+  }
+  fence_proxy_async_smem();  // Q (generic stores) before the MMAs read it
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  if (abort_flag_s) ntiles = 0;  // an earlier launch timed out: do nothing, write nothing
+
+  if (warp == 8) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = instr_desc(HT, TS, kAB, 0u);
+      const uint32_t id_pv = instr_desc(HT, 256, kAB, 1u);
+      const uint64_t qdesc0 = smem_desc(sb + OFF_Q, 16, 1024, 2);
+      const uint64_t pdesc0 = smem_desc(sb + OFF_P, 16, 512, 4);  // hi; lo P_BYTES after
+      auto pv = [&](int i) {
+        if (!mbar_wait(bar(B_PFULL), (uint32_t)(i & 1), abort_flag)) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+        }
+        tc_fence_after();
+        const uint32_t stage = sb + OFF_STAGE + (i % NST) * STAGE_BYTES;
+        const uint64_t vdesc0 = smem_desc(stage, 4096, 1024, 2);  // V^T: MN-major
+        // O += P_hi V + P_lo V: P = P_hi + P_lo to about 2^-17, so rounding P to 16 bits
+        // costs no accuracy
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            tc_mma(tmem + TM_O, pdesc0 + (uint64_t)((part * P_BYTES + ks * 32) >> 4),
+                   vdesc0 + (uint64_t)(ks * 2048 >> 4), id_pv,
+                   (i > 0 || part > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(B_PVDONE));
+        tc_commit(bar(B_EMPTY + i % NST));
+      };
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NST;
+        if (!mbar_wait(bar(B_FULL + s), (uint32_t)((j / NST) & 1), abort_flag)) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+        }
+        fence_proxy_async_smem();  // the cp.async (generic) writes before the tensor core reads
+        tc_fence_after();
+        const uint32_t stage = sb + OFF_STAGE + s * STAGE_BYTES;
+        const uint64_t kdesc0 = smem_desc(stage, 16, 1024, 2);
+        for (int b = 0; b < nblk; ++b)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(tmem + TM_S + 32 * (j & 1),
+                   qdesc0 + (uint64_t)((b * QBLK_BYTES + kk * 32) >> 4),
+                   kdesc0 + (uint64_t)((b * BLK_BYTES + kk * 32) >> 4), id_qk,
+                   (b | kk) ? 1u : 0u);
+        tc_commit(bar(B_SFULL + (j & 1)));
+        if (j > 0) pv(j - 1);
+      }
+      if (ntiles > 0) pv(ntiles - 1);
+      tc_commit(bar(B_FINAL));
+      volatile int never = 0;
+      mbar_wait(bar(B_FINAL), 0u, &never);  // every MMA done before TMEM is freed
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================================================================ producer
+    const int pw = warp - 4;  // rows 8 pw .. 8 pw + 7 of each tile
+    const int ps = p.page_size;
+    const char* ckv = static_cast<const char*>(p.ckv) + rank * 512;
+    const char* kpe = static_cast<const char*>(p.kpe);
+    const uint64_t pol = policy_evict_first();
+    // lane r (< 8): page id of tile row 8 pw + r of tile i, one tile ahead; -1: not a token of
+    // the item (the row is zero-filled)
+    auto page_of = [&](int i) -> int64_t {
+      const int t = it.chunk_tok0 + (j0 + i) * TS + 8 * pw + (lane & 7);
+      return (i < ntiles && t >= it.tok_begin && t < it.tok_end)
+                 ? (int64_t)__ldg(p.indices + it.page_base + t / ps)
+                 : -1;
+    };
+    int64_t pid_next = page_of(0);
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NST;
+      const int64_t pid_mine = pid_next;
+      pid_next = page_of(i + 1);
+      if (i >= NST) {
+        int freed = 1;
+        if (lane == 0)
+          freed = mbar_wait(bar(B_EMPTY + s), (uint32_t)(((i / NST) - 1) & 1), abort_flag) ? 1 : 0;
+        if (!__shfl_sync(~0u, freed, 0) && lane == 0) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+        }
+      }
+      const uint32_t stage = sb + OFF_STAGE + s * STAGE_BYTES;
+      const int tt0 = it.chunk_tok0 + (j0 + i) * TS;
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int row = 8 * pw + rr;
+        const int64_t pid = __shfl_sync(~0u, pid_mine, rr);
+        const bool ok = pid >= 0 && pid < p.num_pages;
+        const int64_t prow = ok ? pid * ps + (tt0 + row) % ps : 0;
+        const uint32_t sw = (uint32_t)(row & 7);
+        // ckv: lane = 16-byte chunk c of this CTA's 512 bytes (block c / 8)
+        cp_async16(stage + (lane >> 3) * BLK_BYTES + row * 128 + (((uint32_t)(lane & 7) ^ sw) << 4),
+                   ckv + prow * (DC * 2) + lane * 16, ok ? 16u : 0u, pol);
+        if (rank && lane < 8)
+          cp_async16(stage + 4 * BLK_BYTES + row * 128 + (((uint32_t)lane ^ sw) << 4),
+                     kpe + prow * (DP * 2) + lane * 16, ok ? 16u : 0u, pol);
+      }
+      cp_async_arrive(bar(B_FULL + s));
+    }
+    cp_async_wait_all();
+  } else {
+    // ================================================================ softmax (thread = head)
+    const int h = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + TM_S + lane_off, tO = tmem + TM_O + lane_off;
+    const uint32_t peer = (uint32_t)(rank ^ 1);
+    const uint32_t xrow = (uint32_t)h * 128u, xsw = (uint32_t)(h & 7);
+    const uint32_t xin_peer = map_peer(sb + OFF_XIN, peer);
+    const uint32_t xfull_peer = map_peer(bar(B_XFULL), peer);
+    const uint32_t xempty_peer = map_peer(bar(B_XEMPTY), peer);
+    const uint32_t prow_addr = sb + OFF_P + h * 64;
+    const uint32_t psw = (uint32_t)((h >> 1) & 3);
+    float m_ref = kNegInfF, lsum = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
+      bool ok = mbar_wait(bar(B_SFULL + b), ph, abort_flag);
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(tS + 32 * b, v);
+      // ---- exchange the partial logits with the peer CTA: my partial goes to the peer's
+      // buffer b in one bulk copy once the peer has read what I sent two tiles ago (which
+      // also means that copy has finished reading my buffer b)
+      if (h == 0 && j >= 2) ok &= wait_cluster(bar(B_XEMPTY + b), ph ^ 1u, abort_flag);
+      named_bar_sync(2, NSOFT);
+      const uint32_t xout = sb + OFF_XOUT + b * XBUF_BYTES + xrow;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         xout + ((((uint32_t)q) ^ xsw) << 4)),
+                     "f"(v[4 * q]), "f"(v[4 * q + 1]), "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                     : "memory");
+      fence_proxy_async_smem();  // generic stores before the bulk copy reads them
+      named_bar_sync(2, NSOFT);
+      if (h == 0) {
+        mbar_arrive_expect_tx(bar(B_XFULL + b), (uint32_t)XBUF_BYTES);  // the peer's copy to me
+        bulk_copy_to_peer(xin_peer + b * XBUF_BYTES, sb + OFF_XOUT + b * XBUF_BYTES,
+                          (uint32_t)XBUF_BYTES, xfull_peer + 8 * b);
+      }
+      ok &= mbar_wait(bar(B_XFULL + b), ph, abort_flag);
+      const uint32_t xin = sb + OFF_XIN + b * XBUF_BYTES + xrow;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 w = lds_v4(xin + ((((uint32_t)q) ^ xsw) << 4));
+        v[4 * q] += __uint_as_float(w.x);
+        v[4 * q + 1] += __uint_as_float(w.y);
+        v[4 * q + 2] += __uint_as_float(w.z);
+        v[4 * q + 3] += __uint_as_float(w.w);
+      }
+      __syncwarp();
+      if (lane == 0) arrive_remote(xempty_peer + 8 * b);  // my buffer b read: the peer may refill
+      // ---- logits, lazy online softmax
+      const int t0 = it.chunk_tok0 + (j0 + j) * TS;
+      float mx = kNegInfF;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int t = t0 + e;
+        v[e] = (t >= it.tok_begin && t < it.tok_end) ? v[e] * p.scale_log2 : kNegInfF;
+        mx = fmaxf(mx, v[e]);
+      }
+      float alpha = 1.f;
+      bool resc = false;
+      if (mx > m_ref + kLazyMax) {  // also the first tile (m_ref = -inf)
+        if (m_ref != kNegInfF) {
+          alpha = fast_exp2(m_ref - mx);
+          resc = true;
+        }
+        m_ref = mx;
+      }
+      const float ref = m_ref == kNegInfF ? 0.f : m_ref;
+      float ps = 0.f;
+      uint32_t pk[16], pl[16];  // P rounded to 16 bits, and the rounding remainder
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float a = fast_exp2(v[e] - ref), c = fast_exp2(v[e + 1] - ref);
+        ps += a + c;
+        pk[e >> 1] = pack2<T>(a, c);
+        const float2 r = unpack2<T>(pk[e >> 1]);
+        pl[e >> 1] = pack2<T>(a - r.x, c - r.y);
+      }
+      lsum = lsum * alpha + ps;
+      // ---- P V of the previous tile done: P buffer free, O stable
+      if (j > 0) ok &= mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), abort_flag);
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.status, kStatusTimeout);
+      }
+      tc_fence_after();
+      if (__any_sync(~0u, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float o[32];
+          tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tO + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t a = prow_addr + ((((uint32_t)q) ^ psw) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * q]),
+                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + P_BYTES), "r"(pl[4 * q]),
+                     "r"(pl[4 * q + 1]), "r"(pl[4 * q + 2]), "r"(pl[4 * q + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL));
+    }
+    if (ntiles > 0) {
+      if (!mbar_wait(bar(B_PVDONE), (uint32_t)((ntiles - 1) & 1), abort_flag)) {
+        *abort_flag = 1;
+        atomicOr(p.status, kStatusTimeout);
+      }
+      tc_fence_after();
+    }
+    named_bar_sync(1, NSOFT);
+    const bool aborted = *abort_flag != 0;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float lse2 = lsum > 0.f ? m_ref + log2f(lsum) : kNegInfF;
+    constexpr float kLn2f = 0.6931471805599453f;
+    const bool live = h < gcnt && !aborted;
+    const size_t orow = (size_t)it.req * H + g0 + h;
+    const size_t prow_o = ((size_t)(it.out_slot < 0 ? 0 : it.out_slot) * 2 + rank) * H + g0 + h;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      float o[32];
+      if (ntiles > 0) {
+        tmem_ld32(tO + 32 * c, o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (!live) continue;
+      if (it.out_slot < 0) {
+        T* dst = static_cast<T*>(p.o) + orow * DC + rank * 256 + c * 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack2<T>(o[8 * q] * inv, o[8 * q + 1] * inv);
+          w.y = pack2<T>(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+          w.z = pack2<T>(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+          w.w = pack2<T>(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+          *reinterpret_cast<uint4*>(dst + 8 * q) = w;
+        }
+      } else {
+        float* dst = p.part_o + prow_o * 256 + c * 32;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(dst + 4 * q) =
+              make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+      }
+    }
+    if (live) {
+      if (it.out_slot < 0) {
+        if (rank == 0 && p.lse) p.lse[orow] = p.lse_base_e ? lse2 * kLn2f : lse2;
+      } else {
+        p.part_lse[prow_o] = lse2;
+      }
+    }
+    // ---- fused merge: the CTA finishing a split request's last chunk for its (tile, half)
+    if (it.out_slot >= 0) {
+      __threadfence();
+      named_bar_sync(1, NSOFT);
+      if (h == 0) {
+        int last = 0;
+        if (!aborted) {
+          uint32_t* ctr = p.counters + (size_t)it.merge_idx * p.gslices + gs;
+          const uint32_t prev = atomicAdd(ctr, 1u);
+          last = (prev + 1u == (uint32_t)p.merges[it.merge_idx].n_chunks) ? 1 : 0;
+          if (last) *ctr = 0u;
+        }
+        merge_last_s = last;
+      }
+      named_bar_sync(1, NSOFT);
+      if (merge_last_s) {
+        __threadfence();
+        const MergeEntry me = p.merges[it.merge_idx];
+        for (int u = h; u < gcnt * 32; u += NSOFT) {
+          const int hd = u >> 5, d0 = (u & 31) * 8;
+          auto pidx = [&](int c) -> size_t {
+            return ((size_t)(me.first_slot + c) * 2 + rank) * H + g0 + hd;
+          };
+          float M = kNegInfF;
+          for (int c = 0; c < me.n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + pidx(c)));
+          float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float W = 0.f;
+          if (M != kNegInfF) {
+            for (int c = 0; c < me.n_chunks; ++c) {
+              const size_t pi = pidx(c);
+              const float w = fast_exp2(__ldcg(p.part_lse + pi) - M);
+              const float4* src = reinterpret_cast<const float4*>(p.part_o + pi * 256 + d0);
+              const float4 a = __ldcg(src), bq = __ldcg(src + 1);
+              W += w;
+              o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
+              o[4] += w * bq.x; o[5] += w * bq.y; o[6] += w * bq.z; o[7] += w * bq.w;
+            }
+          }
+          const float iw = W > 0.f ? 1.f / W : 0.f;
+          uint4 w;
+          w.x = pack2<T>(o[0] * iw, o[1] * iw);
+          w.y = pack2<T>(o[2] * iw, o[3] * iw);
+          w.z = pack2<T>(o[4] * iw, o[5] * iw);
+          w.w = pack2<T>(o[6] * iw, o[7] * iw);
+          *reinterpret_cast<uint4*>(static_cast<T*>(p.o) +
+                                    ((size_t)me.req * H + g0 + hd) * DC + rank * 256 + d0) = w;
+          if (rank == 0 && d0 == 0 && p.lse) {
+            const float l2 = W > 0.f ? M + log2f(W) : kNegInfF;
+            p.lse[(size_t)me.req * H + g0 + hd] = p.lse_base_e ? l2 * kLn2f : l2;
+          }
+        }
+      }
+    }
+  }
+  // ---- teardown: no CTA leaves while its peer may still write to it; TMEM freed last
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();
+  if (warp == 8) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace pkd

@@ -46,13 +46,14 @@ void init_registry() {
     register_decode_rope(g_decode);
     register_merge(g_merge);
     register_mla(g_mla);
+    register_mla_tc(g_mla);
   });
 }
 
-const MlaKernel* find_mla(int dtype) {
+const MlaKernel* find_mla(int dtype, int variant) {
   init_registry();
   for (const auto& k : g_mla)
-    if (k.dtype == dtype) return &k;
+    if (k.dtype == dtype && k.variant == variant) return &k;
   return nullptr;
 }
 
@@ -124,6 +125,7 @@ struct pkd_handle {
   int pos_mode = 0;  // PKD_POS_*
   bool mla = false;  // the current plan is an MLA plan (pkd_mla_plan)
   const MlaKernel* mla_kernel = nullptr;
+  int mla_backend = PKD_MLA_BACKEND_AUTO;  // pkd_mla_set_backend
   int q_dtype = 0, kv_dtype = 0, o_dtype = 0;
   float sm_scale = 0.f, cap = 0.f;
   const int32_t* indices = nullptr;
@@ -668,6 +670,13 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   if (batch > 0 && (!kv_indices_dev || num_indices < (int64_t)kv_indptr_host[batch]))
     return fail(PKD_ERR_INVALID_ARG, "kv_indices holds fewer than kv_indptr[batch] page ids");
 
+  // auto: the tcgen05 pair kernel when a head tile of 128 is at least half full
+  int variant = h->mla_backend == PKD_MLA_BACKEND_MMA_SYNC   ? kMlaMmaSync
+                : h->mla_backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
+                : num_heads > 64                            ? kMlaTcgen05
+                                                            : kMlaMmaSync;
+  const MlaKernel* k = find_mla(q_dtype, variant);
+  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
   PlanRequest r;
   std::memset(&r, 0, sizeof r);
   r.indptr = kv_indptr_host;
@@ -683,18 +692,20 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   r.num_sms = h->num_sms;
   r.q_len = 1;
   r.mla = 1;
-  r.mla_heads_per_cta = 32;
-  r.mla_tile_tokens = 32;
-  r.ctas_per_sm = 1;  // the MLA kernel takes most of an SM's shared memory
+  r.mla_heads_per_cta = k->heads_per_cta;
+  r.mla_tile_tokens = k->tile_tokens;
+  r.mla_ctas_per_head_tile = k->ctas_per_head_tile;
+  r.ctas_per_sm = 1;  // both MLA kernels take most of an SM's shared memory
   Plan plan;
   const char* err = "";
   int rc = build_plan(r, &plan, &err);
   if (rc) return fail(rc, err);
-  const MlaKernel* k = find_mla(q_dtype);
-  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
 
+  // partials: [slots, H * cph, 512 / cph] fp32 and [slots, H * cph] lse (cph CTAs per head tile
+  // each keep their own lse copy)
+  const int cph = k->ctas_per_head_tile;
   const WsLayout lay = layout_of(plan, 1);
-  const size_t need_f = float_ws_bytes_of(lay, num_heads, head_dim_ckv);
+  const size_t need_f = float_ws_bytes_of(lay, num_heads * cph, head_dim_ckv / cph);
   const size_t need_i = int_ws_bytes_of(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
     char buf[200];
@@ -795,10 +806,18 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
   prm.o = o;
   prm.lse = lse;
   prm.part_o = reinterpret_cast<float*>(fws);
-  prm.part_lse = reinterpret_cast<float*>(fws + part_lse_offset(lay, h->num_qo_heads, h->head_dim));
+  const int cph = h->mla_kernel->ctas_per_head_tile;
+  prm.part_lse = reinterpret_cast<float*>(
+      fws + part_lse_offset(lay, h->num_qo_heads * cph, h->head_dim / cph));
   prm.num_pages = num_pages;
   prm.num_heads = h->num_qo_heads;
   prm.gslices = h->plan.gslices;
+  // mma.sync kernel: the head slices of one item share every K row and form a cluster of up
+  // to 8 CTAs (one copy of each row, multicast); tcgen05 kernel: the CTA pair of a head tile
+  int csize = 8;
+  while (prm.gslices % csize) csize >>= 1;
+  if (h->mla_kernel->variant == kMlaTcgen05) csize = 2;
+  prm.cluster_size = csize;
   prm.page_size = h->page_size;
   prm.lse_base_e = lse_base_e ? 1 : 0;
   prm.scale_log2 = (float)((double)h->sm_scale * 1.4426950408889634);
@@ -814,16 +833,29 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
     cfg.blockDim = dim3(h->mla_kernel->threads);
     cfg.dynamicSmemBytes = (size_t)h->mla_kernel->smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = h->pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)csize;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelExC(&cfg, h->mla_kernel->fn, args);
   }
   if (e != cudaSuccess) return cuda_fail(e, "MLA decode kernel launch");
   if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
+  return PKD_OK;
+}
+
+int pkd_mla_set_backend(pkd_handle* h, int backend) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (backend != PKD_MLA_BACKEND_AUTO && backend != PKD_MLA_BACKEND_MMA_SYNC &&
+      backend != PKD_MLA_BACKEND_TCGEN05)
+    return fail(PKD_ERR_INVALID_ARG, "backend must be PKD_MLA_BACKEND_AUTO, _MMA_SYNC or _TCGEN05");
+  h->mla_backend = backend;
   return PKD_OK;
 }
 

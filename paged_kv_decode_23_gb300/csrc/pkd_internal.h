@@ -131,22 +131,30 @@ struct MlaParams {
   uint32_t* counters;     // per (merge entry, head slice)
   int64_t num_pages;      // pages in the caches: ids outside [0, num_pages) read as zeros
   int num_heads;
-  int gslices;            // ceil(H / 32)
+  int gslices;            // CTAs per item: head tiles x CTAs per head tile
+  int cluster_size;       // CTAs per cluster: largest of 8, 4, 2, 1 dividing gslices
   int page_size;
   int lse_base_e;         // 1: lse as natural log, 0: base 2 (run()'s default)
   float scale_log2;       // sm_scale * log2(e)
 };
 
-// MLA decode kernels (mla.cu): latent 512 + rope 64, one kernel per q / cache dtype.
+// MLA decode kernels, latent 512 + rope 64, one per q / cache dtype and variant:
+//   kMlaMmaSync (mla.cu): 32 heads per CTA, mma.sync, register accumulators;
+//   kMlaTcgen05 (mla_tc.cu): 128 heads per CTA pair (a 2-CTA cluster splitting the features),
+//   tcgen05 MMAs with TMEM accumulators.
+enum MlaVariant { kMlaAuto = 0, kMlaMmaSync = 1, kMlaTcgen05 = 2 };
 struct MlaKernel {
   int dtype;
+  int variant;
   const void* fn;
   int threads;
   int smem_bytes;
   int heads_per_cta;
   int tile_tokens;
+  int ctas_per_head_tile;  // CTAs sharing one head tile (each with its own lse partials)
 };
 void register_mla(std::vector<MlaKernel>& out);
+void register_mla_tc(std::vector<MlaKernel>& out);
 void register_merge(std::vector<MergeKernel>& out);
 
 // ----------------------------------------------------------------------------- planner
@@ -173,6 +181,7 @@ struct PlanRequest {
   int mla = 0;
   int mla_heads_per_cta = 32;
   int mla_tile_tokens = 32;
+  int mla_ctas_per_head_tile = 1;
   int ctas_per_sm = 2;
 };
 

@@ -86,6 +86,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     plan->heads_per_cta = r.mla_heads_per_cta;
   }
   plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
+  if (r.mla) plan->gslices *= r.mla_ctas_per_head_tile;
   if (r.rope && plan->kind == kCudaCore) {
     *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
     return kErrUnsupported;
@@ -185,6 +186,23 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
         if (ctas_with(mid) <= slots) hi = mid; else lo = mid + ps;
       }
       C = longest > lo ? lo : 0;
+    } else if (r.mla) {
+      // MLA kernels hold one CTA (pair) per SM and whole waves of them: split the requests
+      // into k equal chunks for the k that minimises waves x (chunk + per-item overhead)
+      // tokens (batch 114 x 999 tokens: two chunks, three full waves instead of 1.5).
+      constexpr int64_t kItemOverhead = 64;
+      double best_cost = 0.0;
+      for (int64_t k = 1; k <= 16; ++k) {
+        const int64_t c = ((longest + k - 1) / k + ps - 1) / ps * ps;
+        if (k > 1 && c < c_min) break;
+        const int64_t ctas = k == 1 ? (int64_t)rows * ctas_per_item : ctas_with(c);
+        const double cost =
+            (double)((ctas + slots - 1) / slots) * (double)(std::min(c, longest) + kItemOverhead);
+        if (k == 1 || cost < best_cost) {
+          best_cost = cost;
+          C = (k == 1 || c >= longest) ? 0 : c;
+        }
+      }
     } else {
       // More requests than one wave: chunks of about the average load of a CTA slot over
       // kWavesTarget waves, so the longest requests stop bounding the tail.

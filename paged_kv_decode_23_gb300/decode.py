@@ -337,13 +337,22 @@ class CUDAGraphBatchDecodePagedKV(BatchDecodePagedKV):
                          int_workspace_buffer=int_workspace_buffer, max_items=max_items)
 
 
+_MLA_BACKEND = {"auto": 0, "fa2": 1, "tcgen05": 2}
+
+
 class BatchMLAPagedAttention:
     """MLA paged decode (the pages' BatchMLAPagedAttentionWrapper): every query head attends
     over one latent cache; key = [ckv, kpe] (512 + 64), value = ckv.  Decode only: every
-    query length in ``qo_indptr`` must be 1."""
+    query length in ``qo_indptr`` must be 1.
+
+    ``backend``: "auto" (the tcgen05 kernel for more than 64 heads, else "fa2"), "fa2" (32
+    heads per CTA on mma.sync with register accumulators) or "tcgen05" (128 heads per 2-CTA
+    cluster on the 5th-generation tensor cores, accumulators in tensor memory)."""
 
     def __init__(self, float_workspace_buffer: torch.Tensor,
-                 int_workspace_buffer: Optional[torch.Tensor] = None):
+                 int_workspace_buffer: Optional[torch.Tensor] = None, backend: str = "auto"):
+        if backend not in _MLA_BACKEND:
+            raise ValueError(f"backend must be one of {sorted(_MLA_BACKEND)}")
         if not float_workspace_buffer.is_cuda:
             raise ValueError("the float workspace must be a CUDA tensor")
         if int_workspace_buffer is None:
@@ -359,6 +368,7 @@ class BatchMLAPagedAttention:
                                    self._int_ws.numel() * self._int_ws.element_size(),
                                    L.LAYOUT_NHD))
         self._h = h
+        L.check(L.lib().pkd_mla_set_backend(h, _MLA_BACKEND[backend]))
 
     def __del__(self):
         h = getattr(self, "_h", None)

@@ -13,10 +13,14 @@ pytestmark = pytest.mark.gpu
 CODE = {"bf16": oracle.BF16, "f16": oracle.F16}
 
 
-def _run(w, qn, qp, ckv, kpe, base_e=True, ws_mb=256):
+BACKENDS = ["fa2", "tcgen05"]
+
+
+def _run(w, qn, qp, ckv, kpe, base_e=True, ws_mb=256, backend="auto"):
     from paged_kv_decode_23_gb300 import BatchMLAPagedAttention
     dev = torch.device("cuda")
-    mla = BatchMLAPagedAttention(torch.zeros(ws_mb << 20, dtype=torch.uint8, device=dev))
+    mla = BatchMLAPagedAttention(torch.zeros(ws_mb << 20, dtype=torch.uint8, device=dev),
+                                 backend=backend)
     idx = torch.from_numpy(w.kv_indices if len(w.kv_indices) else np.zeros(1, np.int32)).to(dev)
     mla.plan(torch.arange(w.batch + 1, dtype=torch.int32), torch.from_numpy(w.kv_indptr), idx,
              torch.from_numpy(w.kv_lens), w.num_heads, 512, 64, w.page_size, False, w.sm_scale,
@@ -47,37 +51,57 @@ def _close(got, ref, what, lse_base_e=True):
     assert fin.sum() == 0 or np.abs(lse[fin] - rl[fin]).max() <= 1e-3, f"{what}: lse"
 
 
+@pytest.mark.parametrize("backend", BACKENDS)
 @pytest.mark.parametrize("ps", [1, 16, 64])
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
-def test_mla_lengths_pages_dtypes(ps, dt):
+def test_mla_lengths_pages_dtypes(ps, dt, backend):
     lens = [1, 31, 32, 33, 0, 100, 777, 64]
-    w = W.mla_custom(lens, 40, ps, dt, seed=ps, extra_pages=1)  # 40 heads: a partial slice
+    # 40 heads: a partial head slice (fa2) or a head tile of 128 with 88 empty rows (tcgen05)
+    w = W.mla_custom(lens, 40, ps, dt, seed=ps, extra_pages=1)
     qn, qp = W.make_mla_q(w)
     ckv, kpe = W.make_mla_cache(w)
     ref = _oracle(w, qn, qp, ckv, kpe)
-    _close(_run(w, qn, qp, ckv, kpe), ref, f"mla ps={ps} {dt}")
-    _close(_run(w, qn, qp, ckv, kpe, base_e=False), ref, f"mla ps={ps} {dt} base 2",
-           lse_base_e=False)
+    _close(_run(w, qn, qp, ckv, kpe, backend=backend), ref, f"mla ps={ps} {dt} {backend}")
+    _close(_run(w, qn, qp, ckv, kpe, base_e=False, backend=backend), ref,
+           f"mla ps={ps} {dt} {backend} base 2", lse_base_e=False)
 
 
-@pytest.mark.parametrize("heads", [16, 32, 128])
-def test_mla_split_requests(heads):
+@pytest.mark.parametrize("backend", BACKENDS)
+@pytest.mark.parametrize("heads", [16, 32, 128, 192])
+def test_mla_split_requests(heads, backend):
     """A small batch of long requests is split into chunks (one wave of CTAs) and merged
-    inside the launch."""
+    inside the launch; 192 heads take two head tiles on the tcgen05 kernel."""
     w = W.mla_custom([3000, 4500, 20], heads, 1, "bf16", seed=heads)
     qn, qp = W.make_mla_q(w)
     ckv, kpe = W.make_mla_cache(w)
-    _close(_run(w, qn, qp, ckv, kpe), _oracle(w, qn, qp, ckv, kpe), f"mla split H={heads}")
+    _close(_run(w, qn, qp, ckv, kpe, backend=backend), _oracle(w, qn, qp, ckv, kpe),
+           f"mla split H={heads} {backend}")
 
 
-def test_mla_full_example_sampled():
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_mla_logits_far_apart(backend):
+    """Latent rows shifted by a ramp over the page pool spread the logits over tens of units,
+    so the running maximum of a head jumps by more than 8 (log2) several times along a
+    request and the lazily kept output must be rescaled; the softmax is nearly one-hot."""
+    w = W.mla_custom([700, 64, 2000], 128, 1, "bf16", seed=5)
+    w.sm_scale = 0.5
+    qn, qp = W.make_mla_q(w)
+    ckv, kpe = W.make_mla_cache(w)
+    ramp = torch.linspace(0.0, 3.0, ckv.shape[0]).to(ckv.dtype).view(-1, 1, 1)
+    ckv = (ckv.float() + ramp.float() * qn.float().mean(dim=(0, 1)).sign()).to(ckv.dtype)
+    _close(_run(w, qn, qp, ckv, kpe, backend=backend), _oracle(w, qn, qp, ckv, kpe),
+           f"mla far-apart logits {backend}")
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_mla_full_example_sampled(backend):
     """The pages' example at full size (batch 114, 128 heads, kv_len 999, page_size 1),
     sampled requests against the oracle."""
     w = W.mla_workload()
     dev = torch.device("cuda")
     qn, qp = W.make_mla_q(w, device=dev)
     ckv, kpe = W.make_mla_cache(w, device=dev)
-    got = _run(w, qn, qp, ckv, kpe)
+    got = _run(w, qn, qp, ckv, kpe, backend=backend)
     for i in (0, 57, 113):
         sub = W.mla_custom([int(w.kv_lens[i])], w.num_heads, 1, "bf16")
         pages = w.kv_indices[w.kv_indptr[i]:w.kv_indptr[i + 1]]
@@ -102,6 +126,30 @@ def test_mla_rejects_other_shapes():
         mla.plan(torch.tensor([0, 1], dtype=torch.int32), torch.tensor([0, 4], dtype=torch.int32),
                  idx, torch.tensor([5], dtype=torch.int32), 16, 512, 64, 1, False, 0.1,
                  torch.bfloat16, torch.bfloat16)
+    with pytest.raises(ValueError):
+        BatchMLAPagedAttention(torch.zeros(1 << 20, dtype=torch.uint8, device=dev), backend="fa3")
     with pytest.raises(NotImplementedError):  # two queries in a request
         mla.plan(torch.tensor([0, 2], dtype=torch.int32), *args[1:], 512, 64, 1, False, 0.1,
                  torch.bfloat16, torch.bfloat16)
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_mla_page_ids_outside_the_caches_read_as_zero_rows(backend):
+    """A page id outside [0, num_pages) reads as a zero row (logit 0, value 0), as a read past
+    the end of the caches does; checked against the oracle on caches with an appended zero page
+    that those ids point to."""
+    w = W.mla_custom([40, 300, 77], 128, 4, "bf16", seed=11)
+    qn, qp = W.make_mla_q(w)
+    ckv, kpe = W.make_mla_cache(w)
+    npg = ckv.shape[0]
+    bad = w.kv_indices.copy()
+    bad[[0, 5, 13, 40, 41, len(bad) - 1]] = [npg, -1, npg + 7, -5, npg, 2 ** 30]
+    w_bad = W.mla_custom([40, 300, 77], 128, 4, "bf16", seed=11)
+    w_bad.kv_indices = bad
+    got = _run(w_bad, qn, qp, ckv, kpe, backend=backend)
+    ref_idx = np.where((bad < 0) | (bad >= npg), npg, bad).astype(np.int32)
+    w_ref = W.mla_custom([40, 300, 77], 128, 4, "bf16", seed=11)
+    w_ref.kv_indices = ref_idx
+    zc = torch.cat([ckv, torch.zeros_like(ckv[:1])])
+    zk = torch.cat([kpe, torch.zeros_like(kpe[:1])])
+    _close(got, _oracle(w_ref, qn, qp, zc, zk), f"mla bad page ids {backend}")
