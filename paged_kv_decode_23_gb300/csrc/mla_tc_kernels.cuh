@@ -8,23 +8,29 @@
 //   CTA 0 holds q_nope[:, 0:256], loads ckv[t, 0:256] and owns O[:, 0:256];
 //   CTA 1 holds q_nope[:, 256:512] and q_pe, loads ckv[t, 256:512] and kpe[t], owns O[:, 256:512].
 // Each CTA's logit MMA gives a partial S over its features; the two partials are exchanged
-// through distributed shared memory and added (a + b == b + a exactly, so both CTAs hold the
-// same S, the same softmax and the same P), and each CTA multiplies P by the value columns it
-// loaded itself.  Every byte of the caches is read once, by one CTA.
+// through distributed shared memory (one bulk shared-to-shared copy per tile) and added
+// (a + b == b + a exactly, so both CTAs hold the same S, the same softmax and the same P), and
+// each CTA multiplies P by the value columns it loaded itself.  Every byte of the caches is
+// read once, by one CTA.
 //
 // Roles (288 threads):
-//   warps 0-3  softmax: thread h owns head h (TMEM lane h): reads its partial S row, exchanges
-//              it, runs the online softmax (lazy reference, rescaling O in TMEM only when the
-//              running maximum grows by more than 2^8), writes P (bf16 / fp16) to shared memory;
-//              epilogue and fused merge.
+//   warps 0-3  softmax: thread h owns head h (TMEM lane h).  The exchange runs two tiles
+//              ahead of the softmax (S is triple-buffered in TMEM), so its latency hides behind
+//              the softmax of the tiles in between.  Online softmax with a lazy reference (O in
+//              TMEM is rescaled only when the running maximum grows by more than 2^8); P goes to
+//              TMEM as a 16-bit value and its rounding remainder (P_hi + P_lo), so the 16-bit
+//              rounding of P costs no accuracy.  Epilogue through shared memory (coalesced
+//              stores) and the fused merge of split requests.
 //   warps 4-7  producer: 16-byte cp.async gathers of the token rows (any page size; a TMA
 //              request per row is rate-bound for rows this small), zero-filled for tokens
 //              outside the item and for page ids outside the caches, into NST stages laid out
-//              as the MMA's 128-byte-swizzled K-major blocks (8 rows x 128 bytes per atom).
+//              as the MMA's 128-byte-swizzled K-major blocks (8 rows x 128 bytes per atom).  It
+//              starts before Q is loaded.
 //   warp 8     MMA issuer (one thread) and TMEM owner: S = Q K^T as M=128 x N=32 MMAs over
-//              16-feature steps into one of two S buffers, then O += P V as two M=128 x N=256
-//              MMAs with V read MN-major from the same stage blocks.  tcgen05.commit signals the
-//              softmax (S ready, PV done) and the producer (stage free).
+//              16-feature steps, issued two tiles ahead of O += P V (four M=128 x N=256 MMAs,
+//              A = P_hi / P_lo from TMEM, V read MN-major from the same stage blocks).
+//              tcgen05.commit signals the softmax (S ready, PV done) and the producer (stage
+//              free).
 // Every wait is bounded; a timeout sets the status word and the kernel runs on without waiting
 // (the output is then not written).  No CTA leaves before its peer (cluster barrier).
 #pragma once
@@ -42,44 +48,50 @@ constexpr int DC = 512;
 constexpr int DP = 64;
 constexpr int HT = 128;                       // heads per CTA: the MMA's M
 constexpr int TS = 32;                        // tokens per tile: the logit MMA's N
-constexpr int NST = 3;                        // pipeline stages
+constexpr int NST = 4;                        // pipeline stages
 constexpr int QBLK = 5;                       // 64-feature blocks held by CTA 1 (CTA 0: 4)
 constexpr int QBLK_BYTES = HT * 128;          // 16384
 constexpr int BLK_BYTES = TS * 128;           // 4096: one 64-feature block of a tile
 constexpr int STAGE_BYTES = QBLK * BLK_BYTES;  // 20480
 constexpr int XBUF_BYTES = HT * TS * 4;      // 16384: a partial S tile, 128-byte rows, chunk
                                               // q of head h at chunk q ^ (h & 7)
-constexpr int P_BYTES = HT * 64;              // 32 tokens x 2 bytes per head, 64-byte swizzle
 constexpr int OFF_Q = 0;
 constexpr int OFF_STAGE = OFF_Q + QBLK * QBLK_BYTES;         // 81920
 constexpr int OFF_XOUT = OFF_STAGE + NST * STAGE_BYTES;      // 143360: my partial, 2 buffers
-constexpr int OFF_XIN = OFF_XOUT + 2 * XBUF_BYTES;           // 176128: the peer's, 2 buffers
-constexpr int OFF_P = OFF_XIN + 2 * XBUF_BYTES;              // 208896: P hi, then P lo
-constexpr int SMEM_BYTES = OFF_P + 2 * P_BYTES + 1024;       // + alignment slack
+constexpr int OFF_XIN = OFF_XOUT + 2 * XBUF_BYTES;           // the peer's partials, 2 buffers
+constexpr int SMEM_BYTES = OFF_XIN + 2 * XBUF_BYTES + 1024;  // + alignment slack
+// epilogue staging (rows of 256 outputs) reuses [OFF_STAGE, ...): stages, then the exchange
+constexpr int STAGE_OUT_BYTES = HT * 256 * 4;
 constexpr int NSOFT = 128;
 constexpr int NPROD = 128;
 constexpr int THREADS = NSOFT + NPROD + 32;
 constexpr int TMEM_COLS = 512;
-constexpr int TM_S = 0;    // two S buffers: columns [0, 32) and [32, 64)
-constexpr int TM_O = 256;  // O: columns [256, 512)
+constexpr int TM_S = 0;      // three S buffers: columns [0, 96)
+constexpr int TM_PHI = 96;   // P, 16-bit pairs: columns [96, 112)
+constexpr int TM_PLO = 112;  // its rounding remainder: columns [112, 128)
+constexpr int TM_O = 256;    // O: columns [256, 512)
 constexpr float kLazyMax = 8.f;  // log2 growth of the running maximum that forces a rescale
-static_assert(OFF_STAGE % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_P % 1024 == 0 &&
-                  OFF_XOUT % 1024 == 0 && OFF_XIN % 1024 == 0,
+constexpr int kIdTiles = 8;  // the producer loads page ids this many tiles ahead
+static_assert(OFF_STAGE % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_XOUT % 1024 == 0 &&
+                  OFF_XIN % 1024 == 0,
               "align");
+static_assert(OFF_STAGE + STAGE_OUT_BYTES <= OFF_XIN + XBUF_BYTES, "epilogue staging fits");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // mbarriers
 enum {
   B_FULL = 0,                 // [NST] producer -> MMA: stage filled (128 cp.async arrivals)
   B_EMPTY = B_FULL + NST,     // [NST] MMA -> producer: stage read (tcgen05.commit)
-  B_SFULL = B_EMPTY + NST,    // [2]   MMA -> softmax: S buffer ready (tcgen05.commit)
-  B_PFULL = B_SFULL + 2,      //       softmax -> MMA: P written (128 arrivals)
+  B_SFULL = B_EMPTY + NST,    // [3]   MMA -> softmax: S buffer ready (tcgen05.commit)
+  B_PFULL = B_SFULL + 3,      //       softmax -> MMA: P written (128 arrivals)
   B_PVDONE = B_PFULL + 1,     //       MMA -> softmax: P V done (tcgen05.commit)
   B_XFULL = B_PVDONE + 1,     // [2]   the peer's partial S landed (own expect_tx + the
                               //       peer's bulk copy bytes)
-  B_XEMPTY = B_XFULL + 2,     // [2]   the peer read the partial I sent (4 remote arrivals)
+  B_XEMPTY = B_XFULL + 2,     // [2]   the peer read the partial I sent (one remote arrival
+                              //       per softmax warp)
   B_FINAL = B_XEMPTY + 2,     //       every MMA of the CTA complete
-  NBARS = B_FINAL + 1
+  B_MERGE = B_FINAL + 1,      //       a block of another chunk's partials loaded (merge)
+  NBARS = B_MERGE + 1
 };
 
 }  // namespace mlatc
@@ -98,6 +110,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -105,8 +123,10 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+// Relaxed: no cluster-scope fence.  Used only to say "I have read buffer b", after the values
+// read have been consumed (so the loads are complete when this issues).
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
@@ -190,6 +210,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       : "memory");
 }
 
+// The same with A (M=128 rows x 16 values, two 16-bit values per column) read from TMEM.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -233,6 +263,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -245,11 +286,13 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
   using namespace mlatc;
   using namespace mlatc_detail;
   constexpr float kNegInfF = -__builtin_huge_valf();
+  constexpr float kLn2f = 0.6931471805599453f;
   constexpr uint32_t kAB = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   __shared__ __align__(8) uint64_t bars[NBARS];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag_s;
   __shared__ int merge_last_s;
+  __shared__ float wself_s[HT], wchunk_s[HT];  // merge weights per head
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* base =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -257,6 +300,10 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
   const uint32_t bar0 = smem_u32(&bars[0]);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   volatile int* abort_flag = &abort_flag_s;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(p.status, kStatusTimeout);
+  };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_rank();  // 0: features [0, 256); 1: [256, 512) and the rope part
   const int nblk = rank ? QBLK : QBLK - 1;
@@ -281,8 +328,8 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
       mbar_init(bar(B_FULL + s), NPROD);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
+#pragma unroll
+    for (int s = 0; s < 3; ++s) mbar_init(bar(B_SFULL + s), 1);
     mbar_init(bar(B_PFULL), NSOFT);
     mbar_init(bar(B_PVDONE), 1);
     mbar_init(bar(B_XFULL), 1);
@@ -290,6 +337,7 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
     mbar_init(bar(B_XEMPTY), NSOFT / 32);
     mbar_init(bar(B_XEMPTY + 1), NSOFT / 32);
     mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_MERGE), 1);
     abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
     fence_mbar_init();
   }
@@ -300,125 +348,55 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Q part of this CTA -> 128-byte-swizzled K-major blocks (heads past H are zero rows); all
-  // loads are issued before the first store so their latencies overlap
-  {
-    constexpr int kQIter = (HT * QBLK * 8 + THREADS - 1) / THREADS;
-    const int nch = nblk * 8;
-    uint4 v[kQIter];
-#pragma unroll
-    for (int k = 0; k < kQIter; ++k) {
-      const int u = threadIdx.x + k * THREADS;
-      const int h = u / nch, c = u - h * nch;
-      const int b = c >> 3, ch = c & 7;
-      v[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (u < HT * nch && h < gcnt) {
-        const size_t row = (size_t)it.req * H + g0 + h;
-        const T* src = b < 4 ? static_cast<const T*>(p.q_nope) + row * DC + rank * 256 + b * 64 + ch * 8
-                             : static_cast<const T*>(p.q_pe) + row * DP + ch * 8;
-        v[k] = __ldg(reinterpret_cast<const uint4*>(src));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kQIter; ++k) {
-      const int u = threadIdx.x + k * THREADS;
-      const int h = u / nch, c = u - h * nch;
-      const int b = c >> 3, ch = c & 7;
-      if (u < HT * nch)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         sb + OFF_Q + b * QBLK_BYTES + h * 128 + ((ch ^ (h & 7)) << 4)),
-                     "r"(v[k].x), "r"(v[k].y), "r"(v[k].z), "r"(v[k].w)
-                     : "memory");
-    }
-  }
-  fence_proxy_async_smem();  // Q (generic stores) before the MMAs read it
   tc_fence_before();
-  cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   if (abort_flag_s) ntiles = 0;  // an earlier launch timed out: do nothing, write nothing
 
-  if (warp == 8) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_qk = instr_desc(HT, TS, kAB, 0u);
-      const uint32_t id_pv = instr_desc(HT, 256, kAB, 1u);
-      const uint64_t qdesc0 = smem_desc(sb + OFF_Q, 16, 1024, 2);
-      const uint64_t pdesc0 = smem_desc(sb + OFF_P, 16, 512, 4);  // hi; lo P_BYTES after
-      auto pv = [&](int i) {
-        if (!mbar_wait(bar(B_PFULL), (uint32_t)(i & 1), abort_flag)) {
-          *abort_flag = 1;
-          atomicOr(p.status, kStatusTimeout);
-        }
-        tc_fence_after();
-        const uint32_t stage = sb + OFF_STAGE + (i % NST) * STAGE_BYTES;
-        const uint64_t vdesc0 = smem_desc(stage, 4096, 1024, 2);  // V^T: MN-major
-        // O += P_hi V + P_lo V: P = P_hi + P_lo to about 2^-17, so rounding P to 16 bits
-        // costs no accuracy
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            tc_mma(tmem + TM_O, pdesc0 + (uint64_t)((part * P_BYTES + ks * 32) >> 4),
-                   vdesc0 + (uint64_t)(ks * 2048 >> 4), id_pv,
-                   (i > 0 || part > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(bar(B_PVDONE));
-        tc_commit(bar(B_EMPTY + i % NST));
-      };
-      for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NST;
-        if (!mbar_wait(bar(B_FULL + s), (uint32_t)((j / NST) & 1), abort_flag)) {
-          *abort_flag = 1;
-          atomicOr(p.status, kStatusTimeout);
-        }
-        fence_proxy_async_smem();  // the cp.async (generic) writes before the tensor core reads
-        tc_fence_after();
-        const uint32_t stage = sb + OFF_STAGE + s * STAGE_BYTES;
-        const uint64_t kdesc0 = smem_desc(stage, 16, 1024, 2);
-        for (int b = 0; b < nblk; ++b)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma(tmem + TM_S + 32 * (j & 1),
-                   qdesc0 + (uint64_t)((b * QBLK_BYTES + kk * 32) >> 4),
-                   kdesc0 + (uint64_t)((b * BLK_BYTES + kk * 32) >> 4), id_qk,
-                   (b | kk) ? 1u : 0u);
-        tc_commit(bar(B_SFULL + (j & 1)));
-        if (j > 0) pv(j - 1);
-      }
-      if (ntiles > 0) pv(ntiles - 1);
-      tc_commit(bar(B_FINAL));
-      volatile int never = 0;
-      mbar_wait(bar(B_FINAL), 0u, &never);  // every MMA done before TMEM is freed
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
+  if (warp >= 4 && warp < 8) {
     // ================================================================ producer
+    cluster_arrive();  // nothing here depends on the peer: start at once
     const int pw = warp - 4;  // rows 8 pw .. 8 pw + 7 of each tile
     const int ps = p.page_size;
     const char* ckv = static_cast<const char*>(p.ckv) + rank * 512;
     const char* kpe = static_cast<const char*>(p.kpe);
     const uint64_t pol = policy_evict_first();
-    // lane r (< 8): page id of tile row 8 pw + r of tile i, one tile ahead; -1: not a token of
-    // the item (the row is zero-filled)
-    auto page_of = [&](int i) -> int64_t {
+    // lane r (< 8; lanes 8-31 repeat lanes 0-7): page id of tile row 8 pw + r of tile i, or -1
+    // for a row that is not a token of the item (zero-filled).  ids[k] holds tile i + k: the
+    // ids of a tile are loaded kIdTiles iterations before its copies, and the rows of tile
+    // i + kIdTiles - 2 are prefetched into L2 (a stage is refilled only after the P V that
+    // reads it, so without the prefetch each refill would wait a full DRAM latency).
+    auto page_of = [&](int i) -> int {
       const int t = it.chunk_tok0 + (j0 + i) * TS + 8 * pw + (lane & 7);
       return (i < ntiles && t >= it.tok_begin && t < it.tok_end)
-                 ? (int64_t)__ldg(p.indices + it.page_base + t / ps)
+                 ? __ldg(p.indices + it.page_base + t / ps)
                  : -1;
     };
-    int64_t pid_next = page_of(0);
+    int ids[kIdTiles];
+#pragma unroll
+    for (int k = 0; k < kIdTiles; ++k) ids[k] = page_of(k);
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % NST;
-      const int64_t pid_mine = pid_next;
-      pid_next = page_of(i + 1);
+      const int64_t pid_mine = ids[0];
+      {
+        const int pf = __shfl_sync(~0u, ids[kIdTiles - 2], lane >> 2);  // row lane / 4
+        const int tpf = it.chunk_tok0 + (j0 + i + kIdTiles - 2) * TS + 8 * pw + (lane >> 2);
+        if (pf >= 0 && (int64_t)pf < p.num_pages) {
+          const int64_t r = (int64_t)pf * ps + tpf % ps;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(ckv + r * (DC * 2) + (lane & 3) * 128));
+          if (rank && (lane & 3) == 0)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(kpe + r * (DP * 2)));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k + 1 < kIdTiles; ++k) ids[k] = ids[k + 1];
+      ids[kIdTiles - 1] = page_of(i + kIdTiles);
       if (i >= NST) {
         int freed = 1;
         if (lane == 0)
           freed = mbar_wait(bar(B_EMPTY + s), (uint32_t)(((i / NST) - 1) & 1), abort_flag) ? 1 : 0;
-        if (!__shfl_sync(~0u, freed, 0) && lane == 0) {
-          *abort_flag = 1;
-          atomicOr(p.status, kStatusTimeout);
-        }
+        if (!__shfl_sync(~0u, freed, 0) && lane == 0) fail();
       }
       const uint32_t stage = sb + OFF_STAGE + s * STAGE_BYTES;
       const int tt0 = it.chunk_tok0 + (j0 + i) * TS;
@@ -439,219 +417,379 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
       cp_async_arrive(bar(B_FULL + s));
     }
     cp_async_wait_all();
+    cluster_wait();
   } else {
-    // ================================================================ softmax (thread = head)
-    const int h = threadIdx.x;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + TM_S + lane_off, tO = tmem + TM_O + lane_off;
-    const uint32_t peer = (uint32_t)(rank ^ 1);
-    const uint32_t xrow = (uint32_t)h * 128u, xsw = (uint32_t)(h & 7);
-    const uint32_t xin_peer = map_peer(sb + OFF_XIN, peer);
-    const uint32_t xfull_peer = map_peer(bar(B_XFULL), peer);
-    const uint32_t xempty_peer = map_peer(bar(B_XEMPTY), peer);
-    const uint32_t prow_addr = sb + OFF_P + h * 64;
-    const uint32_t psw = (uint32_t)((h >> 1) & 3);
-    float m_ref = kNegInfF, lsum = 0.f;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      bool ok = mbar_wait(bar(B_SFULL + b), ph, abort_flag);
-      tc_fence_after();
-      float v[32];
-      tmem_ld32(tS + 32 * b, v);
-      // ---- exchange the partial logits with the peer CTA: my partial goes to the peer's
-      // buffer b in one bulk copy once the peer has read what I sent two tiles ago (which
-      // also means that copy has finished reading my buffer b)
-      if (h == 0 && j >= 2) ok &= wait_cluster(bar(B_XEMPTY + b), ph ^ 1u, abort_flag);
-      named_bar_sync(2, NSOFT);
-      const uint32_t xout = sb + OFF_XOUT + b * XBUF_BYTES + xrow;
+    // Q part of this CTA -> 128-byte-swizzled K-major blocks (heads past H are zero rows), by
+    // the softmax and MMA warps while the producer already streams K; loads are issued in
+    // batches of 16 before their stores so their latencies overlap
+    {
+      constexpr int kQT = NSOFT + 32;
+      constexpr int kBatch = 16;
+      const int nch = nblk * 8;
+      const int tq = warp == 8 ? NSOFT + lane : (int)threadIdx.x;
+      for (int k0 = 0; k0 * kQT < HT * QBLK * 8; k0 += kBatch) {
+        uint4 v[kBatch];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         xout + ((((uint32_t)q) ^ xsw) << 4)),
-                     "f"(v[4 * q]), "f"(v[4 * q + 1]), "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
-                     : "memory");
-      fence_proxy_async_smem();  // generic stores before the bulk copy reads them
-      named_bar_sync(2, NSOFT);
-      if (h == 0) {
-        mbar_arrive_expect_tx(bar(B_XFULL + b), (uint32_t)XBUF_BYTES);  // the peer's copy to me
-        bulk_copy_to_peer(xin_peer + b * XBUF_BYTES, sb + OFF_XOUT + b * XBUF_BYTES,
-                          (uint32_t)XBUF_BYTES, xfull_peer + 8 * b);
+        for (int k = 0; k < kBatch; ++k) {
+          const int u = tq + (k0 + k) * kQT;
+          const int h = u / nch, c = u - h * nch;
+          const int b = c >> 3, ch = c & 7;
+          v[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (u < HT * nch && h < gcnt) {
+            const size_t row = (size_t)it.req * H + g0 + h;
+            const T* src = b < 4 ? static_cast<const T*>(p.q_nope) + row * DC + rank * 256 + b * 64 +
+                                       ch * 8
+                                 : static_cast<const T*>(p.q_pe) + row * DP + ch * 8;
+            v[k] = __ldg(reinterpret_cast<const uint4*>(src));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int u = tq + (k0 + k) * kQT;
+          const int h = u / nch, c = u - h * nch;
+          const int b = c >> 3, ch = c & 7;
+          if (u < HT * nch)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             sb + OFF_Q + b * QBLK_BYTES + h * 128 + ((ch ^ (h & 7)) << 4)),
+                         "r"(v[k].x), "r"(v[k].y), "r"(v[k].z), "r"(v[k].w)
+                         : "memory");
+        }
       }
-      ok &= mbar_wait(bar(B_XFULL + b), ph, abort_flag);
-      const uint32_t xin = sb + OFF_XIN + b * XBUF_BYTES + xrow;
+    }
+    fence_proxy_async_smem();  // Q (generic stores) before the MMAs read it
+    cluster_arrive();          // also: both CTAs' barriers initialised before any remote use
+    cluster_wait();
+
+    if (warp == 8) {
+      // ============================================================== MMA issuer
+      if (lane == 0) {
+        const uint32_t id_qk = instr_desc(HT, TS, kAB, 0u);
+        const uint32_t id_pv = instr_desc(HT, 256, kAB, 1u);
+        const uint64_t qdesc0 = smem_desc(sb + OFF_Q, 16, 1024, 2);
+        auto qk = [&](int i) {
+          const int s = i % NST;
+          if (!mbar_wait(bar(B_FULL + s), (uint32_t)((i / NST) & 1), abort_flag)) fail();
+          fence_proxy_async_smem();  // the cp.async (generic) writes before the tensor core reads
+          tc_fence_after();
+          const uint64_t kdesc0 = smem_desc(sb + OFF_STAGE + s * STAGE_BYTES, 16, 1024, 2);
+          const uint32_t d = tmem + TM_S + 32 * (i % 3);
+          for (int b = 0; b < nblk; ++b)
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 w = lds_v4(xin + ((((uint32_t)q) ^ xsw) << 4));
-        v[4 * q] += __uint_as_float(w.x);
-        v[4 * q + 1] += __uint_as_float(w.y);
-        v[4 * q + 2] += __uint_as_float(w.z);
-        v[4 * q + 3] += __uint_as_float(w.w);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma(d, qdesc0 + (uint64_t)((b * QBLK_BYTES + kk * 32) >> 4),
+                     kdesc0 + (uint64_t)((b * BLK_BYTES + kk * 32) >> 4), id_qk,
+                     (b | kk) ? 1u : 0u);
+          tc_commit(bar(B_SFULL + i % 3));
+        };
+        auto pv = [&](int i) {
+          if (!mbar_wait(bar(B_PFULL), (uint32_t)(i & 1), abort_flag)) fail();
+          tc_fence_after();
+          const uint64_t vdesc0 =
+              smem_desc(sb + OFF_STAGE + (i % NST) * STAGE_BYTES, 4096, 1024, 2);  // MN-major
+          // O += P_hi V + P_lo V: P = P_hi + P_lo to about 2^-17
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)
+              tc_mma_ts(tmem + TM_O, tmem + (part ? TM_PLO : TM_PHI) + ks * 8,
+                        vdesc0 + (uint64_t)(ks * 2048 >> 4), id_pv,
+                        (i > 0 || part > 0 || ks > 0) ? 1u : 0u);
+          tc_commit(bar(B_PVDONE));
+          tc_commit(bar(B_EMPTY + i % NST));
+        };
+        // logits run two tiles ahead of P V (three S buffers)
+        if (ntiles > 0) qk(0);
+        if (ntiles > 1) qk(1);
+        for (int i = 0; i < ntiles; ++i) {
+          if (i + 2 < ntiles) qk(i + 2);
+          pv(i);
+        }
+        tc_commit(bar(B_FINAL));
+        volatile int never = 0;
+        mbar_wait(bar(B_FINAL), 0u, &never);  // every MMA done before TMEM is freed
       }
       __syncwarp();
-      if (lane == 0) arrive_remote(xempty_peer + 8 * b);  // my buffer b read: the peer may refill
-      // ---- logits, lazy online softmax
-      const int t0 = it.chunk_tok0 + (j0 + j) * TS;
-      float mx = kNegInfF;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = t0 + e;
-        v[e] = (t >= it.tok_begin && t < it.tok_end) ? v[e] * p.scale_log2 : kNegInfF;
-        mx = fmaxf(mx, v[e]);
-      }
-      float alpha = 1.f;
-      bool resc = false;
-      if (mx > m_ref + kLazyMax) {  // also the first tile (m_ref = -inf)
-        if (m_ref != kNegInfF) {
-          alpha = fast_exp2(m_ref - mx);
-          resc = true;
-        }
-        m_ref = mx;
-      }
-      const float ref = m_ref == kNegInfF ? 0.f : m_ref;
-      float ps = 0.f;
-      uint32_t pk[16], pl[16];  // P rounded to 16 bits, and the rounding remainder
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float a = fast_exp2(v[e] - ref), c = fast_exp2(v[e + 1] - ref);
-        ps += a + c;
-        pk[e >> 1] = pack2<T>(a, c);
-        const float2 r = unpack2<T>(pk[e >> 1]);
-        pl[e >> 1] = pack2<T>(a - r.x, c - r.y);
-      }
-      lsum = lsum * alpha + ps;
-      // ---- P V of the previous tile done: P buffer free, O stable
-      if (j > 0) ok &= mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), abort_flag);
-      if (!ok) {
-        *abort_flag = 1;
-        atomicOr(p.status, kStatusTimeout);
-      }
-      tc_fence_after();
-      if (__any_sync(~0u, resc)) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float o[32];
-          tmem_ld32(tO + 32 * c, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tO + 32 * c, o);
-        }
-        tmem_wait_st();
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t a = prow_addr + ((((uint32_t)q) ^ psw) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * q]),
-                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + P_BYTES), "r"(pl[4 * q]),
-                     "r"(pl[4 * q + 1]), "r"(pl[4 * q + 2]), "r"(pl[4 * q + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
-    }
-    if (ntiles > 0) {
-      if (!mbar_wait(bar(B_PVDONE), (uint32_t)((ntiles - 1) & 1), abort_flag)) {
-        *abort_flag = 1;
-        atomicOr(p.status, kStatusTimeout);
-      }
-      tc_fence_after();
-    }
-    named_bar_sync(1, NSOFT);
-    const bool aborted = *abort_flag != 0;
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    const float lse2 = lsum > 0.f ? m_ref + log2f(lsum) : kNegInfF;
-    constexpr float kLn2f = 0.6931471805599453f;
-    const bool live = h < gcnt && !aborted;
-    const size_t orow = (size_t)it.req * H + g0 + h;
-    const size_t prow_o = ((size_t)(it.out_slot < 0 ? 0 : it.out_slot) * 2 + rank) * H + g0 + h;
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      float o[32];
-      if (ntiles > 0) {
-        tmem_ld32(tO + 32 * c, o);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
-      }
-      if (!live) continue;
-      if (it.out_slot < 0) {
-        T* dst = static_cast<T*>(p.o) + orow * DC + rank * 256 + c * 32;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack2<T>(o[8 * q] * inv, o[8 * q + 1] * inv);
-          w.y = pack2<T>(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-          w.z = pack2<T>(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-          w.w = pack2<T>(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-          *reinterpret_cast<uint4*>(dst + 8 * q) = w;
-        }
-      } else {
-        float* dst = p.part_o + prow_o * 256 + c * 32;
+    } else {
+      // ============================================================== softmax (thread = head)
+      const int h = threadIdx.x;
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      const uint32_t peer = (uint32_t)(rank ^ 1);
+      const uint32_t xrow = (uint32_t)h * 128u, xsw = (uint32_t)(h & 7);
+      const uint32_t xin_peer = map_peer(sb + OFF_XIN, peer);
+      const uint32_t xfull_peer = map_peer(bar(B_XFULL), peer);
+      const uint32_t xempty_peer = map_peer(bar(B_XEMPTY), peer);
+      bool ok = true;
+      // My partial S of tile j: into v, and into the peer's exchange buffer j % 2, each warp
+      // its 32 rows by one bulk copy, once the peer has read what I sent there two tiles ago
+      // (which also means those copies have finished reading my buffer j % 2).
+      auto send = [&](int j, float (&v)[32]) {
+        const uint32_t b = (uint32_t)(j & 1);
+        ok &= mbar_wait(bar(B_SFULL + j % 3), (uint32_t)((j / 3) & 1), abort_flag);
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + TM_S + 32 * (j % 3), v);
+        if (lane == 0 && j >= 2)
+          ok &= wait_cluster(bar(B_XEMPTY + b), (uint32_t)(((j >> 1) - 1) & 1), abort_flag);
+        __syncwarp();
+        const uint32_t xo = sb + OFF_XOUT + b * XBUF_BYTES + xrow;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(dst + 4 * q) =
-              make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv, o[4 * q + 3] * inv);
-      }
-    }
-    if (live) {
-      if (it.out_slot < 0) {
-        if (rank == 0 && p.lse) p.lse[orow] = p.lse_base_e ? lse2 * kLn2f : lse2;
-      } else {
-        p.part_lse[prow_o] = lse2;
-      }
-    }
-    // ---- fused merge: the CTA finishing a split request's last chunk for its (tile, half)
-    if (it.out_slot >= 0) {
-      __threadfence();
-      named_bar_sync(1, NSOFT);
-      if (h == 0) {
-        int last = 0;
-        if (!aborted) {
-          uint32_t* ctr = p.counters + (size_t)it.merge_idx * p.gslices + gs;
-          const uint32_t prev = atomicAdd(ctr, 1u);
-          last = (prev + 1u == (uint32_t)p.merges[it.merge_idx].n_chunks) ? 1 : 0;
-          if (last) *ctr = 0u;
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           xo + ((((uint32_t)q) ^ xsw) << 4)),
+                       "f"(v[4 * q]), "f"(v[4 * q + 1]), "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                       : "memory");
+        fence_proxy_async_smem();  // generic stores before the bulk copy reads them
+        __syncwarp();
+        if (lane == 0) {
+          if (h == 0)  // the peer's four copies to me, 16 KB in all
+            mbar_arrive_expect_tx(bar(B_XFULL + b), (uint32_t)XBUF_BYTES);
+          const uint32_t off = b * XBUF_BYTES + (uint32_t)warp * 32u * 128u;
+          bulk_copy_to_peer(xin_peer + off, sb + OFF_XOUT + off, 32u * 128u, xfull_peer + 8 * b);
         }
-        merge_last_s = last;
+      };
+      float m_ref = kNegInfF, lsum = 0.f;
+      float va[32], vb[32];  // my partials of tiles j and j + 1
+      if (ntiles > 0) send(0, va);
+      if (ntiles > 1) send(1, vb);
+      for (int j = 0; j < ntiles; ++j) {
+        const uint32_t b = (uint32_t)(j & 1);
+        // ---- the peer's partial of tile j
+        ok &= mbar_wait(bar(B_XFULL + b), (uint32_t)((j >> 1) & 1), abort_flag);
+        const uint32_t xi = sb + OFF_XIN + b * XBUF_BYTES + xrow;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = lds_v4(xi + ((((uint32_t)q) ^ xsw) << 4));
+          va[4 * q] += __uint_as_float(w.x);
+          va[4 * q + 1] += __uint_as_float(w.y);
+          va[4 * q + 2] += __uint_as_float(w.z);
+          va[4 * q + 3] += __uint_as_float(w.w);
+        }
+        // ---- logits, lazy online softmax
+        const int t0 = it.chunk_tok0 + (j0 + j) * TS;
+        float mx = kNegInfF;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int t = t0 + e;
+          va[e] = (t >= it.tok_begin && t < it.tok_end) ? va[e] * p.scale_log2 : kNegInfF;
+          mx = fmaxf(mx, va[e]);
+        }
+        float alpha = 1.f;
+        bool resc = false;
+        if (mx > m_ref + kLazyMax) {  // also the first tile (m_ref = -inf)
+          if (m_ref != kNegInfF) {
+            alpha = fast_exp2(m_ref - mx);
+            resc = true;
+          }
+          m_ref = mx;
+        }
+        const float ref = m_ref == kNegInfF ? 0.f : m_ref;
+        float ps = 0.f;
+        uint32_t pk[16], pl[16];  // P rounded to 16 bits, and the rounding remainder
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float a = fast_exp2(va[e] - ref), c = fast_exp2(va[e + 1] - ref);
+          ps += a + c;
+          pk[e >> 1] = pack2<T>(a, c);
+          const float2 r = unpack2<T>(pk[e >> 1]);
+          pl[e >> 1] = pack2<T>(a - r.x, c - r.y);
+        }
+        lsum = lsum * alpha + ps;
+        // buffer b read (the values are consumed above): the peer may refill it
+        __syncwarp();
+        if (lane == 0) arrive_remote_relaxed(xempty_peer + 8 * b);
+        // ---- P V of the previous tile done: P columns free, O stable
+        if (j > 0) ok &= mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), abort_flag);
+        if (!ok) {
+          fail();
+          ok = true;
+        }
+        tc_fence_after();
+        if (__any_sync(~0u, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tmem + lane_off + TM_O + 32 * c, o);
+          }
+        }
+        tmem_st16(tmem + lane_off + TM_PHI, pk);
+        tmem_st16(tmem + lane_off + TM_PLO, pl);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL));
+        // ---- the exchange two tiles ahead
+#pragma unroll
+        for (int e = 0; e < 32; ++e) va[e] = vb[e];
+        if (j + 2 < ntiles) send(j + 2, vb);
+      }
+
+      // ---- epilogue: O / l through shared memory (stages and exchange buffers, now idle)
+      if (ntiles > 0) {
+        ok &= mbar_wait(bar(B_PVDONE), (uint32_t)((ntiles - 1) & 1), abort_flag);
+        tc_fence_after();
+      }
+      if (h == 0)  // my last copies have landed and been read (their sources are reused here)
+        for (int jj = ntiles - 2; jj < ntiles; ++jj)
+          if (jj >= 0)
+            ok &= wait_cluster(bar(B_XEMPTY + (jj & 1)), (uint32_t)((jj >> 1) & 1), abort_flag);
+      if (!ok) fail();
+      named_bar_sync(1, NSOFT);
+      const bool aborted = *abort_flag != 0;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float lse2 = lsum > 0.f ? m_ref + log2f(lsum) : kNegInfF;
+      const bool split = it.out_slot >= 0;
+      auto prow_of = [&](int slot, int row) -> size_t {  // [slots, 2 (rank), H] partial rows
+        return ((size_t)slot * 2 + rank) * H + g0 + row;
+      };
+      // row r in 16-byte chunks q at (q & ~7) | ((q ^ r) & 7): conflict-free per warp
+      auto swz = [](int q, int r) -> uint32_t { return (uint32_t)((q & ~7) | ((q ^ r) & 7)) << 4; };
+      const uint32_t stg = sb + OFF_STAGE;
+      const int row_bytes = split ? 1024 : 512;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float o[32];
+        if (ntiles > 0) {
+          tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (split) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stg + h * row_bytes + swz(c * 8 + k, h)),
+                         "f"(o[4 * k] * inv), "f"(o[4 * k + 1] * inv), "f"(o[4 * k + 2] * inv),
+                         "f"(o[4 * k + 3] * inv)
+                         : "memory");
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stg + h * row_bytes + swz(c * 4 + k, h)),
+                         "r"(pack2<T>(o[8 * k] * inv, o[8 * k + 1] * inv)),
+                         "r"(pack2<T>(o[8 * k + 2] * inv, o[8 * k + 3] * inv)),
+                         "r"(pack2<T>(o[8 * k + 4] * inv, o[8 * k + 5] * inv)),
+                         "r"(pack2<T>(o[8 * k + 6] * inv, o[8 * k + 7] * inv))
+                         : "memory");
+        }
       }
       named_bar_sync(1, NSOFT);
-      if (merge_last_s) {
+      const int qrow = row_bytes / 16;
+      if (!aborted) {
+#pragma unroll 4
+        for (int u = h; u < gcnt * qrow; u += NSOFT) {
+          const int r = u / qrow, q = u - r * qrow;
+          const uint4 v = lds_v4(stg + r * row_bytes + swz(q, r));
+          if (split)
+            *reinterpret_cast<uint4*>(p.part_o + prow_of(it.out_slot, r) * 256 + q * 4) = v;
+          else
+            *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + ((size_t)it.req * H + g0 + r) * DC +
+                                      rank * 256 + q * 8) = v;
+        }
+        if (h < gcnt) {
+          if (split)
+            p.part_lse[prow_of(it.out_slot, h)] = lse2;
+          else if (rank == 0 && p.lse)
+            p.lse[(size_t)it.req * H + g0 + h] = p.lse_base_e ? lse2 * kLn2f : lse2;
+        }
+      }
+      // ---- fused merge: the CTA finishing a split request's last chunk for its (tile, half)
+      if (split) {
         __threadfence();
-        const MergeEntry me = p.merges[it.merge_idx];
-        for (int u = h; u < gcnt * 32; u += NSOFT) {
-          const int hd = u >> 5, d0 = (u & 31) * 8;
-          auto pidx = [&](int c) -> size_t {
-            return ((size_t)(me.first_slot + c) * 2 + rank) * H + g0 + hd;
-          };
-          float M = kNegInfF;
-          for (int c = 0; c < me.n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + pidx(c)));
-          float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          float W = 0.f;
-          if (M != kNegInfF) {
-            for (int c = 0; c < me.n_chunks; ++c) {
-              const size_t pi = pidx(c);
-              const float w = fast_exp2(__ldcg(p.part_lse + pi) - M);
-              const float4* src = reinterpret_cast<const float4*>(p.part_o + pi * 256 + d0);
-              const float4 a = __ldcg(src), bq = __ldcg(src + 1);
-              W += w;
-              o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
-              o[4] += w * bq.x; o[5] += w * bq.y; o[6] += w * bq.z; o[7] += w * bq.w;
-            }
+        named_bar_sync(1, NSOFT);
+        if (h == 0) {
+          int last = 0;
+          if (!aborted) {
+            uint32_t* ctr = p.counters + (size_t)it.merge_idx * p.gslices + gs;
+            const uint32_t prev = atomicAdd(ctr, 1u);
+            last = (prev + 1u == (uint32_t)p.merges[it.merge_idx].n_chunks) ? 1 : 0;
+            if (last) *ctr = 0u;
           }
+          merge_last_s = last;
+        }
+        named_bar_sync(1, NSOFT);
+        if (merge_last_s) {
+          // This CTA's own partial is still in the staging rows (fp32, 1 KB per head).  The
+          // other chunks' partials of this (head tile, half) are contiguous rows in global
+          // memory: each is brought in 64 heads at a time by one bulk copy into the (now idle)
+          // Q area and folded into the staging rows with coalesced shared-memory passes.
+          __threadfence();
+          const MergeEntry me = p.merges[it.merge_idx];
+          float M = lse2;
+          if (h < gcnt)
+            for (int c = 0; c < me.n_chunks; ++c)
+              if (me.first_slot + c != it.out_slot)
+                M = fmaxf(M, __ldcg(p.part_lse + prow_of(me.first_slot + c, h)));
+          float W = 0.f;
+          if (h < gcnt && M != kNegInfF)
+            for (int c = 0; c < me.n_chunks; ++c)
+              W += fast_exp2((me.first_slot + c == it.out_slot
+                                  ? lse2
+                                  : __ldcg(p.part_lse + prow_of(me.first_slot + c, h))) -
+                             M);
           const float iw = W > 0.f ? 1.f / W : 0.f;
-          uint4 w;
-          w.x = pack2<T>(o[0] * iw, o[1] * iw);
-          w.y = pack2<T>(o[2] * iw, o[3] * iw);
-          w.z = pack2<T>(o[4] * iw, o[5] * iw);
-          w.w = pack2<T>(o[6] * iw, o[7] * iw);
-          *reinterpret_cast<uint4*>(static_cast<T*>(p.o) +
-                                    ((size_t)me.req * H + g0 + hd) * DC + rank * 256 + d0) = w;
-          if (rank == 0 && d0 == 0 && p.lse) {
+          wself_s[h] = (M != kNegInfF) ? fast_exp2(lse2 - M) * iw : 0.f;
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // partials: generic -> TMA
+          uint32_t mphase = 0;
+          bool first = true;
+          for (int c = 0; c < me.n_chunks; ++c) {
+            const int slot = me.first_slot + c;
+            if (slot == it.out_slot) continue;
+            named_bar_sync(1, NSOFT);  // the previous chunk's passes are done with wchunk_s
+            wchunk_s[h] = (h < gcnt && M != kNegInfF)
+                              ? fast_exp2(__ldcg(p.part_lse + prow_of(slot, h)) - M) * iw
+                              : 0.f;
+            for (int r0 = 0; r0 < gcnt; r0 += 64) {
+              const int rows = min(64, gcnt - r0);
+              named_bar_sync(1, NSOFT);  // the buffer and the weights are ready for reuse
+              if (h == 0) {
+                mbar_arrive_expect_tx(bar(B_MERGE), (uint32_t)rows * 1024u);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                    "%2, [%3];" ::"r"(sb + OFF_Q),
+                    "l"(p.part_o + prow_of(slot, r0) * 256), "r"((uint32_t)rows * 1024u),
+                    "r"(bar(B_MERGE))
+                    : "memory");
+              }
+              if (!mbar_wait(bar(B_MERGE), mphase, abort_flag)) fail();
+              mphase ^= 1u;
+#pragma unroll 4
+              for (int u = h; u < rows * 64; u += NSOFT) {
+                const int r = u >> 6, q = u & 63, row = r0 + r;
+                const uint32_t oa = stg + row * 1024 + swz(q, row);
+                float4 o = *reinterpret_cast<const float4*>(base + (oa - sb));
+                const float4 x =
+                    *reinterpret_cast<const float4*>(base + OFF_Q + r * 1024 + q * 16);
+                const float ws = first ? wself_s[row] : 1.f, wc = wchunk_s[row];
+                o.x = o.x * ws + x.x * wc;
+                o.y = o.y * ws + x.y * wc;
+                o.z = o.z * ws + x.z * wc;
+                o.w = o.w * ws + x.w * wc;
+                *reinterpret_cast<float4*>(base + (oa - sb)) = o;
+              }
+            }
+            first = false;
+          }
+          named_bar_sync(1, NSOFT);
+#pragma unroll 4
+          for (int u = h; u < gcnt * 32; u += NSOFT) {
+            const int r = u >> 5, q = u & 31;
+            const float4 a = *reinterpret_cast<const float4*>(base + (stg - sb) + r * 1024 + swz(2 * q, r));
+            const float4 c2 =
+                *reinterpret_cast<const float4*>(base + (stg - sb) + r * 1024 + swz(2 * q + 1, r));
+            uint4 v;
+            v.x = pack2<T>(a.x, a.y);
+            v.y = pack2<T>(a.z, a.w);
+            v.z = pack2<T>(c2.x, c2.y);
+            v.w = pack2<T>(c2.z, c2.w);
+            *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + ((size_t)me.req * H + g0 + r) * DC +
+                                      rank * 256 + q * 8) = v;
+          }
+          if (h < gcnt && rank == 0 && p.lse) {
             const float l2 = W > 0.f ? M + log2f(W) : kNegInfF;
-            p.lse[(size_t)me.req * H + g0 + hd] = p.lse_base_e ? l2 * kLn2f : l2;
+            p.lse[(size_t)me.req * H + g0 + h] = p.lse_base_e ? l2 * kLn2f : l2;
           }
         }
       }
