@@ -39,12 +39,12 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on: once the sources differ, the figure no longer describes the kernel and the line
 # reports null.
 MEASURED_TRAFFIC = {
-    "sources_sha256": "a1d1d623e9ff105b52265e0316fdffd1bafe5c7895ba1a570d4cf03cdb2d1812",
-    # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set)
-    "uniform": 618.43e6,
-    "mix": 417.75e6,
-    "long": 2.153e9,
-    "lognormal": 3.524e9,
+    "sources_sha256": "3141d7e4f78165acc167263fb83df49a4e61edebc111305d667059e8a4c7c455",
+    # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set, bytes)
+    "uniform": 618456576.0,
+    "mix": 417777408.0,
+    "long": 2150532864.0,
+    "lognormal": 3525860352.0,
 }
 
 
