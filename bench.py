@@ -305,17 +305,14 @@ def gpu_arm(args, w, rank, world):
     seg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range((layers + 1) * args.steps)] if flush is not None else None
 
-    host_plan_s = [0.0]
     kernel_pass = [False]  # per-kernel events (they sit between launches, so a separate pass)
 
     def step(k=None):
         timed = seg is not None and k is not None and not kernel_pass[0]
         if timed:
             seg[k * (layers + 1)][0].record(stream)
-        t_h = time.perf_counter()
         dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                  w.page_size, **plan_kw)
-        host_plan_s[0] += time.perf_counter() - t_h
         if timed:
             seg[k * (layers + 1)][1].record(stream)
         for l in range(layers):
@@ -369,7 +366,15 @@ def gpu_arm(args, w, rank, world):
                       for k in range(args.steps))
         seg_detail = {"plan_us_per_step": plan_ms * 1e3 / args.steps,
                       "run_us_per_call": (ms_total - plan_ms) * 1e3 / (args.steps * layers)}
-    host_plan_us = host_plan_s[0] * 1e6 / (args.steps + args.warmup)
+    # the planner's own host cost: plan() calls with the GPU idle (inside the timed loop the
+    # host runs ahead of the GPU and plan() would also measure the queue's back-pressure)
+    torch.cuda.synchronize()
+    t_h = time.perf_counter()
+    for _ in range(20):
+        dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                 w.page_size, **plan_kw)
+    host_plan_us = (time.perf_counter() - t_h) * 1e6 / 20
+    torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in ev]
     assert dec.check_status() == 0, "device status word reports a failure"
 

@@ -132,10 +132,17 @@ struct pkd_handle {
   const DecodeKernel* kernel = nullptr;
   const MergeKernel* merge = nullptr;
 
-  void* staging = nullptr;  // pinned copy of the work list for the async upload
-  size_t staging_bytes = 0;
-  cudaEvent_t staging_done = nullptr;
-  bool staging_pending = false;
+  // Pinned copies of the work list for the async uploads, used in turn: plan() waits only for
+  // the upload of kStagingSlots plans ago, so a host that plans ahead of the GPU is not held up.
+  struct StagingSlot {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    cudaEvent_t done = nullptr;
+    bool pending = false;
+  };
+  static constexpr int kStagingSlots = 4;
+  StagingSlot staging[kStagingSlots];
+  int staging_next = 0;
   bool pdl = true;  // launch the decode kernel as a programmatic dependent of its predecessor
 
   // The workspace layout the current plan was uploaded in (its own counts, or capacities).
@@ -155,6 +162,40 @@ struct pkd_handle {
 };
 
 namespace {
+
+// The next staging slot with room for `bytes`, once its previous upload has completed.
+int staging_acquire(pkd_handle* h, size_t bytes, char** out, int* slot_out) {
+  const int slot = h->staging_next;
+  auto& st = h->staging[slot];
+  cudaError_t e;
+  if (st.pending) {
+    e = cudaEventSynchronize(st.done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    st.pending = false;
+  }
+  if (bytes > st.bytes) {
+    if (st.ptr) cudaFreeHost(st.ptr);
+    st.ptr = nullptr;
+    st.bytes = 0;
+    const size_t cap = std::max<size_t>(bytes * 2, 1 << 16);
+    e = cudaHostAlloc(&st.ptr, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    st.bytes = cap;
+  }
+  *out = static_cast<char*>(st.ptr);
+  *slot_out = slot;
+  return PKD_OK;
+}
+
+// Marks the slot's upload (already enqueued on `s`) and moves to the next slot.
+int staging_release(pkd_handle* h, int slot, cudaStream_t s) {
+  auto& st = h->staging[slot];
+  cudaError_t e = cudaEventRecord(st.done, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  st.pending = true;
+  h->staging_next = (slot + 1) % pkd_handle::kStagingSlots;
+  return PKD_OK;
+}
 
 // 4-D TMA view of one K or V pool: dims (d, head, slot, page) for NHD and (d, slot, head, page)
 // for HND, i.e. ordered by increasing stride; a box is 128 bytes of d by `box_rows` slots of
@@ -275,10 +316,14 @@ int pkd_create(pkd_handle** out, void* float_ws, size_t float_ws_bytes, void* in
   h->layout = kv_layout;
   h->device = dev;
   h->num_sms = sms;
-  e = cudaEventCreateWithFlags(&h->staging_done, cudaEventDisableTiming);
-  if (e != cudaSuccess) {
-    delete h;
-    return cuda_fail(e, "cudaEventCreate");
+  for (auto& st : h->staging) {
+    e = cudaEventCreateWithFlags(&st.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (auto& t : h->staging)
+        if (t.done) cudaEventDestroy(t.done);
+      delete h;
+      return cuda_fail(e, "cudaEventCreate");
+    }
   }
   *out = h;
   g_last_error.clear();
@@ -300,9 +345,11 @@ int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, vo
 
 int pkd_destroy(pkd_handle* h) {
   if (!h) return PKD_OK;
-  if (h->staging_pending) cudaEventSynchronize(h->staging_done);
-  if (h->staging) cudaFreeHost(h->staging);
-  if (h->staging_done) cudaEventDestroy(h->staging_done);
+  for (auto& st : h->staging) {
+    if (st.pending) cudaEventSynchronize(st.done);
+    if (st.ptr) cudaFreeHost(st.ptr);
+    if (st.done) cudaEventDestroy(st.done);
+  }
   delete h;
   return PKD_OK;
 }
@@ -451,21 +498,9 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
                                           : merges_off + merges_b;
   const size_t table_b = h->graph ? (size_t)(2 * batch + 1) * sizeof(int32_t) : 0;
   const size_t bytes = img_bytes + table_b;
-  if (h->staging_pending) {
-    e = cudaEventSynchronize(h->staging_done);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
-    h->staging_pending = false;
-  }
-  if (bytes > h->staging_bytes) {
-    if (h->staging) cudaFreeHost(h->staging);
-    h->staging = nullptr;
-    h->staging_bytes = 0;
-    const size_t cap = std::max<size_t>(bytes * 2, 1 << 16);
-    e = cudaHostAlloc(&h->staging, cap, cudaHostAllocDefault);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
-    h->staging_bytes = cap;
-  }
-  char* img = static_cast<char*>(h->staging);
+  char* img = nullptr;
+  int slot = 0;
+  if (int rc2 = staging_acquire(h, bytes, &img, &slot)) return rc2;
   std::memset(img, 0, merges_off);
   if (h->graph) {
     const int32_t count = (int32_t)plan.items.size();
@@ -511,9 +546,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
                           cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "copying the page table into the graph buffers");
   }
-  e = cudaEventRecord(h->staging_done, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  h->staging_pending = true;
+  if (int rc2 = staging_release(h, slot, s)) return rc2;
 
   h->plan = std::move(plan);
   h->batch = batch;
@@ -728,29 +761,15 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   const size_t items_b = plan.items.size() * sizeof(WorkItem);
   const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
   const size_t bytes = merges_off + merges_b;
-  if (h->staging_pending) {
-    e = cudaEventSynchronize(h->staging_done);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
-    h->staging_pending = false;
-  }
-  if (bytes > h->staging_bytes) {
-    if (h->staging) cudaFreeHost(h->staging);
-    h->staging = nullptr;
-    h->staging_bytes = 0;
-    const size_t cap = std::max<size_t>(bytes * 2, 1 << 16);
-    e = cudaHostAlloc(&h->staging, cap, cudaHostAllocDefault);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
-    h->staging_bytes = cap;
-  }
-  char* img = static_cast<char*>(h->staging);
+  char* img = nullptr;
+  int slot = 0;
+  if (int rc2 = staging_acquire(h, bytes, &img, &slot)) return rc2;
   std::memset(img, 0, merges_off);
   if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
   if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
   e = cudaMemcpyAsync(h->int_ws, img, bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
-  e = cudaEventRecord(h->staging_done, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  h->staging_pending = true;
+  if (int rc2 = staging_release(h, slot, s)) return rc2;
 
   h->plan = std::move(plan);
   h->batch = batch;
