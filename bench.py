@@ -520,7 +520,7 @@ def mla_reference_arm(args, w):
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
         "steps": steps, "warmup": warmup, "ms_per_step": t / steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": mla_describe(w), "batch": w.batch},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
