@@ -210,20 +210,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       : "memory");
 }
 
-// The same with the accumulate flag fixed at compile time (no predicate set-up per MMA).
-template <bool kAccumulate>
-__device__ __forceinline__ void tc_mma_const(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                             uint32_t idesc) {
-  if (kAccumulate)
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(a),
-                 "l"(b), "r"(idesc)
-                 : "memory");
-  else
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem), "l"(a),
-                 "l"(b), "r"(idesc)
-                 : "memory");
-}
-
 // The same with A (M=128 rows x 16 values, two 16-bit values per column) read from TMEM.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -487,21 +473,12 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
           tc_fence_after();
           const uint64_t kdesc0 = smem_desc(sb + OFF_STAGE + s * STAGE_BYTES, 16, 1024, 2);
           const uint32_t d = tmem + TM_S + 32 * (i % 3);
-          // fully unrolled (4 or 5 blocks x 4 steps): descriptors are constant offsets
-          tc_mma_const<false>(d, qdesc0, kdesc0, id_qk);
+          for (int b = 0; b < nblk; ++b)
 #pragma unroll
-          for (int st = 1; st < 16; ++st)
-            tc_mma_const<true>(d, qdesc0 + (uint64_t)(((st >> 2) * QBLK_BYTES + (st & 3) * 32) >> 4),
-                               kdesc0 + (uint64_t)(((st >> 2) * BLK_BYTES + (st & 3) * 32) >> 4),
-                               id_qk);
-          if (nblk == QBLK) {
-#pragma unroll
-            for (int st = 16; st < 20; ++st)
-              tc_mma_const<true>(d,
-                                 qdesc0 + (uint64_t)(((st >> 2) * QBLK_BYTES + (st & 3) * 32) >> 4),
-                                 kdesc0 + (uint64_t)(((st >> 2) * BLK_BYTES + (st & 3) * 32) >> 4),
-                                 id_qk);
-          }
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma(d, qdesc0 + (uint64_t)((b * QBLK_BYTES + kk * 32) >> 4),
+                     kdesc0 + (uint64_t)((b * BLK_BYTES + kk * 32) >> 4), id_qk,
+                     (b | kk) ? 1u : 0u);
           tc_commit(bar(B_SFULL + i % 3));
         };
         auto pv = [&](int i) {
