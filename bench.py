@@ -55,13 +55,32 @@ KERNEL_SOURCES = ("decode_kernels.cuh", "pkd_device.cuh", "pkd_internal.h", "dec
 
 
 def kernel_sources_digest() -> str:
+    return sources_digest(KERNEL_SOURCES)
+
+
+# The same for the tcgen05 MLA kernel on the `mla` workload (profiles/mla_tc_kernel_mla.md).
+MLA_KERNEL_SOURCES = ("mla_tc_kernels.cuh", "pkd_device.cuh", "pkd_internal.h", "mla_tc.cu",
+                      "planner.cpp")
+MLA_MEASURED_TRAFFIC = {
+    "sources_sha256": "ce9afa2dad7ab2ffc962a4d962e3f4276c5c9eaf14472f7a6e623212e55969c5",
+    "mla_tc_kernel": 172486400.0,
+}
+
+
+def sources_digest(names) -> str:
     csrc = os.path.join(ROOT, "paged_kv_decode_23_gb300", "csrc")
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         h.update(name.encode())
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def mla_measured_traffic(kernel: str):
+    if MLA_MEASURED_TRAFFIC.get("sources_sha256") != sources_digest(MLA_KERNEL_SOURCES):
+        return None
+    return MLA_MEASURED_TRAFFIC.get(kernel)
 
 
 def measured_traffic(name: str):
@@ -667,7 +686,10 @@ def mla_gpu_arm(args, w, rank, world):
         "pct_of_hbm_peak": 100.0 * (bytes_call / (ms_step * 1e-3) / 1e9) / hbm_peak,
         "peak_kind": peak_kind,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s",
-                     "frac": tflops / tf_peak, "traffic": None, "kernel": mla_kernel_name(args, w),
+                     "frac": tflops / tf_peak,
+                     "traffic": mla_measured_traffic(mla_kernel_name(args, w))
+                     if w.name == "mla" else None,
+                     "kernel": mla_kernel_name(args, w),
                      "kernel_us": kern_ms * 1e3, "algorithmic_flops_per_launch": flops_call,
                      "peak_kind": tf_kind,
                      "hbm": {"achieved": bytes_call / (kern_ms * 1e-3) / 1e9, "peak": hbm_peak,
