@@ -235,6 +235,23 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
 #define PKD_MLA_BACKEND_TCGEN05 2
 int pkd_mla_set_backend(pkd_handle* h, int backend);
 
+/*
+ * Host-only MLA planning (no GPU, no handle): the work list pkd_mla_plan would upload for this
+ * batch with this backend, for inspection and tests.  kv_indptr_host / kv_len_host as in
+ * pkd_mla_plan; dtype PKD_DTYPE_F16 or _BF16; num_sms <= 0 means 152.  items_out receives up
+ * to max_items work items of 8 int32 (output row, offset of the request's first page id,
+ * first token of the chunk's first tile, attended begin, attended end, partial slot or -1,
+ * merge entry or -1, query position) and merges_out up to max_merges entries of 4 int32
+ * (row, first slot, chunk count, 0); either may be NULL.  n_items / n_merges / n_slots receive
+ * the counts, ctas_per_item the CTAs each item launches, float_ws_bytes / int_ws_bytes the
+ * workspace sizes pkd_mla_plan needs (any of them may be NULL).
+ */
+int pkd_mla_plan_host(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int batch,
+                      int num_heads, int page_size, int dtype, int backend, int num_sms,
+                      int32_t* items_out, int max_items, int32_t* merges_out, int max_merges,
+                      int* n_items, int* n_merges, int* n_slots, int* ctas_per_item,
+                      size_t* float_ws_bytes, size_t* int_ws_bytes);
+
 /* Free the handle (host memory and pinned staging only; the workspaces are the caller's). */
 int pkd_destroy(pkd_handle* h);
 

@@ -54,6 +54,11 @@ SIGNATURES = {
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkd_set_pdl": (_c_int, [_vp, _c_int]),
     "pkd_mla_set_backend": (_c_int, [_vp, _c_int]),
+    "pkd_mla_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _i32p, _c_int, _i32p, _c_int, ctypes.POINTER(_c_int),
+                                   ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
+                                   ctypes.POINTER(_c_int), ctypes.POINTER(_c_size),
+                                   ctypes.POINTER(_c_size)]),
     "pkd_mla_plan": (_c_int, [_vp, _i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
                               _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _vp]),
     "pkd_mla_run": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _c_int, _vp,

@@ -683,6 +683,85 @@ int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base
                        lse, stream, nullptr, nullptr);
 }
 
+namespace {
+
+// The MLA work list and the kernel that runs it (shared by pkd_mla_plan and the host-only
+// pkd_mla_plan_host): auto takes the tcgen05 pair kernel when a 128-head tile is at least
+// half full.
+int build_mla_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int batch,
+                   int num_heads, int page_size, int dtype, int backend, int num_sms,
+                   const MlaKernel** kernel, Plan* plan) {
+  const int variant = backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
+                      : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
+                      : num_heads > 64                     ? kMlaTcgen05
+                                                           : kMlaMmaSync;
+  const MlaKernel* k = find_mla(dtype, variant);
+  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
+  PlanRequest r;
+  std::memset(&r, 0, sizeof r);
+  r.indptr = kv_indptr_host;
+  r.kv_len = kv_len_host;
+  r.batch = batch;
+  r.num_qo_heads = num_heads;
+  r.num_kv_heads = 1;
+  r.head_dim = 512;
+  r.page_size = page_size;
+  r.window_left = -1;
+  r.kv_dtype = dtype;
+  r.use_tensor_cores = 1;
+  r.num_sms = num_sms;
+  r.q_len = 1;
+  r.mla = 1;
+  r.mla_heads_per_cta = k->heads_per_cta;
+  r.mla_tile_tokens = k->tile_tokens;
+  r.mla_ctas_per_head_tile = k->ctas_per_head_tile;
+  r.ctas_per_sm = 1;  // both MLA kernels take most of an SM's shared memory
+  const char* err = "";
+  const int rc = build_plan(r, plan, &err);
+  if (rc) return fail(rc, err);
+  *kernel = k;
+  return PKD_OK;
+}
+
+}  // namespace
+
+int pkd_mla_plan_host(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int batch,
+                      int num_heads, int page_size, int dtype, int backend, int num_sms,
+                      int32_t* items_out, int max_items, int32_t* merges_out, int max_merges,
+                      int* n_items, int* n_merges, int* n_slots, int* ctas_per_item,
+                      size_t* float_ws_bytes, size_t* int_ws_bytes) {
+  if (batch < 0 || (batch > 0 && (!kv_indptr_host || !kv_len_host)))
+    return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0 and the tables non-null");
+  if (num_heads <= 0) return fail(PKD_ERR_INVALID_ARG, "num_heads must be positive");
+  if (dtype != PKD_DTYPE_F16 && dtype != PKD_DTYPE_BF16)
+    return fail(PKD_ERR_UNSUPPORTED, "MLA takes F16 or BF16");
+  if (backend != PKD_MLA_BACKEND_AUTO && backend != PKD_MLA_BACKEND_MMA_SYNC &&
+      backend != PKD_MLA_BACKEND_TCGEN05)
+    return fail(PKD_ERR_INVALID_ARG, "backend must be PKD_MLA_BACKEND_AUTO, _MMA_SYNC or _TCGEN05");
+  const MlaKernel* k = nullptr;
+  Plan plan;
+  const int rc = build_mla_plan(kv_indptr_host, kv_len_host, batch, num_heads, page_size, dtype,
+                                backend, num_sms > 0 ? num_sms : 152, &k, &plan);
+  if (rc) return rc;
+  const int cph = k->ctas_per_head_tile;
+  const WsLayout lay = layout_of(plan, 1);
+  if (n_items) *n_items = (int)plan.items.size();
+  if (n_merges) *n_merges = (int)plan.merges.size();
+  if (n_slots) *n_slots = plan.num_slots;
+  if (ctas_per_item) *ctas_per_item = plan.gslices;
+  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(lay, num_heads * cph, 512 / cph);
+  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(lay);
+  if (items_out)
+    std::memcpy(items_out, plan.items.data(),
+                sizeof(WorkItem) * std::min<size_t>(plan.items.size(), (size_t)std::max(0, max_items)));
+  if (merges_out)
+    std::memcpy(merges_out, plan.merges.data(),
+                sizeof(MergeEntry) *
+                    std::min<size_t>(plan.merges.size(), (size_t)std::max(0, max_merges)));
+  g_last_error.clear();
+  return PKD_OK;
+}
+
 int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv_len_host,
                  int batch, const int32_t* kv_indices_dev, int64_t num_indices, int num_heads,
                  int head_dim_ckv, int head_dim_kpe, int page_size, int causal, float sm_scale,
@@ -703,36 +782,11 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   if (batch > 0 && (!kv_indices_dev || num_indices < (int64_t)kv_indptr_host[batch]))
     return fail(PKD_ERR_INVALID_ARG, "kv_indices holds fewer than kv_indptr[batch] page ids");
 
-  // auto: the tcgen05 pair kernel when a head tile of 128 is at least half full
-  int variant = h->mla_backend == PKD_MLA_BACKEND_MMA_SYNC   ? kMlaMmaSync
-                : h->mla_backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
-                : num_heads > 64                            ? kMlaTcgen05
-                                                            : kMlaMmaSync;
-  const MlaKernel* k = find_mla(q_dtype, variant);
-  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
-  PlanRequest r;
-  std::memset(&r, 0, sizeof r);
-  r.indptr = kv_indptr_host;
-  r.kv_len = kv_len_host;
-  r.batch = batch;
-  r.num_qo_heads = num_heads;
-  r.num_kv_heads = 1;
-  r.head_dim = head_dim_ckv;
-  r.page_size = page_size;
-  r.window_left = -1;
-  r.kv_dtype = kv_dtype;
-  r.use_tensor_cores = 1;
-  r.num_sms = h->num_sms;
-  r.q_len = 1;
-  r.mla = 1;
-  r.mla_heads_per_cta = k->heads_per_cta;
-  r.mla_tile_tokens = k->tile_tokens;
-  r.mla_ctas_per_head_tile = k->ctas_per_head_tile;
-  r.ctas_per_sm = 1;  // both MLA kernels take most of an SM's shared memory
+  const MlaKernel* k = nullptr;
   Plan plan;
-  const char* err = "";
-  int rc = build_plan(r, &plan, &err);
-  if (rc) return fail(rc, err);
+  int rc = build_mla_plan(kv_indptr_host, kv_len_host, batch, num_heads, page_size, q_dtype,
+                          h->mla_backend, h->num_sms, &k, &plan);
+  if (rc) return rc;
 
   // partials: [slots, H * cph, 512 / cph] fp32 and [slots, H * cph] lse (cph CTAs per head tile
   // each keep their own lse copy)

@@ -293,6 +293,33 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
                 num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
 
 
+def mla_plan_host(kv_indptr, kv_len_arr, num_heads: int, page_size: int,
+                  dtype: int = L.DTYPE_BF16, backend: str = "auto", num_sms: int = 152):
+    """The MLA work list ``BatchMLAPagedAttention.plan`` would upload, built on the host alone
+    (no GPU): items ``[n, 8]`` (row, first page index, chunk start, begin, end, slot, merge
+    entry, query position), merge entries ``[m, 4]``, slot count, CTAs per item and the
+    float / int workspace bytes the plan needs."""
+    if backend not in _MLA_BACKEND:
+        raise ValueError(f"backend must be one of {sorted(_MLA_BACKEND)}")
+    ip = _host_i32(kv_indptr)
+    kl = _host_i32(kv_len_arr)
+    batch = len(kl)
+    n_items, n_merges, n_slots, cpi = (ctypes.c_int() for _ in range(4))
+    fb, ib = ctypes.c_size_t(), ctypes.c_size_t()
+    args = (_i32p(ip), _i32p(kl), batch, num_heads, page_size, dtype, _MLA_BACKEND[backend],
+            num_sms)
+    outs = (ctypes.byref(n_items), ctypes.byref(n_merges), ctypes.byref(n_slots),
+            ctypes.byref(cpi), ctypes.byref(fb), ctypes.byref(ib))
+    L.check(L.lib().pkd_mla_plan_host(*args, None, 0, None, 0, *outs))
+    items = np.zeros((max(1, n_items.value), 8), dtype=np.int32)
+    merges = np.zeros((max(1, n_merges.value), 4), dtype=np.int32)
+    L.check(L.lib().pkd_mla_plan_host(*args, _i32p(items), n_items.value, _i32p(merges),
+                                      n_merges.value, *outs))
+    return dict(items=items[:n_items.value], merges=merges[:n_merges.value],
+                num_slots=n_slots.value, ctas_per_item=cpi.value, float_ws_bytes=fb.value,
+                int_ws_bytes=ib.value)
+
+
 def workspace_bytes(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                     page_size: int, window_left: int = -1, fixed_split_size: int = 0,
                     disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,

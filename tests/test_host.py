@@ -233,3 +233,67 @@ def test_multi_token_rows_partition_their_causal_keys(pkd, q_len, mode):
             assert int(a[4]) == int(b[3])
         if len(its) > 1:
             assert plan["merges"][int(its[0][6])][0] == row
+
+
+def _mla_partition_ok(plan, kv_indptr, kv_lens):
+    """Every request's [0, kv_len) is covered exactly once by its items, in chunk order, and the
+    merge entries list exactly the split requests with their consecutive slots."""
+    items, merges = plan["items"], plan["merges"]
+    by_req = {}
+    for it in items:
+        by_req.setdefault(int(it[0]), []).append(it)
+    assert sorted(by_req) == list(range(len(kv_lens)))
+    split = {}
+    for r, its in by_req.items():
+        n = int(kv_lens[r])
+        assert all(int(it[1]) == int(kv_indptr[r]) for it in its)  # the request's first page id
+        if n == 0:
+            assert len(its) == 1 and its[0][3] == its[0][4] == 0 and its[0][5] == -1
+            continue
+        spans = sorted((int(it[3]), int(it[4])) for it in its)
+        assert spans[0][0] == 0 and spans[-1][1] == n
+        assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+        assert all(it[2] <= it[3] and it[3] < it[4] for it in its)
+        if len(its) > 1:
+            slots = sorted(int(it[5]) for it in its)
+            assert slots == list(range(slots[0], slots[0] + len(its)))
+            assert len({int(it[6]) for it in its}) == 1
+            split[r] = (slots[0], len(its))
+        else:
+            assert its[0][5] == -1 and its[0][6] == -1
+    assert {int(m[0]): (int(m[1]), int(m[2])) for m in merges} == split
+    return split
+
+
+@pytest.mark.parametrize("backend,heads,ctas", [("fa2", 40, 2), ("fa2", 128, 4),
+                                                ("tcgen05", 40, 2), ("tcgen05", 128, 2),
+                                                ("tcgen05", 192, 4), ("auto", 64, 2),
+                                                ("auto", 128, 2)])
+def test_mla_plan_partitions_requests(pkd, backend, heads, ctas):
+    """MLA work lists (host-only planner): a partition of every request for each kernel, with
+    the kernel's CTAs per item (32-head slices for fa2, 128-head CTA pairs for tcgen05)."""
+    w = W.mla_custom([1, 31, 32, 33, 0, 100, 777, 64, 5000, 12000], heads, 16, "bf16", seed=3)
+    plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, heads, 16, backend=backend)
+    assert plan["ctas_per_item"] == ctas
+    _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)
+    assert plan["float_ws_bytes"] > 0 and plan["int_ws_bytes"] > 0
+
+
+def test_mla_plan_splits_the_example_into_full_waves(pkd):
+    """The wrapper's example (114 x 999 tokens, 128 heads) on 152 SMs: 2 chunks per request,
+    456 CTAs = three full waves of one CTA per SM (unsplit it would be 228 CTAs, 1.5 waves)."""
+    w = W.mla_workload()
+    plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, 128, 1, backend="auto")
+    split = _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)
+    assert len(plan["items"]) == 228 and plan["ctas_per_item"] == 2
+    assert len(split) == 114 and all(n == 2 for _, n in split.values())
+    lens = plan["items"][:, 4] - plan["items"][:, 3]
+    assert lens.min() >= 499 and lens.max() <= 500
+
+
+def test_mla_plan_rejects_bad_input(pkd):
+    with pytest.raises(pkd.PkdError):  # kv_len beyond the pages
+        pkd.mla_plan_host(np.array([0, 1], np.int32), np.array([5], np.int32), 16, 4)
+    with pytest.raises(ValueError):
+        pkd.mla_plan_host(np.array([0, 1], np.int32), np.array([1], np.int32), 16, 4,
+                          backend="fa3")
