@@ -13,12 +13,6 @@
 //             apart (1152 + 16: eight consecutive rows fall in eight different 16-byte bank
 //             groups, so ldmatrix reads are conflict-free without a swizzle).  Completion is
 //             the stage's full mbarrier transaction count.
-//   cluster   the head-slice CTAs of one work item (up to 8) form a thread-block cluster and
-//             read every row once: CTA k copies rows r with r % size == k and multicasts
-//             them into every CTA of the cluster.  A stage is refilled only after the
-//             consumers of every CTA have released it (each consumer warp arrives on the
-//             stage's empty barrier in every CTA).  Cluster barriers after the barriers' init
-//             and before exit; no CTA returns early, so every CTA reaches both.
 //   consumers warp w owns latent dims [64w, 64w + 64): it forms the partial logits S_w^T
 //             (32 tokens x 32 heads) over those dims with mma.m16n8k16 (warps 0-3 also add
 //             one 16-dim k step of the kpe part each), the partials meet in shared memory,
@@ -76,36 +70,6 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// The same copy delivered to the same offsets (data and mbarrier) in every CTA of `mask`.
-__device__ __forceinline__ void bulk_copy_multicast(uint32_t dst, const void* src, uint32_t bytes,
-                                                    uint32_t bar, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1], %2, [%3], %4, %5;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "h"(mask), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-
-// Arrive on the mbarrier at local shared address `bar` of CTA `rank` of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
-               : "memory");
-}
-
 // Byte offset of 16-byte chunk c (0..63 ckv, 64..71 kpe) of tile row r inside a stage.
 __device__ __forceinline__ uint32_t row_chunk(int r, int c) {
   return (uint32_t)(r * mla::ROW_STRIDE + c * 16);
@@ -114,7 +78,7 @@ __device__ __forceinline__ uint32_t row_chunk(int r, int c) {
 template <typename T>
 __device__ __forceinline__ void produce(const MlaParams& p, const WorkItem& it, int j0, int ntiles,
                                         uint32_t smem, uint32_t full0, uint32_t empty0,
-                                        volatile int* abort_flag, int lane, int csize, int rank,
+                                        volatile int* abort_flag, int lane,
                                         volatile uint32_t* bad_rows) {
   const int ps = p.page_size;
   const char* ckv = static_cast<const char*>(p.ckv);
@@ -156,19 +120,11 @@ __device__ __forceinline__ void produce(const MlaParams& p, const WorkItem& it, 
       mbar_arrive_expect_tx(full0 + 8 * s, __popc(m) * (uint32_t)mla::ROW_BYTES);
     }
     __syncwarp();
-    // rows not copied keep stale data: their logits are masked, their V zeroed.  In a
-    // cluster this CTA copies rows lane % csize == rank into every CTA.
-    if (ok_row && lane % csize == rank) {
+    // rows not copied keep stale data: their logits are masked, their V zeroed
+    if (ok_row) {
       const uint32_t dst = stage + lane * mla::ROW_STRIDE;
-      if (csize == 1) {
-        bulk_copy(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, pol);
-        bulk_copy(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2, full0 + 8 * s, pol);
-      } else {
-        const uint16_t mask = (uint16_t)((1u << csize) - 1u);
-        bulk_copy_multicast(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, mask, pol);
-        bulk_copy_multicast(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2,
-                            full0 + 8 * s, mask, pol);
-      }
+      bulk_copy(dst, ckv + prow * (mla::DC * 2), mla::DC * 2, full0 + 8 * s, pol);
+      bulk_copy(dst + mla::DC * 2, kpe + prow * (mla::DP * 2), mla::DP * 2, full0 + 8 * s, pol);
     }
     issued = i + 1;
   }
@@ -217,7 +173,7 @@ template <typename T>
 __device__ __forceinline__ void consume(const MlaParams& p, const WorkItem& it, int j0, int ntiles,
                                         int gs, int g0, int gcnt, uint8_t* base, uint32_t smem,
                                         uint32_t full0, uint32_t empty0, volatile int* abort_flag,
-                                        int* merge_last_s, int csize,
+                                        int* merge_last_s,
                                         const volatile uint32_t* bad_rows) {
   using namespace dev;
   using namespace mla_detail;
@@ -427,11 +383,7 @@ __device__ __forceinline__ void consume(const MlaParams& p, const WorkItem& it, 
     }
     if (wrote) fence_proxy_async_smem();  // the zeroing stores before the next TMA copies
     __syncwarp();
-    if (csize == 1) {
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    } else if (lane < csize) {
-      mbar_arrive_cluster(empty0 + 8 * s, (uint32_t)lane);  // the stage in every CTA
-    }
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
   if (stg == 0) {
     m_s[sh] = m2;
@@ -563,8 +515,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
   const uint32_t empty0 = smem_u32(&bars[mla::NSTAGES]);
   volatile int* abort_flag = &abort_flag_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int csize = p.cluster_size;  // CTAs of the cluster: head slices of one work item
-  const int rank = csize > 1 ? (int)cluster_rank() : 0;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -582,28 +532,20 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
 #pragma unroll
     for (int s = 0; s < mla::NSTAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);         // the producer's expect_tx arrival
-      mbar_init(empty0 + 8 * s, mla::NW * csize);  // one per consumer warp of the cluster
+      mbar_init(empty0 + 8 * s, mla::NW);  // one per consumer warp
     }
     abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
     fence_mbar_init();
   }
   // peers' copies and arrivals reach this CTA's barriers only after their init
-  if (csize > 1)
-    cluster_sync();
-  else
-    __syncthreads();
-  // an earlier launch timed out: do nothing (a peer that read the status word before it was
-  // set finds its waits bounded); the output is left unwritten
-  if (abort_flag_s) ntiles = 0;
+  __syncthreads();
+  if (abort_flag_s) ntiles = 0;  // an earlier launch timed out: do nothing, write nothing
 
   if (warp == mla::NW)
-    produce<T>(p, it, j0, ntiles, smem, full0, empty0, abort_flag, lane, csize, rank, bad_rows_s);
+    produce<T>(p, it, j0, ntiles, smem, full0, empty0, abort_flag, lane, bad_rows_s);
   else
     consume<T>(p, it, j0, ntiles, gs, g0, gcnt, base, smem, full0, empty0, abort_flag,
-               &merge_last_s, csize, bad_rows_s);
-  __syncwarp();
-  // no CTA leaves while a peer may still copy into its shared memory or arrive on its barriers
-  if (csize > 1) cluster_sync();
+               &merge_last_s, bad_rows_s);
 }
 
 }  // namespace pkd

@@ -885,12 +885,8 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
   prm.num_pages = num_pages;
   prm.num_heads = h->num_qo_heads;
   prm.gslices = h->plan.gslices;
-  // mma.sync kernel: the head slices of one item share every K row and form a cluster of up
-  // to 8 CTAs (one copy of each row, multicast); tcgen05 kernel: the CTA pair of a head tile
-  int csize = 8;
-  while (prm.gslices % csize) csize >>= 1;
-  if (h->mla_kernel->variant == kMlaTcgen05) csize = 2;
-  prm.cluster_size = csize;
+  // the tcgen05 kernel runs as CTA pairs (one per head tile); the mma.sync kernel alone
+  const int csize = h->mla_kernel->variant == kMlaTcgen05 ? 2 : 1;
   prm.page_size = h->page_size;
   prm.lse_base_e = lse_base_e ? 1 : 0;
   prm.scale_log2 = (float)((double)h->sm_scale * 1.4426950408889634);

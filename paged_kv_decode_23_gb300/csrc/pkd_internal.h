@@ -132,7 +132,6 @@ struct MlaParams {
   int64_t num_pages;      // pages in the caches: ids outside [0, num_pages) read as zeros
   int num_heads;
   int gslices;            // CTAs per item: head tiles x CTAs per head tile
-  int cluster_size;       // CTAs per cluster: largest of 8, 4, 2, 1 dividing gslices
   int page_size;
   int lse_base_e;         // 1: lse as natural log, 0: base 2 (run()'s default)
   float scale_log2;       // sm_scale * log2(e)
