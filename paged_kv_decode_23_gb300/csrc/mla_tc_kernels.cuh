@@ -563,15 +563,25 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
           va[4 * q + 2] += __uint_as_float(w.z);
           va[4 * q + 3] += __uint_as_float(w.w);
         }
-        // ---- logits, lazy online softmax
+        // ---- logits, lazy online softmax.  The maximum is taken on the unscaled partial sums
+        // (sm_scale > 0 keeps their order, and rounding is monotone, so max(s)·c = max(s·c)), and
+        // the scale is folded into the exponent's FMA; only a tile cut by the item's bounds
+        // needs the per-token mask.
         const int t0 = it.chunk_tok0 + (j0 + j) * TS;
-        float mx = kNegInfF;
+        if (t0 < it.tok_begin || t0 + TS > it.tok_end) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = t0 + e;
-          va[e] = (t >= it.tok_begin && t < it.tok_end) ? va[e] * p.scale_log2 : kNegInfF;
-          mx = fmaxf(mx, va[e]);
+          for (int e = 0; e < 32; ++e) {
+            const int t = t0 + e;
+            if (t < it.tok_begin || t >= it.tok_end) va[e] = kNegInfF;
+          }
         }
+        float mq[4] = {va[0], va[1], va[2], va[3]};
+#pragma unroll
+        for (int e = 4; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], va[e]);
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+        // buffer b read (the values are consumed above): the peer may refill it
+        __syncwarp();
+        if (lane == 0) arrive_remote_relaxed(xempty_peer + 8 * b);
         float alpha = 1.f;
         bool resc = false;
         if (mx > m_ref + kLazyMax) {  // also the first tile (m_ref = -inf)
@@ -581,21 +591,19 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
           }
           m_ref = mx;
         }
-        const float ref = m_ref == kNegInfF ? 0.f : m_ref;
-        float ps = 0.f;
+        const float nref = m_ref == kNegInfF ? 0.f : -m_ref;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[16], pl[16];  // P rounded to 16 bits, and the rounding remainder
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float a = fast_exp2(va[e] - ref), c = fast_exp2(va[e + 1] - ref);
-          ps += a + c;
+          const float a = fast_exp2(fmaf(va[e], p.scale_log2, nref));
+          const float c = fast_exp2(fmaf(va[e + 1], p.scale_log2, nref));
+          ps[(e >> 1) & 3] += a + c;
           pk[e >> 1] = pack2<T>(a, c);
           const float2 r = unpack2<T>(pk[e >> 1]);
           pl[e >> 1] = pack2<T>(a - r.x, c - r.y);
         }
-        lsum = lsum * alpha + ps;
-        // buffer b read (the values are consumed above): the peer may refill it
-        __syncwarp();
-        if (lane == 0) arrive_remote_relaxed(xempty_peer + 8 * b);
+        lsum = lsum * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
         // ---- P V of the previous tile done: P columns free, O stable
         if (j > 0) ok &= mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), abort_flag);
         if (!ok) {
