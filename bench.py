@@ -83,6 +83,23 @@ def mla_measured_traffic(kernel: str):
     return MLA_MEASURED_TRAFFIC.get(kernel)
 
 
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise maximum of `values` over all ranks of the process group: the slowest
+    replica's times set the job's time (every rank gets the result)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def replica_value(bytes_per_rank_step: float, world: int, ms_step: float) -> float:
+    """Whole-job GB/s of `world` replicas, each moving `bytes_per_rank_step` per step, timed by
+    the slowest rank's ms per step."""
+    return world * bytes_per_rank_step / (ms_step * 1e-3) / 1e9
+
+
 def measured_traffic(name: str):
     if MEASURED_TRAFFIC.get("sources_sha256") != kernel_sources_digest():
         return None
@@ -433,15 +450,12 @@ def gpu_arm(args, w, rank, world):
     h2d = q_all_host.numel() * q_all_host.element_size() + idx_host.numel() * 4
     d2h = o_all_host.numel() * o_all_host.element_size() + l_all_host.numel() * 4
 
-    if world > 1:
-        t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total, e2e_s = float(t[0]), float(t[1])
+    ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, device=dev)
 
     bytes_call = algorithmic_bytes(w)
     bytes_step = bytes_call * layers
     ms_step = ms_total / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    value = replica_value(bytes_step, world, ms_step)
     peak, peak_kind = load_peaks()
     kern_avg_ms = statistics.mean(kern_ms)
     achieved = bytes_call / (kern_avg_ms * 1e-3) / 1e9
@@ -461,7 +475,7 @@ def gpu_arm(args, w, rank, world):
                      else None,
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": bytes_call},
-        "e2e": {"value": world * bytes_step / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
+        "e2e": {"value": replica_value(bytes_step, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s / args.steps * 1e3},
         "gpu_launches": args.steps * layers,
@@ -656,10 +670,7 @@ def mla_gpu_arm(args, w, rank, world):
     for _ in range(args.steps):
         e2e_step()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([ms_total, e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total, e2e_s = float(t[0]), float(t[1])
+    ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, device=dev)
     bytes_call, flops_call = mla_bytes_flops(w)
     ms_step = ms_total / args.steps
     hbm_peak, peak_kind = load_peaks()
@@ -672,7 +683,7 @@ def mla_gpu_arm(args, w, rank, world):
     h2d = (qn_h.numel() + qp_h.numel()) * qn_h.element_size() + idx_h.numel() * 4
     d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
     return {
-        "metric": METRIC, "value": world * bytes_call / (ms_step * 1e-3) / 1e9, "unit": "GB/s",
+        "metric": METRIC, "value": replica_value(bytes_call, world, ms_step), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
@@ -695,7 +706,7 @@ def mla_gpu_arm(args, w, rank, world):
                      "hbm": {"achieved": bytes_call / (kern_ms * 1e-3) / 1e9, "peak": hbm_peak,
                              "unit": "GB/s", "frac": bytes_call / (kern_ms * 1e-3) / 1e9 / hbm_peak,
                              "algorithmic_bytes_per_launch": bytes_call}},
-        "e2e": {"value": world * bytes_call / (e2e_s / args.steps) / 1e9, "unit": "GB/s",
+        "e2e": {"value": replica_value(bytes_call, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s / args.steps * 1e3},
         "gpu_launches": args.steps,
