@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstring>
 #include <limits>
+#include <utility>
 
 #include "pkd_internal.h"
 
@@ -150,8 +151,10 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     longest = std::max(longest, n[row] - w[row]);
   }
 
-  // chunk size in tokens (a multiple of the page size); 0 = one chunk per request
+  // chunk size in tokens (a multiple of the page size); 0 = one chunk per request.  An MLA
+  // plan may instead give every row its own chunk count in kc.
   int64_t C = 0;
+  std::vector<int32_t> kc;
   const int64_t ctas_per_item = (int64_t)r.num_kv_heads * plan->gslices;
   // work items with heuristic (equal) chunks of c tokens; an empty request is one item
   auto items_with = [&](int64_t c) {
@@ -187,22 +190,89 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       }
       C = longest > lo ? lo : 0;
     } else if (r.mla) {
-      // MLA kernels hold one CTA (pair) per SM and whole waves of them: split the requests
-      // into k equal chunks for the k that minimises waves x (chunk + per-item overhead)
-      // tokens (batch 114 x 999 tokens: two chunks, three full waves instead of 1.5).
-      constexpr int64_t kItemOverhead = 64;
-      double best_cost = 0.0;
+      // MLA kernels hold one CTA (pair) per SM, so the grid runs in waves of whole items, and
+      // every item pays a fixed cost on top of its tokens (Q load, pipeline fill and drain,
+      // epilogue: about 11 tiles of 32 tokens measured on GB300).  Candidates: for k = 1..16,
+      // chunks of at most C = longest / k tokens (a row cut into ceil(a / C) equal chunks),
+      // and the same with the rows of the longest chunks cut once more, as many as fill the
+      // last wave.  Each is scored by a wave model -- items launch longest first, and a wave
+      // costs its longest item plus the overhead -- and the cheapest kept.  Batch 114 x 999
+      // tokens: 76 whole requests, then 38 requests in halves, two full waves (one chunk size
+      // for all would take 1.5 waves unsplit or three waves of halves).
+      constexpr int64_t kItemOverhead = 352;
+      const int64_t item_slots = std::max<int64_t>(1, slots / ctas_per_item);
+      // rows by chunk length, longest first, as one integer key each: length << 32 | ~row
+      std::vector<uint64_t> by_len(rows);
+      std::vector<int32_t> cand(rows);
+      std::vector<uint32_t> att(rows);  // attended tokens per row (< 2^31)
+      for (int i = 0; i < rows; ++i) att[i] = (uint32_t)(n[i] - w[i]);
+      auto chunk_len = [&](int i, int32_t k) -> uint32_t {
+        return att[i] > 0 ? (att[i] - 1) / (uint32_t)k + 1 : 0u;
+      };
+      auto row_of = [](uint64_t key) { return (int)(~(uint32_t)key); };
+      auto desc = [](uint64_t x, uint64_t y) { return x > y; };
+      // rekey in the previous order (chunk lengths mostly keep it), re-sort only if needed
+      auto sort_rows = [&](const std::vector<int32_t>& kk) {
+        for (uint64_t& key : by_len) {
+          const int i = row_of(key);
+          key = ((uint64_t)chunk_len(i, kk[i]) << 32) | (uint64_t)(~(uint32_t)i);
+        }
+        if (!std::is_sorted(by_len.begin(), by_len.end(), desc))
+          std::sort(by_len.begin(), by_len.end(), desc);
+      };
+      for (int i = 0; i < rows; ++i) by_len[i] = (uint64_t)(~(uint32_t)i);
+      // by_len sorted for kk: sum over waves of (first item's length + overhead)
+      auto wave_cost = [&](const std::vector<int32_t>& kk) -> int64_t {
+        int64_t cost = 0, pos = 0, next_wave = 0;
+        for (const uint64_t key : by_len) {
+          const int i = row_of(key);
+          pos += att[i] > 0 ? kk[i] : 1;
+          for (; next_wave < pos; next_wave += item_slots)
+            cost += (int64_t)(key >> 32) + kItemOverhead;
+        }
+        return cost;
+      };
+      int64_t best_cost = -1;
       for (int64_t k = 1; k <= 16; ++k) {
         const int64_t c = ((longest + k - 1) / k + ps - 1) / ps * ps;
         if (k > 1 && c < c_min) break;
-        const int64_t ctas = k == 1 ? (int64_t)rows * ctas_per_item : ctas_with(c);
-        const double cost =
-            (double)((ctas + slots - 1) / slots) * (double)(std::min(c, longest) + kItemOverhead);
-        if (k == 1 || cost < best_cost) {
-          best_cost = cost;
-          C = (k == 1 || c >= longest) ? 0 : c;
+        int64_t items_k = 0;
+        const uint32_t c32 = (uint32_t)std::min<int64_t>(c, std::numeric_limits<int32_t>::max());
+        for (int i = 0; i < rows; ++i) {
+          cand[i] = att[i] > c32 ? (int32_t)((att[i] - 1) / c32 + 1) : 1;
+          items_k += cand[i];
+        }
+        if (r.max_items > 0 && items_k > r.max_items) break;
+        sort_rows(cand);
+        const int64_t cost0 = wave_cost(cand);
+        if (best_cost < 0 || cost0 < best_cost) {
+          best_cost = cost0;
+          kc = cand;
+        }
+        // the same with the longest chunks cut once more, to fill the last wave
+        int64_t fill = (item_slots - items_k % item_slots) % item_slots;
+        if (fill == 0 || (r.max_items > 0 && items_k + fill > r.max_items)) continue;
+        for (const uint64_t key : by_len) {
+          if (fill == 0) break;
+          const int i = row_of(key);
+          if ((int64_t)chunk_len(i, cand[i] + 1) < c_min) continue;
+          ++cand[i];
+          --fill;
+        }
+        sort_rows(cand);
+        const int64_t cost1 = wave_cost(cand);
+        if (cost1 < best_cost) {
+          best_cost = cost1;
+          kc = cand;
         }
       }
+      bool any_split = false;
+      for (int i = 0; i < rows && !any_split; ++i) any_split = kc[i] > 1;
+      if (!any_split) kc.clear();
+      int64_t c_big = 0;
+      for (int i = 0; i < (int)kc.size(); ++i)
+        c_big = std::max<int64_t>(c_big, chunk_len(i, kc[i]));
+      C = c_big;
     } else {
       // More requests than one wave: chunks of about the average load of a CTA slot over
       // kWavesTarget waves, so the longest requests stop bounding the tail.
@@ -212,7 +282,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       c = (c + ps - 1) / ps * ps;
       C = longest > c ? c : 0;
     }
-    if (C > 0 && r.max_items > 0 && items_with(C) > r.max_items) {
+    if (C > 0 && kc.empty() && r.max_items > 0 && items_with(C) > r.max_items) {
       // a bounded work list (CUDA-graph mode): the smallest larger chunk that fits
       int64_t lo = C, hi = std::max(C, c_max);
       while (lo < hi) {
@@ -246,7 +316,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     // chunk boundaries: [bounds[j], bounds[j+1]); chunk j's tiles start at tile0[j]
     bounds.clear();
     tile0.clear();
-    if (C == 0) {
+    if (C == 0 && kc.empty()) {
       bounds = {w[i], n[i]};
       tile0 = {0};
     } else if (fixed) {
@@ -260,7 +330,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       // heuristic: k equal page-aligned chunks, so no short remainder chunk (which would
       // launch last and do the request's merge at the very end of the grid)
       const int64_t a = n[i] - w[i];
-      const int64_t k = (a + C - 1) / C;
+      const int64_t k = kc.empty() ? (a + C - 1) / C : kc[i];
       bounds.push_back(w[i]);
       tile0.push_back(w[i] / ps * ps);
       for (int64_t j = 1; j < k; ++j) {

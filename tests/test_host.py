@@ -280,15 +280,35 @@ def test_mla_plan_partitions_requests(pkd, backend, heads, ctas):
 
 
 def test_mla_plan_splits_the_example_into_full_waves(pkd):
-    """The wrapper's example (114 x 999 tokens, 128 heads) on 152 SMs: 2 chunks per request,
-    456 CTAs = three full waves of one CTA per SM (unsplit it would be 228 CTAs, 1.5 waves)."""
+    """The wrapper's example (114 x 999 tokens, 128 heads) on 152 SMs (76 CTA pairs): 76 whole
+    requests, then 38 requests in two halves -- two full waves of one CTA per SM.  One chunk size
+    for every request would give 1.5 waves unsplit or three waves of halves, each wave paying
+    the per-item overhead once more."""
     w = W.mla_workload()
     plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, 128, 1, backend="auto")
     split = _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)
-    assert len(plan["items"]) == 228 and plan["ctas_per_item"] == 2
-    assert len(split) == 114 and all(n == 2 for _, n in split.values())
+    assert plan["ctas_per_item"] == 2
+    assert len(plan["items"]) == 152 and len(plan["merges"]) == 38
+    assert len(split) == 38 and all(n == 2 for _, n in split.values())
     lens = plan["items"][:, 4] - plan["items"][:, 3]
-    assert lens.min() >= 499 and lens.max() <= 500
+    # longest first: the whole requests fill the first wave, the halves the second
+    assert (lens[:76] == 999).all()
+    assert lens[76:].min() >= 499 and lens[76:].max() <= 500
+
+
+def test_mla_plan_fills_whole_waves_on_mixed_lengths(pkd):
+    """A batch more than one wave deep: whatever the split, the work items cover every request
+    exactly once, and no item is shorter than the minimum chunk unless its request is."""
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 6000, size=300).astype(np.int32)
+    w = W.mla_custom(lens.tolist(), 128, 1, "bf16", seed=11)
+    plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, 128, 1, backend="tcgen05")
+    split = _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)
+    items = plan["items"]
+    ilen = items[:, 4] - items[:, 3]
+    assert (np.diff(ilen) <= 0).all()  # longest first
+    for r, (_, k) in split.items():
+        assert k * 128 <= int(lens[r])  # halves of at least 128 tokens
 
 
 def test_mla_plan_rejects_bad_input(pkd):
