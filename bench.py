@@ -62,8 +62,8 @@ def kernel_sources_digest() -> str:
 MLA_KERNEL_SOURCES = ("mla_tc_kernels.cuh", "pkd_device.cuh", "pkd_internal.h", "mla_tc.cu",
                       "planner.cpp")
 MLA_MEASURED_TRAFFIC = {
-    "sources_sha256": "3b62ea12e53745d0a80fdff933e4b55c8811546b361444b9ab001a3b052978e8",
-    "mla_tc_kernel": 151428096.0,
+    "sources_sha256": "507dc4f7a1baf2c4026ec1ef11d2e4dccf68d154681d41907cad158f02cff380",
+    "mla_tc_kernel": 151686656.0,
 }
 
 

@@ -713,6 +713,10 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
           // other chunks' partials of this (head tile, half) are contiguous rows in global
           // memory: each is brought in 64 heads at a time by one bulk copy into the (now idle)
           // Q area and folded into the staging rows with coalesced shared-memory passes.
+          // Every element is summed in slot order, whichever chunk finished last, so repeated
+          // launches agree bit for bit: with two chunks, w0 x0 is rounded first and w1 x1
+          // added by one fma (the own partial taken from the staging rows); with more, every
+          // chunk, the own one included, comes from global memory in slot order.
           __threadfence();
           const MergeEntry me = p.merges[it.merge_idx];
           float M = lse2;
@@ -731,14 +735,21 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
           wself_s[h] = (M != kNegInfF) ? fast_exp2(lse2 - M) * iw : 0.f;
           asm volatile("fence.proxy.async.global;" ::: "memory");  // partials: generic -> TMA
           uint32_t mphase = 0;
-          bool first = true;
+          const bool two = me.n_chunks == 2;
+          const bool own_first = it.out_slot == me.first_slot;
           for (int c = 0; c < me.n_chunks; ++c) {
             const int slot = me.first_slot + c;
-            if (slot == it.out_slot) continue;
+            if (two && slot == it.out_slot) continue;
             named_bar_sync(1, NSOFT);  // the previous chunk's passes are done with wchunk_s
             wchunk_s[h] = (h < gcnt && M != kNegInfF)
-                              ? fast_exp2(__ldcg(p.part_lse + prow_of(slot, h)) - M) * iw
+                              ? fast_exp2((slot == it.out_slot
+                                               ? lse2
+                                               : __ldcg(p.part_lse + prow_of(slot, h))) -
+                                          M) *
+                                    iw
                               : 0.f;
+            const bool swap = two && !own_first;  // two chunks, the own one second
+            const bool zero_b = !two && c == 0;
             for (int r0 = 0; r0 < gcnt; r0 += 64) {
               const int rows = min(64, gcnt - r0);
               named_bar_sync(1, NSOFT);  // the buffer and the weights are ready for reuse
@@ -760,15 +771,19 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
                 float4 o = *reinterpret_cast<const float4*>(base + (oa - sb));
                 const float4 x =
                     *reinterpret_cast<const float4*>(base + OFF_Q + r * 1024 + q * 16);
-                const float ws = first ? wself_s[row] : 1.f, wc = wchunk_s[row];
-                o.x = o.x * ws + x.x * wc;
-                o.y = o.y * ws + x.y * wc;
-                o.z = o.z * ws + x.z * wc;
-                o.w = o.w * ws + x.w * wc;
+                // o = fma(a, wa, b * wb): with two chunks, (a, b) = (chunk 1, chunk 0); with
+                // more, a = this chunk and b the running sum (zero for chunk 0)
+                const float wc = wchunk_s[row], ws = wself_s[row];
+                const float wa = swap ? ws : wc, wb = swap ? wc : (two ? ws : 1.f);
+                const float4 a = swap ? o : x;
+                const float4 b = swap ? x : (zero_b ? make_float4(0.f, 0.f, 0.f, 0.f) : o);
+                o.x = fmaf(a.x, wa, __fmul_rn(b.x, wb));
+                o.y = fmaf(a.y, wa, __fmul_rn(b.y, wb));
+                o.z = fmaf(a.z, wa, __fmul_rn(b.z, wb));
+                o.w = fmaf(a.w, wa, __fmul_rn(b.w, wb));
                 *reinterpret_cast<float4*>(base + (oa - sb)) = o;
               }
             }
-            first = false;
           }
           named_bar_sync(1, NSOFT);
 #pragma unroll 4

@@ -79,6 +79,38 @@ def test_mla_split_requests(heads, backend):
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
+def test_mla_many_chunks_one_request(backend):
+    """One request long enough that the one-wave plan cuts it into one chunk per CTA slot
+    (76 chunks on the tcgen05 kernel's CTA pairs): the fused merge folds them all."""
+    w = W.mla_custom([40000, 300], 16, 1, "bf16", seed=21)
+    qn, qp = W.make_mla_q(w)
+    ckv, kpe = W.make_mla_cache(w)
+    _close(_run(w, qn, qp, ckv, kpe, backend=backend), _oracle(w, qn, qp, ckv, kpe),
+           f"mla many chunks {backend}")
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_mla_split_run_to_run_determinism(backend):
+    """Split requests: the merge folds the chunks in slot order whichever CTA finishes last,
+    so repeated launches agree bit for bit."""
+    from paged_kv_decode_23_gb300 import BatchMLAPagedAttention
+    w = W.mla_custom([3000, 4500, 20, 999], 128, 1, "bf16", seed=22)
+    dev = torch.device("cuda")
+    qn, qp = W.make_mla_q(w, device=dev)
+    ckv, kpe = W.make_mla_cache(w, device=dev)
+    mla = BatchMLAPagedAttention(torch.zeros(256 << 20, dtype=torch.uint8, device=dev),
+                                 backend=backend)
+    mla.plan(torch.arange(w.batch + 1, dtype=torch.int32), torch.from_numpy(w.kv_indptr),
+             torch.from_numpy(w.kv_indices).to(dev), torch.from_numpy(w.kv_lens), w.num_heads,
+             512, 64, w.page_size, False, w.sm_scale, torch.bfloat16, torch.bfloat16)
+    outs = [mla.run(qn, qp, ckv, kpe, return_lse=True) for _ in range(6)]
+    torch.cuda.synchronize()
+    assert mla.check_status() == 0
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
 def test_mla_logits_far_apart(backend):
     """Latent rows shifted by a ramp over the page pool spread the logits over tens of units,
     so the running maximum of a head jumps by more than 8 (log2) several times along a

@@ -311,6 +311,16 @@ def test_mla_plan_fills_whole_waves_on_mixed_lengths(pkd):
         assert k * 128 <= int(lens[r])  # halves of at least 128 tokens
 
 
+def test_mla_plan_one_long_request_fills_the_gpu(pkd):
+    """One long request alone: the one-wave rule cuts it into one chunk per CTA slot (76 CTA
+    pairs of the tcgen05 kernel on 152 SMs), and on a larger GPU into more."""
+    w = W.mla_custom([300000], 16, 1, "bf16", seed=2)
+    plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, 16, 1, backend="tcgen05")
+    assert _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)[0][1] == 76
+    plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, 16, 1, backend="tcgen05", num_sms=400)
+    assert _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)[0][1] == 200
+
+
 def test_mla_plan_rejects_bad_input(pkd):
     with pytest.raises(pkd.PkdError):  # kv_len beyond the pages
         pkd.mla_plan_host(np.array([0, 1], np.int32), np.array([5], np.int32), 16, 4)
