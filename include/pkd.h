@@ -166,9 +166,10 @@ int pkd_set_pdl(pkd_handle* h, int enable);
 
 /*
  * CUDA-graph mode: the page's BatchDecodeWithPagedKVCacheWrapper(use_cuda_graph=True,
- * paged_kv_indptr_buffer, paged_kv_indices_buffer, paged_kv_last_page_len_buffer) and
+ * paged_kv_indptr_buffer, paged_kv_indices_buffer, paged_kv_last_page_len_buffer),
  * CUDAGraphBatchDecodeWithPagedKVCacheWrapper(workspace, indptr_buffer, indices_buffer,
- * last_page_len_buffer).  After this call (it cannot be undone on the handle):
+ * last_page_len_buffer) and BatchMLAPagedAttentionWrapper(use_cuda_graph=True, ...,
+ * kv_indptr, kv_indices, kv_len_arr).  After this call (it cannot be undone on the handle):
  *   - pkd_plan copies the page table into the caller's device buffers (indptr_buf: >=
  *     max_batch + 1 int32, indices_buf: >= max_pages int32, last_page_len_buf: >= max_batch
  *     int32) and the kernel reads page ids from indices_buf;
@@ -181,6 +182,10 @@ int pkd_set_pdl(pkd_handle* h, int enable);
  *     the plan's chunk count exit at once), so a run captured in a CUDA graph replays
  *     correctly after later plans.  pkd_plan itself is not capturable, as the page notes for
  *     plan().
+ *   - MLA (pkd_mla_plan / pkd_mla_run) works the same way: last_page_len_buf receives
+ *     kv_len; the first plan also fixes num_heads, page_size, sm_scale, the dtype and the
+ *     kernel; the workspaces must hold pkd_mla_graph_workspace_bytes.  A handle holds decode
+ *     plans or MLA plans in this mode, not both.
  * The buffers are the caller's and must outlive every run.
  */
 int pkd_enable_cuda_graph(pkd_handle* h, int32_t* indptr_buf, int32_t* indices_buf,
@@ -191,6 +196,9 @@ int pkd_enable_cuda_graph(pkd_handle* h, int32_t* indptr_buf, int32_t* indices_b
 int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads, int head_dim,
                               int use_tensor_cores, size_t* float_ws_bytes,
                               size_t* int_ws_bytes);
+/* The same for MLA plans of num_heads heads on the kernel `backend` (PKD_MLA_BACKEND_*) picks. */
+int pkd_mla_graph_workspace_bytes(int max_items, int num_heads, int backend,
+                                  size_t* float_ws_bytes, size_t* int_ws_bytes);
 
 /*
  * MLA paged decode: the page's flashinfer.mla.BatchMLAPagedAttentionWrapper plan() / run()
@@ -205,7 +213,8 @@ int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads,
  *   page_size >= 1 (any integer, 1 included); sm_scale > 0 (the page's example uses
  *   1 / sqrt(128 + 64)); q_dtype == kv_dtype in {F16, BF16}; causal is accepted and has no
  *   effect with one query per request.  The handle then holds an MLA plan: pkd_run refuses
- *   it, pkd_mla_run refuses a pkd_plan plan.  Not capturable; CUDA-graph mode is refused.
+ *   it, pkd_mla_run refuses a pkd_plan plan.  pkd_mla_plan is not capturable; in CUDA-graph
+ *   mode (pkd_enable_cuda_graph) pkd_mla_run is.
  * pkd_mla_run:
  *   q_nope [batch, num_heads, 512], q_pe [batch, num_heads, 64]; ckv_cache [num_pages,
  *   page_size, 512], kpe_cache [num_pages, page_size, 64] (all device, contiguous, 16-byte

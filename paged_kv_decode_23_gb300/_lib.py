@@ -64,6 +64,8 @@ SIGNATURES = {
     "pkd_mla_run": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _c_int, _vp,
                              _vp, _vp]),
     "pkd_enable_cuda_graph": (_c_int, [_vp, _vp, _vp, _vp, _c_int, ctypes.c_int64, _c_int]),
+    "pkd_mla_graph_workspace_bytes": (_c_int, [_c_int, _c_int, _c_int, ctypes.POINTER(_c_size),
+                                               ctypes.POINTER(_c_size)]),
     "pkd_graph_workspace_bytes": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
                                            ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
     "pkd_decode_noalloc": (_c_int, [_i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,

@@ -520,7 +520,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int item = blockIdx.x / p.gslices;
   const int gs = blockIdx.x - item * p.gslices;
-  const WorkItem it = p.items[item];
+  const WorkItem it = p.items[item];  // within the capacity in CUDA-graph mode
+  if (p.item_count && item >= *p.item_count) return;  // CUDA-graph mode: past the work list
   const int g0 = gs * mla::HT;
   const int gcnt = min(mla::HT, p.num_heads - g0);
   int j0 = 0, ntiles = 0;

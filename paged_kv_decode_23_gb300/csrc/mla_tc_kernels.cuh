@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int item = blockIdx.x / p.gslices;
   const int gs = blockIdx.x - item * p.gslices;  // head tile * 2 + rank
-  const WorkItem it = p.items[item];
+  const WorkItem it = p.items[item];  // within the capacity in CUDA-graph mode
+  // CUDA-graph mode: the grid covers the work list's capacity; both CTAs of a pair hold the
+  // same item, so both leave here, before any barrier or tensor-memory use
+  if (p.item_count && item >= *p.item_count) return;
   const int H = p.num_heads;
   const int g0 = (gs >> 1) * HT;
   const int gcnt = min(HT, H - g0);

@@ -159,6 +159,7 @@ struct pkd_handle {
   int64_t g_max_pages = 0;
   int g_max_items = 0;
   int g_batch = -1;  // fixed by the first plan in graph mode
+  int planned_heads = 0;  // MLA: num_heads of the last plan (fixed in graph mode)
 };
 
 namespace {
@@ -447,6 +448,8 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     if (h->g_batch >= 0 && q_len_per_req != h->q_len)
       return fail(PKD_ERR_INVALID_ARG,
                   "CUDA-graph mode: q_len_per_req is fixed by the first plan");
+    if (h->g_batch >= 0 && h->mla)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: the handle holds MLA plans");
   }
 
   PlanRequest r;
@@ -690,7 +693,7 @@ namespace {
 // half full.
 int build_mla_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int batch,
                    int num_heads, int page_size, int dtype, int backend, int num_sms,
-                   const MlaKernel** kernel, Plan* plan) {
+                   const MlaKernel** kernel, Plan* plan, int max_items = 0) {
   const int variant = backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
                       : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
                       : num_heads > 64                     ? kMlaTcgen05
@@ -716,6 +719,7 @@ int build_mla_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, in
   r.mla_tile_tokens = k->tile_tokens;
   r.mla_ctas_per_head_tile = k->ctas_per_head_tile;
   r.ctas_per_sm = 1;  // both MLA kernels take most of an SM's shared memory
+  r.max_items = max_items;
   const char* err = "";
   const int rc = build_plan(r, plan, &err);
   if (rc) return fail(rc, err);
@@ -769,7 +773,6 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   (void)causal;  // one query per request: nothing is masked
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
   h->planned = false;
-  if (h->graph) return fail(PKD_ERR_UNSUPPORTED, "CUDA-graph mode is built for pkd_plan only");
   if (head_dim_ckv != 512 || head_dim_kpe != 64)
     return fail(PKD_ERR_UNSUPPORTED, "MLA is built for head_dim_ckv 512 and head_dim_kpe 64");
   if (q_dtype != kv_dtype || (q_dtype != PKD_DTYPE_F16 && q_dtype != PKD_DTYPE_BF16))
@@ -781,17 +784,37 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
     return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0 and the tables non-null");
   if (batch > 0 && (!kv_indices_dev || num_indices < (int64_t)kv_indptr_host[batch]))
     return fail(PKD_ERR_INVALID_ARG, "kv_indices holds fewer than kv_indptr[batch] page ids");
+  if (h->graph) {
+    if (batch < 1 || batch > h->g_max_batch)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: batch must lie in [1, max_batch]");
+    if (h->g_batch >= 0 && batch != h->g_batch)
+      return fail(PKD_ERR_INVALID_ARG,
+                  "CUDA-graph mode: the batch size is fixed by the first plan (pad the batch "
+                  "with zero-length requests instead)");
+    if ((int64_t)kv_indptr_host[batch] > h->g_max_pages)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: kv_indptr[batch] exceeds max_pages");
+    if (h->g_batch >= 0 && !h->mla)
+      return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: the handle holds decode plans");
+    if (h->g_batch >= 0 &&
+        (h->planned_heads != num_heads || h->page_size != page_size || h->sm_scale != sm_scale))
+      return fail(PKD_ERR_INVALID_ARG,
+                  "CUDA-graph mode: num_heads, page_size and sm_scale are fixed by the first "
+                  "plan (a captured run holds them)");
+  }
 
   const MlaKernel* k = nullptr;
   Plan plan;
   int rc = build_mla_plan(kv_indptr_host, kv_len_host, batch, num_heads, page_size, q_dtype,
-                          h->mla_backend, h->num_sms, &k, &plan);
+                          h->mla_backend, h->num_sms, &k, &plan, h->graph ? h->g_max_items : 0);
   if (rc) return rc;
+  if (h->graph && h->g_batch >= 0 && h->mla && k != h->mla_kernel)
+    return fail(PKD_ERR_INVALID_ARG, "CUDA-graph mode: the kernel is fixed by the first plan");
 
   // partials: [slots, H * cph, 512 / cph] fp32 and [slots, H * cph] lse (cph CTAs per head tile
-  // each keep their own lse copy)
+  // each keep their own lse copy); CUDA-graph mode cuts the workspaces for the capacities
   const int cph = k->ctas_per_head_tile;
-  const WsLayout lay = layout_of(plan, 1);
+  const WsLayout lay =
+      h->graph ? capacity_layout(h->g_max_items, 1, plan.gslices) : layout_of(plan, 1);
   const size_t need_f = float_ws_bytes_of(lay, num_heads * cph, head_dim_ckv / cph);
   const size_t need_i = int_ws_bytes_of(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
@@ -810,19 +833,40 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
   // one upload of the int workspace image: zeroed status block and counters, items, merges
+  // (CUDA-graph mode: also the item count, and the page table into the caller's buffers)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t items_off = items_offset(lay), merges_off = merges_offset(lay);
   const size_t items_b = plan.items.size() * sizeof(WorkItem);
   const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
-  const size_t bytes = merges_off + merges_b;
+  const size_t img_bytes = merges_off + merges_b;
+  const size_t table_b = h->graph ? (size_t)(2 * batch + 1) * sizeof(int32_t) : 0;
   char* img = nullptr;
   int slot = 0;
-  if (int rc2 = staging_acquire(h, bytes, &img, &slot)) return rc2;
+  if (int rc2 = staging_acquire(h, img_bytes + table_b, &img, &slot)) return rc2;
   std::memset(img, 0, merges_off);
+  if (h->graph) {
+    const int32_t count = (int32_t)plan.items.size();
+    std::memcpy(img + kItemCountOffset, &count, sizeof count);
+  }
   if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
   if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
-  e = cudaMemcpyAsync(h->int_ws, img, bytes, cudaMemcpyHostToDevice, s);
+  e = cudaMemcpyAsync(h->int_ws, img, img_bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  if (h->graph) {
+    int32_t* tbl = reinterpret_cast<int32_t*>(img + img_bytes);
+    std::memcpy(tbl, kv_indptr_host, (size_t)(batch + 1) * sizeof(int32_t));
+    std::memcpy(tbl + batch + 1, kv_len_host, (size_t)batch * sizeof(int32_t));
+    e = cudaMemcpyAsync(h->g_indptr, tbl, (size_t)(batch + 1) * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->g_lpl, tbl + batch + 1, (size_t)batch * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, s);
+    const int64_t n_ids = kv_indptr_host[batch];
+    if (e == cudaSuccess && n_ids > 0 && kv_indices_dev != h->g_indices)
+      e = cudaMemcpyAsync(h->g_indices, kv_indices_dev, (size_t)n_ids * sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the page table into the graph buffers");
+  }
   if (int rc2 = staging_release(h, slot, s)) return rc2;
 
   h->plan = std::move(plan);
@@ -837,8 +881,10 @@ int pkd_mla_plan(pkd_handle* h, const int32_t* kv_indptr_host, const int32_t* kv
   h->o_dtype = q_dtype;
   h->sm_scale = sm_scale;
   h->cap = 0.f;
-  h->indices = kv_indices_dev;
+  h->indices = h->graph ? h->g_indices : kv_indices_dev;
   h->ws_layout = lay;
+  if (h->graph) h->g_batch = batch;
+  h->planned_heads = num_heads;
   h->pos_mode = PKD_POS_NONE;
   h->kernel = nullptr;
   h->mla = true;
@@ -855,7 +901,7 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
   if (!h->planned || !h->mla)
     return fail(PKD_ERR_NOT_PLANNED, "pkd_mla_run called without a successful pkd_mla_plan");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (h->plan.items.empty()) return PKD_OK;
+  if (h->plan.items.empty() && !h->graph) return PKD_OK;
   if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !o)
     return fail(PKD_ERR_INVALID_ARG, "null q_nope / q_pe / ckv / kpe / o");
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(ckv_cache, 16) ||
@@ -871,6 +917,7 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
   prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(lay));
   prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
   prm.status = reinterpret_cast<uint32_t*>(iws);
+  prm.item_count = h->graph ? reinterpret_cast<const int32_t*>(iws + kItemCountOffset) : nullptr;
   prm.indices = h->indices;
   prm.ckv = ckv_cache;
   prm.kpe = kpe_cache;
@@ -890,7 +937,9 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
   prm.page_size = h->page_size;
   prm.lse_base_e = lse_base_e ? 1 : 0;
   prm.scale_log2 = (float)((double)h->sm_scale * 1.4426950408889634);
-  const int64_t grid = (int64_t)h->plan.items.size() * h->plan.gslices;
+  // CUDA-graph mode: the same grid for every plan (the capacity), CTAs past the count exit
+  const int64_t grid =
+      (h->graph ? (int64_t)h->g_max_items : (int64_t)h->plan.items.size()) * h->plan.gslices;
   void* args[] = {&prm};
   cudaError_t e;
   if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
@@ -974,6 +1023,27 @@ int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads,
   }
   const WsLayout lay = capacity_layout(max_items, num_kv_heads, (G + hpc - 1) / hpc);
   if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(lay, num_qo_heads, head_dim);
+  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(lay);
+  return PKD_OK;
+}
+
+int pkd_mla_graph_workspace_bytes(int max_items, int num_heads, int backend,
+                                  size_t* float_ws_bytes, size_t* int_ws_bytes) {
+  if (max_items < 1 || num_heads <= 0)
+    return fail(PKD_ERR_INVALID_ARG, "bad capacity or head count");
+  if (backend != PKD_MLA_BACKEND_AUTO && backend != PKD_MLA_BACKEND_MMA_SYNC &&
+      backend != PKD_MLA_BACKEND_TCGEN05)
+    return fail(PKD_ERR_INVALID_ARG, "backend must be PKD_MLA_BACKEND_AUTO, _MMA_SYNC or _TCGEN05");
+  const int variant = backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
+                      : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
+                      : num_heads > 64                     ? kMlaTcgen05
+                                                           : kMlaMmaSync;
+  const MlaKernel* k = find_mla(kBF16, variant);
+  if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built");
+  const int cph = k->ctas_per_head_tile;
+  const int gslices = (num_heads + k->heads_per_cta - 1) / k->heads_per_cta * cph;
+  const WsLayout lay = capacity_layout(max_items, 1, gslices);
+  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(lay, num_heads * cph, 512 / cph);
   if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(lay);
   return PKD_OK;
 }

@@ -129,6 +129,8 @@ struct MlaParams {
   uint32_t* status;
   const MergeEntry* merges;
   uint32_t* counters;     // per (merge entry, head slice)
+  const int32_t* item_count;  // CUDA-graph mode: the plan's item count, read on the device (the
+                              // grid is cut for a fixed capacity); null: the grid is exact
   int64_t num_pages;      // pages in the caches: ids outside [0, num_pages) read as zeros
   int num_heads;
   int gslices;            // CTAs per item: head tiles x CTAs per head tile

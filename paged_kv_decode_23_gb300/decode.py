@@ -293,6 +293,18 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
                 num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
 
 
+def mla_graph_workspace_bytes(max_items: int, num_heads: int, backend: str = "auto"):
+    """(float, int) workspace bytes BatchMLAPagedAttention needs in CUDA-graph mode for a work
+    list of max_items chunks."""
+    if backend not in _MLA_BACKEND:
+        raise ValueError(f"backend must be one of {sorted(_MLA_BACKEND)}")
+    fb, ib = ctypes.c_size_t(), ctypes.c_size_t()
+    L.check(L.lib().pkd_mla_graph_workspace_bytes(int(max_items), num_heads,
+                                                  _MLA_BACKEND[backend], ctypes.byref(fb),
+                                                  ctypes.byref(ib)))
+    return fb.value, ib.value
+
+
 def mla_plan_host(kv_indptr, kv_len_arr, num_heads: int, page_size: int,
                   dtype: int = L.DTYPE_BF16, backend: str = "auto", num_sms: int = 152):
     """The MLA work list ``BatchMLAPagedAttention.plan`` would upload, built on the host alone
@@ -374,10 +386,22 @@ class BatchMLAPagedAttention:
 
     ``backend``: "auto" (the tcgen05 kernel for more than 64 heads, else "fa2"), "fa2" (32
     heads per CTA on mma.sync with register accumulators) or "tcgen05" (128 heads per 2-CTA
-    cluster on the 5th-generation tensor cores, accumulators in tensor memory)."""
+    cluster on the 5th-generation tensor cores, accumulators in tensor memory).
 
-    def __init__(self, float_workspace_buffer: torch.Tensor,
-                 int_workspace_buffer: Optional[torch.Tensor] = None, backend: str = "auto"):
+    ``use_cuda_graph=True`` with the device int32 buffers ``qo_indptr`` / ``kv_indptr``
+    ``[max_batch + 1]``, ``kv_indices`` ``[max_pages]`` and ``kv_len_arr`` ``[max_batch]``
+    makes ``run`` capturable in a CUDA graph whose replays stay valid across later ``plan``
+    calls: ``plan`` copies the page table into those buffers; the first plan fixes the batch
+    size (pad with zero-length requests), the head count, page size, sm_scale and dtype; the
+    work list holds at most ``max_items`` chunks (default: max_batch + the SM count)."""
+
+    def __init__(self, float_workspace_buffer: torch.Tensor, use_cuda_graph: bool = False,
+                 qo_indptr: Optional[torch.Tensor] = None,
+                 kv_indptr: Optional[torch.Tensor] = None,
+                 kv_indices: Optional[torch.Tensor] = None,
+                 kv_len_arr: Optional[torch.Tensor] = None, backend: str = "auto",
+                 int_workspace_buffer: Optional[torch.Tensor] = None,
+                 max_items: Optional[int] = None):
         if backend not in _MLA_BACKEND:
             raise ValueError(f"backend must be one of {sorted(_MLA_BACKEND)}")
         if not float_workspace_buffer.is_cuda:
@@ -388,6 +412,7 @@ class BatchMLAPagedAttention:
         self._float_ws = float_workspace_buffer
         self._int_ws = int_workspace_buffer
         self._plan_args = None
+        self.use_cuda_graph = bool(use_cuda_graph)
         h = ctypes.c_void_p()
         L.check(L.lib().pkd_create(ctypes.byref(h), self._float_ws.data_ptr(),
                                    self._float_ws.numel() * self._float_ws.element_size(),
@@ -396,6 +421,23 @@ class BatchMLAPagedAttention:
                                    L.LAYOUT_NHD))
         self._h = h
         L.check(L.lib().pkd_mla_set_backend(h, _MLA_BACKEND[backend]))
+        if self.use_cuda_graph:
+            if kv_indptr is None or kv_indices is None or kv_len_arr is None:
+                raise ValueError("use_cuda_graph=True needs kv_indptr, kv_indices and kv_len_arr "
+                                 "buffers")
+            lens = _graph_buffer(kv_len_arr, "kv_len_arr", 1)
+            max_batch = lens.numel()
+            ip = _graph_buffer(kv_indptr, "kv_indptr", max_batch + 1)
+            ix = _graph_buffer(kv_indices, "kv_indices", 0)
+            qo = _graph_buffer(qo_indptr, "qo_indptr", max_batch + 1) if qo_indptr is not None \
+                else None
+            self._graph_buffers = (qo, ip, ix, lens)
+            if max_items is None:
+                props = torch.cuda.get_device_properties(float_workspace_buffer.device)
+                max_items = max_batch + props.multi_processor_count
+            L.check(L.lib().pkd_enable_cuda_graph(self._h, ip.data_ptr(), ix.data_ptr(),
+                                                  lens.data_ptr(), max_batch, ix.numel(),
+                                                  int(max_items)))
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -430,6 +472,10 @@ class BatchMLAPagedAttention:
             kv_indices.numel(), num_heads, head_dim_ckv, head_dim_kpe, page_size,
             int(bool(causal)), float(sm_scale), _DTYPE_CODE[q_dt], _DTYPE_CODE[kv_dt],
             _stream_ptr(stream)))
+        if self.use_cuda_graph and self._graph_buffers[0] is not None:
+            # the qo_indptr buffer holds 0, 1, ..., batch like the page's wrapper (no kernel
+            # reads it: one query per request)
+            self._graph_buffers[0][:batch + 1].copy_(torch.from_numpy(q_ip), non_blocking=True)
         self._indices = kv_indices
         self._plan_args = dict(batch=batch, num_heads=num_heads, page_size=page_size, dtype=q_dt)
 

@@ -185,3 +185,99 @@ def test_mla_page_ids_outside_the_caches_read_as_zero_rows(backend):
     zc = torch.cat([ckv, torch.zeros_like(ckv[:1])])
     zk = torch.cat([kpe, torch.zeros_like(kpe[:1])])
     _close(got, _oracle(w_ref, qn, qp, zc, zk), f"mla bad page ids {backend}")
+
+
+@pytest.mark.parametrize("backend,heads", [("fa2", 32), ("tcgen05", 128)])
+def test_mla_cuda_graph_replays_across_plans(backend, heads):
+    """The wrapper's use_cuda_graph=True: run() captured once replays correctly after later
+    plans of the same batch size (different lengths, splits and zero-length padding), each
+    checked against the oracle."""
+    from paged_kv_decode_23_gb300 import BatchMLAPagedAttention, mla_graph_workspace_bytes
+    dev = torch.device("cuda")
+    ps, batch = 16, 4
+    base = W.mla_custom([3000] * batch, heads, ps, "bf16", seed=31, pool_factor=1.0)
+    ckv, kpe = W.make_mla_cache(base)
+    ckv_d, kpe_d = ckv.to(dev), kpe.to(dev)
+    max_pages = base.num_pages
+    fb, ib = mla_graph_workspace_bytes(batch + 152, heads, backend)
+    ws = torch.zeros(fb, dtype=torch.uint8, device=dev)
+    iws = torch.zeros(ib, dtype=torch.uint8, device=dev)
+    bufs = dict(qo_indptr=torch.zeros(batch + 1, dtype=torch.int32, device=dev),
+                kv_indptr=torch.zeros(batch + 1, dtype=torch.int32, device=dev),
+                kv_indices=torch.zeros(max_pages, dtype=torch.int32, device=dev),
+                kv_len_arr=torch.zeros(batch, dtype=torch.int32, device=dev))
+    mla = BatchMLAPagedAttention(ws, use_cuda_graph=True, backend=backend,
+                                 int_workspace_buffer=iws, max_items=batch + 152, **bufs)
+    qn_s = torch.zeros(batch, heads, 512, dtype=torch.bfloat16, device=dev)
+    qp_s = torch.zeros(batch, heads, 64, dtype=torch.bfloat16, device=dev)
+    o_s = torch.zeros_like(qn_s)
+    lse_s = torch.zeros(batch, heads, dtype=torch.float32, device=dev)
+    rng = np.random.default_rng(6)
+    plans = [[3000, 17, 250, 999], [100, 2900, 0, 0], [1, 1, 1, 1], [2990, 2980, 2970, 2960]]
+    graph = None
+    for k, lens in enumerate(plans):
+        lens = np.asarray(lens, dtype=np.int64)
+        pages = np.where(lens > 0, (lens + ps - 1) // ps, 0)
+        indptr = np.zeros(batch + 1, dtype=np.int32)
+        np.cumsum(pages, out=indptr[1:])
+        indices = rng.permutation(max_pages)[:indptr[-1]].astype(np.int32)
+        w = W.MlaWorkload("graph", batch, heads, ps, "bf16", lens.astype(np.int32), indptr,
+                          indices, max_pages, sm_scale=base.sm_scale, seed=31 + k)
+        idx_dev = torch.from_numpy(indices if len(indices) else np.zeros(1, np.int32)).to(dev)
+        mla.plan(torch.arange(batch + 1, dtype=torch.int32), torch.from_numpy(indptr), idx_dev,
+                 torch.from_numpy(w.kv_lens), heads, 512, 64, ps, False, w.sm_scale,
+                 torch.bfloat16, torch.bfloat16)
+        qn, qp = W.make_mla_q(w, layer=k)
+        qn_s.copy_(qn.to(dev))
+        qp_s.copy_(qp.to(dev))
+        if graph is None:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):  # warm-up outside the capture
+                mla.run(qn_s, qp_s, ckv_d, kpe_d, out=o_s, lse=lse_s, return_lse=True,
+                        return_lse_base_on_e=True)
+            torch.cuda.current_stream().wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                mla.run(qn_s, qp_s, ckv_d, kpe_d, out=o_s, lse=lse_s, return_lse=True,
+                        return_lse_base_on_e=True)
+        o_s.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert mla.check_status() == 0
+        assert torch.equal(bufs["kv_len_arr"].cpu(), torch.from_numpy(w.kv_lens))
+        _close((o_s.double().cpu().numpy(), lse_s.double().cpu().numpy()),
+               _oracle(w, qn, qp, ckv, kpe), f"mla graph plan {k} {backend}")
+
+
+def test_mla_cuda_graph_rejects_changed_shapes():
+    """In CUDA-graph mode the first plan fixes the batch size and what a captured run holds."""
+    from paged_kv_decode_23_gb300 import BatchMLAPagedAttention, PkdError
+    dev = torch.device("cuda")
+    bufs = dict(kv_indptr=torch.zeros(5, dtype=torch.int32, device=dev),
+                kv_indices=torch.zeros(64, dtype=torch.int32, device=dev),
+                kv_len_arr=torch.zeros(4, dtype=torch.int32, device=dev))
+    mla = BatchMLAPagedAttention(torch.zeros(64 << 20, dtype=torch.uint8, device=dev),
+                                 use_cuda_graph=True, **bufs)
+    idx = torch.arange(8, dtype=torch.int32, device=dev)
+
+    def plan(batch, heads=32, ps=1, scale=0.1):
+        lens = np.full(batch, 2, dtype=np.int32)
+        ip = np.arange(0, 2 * batch + 1, 2, dtype=np.int32)
+        mla.plan(torch.arange(batch + 1, dtype=torch.int32), torch.from_numpy(ip), idx,
+                 torch.from_numpy(lens), heads, 512, 64, ps, False, scale, torch.bfloat16,
+                 torch.bfloat16)
+
+    plan(4)
+    with pytest.raises(PkdError):
+        plan(3)          # batch changed
+    with pytest.raises(PkdError):
+        plan(4, heads=16)
+    with pytest.raises(PkdError):
+        plan(4, ps=2)
+    with pytest.raises(PkdError):
+        plan(4, scale=0.2)
+    with pytest.raises(ValueError):
+        BatchMLAPagedAttention(torch.zeros(1 << 20, dtype=torch.uint8, device=dev),
+                               use_cuda_graph=True)
+    plan(4)  # the same shapes plan again

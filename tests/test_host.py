@@ -321,6 +321,20 @@ def test_mla_plan_one_long_request_fills_the_gpu(pkd):
     assert _mla_partition_ok(plan, w.kv_indptr, w.kv_lens)[0][1] == 200
 
 
+def test_mla_graph_workspace_bytes(pkd):
+    """CUDA-graph mode sizes the workspaces for the capacity: partials for every item slot of
+    every head slice, growing with the capacity and the head count."""
+    f1, i1 = pkd.mla_graph_workspace_bytes(100, 128, "tcgen05")
+    f2, i2 = pkd.mla_graph_workspace_bytes(200, 128, "tcgen05")
+    assert f2 > f1 > 100 * 128 * 512 * 4 and i2 > i1 > 100 * 32
+    f3, _ = pkd.mla_graph_workspace_bytes(100, 256, "fa2")
+    assert f3 > 100 * 256 * 512 * 4
+    with pytest.raises(pkd.PkdError):
+        pkd.mla_graph_workspace_bytes(0, 128)
+    with pytest.raises(ValueError):
+        pkd.mla_graph_workspace_bytes(10, 128, "fa3")
+
+
 def test_mla_plan_rejects_bad_input(pkd):
     with pytest.raises(pkd.PkdError):  # kv_len beyond the pages
         pkd.mla_plan_host(np.array([0, 1], np.int32), np.array([5], np.int32), 16, 4)
