@@ -566,6 +566,26 @@ def mla_kernel_name(args, w) -> str:
     return "mla_tc_kernel" if tc else "mla_decode_kernel"
 
 
+def mla_roofline(flops, nbytes, kern_ms, tf_peak, tf_kind, hbm_peak, traffic, kernel):
+    """The roofline that binds one MLA launch: HBM when its arithmetic intensity (algorithmic
+    flops per algorithmic byte) lies below the ridge point of the two measured peaks, else the
+    tensor cores; the other roof is reported beside it."""
+    tflops = flops / (kern_ms * 1e-3) / 1e12
+    gbs = nbytes / (kern_ms * 1e-3) / 1e9
+    intensity = flops / nbytes
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
+    hbm = {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+           "algorithmic_bytes_per_launch": nbytes}
+    tensor = {"achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s", "frac": tflops / tf_peak,
+              "algorithmic_flops_per_launch": flops, "peak_kind": tf_kind}
+    main, other, bound = (hbm, tensor, "hbm") if intensity < ridge else (tensor, hbm, "tensor")
+    out = {"bound": bound, **main, "traffic": traffic, "kernel": kernel,
+           "kernel_us": kern_ms * 1e3, "intensity_flop_per_byte": intensity,
+           "ridge_flop_per_byte": ridge}
+    out["tensor" if bound == "hbm" else "hbm"] = other
+    return out
+
+
 def mla_gpu_arm(args, w, rank, world):
     import torch
 
@@ -679,7 +699,6 @@ def mla_gpu_arm(args, w, rank, world):
             tf_peak, tf_kind = float(json.load(f)["bf16_tflops"]), "measured (burst)"
     except Exception:
         tf_peak, tf_kind = 1900.0, "fallback"
-    tflops = flops_call / (kern_ms * 1e-3) / 1e12
     h2d = (qn_h.numel() + qp_h.numel()) * qn_h.element_size() + idx_h.numel() * 4
     d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
     return {
@@ -696,16 +715,9 @@ def mla_gpu_arm(args, w, rank, world):
         "us_per_call": ms_step * 1e3,
         "pct_of_hbm_peak": 100.0 * (bytes_call / (ms_step * 1e-3) / 1e9) / hbm_peak,
         "peak_kind": peak_kind,
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s",
-                     "frac": tflops / tf_peak,
-                     "traffic": mla_measured_traffic(mla_kernel_name(args, w))
-                     if w.name == "mla" else None,
-                     "kernel": mla_kernel_name(args, w),
-                     "kernel_us": kern_ms * 1e3, "algorithmic_flops_per_launch": flops_call,
-                     "peak_kind": tf_kind,
-                     "hbm": {"achieved": bytes_call / (kern_ms * 1e-3) / 1e9, "peak": hbm_peak,
-                             "unit": "GB/s", "frac": bytes_call / (kern_ms * 1e-3) / 1e9 / hbm_peak,
-                             "algorithmic_bytes_per_launch": bytes_call}},
+        "roofline": mla_roofline(flops_call, bytes_call, kern_ms, tf_peak, tf_kind, hbm_peak,
+                                 mla_measured_traffic(mla_kernel_name(args, w))
+                                 if w.name == "mla" else None, mla_kernel_name(args, w)),
         "e2e": {"value": replica_value(bytes_call, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s / args.steps * 1e3},
