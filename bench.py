@@ -562,7 +562,7 @@ def mla_reference_arm(args, w):
 
 
 def mla_kernel_name(args, w) -> str:
-    tc = args.mla_backend == "tcgen05" or (args.mla_backend == "auto" and w.num_heads > 64)
+    tc = args.mla_backend == "tcgen05" or (args.mla_backend == "auto" and w.num_heads > 32)
     return "mla_tc_kernel" if tc else "mla_decode_kernel"
 
 
@@ -741,7 +741,7 @@ def main():
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
                     help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
     ap.add_argument("--mla-backend", choices=["auto", "fa2", "tcgen05"], default="auto",
-                    help="MLA kernel (--workload mla): auto picks tcgen05 for > 64 heads")
+                    help="MLA kernel (--workload mla): auto picks tcgen05 for > 32 heads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,

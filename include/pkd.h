@@ -233,7 +233,7 @@ int pkd_mla_run(pkd_handle* h, const void* q_nope, const void* q_pe, const void*
 
 /*
  * MLA kernel used by later pkd_mla_plan calls on this handle (the wrapper's backend argument):
- *   PKD_MLA_BACKEND_AUTO      the tcgen05 kernel when num_heads > 64, else the mma.sync kernel;
+ *   PKD_MLA_BACKEND_AUTO      the tcgen05 kernel when num_heads > 32, else the mma.sync kernel;
  *   PKD_MLA_BACKEND_MMA_SYNC  32 heads per CTA, mma.sync with register accumulators;
  *   PKD_MLA_BACKEND_TCGEN05   128 heads per 2-CTA cluster (the pair splits the 576 features),
  *                             tcgen05 MMAs with accumulators in tensor memory.

@@ -688,16 +688,23 @@ int pkd_run(pkd_handle* h, const void* q, const void* k_base, const void* v_base
 
 namespace {
 
+// The kernel `backend` names; auto takes the tcgen05 pair kernel above 32 heads.  Measured on
+// GB300 (page 1, bf16): the pair kernel's time barely depends on the head count (its row
+// gathers set the pace), while the mma.sync kernel re-reads the rows for every 32-head slice --
+// at 64 heads the pair kernel is 1.5-1.7x faster, at 16-32 heads the two are within 10 %.
+int mla_variant_for(int backend, int num_heads) {
+  return backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
+         : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
+         : num_heads > 32                     ? kMlaTcgen05
+                                              : kMlaMmaSync;
+}
+
 // The MLA work list and the kernel that runs it (shared by pkd_mla_plan and the host-only
-// pkd_mla_plan_host): auto takes the tcgen05 pair kernel when a 128-head tile is at least
-// half full.
+// pkd_mla_plan_host).
 int build_mla_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int batch,
                    int num_heads, int page_size, int dtype, int backend, int num_sms,
                    const MlaKernel** kernel, Plan* plan, int max_items = 0) {
-  const int variant = backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
-                      : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
-                      : num_heads > 64                     ? kMlaTcgen05
-                                                           : kMlaMmaSync;
+  const int variant = mla_variant_for(backend, num_heads);
   const MlaKernel* k = find_mla(dtype, variant);
   if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built for this dtype");
   PlanRequest r;
@@ -1034,10 +1041,7 @@ int pkd_mla_graph_workspace_bytes(int max_items, int num_heads, int backend,
   if (backend != PKD_MLA_BACKEND_AUTO && backend != PKD_MLA_BACKEND_MMA_SYNC &&
       backend != PKD_MLA_BACKEND_TCGEN05)
     return fail(PKD_ERR_INVALID_ARG, "backend must be PKD_MLA_BACKEND_AUTO, _MMA_SYNC or _TCGEN05");
-  const int variant = backend == PKD_MLA_BACKEND_MMA_SYNC  ? kMlaMmaSync
-                      : backend == PKD_MLA_BACKEND_TCGEN05 ? kMlaTcgen05
-                      : num_heads > 64                     ? kMlaTcgen05
-                                                           : kMlaMmaSync;
+  const int variant = mla_variant_for(backend, num_heads);
   const MlaKernel* k = find_mla(kBF16, variant);
   if (!k) return fail(PKD_ERR_UNSUPPORTED, "no MLA kernel built");
   const int cph = k->ctas_per_head_tile;

@@ -384,7 +384,7 @@ class BatchMLAPagedAttention:
     over one latent cache; key = [ckv, kpe] (512 + 64), value = ckv.  Decode only: every
     query length in ``qo_indptr`` must be 1.
 
-    ``backend``: "auto" (the tcgen05 kernel for more than 64 heads, else "fa2"), "fa2" (32
+    ``backend``: "auto" (the tcgen05 kernel for more than 32 heads, else "fa2"), "fa2" (32
     heads per CTA on mma.sync with register accumulators) or "tcgen05" (128 heads per 2-CTA
     cluster on the 5th-generation tensor cores, accumulators in tensor memory).
 

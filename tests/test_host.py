@@ -268,10 +268,12 @@ def _mla_partition_ok(plan, kv_indptr, kv_lens):
 @pytest.mark.parametrize("backend,heads,ctas", [("fa2", 40, 2), ("fa2", 128, 4),
                                                 ("tcgen05", 40, 2), ("tcgen05", 128, 2),
                                                 ("tcgen05", 192, 4), ("auto", 64, 2),
-                                                ("auto", 128, 2)])
+                                                ("auto", 128, 2), ("auto", 32, 1),
+                                                ("auto", 96, 2)])
 def test_mla_plan_partitions_requests(pkd, backend, heads, ctas):
     """MLA work lists (host-only planner): a partition of every request for each kernel, with
-    the kernel's CTAs per item (32-head slices for fa2, 128-head CTA pairs for tcgen05)."""
+    the kernel's CTAs per item (32-head slices for fa2, 128-head CTA pairs for tcgen05; auto
+    takes the pair kernel above 32 heads: 96 heads are one pair, not three slices)."""
     w = W.mla_custom([1, 31, 32, 33, 0, 100, 777, 64, 5000, 12000], heads, 16, "bf16", seed=3)
     plan = pkd.mla_plan_host(w.kv_indptr, w.kv_lens, heads, 16, backend=backend)
     assert plan["ctas_per_item"] == ctas
