@@ -425,13 +425,17 @@ def gpu_arm(args, w, rank, world):
     idx_host = torch.from_numpy(w.indices).pin_memory()
     idx_dev = torch.empty_like(indices)
 
+    # With one layer the L2 flush runs before each step's clock starts (every step still starts
+    # cold); with several it stays between the layers, inside the step.
+    flush_before = flush is not None and layers == 1
+
     def e2e_step():
         idx_dev.copy_(idx_host, non_blocking=True)
         q_all_dev.copy_(q_all_host, non_blocking=True)
         dec.plan(indptr_t, idx_dev, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                  w.page_size, **plan_kw)
         for l in range(layers):
-            if flush is not None:
+            if flush is not None and not flush_before:
                 flush(float(l))
             dec.run(q_all_dev[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale,
                     out=o_all_dev[l], lse=l_all_dev[l])
@@ -442,11 +446,15 @@ def gpu_arm(args, w, rank, world):
     for _ in range(args.warmup):
         e2e_step()
     barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
+    e2e_s = 0.0
+    for k in range(args.steps):
+        if flush_before:
+            flush(float(k))
+            torch.cuda.current_stream().synchronize()
+        t0 = time.perf_counter()
         e2e_step()
+        e2e_s += time.perf_counter() - t0
     barrier()
-    e2e_s = time.perf_counter() - t0
     h2d = q_all_host.numel() * q_all_host.element_size() + idx_host.numel() * 4
     d2h = o_all_host.numel() * o_all_host.element_size() + l_all_host.numel() * 4
 
@@ -477,7 +485,10 @@ def gpu_arm(args, w, rank, world):
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": {"value": replica_value(bytes_step, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s / args.steps * 1e3},
+                "ms_per_step": e2e_s / args.steps * 1e3,
+                "l2": ("flushed before each step, outside its clock" if flush_before else
+                       "flushed between layers, inside the step" if flush is not None else
+                       "every layer reads its own pool, far larger than L2")},
         "gpu_launches": args.steps * layers,
         "clocks": clk,
         "host_plan_us": host_plan_us,
@@ -678,18 +689,22 @@ def mla_gpu_arm(args, w, rank, world):
         qn_d.copy_(qn_h, non_blocking=True)
         qp_d.copy_(qp_h, non_blocking=True)
         plan(idx_d)
-        flush(1.0)
         mla.run(qn_d, qp_d, ckv, kpe, out=out, lse=lse)
         o_h.copy_(out, non_blocking=True)
         l_h.copy_(lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
+    # the L2 flush runs before each step's clock starts: every step starts cold
     for _ in range(args.warmup):
+        flush(1.0)
         e2e_step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
+    e2e_s = 0.0
+    for k in range(args.steps):
+        flush(float(k))
+        torch.cuda.current_stream().synchronize()
+        t0 = time.perf_counter()
         e2e_step()
-    e2e_s = time.perf_counter() - t0
+        e2e_s += time.perf_counter() - t0
     ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, device=dev)
     bytes_call, flops_call = mla_bytes_flops(w)
     ms_step = ms_total / args.steps
@@ -720,7 +735,8 @@ def mla_gpu_arm(args, w, rank, world):
                                  if w.name == "mla" else None, mla_kernel_name(args, w)),
         "e2e": {"value": replica_value(bytes_call, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s / args.steps * 1e3},
+                "ms_per_step": e2e_s / args.steps * 1e3,
+                "l2": "flushed before each step, outside its clock"},
         "gpu_launches": args.steps,
         "clocks": clk,
         "segments": {"plan_us_per_step": plan_ms * 1e3 / args.steps,
