@@ -13,7 +13,7 @@
 // each CTA multiplies P by the value columns it loaded itself.  Every byte of the caches is
 // read once, by one CTA.
 //
-// Roles (288 threads):
+// Roles (416 threads):
 //   warps 0-3  softmax: thread h owns head h (TMEM lane h).  The exchange runs two tiles
 //              ahead of the softmax (S is triple-buffered in TMEM), so its latency hides behind
 //              the softmax of the tiles in between.  Online softmax with a lazy reference (O in
@@ -21,7 +21,7 @@
 //              TMEM as a 16-bit value and its rounding remainder (P_hi + P_lo), so the 16-bit
 //              rounding of P costs no accuracy.  Epilogue through shared memory (coalesced
 //              stores) and the fused merge of split requests.
-//   warps 4-7  producer: 16-byte cp.async gathers of the token rows (any page size; a TMA
+//   warps 4-7, 9-12  producer: 16-byte cp.async gathers of the token rows (any page size; a TMA
 //              request per row is rate-bound for rows this small), zero-filled for tokens
 //              outside the item and for page ids outside the caches, into NST stages laid out
 //              as the MMA's 128-byte-swizzled K-major blocks (8 rows x 128 bytes per atom).  It
@@ -63,7 +63,8 @@ constexpr int SMEM_BYTES = OFF_XIN + 2 * XBUF_BYTES + 1024;  // + alignment slac
 // epilogue staging (rows of 256 outputs) reuses [OFF_STAGE, ...): stages, then the exchange
 constexpr int STAGE_OUT_BYTES = HT * 256 * 4;
 constexpr int NSOFT = 128;
-constexpr int NPROD = 128;
+constexpr int NPW = 8;                        // producer warps: 4-7 and 9-12 (row pw + 8 k)
+constexpr int NPROD = NPW * 32;
 constexpr int THREADS = NSOFT + NPROD + 32;
 constexpr int TMEM_COLS = 512;
 constexpr int TM_S = 0;      // three S buffers: columns [0, 96)
@@ -357,22 +358,26 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
   const uint32_t tmem = tmem_base_s;
   if (abort_flag_s) ntiles = 0;  // an earlier launch timed out: do nothing, write nothing
 
-  if (warp >= 4 && warp < 8) {
+  if ((warp >= 4 && warp < 8) || warp >= 9) {
     // ================================================================ producer
     cluster_arrive();  // nothing here depends on the peer: start at once
-    const int pw = warp - 4;  // rows 8 pw .. 8 pw + 7 of each tile
+    const int pw = warp < 8 ? warp - 4 : warp - 5;  // rows pw, pw + NPW, ... of each tile
     const int ps = p.page_size;
     const char* ckv = static_cast<const char*>(p.ckv) + rank * 512;
     const char* kpe = static_cast<const char*>(p.kpe);
     const uint64_t pol = policy_evict_first();
-    // lane r (< 8; lanes 8-31 repeat lanes 0-7): page id of tile row 8 pw + r of tile i, or -1
+    // Eight warps, not four: the gathers are bound by the copies in flight, and more issuing
+    // warps keep more in flight (114.4 us with six warps, 110.2 with eight, 120.6 with four on
+    // the batch-114 example).
+    // lane r (< 8; lanes 8-31 repeat lanes 0-7): page id of tile row pw + NPW r of tile i, or -1
     // for a row that is not a token of the item (zero-filled).  ids[k] holds tile i + k: the
     // ids of a tile are loaded kIdTiles iterations before its copies.  (An L2 prefetch of the
     // rows a few tiles ahead measured 3 % slower: the gathers are rate-bound per SM, not by
     // DRAM latency.)
     auto page_of = [&](int i) -> int {
-      const int t = it.chunk_tok0 + (j0 + i) * TS + 8 * pw + (lane & 7);
-      return (i < ntiles && t >= it.tok_begin && t < it.tok_end)
+      const int r = pw + NPW * (lane & 7);
+      const int t = it.chunk_tok0 + (j0 + i) * TS + r;
+      return (i < ntiles && r < TS && t >= it.tok_begin && t < it.tok_end)
                  ? __ldg(p.indices + it.page_base + t / ps)
                  : -1;
     };
@@ -394,8 +399,9 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
       const uint32_t stage = sb + OFF_STAGE + s * STAGE_BYTES;
       const int tt0 = it.chunk_tok0 + (j0 + i) * TS;
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int row = 8 * pw + rr;
+      for (int rr = 0; rr < (TS + NPW - 1) / NPW; ++rr) {
+        const int row = pw + NPW * rr;
+        if (row >= TS) break;  // the same for every lane
         const int64_t pid = __shfl_sync(~0u, pid_mine, rr);
         const bool ok = pid >= 0 && pid < p.num_pages;
         const int64_t prow = ok ? pid * ps + (tt0 + row) % ps : 0;
