@@ -62,8 +62,8 @@ def kernel_sources_digest() -> str:
 MLA_KERNEL_SOURCES = ("mla_tc_kernels.cuh", "pkd_device.cuh", "pkd_internal.h", "mla_tc.cu",
                       "planner.cpp")
 MLA_MEASURED_TRAFFIC = {
-    "sources_sha256": "b4a3e3bed16047de17480bc3a613160ca60058d8b4bdedeb0267f4e758af920e",
-    "mla_tc_kernel": 151361280.0,
+    "sources_sha256": "be60d2270a553b21513343a0400e914bf920f35ebf81494b01bd9bd705bec2b3",
+    "mla_tc_kernel": 151634176.0,
 }
 
 
