@@ -6,7 +6,8 @@ wrong lse, a soft cap without the division, swapped strides, a wrong kv-length r
 unweighted merge, a missing v_scale, wrong fp16 / e4m3 decoders, and for several query tokens
 per request a causal limit one past the query, reversed token positions and token-major rows,
 for the positional encodings a reversed RoPE rotation, a rope_scale that multiplies and an
-ALiBi bias of the wrong sign, and an MLA logit without its rope (kpe) part.  The pin suite in
+ALiBi bias of the wrong sign and the wrong half of
+the 2m-head slope set for head counts that are not a power of two, and an MLA logit without its rope (kpe) part.  The pin suite in
 ``test_oracle_pins.py`` runs against each mutant and must fail.
 """
 import os
@@ -28,6 +29,8 @@ MUTANTS = {
     "rope_rotation_reversed": ("x[i] = x0 * c - x1 * s;", "x[i] = x0 * c + x1 * s;"),
     "rope_scale_multiplies": ("const double a = (pos / rope_scale)", "const double a = (pos * rope_scale)"),
     "alibi_distance_sign": ("slope * (double)(t - pos)", "slope * (double)(pos - t)"),
+    "alibi_other_heads_take_even_entries": ("-4.0 * (2 * (g - m) + 1) / m",
+                                            "-4.0 * (2 * (g - m) + 2) / m"),
     "mla_rope_part_dropped": ("dot += load_elem(q_pe, w * dp + d, q_dtype) * load_elem(kpe, row * dp + d, kv_dtype);",
                               "dot += 0.0;"),
     "query_rows_token_major": ("(((int64_t)i * p->q_len + j) * p->num_qo_heads + g) * D",

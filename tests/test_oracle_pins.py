@@ -304,6 +304,32 @@ def test_alibi_slopes_of_eight_heads_are_powers_of_one_half():
                                rtol=0, atol=1e-14)
 
 
+def _oracle_alibi_slopes(H):
+    """The slopes the oracle applies, read back from its output: per head, two keys at
+    distances 1 and 0 behind the query with q = 0, V = 1 for the first key and 0 for the
+    second, so o = e^-s / (1 + e^-s) and s = ln((1 - o) / o)."""
+    D = 4
+    q = np.zeros((1, H, D))
+    K = [np.zeros((2, 1, D))]
+    V = [np.stack([np.ones((1, D)), np.zeros((1, D))])]
+    rng = np.random.default_rng(5)
+    indptr, indices, lpl, pool = _scatter([2], K, V, 4, "NHD", rng)
+    o, _ = _run_f64(indptr, indices, lpl, q, pool, "NHD", sm_scale=1.0,
+                    pos_encoding_mode="ALIBI")
+    p = o[0, :, 0]
+    return np.log((1.0 - p) / p)
+
+
+@pytest.mark.parametrize("heads", [8, 16, 12])
+def test_alibi_slopes_match_the_published_sets(heads):
+    """The oracle's ALiBi slopes against the values the ALiBi paper prints (tests/golden/
+    alibi_slopes.json): its 8- and 16-head sets, and for 12 heads (not a power of two, as in
+    the GPU ALiBi test) the 8-head set followed by alternate entries of the 16-head set."""
+    g = json.load(open(os.path.join(GOLDEN, "alibi_slopes.json")))
+    want = 2.0 ** -np.asarray(g[f"heads_{heads}"], dtype=np.float64)
+    np.testing.assert_allclose(_oracle_alibi_slopes(heads), want, rtol=1e-12, atol=0)
+
+
 def test_rope_depends_only_on_relative_position():
     """Rotating q at p and k at t gives a logit that depends only on t - p: a request whose
     keys are preceded by s unattended tokens (window) returns the same output as the bare
