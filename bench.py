@@ -329,40 +329,47 @@ def gpu_arm(args, w, rank, world):
             flush_w.fill_(v)
             torch.sum(flush_r, dim=0, out=flush_sum)
 
-    n_calls = layers
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n_calls * args.steps)]
-    for a, b in ev:  # torch creates the CUDA event on first record; the C ABI records it again
-        a.record(stream)
-        b.record(stream)
+    # Every timed step records events around its plan() upload and around its runs, so the
+    # decode kernel's time is read off the same steps the step time comes from: with several
+    # layers the runs segment holds the layers' launches back to back (programmatic dependent
+    # launch on, as in use); with an L2 flush between calls each call is a segment of its own
+    # and the flushes stay outside every segment.  Per-launch events in a second, untimed pass
+    # (PDL off, so each pair brackets exactly one kernel) give the isolated launch beside it.
+    def new_events(n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:  # torch creates the CUDA event on first record; the C ABI records it again
+            a.record(stream)
+            b.record(stream)
+        return evs
 
-    # With an L2 flush between calls, the step time is the sum of the timed segments (the
-    # plan's upload, then each call), so the flush writes stay outside the timed region.
-    seg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range((layers + 1) * args.steps)] if flush is not None else None
-
-    kernel_pass = [False]  # per-kernel events (they sit between launches, so a separate pass)
+    plan_ev = new_events(args.steps)
+    run_ev = new_events(args.steps * (layers if flush is not None else 1))
+    iso_ev = new_events(args.steps * layers)
+    iso_pass = [False]
 
     def step(k=None):
-        timed = seg is not None and k is not None and not kernel_pass[0]
+        timed = k is not None and not iso_pass[0]
         if timed:
-            seg[k * (layers + 1)][0].record(stream)
+            plan_ev[k][0].record(stream)
         dec.plan(indptr_t, indices, lpl_t, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                  w.page_size, **plan_kw)
         if timed:
-            seg[k * (layers + 1)][1].record(stream)
+            plan_ev[k][1].record(stream)
+            if flush is None:
+                run_ev[k][0].record(stream)
         for l in range(layers):
             if flush is not None:
                 flush(float(l))
-            if timed:
-                seg[k * (layers + 1) + 1 + l][0].record(stream)
-            e = ev[k * n_calls + l] if (k is not None and kernel_pass[0]) else None
-            # the kernel-timing pass launches in plain stream order, so each event pair
-            # brackets exactly one kernel
+                if timed:
+                    run_ev[k * layers + l][0].record(stream)
+            e = iso_ev[k * layers + l] if (k is not None and iso_pass[0]) else None
             dec.run(qs[l], pools[l], k_scale=w.k_scale, v_scale=w.v_scale, out=outs[l],
-                    lse=lses[l], timing_events=e, enable_pdl=not kernel_pass[0])
-            if timed:
-                seg[k * (layers + 1) + 1 + l][1].record(stream)
+                    lse=lses[l], timing_events=e, enable_pdl=not iso_pass[0])
+            if timed and flush is not None:
+                run_ev[k * layers + l][1].record(stream)
+        if timed and flush is None:
+            run_ev[k][1].record(stream)
 
     def barrier():
         if world > 1:
@@ -388,20 +395,18 @@ def gpu_arm(args, w, rank, world):
     torch.cuda.nvtx.range_pop()
     barrier()
     clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    # second pass: the decode kernel alone, timed with events around each launch
-    kernel_pass[0] = True
+    plan_ms = sum(a.elapsed_time(b) for a, b in plan_ev)
+    run_ms = sum(a.elapsed_time(b) for a, b in run_ev)
+    # with flushes the step is its timed segments; without, the whole timed loop
+    ms_total = plan_ms + run_ms if flush is not None else t_start.elapsed_time(t_end)
+    seg_detail = {"plan_us_per_step": plan_ms * 1e3 / args.steps,
+                  "run_us_per_call": run_ms * 1e3 / (args.steps * layers)}
+    # second pass, untimed for the step: each launch alone between its own events
+    iso_pass[0] = True
     for k in range(args.steps):
         step(k)
     torch.cuda.synchronize()
-    kernel_pass[0] = False
-    seg_detail = None
-    if seg is not None:
-        ms_total = sum(a.elapsed_time(b) for a, b in seg)
-        plan_ms = sum(seg[k * (layers + 1)][0].elapsed_time(seg[k * (layers + 1)][1])
-                      for k in range(args.steps))
-        seg_detail = {"plan_us_per_step": plan_ms * 1e3 / args.steps,
-                      "run_us_per_call": (ms_total - plan_ms) * 1e3 / (args.steps * layers)}
+    iso_pass[0] = False
     # the planner's own host cost: plan() calls with the GPU idle (inside the timed loop the
     # host runs ahead of the GPU and plan() would also measure the queue's back-pressure)
     torch.cuda.synchronize()
@@ -411,7 +416,7 @@ def gpu_arm(args, w, rank, world):
                  w.page_size, **plan_kw)
     host_plan_us = (time.perf_counter() - t_h) * 1e6 / 20
     torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    iso_ms = statistics.mean(a.elapsed_time(b) for a, b in iso_ev)
     assert dec.check_status() == 0, "device status word reports a failure"
 
     # End to end through the public API with host buffers: every step copies all layers' q and
@@ -465,7 +470,8 @@ def gpu_arm(args, w, rank, world):
     ms_step = ms_total / args.steps
     value = replica_value(bytes_step, world, ms_step)
     peak, peak_kind = load_peaks()
-    kern_avg_ms = statistics.mean(kern_ms)
+    # the decode kernel's time per call inside the timed steps (cannot exceed the step's share)
+    kern_avg_ms = run_ms / (args.steps * layers)
     achieved = bytes_call / (kern_avg_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -479,9 +485,13 @@ def gpu_arm(args, w, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else
-                     measured_traffic(w.name) if (args.kernel, args.pos_encoding) == ("auto", "NONE")
+                     measured_traffic(w.name)
+                     if (args.kernel, args.pos_encoding, args.qo_heads) == ("auto", "NONE", None)
                      else None,
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
+                     "kernel_us_source": "CUDA events around the runs of the timed steps "
+                                         "(plan upload and L2 flushes outside), per call",
+                     "kernel_us_isolated": iso_ms * 1e3,
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": {"value": replica_value(bytes_step, world, e2e_s / args.steps * 1e3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -493,8 +503,7 @@ def gpu_arm(args, w, rank, world):
         "clocks": clk,
         "host_plan_us": host_plan_us,
     }
-    if seg_detail:
-        res["segments"] = seg_detail
+    res["segments"] = seg_detail
     return res
 
 
@@ -753,6 +762,8 @@ def main():
     ap.add_argument("--workload", default="uniform",
                     choices=["worked", "uniform", "lognormal", "long", "mix", "mla"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--qo-heads", type=int, default=None,
+                    help="override num_qo_heads (a GQA-group variant of the workload)")
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
                     help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
@@ -789,6 +800,10 @@ def main():
     w = W.workload(args.workload)
     if args.layers:
         w.layers = args.layers
+    if args.qo_heads:
+        if args.qo_heads % w.num_kv_heads:
+            ap.error("--qo-heads must be a multiple of the workload's kv heads")
+        w.num_qo_heads = args.qo_heads
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, w)

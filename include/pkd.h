@@ -50,6 +50,10 @@ extern "C" {
 #define PKD_ERR_UNSUPPORTED (-5)         /* valid but not built (head_dim, page_size, dtypes) */
 #define PKD_ERR_DEVICE (-6)              /* a kernel reported an error in the status word */
 
+/* Bits of the device status word (pkd_check_status). */
+#define PKD_STATUS_TIMEOUT 1u  /* a pipeline wait ran out: the kernel gave up, outputs incomplete */
+#define PKD_STATUS_BAD_PAGE 2u /* a page id outside [0, num_pages) was read (as zeros) */
+
 #define PKD_DTYPE_F16 0
 #define PKD_DTYPE_BF16 1
 #define PKD_DTYPE_E4M3 2
@@ -92,7 +96,9 @@ int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, vo
  *     pages; ignored for requests without pages).
  *   indices_dev [num_indices]: device int32 physical page ids, num_indices >= indptr[batch].
  *     The pointer is stored and read by every later pkd_run: keep it valid and unchanged.
- *     Ids outside [0, num_pages) read zeros (the hardware bounds-checks them).
+ *     Ids outside [0, num_pages) read zeros (the hardware bounds-checks them) and set
+ *     PKD_STATUS_BAD_PAGE in the status word; pkd_check_page_table checks a host copy of
+ *     the table up front.
  *   num_qo_heads must be a multiple of num_kv_heads.  head_dim in {64, 128, 256}
  *   (e4m3 KV: {128, 256}).  page_size a power of two in [8, 256].
  *   sm_scale: NaN selects 1/sqrt(head_dim).  logits_soft_cap <= 0: no cap.
@@ -299,12 +305,39 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
 
 /*
  * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no
- * kernel since the last plan or check reported a problem, else a bit set: 1 = a pipeline
- * wait timed out (the kernel gave up and left its outputs incomplete).  When it is nonzero,
- * the split-merge chunk counters in the int workspace are zeroed with it, so later runs of
- * the same plan start clean.
+ * kernel since the last plan or check reported a problem, else PKD_STATUS_* bits:
+ *   PKD_STATUS_TIMEOUT   a pipeline wait ran out (pkd_set_wait_limit): the CTAs that gave up
+ *                        wrote none of their outputs, and every later launch on this handle
+ *                        returns at once, writing nothing, until this call clears the bit;
+ *   PKD_STATUS_BAD_PAGE  a decode launch read a page id outside [0, num_pages) (read as zeros;
+ *                        later launches are not affected).
+ * When it is nonzero, the split-merge chunk counters in the int workspace are zeroed with it,
+ * so later runs of the same plan start clean.
+ * h == NULL reads and clears the status word of pkd_decode_noalloc's built-in scratch on the
+ * current device instead (the status of the last pkd_decode_noalloc call there).
  */
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
+
+/*
+ * Limit of the decode kernel's pipeline waits (a consumer waiting for a tile's copies, the
+ * producer waiting for a free stage) for later pkd_run calls on this handle, in ns; the
+ * default and largest value is 2e9 (2 s).  A wait that runs out sets PKD_STATUS_TIMEOUT and
+ * the CTA gives up (see pkd_check_status).  0 makes every wait test its barrier once and give
+ * up if the tile is not already there; it exists to exercise that failure path.  A CTA that
+ * gives up still waits, with the full 2 s limit, for the copies it has already issued to
+ * land before it exits.  INVALID_ARG above 2e9.
+ */
+int pkd_set_wait_limit(pkd_handle* h, uint64_t limit_ns);
+
+/*
+ * Optional host validation of a page table (no handle, no CUDA call): indptr_host [batch+1]
+ * non-decreasing from indptr[0] >= 0, indptr[batch] <= num_indices, and every page id a
+ * request owns (indices_host[indptr[0] .. indptr[batch])) inside [0, num_pages).  Returns
+ * PKD_OK or PKD_ERR_INVALID_ARG with a message naming the first offending request and id.
+ * The kernels themselves read such ids as zeros and report PKD_STATUS_BAD_PAGE.
+ */
+int pkd_check_page_table(const int32_t* indptr_host, int batch, const int32_t* indices_host,
+                         int64_t num_indices, int64_t num_pages);
 
 /*
  * pkd_decode_noalloc -- plan + run in one call, using only scratch memory built into the
@@ -328,6 +361,11 @@ int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
  * built in static host storage).  The first call on a device does a one-time set-up with that
  * device current: it reads the array's device address (cudaGetSymbolAddress) and raises the
  * kernels' shared-memory limit.  Make that first call before any stream capture.
+ *
+ * Failures on the GPU: the call's kernels report into the status word at the start of the
+ * array, which every call clears first.  pkd_check_status(NULL, &status, stream) reads and
+ * clears it after the call (PKD_STATUS_TIMEOUT: a pipeline wait ran out and o / lse are
+ * incomplete; PKD_STATUS_BAD_PAGE: a page id outside [0, num_pages) was read as zeros).
  *
  * Every call shares the one array and overwrites what the last call left there.  Calls whose
  * GPU work overlaps (on two streams, or from two host threads) race and corrupt each other's

@@ -6,9 +6,10 @@ in ``include/pkd.h``).  Build it with ``paged_kv_decode_23_gb300.build.build()``
 """
 from ._lib import PkdError, LIB_PATH  # noqa: F401
 from .decode import (BatchDecodePagedKV, BatchMLAPagedAttention,  # noqa: F401
-                     CUDAGraphBatchDecodePagedKV, graph_workspace_bytes,
-                     mla_graph_workspace_bytes, mla_plan_host, plan_host, workspace_bytes)
+                     CUDAGraphBatchDecodePagedKV, check_page_table, graph_workspace_bytes,
+                     mla_graph_workspace_bytes, mla_plan_host, noalloc_check_status, plan_host,
+                     workspace_bytes)
 
 __all__ = ["BatchDecodePagedKV", "BatchMLAPagedAttention", "CUDAGraphBatchDecodePagedKV",
-           "PkdError", "graph_workspace_bytes", "mla_graph_workspace_bytes", "mla_plan_host",
-           "plan_host", "workspace_bytes"]
+           "PkdError", "check_page_table", "graph_workspace_bytes", "mla_graph_workspace_bytes",
+           "mla_plan_host", "noalloc_check_status", "plan_host", "workspace_bytes"]

@@ -25,6 +25,7 @@ ERRORS = {
 DTYPE_F16, DTYPE_BF16, DTYPE_E4M3 = 0, 1, 2
 LAYOUT_NHD, LAYOUT_HND = 0, 1
 KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TENSOR_CORE = -1, 0, 1
+STATUS_TIMEOUT, STATUS_BAD_PAGE = 1, 2
 
 # every symbol include/pkd.h declares, with its ctypes signature
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -53,6 +54,8 @@ SIGNATURES = {
                                ctypes.POINTER(_c_int), _c_int, _c_int]),
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkd_set_pdl": (_c_int, [_vp, _c_int]),
+    "pkd_set_wait_limit": (_c_int, [_vp, ctypes.c_uint64]),
+    "pkd_check_page_table": (_c_int, [_i32p, _c_int, _i32p, ctypes.c_int64, ctypes.c_int64]),
     "pkd_mla_set_backend": (_c_int, [_vp, _c_int]),
     "pkd_mla_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _i32p, _c_int, _i32p, _c_int, ctypes.POINTER(_c_int),

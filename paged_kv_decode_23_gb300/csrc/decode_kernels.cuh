@@ -102,12 +102,12 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords
     prefetch_tmap(&p.tmap_v);
   }
   int issued = 0;
-  bool ok = true;
+  bool ok = true, bad_page = false;
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
     // one decision per warp: a lane that gave up takes the whole warp out of the loop
-    if (i >= NSTAGES &&
-        !__all_sync(~0u, mbar_wait(empty0 + 8 * s, ((i / NSTAGES) - 1) & 1, abort_flag))) {
+    if (i >= NSTAGES && !__all_sync(~0u, mbar_wait(empty0 + 8 * s, ((i / NSTAGES) - 1) & 1,
+                                                   abort_flag, p.wait_ns))) {
       ok = false;
       break;
     }
@@ -116,6 +116,7 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords
     const bool need = lane < boxes && bt0 < b.it.tok_end && bt0 + br > b.it.tok_begin;
     int pid = 0;
     if (need) pid = __ldg(p.indices + b.it.page_base + bt0 / ps);
+    bad_page |= need && (uint32_t)pid >= p.num_pages;
     const unsigned m = __ballot_sync(0xffffffffu, need);
     if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, __popc(m) * tx_per_box);
     __syncwarp();
@@ -134,15 +135,20 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords
     }
     issued = i + 1;
   }
+  // A page id outside the pool: reported, and its box read as zeros (the tensor map's bounds).
+  if (__any_sync(~0u, bad_page) && lane == 0) atomicOr(p.status, kStatusBadPage);
   if (!ok) {
     *abort_flag = 1;
-    if (lane == 0) {
-      atomicOr(p.status, kStatusTimeout);
-      // Let the copies already in flight land before the CTA may exit.
-      volatile int never = 0;
-      for (int u = issued - NSTAGES < 0 ? 0 : issued - NSTAGES; u < issued; ++u)
-        mbar_wait(full0 + 8 * (u % NSTAGES), (u / NSTAGES) & 1, &never);
-    }
+    if (lane == 0) atomicOr(p.status, kStatusTimeout);
+  }
+  // The producer warp stays until the copies of the last NSTAGES tiles it issued have landed
+  // (an earlier tile's stage was reused only after its copies landed), so the CTA never exits
+  // with a copy in flight into its shared memory -- also when the consumers gave up after the
+  // last tile was issued.  These waits keep the full limit whatever the launch's wait_ns.
+  if (lane == 0) {
+    volatile int never = 0;
+    for (int u = issued - NSTAGES < 0 ? 0 : issued - NSTAGES; u < issued; ++u)
+      mbar_wait(full0 + 8 * (u % NSTAGES), (u / NSTAGES) & 1, &never);
   }
 }
 
@@ -475,6 +481,7 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   using T = typename std::conditional<KV_FP8, __half, TQ>::type;      // P*V operand type
   using TQK = typename std::conditional<KV_FP8 || ROPE, __half, TQ>::type;  // QK operand type
   using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
+  constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;  // P as bf16 hi + lo
   uint32_t qb[D / 16][2];
   float qmul;
   load_q_frags<TQ, TQK, D, KV_FP8, ROPE>(p, b, lane, qb, qmul);
@@ -508,7 +515,7 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag))) {
+    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
@@ -659,9 +666,20 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
           lsum[j] += sc[j] + sc[j + 2];
         }
       }
-      // ---- P^T as the B operand (k = token, n = qo head): transpose the C fragment
-      const uint32_t b0 = movmatrix_trans(pack2<T>(sc[0], sc[1]));
-      const uint32_t b1 = movmatrix_trans(pack2<T>(sc[2], sc[3]));
+      // ---- P^T as the B operand (k = token, n = qo head): transpose the C fragment.  A
+      // bf16 P keeps only 8 significant bits: its rounding error, 2^-9 of each weight, can
+      // exceed the output tolerance where a few large weights cancel.  So with bf16 V the
+      // weights go in as P_hi + P_lo (the bf16 value and its bf16 rounding remainder, one more
+      // MMA per block), which carries ~16 bits; fp16 P (11 bits) goes in alone.
+      const uint32_t h01 = pack2<T>(sc[0], sc[1]), h23 = pack2<T>(sc[2], sc[3]);
+      const uint32_t b0 = movmatrix_trans(h01);
+      const uint32_t b1 = movmatrix_trans(h23);
+      uint32_t b0_lo = 0u, b1_lo = 0u;
+      if constexpr (kSplitP) {
+        const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
+        b0_lo = movmatrix_trans(pack2<T>(sc[0] - r01.x, sc[1] - r01.y));
+        b1_lo = movmatrix_trans(pack2<T>(sc[2] - r23.x, sc[3] - r23.y));
+      }
       // ---- O^T += V^T * P^T : rows = head_dim (16 per block), cols = 8 qo heads
       if constexpr (KV_FP8) {
         uint32_t va[4], vb[4];  // even / odd q4
@@ -703,6 +721,7 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
           uint32_t a[4];
           ldsm_x4_trans(vtile + swz_off(r0 + row, mb * 2 + csel, TS), a);
           mma_16816<T>(acc[mb], a, b0, b1);
+          if constexpr (kSplitP) mma_16816<T>(acc[mb], a, b0_lo, b1_lo);
         }
       }
     }
@@ -826,7 +845,7 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag))) {
+    if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
@@ -960,11 +979,11 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, G::NW);
     }
-    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
     fence_mbar_init();
   }
   __syncthreads();
-  if (abort_flag_s) return;  // an earlier launch reported a failure: touch nothing
+  if (abort_flag_s) return;  // an earlier launch timed out: touch nothing
 
   if (warp == G::NW) {
     produce<G, TS, NSTAGES>(p, b, smem, full0, empty0, abort_flag, lane);

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) merge_states_kernel(const MergeParams p) 
   const int entry = wid / p.num_qo_heads;
   const int qo = wid - entry * p.num_qo_heads;
   if (entry >= p.num_merges) return;
-  if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) return;
+  if ((*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) != 0u) return;
   const MergeEntry me = p.merges[entry];
   const float neg_inf = -__int_as_float(0x7f800000);
   float M = neg_inf;

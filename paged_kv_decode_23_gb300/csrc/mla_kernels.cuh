@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const MlaPa
       mbar_init(full0 + 8 * s, mla::NPW * 32 + 1);  // the producers' cp.async arrivals + 1
       mbar_init(empty0 + 8 * s, mla::NW);  // one per consumer warp
     }
-    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    abort_flag_s = ((*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) != 0u) ? 1 : 0;
     fence_mbar_init();
   }
   // peers' copies and arrivals reach this CTA's barriers only after their init

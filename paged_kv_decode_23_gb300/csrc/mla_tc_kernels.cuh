@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(mlatc::THREADS, 1) mla_tc_kernel(const MlaPara
     mbar_init(bar(B_XEMPTY + 1), NSOFT / 32);
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_MERGE), 1);
-    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u) ? 1 : 0;
+    abort_flag_s = ((*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) != 0u) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 8) {

@@ -289,6 +289,25 @@ bool na_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+// pkd_check_status(NULL, ...): the status word at the start of this device's built-in array,
+// read after the stream's earlier work and then cleared.  No allocation either.
+int pkd::noalloc_check_status(uint32_t* status, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return na_fail(PKD_ERR_CUDA, "cudaGetDevice failed");
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  int rc = na_setup(dev);
+  if (rc) return rc;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, g_na_scratch[dev], sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && v) e = cudaMemsetAsync(g_na_scratch[dev], 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return na_fail(PKD_ERR_CUDA, "reading the built-in status word failed");
+  *status = v;
+  return PKD_OK;
+}
+
 extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* last_page_len_host,
                                   int batch, const int32_t* indices_dev, int64_t num_indices,
                                   int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
@@ -390,6 +409,8 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
   prm.part_o = reinterpret_cast<float*>(scratch + kNaFloatOff);
   prm.part_lse = reinterpret_cast<float*>(scratch + kNaFloatOff + part_o_bytes);
   prm.status = reinterpret_cast<uint32_t*>(scratch);
+  prm.wait_ns = kWaitLimitNs;
+  prm.num_pages = (uint32_t)num_pages;
   prm.num_qo_heads = num_qo_heads;
   prm.num_kv_heads = num_kv_heads;
   prm.group = num_qo_heads / num_kv_heads;

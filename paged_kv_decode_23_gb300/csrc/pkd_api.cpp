@@ -144,6 +144,7 @@ struct pkd_handle {
   StagingSlot staging[kStagingSlots];
   int staging_next = 0;
   bool pdl = true;  // launch the decode kernel as a programmatic dependent of its predecessor
+  unsigned long long wait_ns = kWaitLimitNs;  // decode pipeline wait limit (pkd_set_wait_limit)
 
   // The workspace layout the current plan was uploaded in (its own counts, or capacities).
   WsLayout ws_layout{};
@@ -634,6 +635,8 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   prm.part_o = reinterpret_cast<float*>(fws);
   prm.part_lse = reinterpret_cast<float*>(fws + part_o_bytes);
   prm.status = reinterpret_cast<uint32_t*>(iws);
+  prm.wait_ns = h->wait_ns;
+  prm.num_pages = (uint32_t)num_pages;
   prm.num_qo_heads = h->num_qo_heads;
   prm.num_kv_heads = h->num_kv_heads;
   prm.group = h->num_qo_heads / h->num_kv_heads;
@@ -990,6 +993,38 @@ int pkd_set_pdl(pkd_handle* h, int enable) {
   return PKD_OK;
 }
 
+int pkd_set_wait_limit(pkd_handle* h, uint64_t limit_ns) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (limit_ns > kWaitLimitNs)
+    return fail(PKD_ERR_INVALID_ARG, "the wait limit must lie in [0, 2e9] ns");
+  h->wait_ns = limit_ns;
+  return PKD_OK;
+}
+
+int pkd_check_page_table(const int32_t* indptr_host, int batch, const int32_t* indices_host,
+                         int64_t num_indices, int64_t num_pages) {
+  if (batch < 0 || (batch > 0 && (!indptr_host || (!indices_host && indptr_host[batch] > 0))))
+    return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0 and the page table pointers non-null");
+  if (batch == 0) return PKD_OK;
+  if (indptr_host[0] < 0) return fail(PKD_ERR_INVALID_ARG, "indptr[0] must be >= 0");
+  for (int i = 0; i < batch; ++i)
+    if (indptr_host[i + 1] < indptr_host[i])
+      return fail(PKD_ERR_INVALID_ARG, "indptr must be non-decreasing");
+  if ((int64_t)indptr_host[batch] > num_indices)
+    return fail(PKD_ERR_INVALID_ARG, "indices holds fewer than indptr[batch] page ids");
+  for (int i = 0; i < batch; ++i)
+    for (int32_t j = indptr_host[i]; j < indptr_host[i + 1]; ++j)
+      if (indices_host[j] < 0 || (int64_t)indices_host[j] >= num_pages) {
+        char buf[200];
+        std::snprintf(buf, sizeof buf,
+                      "request %d: page id %d at indices[%d] lies outside [0, %lld)", i,
+                      (int)indices_host[j], (int)j, (long long)num_pages);
+        return fail(PKD_ERR_INVALID_ARG, buf);
+      }
+  g_last_error.clear();
+  return PKD_OK;
+}
+
 int pkd_enable_cuda_graph(pkd_handle* h, int32_t* indptr_buf, int32_t* indices_buf,
                           int32_t* last_page_len_buf, int max_batch, int64_t max_pages,
                           int max_items) {
@@ -1053,8 +1088,9 @@ int pkd_mla_graph_workspace_bytes(int max_items, int num_heads, int backend,
 }
 
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
-  if (!h || !status) return fail(PKD_ERR_INVALID_ARG, "null handle or status");
+  if (!status) return fail(PKD_ERR_INVALID_ARG, "status is null");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!h) return noalloc_check_status(status, s);  // pkd_decode_noalloc's built-in status word
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyAsync(&v, h->int_ws, sizeof v, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);

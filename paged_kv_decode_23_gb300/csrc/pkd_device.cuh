@@ -6,12 +6,19 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include "pkd_internal.h"
+
 namespace pkd {
 namespace dev {
 
-// A pipeline wait that has not completed after this long gives up (status bit 0).
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// A pipeline wait that has not completed after this long gives up (status bit 0).  The decode
+// kernel's pipeline waits take their limit from the launch (DecodeParams::wait_ns); the waits
+// that let copies in flight land before a CTA exits always keep this one.
+constexpr unsigned long long kWaitTimeoutNs = kWaitLimitNs;
+// Status word bits.  A timeout makes every later launch on the same status word return at
+// once (until the host clears it); a page id outside the pool is reported and read as zeros.
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBadPage = 2u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -54,16 +61,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Whether phase `parity` of `bar` has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when *abort is
-// set by another warp or after kWaitTimeoutNs; every wait in these kernels is bounded.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// set by another warp or after limit_ns; every wait in these kernels is bounded.  A limit of
+// 0 tests the phase once and gives up at once if it has not completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
+  if (limit_ns == 0) return mbar_test(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

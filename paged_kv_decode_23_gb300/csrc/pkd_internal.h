@@ -37,6 +37,13 @@ struct MergeEntry {
 static_assert(sizeof(MergeEntry) == 16, "MergeEntry is 4 int32");
 
 enum DType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+// Default (and largest) limit of a kernel's pipeline waits, in ns of the global timer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Reads and clears the status word of pkd_decode_noalloc's built-in scratch on the current
+// device (noalloc.cu), for pkd_check_status(NULL, ...).
+int noalloc_check_status(uint32_t* status, cudaStream_t stream);
 enum KernelKind { kCudaCore = 0, kTensorCore = 1 };
 
 // Kernel parameters, passed by value as a __grid_constant__ so the tensor maps stay in
@@ -61,6 +68,10 @@ struct DecodeParams {
   // rate rope_theta^(-2i/D) / rope_scale (a float pair) and the rotation across 8 positions,
   // then [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
   const float* pos_table;
+  unsigned long long wait_ns;  // limit of every pipeline wait (0: test once); the wait for
+                               // copies in flight before a CTA exits keeps its own 2 s limit
+  uint32_t num_pages;   // pages in the pool: an id outside [0, num_pages) sets status bit 1
+                        // (the load itself reads zeros: the tensor map bounds-checks it)
   int alibi;            // 1: add pos_table[qo head] * (t - q_pos) to every logit
   int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
   int num_qo_heads;

@@ -256,10 +256,34 @@ class BatchDecodePagedKV:
         return (out, lse) if return_lse else out
 
     def check_status(self, stream=None) -> int:
-        """Read and clear the device status word (synchronises the stream); 0 = no error."""
+        """Read and clear the device status word (synchronises the stream); 0 = no error,
+        else STATUS_TIMEOUT / STATUS_BAD_PAGE bits (include/pkd.h, pkd_check_status)."""
         v = ctypes.c_uint32()
         L.check(L.lib().pkd_check_status(self._h, ctypes.byref(v), _stream_ptr(stream)))
         return v.value
+
+    def set_wait_limit(self, limit_ns: int) -> None:
+        """Limit of the decode kernel's pipeline waits for later runs, in ns (default and
+        maximum 2e9); a wait that runs out sets STATUS_TIMEOUT and its CTA gives up."""
+        L.check(L.lib().pkd_set_wait_limit(self._h, int(limit_ns)))
+
+
+def check_page_table(indptr, indices, num_pages: int) -> None:
+    """Host validation of a page table (pkd_check_page_table): raises PkdError
+    (PKD_ERR_INVALID_ARG) naming the first request whose page id lies outside
+    [0, num_pages).  Device tensors are copied to the host first."""
+    ip = _host_i32(indptr)
+    ix = _host_i32(indices) if len(indices) else np.zeros(1, dtype=np.int32)
+    L.check(L.lib().pkd_check_page_table(_i32p(ip), len(ip) - 1, _i32p(ix), len(indices),
+                                         int(num_pages)))
+
+
+def noalloc_check_status(stream=None) -> int:
+    """Read and clear the status word of pkd_decode_noalloc's built-in scratch on the current
+    device (pkd_check_status with a null handle); 0 = the last call reported nothing."""
+    v = ctypes.c_uint32()
+    L.check(L.lib().pkd_check_status(None, ctypes.byref(v), _stream_ptr(stream)))
+    return v.value
 
 
 def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int,

@@ -37,28 +37,30 @@ def gpu_decoder(w: W.Workload, ws_bytes: int = 256 << 20, **plan_over):
     return dec
 
 
-def run_gpu(w: W.Workload, q: torch.Tensor, pool, dec=None, **plan_over):
-    """o (float64) and lse (float64) from the CUDA path; q / pool may live on either device."""
+def run_gpu(w: W.Workload, q: torch.Tensor, pool, dec=None, q_scale: float = 1.0, **plan_over):
+    """o (float64) and lse (float64) from the CUDA path; q / pool may live on either device.
+    ``q_scale`` is run()'s; k_scale and v_scale come from the workload."""
     dec = dec or gpu_decoder(w, **plan_over)
     dev = torch.device("cuda")
     if isinstance(pool, (tuple, list)):
         kv = tuple(t.to(dev) for t in pool)
     else:
         kv = pool.to(dev)
-    o, lse = dec.run(q.to(dev), kv, k_scale=w.k_scale, v_scale=w.v_scale, return_lse=True)
+    o, lse = dec.run(q.to(dev), kv, q_scale=q_scale, k_scale=w.k_scale, v_scale=w.v_scale,
+                     return_lse=True)
     torch.cuda.synchronize()
     assert dec.check_status() == 0, "device status word reports a failure"
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
 def run_oracle(w: W.Workload, q: torch.Tensor, pool: torch.Tensor, chunk_tokens: int = 0,
-               q_len: int = 1, **pos):
+               q_len: int = 1, q_scale: float = 1.0, **pos):
     """``pos``: pos_encoding_mode / rope_scale / rope_theta, passed to the oracle."""
     return oracle.batch_decode_pool(
         w.indptr, w.indices, w.last_page_len, W.raw_bits(q.cpu()), ORACLE_CODE[w.q_dtype],
         W.raw_bits(pool.cpu()), ORACLE_CODE[w.kv_dtype], w.layout, sm_scale=w.sm_scale,
-        logits_soft_cap=w.logits_soft_cap, window_left=w.window_left, k_scale=w.k_scale,
-        v_scale=w.v_scale, chunk_tokens=chunk_tokens, q_len=q_len, **pos)
+        logits_soft_cap=w.logits_soft_cap, window_left=w.window_left, q_scale=q_scale,
+        k_scale=w.k_scale, v_scale=w.v_scale, chunk_tokens=chunk_tokens, q_len=q_len, **pos)
 
 
 def assert_close(w: W.Workload, got, ref, what=""):
@@ -80,22 +82,20 @@ def assert_close(w: W.Workload, got, ref, what=""):
 
 def sub_problem(w: W.Workload, reqs, q: torch.Tensor, pool: torch.Tensor):
     """The workload restricted to requests `reqs`, with only their pages copied to the host
-    (pages keep their contents; ids are renumbered).  Used to check sampled outputs of
-    full-size runs against the oracle."""
+    (pages keep their contents; ids are renumbered).  Used to check full-size runs, and
+    single requests of a batch, against the oracle."""
     reqs = list(reqs)
     pages = [w.indices[w.indptr[i]:w.indptr[i + 1]] for i in reqs]
-    uniq = np.unique(np.concatenate(pages)) if pages else np.zeros(0, np.int32)
-    remap = {int(p): k for k, p in enumerate(uniq)}
+    flat = np.concatenate(pages) if pages else np.zeros(0, np.int32)
+    uniq = np.unique(flat)
     indptr = np.zeros(len(reqs) + 1, dtype=np.int32)
-    indices = []
-    for k, pg in enumerate(pages):
-        indptr[k + 1] = indptr[k] + len(pg)
-        indices.extend(remap[int(p)] for p in pg)
+    indptr[1:] = np.cumsum([len(pg) for pg in pages])
+    indices = np.searchsorted(uniq, flat).astype(np.int32)  # ids renumbered into sub_pool
     idx_t = torch.from_numpy(uniq.astype(np.int64)).to(pool.device)
     sub_pool = pool.index_select(0, idx_t).cpu()
     sub = W.Workload(w.name + "-sub", len(reqs), w.num_qo_heads, w.num_kv_heads, w.head_dim,
                      w.page_size, w.layout, w.q_dtype, w.kv_dtype, w.o_dtype,
-                     w.kv_lens[reqs], indptr, np.asarray(indices, dtype=np.int32),
+                     w.kv_lens[reqs], indptr, indices,
                      w.last_page_len[reqs], len(uniq), sm_scale=w.sm_scale,
                      logits_soft_cap=w.logits_soft_cap, window_left=w.window_left,
                      kv_store_scale=w.kv_store_scale, k_scale=w.k_scale, v_scale=w.v_scale)

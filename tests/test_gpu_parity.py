@@ -5,8 +5,8 @@ CUDA-core kernels, NHD/HND, 5-D pool and (k, v) pair, fp16/bf16/e4m3, head_dim 6
 GQA groups 1..16, page sizes 8..128, soft cap, window, split modes).  Edge cases: empty
 requests, single tokens, window 0, an empty batch, NaN/Inf in every slot no request owns.
 Properties the pages fix: batch invariance under fixed_split_size, run-to-run determinism.
-Full-size workloads are checked on sampled requests in the same launch configuration the
-benchmark times.
+Full-size workloads are checked on every request in the same launch configuration the
+benchmark times.  run()'s calibration scales are checked on every KV dtype and both kernels.
 """
 import numpy as np
 import pytest
@@ -191,46 +191,62 @@ def test_plan_reused_across_layers():
 
 
 # ----------------------------------------------------------------- full-size workloads
-def _full(name, sample, layers=(0,), tc=None):
+def _full(name, layers=(0,), tc=None):
+    """The named workload at full size, planned and launched as the benchmark does, with
+    every request's output compared against the oracle (the oracle reads only the pages the
+    batch uses, copied to the host)."""
     w = W.workload(name)
     dev = torch.device("cuda")
     dec = gpu_decoder(w, **({} if tc is None else dict(use_tensor_cores=tc)))
+    every = list(range(w.batch))
     for layer in layers:
         q = W.make_q(w, device=dev, layer=layer)
         pool = W.make_pool(w, device=dev, layer=layer)
         got = run_gpu(w, q, pool, dec=dec)
-        sub, qs, ps_ = sub_problem(w, sample, q, pool)
-        ref = run_oracle(sub, qs, ps_)
-        assert_close(sub, (got[0][sample], got[1][sample]), ref, f"{name} layer {layer}")
+        sub, qs, ps_ = sub_problem(w, every, q, pool)
         del pool
         torch.cuda.empty_cache()
-
-
-def _sample(w, k=4, seed=0):
-    lens = np.asarray(w.kv_lens)
-    rng = np.random.default_rng(seed)
-    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
-    pick.update(int(x) for x in rng.choice(len(lens), size=k, replace=False))
-    return sorted(pick)
+        assert_close(sub, got, run_oracle(sub, qs, ps_), f"{name} layer {layer}")
 
 
 def test_full_uniform_bf16_nhd():
-    w = W.workload("uniform")
-    _full("uniform", _sample(w), layers=(0, 31))
+    _full("uniform", layers=(0, 31))
 
 
 def test_full_lognormal_f16_split():
-    w = W.workload("lognormal")
-    _full("lognormal", _sample(w, 3))
+    _full("lognormal")
 
 
 def test_full_long_hnd_fixed_split():
-    _full("long", [0, 3])
+    _full("long")
 
 
 def test_full_mix_e4m3_cap_window():
-    w = W.workload("mix")
-    _full("mix", _sample(w, 6))
+    _full("mix")
+
+
+def test_full_worked_example():
+    _full("worked")
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("kv", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("mode", [dict(fixed_split_size=8), {}])
+@pytest.mark.parametrize("scales", [(0.37, 1.0, 1.0), (3.0, 1.0, 1.0), (1.0, 1.7, 0.6),
+                                    (0.37, 2.5, 1.9), (3.0, 0.45, 2.2)])
+def test_calibration_scales(tc, kv, mode, scales):
+    """run()'s q_scale, k_scale and v_scale (the page's calibration scales) on every KV dtype:
+    q_scale and k_scale multiply the logit ahead of the soft cap, v_scale the output, through
+    split requests merged inside the launch."""
+    q_scale, k_scale, v_scale = scales
+    w, q, pool = _case([1, 40, 700, 2100, 0, 3000], 16, 2, 128, 16, "NHD",
+                       "bf16" if kv == "e4m3" else kv, kv=kv, seed=51, logits_soft_cap=12.0)
+    w.k_scale *= k_scale
+    w.v_scale *= v_scale
+    q = q * 4  # logits of a few units, so the cap bends them and a dropped scale shows
+    got = run_gpu(w, q, pool, q_scale=q_scale, use_tensor_cores=tc, **mode)
+    assert_close(w, got, run_oracle(w, q, pool, q_scale=q_scale),
+                 f"scales {scales} {kv} tc={tc} {mode}")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])

@@ -161,6 +161,28 @@ def test_plan_rejects_bad_input(pkd, bad):
     assert e.value.code in (-1, -5)
 
 
+def test_check_page_table_names_the_first_bad_id(pkd):
+    """The optional host validation of a page table (pkd_check_page_table): ids must lie in
+    [0, num_pages); the message names the request and the position of the first bad id."""
+    from paged_kv_decode_23_gb300 import PkdError
+    ip = np.array([0, 3, 3, 6], dtype=np.int32)
+    ix = np.array([4, 0, 9, 1, 2, 3, 77], dtype=np.int32)  # the tail past indptr[-1] is ignored
+    pkd.check_page_table(ip, ix, 10)
+    pkd.check_page_table(ip, ix[:6], 10)
+    for pos, val, req in ((2, 10, 0), (4, -1, 2), (0, 2 ** 31 - 1, 0)):
+        bad = ix.copy()
+        bad[pos] = val
+        with pytest.raises(PkdError) as e:
+            pkd.check_page_table(ip, bad, 10)
+        assert e.value.code == -1
+        assert f"request {req}" in str(e.value) and f"indices[{pos}]" in str(e.value)
+    with pytest.raises(PkdError):
+        pkd.check_page_table(ip, ix[:5], 10)  # fewer ids than indptr[-1]
+    with pytest.raises(PkdError):
+        pkd.check_page_table(np.array([0, 3, 2, 6], dtype=np.int32), ix, 10)  # decreasing
+    pkd.check_page_table(np.array([0], dtype=np.int32), np.zeros(0, np.int32), 1)  # empty batch
+
+
 def test_workspace_bytes_covers_partials(pkd):
     w = W.workload("long")
     fb, ib = pkd.workspace_bytes(w.indptr, w.last_page_len, 32, 8, 128, 64,
