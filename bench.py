@@ -504,6 +504,7 @@ def gpu_arm(args, w, rank, world):
         "host_plan_us": host_plan_us,
     }
     res["segments"] = seg_detail
+    res["launch"] = dec.plan_info()
     return res
 
 

@@ -284,24 +284,29 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
                         int q_len_per_req, size_t* float_ws_bytes, size_t* int_ws_bytes);
 
 /*
- * The planner alone (host-only; no CUDA call), for inspection and tests.  Writes up to
- * max_items work items of 8 int32 each:
- *   {request, first page index into `indices`, chunk start token, first attended token,
- *    end token, partial slot (-1 = final), merge entry (-1 = none), 0}
- *   (tokens count from the request's start)
- * in launch order, and up to max_merges merge entries of 4 int32 {request, first slot,
- * chunk count, 0}.  n_items / n_merges / n_slots receive the full counts.  kernel_out
- * receives the chosen PKD_KERNEL_* and tile_tokens_out the tokens per pipeline stage.
- * work_capacity > 0 bounds the work list the way CUDA-graph mode does (pkd_enable_cuda_graph's
- * max_items); 0 leaves it unbounded.
+ * The decode planner alone (host-only; no CUDA call), for inspection and tests.  The plan
+ * is a list of tasks for a persistent grid of num_sms x 2 CTAs (num_sms <= 0 means 152): a
+ * task is a chunk of one output row's attended tokens for one kv head and one slice of its
+ * qo-head group (8 qo heads on the tensor-core kernel).  Writes up to max_tasks tasks of 12
+ * int32 each:
+ *   {output row, first page index into `indices`, first token of the chunk's first tile,
+ *    first attended token, end token, partial slot (-1 = final), merge entry (-1 = none),
+ *    query position, kv head, slice, CTA, 0}
+ *   (tokens count from the request's start), grouped by CTA in the order each CTA runs them,
+ * and up to max_merges merge entries of 4 int32 {row, first slot, chunk count, unit} (unit =
+ * kv head x slices + slice).  n_tasks / n_merges / n_slots / n_ctas receive the full counts
+ * (n_ctas: CTAs with at least one task).  kernel_out receives the chosen PKD_KERNEL_* and
+ * tile_tokens_out the tokens per pipeline stage.  work_capacity > 0 bounds the work list the
+ * way CUDA-graph mode does (pkd_enable_cuda_graph's max_items, chunks per row summed over
+ * rows); 0 leaves it unbounded.
  */
 int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
                   int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
-                  int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
-                  int32_t* merges_out, int max_merges, int* n_items, int* n_merges,
+                  int use_tensor_cores, int num_sms, int32_t* tasks_out, int max_tasks,
+                  int32_t* merges_out, int max_merges, int* n_tasks, int* n_merges,
                   int* n_slots, int* kernel_out, int* tile_tokens_out, int work_capacity,
-                  int q_len_per_req);
+                  int q_len_per_req, int* n_ctas);
 
 /*
  * Read and clear the device status word (synchronises `stream`).  *status receives 0 if no
@@ -317,6 +322,15 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
  * current device instead (the status of the last pkd_decode_noalloc call there).
  */
 int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream);
+
+/*
+ * The current decode plan's launch shape: *grid receives the CTAs pkd_run launches (the
+ * persistent grid, or in CUDA-graph mode the fixed one), *ctas_per_sm the CTAs of the plan's
+ * kernel one SM holds, *n_tasks / *n_merges the tasks and split units (any may be NULL).
+ * NOT_PLANNED without a decode plan.
+ */
+int pkd_plan_info(pkd_handle* h, int* grid, int* ctas_per_sm, int64_t* n_tasks,
+                  int64_t* n_merges);
 
 /*
  * Limit of the decode kernel's pipeline waits (a consumer waiting for a tile's copies, the
@@ -380,7 +394,7 @@ int pkd_check_page_table(const int32_t* indptr_host, int batch, const int32_t* i
 #define PKD_NOALLOC_SCRATCH_BYTES (16u << 20)
 #define PKD_NOALLOC_MAX_ITEMS 24576
 #define PKD_NOALLOC_MAX_MERGES 16384
-#define PKD_NOALLOC_PARTIAL_BYTES ((16u << 20) - (1u << 20) - 512u)
+#define PKD_NOALLOC_PARTIAL_BYTES ((16u << 20) - (2u << 20))
 int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
                        const int32_t* indices_dev, int64_t num_indices, int num_qo_heads,
                        int num_kv_heads, int head_dim, int page_size, float sm_scale,

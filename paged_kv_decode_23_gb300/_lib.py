@@ -51,10 +51,12 @@ SIGNATURES = {
                                _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _c_int, _i32p,
                                _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
-                               ctypes.POINTER(_c_int), _c_int, _c_int]),
+                               ctypes.POINTER(_c_int), _c_int, _c_int, ctypes.POINTER(_c_int)]),
     "pkd_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkd_set_pdl": (_c_int, [_vp, _c_int]),
     "pkd_set_wait_limit": (_c_int, [_vp, ctypes.c_uint64]),
+    "pkd_plan_info": (_c_int, [_vp, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
+                               ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "pkd_check_page_table": (_c_int, [_i32p, _c_int, _i32p, ctypes.c_int64, ctypes.c_int64]),
     "pkd_mla_set_backend": (_c_int, [_vp, _c_int]),
     "pkd_mla_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,

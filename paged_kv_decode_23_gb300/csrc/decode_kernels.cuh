@@ -1,9 +1,11 @@
 // decode_kernels.cuh -- batch decode attention over a paged KV cache, sm_103a.
 //
 // What one CTA computes (FlashInfer attention API page, BatchDecodeWithPagedKVCacheWrapper,
-// plan()/run()): for one work item (a chunk of one request's KV tokens) and one kv head, the
-// attention of the group's qo heads (GQA: qo head g reads kv head g / group) over the
-// chunk's attended tokens: s_t = soft_cap(sm_scale * <q, k_t>), online softmax, o = sum p_t v_t.
+// plan()/run()): one task -- a chunk of one output row's KV tokens for one kv head and one
+// slice of its qo-head group -- that is, the attention of the slice's qo heads (GQA: qo head g
+// reads kv head g / group) over the chunk's attended tokens: s_t = soft_cap(sm_scale * <q, k_t>),
+// online softmax, o = sum p_t v_t.  Tasks are launched longest first; the hardware hands each
+// free CTA slot the next one.
 //
 // Structure (one CTA = NW consumer warps + 1 producer warp):
 //   producer  streams the chunk tile by tile (TS tokens per tile) with 4-D TMA tensor loads:
@@ -17,8 +19,9 @@
 //             movmatrix, O^T += V_tile^T * P^T (ldmatrix.trans).  CUDA-core variant: lanes
 //             own head_dim slices, dot products are finished with a 31-shuffle
 //             reduce-scatter over 32 (token, head) pairs, P*V with fp32 FMAs.
-//   epilogue  merges the warps' states in shared memory and writes either the final o / lse
-//             or an fp32 partial (normalised o, base-2 lse) for merge_states.
+//   epilogue  merges the warps' states in shared memory (the idle pipeline stages) and writes
+//             either the final o / lse or an fp32 partial (normalised o, base-2 lse); the CTA
+//             that finishes a split unit's last chunk merges the unit's partials.
 // Slots past a request's last token and pages outside the chunk are loaded or left stale;
 // their logits are replaced by -inf (a select, so NaN/Inf garbage cannot leak) and their V
 // rows are zeroed or skipped before P*V.
@@ -47,35 +50,33 @@ struct DecodeGeom {
   static constexpr int BOX_ELEMS = 128 / KV_ELT;
   static constexpr int TILE_BYTES = TS * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int EPI_BYTES = NW * (8 * D + 16) * 4;
+  // the epilogue's image of every warp's state, in the stages once they are idle
+  static constexpr int EPI_BYTES = NW * (kSlotHeads * D + 2 * kSlotHeads) * 4;
   static constexpr int PIPE_BYTES = NSTAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = (PIPE_BYTES > EPI_BYTES ? PIPE_BYTES : EPI_BYTES) + 1024;
+  static constexpr int SMEM_BYTES = PIPE_BYTES + 1024;
   static_assert(ROW_BYTES % 128 == 0, "K/V rows must be whole 128-byte blocks");
   static_assert(TS % 16 == 0 && NW >= 1 && NW <= 8, "tile of 16-token warp slices");
+  static_assert(EPI_BYTES <= PIPE_BYTES, "the epilogue's image fits in the pipeline stages");
 };
 
 struct BlockCoords {
-  WorkItem it;
+  DecodeTask it;
   int kvh;    // kv head
-  int g0;     // first qo head of this CTA
-  int gcnt;   // qo heads of this CTA
+  int g0;     // first qo head of this task
+  int gcnt;   // qo heads of this task
   int gs;     // which slice of the kv head's qo-head group
   int j0;     // first tile (relative to the chunk start)
   int ntiles;
 };
 
 template <int TS, int HEADS>
-__device__ __forceinline__ BlockCoords block_coords(const DecodeParams& p) {
+__device__ __forceinline__ BlockCoords task_coords(const DecodeParams& p) {
   BlockCoords b;
-  const int per_item = p.num_kv_heads * p.gslices;
-  const int item = blockIdx.x / per_item;
-  const int rem = blockIdx.x - item * per_item;
-  b.kvh = rem / p.gslices;
-  const int gs = rem - b.kvh * p.gslices;
-  b.gs = gs;
-  b.it = p.items[item];
-  b.g0 = b.kvh * p.group + gs * HEADS;
-  b.gcnt = min(HEADS, p.group - gs * HEADS);
+  b.it = p.tasks[blockIdx.x];
+  b.kvh = b.it.kvh;
+  b.gs = b.it.gs;
+  b.g0 = b.kvh * p.group + b.gs * HEADS;
+  b.gcnt = min(HEADS, p.group - b.gs * HEADS);
   if (b.it.tok_end > b.it.tok_begin) {
     b.j0 = (b.it.tok_begin - b.it.chunk_tok0) / TS;
     b.ntiles = (b.it.tok_end - b.it.chunk_tok0 + TS - 1) / TS - b.j0;
@@ -153,8 +154,9 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const BlockCoords
 }
 
 // ------------------------------------------------------------------------------ epilogue
-// Shared-memory image of the consumer warps' states: acc[w][g][d] (unnormalised, relative
-// to m[w][g]), m[w][g] (base-2 running max), l[w][g] (sum of exp2(s - m)).
+// Shared-memory image of the consumer warps' states, in the idle pipeline stages: acc[w][g][d]
+// (unnormalised, relative to m[w][g]), m[w][g] (base-2 running max), l[w][g] (sum of
+// exp2(s - m)).
 template <int D>
 struct EpiView {
   float* acc;
@@ -162,14 +164,15 @@ struct EpiView {
   float* l;
   __device__ __forceinline__ EpiView(uint8_t* base, int nw) {
     acc = reinterpret_cast<float*>(base);
-    m = acc + nw * 8 * D;
-    l = m + nw * 8;
+    m = acc + nw * kSlotHeads * D;
+    l = m + nw * kSlotHeads;
   }
 };
 
+// Combines every warp's state and writes the task's final o / lse, or its fp32 partial.
 template <typename TQ, int D, int NW>
-__device__ __forceinline__ void combine_and_store(const DecodeParams& p, const BlockCoords& b,
-                                                  const EpiView<D>& e, int tid, bool aborted) {
+__device__ __forceinline__ void store_task(const DecodeParams& p, const BlockCoords& b,
+                                           const EpiView<D>& e, int tid) {
   using namespace dev;
   constexpr int NCONS = NW * 32;
   constexpr int D8 = D / 8;
@@ -178,7 +181,7 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const B
     const int d0 = (u - g * D8) * 8;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, e.m[w * 8 + g]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, e.m[w * kSlotHeads + g]);
     float o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) o[k] = 0.f;
@@ -186,9 +189,9 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const B
     if (M != kNegInf) {
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float f = fast_exp2(e.m[w * 8 + g] - M);
-        L += f * e.l[w * 8 + g];
-        const float4* a = reinterpret_cast<const float4*>(e.acc + (w * 8 + g) * D + d0);
+        const float f = fast_exp2(e.m[w * kSlotHeads + g] - M);
+        L += f * e.l[w * kSlotHeads + g];
+        const float4* a = reinterpret_cast<const float4*>(e.acc + (w * kSlotHeads + g) * D + d0);
         const float4 a0 = a[0], a1 = a[1];
         o[0] += f * a0.x; o[1] += f * a0.y; o[2] += f * a0.z; o[3] += f * a0.w;
         o[4] += f * a1.x; o[5] += f * a1.y; o[6] += f * a1.z; o[7] += f * a1.w;
@@ -197,7 +200,6 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const B
     const float inv = L > 0.f ? p.v_scale / L : 0.f;
     const float lse2 = L > 0.f ? M + log2f(L) : kNegInf;
     const int qo = b.g0 + g;
-    if (aborted) continue;
     if (b.it.out_slot < 0) {
       uint4 v;
       v.x = pack2<TQ>(o[0] * inv, o[1] * inv);
@@ -208,48 +210,45 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const B
       *reinterpret_cast<uint4*>(dst) = v;
       if (d0 == 0 && p.lse) p.lse[(size_t)b.it.req * p.num_qo_heads + qo] = lse2 * kLn2;
     } else {
-      float* dst = p.part_o + ((size_t)b.it.out_slot * p.num_qo_heads + qo) * D + d0;
+      float* dst = p.part_o + ((size_t)b.it.out_slot * kSlotHeads + g) * D + d0;
       reinterpret_cast<float4*>(dst)[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
       reinterpret_cast<float4*>(dst)[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
-      if (d0 == 0) p.part_lse[(size_t)b.it.out_slot * p.num_qo_heads + qo] = lse2;
+      if (d0 == 0) p.part_lse[(size_t)b.it.out_slot * kSlotHeads + g] = lse2;
     }
   }
 }
 
-// merge_states fused into the decode kernel: the CTA that finishes a split request's last
-// chunk (for its kv head and head slice) combines all chunks' partials, in chunk order, with
-// the arithmetic of merge_states_kernel.  Writers publish their partial with a fence before
-// counting; the last CTA fences again, reads the partials from L2 and resets the counter for
-// the next run of the plan.  No CTA waits for another.
-template <typename TQ, int D, int NW>
-__device__ __forceinline__ void fused_merge_tail(const DecodeParams& p, const BlockCoords& b,
-                                                 int tid, bool aborted, volatile int* last_flag) {
+// merge_states, fused: the CTA that finishes the last chunk of a split (row, kv head, slice)
+// unit combines all its chunks' partials, in chunk order: M = max lse_c, w_c = 2^(lse_c - M),
+// o = sum w_c o_c / sum w_c, lse = M + log2 sum w_c.  Writers publish their partial with a
+// fence before counting; the last one fences again, reads the partials from L2 and resets the
+// counter for the next run of the plan.  No CTA waits for another.
+template <typename TQ, int D, int NCONS>
+__device__ __forceinline__ void merge_unit(const DecodeParams& p, const BlockCoords& b, int tid,
+                                           volatile int* last_flag) {
   using namespace dev;
-  constexpr int NCONS = NW * 32;
   constexpr int D8 = D / 8;
-  if (!p.fuse_merge || b.it.out_slot < 0) return;  // uniform over the CTA
-  __threadfence();
+  // the CTA's partial stores are ordered before thread 0's fence by the barrier; one fence
+  // then publishes them all before the count
   named_bar_sync(1, NCONS);
   if (tid == 0) {
-    int last = 0;
-    if (!aborted) {
-      uint32_t* ctr = p.counters +
-                      ((size_t)b.it.merge_idx * p.num_kv_heads + b.kvh) * p.gslices + b.gs;
-      const uint32_t prev = atomicAdd(ctr, 1u);
-      last = (prev + 1u == (uint32_t)p.merges[b.it.merge_idx].n_chunks) ? 1 : 0;
-      if (last) *ctr = 0u;
+    __threadfence();
+    uint32_t* ctr = p.counters + b.it.merge_idx;
+    const uint32_t prev = atomicAdd(ctr, 1u);
+    const int last = (prev + 1u == (uint32_t)p.merges[b.it.merge_idx].n_chunks) ? 1 : 0;
+    if (last) {
+      *ctr = 0u;
+      __threadfence();  // the other chunks' partials are visible to this CTA's reads below
     }
     *last_flag = last;
   }
   named_bar_sync(1, NCONS);
   if (!*last_flag) return;
-  __threadfence();
   const MergeEntry me = p.merges[b.it.merge_idx];
   const int hq = p.num_qo_heads;
   for (int u = tid; u < b.gcnt * D8; u += NCONS) {
     const int g = u / D8;
     const int d0 = (u - g * D8) * 8;
-    const int qo = b.g0 + g;
     // Loads go four chunks at a time, independent of each other, so a merge costs about two
     // L2 round trips; the sums still run in chunk order.
     constexpr int U = 4;
@@ -259,7 +258,7 @@ __device__ __forceinline__ void fused_merge_tail(const DecodeParams& p, const Bl
 #pragma unroll
       for (int j = 0; j < U; ++j)
         l[j] = c0 + j < me.n_chunks
-                   ? __ldcg(p.part_lse + (size_t)(me.first_slot + c0 + j) * hq + qo)
+                   ? __ldcg(p.part_lse + (size_t)(me.first_slot + c0 + j) * kSlotHeads + g)
                    : kNegInf;
 #pragma unroll
       for (int j = 0; j < U; ++j) M = fmaxf(M, l[j]);
@@ -275,7 +274,7 @@ __device__ __forceinline__ void fused_merge_tail(const DecodeParams& p, const Bl
 #pragma unroll
         for (int j = 0; j < U; ++j) {
           const bool in = c0 + j < me.n_chunks;
-          const size_t row = (size_t)(me.first_slot + (in ? c0 + j : 0)) * hq + qo;
+          const size_t row = (size_t)(me.first_slot + (in ? c0 + j : 0)) * kSlotHeads + g;
           const float4* src = reinterpret_cast<const float4*>(p.part_o + row * D + d0);
           l[j] = in ? __ldcg(p.part_lse + row) : kNegInf;
           a[j][0] = __ldcg(src);
@@ -299,6 +298,7 @@ __device__ __forceinline__ void fused_merge_tail(const DecodeParams& p, const Bl
     v.y = pack2<TQ>(o[2] * inv, o[3] * inv);
     v.z = pack2<TQ>(o[4] * inv, o[5] * inv);
     v.w = pack2<TQ>(o[6] * inv, o[7] * inv);
+    const int qo = b.g0 + g;
     TQ* dst = reinterpret_cast<TQ*>(p.o) + ((size_t)me.req * hq + qo) * D + d0;
     *reinterpret_cast<uint4*>(dst) = v;
     if (d0 == 0 && p.lse)
@@ -731,9 +731,13 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   }
 }
 
+// A tensor-core warp's state into its own slot of the epilogue image.  Lane (row r = lane / 4,
+// tig = lane % 4) holds columns 2 tig, 2 tig + 1 (qo heads) of every O^T block; m2 is the same
+// on the 8 lanes of a column, lsum their partial sums.
 template <int D, bool KV_FP8>
-__device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane, float (&m2)[2],
-                                         float (&lsum)[2], float (&acc)[D / 16][4]) {
+__device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane,
+                                             float (&m2)[2], float (&lsum)[2],
+                                             float (&acc)[D / 16][4]) {
   const int gr = lane >> 2, tig = lane & 3;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -742,11 +746,11 @@ __device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane
     l += __shfl_xor_sync(~0u, l, 8);
     l += __shfl_xor_sync(~0u, l, 16);
     if (gr == 0) {
-      e.m[warp * 8 + tig * 2 + j] = m2[j];
-      e.l[warp * 8 + tig * 2 + j] = l;
+      e.m[warp * kSlotHeads + tig * 2 + j] = m2[j];
+      e.l[warp * kSlotHeads + tig * 2 + j] = l;
     }
   }
-  float* a = e.acc + warp * 8 * D;
+  float* a = e.acc + warp * kSlotHeads * D;
 #pragma unroll
   for (int mb = 0; mb < D / 16; ++mb) {
     const int da = acc_dim<KV_FP8>(mb, gr), db = acc_dim<KV_FP8>(mb, gr + 8);
@@ -921,18 +925,21 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
   }
 }
 
+// A CUDA-core warp's state into its own slot of the epilogue image.  Lane owns dims
+// [lane * EPL, lane * EPL + EPL) of every head; head g's m2 / lsum live on the lanes with
+// lane % GP == g (lane g holds the reduced values after the shuffles below).
 template <int D, int GP>
-__device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane, float m2, float lsum,
-                                         float (&acc)[GP][D / 32]) {
+__device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane, float m2,
+                                             float lsum, float (&acc)[GP][D / 32]) {
   constexpr int EPL = D / 32;
   float l = lsum;
 #pragma unroll
   for (int off = GP; off < 32; off <<= 1) l += __shfl_xor_sync(~0u, l, off);
   if (lane < GP) {
-    e.m[warp * 8 + lane] = m2;
-    e.l[warp * 8 + lane] = l;
+    e.m[warp * kSlotHeads + lane] = m2;
+    e.l[warp * kSlotHeads + lane] = l;
   }
-  float* a = e.acc + warp * 8 * D;
+  float* a = e.acc + warp * kSlotHeads * D;
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
@@ -940,8 +947,8 @@ __device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane
 }
 
 // ------------------------------------------------------------------------------ kernel
-// KIND: kTensorCore (HEADS = 8 qo heads per CTA) or kCudaCore (HEADS = GP).  ROPE: the
-// tensor-core kernel with ROPE_LLAMA applied to q and K.
+// KIND: kTensorCore (HEADS = 8 qo heads per task) or kCudaCore (HEADS = GP).  ROPE: the
+// tensor-core kernel with ROPE_LLAMA applied to q and K.  CTA blockIdx.x runs task blockIdx.x.
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP, bool ROPE = false>
 __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREADS,
                                   KIND == kTensorCore ? 2 : 1)
@@ -968,11 +975,9 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // CUDA-graph mode: the grid is cut for a fixed work-list capacity; CTAs past this plan's
-  // items have nothing to do (the whole CTA leaves before touching shared memory).
-  if (p.item_count != nullptr &&
-      (int)(blockIdx.x / (p.num_kv_heads * p.gslices)) >= *p.item_count)
-    return;
-  const BlockCoords b = block_coords<TS, HEADS>(p);
+  // tasks have nothing to do (the whole CTA leaves before touching shared memory).
+  if (p.task_count != nullptr && (int)blockIdx.x >= *p.task_count) return;
+  const BlockCoords b = task_coords<TS, HEADS>(p);
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < NSTAGES; ++s) {
@@ -997,7 +1002,8 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
     for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
     consume_tc<TQ, KV_FP8, D, TS, NSTAGES, ROPE>(p, b, smem, full0, empty0, abort_flag, warp,
                                                  lane, m2, lsum, acc);
-    named_bar_sync(1, G::NCONS);  // every consumer is done with the stages
+    // every consumer is done with the stages; one shared decision whether any wait gave up
+    if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
     stash_tc<D, KV_FP8>(epi, warp, lane, m2, lsum, acc);
   } else {
     float m2 = kNegInf, lsum = 0.f;
@@ -1008,13 +1014,12 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
       for (int k = 0; k < D / 32; ++k) acc[g][k] = 0.f;
     consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP>(p, b, smem, full0, empty0, abort_flag, warp, lane,
                                                m2, lsum, acc);
-    named_bar_sync(1, G::NCONS);
+    if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
     stash_cc<D, GP>(epi, warp, lane, m2, lsum, acc);
   }
   named_bar_sync(1, G::NCONS);
-  const bool aborted = *abort_flag != 0;
-  combine_and_store<TQ, D, G::NW>(p, b, epi, threadIdx.x, aborted);
-  fused_merge_tail<TQ, D, G::NW>(p, b, threadIdx.x, aborted, &merge_last_s);
+  store_task<TQ, D, G::NW>(p, b, epi, threadIdx.x);
+  if (b.it.out_slot >= 0) merge_unit<TQ, D, G::NCONS>(p, b, threadIdx.x, &merge_last_s);
 }
 
 // ------------------------------------------------------------------------------ registry
@@ -1030,6 +1035,7 @@ DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   k.fn = reinterpret_cast<const void*>(
       &decode_paged_kernel<TQ, KV_FP8, D, TS, NSTAGES, KIND, GP, ROPE>);
   k.rope = ROPE ? 1 : 0;
+  k.nstages = NSTAGES;
   k.threads = G::THREADS;
   k.smem_bytes = G::SMEM_BYTES;
   k.tile_tokens = TS;

@@ -2,10 +2,11 @@
 //
 // For callers that may not allocate device memory and have no workspace to lend (a runtime
 // that owns every allocation through its own pool or budget).  The scratch they would have
-// passed -- status word, work list, split partials -- lives in one file-scope device array.
-// The plan is built in static host storage, so a call allocates nothing.  The kernels are the
-// tensor-core decode and merge_states kernels of the rest of the library, instantiated here
-// with the same parameters.
+// passed -- status word, merge counters, tasks, merge entries, split partials --
+// lives in one file-scope device array.  The plan is built by the library's decode planner
+// into static host storage, so a call allocates nothing.  The kernel is the tensor-core decode
+// kernel of the rest of the library (split units are merged inside it), instantiated here with
+// the same parameters.
 //
 // The array is shared by every call in the process: calls whose GPU work overlaps race.
 #include "../../include/pkd.h"
@@ -20,7 +21,6 @@
 #include <mutex>
 
 #include "decode_kernels.cuh"
-#include "merge_kernel.cuh"
 
 namespace pkd {
 void set_error_message(const char* msg);  // pkd_api.cpp: what pkd_last_error() returns
@@ -33,13 +33,14 @@ static __device__ __align__(256) unsigned char pkd_noalloc_scratch[PKD_NOALLOC_S
 
 namespace {
 
-constexpr size_t kNaItemsOff = kStatusBytes;                           // work list
-constexpr size_t kNaMergesOff = kNaItemsOff + PKD_NOALLOC_MAX_ITEMS * sizeof(WorkItem);
-constexpr size_t kNaFloatOff = (1u << 20) + 512u;                      // split partials
+// The array: [status block | counters | tasks | merge entries | partials].
+constexpr size_t kNaCountersOff = kStatusBytes;
+constexpr size_t kNaTasksOff = kNaCountersOff + (PKD_NOALLOC_MAX_MERGES * 4 + 255) / 256 * 256;
+constexpr size_t kNaMergesOff = kNaTasksOff + PKD_NOALLOC_MAX_ITEMS * sizeof(DecodeTask);
+constexpr size_t kNaFloatOff = PKD_NOALLOC_SCRATCH_BYTES - PKD_NOALLOC_PARTIAL_BYTES;
 static_assert(kNaMergesOff + PKD_NOALLOC_MAX_MERGES * sizeof(MergeEntry) <= kNaFloatOff,
               "work list region overlaps the partials");
-static_assert(kNaFloatOff + PKD_NOALLOC_PARTIAL_BYTES == PKD_NOALLOC_SCRATCH_BYTES,
-              "partials region ends at the end of the array");
+static_assert(kNaFloatOff % 256 == 0, "partials region is 256-byte aligned");
 
 struct NaDecode {
   int q_dtype, kv_dtype, head_dim;
@@ -67,19 +68,7 @@ const NaDecode kNaDecode[] = {
     PKD_NA_DEC(__nv_bfloat16, true, 256, 64, 3, kBF16, kE4M3),
 };
 #undef PKD_NA_DEC
-
-struct NaMerge {
-  int o_dtype, head_dim;
-  const void* fn;
-};
-const NaMerge kNaMerge[] = {
-    {kF16, 64, reinterpret_cast<const void*>(&merge_states_kernel<__half, 64>)},
-    {kF16, 128, reinterpret_cast<const void*>(&merge_states_kernel<__half, 128>)},
-    {kF16, 256, reinterpret_cast<const void*>(&merge_states_kernel<__half, 256>)},
-    {kBF16, 64, reinterpret_cast<const void*>(&merge_states_kernel<__nv_bfloat16, 64>)},
-    {kBF16, 128, reinterpret_cast<const void*>(&merge_states_kernel<__nv_bfloat16, 128>)},
-    {kBF16, 256, reinterpret_cast<const void*>(&merge_states_kernel<__nv_bfloat16, 256>)},
-};
+constexpr int kNaKernels = sizeof(kNaDecode) / sizeof(kNaDecode[0]);
 
 // ---------------------------------------------------------------- per-device set-up
 constexpr int kMaxDevices = 64;
@@ -87,6 +76,7 @@ std::mutex g_na_mutex;  // guards the set-up table and the static host plan belo
 bool g_na_ready[kMaxDevices];
 unsigned char* g_na_scratch[kMaxDevices];
 int g_na_sms[kMaxDevices];
+int g_na_per_sm[kMaxDevices][kNaKernels];  // resident CTAs per SM of each kernel
 
 int na_fail(int code, const char* msg) {
   set_error_message(msg);
@@ -102,149 +92,26 @@ int na_setup(int dev) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return na_fail(PKD_ERR_CUDA, "cudaDeviceGetAttribute(multiProcessorCount) failed");
-  for (const NaDecode& k : kNaDecode)
+  for (int i = 0; i < kNaKernels; ++i) {
+    const NaDecode& k = kNaDecode[i];
     if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
         cudaSuccess)
       return na_fail(PKD_ERR_CUDA, "cudaFuncSetAttribute on a decode kernel failed");
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.fn, k.threads, (size_t)k.smem) !=
+        cudaSuccess)
+      return na_fail(PKD_ERR_CUDA, "cudaOccupancyMaxActiveBlocksPerMultiprocessor failed");
+    g_na_per_sm[dev][i] = std::max(1, std::min(n, kDecodeCtasPerSm));
+  }
   g_na_scratch[dev] = static_cast<unsigned char*>(ptr);
   g_na_sms[dev] = sms;
   g_na_ready[dev] = true;
   return PKD_OK;
 }
 
-// ---------------------------------------------------------------- planning into static storage
-WorkItem g_na_items[PKD_NOALLOC_MAX_ITEMS];
+// ---------------------------------------------------------------- static host plan storage
+DecodeTask g_na_tasks[PKD_NOALLOC_MAX_ITEMS];
 MergeEntry g_na_merges[PKD_NOALLOC_MAX_MERGES];
-
-struct NaCounts {
-  int64_t items = 0, merges = 0, slots = 0;
-};
-
-inline int64_t na_len(const int32_t* indptr, const int32_t* lpl, int i, int ps) {
-  const int64_t pages = (int64_t)indptr[i + 1] - indptr[i];
-  return pages <= 0 ? 0 : (int64_t)ps * (pages - 1) + lpl[i];
-}
-
-inline int64_t na_start(int64_t n, int window_left) {
-  return (window_left >= 0 && n - 1 - window_left > 0) ? n - 1 - window_left : 0;
-}
-
-NaCounts na_count(const int32_t* indptr, const int32_t* lpl, int batch, int ps, int wl, int64_t C) {
-  NaCounts c;
-  for (int i = 0; i < batch; ++i) {
-    const int64_t n = na_len(indptr, lpl, i, ps);
-    const int64_t nch = (n == 0 || C == 0) ? 1 : (n - 1) / C - na_start(n, wl) / C + 1;
-    c.items += nch;
-    if (nch > 1) {
-      c.merges += 1;
-      c.slots += nch;
-    }
-  }
-  return c;
-}
-
-size_t na_partial_bytes(int64_t slots, int hq, int d) {
-  const size_t o = (size_t)slots * hq * d * sizeof(float);
-  const size_t l = (size_t)slots * hq * sizeof(float);
-  return (o + 255) / 256 * 256 + (l + 255) / 256 * 256;
-}
-
-bool na_fits(const NaCounts& c, int hq, int d) {
-  return c.items <= PKD_NOALLOC_MAX_ITEMS && c.merges <= PKD_NOALLOC_MAX_MERGES &&
-         na_partial_bytes(c.slots, hq, d) <= PKD_NOALLOC_PARTIAL_BYTES;
-}
-
-// The same rules as the handle-based planner: chunks of C tokens counted from each request's
-// token 0 (C = 0: one chunk), chunks the window leaves empty dropped, longest chunks first.
-// The heuristic C grows until the plan fits the built-in scratch.
-int na_plan(const int32_t* indptr, const int32_t* lpl, int batch, int hq, int hkv, int d, int ps,
-            int wl, int fixed, int disable, int sms, NaCounts* out) {
-  int64_t total = 0, longest = 0;
-  for (int i = 0; i < batch; ++i) {
-    if (indptr[i + 1] < indptr[i]) return na_fail(PKD_ERR_INVALID_ARG, "indptr must be non-decreasing");
-    const int64_t pages = (int64_t)indptr[i + 1] - indptr[i];
-    if (pages > 0 && (lpl[i] < 1 || lpl[i] > ps))
-      return na_fail(PKD_ERR_INVALID_ARG,
-                     "last_page_len must lie in [1, page_size] for every request with pages");
-    const int64_t n = na_len(indptr, lpl, i, ps);
-    if (n > (int64_t)std::numeric_limits<int32_t>::max() - 4096)
-      return na_fail(PKD_ERR_INVALID_ARG, "a request is longer than 2^31 - 4096 tokens");
-    total += n - na_start(n, wl);
-    longest = std::max(longest, n - na_start(n, wl));
-  }
-  int64_t C = 0;
-  const bool heuristic = !disable && fixed <= 0;
-  if (disable) {
-    C = 0;
-  } else if (fixed > 0) {
-    C = (int64_t)fixed * ps;
-  } else {
-    const int64_t slots = (int64_t)(sms > 0 ? sms : 152) * 2 * 2;
-    const int64_t per_cta = (total * hkv + slots - 1) / slots;  // one head slice per CTA (G <= 8)
-    int64_t c = std::max<int64_t>(256, per_cta);
-    c = (c + ps - 1) / ps * ps;
-    C = longest > c ? c : 0;
-  }
-  NaCounts cnt = na_count(indptr, lpl, batch, ps, wl, C);
-  while (heuristic && C > 0 && !na_fits(cnt, hq, d)) {
-    C = C * 2 >= longest ? 0 : C * 2;
-    cnt = na_count(indptr, lpl, batch, ps, wl, C);
-  }
-  if (cnt.items > PKD_NOALLOC_MAX_ITEMS)
-    return na_fail(PKD_ERR_WORKSPACE_TOO_SMALL,
-                   "plan needs more chunks than the built-in scratch holds (PKD_NOALLOC_MAX_ITEMS)");
-  if (cnt.merges > PKD_NOALLOC_MAX_MERGES)
-    return na_fail(PKD_ERR_WORKSPACE_TOO_SMALL,
-                   "plan splits more requests than the built-in scratch holds (PKD_NOALLOC_MAX_MERGES)");
-  if (na_partial_bytes(cnt.slots, hq, d) > PKD_NOALLOC_PARTIAL_BYTES)
-    return na_fail(PKD_ERR_WORKSPACE_TOO_SMALL,
-                   "split partials exceed the built-in scratch (PKD_NOALLOC_PARTIAL_BYTES); use a "
-                   "larger fixed_split_size or disable_split_kv");
-  int ni = 0, nm = 0, slot = 0;
-  for (int i = 0; i < batch; ++i) {
-    WorkItem it;
-    std::memset(&it, 0, sizeof it);
-    it.req = i;
-    it.page_base = indptr[i];
-    const int64_t n = na_len(indptr, lpl, i, ps);
-    if (n == 0) {
-      it.out_slot = -1;
-      g_na_items[ni++] = it;
-      continue;
-    }
-    const int64_t w = na_start(n, wl);
-    const int64_t k0 = C > 0 ? w / C : 0, k1 = C > 0 ? (n - 1) / C : 0;
-    const int64_t nch = k1 - k0 + 1;
-    const int first = slot;
-    for (int64_t k = k0; k <= k1; ++k) {
-      const int64_t c0 = C > 0 ? k * C : 0;
-      const int64_t c1 = C > 0 ? std::min(n, (k + 1) * C) : n;
-      it.chunk_tok0 = (int32_t)c0;
-      it.tok_begin = (int32_t)std::max(c0, w);
-      it.tok_end = (int32_t)c1;
-      it.out_slot = nch > 1 ? slot++ : -1;
-      g_na_items[ni++] = it;
-    }
-    if (nch > 1) {
-      MergeEntry me;
-      me.req = i;
-      me.first_slot = first;
-      me.n_chunks = (int32_t)nch;
-      me.pad = 0;
-      g_na_merges[nm++] = me;
-    }
-  }
-  std::sort(g_na_items, g_na_items + ni, [](const WorkItem& a, const WorkItem& b) {
-    const int la = a.tok_end - a.tok_begin, lb = b.tok_end - b.tok_begin;
-    if (la != lb) return la > lb;
-    if (a.req != b.req) return a.req < b.req;
-    return a.chunk_tok0 < b.chunk_tok0;
-  });
-  out->items = ni;
-  out->merges = nm;
-  out->slots = slot;
-  return PKD_OK;
-}
 
 // ---------------------------------------------------------------- tensor maps
 typedef CUresult (*NaEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -337,10 +204,7 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
   const NaDecode* dk = nullptr;
   for (const NaDecode& k : kNaDecode)
     if (k.q_dtype == q_dtype && k.kv_dtype == kv_dtype && k.head_dim == head_dim) dk = &k;
-  const NaMerge* mk = nullptr;
-  for (const NaMerge& k : kNaMerge)
-    if (k.o_dtype == o_dtype && k.head_dim == head_dim) mk = &k;
-  if (!dk || !mk)
+  if (!dk)
     return na_fail(PKD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (128 or 256 for e4m3 KV)");
   if (batch > 0 && (indptr_host[0] < 0 || num_indices < (int64_t)indptr_host[batch]))
     return na_fail(PKD_ERR_INVALID_ARG, "indices must hold indptr[batch] page ids from indptr[0] >= 0");
@@ -370,26 +234,67 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
   std::lock_guard<std::mutex> lock(g_na_mutex);
   int rc = na_setup(dev);
   if (rc) return rc;
-  NaCounts cnt;
-  rc = na_plan(indptr_host, last_page_len_host, batch, num_qo_heads, num_kv_heads, head_dim,
-               page_size, window_left, fixed_split_size, disable_split_kv, g_na_sms[dev], &cnt);
-  if (rc) return rc;
+  const int kidx = (int)(dk - kNaDecode);
+  const int ctas = g_na_sms[dev] * g_na_per_sm[dev][kidx];
 
-  // ---- upload: clear the status word, copy the work list (pageable source: the copy has
-  // left the host buffers when cudaMemcpyAsync returns, so they may be rewritten next call)
+  // ---- plan with the library's decode planner, into the static host storage
+  PlanRequest r;
+  r.indptr = indptr_host;
+  r.last_page_len = last_page_len_host;
+  r.batch = batch;
+  r.num_qo_heads = num_qo_heads;
+  r.num_kv_heads = num_kv_heads;
+  r.head_dim = head_dim;
+  r.page_size = page_size;
+  r.window_left = window_left;
+  r.fixed_split_size = fixed_split_size;
+  r.disable_split_kv = disable_split_kv;
+  r.kv_dtype = kv_dtype;
+  r.use_tensor_cores = PKD_KERNEL_TENSOR_CORE;
+  r.num_sms = g_na_sms[dev];
+  const char* err = "";
+  DecodeSchedule sch;
+  sch.tasks = g_na_tasks;
+  sch.tasks_cap = PKD_NOALLOC_MAX_ITEMS;
+  sch.merges = g_na_merges;
+  sch.merges_cap = PKD_NOALLOC_MAX_MERGES;
+  // partial slots: kSlotHeads rows of head_dim + 1 floats each, in the partials region
+  sch.max_slots = (int64_t)((PKD_NOALLOC_PARTIAL_BYTES - 512) /
+                            ((size_t)kSlotHeads * (head_dim + 1) * sizeof(float)));
+  rc = build_decode_schedule(r, ctas, &sch, &err);
+  if (rc == PKD_ERR_WORKSPACE_TOO_SMALL) {
+    // name the limit of the built-in scratch that the plan ran into
+    const bool merges_full = std::strstr(err, "merge") != nullptr;
+    const bool partials_full = std::strstr(err, "partials") != nullptr;
+    return na_fail(rc, merges_full ? "plan splits more units than the built-in scratch holds "
+                                     "(PKD_NOALLOC_MAX_MERGES)"
+                       : partials_full
+                           ? "split partials exceed the built-in scratch "
+                             "(PKD_NOALLOC_PARTIAL_BYTES); use a larger fixed_split_size or "
+                             "disable_split_kv"
+                           : "plan needs more tasks than the built-in scratch holds "
+                             "(PKD_NOALLOC_MAX_ITEMS)");
+  }
+  if (rc) return na_fail(rc, err);
+
+  // ---- upload: clear the status word and the merge counters, copy the tasks and the merge
+  // entries (pageable sources: each copy has left the host buffers when
+  // cudaMemcpyAsync returns, so they may be rewritten by the next call)
   unsigned char* scratch = g_na_scratch[dev];
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, kStatusBytes, s) != cudaSuccess)
-    return na_fail(PKD_ERR_CUDA, "clearing the status word failed");
-  if (cudaMemcpyAsync(scratch + kNaItemsOff, g_na_items, cnt.items * sizeof(WorkItem),
+  if (cudaMemsetAsync(scratch, 0, kNaTasksOff, s) != cudaSuccess)
+    return na_fail(PKD_ERR_CUDA, "clearing the status word and the merge counters failed");
+  if (sch.n_tasks > 0 &&
+      cudaMemcpyAsync(scratch + kNaTasksOff, g_na_tasks, (size_t)sch.n_tasks * sizeof(DecodeTask),
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return na_fail(PKD_ERR_CUDA, "uploading the work list failed");
-  if (cnt.merges > 0 &&
-      cudaMemcpyAsync(scratch + kNaMergesOff, g_na_merges, cnt.merges * sizeof(MergeEntry),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return na_fail(PKD_ERR_CUDA, "uploading the tasks failed");
+  if (sch.n_merges > 0 &&
+      cudaMemcpyAsync(scratch + kNaMergesOff, g_na_merges,
+                      (size_t)sch.n_merges * sizeof(MergeEntry), cudaMemcpyHostToDevice,
+                      s) != cudaSuccess)
     return na_fail(PKD_ERR_CUDA, "uploading the merge list failed");
 
-  // ---- decode
+  // ---- decode (split units are merged inside the launch)
   DecodeParams prm;
   std::memset(&prm, 0, sizeof prm);
   const int rows = page_size < dk->tile ? page_size : dk->tile;
@@ -400,8 +305,10 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
                      kv_strides, kv_layout, rows);
   if (rc) return rc;
   const size_t part_o_bytes =
-      ((size_t)cnt.slots * num_qo_heads * head_dim * sizeof(float) + 255) / 256 * 256;
-  prm.items = reinterpret_cast<const WorkItem*>(scratch + kNaItemsOff);
+      ((size_t)sch.n_slots * kSlotHeads * head_dim * sizeof(float) + 255) / 256 * 256;
+  prm.tasks = reinterpret_cast<const DecodeTask*>(scratch + kNaTasksOff);
+  prm.merges = reinterpret_cast<const MergeEntry*>(scratch + kNaMergesOff);
+  prm.counters = reinterpret_cast<uint32_t*>(scratch + kNaCountersOff);
   prm.indices = indices_dev;
   prm.q = q;
   prm.o = o;
@@ -414,7 +321,6 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
   prm.num_qo_heads = num_qo_heads;
   prm.num_kv_heads = num_kv_heads;
   prm.group = num_qo_heads / num_kv_heads;
-  prm.gslices = 1;
   prm.page_size = page_size;
   prm.hnd = nhd ? 0 : 1;
   const double sm = (std::isnan(sm_scale) ? 1.0 / std::sqrt((double)head_dim) : (double)sm_scale) *
@@ -428,27 +334,10 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
     prm.cap_log2 = 0.f;
   }
   prm.v_scale = v_scale;
+  if (sch.n_tasks == 0) return PKD_OK;
   void* args[] = {&prm};
-  const unsigned grid = (unsigned)(cnt.items * num_kv_heads);
-  if (cudaLaunchKernel(dk->fn, dim3(grid), dim3(dk->threads), args, (size_t)dk->smem, s) !=
-      cudaSuccess)
+  if (cudaLaunchKernel(dk->fn, dim3((unsigned)sch.n_tasks), dim3(dk->threads), args,
+                       (size_t)dk->smem, s) != cudaSuccess)
     return na_fail(PKD_ERR_CUDA, "decode kernel launch failed");
-
-  // ---- merge_states for split requests
-  if (cnt.merges > 0) {
-    MergeParams mp;
-    mp.merges = reinterpret_cast<const MergeEntry*>(scratch + kNaMergesOff);
-    mp.part_o = prm.part_o;
-    mp.part_lse = prm.part_lse;
-    mp.o = o;
-    mp.lse = lse;
-    mp.status = prm.status;
-    mp.num_merges = (int)cnt.merges;
-    mp.num_qo_heads = num_qo_heads;
-    void* margs[] = {&mp};
-    const unsigned blocks = (unsigned)((cnt.merges * num_qo_heads + 3) / 4);
-    if (cudaLaunchKernel(mk->fn, dim3(blocks), dim3(128), margs, 0, s) != cudaSuccess)
-      return na_fail(PKD_ERR_CUDA, "merge kernel launch failed");
-  }
   return PKD_OK;
 }

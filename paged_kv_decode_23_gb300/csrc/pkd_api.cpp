@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <limits>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -35,7 +36,6 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::once_flag g_registry_once;
 std::vector<DecodeKernel> g_decode;
-std::vector<MergeKernel> g_merge;
 std::vector<MlaKernel> g_mla;
 
 void init_registry() {
@@ -44,7 +44,6 @@ void init_registry() {
     register_decode_bf16(g_decode);
     register_decode_e4m3(g_decode);
     register_decode_rope(g_decode);
-    register_merge(g_merge);
     register_mla(g_mla);
     register_mla_tc(g_mla);
   });
@@ -76,12 +75,6 @@ double alibi_slope_of(int g, int H) {
   return g < m ? std::exp2(-8.0 * (g + 1) / m) : std::exp2(-4.0 * (2 * (g - m) + 1) / m);
 }
 
-const MergeKernel* find_merge(int o_dtype, int head_dim) {
-  init_registry();
-  for (const auto& k : g_merge)
-    if (k.o_dtype == o_dtype && k.head_dim == head_dim) return &k;
-  return nullptr;
-}
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime (no libcuda link).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -130,7 +123,15 @@ struct pkd_handle {
   float sm_scale = 0.f, cap = 0.f;
   const int32_t* indices = nullptr;
   const DecodeKernel* kernel = nullptr;
-  const MergeKernel* merge = nullptr;
+
+  // The decode plan: tasks grouped by CTA, merge entries, CTA ranges, and the grid that runs
+  // them (CUDA-graph mode: fixed by the first plan).
+  std::vector<DecodeTask> tasks;
+  std::vector<MergeEntry> dmerges;
+  DecodeWsLayout dlayout{};
+  int grid = 0;       // CTAs pkd_run launches (one per task; CUDA-graph mode: the capacity)
+  int gslices = 1;
+  int64_t n_tasks = 0;
 
   // Pinned copies of the work list for the async uploads, used in turn: plan() waits only for
   // the upload of kStagingSlots plans ago, so a host that plans ahead of the GPU is not held up.
@@ -288,6 +289,56 @@ int fill_plan_request(PlanRequest* r, const int32_t* indptr, const int32_t* lpl,
 
 }  // namespace
 
+namespace {
+
+// Resident CTAs per SM of a decode kernel (its shared memory raised first), cached per kernel
+// and device.  The persistent grid is this times the SM count.
+int decode_ctas_per_sm(const DecodeKernel* k, int device, int* out) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& c : cache)
+    if (c.first.first == k->fn && c.first.second == device) {
+      *out = c.second;
+      return PKD_OK;
+    }
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k->fn, k->threads,
+                                                                (size_t)k->smem_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  n = std::max(1, std::min(n, kDecodeCtasPerSm));
+  cache.push_back({{k->fn, device}, n});
+  *out = n;
+  return PKD_OK;
+}
+
+// Storage for one decode schedule (host vectors, reused across plans).
+struct ScheduleStore {
+  std::vector<DecodeTask> tasks;
+  std::vector<MergeEntry> merges;
+};
+
+// Plans the batch (the GPU holding `ctas` CTAs at once) into `st`; *s holds the counts.
+int plan_decode(const PlanRequest& r, int ctas, ScheduleStore& st, DecodeSchedule* s) {
+  const char* err = "";
+  int64_t max_tasks = 0, max_merges = 0;
+  int rc = decode_schedule_bounds(r, ctas, s->max_slots, &max_tasks, &max_merges, &err);
+  if (rc) return fail(rc, err);
+  st.tasks.resize((size_t)std::max<int64_t>(1, max_tasks));
+  st.merges.resize((size_t)std::max<int64_t>(1, max_merges));
+  s->tasks = st.tasks.data();
+  s->tasks_cap = max_tasks;
+  s->merges = st.merges.data();
+  s->merges_cap = max_merges;
+  rc = build_decode_schedule(r, ctas, s, &err);
+  if (rc) return fail(rc, err);
+  st.tasks.resize((size_t)s->n_tasks);
+  st.merges.resize((size_t)s->n_merges);
+  return PKD_OK;
+}
+
+}  // namespace
+
 namespace pkd {
 // Lets other translation units of the library report a failure through pkd_last_error().
 void set_error_message(const char* msg) { g_last_error.assign(msg); }
@@ -359,9 +410,10 @@ int pkd_destroy(pkd_handle* h) {
 int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host, int batch,
                   int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                   int window_left, int fixed_split_size, int disable_split_kv, int kv_dtype,
-                  int use_tensor_cores, int num_sms, int32_t* items_out, int max_items,
-                  int32_t* merges_out, int max_merges, int* n_items, int* n_merges, int* n_slots,
-                  int* kernel_out, int* tile_tokens_out, int work_capacity, int q_len_per_req) {
+                  int use_tensor_cores, int num_sms, int32_t* tasks_out, int max_tasks,
+                  int32_t* merges_out, int max_merges, int* n_tasks, int* n_merges, int* n_slots,
+                  int* kernel_out, int* tile_tokens_out, int work_capacity, int q_len_per_req,
+                  int* n_ctas) {
   PlanRequest r;
   int rc = fill_plan_request(&r, indptr_host, last_page_len_host, batch, num_qo_heads,
                              num_kv_heads, head_dim, page_size, window_left, fixed_split_size,
@@ -369,22 +421,23 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
                              q_len_per_req);
   if (rc) return rc;
   r.max_items = work_capacity > 0 ? work_capacity : 0;
-  Plan plan;
-  const char* err = "";
-  rc = build_plan(r, &plan, &err);
-  if (rc) return fail(rc, err);
-  if (n_items) *n_items = (int)plan.items.size();
-  if (n_merges) *n_merges = (int)plan.merges.size();
-  if (n_slots) *n_slots = plan.num_slots;
-  if (kernel_out) *kernel_out = plan.kind;
-  if (tile_tokens_out) *tile_tokens_out = plan.tile_tokens;
-  if (items_out)
-    std::memcpy(items_out, plan.items.data(),
-                sizeof(WorkItem) * std::min<size_t>(plan.items.size(), (size_t)std::max(0, max_items)));
+  ScheduleStore st;
+  DecodeSchedule sch;
+  rc = plan_decode(r, (num_sms > 0 ? num_sms : 152) * kDecodeCtasPerSm, st, &sch);
+  if (rc) return rc;
+  if (n_tasks) *n_tasks = (int)sch.n_tasks;
+  if (n_merges) *n_merges = (int)sch.n_merges;
+  if (n_slots) *n_slots = (int)sch.n_slots;
+  if (kernel_out) *kernel_out = sch.kind;
+  if (tile_tokens_out) *tile_tokens_out = sch.tile_tokens;
+  if (n_ctas) *n_ctas = (int)sch.n_tasks;
+  if (tasks_out)
+    std::memcpy(tasks_out, st.tasks.data(),
+                sizeof(DecodeTask) * std::min<size_t>(st.tasks.size(), (size_t)std::max(0, max_tasks)));
   if (merges_out)
-    std::memcpy(merges_out, plan.merges.data(),
+    std::memcpy(merges_out, st.merges.data(),
                 sizeof(MergeEntry) *
-                    std::min<size_t>(plan.merges.size(), (size_t)std::max(0, max_merges)));
+                    std::min<size_t>(st.merges.size(), (size_t)std::max(0, max_merges)));
   g_last_error.clear();
   return PKD_OK;
 }
@@ -400,12 +453,15 @@ int pkd_workspace_bytes(const int32_t* indptr_host, const int32_t* last_page_len
                              disable_split_kv, kv_dtype, use_tensor_cores, num_sms,
                              q_len_per_req);
   if (rc) return rc;
-  Plan plan;
-  const char* err = "";
-  rc = build_plan(r, &plan, &err);
-  if (rc) return fail(rc, err);
-  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(plan, num_qo_heads, head_dim);
-  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(plan, num_kv_heads);
+  ScheduleStore st;
+  DecodeSchedule sch;
+  const int ctas = (num_sms > 0 ? num_sms : 152) * kDecodeCtasPerSm;
+  rc = plan_decode(r, ctas, st, &sch);
+  if (rc) return rc;
+  DecodeWsLayout lay{(size_t)sch.n_tasks, (size_t)sch.n_merges, (size_t)sch.n_slots};
+  lay.pos_floats = 2 * (size_t)head_dim + num_qo_heads;  // room for a positional encoding
+  if (float_ws_bytes) *float_ws_bytes = dws_float_bytes(lay, head_dim);
+  if (int_ws_bytes) *int_ws_bytes = dws_int_bytes(lay);
   return PKD_OK;
 }
 
@@ -461,23 +517,41 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (rc) return rc;
   if (h->graph) r.max_items = h->g_max_items;
   r.rope = pos_encoding_mode == PKD_POS_ROPE_LLAMA ? 1 : 0;
-  Plan plan;
+  DecodeSchedule sch;
   const char* err = "";
-  rc = build_plan(r, &plan, &err);
+  rc = decode_geometry(r, &sch, &err);
   if (rc) return fail(rc, err);
-
   const DecodeKernel* k =
-      find_decode(plan.kind, q_dtype, kv_dtype, head_dim, plan.heads_per_cta, r.rope);
+      find_decode(sch.kind, q_dtype, kv_dtype, head_dim, sch.heads_per_cta, r.rope);
   if (!k) return fail(PKD_ERR_UNSUPPORTED, "no decode kernel built for this dtype / head_dim");
-  const MergeKernel* mk = find_merge(o_dtype, head_dim);
-  if (!plan.merges.empty() && !mk)
-    return fail(PKD_ERR_UNSUPPORTED, "no merge kernel built for this dtype / head_dim");
+  cudaError_t e = set_smem_limit_once(k, h->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  // every resident CTA slot of the GPU: the persistent grid of the balanced layout
+  int per_sm = 0;
+  if (int rc2 = decode_ctas_per_sm(k, h->device, &per_sm)) return rc2;
+  const int ctas = h->num_sms * per_sm;
+  ScheduleStore st;
+  st.tasks.swap(h->tasks);
+  st.merges.swap(h->dmerges);
+  rc = plan_decode(r, ctas, st, &sch);
+  st.tasks.swap(h->tasks);
+  st.merges.swap(h->dmerges);
+  if (rc) return rc;
+  // one CTA per task; CUDA-graph mode launches the capacity's grid for every plan and the CTAs
+  // past a plan's tasks leave at once
+  const int64_t grid64 = h->graph ? (int64_t)h->g_max_items * num_kv_heads * sch.gslices
+                                  : sch.n_tasks;
+  if (grid64 > std::numeric_limits<int32_t>::max() / 2)
+    return fail(PKD_ERR_INVALID_ARG, "too many work items for one grid");
+  const int grid = (int)grid64;
 
-  WsLayout lay = h->graph ? capacity_layout(h->g_max_items, num_kv_heads, plan.gslices)
-                          : layout_of(plan, num_kv_heads);
+  DecodeWsLayout lay = h->graph ? decode_capacity_layout(h->g_max_items, num_kv_heads,
+                                                         sch.gslices)
+                                : DecodeWsLayout{(size_t)sch.n_tasks, (size_t)sch.n_merges,
+                                                 (size_t)sch.n_slots};
   if (pos_encoding_mode != PKD_POS_NONE) lay.pos_floats = 2 * (size_t)head_dim + num_qo_heads;
-  const size_t need_f = float_ws_bytes_of(lay, num_qo_heads, head_dim);
-  const size_t need_i = int_ws_bytes_of(lay);
+  const size_t need_f = dws_float_bytes(lay, head_dim);
+  const size_t need_i = dws_int_bytes(lay);
   if (need_f > h->float_bytes || need_i > h->int_bytes) {
     char buf[200];
     std::snprintf(buf, sizeof buf, "workspace too small: need %zu float / %zu int bytes", need_f,
@@ -485,19 +559,16 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
     return fail(PKD_ERR_WORKSPACE_TOO_SMALL, buf);
   }
 
-  cudaError_t e = set_smem_limit_once(k, h->device);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-
-  // Upload the int workspace image -- zeroed status block and merge counters, then the work
-  // list and the merge list at the layout's offsets -- with one copy (graph mode adds the page
-  // table's copies into the fixed buffers); wait for the previous upload to leave the pinned
-  // buffer first.
+  // Upload the int workspace image -- zeroed status block and merge counters, the CTA ranges,
+  // the tasks and the merge entries at the layout's offsets (and the positional-encoding
+  // table) -- with one copy (graph mode adds the page table's copies into the fixed buffers);
+  // wait for the upload of four plans ago to leave its pinned buffer first.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t items_off = items_offset(lay);
-  const size_t merges_off = merges_offset(lay);
-  const size_t items_b = plan.items.size() * sizeof(WorkItem);
-  const size_t merges_b = plan.merges.size() * sizeof(MergeEntry);
-  const size_t pos_off = pos_table_offset(lay);
+  const size_t tasks_off = dws_tasks_offset(lay);
+  const size_t merges_off = dws_merges_offset(lay);
+  const size_t pos_off = dws_pos_offset(lay);
+  const size_t tasks_b = (size_t)sch.n_tasks * sizeof(DecodeTask);
+  const size_t merges_b = (size_t)sch.n_merges * sizeof(MergeEntry);
   const size_t img_bytes = lay.pos_floats ? pos_off + lay.pos_floats * sizeof(float)
                                           : merges_off + merges_b;
   const size_t table_b = h->graph ? (size_t)(2 * batch + 1) * sizeof(int32_t) : 0;
@@ -505,13 +576,13 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   char* img = nullptr;
   int slot = 0;
   if (int rc2 = staging_acquire(h, bytes, &img, &slot)) return rc2;
-  std::memset(img, 0, merges_off);
+  std::memset(img, 0, tasks_off);
   if (h->graph) {
-    const int32_t count = (int32_t)plan.items.size();
+    const int32_t count = (int32_t)sch.n_tasks;
     std::memcpy(img + kItemCountOffset, &count, sizeof count);
   }
-  if (items_b) std::memcpy(img + items_off, plan.items.data(), items_b);
-  if (merges_b) std::memcpy(img + merges_off, plan.merges.data(), merges_b);
+  if (tasks_b) std::memcpy(img + tasks_off, h->tasks.data(), tasks_b);
+  if (merges_b) std::memcpy(img + merges_off, h->dmerges.data(), merges_b);
   if (lay.pos_floats) {
     // [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate}: the RoPE angle rate
     // theta^(-2i/D) / rope_scale of dim pair i as a float pair, and the rotation across 8
@@ -552,7 +623,9 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   }
   if (int rc2 = staging_release(h, slot, s)) return rc2;
 
-  h->plan = std::move(plan);
+  h->n_tasks = sch.n_tasks;
+  h->gslices = sch.gslices;
+  h->grid = grid;
   h->batch = batch;
   h->q_len = q_len_per_req;
   h->num_qo_heads = num_qo_heads;
@@ -565,12 +638,11 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   h->sm_scale = std::isnan(sm_scale) ? 1.0f / std::sqrt((float)head_dim) : sm_scale;
   h->cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
   h->indices = h->graph ? h->g_indices : indices_dev;
-  h->ws_layout = lay;
+  h->dlayout = lay;
   if (h->graph) h->g_batch = batch;
   h->kernel = k;
   h->pos_mode = pos_encoding_mode;
   h->mla = false;
-  h->merge = mk;
   h->planned = true;
   g_last_error.clear();
   return PKD_OK;
@@ -583,7 +655,7 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   if (!h->planned || h->mla)
     return fail(PKD_ERR_NOT_PLANNED, "pkd_run called before a successful pkd_plan");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (h->plan.items.empty() && !h->graph) return PKD_OK;  // empty batch
+  if (h->n_tasks == 0 && !h->graph) return PKD_OK;  // empty batch
   if (!q || !k_base || !v_base || !o || !kv_strides)
     return fail(PKD_ERR_INVALID_ARG, "null q / k_base / v_base / o / kv_strides");
   if (num_pages <= 0 || num_pages > (int64_t(1) << 31))
@@ -618,29 +690,26 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
 
   char* iws = static_cast<char*>(h->int_ws);
   char* fws = static_cast<char*>(h->float_ws);
-  const WsLayout& lay = h->ws_layout;
-  const size_t part_o_bytes = part_lse_offset(lay, h->num_qo_heads, h->head_dim);
-  prm.items = reinterpret_cast<const WorkItem*>(iws + items_offset(lay));
-  prm.merges = reinterpret_cast<const MergeEntry*>(iws + merges_offset(lay));
-  prm.counters = reinterpret_cast<uint32_t*>(iws + kStatusBytes);
-  prm.item_count = h->graph ? reinterpret_cast<const int32_t*>(iws + kItemCountOffset) : nullptr;
+  const DecodeWsLayout& lay = h->dlayout;
+  prm.tasks = reinterpret_cast<const DecodeTask*>(iws + dws_tasks_offset(lay));
+  prm.task_count = h->graph ? reinterpret_cast<const int32_t*>(iws + kItemCountOffset) : nullptr;
+  prm.merges = reinterpret_cast<const MergeEntry*>(iws + dws_merges_offset(lay));
+  prm.counters = reinterpret_cast<uint32_t*>(iws + dws_counters_offset());
   prm.pos_table =
-      lay.pos_floats ? reinterpret_cast<const float*>(iws + pos_table_offset(lay)) : nullptr;
+      lay.pos_floats ? reinterpret_cast<const float*>(iws + dws_pos_offset(lay)) : nullptr;
   prm.alibi = h->pos_mode == PKD_POS_ALIBI ? 1 : 0;
-  prm.fuse_merge = 1;
   prm.indices = h->indices;
   prm.q = q;
   prm.o = o;
   prm.lse = lse;
   prm.part_o = reinterpret_cast<float*>(fws);
-  prm.part_lse = reinterpret_cast<float*>(fws + part_o_bytes);
+  prm.part_lse = reinterpret_cast<float*>(fws + dws_part_lse_offset(lay, h->head_dim));
   prm.status = reinterpret_cast<uint32_t*>(iws);
   prm.wait_ns = h->wait_ns;
   prm.num_pages = (uint32_t)num_pages;
   prm.num_qo_heads = h->num_qo_heads;
   prm.num_kv_heads = h->num_kv_heads;
   prm.group = h->num_qo_heads / h->num_kv_heads;
-  prm.gslices = h->plan.gslices;
   prm.page_size = h->page_size;
   prm.hnd = nhd ? 0 : 1;
   const double log2e = 1.4426950408889634;
@@ -654,8 +723,7 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   }
   prm.v_scale = v_scale;
 
-  const int64_t n_items = h->graph ? (int64_t)h->g_max_items : (int64_t)h->plan.items.size();
-  const int64_t grid = n_items * h->num_kv_heads * h->plan.gslices;
+  const int64_t grid = h->grid;  // persistent CTAs (CUDA-graph mode: the fixed grid)
   void* args[] = {&prm};
   cudaError_t e;
   if (ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_start), s)) != cudaSuccess)
@@ -678,7 +746,7 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   if (ev_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_end), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
 
-  // split requests are merged by the decode kernel's last CTA per request (fuse_merge)
+  // split (row, kv head, slice) units are merged by the CTA that finishes their last chunk
   return PKD_OK;
 }
 
@@ -993,6 +1061,19 @@ int pkd_set_pdl(pkd_handle* h, int enable) {
   return PKD_OK;
 }
 
+int pkd_plan_info(pkd_handle* h, int* grid, int* ctas_per_sm, int64_t* n_tasks,
+                  int64_t* n_merges) {
+  if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
+  if (!h->planned || h->mla) return fail(PKD_ERR_NOT_PLANNED, "no decode plan on this handle");
+  int per_sm = 0;
+  if (int rc = decode_ctas_per_sm(h->kernel, h->device, &per_sm)) return rc;
+  if (grid) *grid = h->grid;
+  if (ctas_per_sm) *ctas_per_sm = per_sm;
+  if (n_tasks) *n_tasks = h->n_tasks;
+  if (n_merges) *n_merges = (int64_t)h->dmerges.size();
+  return PKD_OK;
+}
+
 int pkd_set_wait_limit(pkd_handle* h, uint64_t limit_ns) {
   if (!h) return fail(PKD_ERR_INVALID_ARG, "handle is null");
   if (limit_ns > kWaitLimitNs)
@@ -1063,9 +1144,10 @@ int pkd_graph_workspace_bytes(int max_items, int num_qo_heads, int num_kv_heads,
     hpc = 2;
     while (hpc < G && hpc < 8) hpc <<= 1;
   }
-  const WsLayout lay = capacity_layout(max_items, num_kv_heads, (G + hpc - 1) / hpc);
-  if (float_ws_bytes) *float_ws_bytes = float_ws_bytes_of(lay, num_qo_heads, head_dim);
-  if (int_ws_bytes) *int_ws_bytes = int_ws_bytes_of(lay);
+  DecodeWsLayout lay = decode_capacity_layout(max_items, num_kv_heads, (G + hpc - 1) / hpc);
+  lay.pos_floats = 2 * (size_t)head_dim + num_qo_heads;  // room for a positional encoding
+  if (float_ws_bytes) *float_ws_bytes = dws_float_bytes(lay, head_dim);
+  if (int_ws_bytes) *int_ws_bytes = dws_int_bytes(lay);
   return PKD_OK;
 }
 
@@ -1100,7 +1182,9 @@ int pkd_check_status(pkd_handle* h, uint32_t* status, void* stream) {
     // A kernel that gave up may have left a split request's chunk counter part-way; zero the
     // counters with the status word so the next run of this plan merges at the right count.
     e = cudaMemsetAsync(h->int_ws, 0, sizeof v, s);
-    const size_t counters_end = h->planned ? items_offset(h->ws_layout) : kStatusBytes;
+    const size_t counters_end = !h->planned ? kStatusBytes
+                                : h->mla    ? items_offset(h->ws_layout)
+                                            : dws_tasks_offset(h->dlayout);
     if (e == cudaSuccess && counters_end > kStatusBytes)
       e = cudaMemsetAsync(static_cast<char*>(h->int_ws) + kStatusBytes, 0,
                           counters_end - kStatusBytes, s);

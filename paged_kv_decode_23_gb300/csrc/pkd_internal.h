@@ -36,6 +36,29 @@ struct MergeEntry {
 };
 static_assert(sizeof(MergeEntry) == 16, "MergeEntry is 4 int32");
 
+// One task of the persistent decode kernel: a chunk of one output row's attended tokens for
+// one kv head and one slice of that head's qo-head group (at most 8 qo heads).  The fields up
+// to q_pos mean what they mean in a WorkItem.  A CTA runs a list of tasks back to back.
+struct DecodeTask {
+  int32_t req;         // output row: q / o / lse row index
+  int32_t page_base;   // indptr[request]: offset of the request's first page id in `indices`
+  int32_t chunk_tok0;  // first token of the chunk's first tile (a page boundary)
+  int32_t tok_begin;   // attended tokens [tok_begin, tok_end)
+  int32_t tok_end;
+  int32_t out_slot;    // < 0: the task is the whole row for its heads (final o / lse);
+                       // else its fp32 partial goes to slot out_slot
+  int32_t merge_idx;   // the merge entry of the task's (row, kv head, slice) when split
+  int32_t q_pos;       // the row's query position (its last key): ALiBi / RoPE
+  int32_t kvh;         // kv head
+  int32_t gs;          // slice of the kv head's qo-head group
+  int32_t cta;         // the CTA that runs it
+  int32_t pad;
+};
+static_assert(sizeof(DecodeTask) == 48, "DecodeTask is 12 int32");
+
+// Rows of one partial slot: the qo heads of one task (a slice holds at most 8).
+constexpr int kSlotHeads = 8;
+
 enum DType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 // Default (and largest) limit of a kernel's pipeline waits, in ns of the global timer.
@@ -51,18 +74,18 @@ enum KernelKind { kCudaCore = 0, kTensorCore = 1 };
 struct DecodeParams {
   CUtensorMap tmap_k;  // 4-D view of the K pool, see make_kv_tensor_map
   CUtensorMap tmap_v;
-  const WorkItem* items;
+  const DecodeTask* tasks;   // CTA c runs task c (longest first)
+  const int32_t* task_count; // CUDA-graph mode: the plan's task count, read on the device (the
+                             // grid is cut for a fixed capacity); null: the grid is exact
   const int32_t* indices;
   const void* q;        // [batch, Hq, D] q dtype
   void* o;              // [batch, Hq, D] o dtype
   float* lse;           // [batch, Hq] natural log, may be null
-  float* part_o;        // [slots, Hq, D] fp32, normalised partial outputs
-  float* part_lse;      // [slots, Hq] fp32, base-2 log-sum-exp of the partial
+  float* part_o;        // [slots, kSlotHeads, D] fp32, normalised partial outputs
+  float* part_lse;      // [slots, kSlotHeads] fp32, base-2 log-sum-exp of the partial
   uint32_t* status;     // device status word (bit 0: a pipeline wait timed out)
-  const MergeEntry* merges;  // with fuse_merge: the split requests
-  uint32_t* counters;   // with fuse_merge: finished chunks per (merge entry, kv head, slice)
-  const int32_t* item_count;  // CUDA-graph mode: the plan's work-item count, read on the device
-                              // (the grid is cut for a fixed capacity); null: the grid is exact
+  const MergeEntry* merges;  // the split (row, kv head, slice) units: slots and chunk counts
+  uint32_t* counters;   // finished chunks per merge entry (the last one merges)
   // Positional-encoding table (plan's pos_encoding_mode), in the int workspace, 256-byte
   // aligned: [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate} for the RoPE angle
   // rate rope_theta^(-2i/D) / rope_scale (a float pair) and the rotation across 8 positions,
@@ -73,28 +96,15 @@ struct DecodeParams {
   uint32_t num_pages;   // pages in the pool: an id outside [0, num_pages) sets status bit 1
                         // (the load itself reads zeros: the tensor map bounds-checks it)
   int alibi;            // 1: add pos_table[qo head] * (t - q_pos) to every logit
-  int fuse_merge;       // 1: the last CTA of a split request merges its partials in place
   int num_qo_heads;
   int num_kv_heads;
   int group;            // Hq / Hkv
-  int gslices;          // CTAs per (item, kv head): ceil(group / heads per CTA)
   int page_size;
   int hnd;              // 1: the tensor map's dims are (d, slot, head, page); 0: (d, head, slot, page)
   float scale_qk;       // multiplies <q, k>: sm_scale*q_scale*k_scale, times log2(e) without a
                         // cap or divided by the cap with one
   float cap_log2;       // cap * log2(e), 0 = no cap
   float v_scale;
-};
-
-struct MergeParams {
-  const MergeEntry* merges;
-  const float* part_o;
-  const float* part_lse;
-  void* o;
-  float* lse;
-  uint32_t* status;
-  int num_merges;
-  int num_qo_heads;
 };
 
 // A compiled decode kernel and how to launch it.
@@ -109,14 +119,7 @@ struct DecodeKernel {
   int smem_bytes;   // dynamic shared memory
   int tile_tokens;  // tokens per pipeline stage
   int rope;         // 1: rotates q and K (ROPE_LLAMA) before the QK product
-};
-
-struct MergeKernel {
-  int o_dtype;
-  int head_dim;
-  const void* fn;
-  int threads;
-  int heads_per_block;
+  int nstages;      // pipeline stages
 };
 
 // Registries filled by the kernel translation units.
@@ -167,7 +170,6 @@ struct MlaKernel {
 };
 void register_mla(std::vector<MlaKernel>& out);
 void register_mla_tc(std::vector<MlaKernel>& out);
-void register_merge(std::vector<MergeKernel>& out);
 
 // ----------------------------------------------------------------------------- planner
 struct PlanRequest {
@@ -184,7 +186,8 @@ struct PlanRequest {
   int kv_dtype;
   int use_tensor_cores;  // -1 auto, 0, 1
   int num_sms;
-  int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode)
+  int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode;
+                         // for decode: chunks per row, counted over all rows)
   int q_len = 1;         // query tokens per request (run's q_len_per_req)
   int rope = 0;          // 1: ROPE_LLAMA (only the tensor-core kernel is built for it)
   // MLA plans (pkd_mla_plan): lengths come from kv_len (pages may be more than needed), any
@@ -208,8 +211,73 @@ struct Plan {
   int64_t chunk_tokens = 0;  // 0 = no split
 };
 
-// Returns 0 or a PKD_ERR_* code with a message in *err.
+// Returns 0 or a PKD_ERR_* code with a message in *err.  MLA plans (r.mla) only.
 int build_plan(const PlanRequest& r, Plan* plan, const char** err);
+
+// ----------------------------------------------------------------------- decode schedule
+// The decode planner's output, written into storage the caller provides (it allocates
+// nothing: the no-allocation entry point passes static arrays, the handle path vectors).
+struct DecodeSchedule {
+  DecodeTask* tasks = nullptr;  // capacity tasks_cap; task q runs on CTA q (longest first)
+  int64_t tasks_cap = 0;
+  MergeEntry* merges = nullptr;  // capacity merges_cap; {row, first slot, chunks, unit}
+  int64_t merges_cap = 0;
+
+  int64_t max_slots = 0;         // > 0: at most this many partial slots
+  // results
+  int64_t n_tasks = 0, n_merges = 0, n_slots = 0;
+  int kind = kTensorCore, heads_per_cta = 8, gslices = 1, tile_tokens = 64;
+};
+
+// Kernel geometry a decode plan implies (kind, heads per CTA, slices, tile) and validation of
+// the request.  Returns 0 or a PKD_ERR_* code with a message in *err.
+int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err);
+// The tasks and merge entries build_decode_schedule emits when the GPU holds `ctas` CTAs at
+// once (max_slots > 0: at most that many partial slots).
+int decode_schedule_bounds(const PlanRequest& r, int ctas, int64_t max_slots,
+                           int64_t* max_tasks, int64_t* max_merges, const char** err);
+// Cuts every row's attended tokens into tasks per (kv head, slice), one per CTA, longest first.
+int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, const char** err);
+
+// CTAs per SM the decode kernels are sized for.
+constexpr int kDecodeCtasPerSm = 2;
+
+// Decode workspaces.  int: [status block (CUDA-graph mode: the task count at
+// kItemCountOffset) | one merge counter per merge entry | tasks | merge entries |
+// positional-encoding table]; float: [part_o (slots x kSlotHeads x D) | part_lse (slots x
+// kSlotHeads)], every region 256-byte aligned.  A plan's own counts, or in CUDA-graph mode
+// fixed capacities (every address a captured launch holds stays valid).
+struct DecodeWsLayout {
+  size_t tasks, merges, slots;
+  size_t pos_floats = 0;
+};
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+inline size_t dws_counters_offset() { return 256; }
+inline size_t dws_tasks_offset(const DecodeWsLayout& l) {
+  return dws_counters_offset() + align256(l.merges * 4);
+}
+inline size_t dws_merges_offset(const DecodeWsLayout& l) {
+  return dws_tasks_offset(l) + align256(l.tasks * sizeof(DecodeTask));
+}
+inline size_t dws_pos_offset(const DecodeWsLayout& l) {
+  return dws_merges_offset(l) + align256(l.merges * sizeof(MergeEntry));
+}
+inline size_t dws_int_bytes(const DecodeWsLayout& l) {
+  return dws_pos_offset(l) + align256(l.pos_floats * sizeof(float));
+}
+inline size_t dws_part_lse_offset(const DecodeWsLayout& l, int head_dim) {
+  return align256(l.slots * kSlotHeads * (size_t)head_dim * sizeof(float));
+}
+inline size_t dws_float_bytes(const DecodeWsLayout& l, int head_dim) {
+  return dws_part_lse_offset(l, head_dim) + align256(l.slots * kSlotHeads * sizeof(float)) + 256;
+}
+// CUDA-graph mode: a work list of at most max_items chunks per row (summed over rows) holds at
+// most max_items x Hkv x slices tasks (the fixed grid), half as many merge entries, as many
+// slots.
+inline DecodeWsLayout decode_capacity_layout(size_t max_items, int num_kv_heads, int gslices) {
+  const size_t tasks = max_items * (size_t)num_kv_heads * gslices;
+  return {tasks, tasks / 2, tasks, 0};
+}
 
 // Byte offsets inside the int workspace.
 constexpr size_t kStatusBytes = 256;

@@ -1,4 +1,4 @@
-// planner.cpp -- host planner: turns a CSR page table into the split-KV work list.
+// planner.cpp -- host planners: turn a CSR page table into the work a decode launch runs.
 //
 // FlashInfer attention API page, BatchDecodeWithPagedKVCacheWrapper:
 //   - plan() builds auxiliary data structures once and every later run() reuses them
@@ -10,7 +10,11 @@
 //     output, does not depend on the batch; disable_split_kv keeps one chunk per request.
 // With a fixed split, chunks are cut at multiples of the chunk size counted from the request's
 // first token, so a request's partition depends only on its own length, its window and the
-// chunk size.  The heuristic split cuts a long request into equal page-aligned chunks.
+// chunk size.
+//
+// build_plan: the MLA work list (BatchMLAPagedAttentionWrapper; one CTA, or CTA pair, per
+// item and SM, in waves).  build_decode_schedule (below): the persistent decode kernel's task
+// lists.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -26,43 +30,30 @@ namespace {
 constexpr int kErrInvalid = -1;
 constexpr int kErrUnsupported = -5;
 constexpr int kErrWorkspace = -3;
-constexpr int kCtasPerSm = 2;        // every decode kernel is sized for two resident CTAs
-constexpr int kWavesTarget = 1;      // heuristic: about one wave of CTAs (measured best on GB300)
 constexpr int64_t kMinChunk = 256;   // never split below this many tokens
-
-bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-
-int tile_tokens_for(int head_dim, int kv_dtype) {
-  const int row_bytes = head_dim * (kv_dtype == kE4M3 ? 1 : 2);
-  return 16384 / row_bytes;  // a K tile is 16 KiB; K + V make a 32 KiB stage
-}
 
 }  // namespace
 
 int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
   *plan = Plan();
-  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || (!r.last_page_len && !r.kv_len)))) {
+  if (!r.mla) {
+    *err = "build_plan plans MLA batches; decode batches use build_decode_schedule";
+    return kErrInvalid;
+  }
+  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || !r.kv_len))) {
     *err = "batch must be >= 0 and the page table pointers non-null";
     return kErrInvalid;
   }
-  if (r.num_qo_heads <= 0 || r.num_kv_heads <= 0 || r.num_qo_heads % r.num_kv_heads != 0) {
-    *err = "num_qo_heads must be a positive multiple of num_kv_heads";
+  if (r.num_qo_heads <= 0 || r.num_kv_heads != 1) {
+    *err = "num_heads must be positive";
     return kErrInvalid;
   }
-  if (r.kv_dtype != kF16 && r.kv_dtype != kBF16 && r.kv_dtype != kE4M3) {
-    *err = "kv_dtype must be F16, BF16 or E4M3";
+  if (r.kv_dtype != kF16 && r.kv_dtype != kBF16) {
+    *err = "the MLA caches must be F16 or BF16";
     return kErrInvalid;
   }
-  if (!r.mla && r.head_dim != 64 && r.head_dim != 128 && r.head_dim != 256) {
-    *err = "head_dim must be 64, 128 or 256";
-    return kErrUnsupported;
-  }
-  if (r.kv_dtype == kE4M3 && r.head_dim == 64) {
-    *err = "e4m3 KV needs head_dim 128 or 256 (rows of whole 128-byte blocks)";
-    return kErrUnsupported;
-  }
-  if (r.mla ? r.page_size < 1 : (!is_pow2(r.page_size) || r.page_size < 8 || r.page_size > 256)) {
-    *err = r.mla ? "page_size must be >= 1" : "page_size must be a power of two in [8, 256]";
+  if (r.page_size < 1) {
+    *err = "page_size must be >= 1";
     return kErrUnsupported;
   }
   if (r.batch > 0 && r.indptr[0] < 0) {
@@ -70,31 +61,13 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     return kErrInvalid;
   }
   const int ps = r.page_size;
-  const int group = r.num_qo_heads / r.num_kv_heads;
-  const int G = group;
+  plan->kind = kTensorCore;
+  plan->heads_per_cta = r.mla_heads_per_cta;
+  plan->gslices = (r.num_qo_heads + plan->heads_per_cta - 1) / plan->heads_per_cta *
+                  r.mla_ctas_per_head_tile;
+  plan->tile_tokens = r.mla_tile_tokens;
 
-  // kernel choice (use_tensor_cores): auto takes the tensor-core kernel
-  plan->kind = r.use_tensor_cores == 0 ? kCudaCore : kTensorCore;
-  if (plan->kind == kTensorCore) {
-    plan->heads_per_cta = 8;
-  } else {
-    int gp = 2;
-    while (gp < G && gp < 8) gp <<= 1;
-    plan->heads_per_cta = gp;
-  }
-  if (r.mla) {
-    plan->kind = kTensorCore;
-    plan->heads_per_cta = r.mla_heads_per_cta;
-  }
-  plan->gslices = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
-  if (r.mla) plan->gslices *= r.mla_ctas_per_head_tile;
-  if (r.rope && plan->kind == kCudaCore) {
-    *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
-    return kErrUnsupported;
-  }
-  plan->tile_tokens = r.mla ? r.mla_tile_tokens : tile_tokens_for(r.head_dim, r.kv_dtype);
-
-  // per-request lengths
+  // per-request lengths, from kv_len_arr (pages may be more than the length needs)
   std::vector<int64_t> n_req(r.batch);
   for (int i = 0; i < r.batch; ++i) {
     const int64_t pages = (int64_t)r.indptr[i + 1] - r.indptr[i];
@@ -102,28 +75,11 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       *err = "indptr must be non-decreasing";
       return kErrInvalid;
     }
-    if (r.kv_len) {  // lengths given directly (MLA's kv_len_arr); extra pages are ignored
-      if (r.kv_len[i] < 0 || (int64_t)r.kv_len[i] > pages * ps) {
-        *err = "kv_len must lie in [0, pages * page_size] for every request";
-        return kErrInvalid;
-      }
-      n_req[i] = r.kv_len[i];
-      continue;
-    }
-    if (pages == 0) {
-      n_req[i] = 0;
-      continue;
-    }
-    const int lpl = r.last_page_len[i];
-    if (lpl < 1 || lpl > ps) {
-      *err = "last_page_len must lie in [1, page_size] for every request with pages";
+    if (r.kv_len[i] < 0 || (int64_t)r.kv_len[i] > pages * ps) {
+      *err = "kv_len must lie in [0, pages * page_size] for every request";
       return kErrInvalid;
     }
-    n_req[i] = (int64_t)ps * (pages - 1) + lpl;
-    if (n_req[i] > (int64_t)std::numeric_limits<int32_t>::max() - 4096) {
-      *err = "a request is longer than 2^31 - 4096 tokens";
-      return kErrInvalid;
-    }
+    n_req[i] = r.kv_len[i];
   }
 
   // Output rows: query token j of request i is row i * q_len + j, at position
@@ -172,13 +128,9 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     *err = "the batch has more query rows (requests x q_len_per_req) than the work-list capacity";
     return kErrInvalid;
   }
-  if (r.disable_split_kv) {
-    C = 0;
-  } else if (r.fixed_split_size > 0) {
-    C = (int64_t)r.fixed_split_size * ps;
-  } else {
+  {
     const int sms = r.num_sms > 0 ? r.num_sms : 152;
-    const int64_t slots = (int64_t)sms * (r.ctas_per_sm > 0 ? r.ctas_per_sm : kCtasPerSm);
+    const int64_t slots = (int64_t)sms * (r.ctas_per_sm > 0 ? r.ctas_per_sm : 1);
     if ((int64_t)rows * ctas_per_item <= slots) {
       // The unsplit requests already fit in one wave: split only as far as the grid stays
       // one wave, i.e. the smallest page-aligned chunk whose CTAs all start at once.  A second,
@@ -189,7 +141,7 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
         if (ctas_with(mid) <= slots) hi = mid; else lo = mid + ps;
       }
       C = longest > lo ? lo : 0;
-    } else if (r.mla) {
+    } else {
       // MLA kernels hold one CTA (pair) per SM, so the grid runs in waves of whole items, and
       // every item pays a fixed cost on top of its tokens (Q load, pipeline fill and drain,
       // epilogue: about 11 tiles of 32 tokens measured on GB300).  Candidates: for k = 1..16,
@@ -273,14 +225,6 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
       for (int i = 0; i < (int)kc.size(); ++i)
         c_big = std::max<int64_t>(c_big, chunk_len(i, kc[i]));
       C = c_big;
-    } else {
-      // More requests than one wave: chunks of about the average load of a CTA slot over
-      // kWavesTarget waves, so the longest requests stop bounding the tail.
-      const int64_t per_cta = (total * ctas_per_item + slots * kWavesTarget - 1) /
-                              (slots * kWavesTarget);
-      int64_t c = std::max<int64_t>(c_min, per_cta);
-      c = (c + ps - 1) / ps * ps;
-      C = longest > c ? c : 0;
     }
     if (C > 0 && kc.empty() && r.max_items > 0 && items_with(C) > r.max_items) {
       // a bounded work list (CUDA-graph mode): the smallest larger chunk that fits
@@ -296,7 +240,6 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
 
   // work items, partial slots in request order, merge entries
   std::vector<WorkItem>& items = plan->items;
-  const bool fixed = !r.disable_split_kv && r.fixed_split_size > 0;
   std::vector<int64_t> bounds, tile0;
   for (int i = 0; i < rows; ++i) {
     WorkItem it;
@@ -319,13 +262,6 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     if (C == 0 && kc.empty()) {
       bounds = {w[i], n[i]};
       tile0 = {0};
-    } else if (fixed) {
-      // multiples of C counted from token 0: independent of the rest of the batch
-      for (int64_t k = w[i] / C; k <= (n[i] - 1) / C; ++k) {
-        bounds.push_back(std::max(k * C, w[i]));
-        tile0.push_back(k * C);
-      }
-      bounds.push_back(n[i]);
     } else {
       // heuristic: k equal page-aligned chunks, so no short remainder chunk (which would
       // launch last and do the request's merge at the very end of the grid)
@@ -370,10 +306,334 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err) {
     *err = "too many work items for one grid";
     return kErrInvalid;
   }
-  if (r.max_items > 0 && (int64_t)items.size() > r.max_items) {
-    // only a fixed split can get here: the heuristic already fits the capacity
-    *err = "fixed_split_size cuts this batch into more work items than the work-list capacity";
-    return kErrWorkspace;
+  *err = "";
+  return 0;
+}
+
+}  // namespace pkd
+
+// ============================================================================ decode schedule
+//
+// The decode kernel runs one task per CTA: a chunk of one output row's attended tokens for one
+// kv head and one slice of its qo-head group.  Tasks launch longest first and the hardware
+// hands each free CTA slot the next one; the kv heads (and slices) of one chunk are neighbours
+// in that order, so they stream the same tokens at the same time (in the NHD layout they share
+// every slot's row of memory).  Chunks:
+//   - fixed_split_size: at multiples of C tokens from the row's token 0 (the result of a row
+//     does not depend on the batch);
+//   - disable_split_kv: whole rows;
+//   - otherwise: when the unsplit rows' CTAs fit in one wave of CTA slots, the smallest
+//     page-aligned chunk whose CTAs all still fit in one wave (a second, partial wave measured
+//     slower); else chunks of about one CTA slot's average load; a row longer than the chunk
+//     is cut into equal page-aligned parts, so no short remainder launches last.
+// A unit (row, kv head, slice) cut into k > 1 chunks gets k partial slots and a merge entry; the
+// CTA that finishes its last chunk merges them.  The planner writes into storage the caller
+// provides and allocates nothing, so the no-allocation entry point shares it.
+namespace pkd {
+
+namespace {
+
+constexpr int kErrInvalidD = -1;
+constexpr int kErrUnsupportedD = -5;
+constexpr int kErrWorkspaceD = -3;
+
+int64_t request_len(const PlanRequest& r, int i) {
+  const int64_t pages = (int64_t)r.indptr[i + 1] - r.indptr[i];
+  return pages <= 0 ? 0 : (int64_t)r.page_size * (pages - 1) + r.last_page_len[i];
+}
+
+// Output row `row` (query token j of request i): its key count n, first attended token w and
+// the offset of its request's page ids.
+struct RowSpan {
+  int64_t n, w;
+  int32_t base;
+};
+RowSpan row_span(const PlanRequest& r, int row) {
+  const int ql = r.q_len > 0 ? r.q_len : 1;
+  const int i = row / ql, j = row % ql;
+  RowSpan s;
+  s.n = std::max<int64_t>(0, request_len(r, i) - (ql - 1 - j));
+  s.w = (r.window_left >= 0 && s.n - 1 - r.window_left > 0) ? s.n - 1 - r.window_left : 0;
+  s.base = r.indptr[i];
+  return s;
+}
+
+int rows_of(const PlanRequest& r) { return r.batch * (r.q_len > 0 ? r.q_len : 1); }
+
+// chunks of a row with a fixed chunk of C tokens (C = 0: one)
+int64_t fixed_chunks(const RowSpan& s, int64_t C) {
+  if (s.n == 0 || C == 0) return 1;
+  return (s.n - 1) / C - s.w / C + 1;
+}
+
+}  // namespace
+
+int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err) {
+  if (r.batch < 0 || (r.batch > 0 && (!r.indptr || !r.last_page_len))) {
+    *err = "batch must be >= 0 and the page table pointers non-null";
+    return kErrInvalidD;
+  }
+  if (r.num_qo_heads <= 0 || r.num_kv_heads <= 0 || r.num_qo_heads % r.num_kv_heads != 0) {
+    *err = "num_qo_heads must be a positive multiple of num_kv_heads";
+    return kErrInvalidD;
+  }
+  if (r.kv_dtype != kF16 && r.kv_dtype != kBF16 && r.kv_dtype != kE4M3) {
+    *err = "kv_dtype must be F16, BF16 or E4M3";
+    return kErrInvalidD;
+  }
+  if (r.head_dim != 64 && r.head_dim != 128 && r.head_dim != 256) {
+    *err = "head_dim must be 64, 128 or 256";
+    return kErrUnsupportedD;
+  }
+  if (r.kv_dtype == kE4M3 && r.head_dim == 64) {
+    *err = "e4m3 KV needs head_dim 128 or 256 (rows of whole 128-byte blocks)";
+    return kErrUnsupportedD;
+  }
+  if (r.page_size < 8 || r.page_size > 256 || (r.page_size & (r.page_size - 1)) != 0) {
+    *err = "page_size must be a power of two in [8, 256]";
+    return kErrUnsupportedD;
+  }
+  if (r.q_len < 1) {
+    *err = "q_len_per_req must be >= 1";
+    return kErrInvalidD;
+  }
+  if ((int64_t)r.batch * r.q_len > (int64_t)std::numeric_limits<int32_t>::max() / 2) {
+    *err = "batch * q_len_per_req is too large";
+    return kErrInvalidD;
+  }
+  if (r.batch > 0 && r.indptr[0] < 0) {
+    *err = "indptr[0] must be >= 0";
+    return kErrInvalidD;
+  }
+  for (int i = 0; i < r.batch; ++i) {
+    const int64_t pages = (int64_t)r.indptr[i + 1] - r.indptr[i];
+    if (pages < 0) {
+      *err = "indptr must be non-decreasing";
+      return kErrInvalidD;
+    }
+    if (pages > 0 && (r.last_page_len[i] < 1 || r.last_page_len[i] > r.page_size)) {
+      *err = "last_page_len must lie in [1, page_size] for every request with pages";
+      return kErrInvalidD;
+    }
+    if (request_len(r, i) > (int64_t)std::numeric_limits<int32_t>::max() - 4096) {
+      *err = "a request is longer than 2^31 - 4096 tokens";
+      return kErrInvalidD;
+    }
+  }
+  const int G = r.num_qo_heads / r.num_kv_heads;
+  // use_tensor_cores auto takes the tensor-core kernel at every group size: measured on GB300,
+  // it streams faster than the CUDA-core kernel for groups of 1, 2, 4 and 8 alike
+  s->kind = r.use_tensor_cores == 0 ? kCudaCore : kTensorCore;
+  if (s->kind == kTensorCore) {
+    s->heads_per_cta = 8;
+  } else {
+    int gp = 2;
+    while (gp < G && gp < 8) gp <<= 1;
+    s->heads_per_cta = gp;
+  }
+  if (r.rope && s->kind == kCudaCore) {
+    *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
+    return kErrUnsupportedD;
+  }
+  s->gslices = (G + s->heads_per_cta - 1) / s->heads_per_cta;
+  s->tile_tokens = 16384 / (r.head_dim * (r.kv_dtype == kE4M3 ? 1 : 2));
+  return 0;
+}
+
+namespace {
+
+// The chunking of a batch.
+struct DecodeChunking {
+  int64_t C;   // chunk tokens (0 = whole rows)
+  bool equal;  // equal page-aligned parts of rows longer than C (heuristic), else multiples of C
+};
+
+int64_t chunks_of(const RowSpan& sp, int64_t C, bool equal) {
+  const int64_t a = sp.n - sp.w;
+  if (!equal) return fixed_chunks(sp, C);
+  if (sp.n == 0 || C == 0 || a <= C) return 1;
+  return (a + C - 1) / C;
+}
+
+// chunks of every row, the rows split in more than one, and their partial slots
+struct ChunkCounts {
+  int64_t chunks = 0, split = 0, slots = 0;
+};
+ChunkCounts count_chunks(const PlanRequest& r, int64_t C, bool equal) {
+  ChunkCounts c;
+  for (int row = 0; row < rows_of(r); ++row) {
+    const int64_t k = chunks_of(row_span(r, row), C, equal);
+    c.chunks += k;
+    if (k > 1) {
+      ++c.split;
+      c.slots += k;
+    }
+  }
+  return c;
+}
+
+// `slots` CTA slots on the GPU; `max_slots` > 0 bounds the partial slots (per unit).
+DecodeChunking choose_chunking(const PlanRequest& r, const DecodeSchedule& g, int64_t slots,
+                               int64_t max_slots) {
+  const int rows = rows_of(r);
+  const int64_t per_row = (int64_t)r.num_kv_heads * g.gslices;
+  const int ps = r.page_size;
+  if (r.disable_split_kv) return {0, false};
+  if (r.fixed_split_size > 0) return {(int64_t)r.fixed_split_size * ps, false};
+  int64_t total = 0, longest = 0;
+  for (int row = 0; row < rows; ++row) {
+    const RowSpan sp = row_span(r, row);
+    total += sp.n - sp.w;
+    longest = std::max(longest, sp.n - sp.w);
+  }
+  const int64_t c_min = (kMinChunk + ps - 1) / ps * ps;
+  const int64_t c_max = std::max(c_min, (longest + ps - 1) / ps * ps);
+  // the smallest page-aligned chunk in [lo, c_max] for which `fits` holds (fits(c_max) does)
+  auto smallest = [&](int64_t lo, auto fits) {
+    int64_t hi = c_max;
+    while (lo < hi) {
+      const int64_t mid = (lo / ps + (hi / ps - lo / ps) / 2) * ps;
+      if (fits(mid)) hi = mid; else lo = mid + ps;
+    }
+    return lo;
+  };
+  int64_t C;
+  if ((int64_t)rows * per_row <= slots) {
+    // the unsplit rows fit in one wave: split only as far as every CTA still starts at once
+    C = smallest(c_min, [&](int64_t c) {
+      return count_chunks(r, c, true).chunks * per_row <= slots;
+    });
+  } else {
+    // chunks of about the average load of a CTA slot
+    C = std::max<int64_t>(c_min, (total * per_row + slots - 1) / slots);
+    C = (C + ps - 1) / ps * ps;
+  }
+  if (C >= longest) return {0, true};
+  // bounded work lists (CUDA-graph capacity, partial-slot storage): the smallest larger chunk
+  // that fits them
+  auto fits_caps = [&](int64_t c) {
+    const ChunkCounts k = count_chunks(r, c, true);
+    return (r.max_items <= 0 || k.chunks <= r.max_items) &&
+           (max_slots <= 0 || k.slots * per_row <= max_slots);
+  };
+  if (!fits_caps(C)) C = smallest(C, fits_caps);
+  return {C >= longest ? 0 : C, true};
+}
+
+}  // namespace
+
+int decode_schedule_bounds(const PlanRequest& r, int ctas, int64_t max_slots,
+                           int64_t* max_tasks, int64_t* max_merges, const char** err) {
+  DecodeSchedule g;
+  int rc = decode_geometry(r, &g, err);
+  if (rc) return rc;
+  const int64_t per_row = (int64_t)r.num_kv_heads * g.gslices;
+  const DecodeChunking ch = choose_chunking(r, g, std::max(1, ctas), max_slots);
+  const ChunkCounts k = count_chunks(r, ch.C, ch.equal);
+  *max_tasks = k.chunks * per_row;
+  *max_merges = k.split * per_row;
+  *err = "";
+  return 0;
+}
+
+int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, const char** err) {
+  int rc = decode_geometry(r, s, err);
+  if (rc) return rc;
+  s->n_tasks = s->n_merges = s->n_slots = 0;
+  const int rows = rows_of(r);
+  const int ps = r.page_size;
+  const int hkv = r.num_kv_heads, gsl = s->gslices;
+  const int per_row = hkv * gsl;  // units of a row: one per (kv head, slice)
+  const DecodeChunking ch = choose_chunking(r, *s, std::max(1, ctas), s->max_slots);
+  const int64_t C = ch.C;
+  auto too_small = [&](const char* what) {
+    *err = what;
+    return kErrWorkspaceD;
+  };
+  if (r.max_items > 0 && rows > r.max_items)
+    return too_small("the batch has more query rows (requests x q_len_per_req) than the "
+                     "work-list capacity");
+
+  // one task per unit for chunk [b, e) of a row
+  auto emit_chunk = [&](int row, const RowSpan& sp, int64_t b, int64_t e, int64_t tile0) -> bool {
+    if (s->n_tasks + per_row > s->tasks_cap) return false;
+    for (int u = 0; u < per_row; ++u) {
+      DecodeTask& t = s->tasks[s->n_tasks++];
+      t.req = row;
+      t.page_base = sp.base;
+      t.chunk_tok0 = (int32_t)tile0;
+      t.tok_begin = (int32_t)b;
+      t.tok_end = (int32_t)e;
+      t.out_slot = -1;
+      t.merge_idx = -1;
+      t.q_pos = sp.n > 0 ? (int32_t)(sp.n - 1) : 0;
+      t.kvh = u / gsl;
+      t.gs = u % gsl;
+      t.cta = 0;
+      t.pad = (int32_t)(s->n_tasks - 1);  // emission order
+    }
+    return true;
+  };
+  for (int row = 0; row < rows; ++row) {
+    const RowSpan sp = row_span(r, row);
+    const int64_t first = s->n_tasks;
+    const int64_t k = chunks_of(sp, C, ch.equal);
+    bool ok = true;
+    if (sp.n == 0 || C == 0 || (k == 1 && ch.equal)) {
+      ok = emit_chunk(row, sp, sp.n == 0 ? 0 : sp.w, sp.n, sp.n == 0 ? 0 : sp.w / ps * ps);
+    } else if (!ch.equal) {
+      for (int64_t q = sp.w / C; ok && q <= (sp.n - 1) / C; ++q)
+        ok = emit_chunk(row, sp, std::max(q * C, sp.w), std::min((q + 1) * C, sp.n), q * C);
+    } else {
+      const int64_t a = sp.n - sp.w;
+      int64_t b = sp.w, tile0 = sp.w / ps * ps;
+      for (int64_t q = 1; ok && q <= k; ++q) {
+        const int64_t e = q == k ? sp.n : (sp.w + a * q / k) / ps * ps;
+        if (e <= b) continue;
+        ok = emit_chunk(row, sp, b, e, tile0);
+        b = e;
+        tile0 = e;
+      }
+    }
+    if (!ok)
+      return too_small(C > 0 && !ch.equal ? "fixed_split_size cuts this batch into more work "
+                                            "items than the work-list capacity"
+                                          : "work list full");
+    // the units of a split row: chunk q of unit u is task first + q * per_row + u; per unit,
+    // consecutive slots and a merge entry
+    const int64_t nk = (s->n_tasks - first) / per_row;
+    if (nk > 1) {
+      if (s->n_merges + per_row > s->merges_cap) return too_small("merge list full");
+      for (int u = 0; u < per_row; ++u) {
+        MergeEntry& m = s->merges[s->n_merges];
+        m.req = row;
+        m.first_slot = (int32_t)s->n_slots;
+        m.n_chunks = (int32_t)nk;
+        m.pad = u;
+        for (int64_t q = 0; q < nk; ++q) {
+          DecodeTask& t = s->tasks[first + q * per_row + u];
+          t.out_slot = (int32_t)(s->n_slots + q);
+          t.merge_idx = (int32_t)s->n_merges;
+        }
+        s->n_slots += nk;
+        ++s->n_merges;
+      }
+    }
+  }
+  if (r.max_items > 0 && s->n_tasks > (int64_t)r.max_items * per_row)
+    return too_small("fixed_split_size cuts this batch into more work items than the "
+                     "work-list capacity");
+  if (s->max_slots > 0 && s->n_slots > s->max_slots)
+    return too_small("split partials exceed the workspace");
+  // longest first, ties in emission order (a total order, so an in-place sort): the units of
+  // a chunk stay neighbours; task q runs on CTA q
+  std::sort(s->tasks, s->tasks + s->n_tasks, [](const DecodeTask& a, const DecodeTask& b) {
+    const int64_t ca = a.tok_end - a.tok_begin, cb = b.tok_end - b.tok_begin;
+    return ca != cb ? ca > cb : a.pad < b.pad;
+  });
+  for (int64_t q = 0; q < s->n_tasks; ++q) {
+    s->tasks[q].cta = (int32_t)q;
+    s->tasks[q].pad = 0;
   }
   *err = "";
   return 0;

@@ -262,6 +262,14 @@ class BatchDecodePagedKV:
         L.check(L.lib().pkd_check_status(self._h, ctypes.byref(v), _stream_ptr(stream)))
         return v.value
 
+    def plan_info(self) -> dict:
+        """The current plan's launch shape: grid (CTAs per launch), ctas_per_sm, tasks, merges."""
+        g, c = ctypes.c_int(), ctypes.c_int()
+        t, m = ctypes.c_int64(), ctypes.c_int64()
+        L.check(L.lib().pkd_plan_info(self._h, ctypes.byref(g), ctypes.byref(c), ctypes.byref(t),
+                                      ctypes.byref(m)))
+        return dict(grid=g.value, ctas_per_sm=c.value, tasks=t.value, merges=m.value)
+
     def set_wait_limit(self, limit_ns: int) -> None:
         """Limit of the decode kernel's pipeline waits for later runs, in ns (default and
         maximum 2e9); a wait that runs out sets STATUS_TIMEOUT and its CTA gives up."""
@@ -291,30 +299,32 @@ def plan_host(indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, head_
               disable_split_kv: bool = False, kv_dtype: int = L.DTYPE_F16,
               use_tensor_cores: int = L.KERNEL_AUTO, num_sms: int = 152,
               work_capacity: int = 0, q_len_per_req: int = 1):
-    """Run the host planner alone (no GPU): returns a dict with the work items
-    ``[n, 8]`` (request, first page index, chunk start, begin, end, slot, merge entry, 0), the merge
-    entries ``[m, 4]``, the slot count, the chosen kernel and the tile size.  ``work_capacity``
-    > 0 bounds the work list as CUDA-graph mode does."""
+    """Run the decode planner alone (no GPU): returns a dict with the tasks ``[n, 12]``
+    (row, first page index, chunk start, begin, end, slot, merge entry, query position,
+    kv head, slice, CTA, 0) grouped by CTA, the merge entries ``[m, 4]`` (row, first slot,
+    chunk count, unit), the slot count, the CTAs with work, the chosen kernel and the tile
+    size.  ``work_capacity`` > 0 bounds the work list as CUDA-graph mode does."""
     ip = _host_i32(indptr)
     lpl = _host_i32(last_page_len)
     batch = len(lpl)
-    n_items, n_merges, n_slots = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    kern, tile = ctypes.c_int(), ctypes.c_int()
+    n_tasks, n_merges, n_slots = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    kern, tile, n_ctas = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     args = (_i32p(ip), _i32p(lpl), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
             window_left, fixed_split_size, int(disable_split_kv), kv_dtype, use_tensor_cores,
             num_sms)
-    L.check(L.lib().pkd_plan_host(*args, None, 0, None, 0, ctypes.byref(n_items),
+    L.check(L.lib().pkd_plan_host(*args, None, 0, None, 0, ctypes.byref(n_tasks),
                                   ctypes.byref(n_merges), ctypes.byref(n_slots),
                                   ctypes.byref(kern), ctypes.byref(tile), int(work_capacity),
-                                  int(q_len_per_req)))
-    items = np.zeros((max(1, n_items.value), 8), dtype=np.int32)
+                                  int(q_len_per_req), ctypes.byref(n_ctas)))
+    tasks = np.zeros((max(1, n_tasks.value), 12), dtype=np.int32)
     merges = np.zeros((max(1, n_merges.value), 4), dtype=np.int32)
-    L.check(L.lib().pkd_plan_host(*args, _i32p(items), n_items.value, _i32p(merges),
-                                  n_merges.value, ctypes.byref(n_items), ctypes.byref(n_merges),
+    L.check(L.lib().pkd_plan_host(*args, _i32p(tasks), n_tasks.value, _i32p(merges),
+                                  n_merges.value, ctypes.byref(n_tasks), ctypes.byref(n_merges),
                                   ctypes.byref(n_slots), ctypes.byref(kern), ctypes.byref(tile),
-                                  int(work_capacity), int(q_len_per_req)))
-    return dict(items=items[:n_items.value], merges=merges[:n_merges.value],
-                num_slots=n_slots.value, kernel=kern.value, tile_tokens=tile.value)
+                                  int(work_capacity), int(q_len_per_req), ctypes.byref(n_ctas)))
+    return dict(tasks=tasks[:n_tasks.value], merges=merges[:n_merges.value],
+                num_slots=n_slots.value, num_ctas=n_ctas.value, kernel=kern.value,
+                tile_tokens=tile.value)
 
 
 def mla_graph_workspace_bytes(max_items: int, num_heads: int, backend: str = "auto"):

@@ -48,43 +48,58 @@ def test_create_without_device_fails_cleanly(pkd):
     assert L.lib().pkd_last_error().decode()
 
 
-def _check_partition(w, plan, C):
-    """Every request's attended tokens are covered exactly once, chunks start at multiples of C
-    from token 0, finals and partial slots agree with the merge list."""
-    items, merges = plan["items"], plan["merges"]
-    n = W.page_table  # noqa: F841  (lengths come from the workload)
-    by_req = {}
-    for it in items:
-        by_req.setdefault(int(it[0]), []).append(it)
-    merge_of = {int(m[0]): m for m in merges}
+def _units(plan):
+    """Tasks grouped by (row, kv head, slice), each group sorted by its first attended token."""
+    by_unit = {}
+    for t in plan["tasks"]:
+        by_unit.setdefault((int(t[0]), int(t[8]), int(t[9])), []).append(t)
+    return {k: sorted(v, key=lambda x: int(x[3])) for k, v in by_unit.items()}
+
+
+def _check_partition(w, plan, C, q_len=1):
+    """Every (row, kv head, slice) unit's attended tokens are covered exactly once by its
+    tasks; chunks start at page boundaries (at multiples of C from token 0 with a fixed split);
+    a unit of one task writes its final output, a split unit has consecutive partial slots and
+    one merge entry; the tasks are grouped by CTA."""
+    tasks, merges = plan["tasks"], plan["merges"]
+    G = w.num_qo_heads // w.num_kv_heads
+    hpc = 8 if plan["kernel"] == 1 else max(2, min(8, 1 << (G - 1).bit_length()))
+    gsl = (G + hpc - 1) // hpc
+    units = _units(plan)
+    rows = w.batch * q_len
+    assert sorted(units) == [(r, h, g) for r in range(rows) for h in range(w.num_kv_heads)
+                             for g in range(gsl)]
     slots = []
-    for i in range(w.batch):
-        L = int(w.kv_lens[i])
-        lo = 0 if w.window_left < 0 else max(0, L - 1 - w.window_left)
-        its = sorted(by_req[i], key=lambda x: x[3])
-        assert all(int(it[1]) == int(w.indptr[i]) for it in its)
-        if L == 0:
-            assert len(its) == 1 and its[0][3] == its[0][4] == 0 and its[0][5] == -1
+    for (row, kvh, gs), ts in units.items():
+        i, j = divmod(row, q_len)
+        n = max(0, int(w.kv_lens[i]) - (q_len - 1 - j))
+        lo = 0 if w.window_left < 0 else max(0, n - 1 - w.window_left)
+        assert all(int(t[1]) == int(w.indptr[i]) for t in ts)
+        if n == 0:
+            assert len(ts) == 1 and ts[0][3] == ts[0][4] == 0 and ts[0][5] == -1
             continue
-        assert int(its[0][3]) == lo and int(its[-1][4]) == L
-        for a, b in zip(its, its[1:]):
+        assert all(int(t[7]) == n - 1 for t in ts)
+        assert int(ts[0][3]) == lo and int(ts[-1][4]) == n
+        for a, b in zip(ts, ts[1:]):
             assert int(a[4]) == int(b[3])
-        for it in its:
-            c0, b0, e0 = int(it[2]), int(it[3]), int(it[4])
+        for t in ts:
+            c0, b0, e0 = int(t[2]), int(t[3]), int(t[4])
             assert c0 % w.page_size == 0 and c0 <= b0 < e0
             if C:
                 assert c0 % C == 0 and e0 - c0 <= C
-        if len(its) == 1:
-            assert its[0][5] == -1 and i not in merge_of and its[0][6] == -1
+        if len(ts) == 1:
+            assert ts[0][5] == -1 and ts[0][6] == -1
         else:
-            m = merge_of[i]
-            assert all(merges[int(it[6])][0] == i for it in its)
-            assert int(m[2]) == len(its)
-            assert [int(it[5]) for it in its] == list(range(int(m[1]), int(m[1]) + len(its)))
-            slots += [int(it[5]) for it in its]
+            m = merges[int(ts[0][6])]
+            assert all(int(t[6]) == int(ts[0][6]) for t in ts)
+            assert int(m[0]) == row and int(m[2]) == len(ts) and int(m[3]) == kvh * gsl + gs
+            assert [int(t[5]) for t in ts] == list(range(int(m[1]), int(m[1]) + len(ts)))
+            slots += [int(t[5]) for t in ts]
     assert sorted(slots) == list(range(plan["num_slots"]))
-    lens = items[:, 4] - items[:, 3]
-    assert np.all(np.diff(lens) <= 0), "items are launched longest first"
+    # one CTA per task, launched longest first
+    assert plan["num_ctas"] == len(tasks) and np.array_equal(tasks[:, 10], np.arange(len(tasks)))
+    lens = tasks[:, 4] - tasks[:, 3]
+    assert np.all(np.diff(lens) <= 0)
 
 
 @pytest.mark.parametrize("name", ["worked", "uniform", "lognormal", "long", "mix"])
@@ -96,8 +111,11 @@ def test_plan_partitions_every_workload(pkd, name):
                          kv_dtype={"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype])
     C = w.fixed_split_size * w.page_size
     _check_partition(w, plan, C)
-    if name == "long":
-        assert len(plan["items"]) == 4 * 8 and len(plan["merges"]) == 4
+    if name == "long":  # 4 requests x 8 chunks of 256 pages, per kv head
+        assert len(plan["tasks"]) == 4 * 8 * 8 and len(plan["merges"]) == 4 * 8
+    elif w.batch * w.num_kv_heads <= 304:
+        # the unsplit rows fit one wave of CTA slots: split only as far as one wave holds
+        assert len(plan["tasks"]) <= 304
 
 
 @pytest.mark.parametrize("fixed", [0, 1, 2, 7, 64])
@@ -111,7 +129,7 @@ def test_plan_modes(pkd, fixed, window):
     nosplit = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 8, window_left=window,
                             fixed_split_size=fixed, disable_split_kv=True)
     _check_partition(w, nosplit, 0)
-    assert len(nosplit["items"]) == len(lens) and len(nosplit["merges"]) == 0
+    assert len(nosplit["tasks"]) == len(lens) * 2 and len(nosplit["merges"]) == 0
 
 
 def test_fixed_split_is_batch_invariant(pkd):
@@ -121,9 +139,23 @@ def test_fixed_split_is_batch_invariant(pkd):
     for i in range(3):
         wi = W.custom([lens[i]], 8, 2, 128, 16)
         alone = pkd.plan_host(wi.indptr, wi.last_page_len, 8, 2, 128, 16, fixed_split_size=16)
-        mine = sorted((int(x[2]), int(x[3]), int(x[4])) for x in full["items"] if x[0] == i)
-        theirs = sorted((int(x[2]), int(x[3]), int(x[4])) for x in alone["items"])
+        mine = sorted((int(x[8]), int(x[2]), int(x[3]), int(x[4])) for x in full["tasks"]
+                      if x[0] == i)
+        theirs = sorted((int(x[8]), int(x[2]), int(x[3]), int(x[4])) for x in alone["tasks"])
         assert mine == theirs
+
+
+def test_one_wave_plan_cuts_a_long_row_into_equal_chunks(pkd):
+    """Rows that fit one wave of CTA slots unsplit: the longest is cut into equal page-aligned
+    chunks, as many as keep every CTA in that one wave."""
+    lens = [200000, 50, 3000, 7]
+    w = W.custom(lens, 8, 1, 128, 16)
+    plan = pkd.plan_host(w.indptr, w.last_page_len, 8, 1, 128, 16)
+    _check_partition(w, plan, 0)
+    assert 250 <= len(plan["tasks"]) <= 304
+    ts = plan["tasks"][plan["tasks"][:, 0] == 0]
+    lens0 = ts[:, 4] - ts[:, 3]
+    assert lens0.max() - lens0.min() <= 16
 
 
 def test_kernel_choice_and_tiles(pkd):
@@ -201,29 +233,30 @@ def test_work_capacity_bounds_the_plan(pkd, name):
         plan = pkd.plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads,
                              w.head_dim, w.page_size, window_left=w.window_left, kv_dtype=kv,
                              work_capacity=cap)
-        assert len(plan["items"]) <= cap
+        assert len(plan["tasks"]) <= cap * w.num_kv_heads
         _check_partition(w, plan, 0)
 
 
 def test_work_capacity_rejects_what_cannot_fit(pkd):
     from paged_kv_decode_23_gb300 import PkdError
-    w = W.workload("long")  # fixed split of 256 pages: 8 chunks per request, 32 items
+    w = W.workload("long")  # fixed split of 256 pages: 8 chunks per request, 32 in all
     with pytest.raises(PkdError) as e:
         pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, fixed_split_size=256,
                       kv_dtype=1, work_capacity=31)
     assert e.value.code == -3
     ok = pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, fixed_split_size=256,
                        kv_dtype=1, work_capacity=32)
-    assert len(ok["items"]) == 32
+    assert len(ok["tasks"]) == 32 * 8
     with pytest.raises(PkdError):  # more requests than items
         pkd.plan_host(w.indptr, w.last_page_len, 32, 8, 128, 64, work_capacity=3)
 
 
 def test_graph_workspace_bytes(pkd):
     fb, ib = pkd.graph_workspace_bytes(100, 32, 8, 128)
-    # 100 partial slots x 32 heads x 128 floats, their lses, and 100 items + 50 merges
-    assert fb >= 100 * 32 * 128 * 4 + 100 * 32 * 4
-    assert ib >= 256 + 50 * 8 * 4 + 100 * 32 + 50 * 16
+    # 100 chunks per row in all, per kv head: 800 tasks and slots of 8 heads x 128 floats (and
+    # their lses), 400 merge entries with their counters
+    assert fb >= 800 * 8 * 128 * 4 + 800 * 8 * 4
+    assert ib >= 256 + 400 * 4 + 800 * 48 + 400 * 16
 
 
 @pytest.mark.parametrize("q_len", [1, 2, 5])
@@ -236,25 +269,8 @@ def test_multi_token_rows_partition_their_causal_keys(pkd, q_len, mode):
     w = W.custom(lens, 8, 2, 128, 16, window_left=window)
     plan = pkd.plan_host(w.indptr, w.last_page_len, 8, 2, 128, 16, window_left=window,
                          q_len_per_req=q_len, **mode)
-    items = plan["items"]
-    by_row = {}
-    for it in items:
-        by_row.setdefault(int(it[0]), []).append(it)
-    assert sorted(by_row) == list(range(len(lens) * q_len))
-    for row, its in by_row.items():
-        i, j = divmod(row, q_len)
-        n = max(0, lens[i] - (q_len - 1 - j))
-        lo = 0 if window < 0 else max(0, n - 1 - window)
-        its = sorted(its, key=lambda x: x[3])
-        assert all(int(it[1]) == int(w.indptr[i]) for it in its)
-        if n == 0:
-            assert len(its) == 1 and its[0][3] == its[0][4] == 0
-            continue
-        assert int(its[0][3]) == lo and int(its[-1][4]) == n
-        for a, b in zip(its, its[1:]):
-            assert int(a[4]) == int(b[3])
-        if len(its) > 1:
-            assert plan["merges"][int(its[0][6])][0] == row
+    C = mode.get("fixed_split_size", 0) * 16
+    _check_partition(w, plan, C, q_len=q_len)
 
 
 def _mla_partition_ok(plan, kv_indptr, kv_lens):
