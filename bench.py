@@ -39,12 +39,12 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on: once the sources differ, the figure no longer describes the kernel and the line
 # reports null.
 MEASURED_TRAFFIC = {
-    "sources_sha256": "9f13d7fd6fec034fe6fe529e34c2066b5eff2f11ad2a8734e695319908c4a2bc",
+    "sources_sha256": "be14db61acbd145a60787bf5060a7a00433c5927e86f7188646f33712b72b7f6",
     # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set, bytes)
-    "uniform": 618490112.0,
-    "mix": 417738240.0,
-    "long": 2150562048.0,
-    "lognormal": 3525879808.0,
+    "uniform": 618817792.0,
+    "mix": 417762816.0,
+    "long": 2150523904.0,
+    "lognormal": 3525928704.0,
 }
 
 
