@@ -27,15 +27,15 @@ LAYOUT_NHD, LAYOUT_HND = 0, 1
 KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TENSOR_CORE = -1, 0, 1
 STATUS_TIMEOUT, STATUS_BAD_PAGE = 1, 2
 
-# every symbol include/pkd.h declares, with its ctypes signature
-_i32p = ctypes.POINTER(ctypes.c_int32)
+# every symbol include/pkd.h declares, with its ctypes signature (pointers, host or device, pass
+# as addresses)
 _vp = ctypes.c_void_p
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _c_int, _c_float, _c_size = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "pkd_create": (_c_int, [ctypes.POINTER(_vp), _vp, _c_size, _vp, _c_size, _c_int]),
     "pkd_reset_workspace": (_c_int, [_vp, _vp, _c_size, _vp, _c_size]),
-    "pkd_plan": (_c_int, [_vp, _i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int, _c_int,
+    "pkd_plan": (_c_int, [_vp, _vp, _vp, _c_int, _vp, ctypes.c_int64, _c_int, _c_int, _c_int,
                           _c_int, _c_float, _c_float, _c_int, _c_int, _c_int, _c_int, _c_int,
                           _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _vp]),
     "pkd_run": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, _i64p, _c_float, _c_float, _c_float,
@@ -44,11 +44,11 @@ SIGNATURES = {
                                _c_float, _vp, _vp, _vp, _vp, _vp]),
     "pkd_destroy": (_c_int, [_vp]),
     "pkd_last_error": (ctypes.c_char_p, []),
-    "pkd_workspace_bytes": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+    "pkd_workspace_bytes": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
-    "pkd_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                               _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _c_int, _i32p,
+    "pkd_plan_host": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                               _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
                                _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(_c_int), _c_int, _c_int, ctypes.POINTER(_c_int)]),
@@ -57,14 +57,14 @@ SIGNATURES = {
     "pkd_set_wait_limit": (_c_int, [_vp, ctypes.c_uint64]),
     "pkd_plan_info": (_c_int, [_vp, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
-    "pkd_check_page_table": (_c_int, [_i32p, _c_int, _i32p, ctypes.c_int64, ctypes.c_int64]),
+    "pkd_check_page_table": (_c_int, [_vp, _c_int, _vp, ctypes.c_int64, ctypes.c_int64]),
     "pkd_mla_set_backend": (_c_int, [_vp, _c_int]),
-    "pkd_mla_plan_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                   _i32p, _c_int, _i32p, _c_int, ctypes.POINTER(_c_int),
+    "pkd_mla_plan_host": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _vp, _c_int, _vp, _c_int, ctypes.POINTER(_c_int),
                                    ctypes.POINTER(_c_int), ctypes.POINTER(_c_int),
                                    ctypes.POINTER(_c_int), ctypes.POINTER(_c_size),
                                    ctypes.POINTER(_c_size)]),
-    "pkd_mla_plan": (_c_int, [_vp, _i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
+    "pkd_mla_plan": (_c_int, [_vp, _vp, _vp, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
                               _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _vp]),
     "pkd_mla_run": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _c_int, _vp,
                              _vp, _vp]),
@@ -73,7 +73,7 @@ SIGNATURES = {
                                                ctypes.POINTER(_c_size)]),
     "pkd_graph_workspace_bytes": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
                                            ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
-    "pkd_decode_noalloc": (_c_int, [_i32p, _i32p, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
+    "pkd_decode_noalloc": (_c_int, [_vp, _vp, _c_int, _vp, ctypes.c_int64, _c_int, _c_int,
                                     _c_int, _c_int, _c_float, _c_float, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                     ctypes.c_int64, _i64p, _c_float, _c_float, _c_float, _vp,

@@ -112,6 +112,7 @@ int na_setup(int dev) {
 // ---------------------------------------------------------------- static host plan storage
 DecodeTask g_na_tasks[PKD_NOALLOC_MAX_ITEMS];
 MergeEntry g_na_merges[PKD_NOALLOC_MAX_MERGES];
+DecodeChunk g_na_chunks[PKD_NOALLOC_MAX_ITEMS];  // planner scratch
 
 // ---------------------------------------------------------------- tensor maps
 typedef CUresult (*NaEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -258,6 +259,8 @@ extern "C" int pkd_decode_noalloc(const int32_t* indptr_host, const int32_t* las
   sch.tasks_cap = PKD_NOALLOC_MAX_ITEMS;
   sch.merges = g_na_merges;
   sch.merges_cap = PKD_NOALLOC_MAX_MERGES;
+  sch.chunks = g_na_chunks;
+  sch.chunks_cap = PKD_NOALLOC_MAX_ITEMS;
   // partial slots: kSlotHeads rows of head_dim + 1 floats each, in the partials region
   sch.max_slots = (int64_t)((PKD_NOALLOC_PARTIAL_BYTES - 512) /
                             ((size_t)kSlotHeads * (head_dim + 1) * sizeof(float)));

@@ -126,10 +126,24 @@ struct pkd_handle {
 
   // The decode plan: tasks grouped by CTA, merge entries, CTA ranges, and the grid that runs
   // them (CUDA-graph mode: fixed by the first plan).
-  std::vector<DecodeTask> tasks;
-  std::vector<MergeEntry> dmerges;
+  std::vector<DecodeTask> tasks;     // the plan's tasks (the first n_tasks entries)
+  std::vector<MergeEntry> dmerges;   // its merge entries (the first n_merges)
+  std::vector<DecodeChunk> dchunks;  // planner scratch
   DecodeWsLayout dlayout{};
+  int64_t n_dmerges = 0;
   int grid = 0;       // CTAs pkd_run launches (one per task; CUDA-graph mode: the capacity)
+  // K / V tensor maps of the pools runs have used, so a run on a pool seen before (every layer
+  // of every later step) skips the encoding: a map depends only on these fields
+  struct TmapEntry {
+    const void* base;
+    int64_t num_pages;
+    int64_t strides[3];
+    int kv_dtype, head_dim, page_size, num_kv_heads, layout, box_rows;
+    CUtensorMap map;
+  };
+  static constexpr size_t kTmapCacheSize = 256;
+  std::vector<TmapEntry> tmaps;
+  size_t tmap_next = 0;
   int gslices = 1;
   int64_t n_tasks = 0;
 
@@ -316,25 +330,27 @@ int decode_ctas_per_sm(const DecodeKernel* k, int device, int* out) {
 struct ScheduleStore {
   std::vector<DecodeTask> tasks;
   std::vector<MergeEntry> merges;
+  std::vector<DecodeChunk> chunks;
 };
 
-// Plans the batch (the GPU holding `ctas` CTAs at once) into `st`; *s holds the counts.
+// Plans the batch (the GPU holding `ctas` CTAs at once) into `st`, growing its vectors when a
+// plan needs more; *s holds the counts.
 int plan_decode(const PlanRequest& r, int ctas, ScheduleStore& st, DecodeSchedule* s) {
   const char* err = "";
-  int64_t max_tasks = 0, max_merges = 0;
-  int rc = decode_schedule_bounds(r, ctas, s->max_slots, &max_tasks, &max_merges, &err);
-  if (rc) return fail(rc, err);
-  st.tasks.resize((size_t)std::max<int64_t>(1, max_tasks));
-  st.merges.resize((size_t)std::max<int64_t>(1, max_merges));
-  s->tasks = st.tasks.data();
-  s->tasks_cap = max_tasks;
-  s->merges = st.merges.data();
-  s->merges_cap = max_merges;
-  rc = build_decode_schedule(r, ctas, s, &err);
-  if (rc) return fail(rc, err);
-  st.tasks.resize((size_t)s->n_tasks);
-  st.merges.resize((size_t)s->n_merges);
-  return PKD_OK;
+  for (int attempt = 0;; ++attempt) {
+    s->tasks = st.tasks.data();
+    s->tasks_cap = (int64_t)st.tasks.size();
+    s->merges = st.merges.data();
+    s->merges_cap = (int64_t)st.merges.size();
+    s->chunks = st.chunks.data();
+    s->chunks_cap = (int64_t)st.chunks.size();
+    const int rc = build_decode_schedule(r, ctas, s, &err);
+    if (rc == 0) return PKD_OK;
+    if (!s->storage_short || attempt > 0) return fail(rc, err);
+    st.tasks.resize((size_t)std::max<int64_t>(s->n_tasks, (int64_t)st.tasks.size()));
+    st.merges.resize((size_t)std::max<int64_t>(s->n_merges, (int64_t)st.merges.size()));
+    st.chunks.resize((size_t)std::max<int64_t>(s->n_chunks, (int64_t)st.chunks.size()));
+  }
 }
 
 }  // namespace
@@ -433,11 +449,12 @@ int pkd_plan_host(const int32_t* indptr_host, const int32_t* last_page_len_host,
   if (n_ctas) *n_ctas = (int)sch.n_tasks;
   if (tasks_out)
     std::memcpy(tasks_out, st.tasks.data(),
-                sizeof(DecodeTask) * std::min<size_t>(st.tasks.size(), (size_t)std::max(0, max_tasks)));
+                sizeof(DecodeTask) *
+                    std::min<size_t>((size_t)sch.n_tasks, (size_t)std::max(0, max_tasks)));
   if (merges_out)
     std::memcpy(merges_out, st.merges.data(),
                 sizeof(MergeEntry) *
-                    std::min<size_t>(st.merges.size(), (size_t)std::max(0, max_merges)));
+                    std::min<size_t>((size_t)sch.n_merges, (size_t)std::max(0, max_merges)));
   g_last_error.clear();
   return PKD_OK;
 }
@@ -533,9 +550,11 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   ScheduleStore st;
   st.tasks.swap(h->tasks);
   st.merges.swap(h->dmerges);
+  st.chunks.swap(h->dchunks);
   rc = plan_decode(r, ctas, st, &sch);
   st.tasks.swap(h->tasks);
   st.merges.swap(h->dmerges);
+  st.chunks.swap(h->dchunks);
   if (rc) return rc;
   // one CTA per task; CUDA-graph mode launches the capacity's grid for every plan and the CTAs
   // past a plan's tasks leave at once
@@ -624,6 +643,7 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (int rc2 = staging_release(h, slot, s)) return rc2;
 
   h->n_tasks = sch.n_tasks;
+  h->n_dmerges = sch.n_merges;
   h->gslices = sch.gslices;
   h->grid = grid;
   h->batch = batch;
@@ -647,6 +667,39 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   g_last_error.clear();
   return PKD_OK;
 }
+
+}  // extern "C"
+
+namespace {
+
+// make_kv_tensor_map through the handle's cache of maps.
+int cached_kv_tensor_map(pkd_handle* h, CUtensorMap* map, const void* base, int64_t num_pages,
+                         const int64_t strides[3], int box_rows) {
+  for (const auto& t : h->tmaps)
+    if (t.base == base && t.num_pages == num_pages && t.strides[0] == strides[0] &&
+        t.strides[1] == strides[1] && t.strides[2] == strides[2] && t.kv_dtype == h->kv_dtype &&
+        t.head_dim == h->head_dim && t.page_size == h->page_size &&
+        t.num_kv_heads == h->num_kv_heads && t.layout == h->layout && t.box_rows == box_rows) {
+      *map = t.map;
+      return PKD_OK;
+    }
+  int rc = make_kv_tensor_map(map, base, h->kv_dtype, h->head_dim, h->page_size,
+                              h->num_kv_heads, num_pages, strides, h->layout, box_rows);
+  if (rc) return rc;
+  pkd_handle::TmapEntry e{base, num_pages, {strides[0], strides[1], strides[2]}, h->kv_dtype,
+                          h->head_dim, h->page_size, h->num_kv_heads, h->layout, box_rows, *map};
+  if (h->tmaps.size() < pkd_handle::kTmapCacheSize) {
+    h->tmaps.push_back(e);
+  } else {
+    h->tmaps[h->tmap_next] = e;
+    h->tmap_next = (h->tmap_next + 1) % pkd_handle::kTmapCacheSize;
+  }
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
 
 int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* v_base,
                   int64_t num_pages, const int64_t kv_strides[3], float q_scale, float k_scale,
@@ -681,11 +734,9 @@ int pkd_run_timed(pkd_handle* h, const void* q, const void* k_base, const void* 
   std::memset(&prm, 0, sizeof prm);
   const int tile = h->kernel->tile_tokens;
   const int box_rows = h->page_size < tile ? h->page_size : tile;
-  int rc = make_kv_tensor_map(&prm.tmap_k, k_base, h->kv_dtype, h->head_dim, h->page_size,
-                              h->num_kv_heads, num_pages, kv_strides, h->layout, box_rows);
+  int rc = cached_kv_tensor_map(h, &prm.tmap_k, k_base, num_pages, kv_strides, box_rows);
   if (rc) return rc;
-  rc = make_kv_tensor_map(&prm.tmap_v, v_base, h->kv_dtype, h->head_dim, h->page_size,
-                          h->num_kv_heads, num_pages, kv_strides, h->layout, box_rows);
+  rc = cached_kv_tensor_map(h, &prm.tmap_v, v_base, num_pages, kv_strides, box_rows);
   if (rc) return rc;
 
   char* iws = static_cast<char*>(h->int_ws);
@@ -1070,7 +1121,7 @@ int pkd_plan_info(pkd_handle* h, int* grid, int* ctas_per_sm, int64_t* n_tasks,
   if (grid) *grid = h->grid;
   if (ctas_per_sm) *ctas_per_sm = per_sm;
   if (n_tasks) *n_tasks = h->n_tasks;
-  if (n_merges) *n_merges = (int64_t)h->dmerges.size();
+  if (n_merges) *n_merges = h->n_dmerges;
   return PKD_OK;
 }
 

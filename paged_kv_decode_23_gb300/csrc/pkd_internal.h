@@ -217,25 +217,32 @@ int build_plan(const PlanRequest& r, Plan* plan, const char** err);
 // ----------------------------------------------------------------------- decode schedule
 // The decode planner's output, written into storage the caller provides (it allocates
 // nothing: the no-allocation entry point passes static arrays, the handle path vectors).
+// One chunk of one row: [b, e) of its attended tokens (tiles from tile0), chunk q of k; when
+// the row is split (k > 1), unit u of the row takes partial slots slot_base + u k .. + k - 1 and
+// merge entry merge_base + u.
+struct DecodeChunk {
+  int32_t row, b, e, tile0, q, k, slot_base, merge_base;
+};
+
 struct DecodeSchedule {
   DecodeTask* tasks = nullptr;  // capacity tasks_cap; task q runs on CTA q (longest first)
   int64_t tasks_cap = 0;
   MergeEntry* merges = nullptr;  // capacity merges_cap; {row, first slot, chunks, unit}
   int64_t merges_cap = 0;
-
+  DecodeChunk* chunks = nullptr;  // scratch, capacity chunks_cap
+  int64_t chunks_cap = 0;
   int64_t max_slots = 0;         // > 0: at most this many partial slots
   // results
-  int64_t n_tasks = 0, n_merges = 0, n_slots = 0;
+  int64_t n_tasks = 0, n_merges = 0, n_slots = 0, n_chunks = 0;
+  // set with PKD_ERR_WORKSPACE_TOO_SMALL when only the storage above was too small: the
+  // counts then hold what the plan needs, and a call with that much storage succeeds
+  bool storage_short = false;
   int kind = kTensorCore, heads_per_cta = 8, gslices = 1, tile_tokens = 64;
 };
 
 // Kernel geometry a decode plan implies (kind, heads per CTA, slices, tile) and validation of
 // the request.  Returns 0 or a PKD_ERR_* code with a message in *err.
 int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err);
-// The tasks and merge entries build_decode_schedule emits when the GPU holds `ctas` CTAs at
-// once (max_slots > 0: at most that many partial slots).
-int decode_schedule_bounds(const PlanRequest& r, int ctas, int64_t max_slots,
-                           int64_t* max_tasks, int64_t* max_merges, const char** err);
 // Cuts every row's attended tokens into tasks per (kv head, slice), one per CTA, longest first.
 int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, const char** err);
 

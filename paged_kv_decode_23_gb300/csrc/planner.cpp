@@ -522,30 +522,15 @@ DecodeChunking choose_chunking(const PlanRequest& r, const DecodeSchedule& g, in
 
 }  // namespace
 
-int decode_schedule_bounds(const PlanRequest& r, int ctas, int64_t max_slots,
-                           int64_t* max_tasks, int64_t* max_merges, const char** err) {
-  DecodeSchedule g;
-  int rc = decode_geometry(r, &g, err);
-  if (rc) return rc;
-  const int64_t per_row = (int64_t)r.num_kv_heads * g.gslices;
-  const DecodeChunking ch = choose_chunking(r, g, std::max(1, ctas), max_slots);
-  const ChunkCounts k = count_chunks(r, ch.C, ch.equal);
-  *max_tasks = k.chunks * per_row;
-  *max_merges = k.split * per_row;
-  *err = "";
-  return 0;
-}
-
 int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, const char** err) {
   int rc = decode_geometry(r, s, err);
   if (rc) return rc;
-  s->n_tasks = s->n_merges = s->n_slots = 0;
+  s->n_tasks = s->n_merges = s->n_slots = s->n_chunks = 0;
+  s->storage_short = false;
   const int rows = rows_of(r);
   const int ps = r.page_size;
-  const int hkv = r.num_kv_heads, gsl = s->gslices;
-  const int per_row = hkv * gsl;  // units of a row: one per (kv head, slice)
-  const DecodeChunking ch = choose_chunking(r, *s, std::max(1, ctas), s->max_slots);
-  const int64_t C = ch.C;
+  const int gsl = s->gslices;
+  const int per_row = r.num_kv_heads * gsl;  // units of a row: one per (kv head, slice)
   auto too_small = [&](const char* what) {
     *err = what;
     return kErrWorkspaceD;
@@ -553,88 +538,96 @@ int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, con
   if (r.max_items > 0 && rows > r.max_items)
     return too_small("the batch has more query rows (requests x q_len_per_req) than the "
                      "work-list capacity");
+  const DecodeChunking ch = choose_chunking(r, *s, std::max(1, ctas), s->max_slots);
+  const int64_t C = ch.C;
 
-  // one task per unit for chunk [b, e) of a row
-  auto emit_chunk = [&](int row, const RowSpan& sp, int64_t b, int64_t e, int64_t tile0) -> bool {
-    if (s->n_tasks + per_row > s->tasks_cap) return false;
-    for (int u = 0; u < per_row; ++u) {
-      DecodeTask& t = s->tasks[s->n_tasks++];
-      t.req = row;
-      t.page_base = sp.base;
-      t.chunk_tok0 = (int32_t)tile0;
-      t.tok_begin = (int32_t)b;
-      t.tok_end = (int32_t)e;
-      t.out_slot = -1;
-      t.merge_idx = -1;
-      t.q_pos = sp.n > 0 ? (int32_t)(sp.n - 1) : 0;
-      t.kvh = u / gsl;
-      t.gs = u % gsl;
-      t.cta = 0;
-      t.pad = (int32_t)(s->n_tasks - 1);  // emission order
-    }
-    return true;
+  // 1. every row's chunks, its slots and merge entries (row order)
+  int64_t n_chunks = 0, n_slots = 0, n_merges = 0;
+  auto add_chunk = [&](int row, int64_t b, int64_t e, int64_t tile0, int64_t q, int64_t k,
+                       int64_t slot_base, int64_t merge_base) {
+    if (n_chunks < s->chunks_cap)
+      s->chunks[n_chunks] = {row, (int32_t)b, (int32_t)e, (int32_t)tile0, (int32_t)q,
+                             (int32_t)k, (int32_t)slot_base, (int32_t)merge_base};
+    ++n_chunks;
   };
   for (int row = 0; row < rows; ++row) {
     const RowSpan sp = row_span(r, row);
-    const int64_t first = s->n_tasks;
     const int64_t k = chunks_of(sp, C, ch.equal);
-    bool ok = true;
+    const int64_t slot_base = n_slots, merge_base = n_merges;
+    if (k > 1) {
+      for (int u = 0; u < per_row; ++u) {
+        if (n_merges < s->merges_cap)
+          s->merges[n_merges] = {row, (int32_t)(slot_base + u * k), (int32_t)k, u};
+        ++n_merges;
+      }
+      n_slots += per_row * k;
+    }
     if (sp.n == 0 || C == 0 || (k == 1 && ch.equal)) {
-      ok = emit_chunk(row, sp, sp.n == 0 ? 0 : sp.w, sp.n, sp.n == 0 ? 0 : sp.w / ps * ps);
+      add_chunk(row, sp.n == 0 ? 0 : sp.w, sp.n, sp.n == 0 ? 0 : sp.w / ps * ps, 0, 1, slot_base,
+                merge_base);
     } else if (!ch.equal) {
-      for (int64_t q = sp.w / C; ok && q <= (sp.n - 1) / C; ++q)
-        ok = emit_chunk(row, sp, std::max(q * C, sp.w), std::min((q + 1) * C, sp.n), q * C);
+      // multiples of C counted from token 0
+      int64_t q = 0;
+      for (int64_t m = sp.w / C; m <= (sp.n - 1) / C; ++m, ++q)
+        add_chunk(row, std::max(m * C, sp.w), std::min((m + 1) * C, sp.n), m * C, q, k,
+                  slot_base, merge_base);
     } else {
+      // k equal page-aligned parts, so no short remainder chunk launches last
       const int64_t a = sp.n - sp.w;
-      int64_t b = sp.w, tile0 = sp.w / ps * ps;
-      for (int64_t q = 1; ok && q <= k; ++q) {
-        const int64_t e = q == k ? sp.n : (sp.w + a * q / k) / ps * ps;
+      int64_t b = sp.w, tile0 = sp.w / ps * ps, q = 0;
+      for (int64_t m = 1; m <= k; ++m) {
+        const int64_t e = m == k ? sp.n : (sp.w + a * m / k) / ps * ps;
         if (e <= b) continue;
-        ok = emit_chunk(row, sp, b, e, tile0);
+        add_chunk(row, b, e, tile0, q++, k, slot_base, merge_base);
         b = e;
         tile0 = e;
       }
     }
-    if (!ok)
-      return too_small(C > 0 && !ch.equal ? "fixed_split_size cuts this batch into more work "
-                                            "items than the work-list capacity"
-                                          : "work list full");
-    // the units of a split row: chunk q of unit u is task first + q * per_row + u; per unit,
-    // consecutive slots and a merge entry
-    const int64_t nk = (s->n_tasks - first) / per_row;
-    if (nk > 1) {
-      if (s->n_merges + per_row > s->merges_cap) return too_small("merge list full");
-      for (int u = 0; u < per_row; ++u) {
-        MergeEntry& m = s->merges[s->n_merges];
-        m.req = row;
-        m.first_slot = (int32_t)s->n_slots;
-        m.n_chunks = (int32_t)nk;
-        m.pad = u;
-        for (int64_t q = 0; q < nk; ++q) {
-          DecodeTask& t = s->tasks[first + q * per_row + u];
-          t.out_slot = (int32_t)(s->n_slots + q);
-          t.merge_idx = (int32_t)s->n_merges;
-        }
-        s->n_slots += nk;
-        ++s->n_merges;
-      }
-    }
   }
-  if (r.max_items > 0 && s->n_tasks > (int64_t)r.max_items * per_row)
+  const int64_t n_tasks = n_chunks * per_row;
+  if (r.max_items > 0 && n_chunks > r.max_items)
     return too_small("fixed_split_size cuts this batch into more work items than the "
                      "work-list capacity");
-  if (s->max_slots > 0 && s->n_slots > s->max_slots)
+  if (s->max_slots > 0 && n_slots > s->max_slots)
     return too_small("split partials exceed the workspace");
-  // longest first, ties in emission order (a total order, so an in-place sort): the units of
-  // a chunk stay neighbours; task q runs on CTA q
-  std::sort(s->tasks, s->tasks + s->n_tasks, [](const DecodeTask& a, const DecodeTask& b) {
-    const int64_t ca = a.tok_end - a.tok_begin, cb = b.tok_end - b.tok_begin;
-    return ca != cb ? ca > cb : a.pad < b.pad;
-  });
-  for (int64_t q = 0; q < s->n_tasks; ++q) {
-    s->tasks[q].cta = (int32_t)q;
-    s->tasks[q].pad = 0;
+  if (n_chunks > s->chunks_cap || n_tasks > s->tasks_cap || n_merges > s->merges_cap) {
+    s->storage_short = true;
+    s->n_chunks = n_chunks;
+    s->n_tasks = n_tasks;
+    s->n_merges = n_merges;
+    s->n_slots = n_slots;
+    return too_small(n_merges > s->merges_cap ? "merge list full" : "work list full");
   }
+  // 2. chunks longest first, ties in row and chunk order (a total order, so an in-place sort)
+  std::sort(s->chunks, s->chunks + n_chunks, [](const DecodeChunk& x, const DecodeChunk& y) {
+    const int32_t lx = x.e - x.b, ly = y.e - y.b;
+    if (lx != ly) return lx > ly;
+    return x.row != y.row ? x.row < y.row : x.q < y.q;
+  });
+  // 3. one task per unit of each chunk, the units of a chunk neighbours; task q runs on CTA q
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const DecodeChunk& ck = s->chunks[c];
+    const RowSpan sp = row_span(r, ck.row);
+    for (int u = 0; u < per_row; ++u) {
+      DecodeTask& t = s->tasks[c * per_row + u];
+      t.req = ck.row;
+      t.page_base = sp.base;
+      t.chunk_tok0 = ck.tile0;
+      t.tok_begin = ck.b;
+      t.tok_end = ck.e;
+      t.out_slot = ck.k > 1 ? ck.slot_base + u * ck.k + ck.q : -1;
+      t.merge_idx = ck.k > 1 ? ck.merge_base + u : -1;
+      t.q_pos = sp.n > 0 ? (int32_t)(sp.n - 1) : 0;
+      t.kvh = u / gsl;
+      t.gs = u % gsl;
+      t.cta = (int32_t)(c * per_row + u);
+      t.pad = 0;
+    }
+  }
+  s->n_chunks = n_chunks;
+  s->n_tasks = n_tasks;
+  s->n_merges = n_merges;
+  s->n_slots = n_slots;
   *err = "";
   return 0;
 }

@@ -30,14 +30,21 @@ def _as_dtype(x):
 
 
 def _host_i32(t) -> np.ndarray:
+    """A contiguous host int32 array of `t` (no copy when it already is one)."""
     if isinstance(t, torch.Tensor):
-        t = t.detach().to("cpu")
-        return np.ascontiguousarray(t.numpy().astype(np.int32, copy=False))
-    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+        if t.device.type != "cpu":
+            t = t.to("cpu")
+        a = t.detach().numpy()
+    else:
+        a = np.asarray(t)
+    if a.dtype != np.int32 or not a.flags.c_contiguous:
+        a = np.ascontiguousarray(a, dtype=np.int32)
+    return a
 
 
-def _i32p(a: np.ndarray):
-    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+def _i32p(a: np.ndarray) -> int:
+    """The address of a contiguous int32 array, for a pointer argument of the C ABI."""
+    return a.ctypes.data
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
