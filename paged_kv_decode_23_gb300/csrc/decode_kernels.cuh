@@ -59,6 +59,25 @@ struct DecodeGeom {
   static_assert(EPI_BYTES <= PIPE_BYTES, "the epilogue's image fits in the pipeline stages");
 };
 
+// Shared memory of the ROPE_LLAMA kernels, after the pipeline stages.  A "pair" is two
+// consecutive rotation frequencies of one lane's MMA operand slots (D/4 pairs); an entry is
+// their two phasors as {cos half2, sin half2} (8 bytes).
+//   R: 16 rows j of D/4 entries: the rotation by tok(j) * rate, where tok(j) is the token (in
+//      the warp's 16-token slice) that S^T row j holds.  Built once per CTA.
+//   E: per consumer warp, two buffers of D/4 entries: the rotation by (q_pos - t_w) * rate
+//      for the warp's current slice starting at token t_w.  Rebuilt every tile.
+// RoPE's score depends only on the difference of the two positions, so q rotated by
+// (q_pos - t_w) and the key of slice row j rotated by tok(j) give the logit of the key at
+// t_w + tok(j): the per-tile angles are the warp's, not each token's.
+template <int D, int NW>
+struct RopeGeom {
+  static constexpr int PAIRS = D / 4;
+  static constexpr int ROW = PAIRS * 8;  // bytes of an R row or an E buffer
+  static constexpr int R_BYTES = 16 * ROW;
+  static constexpr int BYTES = R_BYTES + NW * 2 * ROW;
+  static_assert(ROW >= 128, "the row swizzle flips bit 6 of an offset inside the row");
+};
+
 struct BlockCoords {
   DecodeTask it;
   int kvh;    // kv head
@@ -328,34 +347,59 @@ __device__ __forceinline__ float alibi_slope(const DecodeParams& p, int qo_head)
   return p.alibi ? __ldg(p.pos_table + 2 * D + qo_head) : 0.f;
 }
 
-// RoPE angle of dims i and i+1 at positions t (row a) and t + 8 (row b), as cos / sin: the
-// row-a angles come reduced from rope_sincos; row b's follow by the fixed rotation by 8 * rate
-// (cos and sin of it from the table: rate entry = {rate hi, rate lo, cos 8 rate, sin 8 rate}).
-struct RopeCS {
-  float c[2][2], s[2][2];  // [row a | row b][dim i | i+1]
-};
-__device__ __forceinline__ RopeCS rope_cs(float t, float4 ri, float4 rj) {
-  using namespace dev;
-  RopeCS r;
-  rope_sincos(t, ri.x, ri.y, r.s[0][0], r.c[0][0]);
-  rope_sincos(t, rj.x, rj.y, r.s[0][1], r.c[0][1]);
-  r.c[1][0] = r.c[0][0] * ri.z - r.s[0][0] * ri.w;
-  r.s[1][0] = r.s[0][0] * ri.z + r.c[0][0] * ri.w;
-  r.c[1][1] = r.c[0][1] * rj.z - r.s[0][1] * rj.w;
-  r.s[1][1] = r.s[0][1] * rj.z + r.c[0][1] * rj.w;
-  return r;
+// ROPE_LLAMA rotation pairs.  Pair P (of D/4) is slot pair P % 2 of k-step block P / 2 =
+// kk * 4 + tig: lane tig's MMA k slots {2tig, 2tig+1} (pair 0) or {2tig+8, 2tig+9} (pair 1) of
+// k step kk < D/32, which hold dims f, f + 1, and in k step kk + D/32 their rotation partners
+// f + D/2, f + D/2 + 1.  PERM: the e4m3 slot order (four consecutive dims per lane).
+template <bool PERM>
+__device__ __forceinline__ int rope_pair_freq(int P) {
+  const int blk = P >> 1, h = P & 1, kk = blk >> 2, tig = blk & 3;
+  return PERM ? kk * 16 + tig * 4 + 2 * h : kk * 16 + tig * 2 + 8 * h;
 }
 
-// ROPE_LLAMA on a 16-bit pair held in registers: lo holds dims (i, i+1) and hi the partner
-// dims (i + D/2, i + D/2 + 1) of one token (row 0 or 1 of cs).  x' = x cos a - y sin a,
-// y' = y cos a + x sin a, rounded to fp16.
-template <typename TIN>
-__device__ __forceinline__ void rope_pair(uint32_t& lo, uint32_t& hi, const RopeCS& cs, int row) {
+// Table entry of the rotation by t * rate for dims f and f + 1: {cos of both, sin of both} as
+// fp16 pairs.  rates[f] = {rate hi, rate lo}.
+__device__ __forceinline__ uint2 rope_entry(float t, const float2* rates, int f) {
   using namespace dev;
-  const float2 x = unpack2<TIN>(lo), y = unpack2<TIN>(hi);
-  const float c0 = cs.c[row][0], s0 = cs.s[row][0], c1 = cs.c[row][1], s1 = cs.s[row][1];
-  lo = pack2<__half>(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
-  hi = pack2<__half>(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
+  const float2 r0 = __ldg(rates + f), r1 = __ldg(rates + f + 1);
+  float s0, c0, s1, c1;
+  rope_sincos(t, r0.x, r0.y, s0, c0);
+  rope_sincos(t, r1.x, r1.y, s1, c1);
+  return make_uint2(pack2<__half>(c0, c1), pack2<__half>(s0, s1));
+}
+
+// Byte offset of pair P's entry in R row j.  The lanes of one shared-memory phase read rows
+// j and j + 1 (g_row 2m and 2m + 1) at the same pairs, so odd rows swap the 64-byte halves of
+// every 128 bytes.
+template <int D>
+__device__ __forceinline__ uint32_t rope_r_off(int j, int P) {
+  return (uint32_t)(j * (D / 4) * 8 + (((P >> 1) * 16) ^ ((j & 1) << 6)) + (P & 1) * 8);
+}
+
+__device__ __forceinline__ void sts_v2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// A warp's E buffer for its slice starting at token t_w: the rotation by (q_pos - t_w) * rate,
+// entry P at byte 8P.  Followed by __syncwarp: every lane reads every lane's entries.
+template <int D, bool PERM>
+__device__ __forceinline__ void rope_build_e(uint32_t ebuf, const float2* rates, float dt, int lane) {
+#pragma unroll
+  for (int P = lane; P < D / 4; P += 32) sts_v2(ebuf + P * 8, rope_entry(dt, rates, rope_pair_freq<PERM>(P)));
+  __syncwarp();
+}
+
+// ROPE_LLAMA on a K fragment register pair: x holds two dims of a token, y their partners
+// (+ D/2), both fp16 after the widening; (c, s) the phasors of the two dims.
+template <typename TIN>
+__device__ __forceinline__ void rope_k(uint32_t& x, uint32_t& y, uint32_t c, uint32_t s) {
+  using namespace dev;
+  if constexpr (std::is_same<TIN, __nv_bfloat16>::value) {
+    const float2 fx = unpack2<__nv_bfloat16>(x), fy = unpack2<__nv_bfloat16>(y);
+    x = pack2<__half>(fx.x, fx.y);
+    y = pack2<__half>(fy.x, fy.y);
+  }
+  rot_h2(x, y, c, s);
 }
 
 // ------------------------------------------------------------------------------ tensor core
@@ -366,8 +410,9 @@ __device__ __forceinline__ void rope_pair(uint32_t& lo, uint32_t& hi, const Rope
 // slots so that lane tig's four slots {2tig, 2tig+1, 2tig+8, 2tig+9} hold d = kk*16 + 4tig ..
 // kk*16 + 4tig + 3: the matching K bytes are then one 32-bit load.  A dot product does not
 // depend on the order of its terms, so K and Q only have to agree.
-// With ROPE, q is rotated at its position (the work item's q_pos) in fp32 before the rounding
-// to fp16: the two halves of a rotation pair sit in k steps kk and kk + D/32 of the same lane.
+// With ROPE the fragments hold q unrotated, in fp16: the consumers rotate them tile by tile
+// (the two halves of a rotation pair sit in k steps kk and kk + D/32 of the same lane).  The
+// scaling keeps |q| * 2^-qexp below 2^15, so a rotated component stays below 2^15.5.
 template <typename TQ, typename T, int D, bool PERM = false, bool ROPE = false>
 __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockCoords& b, int lane,
                                              uint32_t (&qb)[D / 16][2], float& qmul) {
@@ -395,24 +440,6 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const BlockC
         const uint32_t raw =
             live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + (h ? off1 : off0)) : 0u;
         f[kk][h] = unpack2<TQ>(raw);
-      }
-    }
-    if constexpr (ROPE) {
-      const float pos = (float)b.it.q_pos;
-      const float4* rates = reinterpret_cast<const float4*>(p.pos_table);
-#pragma unroll
-      for (int kk = 0; kk < D / 32; ++kk) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = kk * 16 + (h ? off1 : off0);  // dims i, i+1; partners i + D/2, i + D/2 + 1
-          const float4 ri = __ldg(rates + i), rj = __ldg(rates + i + 1);
-          float s0, c0, s1, c1;
-          rope_sincos(pos, ri.x, ri.y, s0, c0);
-          rope_sincos(pos, rj.x, rj.y, s1, c1);
-          const float2 x = f[kk][h], y = f[kk + D / 32][h];
-          f[kk][h] = make_float2(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
-          f[kk + D / 32][h] = make_float2(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
-        }
       }
     }
 #pragma unroll
@@ -451,6 +478,18 @@ __device__ __forceinline__ int perm_tok(int j) {
   return ((j & 7) >> 1) + 4 * (j & 1) + 8 * (j >> 3);
 }
 
+// Fills the CTA's R table (see RopeGeom) with the consumer threads; the caller synchronises
+// them before the first read.
+template <int D, bool PERM>
+__device__ __forceinline__ void rope_build_r(uint32_t rtab, const float2* rates, int tid, int nthreads) {
+  constexpr int PAIRS = D / 4;
+  for (int idx = tid; idx < 16 * PAIRS; idx += nthreads) {
+    const int j = idx / PAIRS, P = idx - j * PAIRS;
+    const int tok = PERM ? perm_tok(j) : j;
+    sts_v2(rtab + rope_r_off<D>(j, P), rope_entry((float)tok, rates, rope_pair_freq<PERM>(P)));
+  }
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -469,9 +508,31 @@ __device__ __forceinline__ int acc_dim(int mb, int row) {
   }
 }
 
-// ROPE: K is rotated in registers before the QK MMAs (the two halves of a rotation pair are
-// k steps kk and kk + D/32 of the same lane) and rounded to fp16, so QK runs in fp16 (q is
-// rotated and rounded the same way); P*V keeps V's type.
+// One k-step pair of S^T = K * Q^T under ROPE_LLAMA: a / h are the K fragments of k steps kk
+// and kk + D/32 (dims f and their partners f + D/2), qx / qy the raw q fragments of the same
+// steps.  q is rotated by the slice's E entries (at address e), the K rows a and b by their R
+// entries (row a at address r, row b eight rows further); then the two MMAs in fp16.
+template <typename TIN, int D>
+__device__ __forceinline__ void rope_qk_step(float (&c)[4], float (&c2)[4], uint32_t (&a)[4],
+                                             uint32_t (&h)[4], const uint32_t (&qx)[2],
+                                             const uint32_t (&qy)[2], uint32_t e, uint32_t r) {
+  using namespace dev;
+  const uint4 ev = lds_v4(e);
+  const uint4 ra = lds_v4(r), rb = lds_v4(r + 8 * (D / 4) * 8);
+  uint32_t q0 = qx[0], q1 = qx[1], p0 = qy[0], p1 = qy[1];
+  rot_h2(q0, p0, ev.x, ev.y);  // slot pair 0 (dims f, f + 1)
+  rot_h2(q1, p1, ev.z, ev.w);  // slot pair 1
+  rope_k<TIN>(a[0], h[0], ra.x, ra.y);
+  rope_k<TIN>(a[1], h[1], rb.x, rb.y);
+  rope_k<TIN>(a[2], h[2], ra.z, ra.w);
+  rope_k<TIN>(a[3], h[3], rb.z, rb.w);
+  mma_16816<__half>(c, a, q0, q1);
+  mma_16816<__half>(c2, h, p0, p1);
+}
+
+// ROPE: per tile, q is rotated by the warp slice's E entries and each K row by its R entries
+// (the two halves of a rotation pair are k steps kk and kk + D/32 of the same lane), in fp16
+// arithmetic, so QK runs in fp16; P*V keeps V's type.
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, bool ROPE = false>
 __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
                                            uint32_t full0, uint32_t empty0, volatile int* abort_flag,
@@ -495,7 +556,15 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
   // partial head slice read the last live head's slope, their results are discarded)
   const float slope0 = alibi_slope<D>(p, b.g0 + min(2 * tig, b.gcnt - 1));
   const float slope1 = alibi_slope<D>(p, b.g0 + min(2 * tig + 1, b.gcnt - 1));
-  const float4* rope_rates = reinterpret_cast<const float4*>(p.pos_table);
+  // ROPE: this warp's E buffers and the lane's R entries (rows g_row and g_row + 8; odd rows
+  // swap 64-byte halves, so an even k step kk reads at base + swz + 64kk, an odd one at
+  // base - swz + 64kk)
+  using RG = RopeGeom<D, G::NW>;
+  const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
+  const uint32_t rope_r = smem + G::PIPE_BYTES;
+  const uint32_t rope_e = rope_r + RG::R_BYTES + warp * 2 * RG::ROW;
+  const uint32_t rope_swz = (uint32_t)(g_row & 1) << 6;
+  const uint32_t rope_ra = rope_r + g_row * RG::ROW + tig * 16;
   // e4m3 path: this lane's byte offsets inside a stage tile, with the 128-byte swizzle of the
   // row already folded in (a chunk index is then applied with one XOR).  K: rows tok_a, tok_b,
   // bytes 4tig.. of each 16-byte chunk.  V: rows tig + 4*t4, bytes 8*(g_row&1).. of chunk
@@ -515,12 +584,15 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
+    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
+    // ROPE: the slice's q rotation, while the stage may still be loading
+    if constexpr (ROPE)
+      rope_build_e<D, KV_FP8>(rope_e + (i & 1) * RG::ROW, rope_rates, (float)(b.it.q_pos - t_w), lane);
     if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
     }
-    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
     const int vlo = max(0, b.it.tok_begin - t_w);
     const int vhi = min(16, b.it.tok_end - t_w);
     const uint32_t ktile = stage_after_wait(smem + s * G::STAGE_BYTES);
@@ -559,21 +631,14 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
           e4m3x4_to_half2x2(wb, a[1], a[3]);
         };
         if constexpr (ROPE) {
-          const float ta = (float)(t_w + tok_a);  // row b (tok_b) is ta + 8
+          const uint32_t eb = rope_e + (i & 1) * RG::ROW + tig * 16;
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
-            uint32_t a[4], h[4];  // k steps kk and kk + D/32: dims i and i + D/2
+            uint32_t a[4], h[4];  // k steps kk and kk + D/32: dims f and f + D/2
             load_k(kk, a);
             load_k(kk + D / 32, h);
-            const int i0 = kk * 16 + tig * 4;  // a[0]/a[1]: dims i0, i0+1; a[2]/a[3]: +2, +3
-            const RopeCS cs0 = rope_cs(ta, __ldg(rope_rates + i0), __ldg(rope_rates + i0 + 1));
-            const RopeCS cs1 = rope_cs(ta, __ldg(rope_rates + i0 + 2), __ldg(rope_rates + i0 + 3));
-            rope_pair<__half>(a[0], h[0], cs0, 0);
-            rope_pair<__half>(a[1], h[1], cs0, 1);
-            rope_pair<__half>(a[2], h[2], cs1, 0);
-            rope_pair<__half>(a[3], h[3], cs1, 1);
-            mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
-            mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
+            rope_qk_step<__half, D>(c, c2, a, h, qb[kk], qb[kk + D / 32], eb + kk * 64,
+                                    rope_ra + ((kk & 1) ? -rope_swz : rope_swz) + kk * 64);
           }
         } else {
 #pragma unroll
@@ -589,21 +654,14 @@ __device__ __forceinline__ void consume_tc(const DecodeParams& p, const BlockCoo
         if constexpr (ROPE) {
           // ldmatrix: a[0] / a[2] are row g_row (token tok_a), dims 16kk + 2tig (+1) and
           // 16kk + 8 + 2tig (+1); a[1] / a[3] the same dims of row g_row + 8 (tok_b)
-          const float ta = (float)(t_w + tok_a);  // row b (tok_b) is ta + 8
+          const uint32_t eb = rope_e + (i & 1) * RG::ROW + tig * 16;
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
             uint32_t a[4], h[4];
             ldsm_x4(ktile + swz_off(r0 + row, kk * 2 + csel, TS), a);
             ldsm_x4(ktile + swz_off(r0 + row, (kk + D / 32) * 2 + csel, TS), h);
-            const int i0 = kk * 16 + tig * 2, i1 = i0 + 8;
-            const RopeCS cs0 = rope_cs(ta, __ldg(rope_rates + i0), __ldg(rope_rates + i0 + 1));
-            const RopeCS cs1 = rope_cs(ta, __ldg(rope_rates + i1), __ldg(rope_rates + i1 + 1));
-            rope_pair<TQ>(a[0], h[0], cs0, 0);
-            rope_pair<TQ>(a[1], h[1], cs0, 1);
-            rope_pair<TQ>(a[2], h[2], cs1, 0);
-            rope_pair<TQ>(a[3], h[3], cs1, 1);
-            mma_16816<TQK>(c, a, qb[kk][0], qb[kk][1]);
-            mma_16816<TQK>(c2, h, qb[kk + D / 32][0], qb[kk + D / 32][1]);
+            rope_qk_step<TQ, D>(c, c2, a, h, qb[kk], qb[kk + D / 32], eb + kk * 64,
+                                rope_ra + ((kk & 1) ? -rope_swz : rope_swz) + kk * 64);
           }
         } else {
 #pragma unroll
@@ -996,6 +1054,11 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
   }
   const EpiView<D> epi(smem_p, G::NW);
   if constexpr (KIND == kTensorCore) {
+    if constexpr (ROPE) {
+      rope_build_r<D, KV_FP8>(smem + G::PIPE_BYTES, reinterpret_cast<const float2*>(p.pos_table),
+                              threadIdx.x, G::NCONS);
+      named_bar_sync(2, G::NCONS);
+    }
     float m2[2] = {kNegInf, kNegInf}, lsum[2] = {0.f, 0.f};
     float acc[D / 16][4];
 #pragma unroll
@@ -1037,7 +1100,7 @@ DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   k.rope = ROPE ? 1 : 0;
   k.nstages = NSTAGES;
   k.threads = G::THREADS;
-  k.smem_bytes = G::SMEM_BYTES;
+  k.smem_bytes = G::SMEM_BYTES + (ROPE ? RopeGeom<D, G::NW>::BYTES : 0);
   k.tile_tokens = TS;
   return k;
 }

@@ -603,19 +603,17 @@ int pkd_plan(pkd_handle* h, const int32_t* indptr_host, const int32_t* last_page
   if (tasks_b) std::memcpy(img + tasks_off, h->tasks.data(), tasks_b);
   if (merges_b) std::memcpy(img + merges_off, h->dmerges.data(), merges_b);
   if (lay.pos_floats) {
-    // [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate}: the RoPE angle rate
-    // theta^(-2i/D) / rope_scale of dim pair i as a float pair, and the rotation across 8
-    // positions; then [num_qo_heads] ALiBi slopes in score units (per unit of t - pos)
+    // [head_dim / 2] x {rate hi, rate lo}: the RoPE angle rate theta^(-2i/D) / rope_scale of
+    // dim pair i as a float pair (head_dim floats); from float 2 * head_dim, [num_qo_heads]
+    // ALiBi slopes in score units (per unit of t - pos)
     float* tbl = reinterpret_cast<float*>(img + pos_off);
     std::memset(tbl, 0, lay.pos_floats * sizeof(float));
     if (pos_encoding_mode == PKD_POS_ROPE_LLAMA) {
       for (int i = 0; i < head_dim / 2; ++i) {
         const double rate = std::pow((double)rope_theta, -2.0 * i / head_dim) / rope_scale;
         const float hi = (float)rate;
-        tbl[4 * i] = hi;
-        tbl[4 * i + 1] = (float)(rate - (double)hi);
-        tbl[4 * i + 2] = (float)std::cos(8.0 * rate);
-        tbl[4 * i + 3] = (float)std::sin(8.0 * rate);
+        tbl[2 * i] = hi;
+        tbl[2 * i + 1] = (float)(rate - (double)hi);
       }
     } else {
       const double unit = logits_soft_cap > 0.f ? 1.0 / logits_soft_cap : 1.4426950408889634;

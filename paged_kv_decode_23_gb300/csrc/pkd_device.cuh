@@ -270,6 +270,18 @@ __device__ __forceinline__ void rope_sincos(float t, float hi, float lo, float& 
   __sincosf(r + e, &s, &c);
 }
 
+// Rotation of two complex numbers held as fp16 pairs: (x, y) -> (x c - y s, y c + x s) per
+// half, where x holds the real parts, y the imaginary parts and (c, s) the two phasors.  Each
+// output is one fp16 product and one fused multiply-add (two roundings).
+__device__ __forceinline__ void rot_h2(uint32_t& x, uint32_t& y, uint32_t c, uint32_t s) {
+  const __half2 X = *reinterpret_cast<const __half2*>(&x), Y = *reinterpret_cast<const __half2*>(&y);
+  const __half2 C = *reinterpret_cast<const __half2*>(&c), S = *reinterpret_cast<const __half2*>(&s);
+  const __half2 nx = __hfma2(X, C, __hneg2(__hmul2(Y, S)));
+  const __half2 ny = __hfma2(Y, C, __hmul2(X, S));
+  x = *reinterpret_cast<const uint32_t*>(&nx);
+  y = *reinterpret_cast<const uint32_t*>(&ny);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

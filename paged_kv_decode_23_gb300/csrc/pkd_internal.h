@@ -87,9 +87,9 @@ struct DecodeParams {
   const MergeEntry* merges;  // the split (row, kv head, slice) units: slots and chunk counts
   uint32_t* counters;   // finished chunks per merge entry (the last one merges)
   // Positional-encoding table (plan's pos_encoding_mode), in the int workspace, 256-byte
-  // aligned: [head_dim / 2] x {rate hi, rate lo, cos 8 rate, sin 8 rate} for the RoPE angle
-  // rate rope_theta^(-2i/D) / rope_scale (a float pair) and the rotation across 8 positions,
-  // then [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
+  // aligned: [head_dim / 2] x {rate hi, rate lo} for the RoPE angle rate
+  // rope_theta^(-2i/D) / rope_scale (a float pair), and from float 2 * head_dim the
+  // [num_qo_heads] ALiBi slopes in score units.  Null without an encoding.
   const float* pos_table;
   unsigned long long wait_ns;  // limit of every pipeline wait (0: test once); the wait for
                                // copies in flight before a CTA exits keeps its own 2 s limit

@@ -328,13 +328,20 @@ def test_rope_llama(kv, d):
                      f"rope {kv} D{d} q_len={q_len} theta={theta}")
 
 
-def test_rope_long_positions_keep_precision():
-    """Positions up to ~20k: the kernel's reduced-angle sine / cosine must track the fp64
-    oracle (an fp32 angle t * rate alone would drift by ~1e-3 rad there)."""
-    w, q, pool = _case([20000, 9000], 8, 1, 128, 64, "HND", "bf16", seed=77)
+@pytest.mark.parametrize("kv,d,layout,lens", [
+    ("bf16", 128, "HND", [20000, 9000]),
+    ("bf16", 128, "HND", [131072, 65553]),
+    ("e4m3", 256, "NHD", [131072, 4097]),
+])
+def test_rope_long_positions_keep_precision(kv, d, layout, lens):
+    """Positions up to 131072 (the long-context configuration's length): the kernel's reduced
+    angles must track the fp64 oracle (an fp32 angle t * rate alone would drift by ~1e-3 rad
+    at 20k and ~1e-2 rad at 131k)."""
+    w, q, pool = _case(lens, 16 if kv == "e4m3" else 8, 2 if kv == "e4m3" else 1, d,
+                       32 if kv == "e4m3" else 64, layout, "bf16", kv=kv, seed=77 + lens[0] % 97)
     pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=1e4, rope_scale=1.0)
     got = run_gpu(w, q, pool, **pos)
-    assert_close(w, got, run_oracle(w, q, pool, **pos), "rope long positions")
+    assert_close(w, got, run_oracle(w, q, pool, **pos), f"rope long positions {kv} D{d} {lens}")
 
 
 def test_rope_on_cuda_cores_is_refused():
