@@ -443,15 +443,24 @@ int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err) {
 namespace {
 
 // The chunking of a batch.
+enum ChunkMode {
+  kChunkFixed,  // multiples of C counted from token 0 (fixed_split_size)
+  kChunkEqual,  // rows longer than C in equal page-aligned parts
+  kChunkHead,   // rows longer than C cut once, after their first C tokens (page-aligned end)
+};
 struct DecodeChunking {
-  int64_t C;   // chunk tokens (0 = whole rows)
-  bool equal;  // equal page-aligned parts of rows longer than C (heuristic), else multiples of C
+  int64_t C;  // chunk tokens (0 = whole rows)
+  int mode;
 };
 
-int64_t chunks_of(const RowSpan& sp, int64_t C, bool equal) {
+// End of the first chunk of a row longer than C under kChunkHead (C >= one page).
+int64_t head_cut(const RowSpan& sp, int64_t C, int ps) { return (sp.w + C) / ps * ps; }
+
+int64_t chunks_of(const RowSpan& sp, int64_t C, int mode) {
   const int64_t a = sp.n - sp.w;
-  if (!equal) return fixed_chunks(sp, C);
+  if (mode == kChunkFixed) return fixed_chunks(sp, C);
   if (sp.n == 0 || C == 0 || a <= C) return 1;
+  if (mode == kChunkHead) return 2;
   return (a + C - 1) / C;
 }
 
@@ -459,10 +468,10 @@ int64_t chunks_of(const RowSpan& sp, int64_t C, bool equal) {
 struct ChunkCounts {
   int64_t chunks = 0, split = 0, slots = 0;
 };
-ChunkCounts count_chunks(const PlanRequest& r, int64_t C, bool equal) {
+ChunkCounts count_chunks(const PlanRequest& r, int64_t C, int mode) {
   ChunkCounts c;
   for (int row = 0; row < rows_of(r); ++row) {
-    const int64_t k = chunks_of(row_span(r, row), C, equal);
+    const int64_t k = chunks_of(row_span(r, row), C, mode);
     c.chunks += k;
     if (k > 1) {
       ++c.split;
@@ -472,14 +481,75 @@ ChunkCounts count_chunks(const PlanRequest& r, int64_t C, bool equal) {
   return c;
 }
 
+// Fixed cost of a decode task in tokens: prologue, pipeline fill and drain, epilogue and merge,
+// about 8 us at the ~24 ns per token of one CTA of the e4m3 head_dim-256 kernel with RoPE
+// (fitted to fixed-split measurements of a 128-row batch on GB300).
+constexpr int64_t kDecodeTaskOverhead = 352;
+// Largest slot count and row count the list-scheduling score handles (its storage is on the
+// stack); beyond them only the one-wave equal split is considered.
+constexpr int kMaxScoredSlots = 1024;
+
+// Finish-time buckets of the list-scheduling score (on the stack).
+constexpr int kSpanBuckets = 1024;
+
+// Makespan, in tokens plus kDecodeTaskOverhead per task, of a batch whose rows (attended
+// lengths `len`, longest first, all at most 2C) are cut under kChunkHead at C, when the tasks
+// (per_row per chunk) launch longest first and each starts on the CTA slot that frees first:
+// how the hardware hands a grid's CTAs to free slots.  Finish times are counted in buckets of
+// q tokens (q chosen so that 3 (C + overhead) / q fits kSpanBuckets; the slots that free first
+// are the lowest non-empty bucket, which never moves down).  `pieces` holds 2 * rows entries.
+int64_t head_cut_makespan(const int32_t* len, int rows, int64_t C, int per_row, int slots,
+                          int32_t* pieces, uint16_t* count) {
+  // chunk lengths, longest first: the cut rows' first chunks (C), then the merge of their
+  // remainders and the uncut rows (both already in descending order, all at most C)
+  int n_cut = 0;
+  while (n_cut < rows && len[n_cut] > C) ++n_cut;
+  int np = 0;
+  for (int i = 0; i < n_cut; ++i) pieces[np++] = (int32_t)C;
+  for (int i = 0, j = n_cut; i < n_cut || j < rows;) {
+    if (j >= rows || (i < n_cut && len[i] - C >= len[j])) pieces[np++] = (int32_t)(len[i++] - C);
+    else pieces[np++] = len[j++];
+  }
+  const int64_t ntask = (int64_t)np * per_row;
+  const int m = (int)std::min<int64_t>(slots, ntask);
+  if (m == 0) return 0;
+  const int64_t q = (3 * (C + kDecodeTaskOverhead)) / (kSpanBuckets - 8) + 1;
+  const double per_q = 1.0 / (double)q;
+  auto units = [&](int32_t piece) {
+    return (int)((double)(piece + kDecodeTaskOverhead) * per_q + 0.5);
+  };
+  // every task of the batch costs at most units(C); a slot never holds more than 2 C of work
+  // past its first task (at most 2 slots' worth of tasks in all), so finish < 3 units(C)
+  const int top = units((int32_t)C);
+  std::memset(count, 0, sizeof(uint16_t) * (size_t)(3 * top + 2));
+  int p = 0, u = 0, lo = 0;  // the next task: unit u of chunk p; lo: the lowest finish time
+  for (int i = 0; i < m; ++i) {
+    lo = units(pieces[p]);
+    ++count[lo];
+    if (++u == per_row) { u = 0; ++p; }
+  }
+  int span = units(pieces[0]);
+  for (; p < np; ++p, u = 0) {
+    const int c = units(pieces[p]);
+    for (; u < per_row; ++u) {
+      while (count[lo] == 0) ++lo;
+      --count[lo];
+      const int f = std::min(lo + c, 3 * top + 1);
+      ++count[f];
+      span = std::max(span, f);
+    }
+  }
+  return (int64_t)span * q;
+}
+
 // `slots` CTA slots on the GPU; `max_slots` > 0 bounds the partial slots (per unit).
 DecodeChunking choose_chunking(const PlanRequest& r, const DecodeSchedule& g, int64_t slots,
                                int64_t max_slots) {
   const int rows = rows_of(r);
   const int64_t per_row = (int64_t)r.num_kv_heads * g.gslices;
   const int ps = r.page_size;
-  if (r.disable_split_kv) return {0, false};
-  if (r.fixed_split_size > 0) return {(int64_t)r.fixed_split_size * ps, false};
+  if (r.disable_split_kv) return {0, kChunkEqual};
+  if (r.fixed_split_size > 0) return {(int64_t)r.fixed_split_size * ps, kChunkFixed};
   int64_t total = 0, longest = 0;
   for (int row = 0; row < rows; ++row) {
     const RowSpan sp = row_span(r, row);
@@ -497,27 +567,78 @@ DecodeChunking choose_chunking(const PlanRequest& r, const DecodeSchedule& g, in
     }
     return lo;
   };
+  // bounded work lists (CUDA-graph capacity, partial-slot storage)
+  auto fits_caps = [&](int64_t c, int mode) {
+    const ChunkCounts k = count_chunks(r, c, mode);
+    return (r.max_items <= 0 || k.chunks <= r.max_items) &&
+           (max_slots <= 0 || k.slots * per_row <= max_slots);
+  };
   int64_t C;
-  if ((int64_t)rows * per_row <= slots) {
-    // the unsplit rows fit in one wave: split only as far as every CTA still starts at once
+  if ((int64_t)rows * per_row <= slots && slots <= kMaxScoredSlots) {
+    // The unsplit rows fit in one wave.  Candidates: the smallest equal split whose CTAs all
+    // start at once (its time is about its longest chunk), and cutting every row longer than
+    // C once, for C from half the longest row up to all of it, which lets a second, partial
+    // wave of short remainders fill the slots the short rows free early.  Each is scored by
+    // its list-scheduling makespan; the cheapest is kept (ties: the one-wave split).
+    int32_t len[kMaxScoredSlots], pieces[2 * kMaxScoredSlots];
+    uint16_t buckets[kSpanBuckets];
+    for (int row = 0; row < rows; ++row) {
+      const RowSpan sp = row_span(r, row);
+      len[row] = (int32_t)(sp.n - sp.w);
+    }
+    // chunks and partial slots (per unit) of the rows under an equal or a head cut at c
+    auto counts = [&](int64_t c, int mode) {
+      ChunkCounts k;
+      for (int row = 0; row < rows; ++row) {
+        const uint32_t a = (uint32_t)len[row], c32 = (uint32_t)c;
+        const int64_t n = a <= c32 ? 1 : mode == kChunkHead ? 2 : (a - 1) / c32 + 1;
+        k.chunks += n;
+        if (n > 1) {
+          ++k.split;
+          k.slots += n;
+        }
+      }
+      return k;
+    };
+    auto fits = [&](int64_t c, int mode) {
+      const ChunkCounts k = counts(c, mode);
+      return (r.max_items <= 0 || k.chunks <= r.max_items) &&
+             (max_slots <= 0 || k.slots * per_row <= max_slots);
+    };
+    C = smallest(c_min, [&](int64_t c) { return counts(c, kChunkEqual).chunks * per_row <= slots; });
+    if (!fits(C, kChunkEqual)) C = smallest(C, [&](int64_t c) { return fits(c, kChunkEqual); });
+    if (C >= longest) C = 0;
+    DecodeChunking best{C, kChunkEqual};
+    int64_t best_cost = (C ? C : longest) + kDecodeTaskOverhead;
+    if (longest > c_min && longest < (int64_t)1 << 30) {
+      std::sort(len, len + rows, [](int32_t x, int32_t y) { return x > y; });
+      for (int k = 8; k < 16; ++k) {
+        const int64_t c = std::max(c_min, ((longest * k + 15) / 16 + ps - 1) / ps * ps);
+        if (c >= longest || c + kDecodeTaskOverhead >= best_cost) break;  // span >= c + overhead
+        if (2 * c < longest || !fits(c, kChunkHead)) continue;
+        const int64_t cost =
+            head_cut_makespan(len, rows, c, (int)per_row, (int)slots, pieces, buckets);
+        if (cost < best_cost) {
+          best_cost = cost;
+          best = {c, kChunkHead};
+        }
+      }
+    }
+    return best;
+  } else if ((int64_t)rows * per_row <= slots) {
+    // one wave without the scored candidates (more slots than the score's storage holds)
     C = smallest(c_min, [&](int64_t c) {
-      return count_chunks(r, c, true).chunks * per_row <= slots;
+      return count_chunks(r, c, kChunkEqual).chunks * per_row <= slots;
     });
   } else {
     // chunks of about the average load of a CTA slot
     C = std::max<int64_t>(c_min, (total * per_row + slots - 1) / slots);
     C = (C + ps - 1) / ps * ps;
   }
-  if (C >= longest) return {0, true};
-  // bounded work lists (CUDA-graph capacity, partial-slot storage): the smallest larger chunk
-  // that fits them
-  auto fits_caps = [&](int64_t c) {
-    const ChunkCounts k = count_chunks(r, c, true);
-    return (r.max_items <= 0 || k.chunks <= r.max_items) &&
-           (max_slots <= 0 || k.slots * per_row <= max_slots);
-  };
-  if (!fits_caps(C)) C = smallest(C, fits_caps);
-  return {C >= longest ? 0 : C, true};
+  if (C >= longest) return {0, kChunkEqual};
+  if (!fits_caps(C, kChunkEqual))
+    C = smallest(C, [&](int64_t c) { return fits_caps(c, kChunkEqual); });
+  return {C >= longest ? 0 : C, kChunkEqual};
 }
 
 }  // namespace
@@ -552,7 +673,7 @@ int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, con
   };
   for (int row = 0; row < rows; ++row) {
     const RowSpan sp = row_span(r, row);
-    const int64_t k = chunks_of(sp, C, ch.equal);
+    const int64_t k = chunks_of(sp, C, ch.mode);
     const int64_t slot_base = n_slots, merge_base = n_merges;
     if (k > 1) {
       for (int u = 0; u < per_row; ++u) {
@@ -562,10 +683,15 @@ int build_decode_schedule(const PlanRequest& r, int ctas, DecodeSchedule* s, con
       }
       n_slots += per_row * k;
     }
-    if (sp.n == 0 || C == 0 || (k == 1 && ch.equal)) {
+    if (sp.n == 0 || C == 0 || (k == 1 && ch.mode != kChunkFixed)) {
       add_chunk(row, sp.n == 0 ? 0 : sp.w, sp.n, sp.n == 0 ? 0 : sp.w / ps * ps, 0, 1, slot_base,
                 merge_base);
-    } else if (!ch.equal) {
+    } else if (ch.mode == kChunkHead) {
+      // the first C tokens (to a page boundary), then the rest
+      const int64_t x = head_cut(sp, C, ps);
+      add_chunk(row, sp.w, x, sp.w / ps * ps, 0, 2, slot_base, merge_base);
+      add_chunk(row, x, sp.n, x, 1, 2, slot_base, merge_base);
+    } else if (ch.mode == kChunkFixed) {
       // multiples of C counted from token 0
       int64_t q = 0;
       for (int64_t m = sp.w / C; m <= (sp.n - 1) / C; ++m, ++q)

@@ -114,8 +114,32 @@ def test_plan_partitions_every_workload(pkd, name):
     if name == "long":  # 4 requests x 8 chunks of 256 pages, per kv head
         assert len(plan["tasks"]) == 4 * 8 * 8 and len(plan["merges"]) == 4 * 8
     elif w.batch * w.num_kv_heads <= 304:
-        # the unsplit rows fit one wave of CTA slots: split only as far as one wave holds
-        assert len(plan["tasks"]) <= 304
+        # the unsplit rows fit one wave of CTA slots: either a split that keeps one wave, or
+        # every long row cut once (a partial second wave of remainders)
+        assert len(plan["tasks"]) <= 304 or all(len(ts) <= 2 for ts in _units(plan).values())
+
+
+def test_one_wave_batch_of_similar_rows_cuts_its_long_rows_once(pkd):
+    """mix: 128 rows x 2 kv heads fit one wave of 304 CTA slots unsplit, but half the rows
+    attend the whole 4097-token window.  The list-scheduling score prefers cutting every row
+    longer than some C once, after its first C tokens (page-aligned), so the remainders run in
+    the slots the short rows free; rows of at most C stay whole."""
+    w = W.workload("mix")
+    ps = w.page_size
+    plan = pkd.plan_host(w.indptr, w.last_page_len, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                         w.page_size, window_left=w.window_left, kv_dtype=2)
+    _check_partition(w, plan, 0)
+    units = _units(plan)
+    cut = [ts for ts in units.values() if len(ts) == 2]
+    assert cut and all(len(ts) <= 2 for ts in units.values())
+    assert len(plan["tasks"]) > 304
+    first = [int(ts[0][4]) - int(ts[0][3]) for ts in cut]
+    C = max(first)
+    assert all(C - ps < f <= C for f in first)
+    assert all(int(ts[0][4]) % ps == 0 for ts in cut)
+    assert all(int(ts[1][4]) - int(ts[1][3]) <= C for ts in cut)
+    whole = [int(ts[0][4]) - int(ts[0][3]) for ts in units.values() if len(ts) == 1]
+    assert max(whole) <= C and 2 * C >= max(int(ts[1][4]) - int(ts[0][3]) for ts in cut)
 
 
 @pytest.mark.parametrize("fixed", [0, 1, 2, 7, 64])
