@@ -110,3 +110,18 @@ def test_noalloc_rejects_a_work_list_beyond_the_scratch():
         _noalloc(w, q, p, disable_split_kv=1)
     assert e.value.code == -3
     assert "PKD_NOALLOC_MAX_ITEMS" in str(e.value)
+
+
+def test_noalloc_mix_configuration_matches_the_handle_path_bit_for_bit():
+    """The full-size e4m3 head_dim-256 batch (128 requests, window 4096, soft cap 30): the
+    planner cuts its long rows once and merges 176 split units inside the launch.  Both entry
+    points share the planner and the kernels, so their outputs agree bit for bit; both match
+    the fp64 oracle."""
+    w = W.workload("mix")
+    q, p = W.make_q(w), W.make_pool(w)
+    got = _noalloc(w, q, p)
+    from paged_kv_decode_23_gb300 import noalloc_check_status
+    assert noalloc_check_status() == 0
+    ref = run_gpu(w, q, p)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    _compare(w, got, run_oracle(w, q, p))
