@@ -405,3 +405,35 @@ def test_mla_plan_rejects_bad_input(pkd):
     with pytest.raises(ValueError):
         pkd.mla_plan_host(np.array([0, 1], np.int32), np.array([1], np.int32), 16, 4,
                           backend="fa3")
+
+
+def _lpt_span(chunk_lens, per_row, slots=304, overhead=352):
+    """Makespan of launching per_row tasks per chunk, longest first, each on the CTA slot that
+    frees first (brute force with a heap)."""
+    import heapq
+    tasks = sorted((c + overhead for c in chunk_lens for _ in range(per_row)), reverse=True)
+    h = [0] * slots
+    for t in tasks:
+        heapq.heapreplace(h, h[0] + t)
+    return max(h)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_one_wave_plans_score_no_worse_than_whole_rows(pkd, seed):
+    """For batches whose whole rows fit one wave of CTA slots, the planner's choice (equal
+    split or head cut) never has a larger list-scheduling makespan than keeping every row
+    whole, counted independently here by brute force (one page of slack: cuts end on page
+    boundaries)."""
+    rng = np.random.default_rng(seed)
+    rows = int(rng.integers(40, 150))
+    lens = rng.integers(1, 9000, size=rows).tolist()
+    if seed % 2:
+        lens[: rows // 2] = [8000] * (rows // 2)  # many long rows, the head cut's case
+    w = W.custom(lens, 16, 2, 256, 32, window_left=4096 if seed % 3 == 0 else -1)
+    plan = pkd.plan_host(w.indptr, w.last_page_len, 16, 2, 256, 32, window_left=w.window_left,
+                         kv_dtype=2)
+    _check_partition(w, plan, 0)
+    units = _units(plan)
+    chunks = [int(t[4]) - int(t[3]) for (r, h, g), ts in units.items() if h == 0 for t in ts]
+    whole = [int(ts[-1][4]) - int(ts[0][3]) for (r, h, g), ts in units.items() if h == 0]
+    assert _lpt_span(chunks, 2) <= _lpt_span(whole, 2) + 32
