@@ -374,7 +374,7 @@ int pkd_check_page_table(const int32_t* indptr_host, int batch, const int32_t* i
  * A call allocates nothing: no cudaMalloc / cudaFree, no pinned or heap memory (the plan is
  * built in static host storage).  The first call on a device does a one-time set-up with that
  * device current: it reads the array's device address (cudaGetSymbolAddress) and raises the
- * kernels' shared-memory limit.  Make that first call before any stream capture.
+ * kernels' shared-memory limit.
  *
  * Failures on the GPU: the call's kernels report into the status word at the start of the
  * array, which every call clears first.  pkd_check_status(NULL, &status, stream) reads and
