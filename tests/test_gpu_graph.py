@@ -114,3 +114,60 @@ def test_graph_mode_fixes_the_batch_size():
                  torch.tensor([3, 16], dtype=torch.int32), 8, 2, 128, 16)
     with pytest.raises(ValueError):  # graph mode without its buffers
         BatchDecodePagedKV(ws, "NHD", use_cuda_graph=True)
+
+
+def test_captured_run_replays_head_cut_plans():
+    """A batch whose whole rows fill most of one wave of CTA slots (128 requests x 2 kv heads,
+    half of them long): the planner cuts the long rows once (a second, partial wave of
+    remainders, merged in the launch).  One captured run replays correctly across three such
+    plans of the same batch size and an evenly split one."""
+    from paged_kv_decode_23_gb300 import CUDAGraphBatchDecodePagedKV
+    dev = torch.device("cuda")
+    ps, batch = 16, 128
+    base = W.custom([4000] * batch, 16, 2, 128, ps, layout="NHD", q_dtype="bf16",
+                    kv_dtype="bf16", seed=23, pool_factor=1.0)
+    pool = W.make_pool(base, device=dev)
+    pool_cpu = pool.cpu()
+    rng = np.random.default_rng(9)
+    indptr_buf = torch.zeros(batch + 1, dtype=torch.int32, device=dev)
+    indices_buf = torch.zeros(base.num_pages, dtype=torch.int32, device=dev)
+    lpl_buf = torch.zeros(batch, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    iws = torch.zeros(8 << 20, dtype=torch.uint8, device=dev)
+    dec = CUDAGraphBatchDecodePagedKV(ws, indptr_buf, indices_buf, lpl_buf, "NHD",
+                                      int_workspace_buffer=iws)
+    q_static = torch.zeros(batch, 16, 128, dtype=torch.bfloat16, device=dev)
+    o_static = torch.zeros_like(q_static)
+    lse_static = torch.zeros(batch, 16, dtype=torch.float32, device=dev)
+    plans = []
+    for _ in range(3):
+        lens = rng.integers(1, 2500, size=batch)
+        lens[rng.permutation(batch)[:batch // 2]] = rng.integers(3600, 4001, size=batch // 2)
+        plans.append(lens.tolist())
+    plans.append([1500] * batch)
+    graph = None
+    for k, lens in enumerate(plans):
+        indptr, indices, lpl = _table(lens, ps, base.num_pages, rng)
+        w = _workload(base, lens, indptr, indices, lpl)
+        dec.plan(torch.from_numpy(indptr), torch.from_numpy(indices).to(dev),
+                 torch.from_numpy(lpl), 16, 2, 128, ps, q_data_type=torch.bfloat16)
+        info = dec.plan_info()
+        if k < 3:  # the head cut: more tasks than the 256 whole-row units, split rows merged
+            assert info["tasks"] > batch * 2 and info["merges"] > 0, info
+        q = W.make_q(w, layer=k)
+        q_static.copy_(q.to(dev))
+        if graph is None:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                dec.run(q_static, pool, out=o_static, lse=lse_static)
+            torch.cuda.current_stream().wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                dec.run(q_static, pool, out=o_static, lse=lse_static)
+        o_static.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert dec.check_status() == 0
+        got = (o_static.double().cpu().numpy(), lse_static.double().cpu().numpy())
+        assert_close(w, got, run_oracle(w, q, pool_cpu), f"head-cut plan {k}")
