@@ -1027,13 +1027,13 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Programmatic dependent launch: this grid may have been started while the previous kernel
-  // in the stream was still running; nothing here is read before that kernel has finished
-  // (its results, and its use of the shared workspaces, are then complete).  The next kernel
-  // may start its own launch as soon as every CTA of this one is running.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // in the stream was still running.  The next kernel may start its own launch as soon as
+  // every CTA of this one is running.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // CUDA-graph mode: the grid is cut for a fixed work-list capacity; CTAs past this plan's
-  // tasks have nothing to do (the whole CTA leaves before touching shared memory).
+  // The work list (and its count) came with the plan's upload, a copy that the stream orders
+  // before this launch, so the CTA reads its task and sets up its barriers while the previous
+  // kernel may still run.  CUDA-graph mode: the grid is cut for a fixed work-list capacity;
+  // CTAs past this plan's tasks have nothing to do (the whole CTA leaves at once).
   if (p.task_count != nullptr && (int)blockIdx.x >= *p.task_count) return;
   const BlockCoords b = task_coords<TS, HEADS>(p);
   if (threadIdx.x == 0) {
@@ -1042,9 +1042,13 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, G::NW);
     }
-    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
     fence_mbar_init();
   }
+  // Everything else (q, the page table, the pools, the status word and the shared partial
+  // slots and counters) is read or written only after the previous kernel has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0)
+    abort_flag_s = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
   __syncthreads();
   if (abort_flag_s) return;  // an earlier launch timed out: touch nothing
 
