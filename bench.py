@@ -39,12 +39,12 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on: once the sources differ, the figure no longer describes the kernel and the line
 # reports null.
 MEASURED_TRAFFIC = {
-    "sources_sha256": "73258706f8f75a5f962f941cf71c76b29e566857ea0c7f67ceb3954a5db513fe",
+    "sources_sha256": "934dc88bd5802c279cf6ed3751ee35f8d8ec67f1d5f1c30d3ec7cc5d33eaaa50",
     # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set, bytes)
-    "uniform": 618781184.0,
-    "mix": 418297344.0,
-    "long": 2150458368.0,
-    "lognormal": 3526342400.0,
+    "uniform": 618803200.0,
+    "mix": 418359296.0,
+    "long": 2150496512.0,
+    "lognormal": 3525938176.0,
 }
 
 
