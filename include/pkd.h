@@ -117,8 +117,8 @@ int pkd_reset_workspace(pkd_handle* h, void* float_ws, size_t float_ws_bytes, vo
  *     the page's defaults 1 and 1e4; both ignored unless ROPE_LLAMA):
  *     PKD_POS_ROPE_LLAMA rotates q (at its position) and each key (at its token index) in
  *       pairs of dims (i, i + head_dim/2) by the angle pos / rope_scale * rope_theta^(-2i/D)
- *       before the dot product; the rotated q and K are rounded to fp16 for the product.
- *       Built for the tensor-core kernel only (PKD_KERNEL_CUDA_CORE gives UNSUPPORTED).
+ *       before the dot product.  The tensor-core kernel rounds the rotated q and K to fp16
+ *       for the product; the CUDA-core kernel rotates and multiplies in fp32.
  *       Angles are accurate to ~1e-6 rad for positions below 2^24.
  *     PKD_POS_ALIBI adds slope_g * (t - pos) to the scaled logit of qo head g (before the soft
  *       cap), with the ALiBi paper's slopes 2^(-8 (g+1) / m) for the largest power of two

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "decode_rope.cu", "mla.cu",
+SOURCES = ["decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "decode_rope.cu",
+           "decode_rope_cc.cu", "decode_rope_cc_e4m3.cu", "mla.cu",
            "mla_tc.cu", "planner.cpp", "pkd_api.cpp", "noalloc.cu"]
 HEADERS = ["pkd_internal.h", "pkd_device.cuh", "decode_kernels.cuh",
            "mla_kernels.cuh", "mla_tc_kernels.cuh"]

@@ -78,6 +78,24 @@ struct RopeGeom {
   static_assert(ROW >= 128, "the row swizzle flips bit 6 of an offset inside the row");
 };
 
+// Shared memory of the CUDA-core ROPE_LLAMA kernels, after the pipeline stages.  Lane l holds
+// dims l*EPL .. l*EPL + EPL - 1, i.e. rotation frequencies f = (l % 16)*EPL + e; its partner
+// dims (f + D/2 or f - D/2) are on lane l ^ 16.
+//   R: the rotations by m * rate, m = 1..8, in fp32: entry (m, h, l16) is the float4
+//      {cos, sin of frequency l16*EPL + 2h, cos, sin of l16*EPL + 2h + 1} at byte
+//      ((m - 1) * EPL/2 + h) * 256 + 16 * l16, so 16 lanes read 256 contiguous bytes.
+//   Q: the task's GP q rows, unrotated, in the q dtype (rows of heads past the group are zero).
+// Each warp rotates q to the middle of its 16-token slice, t_w + 8, so a key at row r of the
+// slice is rotated by m = r - 8 in [-8, 7]: a table row for |m|, with the sine negated below 0.
+template <typename TQ, int D, int GP>
+struct CcRopeGeom {
+  static constexpr int EPL = D / 32;
+  static constexpr int R_BYTES = 8 * (D / 2) * 8;
+  static constexpr int Q_BYTES = GP * D * (int)sizeof(TQ);
+  static constexpr int BYTES = R_BYTES + Q_BYTES;
+  static_assert(EPL % 2 == 0, "frequencies are read in pairs");
+};
+
 struct BlockCoords {
   DecodeTask it;
   int kvh;    // kv head
@@ -875,7 +893,86 @@ struct CcRow {
   }
 };
 
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int GP>
+// ROPE_LLAMA set-up of a CUDA-core CTA, by the consumer threads (tid of nthreads): the R table
+// and the task's q rows, at `base` as CcRopeGeom lays them out.
+template <typename TQ, int D, int GP>
+__device__ __forceinline__ void cc_rope_setup(const DecodeParams& p, const BlockCoords& b,
+                                              uint32_t base, int tid, int nthreads) {
+  using namespace dev;
+  using RG = CcRopeGeom<TQ, D, GP>;
+  constexpr int EPL = RG::EPL;
+  const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
+  for (int idx = tid; idx < 8 * (D / 2); idx += nthreads) {
+    const int m = idx / (D / 2) + 1, f = idx % (D / 2);
+    const int l16 = f / EPL, e = f % EPL;
+    const float2 r = __ldg(rates + f);
+    float s, c;
+    rope_sincos((float)m, r.x, r.y, s, c);
+    sts_v2(base + ((m - 1) * (EPL / 2) + e / 2) * 256 + 16 * l16 + (e & 1) * 8,
+           make_uint2(__float_as_uint(c), __float_as_uint(s)));
+  }
+  constexpr int CHUNKS = D * (int)sizeof(TQ) / 16;  // 16-byte chunks of a q row
+  const uint4* q = reinterpret_cast<const uint4*>(p.q);
+  for (int idx = tid; idx < GP * CHUNKS; idx += nthreads) {
+    const int g = idx / CHUNKS, ch = idx % CHUNKS;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (g < b.gcnt) v = __ldg(q + ((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * CHUNKS + ch);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + RG::R_BYTES + idx * 16),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
+// EPL consecutive q-dtype values at shared address a, widened to fp32.
+template <typename TQ, int EPL>
+__device__ __forceinline__ void lds_widen(uint32_t a, float (&x)[EPL]) {
+  using namespace dev;
+  uint32_t v[EPL / 2];
+  if constexpr (EPL == 2) {
+    v[0] = lds_u32(a);
+  } else if constexpr (EPL == 4) {
+    const uint2 t = lds_v2(a);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+    static_assert(EPL == 8, "head_dim 64, 128 or 256");
+    const uint4 t = lds_v4(a);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  }
+#pragma unroll
+  for (int k = 0; k < EPL / 2; ++k) {
+    const float2 f = unpack2<TQ>(v[k]);
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+}
+
+// A lane's slice of a K row rotated by m * rate (m = the row's offset from the middle of the
+// warp's slice, -8..7).  A dim pair is split over lanes l and l ^ 16; each lane sends its
+// value with the sign its partner's formula needs (the lower lane, first dim: x' = x c - y s;
+// the upper lane: y' = y c + x s), so both apply x' = x c + recv * sin(m * rate).
+template <int EPL>
+__device__ __forceinline__ void cc_rope_k(uint32_t rtab, int m, int l16, float send_sign,
+                                          float (&kx)[EPL]) {
+  using namespace dev;
+  if (m == 0) return;
+  const int am = m < 0 ? -m : m;
+  float kp[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) kp[e] = __shfl_xor_sync(~0u, kx[e] * send_sign, 16);
+#pragma unroll
+  for (int h = 0; h < EPL / 2; ++h) {
+    const uint4 t = lds_v4(rtab + ((am - 1) * (EPL / 2) + h) * 256 + 16 * l16);
+    const float s0 = m < 0 ? -__uint_as_float(t.y) : __uint_as_float(t.y);
+    const float s1 = m < 0 ? -__uint_as_float(t.w) : __uint_as_float(t.w);
+    kx[2 * h] = fmaf(kp[2 * h], s0, kx[2 * h] * __uint_as_float(t.x));
+    kx[2 * h + 1] = fmaf(kp[2 * h + 1], s1, kx[2 * h + 1] * __uint_as_float(t.z));
+  }
+}
+
+// ROPE: q is rotated per tile to the middle of the warp's slice (from the shared q rows), and
+// every K row by its offset from there (the R table): the logit depends only on the difference
+// of the two positions.
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int GP, bool ROPE = false>
 __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
                                            uint32_t full0, uint32_t empty0, volatile int* abort_flag,
                                            int warp, int lane, float& m2, float& lsum,
@@ -886,17 +983,19 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
   constexpr int EPL = R::EPL;
   constexpr int TW = 32 / GP;  // tokens per reduce-scatter group
   static_assert(GP >= 2 && GP <= 8 && 16 % TW == 0, "CUDA-core head group");
-  float qf[GP][EPL];
+  float qf[GP][EPL];  // with ROPE: rotated per tile
+  if constexpr (!ROPE) {
 #pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    const bool live = g < b.gcnt;
-    const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
-                     ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D + lane * EPL;
+    for (int g = 0; g < GP; ++g) {
+      const bool live = g < b.gcnt;
+      const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
+                       ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D + lane * EPL;
 #pragma unroll
-    for (int k = 0; k < EPL; k += 2) {
-      const float2 f = unpack2<TQ>(*reinterpret_cast<const uint32_t*>(qrow + k));
-      qf[g][k] = live ? f.x : 0.f;
-      qf[g][k + 1] = live ? f.y : 0.f;
+      for (int k = 0; k < EPL; k += 2) {
+        const float2 f = unpack2<TQ>(*reinterpret_cast<const uint32_t*>(qrow + k));
+        qf[g][k] = live ? f.x : 0.f;
+        qf[g][k + 1] = live ? f.y : 0.f;
+      }
     }
   }
   const float scale_qk = p.scale_qk;
@@ -904,15 +1003,42 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
   const int my_g = lane % GP;
   const int my_j = lane / GP;
   const float slope = alibi_slope<D>(p, b.g0 + min(my_g, b.gcnt - 1));
+  // ROPE: the shared tables, addressed through an opaque copy so that no read moves above the
+  // barrier that published them
+  using RG = CcRopeGeom<TQ, D, GP>;
+  const uint32_t rope_r = ROPE ? stage_after_wait(smem + G::PIPE_BYTES) : 0u;
+  const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
+  const int l16 = lane & 15;
+  const bool upper = lane >= 16;
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
+    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;
+    if constexpr (ROPE) {
+      // q rotated by (q_pos - t_w - 8) * rate, while the stage may still be loading
+      const float dt = (float)(b.it.q_pos - t_w - 8);
+      float c[EPL], sn[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float2 r = __ldg(rope_rates + l16 * EPL + e);
+        rope_sincos(dt, r.x, r.y, sn[e], c[e]);
+        sn[e] = upper ? sn[e] : -sn[e];
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        float own[EPL], par[EPL];
+        const uint32_t qrow = rope_r + RG::R_BYTES + g * D * (int)sizeof(TQ);
+        lds_widen<TQ, EPL>(qrow + lane * EPL * (int)sizeof(TQ), own);
+        lds_widen<TQ, EPL>(qrow + (lane ^ 16) * EPL * (int)sizeof(TQ), par);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) qf[g][e] = fmaf(par[e], sn[e], own[e] * c[e]);
+      }
+    }
     if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
       break;
     }
-    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;
     const int vlo = max(0, b.it.tok_begin - t_w);
     const int vhi = min(16, b.it.tok_end - t_w);
     const uint32_t ktile = stage_after_wait(smem + s * G::STAGE_BYTES);
@@ -926,6 +1052,7 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
       for (int j = 0; j < TW; ++j) {
         float kx[EPL];
         R::template load<TS>(ktile, warp * 16 + r0 + j, lane, kx);
+        if constexpr (ROPE) cc_rope_k<EPL>(rope_r, r0 + j - 8, l16, upper ? -1.f : 1.f, kx);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
           float d = 0.f;
@@ -1005,8 +1132,8 @@ __device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane
 }
 
 // ------------------------------------------------------------------------------ kernel
-// KIND: kTensorCore (HEADS = 8 qo heads per task) or kCudaCore (HEADS = GP).  ROPE: the
-// tensor-core kernel with ROPE_LLAMA applied to q and K.  CTA blockIdx.x runs task blockIdx.x.
+// KIND: kTensorCore (HEADS = 8 qo heads per task) or kCudaCore (HEADS = GP).  ROPE: ROPE_LLAMA
+// applied to q and K.  CTA blockIdx.x runs task blockIdx.x.
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP, bool ROPE = false>
 __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREADS,
                                   KIND == kTensorCore ? 2 : 1)
@@ -1073,14 +1200,18 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
     if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
     stash_tc<D, KV_FP8>(epi, warp, lane, m2, lsum, acc);
   } else {
+    if constexpr (ROPE) {
+      cc_rope_setup<TQ, D, GP>(p, b, smem + G::PIPE_BYTES, threadIdx.x, G::NCONS);
+      named_bar_sync(2, G::NCONS);
+    }
     float m2 = kNegInf, lsum = 0.f;
     float acc[GP][D / 32];
 #pragma unroll
     for (int g = 0; g < GP; ++g)
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) acc[g][k] = 0.f;
-    consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP>(p, b, smem, full0, empty0, abort_flag, warp, lane,
-                                               m2, lsum, acc);
+    consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP, ROPE>(p, b, smem, full0, empty0, abort_flag, warp,
+                                                     lane, m2, lsum, acc);
     if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
     stash_cc<D, GP>(epi, warp, lane, m2, lsum, acc);
   }
@@ -1104,7 +1235,9 @@ DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   k.rope = ROPE ? 1 : 0;
   k.nstages = NSTAGES;
   k.threads = G::THREADS;
-  k.smem_bytes = G::SMEM_BYTES + (ROPE ? RopeGeom<D, G::NW>::BYTES : 0);
+  k.smem_bytes = G::SMEM_BYTES + (!ROPE                ? 0
+                                   : KIND == kTensorCore ? RopeGeom<D, G::NW>::BYTES
+                                                         : CcRopeGeom<TQ, D, GP>::BYTES);
   k.tile_tokens = TS;
   return k;
 }

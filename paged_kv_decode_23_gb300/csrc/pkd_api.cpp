@@ -44,6 +44,8 @@ void init_registry() {
     register_decode_bf16(g_decode);
     register_decode_e4m3(g_decode);
     register_decode_rope(g_decode);
+    register_decode_rope_cc(g_decode);
+    register_decode_rope_cc_e4m3(g_decode);
     register_mla(g_mla);
     register_mla_tc(g_mla);
   });

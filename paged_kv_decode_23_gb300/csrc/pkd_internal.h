@@ -127,6 +127,8 @@ void register_decode_f16(std::vector<DecodeKernel>& out);
 void register_decode_bf16(std::vector<DecodeKernel>& out);
 void register_decode_e4m3(std::vector<DecodeKernel>& out);
 void register_decode_rope(std::vector<DecodeKernel>& out);
+void register_decode_rope_cc(std::vector<DecodeKernel>& out);
+void register_decode_rope_cc_e4m3(std::vector<DecodeKernel>& out);
 
 // MLA decode kernel parameters (pkd_mla_run -> mla_decode_kernel).
 struct MlaParams {
@@ -189,7 +191,7 @@ struct PlanRequest {
   int max_items = 0;     // > 0: the work list may hold at most this many items (CUDA-graph mode;
                          // for decode: chunks per row, counted over all rows)
   int q_len = 1;         // query tokens per request (run's q_len_per_req)
-  int rope = 0;          // 1: ROPE_LLAMA (only the tensor-core kernel is built for it)
+  int rope = 0;          // 1: ROPE_LLAMA
   // MLA plans (pkd_mla_plan): lengths come from kv_len (pages may be more than needed), any
   // page size >= 1, a fixed head tile and token tile, and the kernel's CTAs per SM.
   const int32_t* kv_len = nullptr;

@@ -431,10 +431,6 @@ int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err) {
     while (gp < G && gp < 8) gp <<= 1;
     s->heads_per_cta = gp;
   }
-  if (r.rope && s->kind == kCudaCore) {
-    *err = "pos_encoding_mode ROPE_LLAMA is built for the tensor-core kernel only";
-    return kErrUnsupportedD;
-  }
   s->gslices = (G + s->heads_per_cta - 1) / s->heads_per_cta;
   s->tile_tokens = 16384 / (r.head_dim * (r.kv_dtype == kE4M3 ? 1 : 2));
   return 0;

@@ -155,8 +155,8 @@ class BatchDecodePagedKV:
         per request (run's parameter of that name; the work list depends on it, so it is fixed
         here): the request's last positions, each attending causally; q / o then have
         ``batch * q_len_per_req`` rows, request-major.  ``pos_encoding_mode``: "NONE",
-        "ROPE_LLAMA" (with ``rope_scale`` / ``rope_theta``, defaults 1 and 1e4; tensor-core
-        kernel only) or "ALIBI"."""
+        "ROPE_LLAMA" (with ``rope_scale`` / ``rope_theta``, defaults 1 and 1e4) or
+        "ALIBI"."""
         pos_code = _POS_CODE.get(pos_encoding_mode)
         if pos_code is None:
             raise ValueError("pos_encoding_mode must be 'NONE', 'ROPE_LLAMA' or 'ALIBI'")

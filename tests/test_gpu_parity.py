@@ -310,12 +310,13 @@ def test_alibi(kv, tc):
                      f"alibi {kv} tc={tc} q_len={q_len}")
 
 
+@pytest.mark.parametrize("tc", [True, False])
 @pytest.mark.parametrize("kv,d", [("f16", 64), ("bf16", 128), ("bf16", 256), ("f16", 256),
                                   ("e4m3", 128), ("e4m3", 256)])
-def test_rope_llama(kv, d):
-    """pos_encoding_mode ROPE_LLAMA (tensor-core kernel): q rotated at its position, every key
-    at its index; non-default theta and scale; a split, a window, a soft cap and two query
-    tokens per request on the second pass."""
+def test_rope_llama(kv, d, tc):
+    """pos_encoding_mode ROPE_LLAMA on both kernels: q rotated at its position, every key at
+    its index; non-default theta and scale; a split, a window, a soft cap and two query tokens
+    per request on the second pass."""
     lens = [1, 17, 333, 1500, 0, 4100]
     qdt = "bf16" if kv == "e4m3" else kv
     w, q, pool = _case(lens, 16, 2, d, 32, "NHD", qdt, kv=kv, seed=d + 5, window_left=2000,
@@ -323,30 +324,38 @@ def test_rope_llama(kv, d):
     for q_len, theta, scale in ((1, 1e4, 1.0), (2, 5e5, 4.0)):
         qq = q.repeat_interleave(q_len, dim=0).contiguous()
         pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=theta, rope_scale=scale)
-        got = run_gpu(w, qq, pool, q_len_per_req=q_len, **pos)
+        got = run_gpu(w, qq, pool, use_tensor_cores=tc, q_len_per_req=q_len, **pos)
         assert_close(w, got, run_oracle(w, qq, pool, q_len=q_len, **pos),
-                     f"rope {kv} D{d} q_len={q_len} theta={theta}")
+                     f"rope {kv} D{d} tc={tc} q_len={q_len} theta={theta}")
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 2), (6, 1), (32, 2)])
+def test_rope_llama_cuda_core_head_groups(kv, hq, hkv):
+    """ROPE_LLAMA on the CUDA-core kernel at every head-group width it is built for (2, 4, 8
+    qo heads per CTA, with dead heads in a partial group), keys straddling every slice offset
+    of a tile, HND pages of 16 tokens."""
+    lens = [1, 8, 9, 16, 250, 1031]
+    w, q, pool = _case(lens, hq, hkv, 128, 16, "HND", "f16" if kv == "e4m3" else kv, kv=kv,
+                       seed=hq * 13 + hkv)
+    pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=1e4, rope_scale=2.0)
+    got = run_gpu(w, q, pool, use_tensor_cores=False, fixed_split_size=256, **pos)
+    assert_close(w, got, run_oracle(w, q, pool, **pos), f"rope cuda-core {kv} G{hq // hkv}")
+
+
+@pytest.mark.parametrize("tc", [True, False])
 @pytest.mark.parametrize("kv,d,layout,lens", [
     ("bf16", 128, "HND", [20000, 9000]),
     ("bf16", 128, "HND", [131072, 65553]),
     ("e4m3", 256, "NHD", [131072, 4097]),
 ])
-def test_rope_long_positions_keep_precision(kv, d, layout, lens):
+def test_rope_long_positions_keep_precision(kv, d, layout, lens, tc):
     """Positions up to 131072 (the long-context configuration's length): the kernel's reduced
     angles must track the fp64 oracle (an fp32 angle t * rate alone would drift by ~1e-3 rad
     at 20k and ~1e-2 rad at 131k)."""
     w, q, pool = _case(lens, 16 if kv == "e4m3" else 8, 2 if kv == "e4m3" else 1, d,
                        32 if kv == "e4m3" else 64, layout, "bf16", kv=kv, seed=77 + lens[0] % 97)
     pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=1e4, rope_scale=1.0)
-    got = run_gpu(w, q, pool, **pos)
-    assert_close(w, got, run_oracle(w, q, pool, **pos), f"rope long positions {kv} D{d} {lens}")
-
-
-def test_rope_on_cuda_cores_is_refused():
-    from paged_kv_decode_23_gb300 import PkdError
-    w, q, pool = _case([40], 8, 2, 128, 16, seed=1)
-    with pytest.raises(PkdError) as e:
-        gpu_decoder(w, use_tensor_cores=False, pos_encoding_mode="ROPE_LLAMA")
-    assert e.value.code == -5
+    got = run_gpu(w, q, pool, use_tensor_cores=tc, **pos)
+    assert_close(w, got, run_oracle(w, q, pool, **pos),
+                 f"rope long positions {kv} D{d} {lens} tc={tc}")
