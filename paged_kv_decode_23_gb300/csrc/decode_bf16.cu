@@ -9,12 +9,15 @@ void register_decode_bf16(std::vector<DecodeKernel>& out) {
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kTensorCore, 8>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kTensorCore, 8>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kTensorCore, 8>(kBF16, kBF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 1>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 2>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 4>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 8>(kBF16, kBF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 1>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 2>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 4>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 8>(kBF16, kBF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 1>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 2>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 4>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 8>(kBF16, kBF16));

@@ -11,15 +11,19 @@ void register_decode_e4m3(std::vector<DecodeKernel>& out) {
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kTensorCore, 8>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kTensorCore, 8>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kTensorCore, 8>(kBF16, kE4M3));
+  out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 1>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 2>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 4>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 8>(kF16, kE4M3));
+  out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 1>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 2>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 4>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 8>(kF16, kE4M3));
+  out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 1>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 2>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 4>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 8>(kBF16, kE4M3));
+  out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 1>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 2>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 4>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 8>(kBF16, kE4M3));

@@ -9,12 +9,15 @@ void register_decode_f16(std::vector<DecodeKernel>& out) {
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kTensorCore, 8>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kTensorCore, 8>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kTensorCore, 8>(kF16, kF16));
+  out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 1>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 2>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 4>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 8>(kF16, kF16));
+  out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 1>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 2>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 4>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 8>(kF16, kF16));
+  out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 1>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 2>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 4>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 8>(kF16, kF16));

@@ -78,24 +78,6 @@ struct RopeGeom {
   static_assert(ROW >= 128, "the row swizzle flips bit 6 of an offset inside the row");
 };
 
-// Shared memory of the CUDA-core ROPE_LLAMA kernels, after the pipeline stages.  Lane l holds
-// dims l*EPL .. l*EPL + EPL - 1, i.e. rotation frequencies f = (l % 16)*EPL + e; its partner
-// dims (f + D/2 or f - D/2) are on lane l ^ 16.
-//   R: the rotations by m * rate, m = 1..8, in fp32: entry (m, h, l16) is the float4
-//      {cos, sin of frequency l16*EPL + 2h, cos, sin of l16*EPL + 2h + 1} at byte
-//      ((m - 1) * EPL/2 + h) * 256 + 16 * l16, so 16 lanes read 256 contiguous bytes.
-//   Q: the task's GP q rows, unrotated, in the q dtype (rows of heads past the group are zero).
-// Each warp rotates q to the middle of its 16-token slice, t_w + 8, so a key at row r of the
-// slice is rotated by m = r - 8 in [-8, 7]: a table row for |m|, with the sine negated below 0.
-template <typename TQ, int D, int GP>
-struct CcRopeGeom {
-  static constexpr int EPL = D / 32;
-  static constexpr int R_BYTES = 8 * (D / 2) * 8;
-  static constexpr int Q_BYTES = GP * D * (int)sizeof(TQ);
-  static constexpr int BYTES = R_BYTES + Q_BYTES;
-  static_assert(EPL % 2 == 0, "frequencies are read in pairs");
-};
-
 struct BlockCoords {
   DecodeTask it;
   int kvh;    // kv head
@@ -838,202 +820,219 @@ __device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane
 }
 
 // ------------------------------------------------------------------------------ CUDA core
-// Lane layout: lane owns head_dim elements [lane*EPL, lane*EPL + EPL) of every row.
-template <typename TQ, bool KV_FP8, int D>
-struct CcRow {
-  static constexpr int EPL = D / 32;
-  static constexpr int BYTES = EPL * (KV_FP8 ? 1 : 2);  // bytes a lane reads per row
-  // Loads this lane's slice of row r of a swizzled tile and widens it to fp32.  The loads are
-  // volatile: their values feed plain FMAs, so only this keeps them ahead of the stage's
-  // release.
-  template <int TS>
-  __device__ __forceinline__ static void load(uint32_t tile, int r, int lane, float (&x)[EPL]) {
-    using namespace dev;
-    const int off = lane * BYTES;
-    const uint32_t a = tile + swz_off(r, off >> 4, TS) + (off & 15);
-    if constexpr (!KV_FP8) {
-      if constexpr (BYTES == 4) {
-        uint32_t v;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-        const float2 f = unpack2<TQ>(v);
-        x[0] = f.x; x[1] = f.y;
-      } else if constexpr (BYTES == 8) {
-        uint32_t v0, v1;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(a));
-        const float2 f0 = unpack2<TQ>(v0), f1 = unpack2<TQ>(v1);
-        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
-      } else {
-        const uint4 v4 = lds_v4(a);
-        const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = unpack2<TQ>(v[k]);
-          x[2 * k] = f.x; x[2 * k + 1] = f.y;
-        }
-      }
-    } else {
-      if constexpr (BYTES == 4) {
-        uint32_t v;
-        v = lds_u32(a);
-        const float2 f0 = unpack2<__half>(e4m3x2_to_half2(v & 0xffff));
-        const float2 f1 = unpack2<__half>(e4m3x2_to_half2(v >> 16));
-        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
-      } else {
-        const uint2 vv2 = lds_v2(a);
-        const uint32_t v0 = vv2.x, v1 = vv2.y;
-        const uint32_t vv[2] = {v0, v1};
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float2 f0 = unpack2<__half>(e4m3x2_to_half2(vv[k] & 0xffff));
-          const float2 f1 = unpack2<__half>(e4m3x2_to_half2(vv[k] >> 16));
-          x[4 * k] = f0.x; x[4 * k + 1] = f0.y; x[4 * k + 2] = f1.x; x[4 * k + 3] = f1.y;
-        }
-      }
-    }
+// Geometry of the CUDA-core consumers.  A K/V row is split over L lanes: lane sub-index
+// h = lane / R owns dims [h*DL, (h+1)*DL) (its 16-byte chunks h*CPL .. h*CPL + CPL - 1), so
+// one warp instruction covers R = 32 / L rows of the warp's 16-token slice and the slice
+// takes NP = 16 / R passes.  L grows with the head group so that a lane's accumulators
+// (GP heads x DL dims, V floats) stay at 128 registers or fewer.  Scores need a reduction over
+// only the L lanes of a row; the P*V products stay in the lane that read the row, and the
+// lanes of a column are summed once per task.
+template <bool KV_FP8, int D, int GP, int NW, bool ROPE>
+struct CcGeom {
+  static constexpr int ELT = KV_FP8 ? 1 : 2;
+  static constexpr int CH = D * ELT / 16;  // 16-byte chunks of a K/V row
+  static constexpr int EPC = 16 / ELT;     // elements of a chunk
+  static constexpr int VMAX = 64;          // accumulators per lane the split aims for
+  static constexpr int L0 = GP * D / VMAX < 2 ? 2 : GP * D / VMAX;
+  static constexpr int L1 = L0 > 32 ? 32 : L0;
+  static constexpr int L = L1 > CH ? CH : L1;
+  static constexpr int R = 32 / L;
+  static constexpr int NP = 16 / R;
+  static constexpr int CPL = CH / L;
+  static constexpr int DL = D / L;
+  static constexpr int V = GP * DL;
+  // Rows of a pass.  The swizzled tile puts chunk c of row r in bank group (c ^ r) & 7; the
+  // eight lanes of a shared-memory phase must hit eight groups.  With R >= 8 they read one
+  // chunk of eight consecutive rows.  With R < 8 they hold 8 / R values of h, whose chunk
+  // indices differ in bits HBITS, so their rows take the other bits of r & 7 (RR_MASK) and
+  // the passes take HBITS and bit 3 (P_MASK).
+  static constexpr int HBITS = R >= 8 ? 0 : (8 / R - 1) * CPL;
+  static constexpr int RR_MASK = R >= 8 ? R - 1 : (7 & ~HBITS);
+  static constexpr int P_MASK = R >= 8 ? (15 & ~(R - 1)) : (8 | HBITS);
+  // q as fp32 [GP][L][QS]: each lane's DL dims of a head in a block, padded by 16 bytes so
+  // that the blocks one phase reads fall in different banks
+  static constexpr int QS = DL + 4;
+  static constexpr int Q_BYTES = GP * L * QS * 4;
+  // ROPE: each warp's q rotated for its current slice (same layout), and the K rotations by
+  // m = -8..7 positions: row m + 8 holds, per frequency pair (f, f+1), {cos f, cos f+1,
+  // sin f, sin f+1}, padded by 16 bytes so that eight rows fall in eight bank groups
+  static constexpr int RT_ROW = D / 2 * 8 + 16;
+  static constexpr int QR_OFF = Q_BYTES;
+  static constexpr int RT_OFF = Q_BYTES + (ROPE ? NW * Q_BYTES : 0);
+  static constexpr int BYTES = RT_OFF + (ROPE ? 16 * RT_ROW : 0);
+  // Registers per thread, capped so that CTAs of `threads` threads can share an SM: each of
+  // its four sub-partitions holds 16384 registers and a CTA's warps are spread over them.
+  // Two CTAs per SM where that leaves at least 160 registers and the accumulators fit in
+  // VMAX, else one.
+  static constexpr int regs_for(int warps_per_sm) {
+    return (16384 / ((warps_per_sm + 3) / 4 * 32)) / 8 * 8 > 255
+               ? 255
+               : (16384 / ((warps_per_sm + 3) / 4 * 32)) / 8 * 8;
   }
+  static constexpr int max_regs(int threads) {
+    return V <= VMAX && regs_for(2 * threads / 32) >= 160 ? regs_for(2 * threads / 32)
+                                                         : regs_for(threads / 32);
+  }
+  static_assert(CPL >= 1 && (CPL & (CPL - 1)) == 0 && HBITS <= 7, "chunks per lane");
+  static_assert(2 * R * L == 64 && V % (2 * R) == 0, "lane split");
 };
 
-// ROPE_LLAMA set-up of a CUDA-core CTA, by the consumer threads (tid of nthreads): the R table
-// and the task's q rows, at `base` as CcRopeGeom lays them out.
-template <typename TQ, int D, int GP>
-__device__ __forceinline__ void cc_rope_setup(const DecodeParams& p, const BlockCoords& b,
-                                              uint32_t base, int tid, int nthreads) {
-  using namespace dev;
-  using RG = CcRopeGeom<TQ, D, GP>;
-  constexpr int EPL = RG::EPL;
-  const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
-  for (int idx = tid; idx < 8 * (D / 2); idx += nthreads) {
-    const int m = idx / (D / 2) + 1, f = idx % (D / 2);
-    const int l16 = f / EPL, e = f % EPL;
-    const float2 r = __ldg(rates + f);
-    float s, c;
-    rope_sincos((float)m, r.x, r.y, s, c);
-    sts_v2(base + ((m - 1) * (EPL / 2) + e / 2) * 256 + 16 * l16 + (e & 1) * 8,
-           make_uint2(__float_as_uint(c), __float_as_uint(s)));
-  }
-  constexpr int CHUNKS = D * (int)sizeof(TQ) / 16;  // 16-byte chunks of a q row
-  const uint4* q = reinterpret_cast<const uint4*>(p.q);
-  for (int idx = tid; idx < GP * CHUNKS; idx += nthreads) {
-    const int g = idx / CHUNKS, ch = idx % CHUNKS;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (g < b.gcnt) v = __ldg(q + ((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * CHUNKS + ch);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + RG::R_BYTES + idx * 16),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-  }
+// The bits of x placed, in order, at the set bits of a 4-bit mask.
+__device__ __forceinline__ int deposit4(int x, int mask) {
+  int out = 0, b = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if ((mask >> i) & 1) out |= ((x >> b++) & 1) << i;
+  return out;
 }
 
-// EPL consecutive q-dtype values at shared address a, widened to fp32.
-template <typename TQ, int EPL>
-__device__ __forceinline__ void lds_widen(uint32_t a, float (&x)[EPL]) {
-  using namespace dev;
-  uint32_t v[EPL / 2];
-  if constexpr (EPL == 2) {
-    v[0] = lds_u32(a);
-  } else if constexpr (EPL == 4) {
-    const uint2 t = lds_v2(a);
-    v[0] = t.x; v[1] = t.y;
-  } else {
-    static_assert(EPL == 8, "head_dim 64, 128 or 256");
-    const uint4 t = lds_v4(a);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  }
-#pragma unroll
-  for (int k = 0; k < EPL / 2; ++k) {
-    const float2 f = unpack2<TQ>(v[k]);
-    x[2 * k] = f.x;
-    x[2 * k + 1] = f.y;
-  }
+// Byte offset of chunk c of tile row r (128-byte column blocks of TS rows, 128-byte swizzle).
+template <int TS>
+__device__ __forceinline__ uint32_t cc_chunk(int r, int c) {
+  return (uint32_t)((c >> 3) * TS * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// A lane's slice of a K row rotated by m * rate (m = the row's offset from the middle of the
-// warp's slice, -8..7).  A dim pair is split over lanes l and l ^ 16; each lane sends its
-// value with the sign its partner's formula needs (the lower lane, first dim: x' = x c - y s;
-// the upper lane: y' = y c + x s), so both apply x' = x c + recv * sin(m * rate).
-template <int EPL>
-__device__ __forceinline__ void cc_rope_k(uint32_t rtab, int m, int l16, float send_sign,
-                                          float (&kx)[EPL]) {
+// A 16-byte chunk of K/V widened to fp32 pairs (element 2j, 2j + 1 in pair j).
+template <typename TQ, bool KV_FP8>
+__device__ __forceinline__ void cc_widen(const uint4& w, float2 (&x)[KV_FP8 ? 8 : 4]) {
   using namespace dev;
-  if (m == 0) return;
-  const int am = m < 0 ? -m : m;
-  float kp[EPL];
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) kp[e] = __shfl_xor_sync(~0u, kx[e] * send_sign, 16);
-#pragma unroll
-  for (int h = 0; h < EPL / 2; ++h) {
-    const uint4 t = lds_v4(rtab + ((am - 1) * (EPL / 2) + h) * 256 + 16 * l16);
-    const float s0 = m < 0 ? -__uint_as_float(t.y) : __uint_as_float(t.y);
-    const float s1 = m < 0 ? -__uint_as_float(t.w) : __uint_as_float(t.w);
-    kx[2 * h] = fmaf(kp[2 * h], s0, kx[2 * h] * __uint_as_float(t.x));
-    kx[2 * h + 1] = fmaf(kp[2 * h + 1], s1, kx[2 * h + 1] * __uint_as_float(t.z));
-  }
-}
-
-// ROPE: q is rotated per tile to the middle of the warp's slice (from the shared q rows), and
-// every K row by its offset from there (the R table): the logit depends only on the difference
-// of the two positions.
-template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int GP, bool ROPE = false>
-__device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoords& b, uint32_t smem,
-                                           uint32_t full0, uint32_t empty0, volatile int* abort_flag,
-                                           int warp, int lane, float& m2, float& lsum,
-                                           float (&acc)[GP][D / 32]) {
-  using namespace dev;
-  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
-  using R = CcRow<TQ, KV_FP8, D>;
-  constexpr int EPL = R::EPL;
-  constexpr int TW = 32 / GP;  // tokens per reduce-scatter group
-  static_assert(GP >= 2 && GP <= 8 && 16 % TW == 0, "CUDA-core head group");
-  float qf[GP][EPL];  // with ROPE: rotated per tile
-  if constexpr (!ROPE) {
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      const bool live = g < b.gcnt;
-      const TQ* qrow = reinterpret_cast<const TQ*>(p.q) +
-                       ((size_t)b.it.req * p.num_qo_heads + b.g0 + (live ? g : 0)) * D + lane * EPL;
-#pragma unroll
-      for (int k = 0; k < EPL; k += 2) {
-        const float2 f = unpack2<TQ>(*reinterpret_cast<const uint32_t*>(qrow + k));
-        qf[g][k] = live ? f.x : 0.f;
-        qf[g][k + 1] = live ? f.y : 0.f;
-      }
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (KV_FP8) {
+      x[2 * k] = unpack2<__half>(e4m3x2_to_half2((uint16_t)(v[k] & 0xffffu)));
+      x[2 * k + 1] = unpack2<__half>(e4m3x2_to_half2((uint16_t)(v[k] >> 16)));
+    } else if constexpr (std::is_same<TQ, __nv_bfloat16>::value) {
+      x[k] = make_float2(__uint_as_float(v[k] << 16), __uint_as_float(v[k] & 0xffff0000u));
+    } else {
+      x[k] = unpack2<__half>(v[k]);
     }
   }
+}
+
+__device__ __forceinline__ uint4 lds_v4_vol(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Set-up of a CUDA-core CTA by its consumer threads (tid of nthreads), at `base` as CcGeom
+// lays it out: the task's GP q rows in fp32 (rows of heads past the group are zero) and, with
+// ROPE, the K rotation table.
+template <typename TQ, bool KV_FP8, int D, int GP, int NW, bool ROPE>
+__device__ __forceinline__ void cc_setup(const DecodeParams& p, const BlockCoords& b,
+                                         uint8_t* base, int tid, int nthreads) {
+  using namespace dev;
+  using C = CcGeom<KV_FP8, D, GP, NW, ROPE>;
+  float* q = reinterpret_cast<float*>(base);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q);
+  for (int idx = tid; idx < GP * D / 2; idx += nthreads) {
+    const int g = idx / (D / 2), d = (idx - g * (D / 2)) * 2;
+    float2 v = make_float2(0.f, 0.f);
+    if (g < b.gcnt)
+      v = unpack2<TQ>(__ldg(src + (((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * D + d) / 2));
+    float* dst = q + (g * C::L + d / C::DL) * C::QS + d % C::DL;
+    dst[0] = v.x;
+    dst[1] = v.y;
+  }
+  if constexpr (ROPE) {
+    const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
+    for (int idx = tid; idx < 16 * (D / 4); idx += nthreads) {
+      const int k = idx / (D / 4), fp = idx - k * (D / 4);  // row k: m = k - 8; pair 2fp, 2fp+1
+      const float2 r0 = __ldg(rates + 2 * fp), r1 = __ldg(rates + 2 * fp + 1);
+      float s0, c0, s1, c1;
+      rope_sincos((float)(k - 8), r0.x, r0.y, s0, c0);
+      rope_sincos((float)(k - 8), r1.x, r1.y, s1, c1);
+      *reinterpret_cast<float4*>(base + C::RT_OFF + k * C::RT_ROW + fp * 16) =
+          make_float4(c0, c1, s0, s1);
+    }
+  }
+}
+
+// ROPE: the warp's q rotated by dt * rate (dt = q_pos minus the middle of its slice) into its
+// own buffer, in the layout of the shared q rows.  Lane handles frequencies f = lane + 32k.
+template <bool KV_FP8, int D, int GP, int NW>
+__device__ __forceinline__ void cc_rotate_q(const float* q, float* qr, const float2* rates,
+                                            float dt, int lane) {
+  using namespace dev;
+  using C = CcGeom<KV_FP8, D, GP, NW, true>;
+  __syncwarp();  // every lane is done reading the previous slice's rotation
+#pragma unroll
+  for (int k = 0; k < D / 64; ++k) {
+    const int f = lane + 32 * k;
+    const float2 r = __ldg(rates + f);
+    float s, c;
+    rope_sincos(dt, r.x, r.y, s, c);
+    const int ox = (f / C::DL) * C::QS + f % C::DL;
+    const int oy = ((f + D / 2) / C::DL) * C::QS + (f + D / 2) % C::DL;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      const float x = q[g * C::L * C::QS + ox], y = q[g * C::L * C::QS + oy];
+      qr[g * C::L * C::QS + ox] = x * c - y * s;
+      qr[g * C::L * C::QS + oy] = y * c + x * s;
+    }
+  }
+  __syncwarp();
+  asm volatile("" ::: "memory");  // the q reads that follow see this slice's rotation
+}
+
+// The CUDA-core consumer warp.  For each tile its 16-token slice is taken in NP passes of R
+// rows (lane: row rr = lane % R of the pass, dims block h = lane / R).  Per pass:
+//  - the partial dot products of the lane's row with its q dims (fp32 pair FMAs), summed over
+//    the row's L lanes;
+//  - the online softmax in base 2 with a lazy reference: m2 moves only when a score exceeds
+//    it by more than kLazyMax, so p <= 2^kLazyMax and most passes skip the cross-lane max;
+//  - p * V into the lane's own accumulators (rows of a window or chunk edge that are not
+//    attended have p = 0 and their V zeroed, so stale values in the stage cannot leak).
+// At the end the accumulators are reduce-scattered over the R row lanes of each dims block
+// and stored, with m2 and l, into the warp's slot of the epilogue image.
+// ROPE: q is rotated per slice to the slice's middle t_w + 8 and each K row by its offset
+// row - 8 from there (the partner dims of a rotation pair are on lane ^ 16): the logit
+// depends only on the difference of the two positions.
+// Returns false when a pipeline wait gave up (the CTA's consumers then leave together).
+template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int GP, bool ROPE>
+__device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoords& b,
+                                           uint32_t smem, uint8_t* smem_p, uint32_t full0,
+                                           uint32_t empty0, volatile int* abort_flag, int warp,
+                                           int lane, const EpiView<D>& epi) {
+  using namespace dev;
+  using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
+  using C = CcGeom<KV_FP8, D, GP, G::NW, ROPE>;
+  constexpr int L = C::L, R = C::R, NP = C::NP, CPL = C::CPL, EPC = C::EPC, DL = C::DL;
+  constexpr int V2 = C::V / 2;  // fp32 pairs of accumulators
+  // passes taken together (independent chains in flight), as many as registers allow
+  constexpr int NB0 = (ROPE ? 8 : 16) / GP < 1 ? 1 : (ROPE ? 8 : 16) / GP;
+  constexpr int NB = NB0 < NP ? NB0 : NP;
+  const int rr = lane % R, h = lane / R;
+  const int rowbase = deposit4(rr, C::RR_MASK);
+  const int hc = h * CPL;
+  float* qs = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES);
+  float* qr = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES + C::QR_OFF) + warp * (C::Q_BYTES / 4);
+  const uint32_t qlane_s = smem_u32((ROPE ? qr : qs) + h * C::QS);
+  const uint8_t* rt = smem_p + G::PIPE_BYTES + C::RT_OFF + ((h % (L / 2)) * DL / 2) * 16;
+  const float send_sign = h >= L / 2 ? -1.f : 1.f;
+  const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
   const float scale_qk = p.scale_qk;
   const float cap_log2 = p.cap_log2;
-  const int my_g = lane % GP;
-  const int my_j = lane / GP;
-  const float slope = alibi_slope<D>(p, b.g0 + min(my_g, b.gcnt - 1));
-  // ROPE: the shared tables, addressed through an opaque copy so that no read moves above the
-  // barrier that published them
-  using RG = CcRopeGeom<TQ, D, GP>;
-  const uint32_t rope_r = ROPE ? stage_after_wait(smem + G::PIPE_BYTES) : 0u;
-  const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
-  const int l16 = lane & 15;
-  const bool upper = lane >= 16;
+
+  float slope[GP], m2[GP], lsum[GP];
+  float2 acc[GP][DL / 2];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    slope[g] = alibi_slope<D>(p, b.g0 + min(g, b.gcnt - 1));
+    m2[g] = kNegInf;
+    lsum[g] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DL / 2; ++k) acc[g][k] = make_float2(0.f, 0.f);
+  }
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
-    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;
-    if constexpr (ROPE) {
-      // q rotated by (q_pos - t_w - 8) * rate, while the stage may still be loading
-      const float dt = (float)(b.it.q_pos - t_w - 8);
-      float c[EPL], sn[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float2 r = __ldg(rope_rates + l16 * EPL + e);
-        rope_sincos(dt, r.x, r.y, sn[e], c[e]);
-        sn[e] = upper ? sn[e] : -sn[e];
-      }
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        float own[EPL], par[EPL];
-        const uint32_t qrow = rope_r + RG::R_BYTES + g * D * (int)sizeof(TQ);
-        lds_widen<TQ, EPL>(qrow + lane * EPL * (int)sizeof(TQ), own);
-        lds_widen<TQ, EPL>(qrow + (lane ^ 16) * EPL * (int)sizeof(TQ), par);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) qf[g][e] = fmaf(par[e], sn[e], own[e] * c[e]);
-      }
-    }
+    const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
+    if constexpr (ROPE)
+      cc_rotate_q<KV_FP8, D, GP, G::NW>(qs, qr, rope_rates, (float)(b.it.q_pos - t_w - 8), lane);
     if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
@@ -1043,92 +1042,164 @@ __device__ __forceinline__ void consume_cc(const DecodeParams& p, const BlockCoo
     const int vhi = min(16, b.it.tok_end - t_w);
     const uint32_t ktile = stage_after_wait(smem + s * G::STAGE_BYTES);
     const uint32_t vtile = ktile + G::TILE_BYTES;
+    if (vlo < vhi) {  // warp-uniform
+      const bool partial = vlo > 0 || vhi < 16;
+#pragma unroll 1
+      for (int pb = 0; pb < NP; pb += NB) {  // a batch of NB passes
+        int row[NB];
+        bool valid[NB];
 #pragma unroll
-    for (int grp = 0; grp < 16 / TW; ++grp) {
-      const int r0 = grp * TW;
-      if (r0 + TW <= vlo || r0 >= vhi) continue;  // warp-uniform
-      float part[32];
+        for (int pp = 0; pp < NB; ++pp) {
+          row[pp] = rowbase | deposit4(pb + pp, C::P_MASK);
+          valid[pp] = row[pp] >= vlo && row[pp] < vhi;
+        }
+        // ---- the lane's partial dot products for every pass (independent chains), with each
+        // q chunk read once and used by all passes
+        float2 s2[NB][GP];
 #pragma unroll
-      for (int j = 0; j < TW; ++j) {
-        float kx[EPL];
-        R::template load<TS>(ktile, warp * 16 + r0 + j, lane, kx);
-        if constexpr (ROPE) cc_rope_k<EPL>(rope_r, r0 + j - 8, l16, upper ? -1.f : 1.f, kx);
+        for (int pp = 0; pp < NB; ++pp)
+#pragma unroll
+          for (int g = 0; g < GP; ++g) s2[pp][g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          float2 kf[NB][EPC / 2];
+#pragma unroll
+          for (int pp = 0; pp < NB; ++pp) {
+            cc_widen<TQ, KV_FP8>(lds_v4_vol(ktile + cc_chunk<TS>(warp * 16 + row[pp], hc + c)),
+                                 kf[pp]);
+            if constexpr (ROPE) {
+              const uint8_t* tr = rt + row[pp] * C::RT_ROW + c * EPC / 2 * 16;
+#pragma unroll
+              for (int j = 0; j < EPC / 2; ++j) {
+                const float4 t = *reinterpret_cast<const float4*>(tr + j * 16);
+                float2 kp;
+                kp.x = __shfl_xor_sync(~0u, kf[pp][j].x * send_sign, 16);
+                kp.y = __shfl_xor_sync(~0u, kf[pp][j].y * send_sign, 16);
+                kf[pp][j] = __ffma2_rn(kp, make_float2(t.z, t.w),
+                                       __fmul2_rn(kf[pp][j], make_float2(t.x, t.y)));
+              }
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+#pragma unroll
+            for (int j = 0; j < EPC / 4; ++j) {
+              const uint4 t = lds_v4_vol(qlane_s + (g * L * C::QS + c * EPC + 4 * j) * 4);
+              const float2 q01 = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
+              const float2 q23 = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
+#pragma unroll
+              for (int pp = 0; pp < NB; ++pp) {
+                s2[pp][g] = __ffma2_rn(kf[pp][2 * j], q01, s2[pp][g]);
+                s2[pp][g] = __ffma2_rn(kf[pp][2 * j + 1], q23, s2[pp][g]);
+              }
+            }
+          }
+        }
+        // ---- scores (summed over the row's L lanes) and the online softmax, once per tile
+        float sc[NB][GP];
+        bool grow = false;
+#pragma unroll
+        for (int pp = 0; pp < NB; ++pp)
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            float d = s2[pp][g].x + s2[pp][g].y;
+#pragma unroll
+            for (int o = R; o < 32; o <<= 1) d += __shfl_xor_sync(~0u, d, o);
+            const float bias = slope[g] * (float)(t_w + row[pp] - b.it.q_pos);
+            sc[pp][g] = valid[pp] ? score_log2(d, scale_qk, bias, cap_log2) : kNegInf;
+            grow |= sc[pp][g] > m2[g] + kLazyMax;
+          }
+        if (__any_sync(~0u, grow)) {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            float mx = sc[0][g];
+#pragma unroll
+            for (int pp = 1; pp < NB; ++pp) mx = fmaxf(mx, sc[pp][g]);
+#pragma unroll
+            for (int o = 1; o < R; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
+            if (mx > m2[g]) {  // warp-uniform: every lane holds the same maximum
+              const float alpha = fast_exp2(m2[g] - mx);
+              lsum[g] *= alpha;
+              const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+              for (int k = 0; k < DL / 2; ++k) acc[g][k] = __fmul2_rn(acc[g][k], a2);
+              m2[g] = mx;
+            }
+          }
+        }
+        float pr[NB][GP];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          float d = 0.f;
+          const float ref = m2[g] == kNegInf ? 0.f : m2[g];
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) d = fmaf(qf[g][e], kx[e], d);
-          part[j * GP + g] = d;
+          for (int pp = 0; pp < NB; ++pp) {
+            pr[pp][g] = fast_exp2(sc[pp][g] - ref);
+            lsum[g] += pr[pp][g];
+          }
         }
-      }
-      // reduce-scatter: lane l ends with the full dot product of pair l = j*GP + g
+        // ---- p * V
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
+        for (int c = 0; c < CPL; ++c) {
 #pragma unroll
-        for (int k = 0; k < off; ++k) {
-          const float send = upper ? part[k] : part[k + off];
-          const float keep = upper ? part[k + off] : part[k];
-          part[k] = keep + __shfl_xor_sync(~0u, send, off);
-        }
-      }
-      const int r = r0 + my_j;
-      const float bias = slope * (float)(t_w + r - b.it.q_pos);
-      float sv = score_log2(part[0], scale_qk, bias, cap_log2);
-      sv = (r >= vlo && r < vhi) ? sv : kNegInf;
-      float mx = sv;
+          for (int pp = 0; pp < NB; ++pp) {
+            uint4 w = lds_v4_vol(vtile + cc_chunk<TS>(warp * 16 + row[pp], hc + c));
+            if (partial && !valid[pp]) w = make_uint4(0u, 0u, 0u, 0u);
+            float2 vf[EPC / 2];
+            cc_widen<TQ, KV_FP8>(w, vf);
 #pragma unroll
-      for (int off = GP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
-      const float mnew = fmaxf(m2, mx);
-      const float ref = mnew == kNegInf ? 0.f : mnew;
-      const float alpha = fast_exp2(m2 - ref);
-      const float pr = fast_exp2(sv - ref);
-      lsum = lsum * alpha + pr;
-      m2 = mnew;
+            for (int g = 0; g < GP; ++g) {
+              const float2 p2 = make_float2(pr[pp][g], pr[pp][g]);
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float a = __shfl_sync(~0u, alpha, g);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] *= a;
-      }
-#pragma unroll
-      for (int j = 0; j < TW; ++j) {
-        if (r0 + j < vlo || r0 + j >= vhi) continue;  // warp-uniform: skip unattended rows
-        float vx[EPL];
-        R::template load<TS>(vtile, warp * 16 + r0 + j, lane, vx);
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float pj = __shfl_sync(~0u, pr, j * GP + g);
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pj, vx[e], acc[g][e]);
+              for (int j = 0; j < EPC / 2; ++j)
+                acc[g][c * EPC / 2 + j] = __ffma2_rn(p2, vf[j], acc[g][c * EPC / 2 + j]);
+            }
+          }
         }
       }
     }
-    (void)my_g;
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
-}
+  // every consumer is done with the stages; one shared decision whether any wait gave up
+  if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return false;
 
-// A CUDA-core warp's state into its own slot of the epilogue image.  Lane owns dims
-// [lane * EPL, lane * EPL + EPL) of every head; head g's m2 / lsum live on the lanes with
-// lane % GP == g (lane g holds the reduced values after the shuffles below).
-template <int D, int GP>
-__device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane, float m2,
-                                             float lsum, float (&acc)[GP][D / 32]) {
-  constexpr int EPL = D / 32;
-  float l = lsum;
+  // ---- into the epilogue image: l summed over the rows (every dims block holds the same
+  // sums); the accumulators reduce-scattered over the row lanes, after which lane rr holds
+  // pairs rr * SEG .. rr * SEG + SEG - 1 of its block's flattened [GP][DL / 2] array
 #pragma unroll
-  for (int off = GP; off < 32; off <<= 1) l += __shfl_xor_sync(~0u, l, off);
-  if (lane < GP) {
-    e.m[warp * kSlotHeads + lane] = m2;
-    e.l[warp * kSlotHeads + lane] = l;
+  for (int g = 0; g < GP; ++g) {
+    float l = lsum[g];
+#pragma unroll
+    for (int o = 1; o < R; o <<= 1) l += __shfl_xor_sync(~0u, l, o);
+    if (lane == 0) {
+      epi.m[warp * kSlotHeads + g] = m2[g];
+      epi.l[warp * kSlotHeads + g] = l;
+    }
   }
-  float* a = e.acc + warp * kSlotHeads * D;
+  float2 a[V2];
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
-    for (int k = 0; k < EPL; ++k) a[g * D + lane * EPL + k] = acc[g][k];
+    for (int k = 0; k < DL / 2; ++k) a[g * (DL / 2) + k] = acc[g][k];
+#pragma unroll
+  for (int o = R / 2, n = V2; o >= 1; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float2 send = up ? a[k] : a[k + n / 2];
+      const float2 keep = up ? a[k + n / 2] : a[k];
+      a[k].x = keep.x + __shfl_xor_sync(~0u, send.x, o);
+      a[k].y = keep.y + __shfl_xor_sync(~0u, send.y, o);
+    }
+  }
+  constexpr int SEG = V2 / R;
+#pragma unroll
+  for (int k = 0; k < SEG; ++k) {
+    const int n = rr * SEG + k;
+    const int g = n / (DL / 2), j = (n % (DL / 2)) * 2;
+    *reinterpret_cast<float2*>(epi.acc + (warp * kSlotHeads + g) * D + h * DL + j) = a[k];
+  }
+  return true;
 }
 
 // ------------------------------------------------------------------------------ kernel
@@ -1137,6 +1208,8 @@ __device__ __forceinline__ void stash_cc(const EpiView<D>& e, int warp, int lane
 template <typename TQ, bool KV_FP8, int D, int TS, int NSTAGES, int KIND, int GP, bool ROPE = false>
 __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREADS,
                                   KIND == kTensorCore ? 2 : 1)
+    __maxnreg__((KIND == kTensorCore ? 255
+                                     : CcGeom<KV_FP8, D, GP, TS / 16, ROPE>::max_regs(TS / 16 * 32 + 32)))
     decode_paged_kernel(const __grid_constant__ DecodeParams p) {
   using namespace dev;
   using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
@@ -1200,20 +1273,11 @@ __global__ void __launch_bounds__(DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>::THREAD
     if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
     stash_tc<D, KV_FP8>(epi, warp, lane, m2, lsum, acc);
   } else {
-    if constexpr (ROPE) {
-      cc_rope_setup<TQ, D, GP>(p, b, smem + G::PIPE_BYTES, threadIdx.x, G::NCONS);
-      named_bar_sync(2, G::NCONS);
-    }
-    float m2 = kNegInf, lsum = 0.f;
-    float acc[GP][D / 32];
-#pragma unroll
-    for (int g = 0; g < GP; ++g)
-#pragma unroll
-      for (int k = 0; k < D / 32; ++k) acc[g][k] = 0.f;
-    consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP, ROPE>(p, b, smem, full0, empty0, abort_flag, warp,
-                                                     lane, m2, lsum, acc);
-    if (named_bar_or(1, G::NCONS, *abort_flag != 0)) return;
-    stash_cc<D, GP>(epi, warp, lane, m2, lsum, acc);
+    cc_setup<TQ, KV_FP8, D, GP, G::NW, ROPE>(p, b, smem_p + G::PIPE_BYTES, threadIdx.x, G::NCONS);
+    named_bar_sync(2, G::NCONS);
+    if (!consume_cc<TQ, KV_FP8, D, TS, NSTAGES, GP, ROPE>(p, b, smem, smem_p, full0, empty0,
+                                                          abort_flag, warp, lane, epi))
+      return;
   }
   named_bar_sync(1, G::NCONS);
   store_task<TQ, D, G::NW>(p, b, epi, threadIdx.x);
@@ -1235,9 +1299,9 @@ DecodeKernel make_decode_kernel(int q_dtype, int kv_dtype) {
   k.rope = ROPE ? 1 : 0;
   k.nstages = NSTAGES;
   k.threads = G::THREADS;
-  k.smem_bytes = G::SMEM_BYTES + (!ROPE                ? 0
-                                   : KIND == kTensorCore ? RopeGeom<D, G::NW>::BYTES
-                                                         : CcRopeGeom<TQ, D, GP>::BYTES);
+  k.smem_bytes = G::SMEM_BYTES + (KIND == kTensorCore
+                                      ? (ROPE ? RopeGeom<D, G::NW>::BYTES : 0)
+                                      : CcGeom<KV_FP8, D, GP, G::NW, ROPE>::BYTES);
   k.tile_tokens = TS;
   return k;
 }

@@ -6,21 +6,27 @@
 namespace pkd {
 
 void register_decode_rope_cc(std::vector<DecodeKernel>& out) {
+  out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 1, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 2, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 4, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 64, 128, 3, kCudaCore, 8, true>(kF16, kF16));
+  out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 1, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 2, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 4, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 128, 64, 3, kCudaCore, 8, true>(kF16, kF16));
+  out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 1, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 2, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 4, true>(kF16, kF16));
   out.push_back(make_decode_kernel<__half, false, 256, 32, 3, kCudaCore, 8, true>(kF16, kF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 1, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 2, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 4, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 64, 128, 3, kCudaCore, 8, true>(kBF16, kBF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 1, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 2, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 4, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 128, 64, 3, kCudaCore, 8, true>(kBF16, kBF16));
+  out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 1, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 2, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 4, true>(kBF16, kBF16));
   out.push_back(make_decode_kernel<__nv_bfloat16, false, 256, 32, 3, kCudaCore, 8, true>(kBF16, kBF16));

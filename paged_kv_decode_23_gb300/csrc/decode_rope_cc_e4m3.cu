@@ -6,15 +6,19 @@
 namespace pkd {
 
 void register_decode_rope_cc_e4m3(std::vector<DecodeKernel>& out) {
+  out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 1, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 2, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 4, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 128, 128, 3, kCudaCore, 8, true>(kF16, kE4M3));
+  out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 1, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 2, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 4, true>(kF16, kE4M3));
   out.push_back(make_decode_kernel<__half, true, 256, 64, 3, kCudaCore, 8, true>(kF16, kE4M3));
+  out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 1, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 2, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 4, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 128, 128, 3, kCudaCore, 8, true>(kBF16, kE4M3));
+  out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 1, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 2, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 4, true>(kBF16, kE4M3));
   out.push_back(make_decode_kernel<__nv_bfloat16, true, 256, 64, 3, kCudaCore, 8, true>(kBF16, kE4M3));

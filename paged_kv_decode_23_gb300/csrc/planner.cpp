@@ -427,7 +427,7 @@ int decode_geometry(const PlanRequest& r, DecodeSchedule* s, const char** err) {
   if (s->kind == kTensorCore) {
     s->heads_per_cta = 8;
   } else {
-    int gp = 2;
+    int gp = 1;
     while (gp < G && gp < 8) gp <<= 1;
     s->heads_per_cta = gp;
   }
