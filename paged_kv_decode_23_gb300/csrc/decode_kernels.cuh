@@ -821,45 +821,51 @@ __device__ __forceinline__ void stash_tc(const EpiView<D>& e, int warp, int lane
 
 // ------------------------------------------------------------------------------ CUDA core
 // Geometry of the CUDA-core consumers.  A K/V row is split over L lanes: lane sub-index
-// h = lane / R owns dims [h*DL, (h+1)*DL) (its 16-byte chunks h*CPL .. h*CPL + CPL - 1), so
-// one warp instruction covers R = 32 / L rows of the warp's 16-token slice and the slice
-// takes NP = 16 / R passes.  L grows with the head group so that a lane's accumulators
-// (GP heads x DL dims, V floats) stay at 128 registers or fewer.  Scores need a reduction over
-// only the L lanes of a row; the P*V products stay in the lane that read the row, and the
-// lanes of a column are summed once per task.
+// h = lane / R owns dims [h*DL, (h+1)*DL), LB bytes of the row read as NU loads ("units") of
+// UB = 16 bytes (chunks h*NU .. h*NU + NU - 1) or, when a lane's share is 8 bytes, one
+// 8-byte half of chunk h / 2.  One warp instruction covers R = 32 / L rows of the warp's
+// 16-token slice and the slice takes NP = 16 / R passes.  L grows with the head group so that
+// a lane's accumulators (GP heads x DL dims, V floats) stay at VMAX.  Scores need a reduction
+// over only the L lanes of a row; the P*V products stay in the lane that read the row, and
+// the lanes of a column are summed once per task.
 template <bool KV_FP8, int D, int GP, int NW, bool ROPE>
 struct CcGeom {
   static constexpr int ELT = KV_FP8 ? 1 : 2;
   static constexpr int CH = D * ELT / 16;  // 16-byte chunks of a K/V row
-  static constexpr int EPC = 16 / ELT;     // elements of a chunk
   static constexpr int VMAX = 64;          // accumulators per lane the split aims for
   static constexpr int L0 = GP * D / VMAX < 2 ? 2 : GP * D / VMAX;
   static constexpr int L1 = L0 > 32 ? 32 : L0;
-  static constexpr int L = L1 > CH ? CH : L1;
+  static constexpr int L = L1 > 2 * CH ? 2 * CH : L1;
   static constexpr int R = 32 / L;
   static constexpr int NP = 16 / R;
-  static constexpr int CPL = CH / L;
+  static constexpr int LB = D * ELT / L;        // bytes of a row per lane
+  static constexpr int UB = LB >= 16 ? 16 : 8;  // bytes per load
+  static constexpr int NU = LB / UB;            // loads per lane and row
+  static constexpr int EPU = UB / ELT;          // elements per load
   static constexpr int DL = D / L;
   static constexpr int V = GP * DL;
-  // Rows of a pass.  The swizzled tile puts chunk c of row r in bank group (c ^ r) & 7; the
-  // eight lanes of a shared-memory phase must hit eight groups.  With R >= 8 they read one
-  // chunk of eight consecutive rows.  With R < 8 they hold 8 / R values of h, whose chunk
-  // indices differ in bits HBITS, so their rows take the other bits of r & 7 (RR_MASK) and
-  // the passes take HBITS and bit 3 (P_MASK).
-  static constexpr int HBITS = R >= 8 ? 0 : (8 / R - 1) * CPL;
+  // Rows of a pass.  The swizzled tile puts chunk c of row r in bank group (c ^ r) & 7.  A
+  // shared-memory phase serves 8 lanes' 16-byte loads (or 16 lanes' 8-byte loads, two per
+  // chunk), which must hit eight groups.  With R >= 8 they read one chunk of eight
+  // consecutive rows.  With R < 8 they hold 8 / R chunk indices, differing in bits HBITS, so
+  // their rows take the other bits of r & 7 (RR_MASK) and the passes take HBITS and bit 3
+  // (P_MASK).
+  static constexpr int HBITS = R >= 8 ? 0 : (8 / R - 1) * (UB == 16 ? NU : 1);
   static constexpr int RR_MASK = R >= 8 ? R - 1 : (7 & ~HBITS);
   static constexpr int P_MASK = R >= 8 ? (15 & ~(R - 1)) : (8 | HBITS);
-  // q as fp32 [GP][L][QS]: each lane's DL dims of a head in a block, padded by 16 bytes so
-  // that the blocks one phase reads fall in different banks
-  static constexpr int QS = DL + 4;
+  // q as fp32 [GP][L][QS]: each lane's DL dims of a head in a block.  The QN blocks that one
+  // phase may read (one per h value in it) must fall in different banks: the blocks are
+  // padded by 16 bytes where DL alone would not spread them.
+  static constexpr int QN = R >= 8 ? 1 : 8 / R;
+  static constexpr int QS = DL * QN <= 32 ? DL : DL + 4;
   static constexpr int Q_BYTES = GP * L * QS * 4;
-  // ROPE: each warp's q rotated for its current slice (same layout), and the K rotations by
-  // m = -8..7 positions: row m + 8 holds, per frequency pair (f, f+1), {cos f, cos f+1,
-  // sin f, sin f+1}, padded by 16 bytes so that eight rows fall in eight bank groups
+  // Without ROPE: the task's q rows.  With ROPE: each warp's q rotated for its current slice
+  // (same layout), then the K rotations by |m| = 0..8 positions: row |m| holds, per frequency
+  // pair (f, f+1), {cos f, cos f+1, sin f, sin f+1}, padded by 16 bytes so that eight rows
+  // fall in eight bank groups (a negative m flips the sine).
   static constexpr int RT_ROW = D / 2 * 8 + 16;
-  static constexpr int QR_OFF = Q_BYTES;
-  static constexpr int RT_OFF = Q_BYTES + (ROPE ? NW * Q_BYTES : 0);
-  static constexpr int BYTES = RT_OFF + (ROPE ? 16 * RT_ROW : 0);
+  static constexpr int RT_OFF = ROPE ? NW * Q_BYTES : 0;
+  static constexpr int BYTES = ROPE ? RT_OFF + 9 * RT_ROW : Q_BYTES;
   // Registers per thread, capped so that CTAs of `threads` threads can share an SM: each of
   // its four sub-partitions holds 16384 registers and a CTA's warps are spread over them.
   // Two CTAs per SM where that leaves at least 160 registers and the accumulators fit in
@@ -873,7 +879,7 @@ struct CcGeom {
     return V <= VMAX && regs_for(2 * threads / 32) >= 160 ? regs_for(2 * threads / 32)
                                                          : regs_for(threads / 32);
   }
-  static_assert(CPL >= 1 && (CPL & (CPL - 1)) == 0 && HBITS <= 7, "chunks per lane");
+  static_assert(NU >= 1 && (NU & (NU - 1)) == 0 && HBITS <= 7 && EPU % 4 == 0, "lane loads");
   static_assert(2 * R * L == 64 && V % (2 * R) == 0, "lane split");
 };
 
@@ -892,13 +898,13 @@ __device__ __forceinline__ uint32_t cc_chunk(int r, int c) {
   return (uint32_t)((c >> 3) * TS * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// A 16-byte chunk of K/V widened to fp32 pairs (element 2j, 2j + 1 in pair j).
-template <typename TQ, bool KV_FP8>
-__device__ __forceinline__ void cc_widen(const uint4& w, float2 (&x)[KV_FP8 ? 8 : 4]) {
+// NWD words of K/V widened to fp32 pairs (element 2j, 2j + 1 in pair j).
+template <typename TQ, bool KV_FP8, int NWD>
+__device__ __forceinline__ void cc_widen(const uint32_t (&v)[NWD],
+                                         float2 (&x)[NWD * (KV_FP8 ? 2 : 1)]) {
   using namespace dev;
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < NWD; ++k) {
     if constexpr (KV_FP8) {
       x[2 * k] = unpack2<__half>(e4m3x2_to_half2((uint16_t)(v[k] & 0xffffu)));
       x[2 * k + 1] = unpack2<__half>(e4m3x2_to_half2((uint16_t)(v[k] >> 16)));
@@ -910,6 +916,53 @@ __device__ __forceinline__ void cc_widen(const uint4& w, float2 (&x)[KV_FP8 ? 8 
   }
 }
 
+// Load u (of NU) of this lane's share of tile row r: UB bytes widened to fp32 pairs (element
+// 2j, 2j + 1 in pair j), or zeros if `zero`.  The load is volatile: its values feed plain
+// FMAs, so only this keeps it ahead of the stage's release.
+template <typename TQ, bool KV_FP8, int TS, int UB, int NU>
+__device__ __forceinline__ void cc_load(uint32_t tile, int r, int h, int u, bool zero,
+                                        float2 (&x)[UB / (KV_FP8 ? 1 : 2) / 2]) {
+  using namespace dev;
+  constexpr int NWD = UB / 4;
+  uint32_t v[NWD];
+  if constexpr (UB == 16) {
+    const uint32_t a = tile + cc_chunk<TS>(r, h * NU + u);
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(a));
+  } else {
+    const uint32_t a = tile + cc_chunk<TS>(r, h >> 1) + (h & 1) * 8;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(a));
+  }
+#pragma unroll
+  for (int k = 0; k < NWD; ++k) v[k] = zero ? 0u : v[k];
+  cc_widen<TQ, KV_FP8, NWD>(v, x);
+}
+
+__device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
+// a[i] for a runtime i < N, by selects (no local-memory indexing).
+template <int N>
+__device__ __forceinline__ float pick(const float (&a)[N], int i) {
+  float v = a[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) v = i == k ? a[k] : v;
+  return v;
+}
+
+// The dims block h (as h bits of the lane) of the lane that finishes score x of a batch after
+// a reduce-scatter over LOG_LR lane bits 16, 8, ...: level k keeps the upper half (bit
+// LOG_X - 1 - k of x) on lanes with bit 4 - k set.
+template <int LOG_X, int LOG_LR, int LOG_R>
+__device__ __forceinline__ constexpr int hsrc(int x) {
+  int h = 0;
+  for (int k = 0; k < LOG_LR; ++k) h |= ((x >> (LOG_X - 1 - k)) & 1) << (4 - k - LOG_R);
+  return h;
+}
+
 __device__ __forceinline__ uint4 lds_v4_vol(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -919,45 +972,49 @@ __device__ __forceinline__ uint4 lds_v4_vol(uint32_t addr) {
 }
 
 // Set-up of a CUDA-core CTA by its consumer threads (tid of nthreads), at `base` as CcGeom
-// lays it out: the task's GP q rows in fp32 (rows of heads past the group are zero) and, with
-// ROPE, the K rotation table.
+// lays it out: the task's GP q rows in fp32 (rows of heads past the group are zero), or with
+// ROPE the K rotation table.
 template <typename TQ, bool KV_FP8, int D, int GP, int NW, bool ROPE>
 __device__ __forceinline__ void cc_setup(const DecodeParams& p, const BlockCoords& b,
                                          uint8_t* base, int tid, int nthreads) {
   using namespace dev;
   using C = CcGeom<KV_FP8, D, GP, NW, ROPE>;
-  float* q = reinterpret_cast<float*>(base);
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q);
-  for (int idx = tid; idx < GP * D / 2; idx += nthreads) {
-    const int g = idx / (D / 2), d = (idx - g * (D / 2)) * 2;
-    float2 v = make_float2(0.f, 0.f);
-    if (g < b.gcnt)
-      v = unpack2<TQ>(__ldg(src + (((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * D + d) / 2));
-    float* dst = q + (g * C::L + d / C::DL) * C::QS + d % C::DL;
-    dst[0] = v.x;
-    dst[1] = v.y;
-  }
-  if constexpr (ROPE) {
+  if constexpr (!ROPE) {
+    float* q = reinterpret_cast<float*>(base);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q);
+    for (int idx = tid; idx < GP * D / 2; idx += nthreads) {
+      const int g = idx / (D / 2), d = (idx - g * (D / 2)) * 2;
+      float2 v = make_float2(0.f, 0.f);
+      if (g < b.gcnt)
+        v = unpack2<TQ>(__ldg(src + (((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * D + d) / 2));
+      float* dst = q + (g * C::L + d / C::DL) * C::QS + d % C::DL;
+      dst[0] = v.x;
+      dst[1] = v.y;
+    }
+  } else {
     const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
-    for (int idx = tid; idx < 16 * (D / 4); idx += nthreads) {
-      const int k = idx / (D / 4), fp = idx - k * (D / 4);  // row k: m = k - 8; pair 2fp, 2fp+1
+    for (int idx = tid; idx < 9 * (D / 4); idx += nthreads) {
+      const int k = idx / (D / 4), fp = idx - k * (D / 4);  // row |m| = k; pair 2fp, 2fp+1
       const float2 r0 = __ldg(rates + 2 * fp), r1 = __ldg(rates + 2 * fp + 1);
       float s0, c0, s1, c1;
-      rope_sincos((float)(k - 8), r0.x, r0.y, s0, c0);
-      rope_sincos((float)(k - 8), r1.x, r1.y, s1, c1);
+      rope_sincos((float)k, r0.x, r0.y, s0, c0);
+      rope_sincos((float)k, r1.x, r1.y, s1, c1);
       *reinterpret_cast<float4*>(base + C::RT_OFF + k * C::RT_ROW + fp * 16) =
           make_float4(c0, c1, s0, s1);
     }
   }
 }
 
-// ROPE: the warp's q rotated by dt * rate (dt = q_pos minus the middle of its slice) into its
-// own buffer, in the layout of the shared q rows.  Lane handles frequencies f = lane + 32k.
-template <bool KV_FP8, int D, int GP, int NW>
-__device__ __forceinline__ void cc_rotate_q(const float* q, float* qr, const float2* rates,
-                                            float dt, int lane) {
+// ROPE: the task's q rows rotated by dt * rate (dt = q_pos minus the middle of the warp's
+// slice) into the warp's buffer, in the layout of the q rows (heads past the group are zero).
+// Lane handles frequencies f = lane + 32k; q is read from global memory (it stays in L1).
+template <typename TQ, bool KV_FP8, int D, int GP, int NW>
+__device__ __forceinline__ void cc_rotate_q(const DecodeParams& p, const BlockCoords& b,
+                                            float* qr, float dt, int lane) {
   using namespace dev;
   using C = CcGeom<KV_FP8, D, GP, NW, true>;
+  const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
+  const TQ* q = reinterpret_cast<const TQ*>(p.q) + ((size_t)b.it.req * p.num_qo_heads + b.g0) * D;
   __syncwarp();  // every lane is done reading the previous slice's rotation
 #pragma unroll
   for (int k = 0; k < D / 64; ++k) {
@@ -969,7 +1026,9 @@ __device__ __forceinline__ void cc_rotate_q(const float* q, float* qr, const flo
     const int oy = ((f + D / 2) / C::DL) * C::QS + (f + D / 2) % C::DL;
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
-      const float x = q[g * C::L * C::QS + ox], y = q[g * C::L * C::QS + oy];
+      const bool live = g < b.gcnt;
+      const float x = live ? to_float(__ldg(q + g * D + f)) : 0.f;
+      const float y = live ? to_float(__ldg(q + g * D + f + D / 2)) : 0.f;
       qr[g * C::L * C::QS + ox] = x * c - y * s;
       qr[g * C::L * C::QS + oy] = y * c + x * s;
     }
@@ -1000,16 +1059,20 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
   using namespace dev;
   using G = DecodeGeom<TQ, KV_FP8, D, TS, NSTAGES>;
   using C = CcGeom<KV_FP8, D, GP, G::NW, ROPE>;
-  constexpr int L = C::L, R = C::R, NP = C::NP, CPL = C::CPL, EPC = C::EPC, DL = C::DL;
+  constexpr int L = C::L, R = C::R, NP = C::NP, NU = C::NU, EPU = C::EPU, DL = C::DL;
   constexpr int V2 = C::V / 2;  // fp32 pairs of accumulators
   // passes taken together (independent chains in flight), as many as registers allow
   constexpr int NB0 = (ROPE ? 8 : 16) / GP < 1 ? 1 : (ROPE ? 8 : 16) / GP;
   constexpr int NB = NB0 < NP ? NB0 : NP;
+  constexpr int X = NB * GP;            // scores a lane holds partial sums of, per batch
+  constexpr int LR = X < L ? X : L;     // lanes a row's scores are scattered over
+  constexpr int XH = X / LR;            // scores a lane finishes
+  constexpr int LOG_X = ilog2(X), LOG_LR = ilog2(LR), LOG_R = ilog2(R);
+  static_assert((X & (X - 1)) == 0 && (1 << LOG_R) == R, "powers of two");
   const int rr = lane % R, h = lane / R;
   const int rowbase = deposit4(rr, C::RR_MASK);
-  const int hc = h * CPL;
   float* qs = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES);
-  float* qr = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES + C::QR_OFF) + warp * (C::Q_BYTES / 4);
+  float* qr = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES) + warp * (C::Q_BYTES / 4);
   const uint32_t qlane_s = smem_u32((ROPE ? qr : qs) + h * C::QS);
   const uint8_t* rt = smem_p + G::PIPE_BYTES + C::RT_OFF + ((h % (L / 2)) * DL / 2) * 16;
   const float send_sign = h >= L / 2 ? -1.f : 1.f;
@@ -1017,22 +1080,34 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
   const float scale_qk = p.scale_qk;
   const float cap_log2 = p.cap_log2;
 
-  float slope[GP], m2[GP], lsum[GP];
+  float m2[GP];
   float2 acc[GP][DL / 2];
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
-    slope[g] = alibi_slope<D>(p, b.g0 + min(g, b.gcnt - 1));
     m2[g] = kNegInf;
-    lsum[g] = 0.f;
 #pragma unroll
     for (int k = 0; k < DL / 2; ++k) acc[g][k] = make_float2(0.f, 0.f);
+  }
+  // the scores this lane finishes: batch entries x = xb + j (pass x / GP, head x % GP), the
+  // same for every batch; their running sums of p
+  int xb = 0;
+#pragma unroll
+  for (int k = 0; k < LOG_LR; ++k) xb |= ((lane >> (4 - k)) & 1) << (LOG_X - 1 - k);
+  int hg[XH], hdep[XH];
+  float hslope[XH], lsum_h[XH];
+#pragma unroll
+  for (int j = 0; j < XH; ++j) {
+    hg[j] = (xb + j) % GP;
+    hdep[j] = deposit4((xb + j) / GP, C::P_MASK);
+    hslope[j] = alibi_slope<D>(p, b.g0 + min(hg[j], b.gcnt - 1));
+    lsum_h[j] = 0.f;
   }
 
   for (int i = 0; i < b.ntiles; ++i) {
     const int s = i % NSTAGES;
     const int t_w = b.it.chunk_tok0 + (b.j0 + i) * TS + warp * 16;  // first token of my slice
     if constexpr (ROPE)
-      cc_rotate_q<KV_FP8, D, GP, G::NW>(qs, qr, rope_rates, (float)(b.it.q_pos - t_w - 8), lane);
+      cc_rotate_q<TQ, KV_FP8, D, GP, G::NW>(p, b, qr, (float)(b.it.q_pos - t_w - 8), lane);
     if (!__all_sync(~0u, mbar_wait(full0 + 8 * s, (i / NSTAGES) & 1, abort_flag, p.wait_ns))) {
       *abort_flag = 1;  // warp-uniform: the warp leaves the loop together
       atomicOr(p.status, kStatusTimeout);
@@ -1061,20 +1136,23 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
 #pragma unroll
           for (int g = 0; g < GP; ++g) s2[pp][g] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          float2 kf[NB][EPC / 2];
+        for (int c = 0; c < NU; ++c) {
+          float2 kf[NB][EPU / 2];
 #pragma unroll
           for (int pp = 0; pp < NB; ++pp) {
-            cc_widen<TQ, KV_FP8>(lds_v4_vol(ktile + cc_chunk<TS>(warp * 16 + row[pp], hc + c)),
-                                 kf[pp]);
+            cc_load<TQ, KV_FP8, TS, C::UB, NU>(ktile, warp * 16 + row[pp], h, c, false, kf[pp]);
             if constexpr (ROPE) {
-              const uint8_t* tr = rt + row[pp] * C::RT_ROW + c * EPC / 2 * 16;
+              // offset m = row - 8 from the slice's middle: table row |m|; a negative m flips
+              // the sine, folded into the value the partner sends
+              const int am = row[pp] < 8 ? 8 - row[pp] : row[pp] - 8;
+              const float sf = row[pp] < 8 ? -send_sign : send_sign;
+              const uint8_t* tr = rt + am * C::RT_ROW + c * EPU / 2 * 16;
 #pragma unroll
-              for (int j = 0; j < EPC / 2; ++j) {
+              for (int j = 0; j < EPU / 2; ++j) {
                 const float4 t = *reinterpret_cast<const float4*>(tr + j * 16);
                 float2 kp;
-                kp.x = __shfl_xor_sync(~0u, kf[pp][j].x * send_sign, 16);
-                kp.y = __shfl_xor_sync(~0u, kf[pp][j].y * send_sign, 16);
+                kp.x = __shfl_xor_sync(~0u, kf[pp][j].x * sf, 16);
+                kp.y = __shfl_xor_sync(~0u, kf[pp][j].y * sf, 16);
                 kf[pp][j] = __ffma2_rn(kp, make_float2(t.z, t.w),
                                        __fmul2_rn(kf[pp][j], make_float2(t.x, t.y)));
               }
@@ -1083,8 +1161,8 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
 #pragma unroll
-            for (int j = 0; j < EPC / 4; ++j) {
-              const uint4 t = lds_v4_vol(qlane_s + (g * L * C::QS + c * EPC + 4 * j) * 4);
+            for (int j = 0; j < EPU / 4; ++j) {
+              const uint4 t = lds_v4_vol(qlane_s + (g * L * C::QS + c * EPU + 4 * j) * 4);
               const float2 q01 = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
               const float2 q23 = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
 #pragma unroll
@@ -1095,63 +1173,89 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
             }
           }
         }
-        // ---- scores (summed over the row's L lanes) and the online softmax, once per tile
-        float sc[NB][GP];
-        bool grow = false;
+        // ---- scores: the batch's NB x GP partial sums reduce-scattered over the row's L
+        // lanes (lane bits 16, 8, ... first), so each lane finishes XH of them; the online
+        // softmax runs on those, and every lane then fetches the p of its own rows
+        float d[X];
 #pragma unroll
         for (int pp = 0; pp < NB; ++pp)
 #pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            float d = s2[pp][g].x + s2[pp][g].y;
+          for (int g = 0; g < GP; ++g) d[pp * GP + g] = s2[pp][g].x + s2[pp][g].y;
 #pragma unroll
-            for (int o = R; o < 32; o <<= 1) d += __shfl_xor_sync(~0u, d, o);
-            const float bias = slope[g] * (float)(t_w + row[pp] - b.it.q_pos);
-            sc[pp][g] = valid[pp] ? score_log2(d, scale_qk, bias, cap_log2) : kNegInf;
-            grow |= sc[pp][g] > m2[g] + kLazyMax;
+        for (int k = 0; k < LOG_LR; ++k) {
+          const int o = 16 >> k, n = X >> k;
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? d[i] : d[i + n / 2];
+            const float keep = up ? d[i + n / 2] : d[i];
+            d[i] = keep + __shfl_xor_sync(~0u, send, o);
           }
+        }
+#pragma unroll
+        for (int o = R; o < 32 / LR; o <<= 1)
+#pragma unroll
+          for (int j = 0; j < XH; ++j) d[j] += __shfl_xor_sync(~0u, d[j], o);
+        const int pbdep = deposit4(pb, C::P_MASK);
+        float sc[XH], m2h[XH];
+        bool grow = false;
+#pragma unroll
+        for (int j = 0; j < XH; ++j) {
+          const int hrow = rowbase | pbdep | hdep[j];
+          const float bias = hslope[j] * (float)(t_w + hrow - b.it.q_pos);
+          sc[j] = hrow >= vlo && hrow < vhi ? score_log2(d[j], scale_qk, bias, cap_log2) : kNegInf;
+          m2h[j] = pick<GP>(m2, hg[j]);
+          grow |= sc[j] > m2h[j] + kLazyMax;
+        }
         if (__any_sync(~0u, grow)) {
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
-            float mx = sc[0][g];
+            float mx = kNegInf;
 #pragma unroll
-            for (int pp = 1; pp < NB; ++pp) mx = fmaxf(mx, sc[pp][g]);
+            for (int j = 0; j < XH; ++j) mx = hg[j] == g ? fmaxf(mx, sc[j]) : mx;
 #pragma unroll
-            for (int o = 1; o < R; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
+            for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
             if (mx > m2[g]) {  // warp-uniform: every lane holds the same maximum
               const float alpha = fast_exp2(m2[g] - mx);
-              lsum[g] *= alpha;
+#pragma unroll
+              for (int j = 0; j < XH; ++j) lsum_h[j] = hg[j] == g ? lsum_h[j] * alpha : lsum_h[j];
               const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
               for (int k = 0; k < DL / 2; ++k) acc[g][k] = __fmul2_rn(acc[g][k], a2);
               m2[g] = mx;
             }
           }
+#pragma unroll
+          for (int j = 0; j < XH; ++j) m2h[j] = pick<GP>(m2, hg[j]);
+        }
+        float prh[XH];
+#pragma unroll
+        for (int j = 0; j < XH; ++j) {
+          prh[j] = fast_exp2(sc[j] - (m2h[j] == kNegInf ? 0.f : m2h[j]));
+          lsum_h[j] += prh[j];
         }
         float pr[NB][GP];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float ref = m2[g] == kNegInf ? 0.f : m2[g];
+        for (int pp = 0; pp < NB; ++pp)
 #pragma unroll
-          for (int pp = 0; pp < NB; ++pp) {
-            pr[pp][g] = fast_exp2(sc[pp][g] - ref);
-            lsum[g] += pr[pp][g];
+          for (int g = 0; g < GP; ++g) {
+            const int x = pp * GP + g;
+            pr[pp][g] = __shfl_sync(~0u, prh[x % XH], rr | (hsrc<LOG_X, LOG_LR, LOG_R>(x) << LOG_R));
           }
-        }
         // ---- p * V
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
+        for (int c = 0; c < NU; ++c) {
 #pragma unroll
           for (int pp = 0; pp < NB; ++pp) {
-            uint4 w = lds_v4_vol(vtile + cc_chunk<TS>(warp * 16 + row[pp], hc + c));
-            if (partial && !valid[pp]) w = make_uint4(0u, 0u, 0u, 0u);
-            float2 vf[EPC / 2];
-            cc_widen<TQ, KV_FP8>(w, vf);
+            float2 vf[EPU / 2];
+            cc_load<TQ, KV_FP8, TS, C::UB, NU>(vtile, warp * 16 + row[pp], h, c,
+                                               partial && !valid[pp], vf);
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
               const float2 p2 = make_float2(pr[pp][g], pr[pp][g]);
 #pragma unroll
-              for (int j = 0; j < EPC / 2; ++j)
-                acc[g][c * EPC / 2 + j] = __ffma2_rn(p2, vf[j], acc[g][c * EPC / 2 + j]);
+              for (int j = 0; j < EPU / 2; ++j)
+                acc[g][c * EPU / 2 + j] = __ffma2_rn(p2, vf[j], acc[g][c * EPU / 2 + j]);
             }
           }
         }
@@ -1166,11 +1270,16 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
   // ---- into the epilogue image: l summed over the rows (every dims block holds the same
   // sums); the accumulators reduce-scattered over the row lanes, after which lane rr holds
   // pairs rr * SEG .. rr * SEG + SEG - 1 of its block's flattened [GP][DL / 2] array
+  // each score was finished by L / LR lanes (the ones differing in the lane bits below the
+  // scatter); count the copy with those bits zero
+  const bool counted = ((lane >> LOG_R) & (L / LR - 1)) == 0;
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
-    float l = lsum[g];
+    float l = 0.f;
 #pragma unroll
-    for (int o = 1; o < R; o <<= 1) l += __shfl_xor_sync(~0u, l, o);
+    for (int j = 0; j < XH; ++j) l += counted && hg[j] == g ? lsum_h[j] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) l += __shfl_xor_sync(~0u, l, o);
     if (lane == 0) {
       epi.m[warp * kSlotHeads + g] = m2[g];
       epi.l[warp * kSlotHeads + g] = l;
