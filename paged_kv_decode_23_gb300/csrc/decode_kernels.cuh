@@ -853,16 +853,22 @@ struct CcGeom {
   static constexpr int HBITS = R >= 8 ? 0 : (8 / R - 1) * (UB == 16 ? NU : 1);
   static constexpr int RR_MASK = R >= 8 ? R - 1 : (7 & ~HBITS);
   static constexpr int P_MASK = R >= 8 ? (15 & ~(R - 1)) : (8 | HBITS);
-  // q as fp32 [GP][L][QS]: each lane's DL dims of a head in a block.  The QN blocks that one
-  // phase may read (one per h value in it) must fall in different banks: the blocks are
-  // padded by 16 bytes where DL alone would not spread them.
-  static constexpr int QN = R >= 8 ? 1 : 8 / R;
-  static constexpr int QS = DL * QN <= 32 ? DL : DL + 4;
-  static constexpr int Q_BYTES = GP * L * QS * 4;
+  // q as fp32 [GP][L][DL]: each lane's DL dims of a head in a block of DL / 4 16-byte chunks.
+  // A phase reads chunk k of the blocks of up to 8 / R values of h at once; chunk k of block h
+  // sits at k ^ QSWZ(h), which puts those reads in different bank groups.
+  static constexpr int QB = DL / 4;  // chunks per block
+  __host__ __device__ static constexpr int qswz(int h) { return ((h * QB) >> 3) & (QB - 1); }
+  // float index of element d of head g
+  __host__ __device__ static constexpr int qidx(int g, int d) {
+    return (g * L + d / DL) * DL + (((d % DL) / 4) ^ qswz(d / DL)) * 4 + d % 4;
+  }
+  static constexpr int Q_BYTES = GP * D * 4;
   // Without ROPE: the task's q rows.  With ROPE: each warp's q rotated for its current slice
-  // (same layout), then the K rotations by |m| = 0..8 positions: row |m| holds, per frequency
-  // pair (f, f+1), {cos f, cos f+1, sin f, sin f+1}, padded by 16 bytes so that eight rows
-  // fall in eight bank groups (a negative m flips the sine).
+  // (same layout), then the K rotations by |m| = 0..8 positions (a negative m flips the
+  // sine): row |m| holds, per frequency pair (f, f+1), {cos f, cos f+1, sin f, sin f+1} at
+  // entry jl * L/2 + hp for f = 2 * (hp * DL/2 + jl), i.e. the lanes' dims blocks hp
+  // interleaved so that a phase reads consecutive entries; rows are padded by 16 bytes so
+  // that eight rows fall in eight bank groups.
   static constexpr int RT_ROW = D / 2 * 8 + 16;
   static constexpr int RT_OFF = ROPE ? NW * Q_BYTES : 0;
   static constexpr int BYTES = ROPE ? RT_OFF + 9 * RT_ROW : Q_BYTES;
@@ -987,19 +993,19 @@ __device__ __forceinline__ void cc_setup(const DecodeParams& p, const BlockCoord
       float2 v = make_float2(0.f, 0.f);
       if (g < b.gcnt)
         v = unpack2<TQ>(__ldg(src + (((size_t)b.it.req * p.num_qo_heads + b.g0 + g) * D + d) / 2));
-      float* dst = q + (g * C::L + d / C::DL) * C::QS + d % C::DL;
-      dst[0] = v.x;
-      dst[1] = v.y;
+      q[C::qidx(g, d)] = v.x;
+      q[C::qidx(g, d + 1)] = v.y;
     }
   } else {
     const float2* rates = reinterpret_cast<const float2*>(p.pos_table);
     for (int idx = tid; idx < 9 * (D / 4); idx += nthreads) {
       const int k = idx / (D / 4), fp = idx - k * (D / 4);  // row |m| = k; pair 2fp, 2fp+1
+      const int hp = fp / (C::DL / 2), jl = fp % (C::DL / 2);
       const float2 r0 = __ldg(rates + 2 * fp), r1 = __ldg(rates + 2 * fp + 1);
       float s0, c0, s1, c1;
       rope_sincos((float)k, r0.x, r0.y, s0, c0);
       rope_sincos((float)k, r1.x, r1.y, s1, c1);
-      *reinterpret_cast<float4*>(base + C::RT_OFF + k * C::RT_ROW + fp * 16) =
+      *reinterpret_cast<float4*>(base + C::RT_OFF + k * C::RT_ROW + (jl * (C::L / 2) + hp) * 16) =
           make_float4(c0, c1, s0, s1);
     }
   }
@@ -1022,15 +1028,14 @@ __device__ __forceinline__ void cc_rotate_q(const DecodeParams& p, const BlockCo
     const float2 r = __ldg(rates + f);
     float s, c;
     rope_sincos(dt, r.x, r.y, s, c);
-    const int ox = (f / C::DL) * C::QS + f % C::DL;
-    const int oy = ((f + D / 2) / C::DL) * C::QS + (f + D / 2) % C::DL;
+    const int ox = C::qidx(0, f), oy = C::qidx(0, f + D / 2);
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       const bool live = g < b.gcnt;
       const float x = live ? to_float(__ldg(q + g * D + f)) : 0.f;
       const float y = live ? to_float(__ldg(q + g * D + f + D / 2)) : 0.f;
-      qr[g * C::L * C::QS + ox] = x * c - y * s;
-      qr[g * C::L * C::QS + oy] = y * c + x * s;
+      qr[g * D + ox] = x * c - y * s;
+      qr[g * D + oy] = y * c + x * s;
     }
   }
   __syncwarp();
@@ -1073,8 +1078,9 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
   const int rowbase = deposit4(rr, C::RR_MASK);
   float* qs = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES);
   float* qr = reinterpret_cast<float*>(smem_p + G::PIPE_BYTES) + warp * (C::Q_BYTES / 4);
-  const uint32_t qlane_s = smem_u32((ROPE ? qr : qs) + h * C::QS);
-  const uint8_t* rt = smem_p + G::PIPE_BYTES + C::RT_OFF + ((h % (L / 2)) * DL / 2) * 16;
+  const uint32_t qlane_s = smem_u32((ROPE ? qr : qs) + h * DL);
+  const int qswz_h = C::qswz(h);
+  const uint8_t* rt = smem_p + G::PIPE_BYTES + C::RT_OFF + (h % (L / 2)) * 16;
   const float send_sign = h >= L / 2 ? -1.f : 1.f;
   const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
   const float scale_qk = p.scale_qk;
@@ -1146,13 +1152,14 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
               // the sine, folded into the value the partner sends
               const int am = row[pp] < 8 ? 8 - row[pp] : row[pp] - 8;
               const float sf = row[pp] < 8 ? -send_sign : send_sign;
-              const uint8_t* tr = rt + am * C::RT_ROW + c * EPU / 2 * 16;
+              const uint8_t* tr = rt + am * C::RT_ROW + c * EPU / 2 * (L / 2) * 16;
 #pragma unroll
               for (int j = 0; j < EPU / 2; ++j) {
-                const float4 t = *reinterpret_cast<const float4*>(tr + j * 16);
+                const float4 t = *reinterpret_cast<const float4*>(tr + j * (L / 2) * 16);
+                const float2 ks = __fmul2_rn(kf[pp][j], make_float2(sf, sf));
                 float2 kp;
-                kp.x = __shfl_xor_sync(~0u, kf[pp][j].x * sf, 16);
-                kp.y = __shfl_xor_sync(~0u, kf[pp][j].y * sf, 16);
+                kp.x = __shfl_xor_sync(~0u, ks.x, 16);
+                kp.y = __shfl_xor_sync(~0u, ks.y, 16);
                 kf[pp][j] = __ffma2_rn(kp, make_float2(t.z, t.w),
                                        __fmul2_rn(kf[pp][j], make_float2(t.x, t.y)));
               }
@@ -1162,7 +1169,7 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
           for (int g = 0; g < GP; ++g) {
 #pragma unroll
             for (int j = 0; j < EPU / 4; ++j) {
-              const uint4 t = lds_v4_vol(qlane_s + (g * L * C::QS + c * EPU + 4 * j) * 4);
+              const uint4 t = lds_v4_vol(qlane_s + (g * D + ((c * EPU / 4 + j) ^ qswz_h) * 4) * 4);
               const float2 q01 = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
               const float2 q23 = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
 #pragma unroll
