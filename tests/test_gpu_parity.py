@@ -93,6 +93,21 @@ def test_e4m3_kv(tc, qdt, d):
                  f"e4m3 {qdt} D{d} tc={tc}")
 
 
+@pytest.mark.parametrize("kv,d", [("bf16", 64), ("f16", 128), ("bf16", 256), ("e4m3", 128),
+                                  ("e4m3", 256)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (6, 1)])
+def test_cuda_core_lane_splits(kv, d, hq, hkv):
+    """The CUDA-core kernel splits a K/V row over 2..32 lanes depending on head_dim, KV dtype
+    and the head group (1, 2, 4, 8 qo heads per CTA, with dead heads in a partial group):
+    every split, with 16- and 8-byte lane loads, against the oracle, with a window and a cap
+    so rows at slice edges are masked."""
+    w, q, pool = _case([1, 9, 64, 300, 1031], hq, hkv, d, 16, "HND",
+                       "bf16" if kv == "e4m3" else kv, kv=kv, seed=d + 7 * hq + hkv,
+                       logits_soft_cap=20.0, window_left=700)
+    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=False, fixed_split_size=16),
+                 run_oracle(w, q, pool), f"cc {kv} D{d} {hq}/{hkv}")
+
+
 def test_e4m3_large_query_values():
     """bf16 q far outside fp16 range still works with e4m3 KV (the tensor-core kernel rescales q)."""
     w, q, pool = _case([40, 300], 8, 1, 128, 16, "NHD", "bf16", kv="e4m3", seed=9,
