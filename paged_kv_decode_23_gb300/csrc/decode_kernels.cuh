@@ -1043,13 +1043,16 @@ __device__ __forceinline__ void cc_rotate_q(const DecodeParams& p, const BlockCo
 }
 
 // The CUDA-core consumer warp.  For each tile its 16-token slice is taken in NP passes of R
-// rows (lane: row rr = lane % R of the pass, dims block h = lane / R).  Per pass:
-//  - the partial dot products of the lane's row with its q dims (fp32 pair FMAs), summed over
-//    the row's L lanes;
+// rows (lane: row rr = lane % R of the pass, dims block h = lane / R), NB passes at a time:
+//  - the partial dot products of the lane's rows with its q dims (fp32 pair FMAs), one
+//    independent chain per pass and head;
+//  - the batch's NB x GP partial sums reduce-scattered over the row's L lanes, so each lane
+//    finishes XH scores (no two lanes repeat the softmax work of a score);
 //  - the online softmax in base 2 with a lazy reference: m2 moves only when a score exceeds
-//    it by more than kLazyMax, so p <= 2^kLazyMax and most passes skip the cross-lane max;
-//  - p * V into the lane's own accumulators (rows of a window or chunk edge that are not
-//    attended have p = 0 and their V zeroed, so stale values in the stage cannot leak).
+//    it by more than kLazyMax, so p <= 2^kLazyMax and most batches skip the cross-lane max;
+//  - every lane fetches p of its own rows and adds p * V into its own accumulators (rows of a
+//    window or chunk edge that are not attended have p = 0 and their V zeroed, so stale
+//    values in the stage cannot leak).
 // At the end the accumulators are reduce-scattered over the R row lanes of each dims block
 // and stored, with m2 and l, into the warp's slot of the epilogue image.
 // ROPE: q is rotated per slice to the slice's middle t_w + 8 and each K row by its offset
@@ -1082,7 +1085,6 @@ __device__ __forceinline__ bool consume_cc(const DecodeParams& p, const BlockCoo
   const int qswz_h = C::qswz(h);
   const uint8_t* rt = smem_p + G::PIPE_BYTES + C::RT_OFF + (h % (L / 2)) * 16;
   const float send_sign = h >= L / 2 ? -1.f : 1.f;
-  const float2* rope_rates = reinterpret_cast<const float2*>(p.pos_table);
   const float scale_qk = p.scale_qk;
   const float cap_log2 = p.cap_log2;
 
