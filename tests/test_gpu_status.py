@@ -31,14 +31,16 @@ def _run_into(dec, w, q, pool, dev):
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def test_wait_limit_zero_gives_up_reports_and_recovers():
+@pytest.mark.parametrize("tc", [True, False])
+def test_wait_limit_zero_gives_up_reports_and_recovers(tc):
     from paged_kv_decode_23_gb300 import _lib as L
     dev = torch.device("cuda")
     lens = [3000, 17, 2000, 4000, 1000, 700, 0, 2500] * 4
     w = W.custom(lens, 16, 2, 128, 16, layout="NHD", q_dtype="bf16", seed=61)
     q, pool = W.make_q(w).to(dev), W.make_pool(w).to(dev)
     ref_o, ref_lse = run_oracle(w, q, pool)
-    dec = gpu_decoder(w, fixed_split_size=8)  # split requests: merges inside the launch too
+    # split requests: merges inside the launch too
+    dec = gpu_decoder(w, fixed_split_size=8, use_tensor_cores=tc)
     atol, rtol = TOL[w.kv_dtype]
 
     # 1. every wait that is not already complete gives up
