@@ -39,12 +39,12 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on: once the sources differ, the figure no longer describes the kernel and the line
 # reports null.
 MEASURED_TRAFFIC = {
-    "sources_sha256": "3bcf1b2910e28fa3e3e3a75e2cd6aacdc9a20dde9b5864a9e8cf9abebd7369a3",
+    "sources_sha256": "134407828756dd62eb8d6960a5b70d9cc75e14acec9c502223049aec2a3e52dd",
     # profiles/decode_paged_kernel_traffic.md (one launch each, 1-pass ncu metric set, bytes)
-    "uniform": 618890240.0,
-    "mix": 418353664.0,
-    "long": 2150649088.0,
-    "lognormal": 3526036480.0,
+    "uniform": 618856704.0,
+    "mix": 418319872.0,
+    "long": 2150457344.0,
+    "lognormal": 3525971712.0,
 }
 
 
