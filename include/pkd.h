@@ -66,7 +66,9 @@ extern "C" {
 #define PKD_POS_ROPE_LLAMA 1
 #define PKD_POS_ALIBI 2
 
-/* Kernel choice for pkd_plan's use_tensor_cores argument (the page's use_tensor_cores). */
+/* Kernel choice for pkd_plan's use_tensor_cores argument (the page's use_tensor_cores).
+ * AUTO takes the tensor-core kernel (mma.sync, 8 qo heads per task), measured at least as
+ * fast as the CUDA-core kernel (fp32 FMAs, 1 to 8 qo heads per task) at every GQA group. */
 #define PKD_KERNEL_AUTO (-1)
 #define PKD_KERNEL_CUDA_CORE 0
 #define PKD_KERNEL_TENSOR_CORE 1

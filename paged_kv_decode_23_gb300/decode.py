@@ -77,6 +77,9 @@ class BatchDecodePagedKV:
     copies the page table into those buffers, the batch size is fixed by the first plan (pad
     with zero-length requests), and the work list holds at most ``max_items`` chunks
     (default: max_batch + 2 x the SM count).
+
+    ``use_tensor_cores``: None (auto: the tensor-core kernel, measured at least as fast at
+    every GQA group), True, or False (the fp32 CUDA-core kernel); ``plan`` may override it.
     """
 
     def __init__(self, float_workspace_buffer: torch.Tensor, kv_layout: str = "NHD",
