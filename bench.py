@@ -493,7 +493,8 @@ def gpu_arm(args, w, rank, world):
                      "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else
                      measured_traffic(w.name)
-                     if (args.kernel, args.pos_encoding, args.qo_heads) == ("auto", "NONE", None)
+                     if (args.kernel, args.pos_encoding, args.qo_heads, args.kv_dtype,
+                         args.head_dim) == ("auto", "NONE", None, None, None)
                      else None,
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
                      "kernel_us_source": "CUDA events around the runs of the timed steps "
@@ -777,6 +778,10 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--qo-heads", type=int, default=None,
                     help="override num_qo_heads (a GQA-group variant of the workload)")
+    ap.add_argument("--kv-dtype", choices=["f16", "bf16", "e4m3"], default=None,
+                    help="override the KV dtype (e4m3 stores values / 0.5, k_scale = v_scale = 0.5)")
+    ap.add_argument("--head-dim", type=int, choices=[64, 128, 256], default=None,
+                    help="override head_dim")
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
                     help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
@@ -817,6 +822,13 @@ def main():
         if args.qo_heads % w.num_kv_heads:
             ap.error("--qo-heads must be a multiple of the workload's kv heads")
         w.num_qo_heads = args.qo_heads
+    if args.head_dim:
+        w.head_dim = args.head_dim
+        w.sm_scale = None
+    if args.kv_dtype:
+        w.kv_dtype = args.kv_dtype
+        if args.kv_dtype == "e4m3":
+            w.kv_store_scale, w.k_scale, w.v_scale = 0.5, 0.5, 0.5
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, w)
