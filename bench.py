@@ -494,7 +494,8 @@ def gpu_arm(args, w, rank, world):
                      "traffic": args.traffic if args.traffic is not None else
                      measured_traffic(w.name)
                      if (args.kernel, args.pos_encoding, args.qo_heads, args.kv_dtype,
-                         args.head_dim) == ("auto", "NONE", None, None, None)
+                         args.head_dim, args.fixed_split_size)
+                     == ("auto", "NONE", None, None, None, None)
                      else None,
                      "kernel": "decode_paged_kernel", "kernel_us": kern_avg_ms * 1e3,
                      "kernel_us_source": "CUDA events around the runs of the timed steps "
@@ -782,6 +783,8 @@ def main():
                     help="override the KV dtype (e4m3 stores values / 0.5, k_scale = v_scale = 0.5)")
     ap.add_argument("--head-dim", type=int, choices=[64, 128, 256], default=None,
                     help="override head_dim")
+    ap.add_argument("--fixed-split-size", type=int, default=None,
+                    help="override the plan's fixed_split_size (pages; 0 = the heuristic)")
     ap.add_argument("--kernel", choices=["auto", "tc", "cc"], default="auto")
     ap.add_argument("--pos-encoding", choices=["NONE", "ROPE_LLAMA", "ALIBI"], default="NONE",
                     help="plan's pos_encoding_mode (rope_theta 1e4, rope_scale 1)")
@@ -825,6 +828,8 @@ def main():
     if args.head_dim:
         w.head_dim = args.head_dim
         w.sm_scale = None
+    if args.fixed_split_size is not None:
+        w.fixed_split_size = args.fixed_split_size
     if args.kv_dtype:
         w.kv_dtype = args.kv_dtype
         if args.kv_dtype == "e4m3":
