@@ -32,7 +32,7 @@ def _workload(base, lens, indptr, indices, lpl):
                       k_scale=base.k_scale, v_scale=base.v_scale)
 
 
-@pytest.mark.parametrize("kv,tc", [("bf16", True), ("bf16", False), ("e4m3", True)])
+@pytest.mark.parametrize("kv,tc", [("bf16", True), ("bf16", False), ("e4m3", True), ("e4m3", False)])
 def test_captured_run_replays_across_plans(kv, tc):
     from paged_kv_decode_23_gb300 import CUDAGraphBatchDecodePagedKV
     dev = torch.device("cuda")
