@@ -96,16 +96,19 @@ def test_e4m3_kv(tc, qdt, d):
 @pytest.mark.parametrize("kv,d", [("bf16", 64), ("f16", 128), ("bf16", 256), ("e4m3", 128),
                                   ("e4m3", 256)])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (6, 1)])
-def test_cuda_core_lane_splits(kv, d, hq, hkv):
+@pytest.mark.parametrize("pos", ["NONE", "ALIBI"])
+def test_cuda_core_lane_splits(kv, d, hq, hkv, pos):
     """The CUDA-core kernel splits a K/V row over 2..32 lanes depending on head_dim, KV dtype
     and the head group (1, 2, 4, 8 qo heads per CTA, with dead heads in a partial group):
     every split, with 16- and 8-byte lane loads, against the oracle, with a window and a cap
-    so rows at slice edges are masked."""
+    so rows at slice edges are masked, and with ALiBi (each lane's finished scores take their
+    own head's slope)."""
     w, q, pool = _case([1, 9, 64, 300, 1031], hq, hkv, d, 16, "HND",
                        "bf16" if kv == "e4m3" else kv, kv=kv, seed=d + 7 * hq + hkv,
                        logits_soft_cap=20.0, window_left=700)
-    assert_close(w, run_gpu(w, q, pool, use_tensor_cores=False, fixed_split_size=16),
-                 run_oracle(w, q, pool), f"cc {kv} D{d} {hq}/{hkv}")
+    got = run_gpu(w, q, pool, use_tensor_cores=False, fixed_split_size=16, pos_encoding_mode=pos)
+    assert_close(w, got, run_oracle(w, q, pool, pos_encoding_mode=pos),
+                 f"cc {kv} D{d} {hq}/{hkv} {pos}")
 
 
 def test_e4m3_large_query_values():
@@ -345,14 +348,15 @@ def test_rope_llama(kv, d, tc):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 2), (6, 1), (32, 2)])
-def test_rope_llama_cuda_core_head_groups(kv, hq, hkv):
-    """ROPE_LLAMA on the CUDA-core kernel at every head-group width it is built for (2, 4, 8
-    qo heads per CTA, with dead heads in a partial group), keys straddling every slice offset
-    of a tile, HND pages of 16 tokens."""
+def test_rope_llama_cuda_core_head_groups(kv, d, hq, hkv):
+    """ROPE_LLAMA on the CUDA-core kernel at every head-group width it is built for (1, 2, 4,
+    8 qo heads per CTA, with dead heads in a partial group; at head_dim 256 the two-stage
+    instances too), keys straddling every slice offset of a tile, HND pages of 16 tokens."""
     lens = [1, 8, 9, 16, 250, 1031]
-    w, q, pool = _case(lens, hq, hkv, 128, 16, "HND", "f16" if kv == "e4m3" else kv, kv=kv,
-                       seed=hq * 13 + hkv)
+    w, q, pool = _case(lens, hq, hkv, d, 16, "HND", "f16" if kv == "e4m3" else kv, kv=kv,
+                       seed=hq * 13 + hkv + d)
     pos = dict(pos_encoding_mode="ROPE_LLAMA", rope_theta=1e4, rope_scale=2.0)
     got = run_gpu(w, q, pool, use_tensor_cores=False, fixed_split_size=256, **pos)
     assert_close(w, got, run_oracle(w, q, pool, **pos), f"rope cuda-core {kv} G{hq // hkv}")
