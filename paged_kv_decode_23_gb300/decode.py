@@ -526,8 +526,17 @@ class BatchMLAPagedAttention:
     def run(self, q_nope: torch.Tensor, q_pe: torch.Tensor, ckv_cache: torch.Tensor,
             kpe_cache: torch.Tensor, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, return_lse: bool = False,
-            return_lse_base_on_e: bool = False, stream=None, timing_events=None,
-            enable_pdl: Optional[bool] = None):
+            profiler_buffer: Optional[torch.Tensor] = None, kv_len: Optional[torch.Tensor] = None,
+            page_table: Optional[torch.Tensor] = None, return_lse_base_on_e: bool = False,
+            stream=None, timing_events=None, enable_pdl: Optional[bool] = None):
+        """The page's run(): ``kv_len`` and ``page_table`` belong to the cutlass backend, which is
+        not built (the plan's lengths and page ids are used), and no profiler is built, so
+        all three must be None."""
+        if profiler_buffer is not None:
+            raise NotImplementedError("no profiler is built (plan with use_profiler=False)")
+        if kv_len is not None or page_table is not None:
+            raise NotImplementedError("kv_len / page_table are the cutlass backend's run() "
+                                      "arguments; that backend is not built")
         a = self._plan_args
         if a is None:
             raise RuntimeError("plan() must be called before run()")

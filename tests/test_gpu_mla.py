@@ -281,3 +281,28 @@ def test_mla_cuda_graph_rejects_changed_shapes():
         BatchMLAPagedAttention(torch.zeros(1 << 20, dtype=torch.uint8, device=dev),
                                use_cuda_graph=True)
     plan(4)  # the same shapes plan again
+
+
+def test_run_accepts_the_page_keywords_and_refuses_unbuilt_ones():
+    """run() takes the page's keyword set: profiler_buffer, kv_len and page_table left as None
+    run normally; given, they name parts that are not built (the profiler, the cutlass
+    backend's run-time page table) and are refused."""
+    from paged_kv_decode_23_gb300 import BatchMLAPagedAttention
+    dev = torch.device("cuda")
+    w = W.mla_custom([5, 40], 16, 16, "bf16", seed=4)
+    qn, qp = W.make_mla_q(w)
+    ckv, kpe = W.make_mla_cache(w)
+    mla = BatchMLAPagedAttention(torch.zeros(64 << 20, dtype=torch.uint8, device=dev))
+    mla.plan(torch.arange(w.batch + 1, dtype=torch.int32), torch.from_numpy(w.kv_indptr),
+             torch.from_numpy(w.kv_indices).to(dev), torch.from_numpy(w.kv_lens), w.num_heads,
+             512, 64, w.page_size, False, w.sm_scale, torch.bfloat16, torch.bfloat16)
+    args = (qn.to(dev), qp.to(dev), ckv.to(dev), kpe.to(dev))
+    o = mla.run(*args, profiler_buffer=None, kv_len=None, page_table=None)
+    torch.cuda.synchronize()
+    ref, _ = _oracle(w, qn, qp, ckv, kpe)
+    got = o.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2e-3 + 1e-2 * np.abs(ref))
+    with pytest.raises(NotImplementedError):
+        mla.run(*args, profiler_buffer=torch.zeros(16, device=dev))
+    with pytest.raises(NotImplementedError):
+        mla.run(*args, kv_len=torch.from_numpy(w.kv_lens).to(dev))
