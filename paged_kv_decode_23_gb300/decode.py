@@ -88,9 +88,16 @@ class BatchDecodePagedKV:
                  paged_kv_indices_buffer: Optional[torch.Tensor] = None,
                  paged_kv_last_page_len_buffer: Optional[torch.Tensor] = None,
                  int_workspace_buffer: Optional[torch.Tensor] = None,
-                 max_items: Optional[int] = None):
+                 max_items: Optional[int] = None, backend: str = "auto",
+                 jit_args: Optional[list] = None):
         if kv_layout not in ("NHD", "HND"):
             raise ValueError("kv_layout must be 'NHD' or 'HND'")
+        # the page's backends name other libraries' kernels; this library has one of its own
+        if backend not in ("auto", "fa2"):
+            raise NotImplementedError(f"backend {backend!r} is not built (auto / fa2 run this "
+                                      "library's kernels)")
+        if jit_args is not None:
+            raise NotImplementedError("JIT variants are not built")
         if not float_workspace_buffer.is_cuda:
             raise ValueError("the float workspace must be a CUDA tensor")
         if int_workspace_buffer is None:
@@ -151,7 +158,8 @@ class BatchDecodePagedKV:
              fixed_split_size: Optional[int] = None, disable_split_kv: bool = False,
              use_tensor_cores: Optional[bool] = None, stream=None,
              q_len_per_req: int = 1, rope_scale: Optional[float] = None,
-             rope_theta: Optional[float] = None) -> None:
+             rope_theta: Optional[float] = None, block_tables: Optional[torch.Tensor] = None,
+             seq_lens: Optional[torch.Tensor] = None) -> None:
         """Plan a batch; ``indptr`` / ``last_page_len`` may live on the host or the device
         (a device copy is read back once here), ``indices`` must be a CUDA int32 tensor and
         stay unchanged while runs of this plan are in flight.  ``q_len_per_req`` query tokens
@@ -160,6 +168,10 @@ class BatchDecodePagedKV:
         ``batch * q_len_per_req`` rows, request-major.  ``pos_encoding_mode``: "NONE",
         "ROPE_LLAMA" (with ``rope_scale`` / ``rope_theta``, defaults 1 and 1e4) or
         "ALIBI"."""
+        if block_tables is not None or seq_lens is not None:
+            raise NotImplementedError("block_tables / seq_lens (the trtllm-gen backend's page "
+                                      "table form) are not built; pass indptr / indices / "
+                                      "last_page_len")
         pos_code = _POS_CODE.get(pos_encoding_mode)
         if pos_code is None:
             raise ValueError("pos_encoding_mode must be 'NONE', 'ROPE_LLAMA' or 'ALIBI'")
@@ -264,6 +276,11 @@ class BatchDecodePagedKV:
             ev0.cuda_event if ev0 is not None else None,
             ev1.cuda_event if ev1 is not None else None))
         return (out, lse) if return_lse else out
+
+    def run_return_lse(self, q: torch.Tensor, paged_kv_cache, *args, **kw):
+        """``run(..., return_lse=True)``: returns ``(o, lse)``."""
+        kw["return_lse"] = True
+        return self.run(q, paged_kv_cache, *args, **kw)
 
     def check_status(self, stream=None) -> int:
         """Read and clear the device status word (synchronises the stream); 0 = no error,

@@ -378,3 +378,25 @@ def test_rope_long_positions_keep_precision(kv, d, layout, lens, tc):
     got = run_gpu(w, q, pool, use_tensor_cores=tc, **pos)
     assert_close(w, got, run_oracle(w, q, pool, **pos),
                  f"rope long positions {kv} D{d} {lens} tc={tc}")
+
+
+def test_wrapper_keywords_of_the_page():
+    """The decode wrapper takes the page's keyword set: run_return_lse is run(return_lse=True);
+    backend 'auto' / 'fa2' run this library's kernels, the others (other libraries' kernels),
+    jit_args, and plan's block_tables / seq_lens (the trtllm-gen page-table form) are refused."""
+    from paged_kv_decode_23_gb300 import BatchDecodePagedKV
+    dev = torch.device("cuda")
+    w, q, pool = _case([33, 250, 1], 8, 2, 128, 16, seed=12)
+    dec = gpu_decoder(w)
+    o1, l1 = dec.run(q.to(dev), pool.to(dev), return_lse=True)
+    o2, l2 = dec.run_return_lse(q.to(dev), pool.to(dev))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+    BatchDecodePagedKV(ws, "NHD", backend="fa2")
+    for bad in ("fa3", "trtllm-gen", "cudnn"):
+        with pytest.raises(NotImplementedError):
+            BatchDecodePagedKV(ws, "NHD", backend=bad)
+    with pytest.raises(NotImplementedError):
+        BatchDecodePagedKV(ws, "NHD", jit_args=[1])
+    with pytest.raises(NotImplementedError):
+        gpu_decoder(w, block_tables=torch.zeros(3, 4, dtype=torch.int32, device=dev))
